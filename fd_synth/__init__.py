@@ -1,0 +1,316 @@
+"""Seeded synthetic inputs for single-query decode attention.
+
+This module holds no attention arithmetic.  It only makes the bf16 bit
+patterns, lengths, page permutations and block tables that both the CPU
+oracle and the CUDA library consume, so that the two sides read identical
+inputs.
+
+Recipe (the same on every machine):
+
+* ``splitmix64``: the counter form of Steele, Lea and Flood's SplitMix64
+  (as published by Vigna): output ``i`` of stream ``seed`` is
+  ``mix(seed + (i + 1) * 0x9E3779B97F4A7C15)`` with the two multiply-xorshift
+  rounds of the published finaliser.
+* Uniforms in (0, 1]: ``((z >> 11) + 1) * 2**-53``.
+* Normals: Box-Muller on consecutive output pairs (u1, u2):
+  ``r = sqrt(-2 ln u1)``, ``n0 = r cos(2 pi u2)``, ``n1 = r sin(2 pi u2)``,
+  computed in fp64.
+* bf16: one round-to-nearest-even from fp64 straight to bf16 (no detour
+  through fp32, which would round twice).
+* Integers in [lo, hi]: ``lo + z % (hi - lo + 1)``.
+* Permutations: Fisher-Yates driven by the same integer draws.
+
+Seeds follow ``0xFD000000 + 16 * config_id + tensor_id`` with tensor ids
+q=0, K=1, V=2, lengths=3, page permutation=4, key mask=5.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+import math
+
+import numpy as np
+
+GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_CHUNK = 1 << 22          # values per worker task
+
+TENSOR_Q, TENSOR_K, TENSOR_V, TENSOR_LENS, TENSOR_PERM, TENSOR_MASK = range(6)
+
+
+def seed_for(config_id: int, tensor_id: int) -> int:
+    return 0xFD000000 + 16 * config_id + tensor_id
+
+
+def splitmix64(seed: int, n: int, offset: int = 0) -> np.ndarray:
+    """Outputs ``offset .. offset+n-1`` of the SplitMix64 stream ``seed``."""
+    with np.errstate(over="ignore"):
+        i = np.arange(offset + 1, offset + n + 1, dtype=np.uint64)
+        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + i * GOLDEN
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        return z ^ (z >> np.uint64(31))
+
+
+def uniform01(z: np.ndarray) -> np.ndarray:
+    """Map 64-bit draws to doubles in (0, 1]."""
+    return ((z >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to bf16 bit patterns, nearest-even, in one step.
+
+    Only zero and normal bf16 magnitudes are expected (|x| >= 2**-126 or 0);
+    anything else raises, rather than being rounded some other way.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    if not np.all(np.isfinite(x)) or np.any((ax != 0) & (ax < 2.0 ** -126)):
+        raise ValueError("f64_to_bf16_bits: non-finite or subnormal input")
+    b = x.view(np.uint64).copy()
+    lsb = (b >> np.uint64(45)) & np.uint64(1)
+    b += np.uint64((1 << 44) - 1) + lsb
+    b &= ~np.uint64((1 << 45) - 1)
+    f = b.view(np.float64).astype(np.float32)      # exact: 7 mantissa bits left
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns exactly to fp64."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def _normal_chunk(seed: int, start: int, n: int) -> np.ndarray:
+    # element e uses the Box-Muller pair (2*(e//2), 2*(e//2)+1)
+    p0 = start // 2
+    p1 = (start + n + 1) // 2
+    z = splitmix64(seed, 2 * (p1 - p0), 2 * p0)
+    u1 = uniform01(z[0::2])
+    u2 = uniform01(z[1::2])
+    r = np.sqrt(-2.0 * np.log(u1))
+    t = 2.0 * math.pi * u2
+    out = np.empty(2 * (p1 - p0), dtype=np.float64)
+    out[0::2] = r * np.cos(t)
+    out[1::2] = r * np.sin(t)
+    off = start - 2 * p0
+    return out[off:off + n]
+
+
+def normal_bf16(seed: int, shape, workers: int | None = None) -> np.ndarray:
+    """i.i.d. N(0,1) values rounded to bf16, returned as uint16 bit patterns."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.uint16)
+
+    def work(start):
+        m = min(_CHUNK, n - start)
+        out[start:start + m] = f64_to_bf16_bits(_normal_chunk(seed, start, m))
+
+    starts = range(0, n, _CHUNK)
+    if n <= _CHUNK:
+        for s in starts:
+            work(s)
+    else:
+        with ThreadPoolExecutor(max_workers=workers or min(32, os.cpu_count() or 1)) as ex:
+            list(ex.map(work, starts))
+    return out.reshape(shape)
+
+
+def randint(seed: int, n: int, lo: int, hi: int) -> np.ndarray:
+    """n integers uniform in [lo, hi] (inclusive)."""
+    z = splitmix64(seed, n)
+    return (np.uint64(lo) + z % np.uint64(hi - lo + 1)).astype(np.int64)
+
+
+def permutation(seed: int, n: int) -> np.ndarray:
+    """Fisher-Yates shuffle of 0..n-1 (step i swaps a[i] with a[i + z_i % (n-i)])."""
+    a = np.arange(n, dtype=np.int64)
+    if n <= 1:
+        return a
+    z = splitmix64(seed, n - 1)
+    for i in range(n - 1):
+        j = i + int(z[i] % np.uint64(n - i))
+        a[i], a[j] = a[j], a[i]
+    return a
+
+
+def choose(seed: int, n: int, k: int) -> np.ndarray:
+    """k distinct values from 0..n-1: the first k steps of the same shuffle."""
+    a = np.arange(n, dtype=np.int64)
+    z = splitmix64(seed, k)
+    pos = {}
+    out = np.empty(k, dtype=np.int64)
+    for i in range(k):
+        j = i + int(z[i] % np.uint64(n - i))
+        ai = pos.get(i, i)
+        aj = pos.get(j, j)
+        pos[i], pos[j] = aj, ai
+        out[i] = aj
+    del a
+    return out
+
+
+BF16_NAN = np.uint16(0x7FC0)
+
+
+def scale_bf16_bits(bits: np.ndarray, factor: float) -> np.ndarray:
+    """Multiply bf16 values by a power of two (exact in bf16 for normal values)."""
+    assert factor > 0 and math.log2(factor).is_integer()
+    f = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32) * np.float32(factor)
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# Workloads
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Workload:
+    """One decode-attention problem, as bf16 bit patterns plus int32 metadata.
+
+    Contiguous: ``k``/``v`` are ``[B, S_max, Hkv, D]``.
+    Paged: ``k``/``v`` are ``[num_pages, P, Hkv, D]`` and ``block_table`` is
+    ``[B, max_blocks]`` int32 with -1 past each request's last page.
+    """
+    name: str
+    q: np.ndarray                      # uint16 [B, Hq, D]
+    k: np.ndarray                      # uint16
+    v: np.ndarray                      # uint16
+    seq_lens: np.ndarray               # int32 [B]
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    scale: float                       # fp32 value (1/sqrt(D) computed in fp32)
+    page_size: int = 0                 # 0 = contiguous
+    block_table: np.ndarray | None = None
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def paged(self) -> bool:
+        return self.page_size > 0
+
+    @property
+    def s_max(self) -> int:
+        return 0 if self.paged else self.k.shape[1]
+
+    @property
+    def num_pages(self) -> int:
+        return self.k.shape[0] if self.paged else 0
+
+    @property
+    def max_blocks(self) -> int:
+        return self.block_table.shape[1] if self.paged else 0
+
+    def kv_bytes(self) -> int:
+        """K+V bytes of the valid tokens, read once each."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 2 * 2
+
+
+def default_scale(head_dim: int) -> float:
+    """1/sqrt(D) evaluated in fp32, as the library's callers pass it."""
+    return float(np.float32(1.0) / np.sqrt(np.float32(head_dim)))
+
+
+def make_contiguous(config_id: int, batch: int, hq: int, hkv: int, d: int, s_max: int,
+                    lens, name: str = "") -> Workload:
+    q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d))
+    k = normal_bf16(seed_for(config_id, TENSOR_K), (batch, s_max, hkv, d))
+    v = normal_bf16(seed_for(config_id, TENSOR_V), (batch, s_max, hkv, d))
+    lens = np.asarray(lens, dtype=np.int32).reshape(batch)
+    return Workload(name or f"contig{config_id}", q, k, v, lens, hq, hkv, d, default_scale(d))
+
+
+def build_block_table(lens, page: int, max_blocks: int, perm: np.ndarray) -> np.ndarray:
+    """Assign physical pages perm[0], perm[1], ... to the logical pages in request order."""
+    table = np.full((len(lens), max_blocks), -1, dtype=np.int32)
+    nxt = 0
+    for b, L in enumerate(lens):
+        nb = (int(L) + page - 1) // page
+        table[b, :nb] = perm[nxt:nxt + nb]
+        nxt += nb
+    return table
+
+
+def make_paged(config_id: int, batch: int, hq: int, hkv: int, d: int, page: int,
+               lens, max_blocks: int, name: str = "", extra_pages: int = 0) -> Workload:
+    lens = np.asarray(lens, dtype=np.int32).reshape(batch)
+    used = int(sum((int(L) + page - 1) // page for L in lens))
+    num_pages = max(1, used + extra_pages)
+    perm = permutation(seed_for(config_id, TENSOR_PERM), num_pages)
+    table = build_block_table(lens, page, max_blocks, perm)
+    q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d))
+    k = normal_bf16(seed_for(config_id, TENSOR_K), (num_pages, page, hkv, d))
+    v = normal_bf16(seed_for(config_id, TENSOR_V), (num_pages, page, hkv, d))
+    return Workload(name or f"paged{config_id}", q, k, v, lens, hq, hkv, d, default_scale(d),
+                    page_size=page, block_table=table)
+
+
+def scale_keys(w: Workload, tokens: np.ndarray, factor: float) -> None:
+    """Multiply the K rows of the given logical tokens (all kv heads, request 0..B-1) by factor."""
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        for t in tokens:
+            t = int(t)
+            if t >= L:
+                continue
+            if w.paged:
+                pg = int(w.block_table[b, t // w.page_size])
+                w.k[pg, t % w.page_size] = scale_bf16_bits(w.k[pg, t % w.page_size], factor)
+            else:
+                w.k[b, t] = scale_bf16_bits(w.k[b, t], factor)
+
+
+def _scale_keys_paged_fast(w: Workload, b: int, tokens: np.ndarray, factor: float) -> None:
+    pg = w.block_table[b, tokens // w.page_size].astype(np.int64)
+    sl = tokens % w.page_size
+    w.k[pg, sl] = scale_bf16_bits(w.k[pg, sl], factor)
+
+
+# The five benchmark workloads (sizes from the task's configuration list).
+CONFIG_NAMES = {
+    1: "mha_single_b1_h32_L4096",
+    2: "mha_long_b1_h32_L65536",
+    3: "gqa_contig_b16_hq32_hkv8_L512-8192",
+    4: "gqa_paged_b64_hq32_hkv8_P16_L1-16384",
+    5: "gqa_paged_b1_hq64_hkv8_P64_L262144_keys_x8",
+}
+
+
+def config_lens(config_id: int) -> np.ndarray:
+    if config_id == 1:
+        return np.array([4096], dtype=np.int32)
+    if config_id == 2:
+        return np.array([65536], dtype=np.int32)
+    if config_id == 3:
+        return randint(seed_for(3, TENSOR_LENS), 16, 512, 8192).astype(np.int32)
+    if config_id == 4:
+        return randint(seed_for(4, TENSOR_LENS), 64, 1, 16384).astype(np.int32)
+    if config_id == 5:
+        return np.array([262144], dtype=np.int32)
+    raise ValueError(config_id)
+
+
+def make_config(config_id: int) -> Workload:
+    """Build benchmark workload 1..5 at full size."""
+    lens = config_lens(config_id)
+    name = CONFIG_NAMES[config_id]
+    if config_id in (1, 2):
+        return make_contiguous(config_id, 1, 32, 32, 128, int(lens[0]), lens, name)
+    if config_id == 3:
+        return make_contiguous(3, 16, 32, 8, 128, 8192, lens, name)
+    if config_id == 4:
+        return make_paged(4, 64, 32, 8, 128, 16, lens, (16384 + 15) // 16, name)
+    if config_id == 5:
+        w = make_paged(5, 1, 64, 8, 128, 64, lens, 262144 // 64, name)
+        n_scaled = int(0.01 * 262144)
+        toks = np.sort(choose(seed_for(5, TENSOR_MASK), 262144, n_scaled))
+        _scale_keys_paged_fast(w, 0, toks, 8.0)
+        w.meta["scaled_tokens"] = toks
+        return w
+    raise ValueError(config_id)

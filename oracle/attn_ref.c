@@ -1,0 +1,258 @@
+/*
+ * attn_ref.c -- CPU oracle for single-query decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the package smoke check and the CPU
+ * baseline leg of the benchmark do.  It shares no code, header or constant
+ * with the CUDA library.
+ *
+ * Everything is plain fp64 on the exact widening of the same bf16 input bits
+ * the GPU reads.  Each function follows one passage of the source pages:
+ *
+ *   oracle_attend       -- the definition S = scale q K^T, P = softmax(S),
+ *                          O = P V, with a full (not online) softmax and the
+ *                          natural-log log-sum-exp of the scores.  Written
+ *                          as in "FlashAttention 与推理算子" (standard
+ *                          attention section; its CPU references
+ *                          attention_cpu and the paged CPU reference that
+ *                          walks the block table), restricted to one query
+ *                          row and to a token range [t0, t1).  With
+ *                          t0 = 0, t1 = L the result is the attention output;
+ *                          a sub-range gives a split's normalised partial
+ *                          output and its log-sum-exp (Flash-Decoding
+ *                          section of the same page).
+ *   oracle_lse_merge    -- the pass-2 merge of "纯手搓 flash decoding sm120"
+ *                          section 2: lse_max = max lse_i,
+ *                          G = lse_max + ln sum exp(lse_i - lse_max),
+ *                          O = sum O_i exp(lse_i - G); segments with
+ *                          lse = -inf are skipped (merge exercise of the
+ *                          handbook page).
+ *   oracle_online_blocks -- the online-softmax recurrence of the handbook's
+ *                          FlashAttention section (m, l and O updated block
+ *                          by block, O divided by l at the end), for one
+ *                          query row with a vector value of width dv.
+ *
+ * GQA head mapping: query head h reads kv head h / (Hq / Hkv) (consecutive
+ * query heads share a kv head).  Paged layout: token t of request b lives
+ * in physical page block_table[b][t / P], slot t % P.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+static double bf16_to_f64(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Where the K (or V) row of logical token t of request b, kv head g lives. */
+typedef struct {
+    const uint16_t *base;     /* K or V */
+    int paged;
+    /* contiguous [B, S_max, Hkv, D] */
+    int s_max;
+    /* paged [num_pages, P, Hkv, D] */
+    const int32_t *block_table;
+    int max_blocks;
+    int page;
+    int num_pages;
+    int hkv;
+    int d;
+} kv_view;
+
+/* Returns NULL if the token's page is not a valid physical page. */
+static const uint16_t *kv_row(const kv_view *w, int b, int t, int g)
+{
+    int64_t row;
+    if (!w->paged) {
+        row = ((int64_t)b * w->s_max + t) * w->hkv + g;
+    } else {
+        int32_t phys = w->block_table[(int64_t)b * w->max_blocks + t / w->page];
+        if (phys < 0 || phys >= w->num_pages)
+            return NULL;
+        row = ((int64_t)phys * w->page + t % w->page) * w->hkv + g;
+    }
+    return w->base + row * w->d;
+}
+
+/*
+ * One query row (request b, query head h) against tokens [t0, t1).
+ * Writes o[0..d) and *lse.  An empty range gives o = 0, lse = -inf.
+ * Returns 0, or -1 when a referenced page is out of range.
+ */
+static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
+                      int b, int h, int hq, int t0, int t1, double scale,
+                      double *s /* scratch, >= t1 - t0 */, double *o, double *lse)
+{
+    const int d = kw->d;
+    const int group = hq / kw->hkv;
+    const int g = h / group;
+    const uint16_t *qrow = q + ((int64_t)b * hq + h) * d;
+    const int n = t1 - t0;
+
+    for (int j = 0; j < d; ++j)
+        o[j] = 0.0;
+    if (n <= 0) {
+        *lse = -INFINITY;
+        return 0;
+    }
+
+    /* S = scale * q . K_t */
+    double mx = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+        const uint16_t *krow = kv_row(kw, b, t0 + i, g);
+        if (!krow)
+            return -1;
+        double dot = 0.0;
+        for (int j = 0; j < d; ++j)
+            dot += bf16_to_f64(qrow[j]) * bf16_to_f64(krow[j]);
+        s[i] = scale * dot;
+        if (s[i] > mx)
+            mx = s[i];
+    }
+
+    /* P = exp(S - max) / Z ; LSE = max + ln Z */
+    double z = 0.0;
+    for (int i = 0; i < n; ++i) {
+        s[i] = exp(s[i] - mx);
+        z += s[i];
+    }
+    *lse = mx + log(z);
+
+    /* O = sum_t P_t V_t */
+    for (int i = 0; i < n; ++i) {
+        const uint16_t *vrow = kv_row(vw, b, t0 + i, g);
+        if (!vrow)
+            return -1;
+        const double p = s[i] / z;
+        for (int j = 0; j < d; ++j)
+            o[j] += p * bf16_to_f64(vrow[j]);
+    }
+    return 0;
+}
+
+/*
+ * For each of npairs items (b, h, t0, t1) in `items` (int32, 4 per item;
+ * t1 < 0 means "to the request's length"), compute the attention of query
+ * (b, h) over tokens [t0, min(t1, L_b)).  o is [npairs][d], lse [npairs].
+ * page_size == 0 selects the contiguous layout (k, v are [B, S_max, Hkv, D]);
+ * otherwise k, v are pages [num_pages, P, Hkv, D] behind block_table.
+ * scratch must hold max token count doubles.  Returns 0, or -1 on a bad page
+ * or a length outside the layout.
+ */
+int oracle_attend(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  const int32_t *seq_lens, int batch, int hq, int hkv, int d,
+                  int s_max, int page_size, const int32_t *block_table,
+                  int max_blocks, int num_pages, double scale,
+                  const int32_t *items, int npairs, double *scratch,
+                  double *o, double *lse)
+{
+    if (hkv <= 0 || hq % hkv != 0)
+        return -1;
+    kv_view kw = {k, page_size > 0, s_max, block_table, max_blocks, page_size, num_pages, hkv, d};
+    kv_view vw = kw;
+    vw.base = v;
+    for (int i = 0; i < npairs; ++i) {
+        const int b = items[4 * i + 0], h = items[4 * i + 1];
+        int t0 = items[4 * i + 2], t1 = items[4 * i + 3];
+        if (b < 0 || b >= batch || h < 0 || h >= hq)
+            return -1;
+        const int L = seq_lens[b];
+        if (L < 0)
+            return -1;
+        if (page_size == 0 && L > s_max)
+            return -1;
+        if (page_size > 0 && L > (int64_t)max_blocks * page_size)
+            return -1;
+        if (t1 < 0 || t1 > L)
+            t1 = L;
+        if (t0 < 0)
+            t0 = 0;
+        if (attend_one(q, &kw, &vw, b, h, hq, t0, t1, scale, scratch,
+                       o + (int64_t)i * d, lse + i) != 0)
+            return -1;
+    }
+    return 0;
+}
+
+/*
+ * Merge n partial results (normalised O_i [n][d], natural-log lse_i) into one
+ * output o[d] and its log-sum-exp.  Partials with lse = -inf carry no tokens
+ * and are skipped; if all are skipped, o = 0 and lse = -inf.
+ */
+void oracle_lse_merge(const double *o_parts, const double *lse_parts, int n, int d,
+                      double *o, double *lse)
+{
+    double lse_max = -INFINITY;
+    for (int i = 0; i < n; ++i)
+        if (lse_parts[i] > lse_max)
+            lse_max = lse_parts[i];
+    for (int j = 0; j < d; ++j)
+        o[j] = 0.0;
+    if (lse_max == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i)
+        if (lse_parts[i] != -INFINITY)
+            sum += exp(lse_parts[i] - lse_max);
+    const double g = lse_max + log(sum);
+    for (int i = 0; i < n; ++i) {
+        if (lse_parts[i] == -INFINITY)
+            continue;
+        const double w = exp(lse_parts[i] - g);
+        for (int j = 0; j < d; ++j)
+            o[j] += o_parts[(int64_t)i * d + j] * w;
+    }
+    *lse = g;
+}
+
+/*
+ * Online softmax over one row of scores s[0..n) with value rows
+ * val[n][dv], taken `block` scores at a time.  After block j it records
+ * m_j, l_j and the unnormalised O_j (dv values) into m_out[j], l_out[j],
+ * o_out[j][dv].  The final output is O_last / l_last, written to o_final.
+ * Returns the number of blocks.
+ */
+int oracle_online_blocks(const double *s, const double *val, int n, int dv, int block,
+                         double *m_out, double *l_out, double *o_out, double *o_final)
+{
+    double m = -INFINITY, l = 0.0;
+    double acc[64];
+    if (dv > 64 || block <= 0)
+        return -1;
+    for (int j = 0; j < dv; ++j)
+        acc[j] = 0.0;
+    int nb = 0;
+    for (int b0 = 0; b0 < n; b0 += block, ++nb) {
+        const int b1 = b0 + block < n ? b0 + block : n;
+        double rowmax = -INFINITY;
+        for (int i = b0; i < b1; ++i)
+            if (s[i] > rowmax)
+                rowmax = s[i];
+        const double m_new = m > rowmax ? m : rowmax;
+        const double corr = (m == -INFINITY) ? 0.0 : exp(m - m_new);
+        double rowsum = 0.0;
+        for (int j = 0; j < dv; ++j)
+            acc[j] *= corr;
+        for (int i = b0; i < b1; ++i) {
+            const double p = exp(s[i] - m_new);
+            rowsum += p;
+            for (int j = 0; j < dv; ++j)
+                acc[j] += p * val[(int64_t)i * dv + j];
+        }
+        l = corr * l + rowsum;
+        m = m_new;
+        m_out[nb] = m;
+        l_out[nb] = l;
+        for (int j = 0; j < dv; ++j)
+            o_out[(int64_t)nb * dv + j] = acc[j];
+    }
+    for (int j = 0; j < dv; ++j)
+        o_final[j] = (nb > 0) ? acc[j] / l : 0.0;
+    return nb;
+}
