@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Benchmark: split-KV decode attention on GB300 (one JSON line on stdout).
+
+Default workload: MHA long-KV decode -- batch 1, 32 query heads = 32 kv heads,
+head_dim 128, kv_len 65536, contiguous [S, H, D] bf16 K/V, scale 1/sqrt(128)
+(1 GiB of K+V, larger than the 129 MB L2, so no flush is needed between
+steps).  A step is one fd_decode call: the split kernel plus the LSE merge.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica of the workload (the path
+shards by request/head with no exchange), the timed region is bracketed by a
+barrier and cudaDeviceSynchronize on every rank, and rank 0 prints the
+whole-job throughput using the slowest rank's time.
+
+`--impl reference` times the CPU oracle (the pages' method as plain fp64 C)
+on the host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import fd_synth as syn  # noqa: E402
+
+METRIC = "decode-attn µs/call and achieved HBM TB/s (fraction of GB300 peak) on 1 GPU"
+KERNEL_SOURCES = ["decode_attention_decoding_gb300/csrc/fd_kernels.cuh",
+                  "decode_attention_decoding_gb300/csrc/fd_device.cuh",
+                  "decode_attention_decoding_gb300/csrc/fd_sched.h"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+TILE = 64
+MAX_CTAS = 1024
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic byte counts (K+V of valid tokens once, q, O, LSE,
+# the workspace partials written once and read once)
+# ---------------------------------------------------------------------------
+
+def partial_count(lens, hkv, P):
+    """Number of (CTA, segment) partials the stream-K split writes (host mirror of fd_sched.h)."""
+    nt = [(int(L) + TILE - 1) // TILE for L in lens]
+    T = hkv * sum(nt)
+    if T == 0:
+        return 0
+    base, rem = divmod(T, P)
+    cut = rem * (base + 1)
+
+    def cta(t):
+        return t // (base + 1) if t < cut else rem + (t - cut) // base
+
+    n = 0
+    first = 0
+    for b, k in enumerate(nt):
+        for _h in range(hkv):
+            if k:
+                c0, c1 = cta(first), cta(first + k - 1)
+                if c1 > c0:
+                    n += c1 - c0 + 1
+                first += k
+    return n
+
+
+def byte_counts(w, P):
+    B, hq, d = w.q.shape
+    hkv, G = w.num_kv_heads, w.num_q_heads // w.num_kv_heads
+    kv = w.kv_bytes()
+    q = B * hq * d * 2
+    out = B * hq * d * 4 + B * hq * 4
+    parts = partial_count(w.seq_lens, hkv, P)
+    ws = parts * G * (d + 1) * 4
+    table = (sum((int(L) + w.page_size - 1) // w.page_size for L in w.seq_lens) * 4) if w.paged else 0
+    return dict(kv=kv, q=q, out=out, ws_partials=parts, ws_once=ws, table=table, lens=B * 4,
+                call=kv + q + out + 2 * ws,
+                split=kv + q + ws + out)   # split reads K,V,q; writes partials or final O/LSE
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.4)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t_start, t_end):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world):
+    import torch
+    import decode_attention_decoding_gb300 as fd
+    from decode_attention_decoding_gb300 import build as fdb
+    fdb.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = syn.make_config(args.config)
+    B, hq, d = w.q.shape
+    hkv = w.num_kv_heads
+
+    def todev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = todev(w.q), todev(w.k), todev(w.v)
+    lens = torch.from_numpy(w.seq_lens.astype(np.int32)).to(dev)
+    lens_h = torch.from_numpy(w.seq_lens.astype(np.int32))
+    table = torch.from_numpy(w.block_table.astype(np.int32)).to(dev) if w.paged else None
+    cap = w.max_blocks * w.page_size if w.paged else w.s_max
+    ws = fd.make_workspace(B, hq, hkv, d, cap, w.page_size, dev)
+    out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    P = props.multi_processor_count
+    l2 = getattr(props, "L2_cache_size", 0) or 0
+
+    # L2 control: rotate through copies of K/V whose total exceeds 2x L2 when
+    # one copy would fit in L2 (config 1); otherwise the inputs alone exceed L2.
+    copies = 1
+    kv_alloc = (w.k.nbytes + w.v.nbytes)
+    if l2 and kv_alloc < 2 * l2:
+        copies = int(np.ceil(2 * l2 / kv_alloc)) + 1
+    kvs = [(k, v)] + [(k.clone(), v.clone()) for _ in range(copies - 1)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, events=None):
+        kk, vv = kvs[i % copies]
+        if w.paged:
+            fd.fd_decode_paged(q, kk, vv, table, lens, scale=w.scale, out=out, lse=lse, workspace=ws,
+                               split_events=events)
+        else:
+            fd.fd_decode(q, kk, vv, lens, scale=w.scale, out=out, lse=lse, workspace=ws,
+                         split_events=events)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert fd.fd_get_device_error(ws) == fd.FD_OK
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        e0.record(stream)
+        for i in range(K):
+            step(i, ev[i])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        if dist:
+            dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    split_ms = [a.elapsed_time(b) for a, b in ev]
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / K
+    bc = byte_counts(w, P)
+    value_tbs = world * bc["call"] / (ms_step * 1e-3) / 1e12
+    split_avg_ms = float(np.mean(split_ms))
+    peaks, peak_src = measured_peaks()
+    achieved_gbs = bc["split"] / (split_avg_ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        tj = json.load(open(TRAFFIC_FILE))
+        if tj.get("kernel_hash") == kernel_hash() and tj.get("workload") == syn.CONFIG_NAMES[args.config]:
+            traffic = tj.get("traffic_bytes_per_launch")
+    except Exception:
+        pass
+
+    # End to end through the public API: pinned host inputs -> device, decode,
+    # result -> host, every step.
+    e2e = None
+    if not args.no_e2e:
+        hq_, hk_, hv_ = (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
+                         for x in (w.q, w.k, w.v))
+        hl_ = lens_h.pin_memory()
+        ho = torch.empty((B, hq, d), dtype=torch.float32).pin_memory()
+        hlse = torch.empty((B, hq), dtype=torch.float32).pin_memory()
+        dq, dk, dv = (torch.empty(x.shape, dtype=torch.int16, device=dev) for x in (hq_, hk_, hv_))
+        dl = torch.empty_like(lens)
+        K2 = max(3, min(K, args.e2e_steps))
+
+        def e2e_step():
+            dq.copy_(hq_, non_blocking=True)
+            dk.copy_(hk_, non_blocking=True)
+            dv.copy_(hv_, non_blocking=True)
+            dl.copy_(hl_, non_blocking=True)
+            qb, kb, vb = dq.view(torch.bfloat16), dk.view(torch.bfloat16), dv.view(torch.bfloat16)
+            if w.paged:
+                fd.fd_decode_paged(qb, kb, vb, table, dl, scale=w.scale, out=out, lse=lse, workspace=ws)
+            else:
+                fd.fd_decode(qb, kb, vb, dl, scale=w.scale, out=out, lse=lse, workspace=ws)
+            ho.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K2):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / K2
+        if dist:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = hq_.nbytes + hk_.nbytes + hv_.nbytes + hl_.nbytes
+        d2h = ho.numel() * 4 + hlse.numel() * 4
+        e2e = {"value": world * bc["call"] / (e2e_ms * 1e-3) / 1e12, "unit": "TB/s",
+               "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": K2}
+
+    err = fd.fd_get_device_error(ws)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value_tbs, "unit": "TB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "us_per_call": ms_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "frac_of_peak_hbm": value_tbs * 1e3 / world / peaks["hbm_gbs"],
+            "dtype": "f32", "input_dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
+            "impl": "ours",
+            "config": {"workload": syn.CONFIG_NAMES[args.config], "batch": B, "num_q_heads": hq,
+                       "num_kv_heads": hkv, "head_dim": d,
+                       "kv_lens": ("uniform " + str(int(w.seq_lens[0]))) if len(set(w.seq_lens.tolist())) == 1
+                       else f"ragged sum={int(w.seq_lens.sum())}",
+                       "layout": f"paged P={w.page_size}" if w.paged else "contiguous",
+                       "split_ctas": P, "parallelism": f"replicas x{world}",
+                       "l2": (f"rotating {copies} K/V copies (> 2x L2)" if copies > 1
+                              else f"inputs {kv_alloc / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB, no flush")},
+            "bytes_per_call": bc["call"], "bytes_detail": bc,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                         "kernel": "fd::split_kernel", "split_us": split_avg_ms * 1e3,
+                         "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"},
+            "gpu_launches": 2 * K,
+            "clocks": clk.summary(t_wall0, t_wall1),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "device_error": fd.fd_status_string(err),
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, n_rows):
+    """The first n_rows (b, h) query rows over their whole length."""
+    B, hq = w.batch, w.num_q_heads
+    rows = [(b, h) for b in range(B) for h in range(hq)][:max(1, n_rows)]
+    items = np.array([[b, h, 0, -1] for b, h in rows], dtype=np.int32)
+    toks = sum(int(w.seq_lens[b]) for b, _ in rows)
+    # bytes the oracle streams for these rows: K+V row per token (per query head)
+    return items, toks * w.head_dim * 2 * 2
+
+
+def time_oracle(w, items, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attend(w, items=items, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, seconds):
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    total_rows = w.batch * w.num_q_heads
+    # calibrate on a few rows, then size the sample to about `seconds`
+    n = min(total_rows, threads)
+    items, by = oracle_sample(w, n)
+    dt = time_oracle(w, items, threads)
+    n = int(min(total_rows, max(n, n * seconds / max(dt, 1e-3))))
+    items, by = oracle_sample(w, n)
+    dt = time_oracle(w, items, threads)
+    return {"value": by / dt / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{n} of {total_rows} query rows (whole kv length each), fp64 C oracle, "
+                      f"{threads} threads; bytes = K+V rows streamed per query row"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = syn.make_config(args.config)
+    threads = os.cpu_count() or 1
+    total_rows = w.batch * w.num_q_heads
+    budget = max(1.0, args.reference_budget_s / max(1, args.steps + args.warmup))
+    n = min(total_rows, threads)
+    items, by = oracle_sample(w, n)
+    dt = time_oracle(w, items, threads)
+    n = int(min(total_rows, max(1, n * budget / max(dt, 1e-3))))
+    items, by = oracle_sample(w, n)
+    for _ in range(args.warmup):
+        time_oracle(w, items, threads)
+    ts = [time_oracle(w, items, threads) for _ in range(args.steps)]
+    t = float(np.sum(ts))
+    value = args.steps * by / t / 1e12
+    sample = (f"{n} of {total_rows} query rows per step (whole kv length each), fp64 C oracle, "
+              f"{threads} threads")
+    line = {"metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "input_dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16)", "impl": "reference",
+            "config": {"workload": syn.CONFIG_NAMES[args.config], "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "TB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

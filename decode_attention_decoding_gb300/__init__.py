@@ -1,0 +1,231 @@
+"""Split-KV ("Flash-Decoding") single-query decode attention for GB300.
+
+A thin ctypes binding over ``libfd.so`` (the C ABI of ``include/fd.h``).  The
+functions carry the C names and only marshal arguments: every step of the
+computation runs in the library's CUDA kernels.  PyTorch supplies device
+memory and the current stream.  There is no CPU fallback: if the library is
+missing, the first call raises ImportError.
+
+Build the library first with ``python -m decode_attention_decoding_gb300.build``
+(or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "FdError", "fd_workspace_size", "fd_workspace_init", "fd_decode", "fd_decode_paged",
+    "fd_get_device_error", "fd_status_string", "fd_version", "make_workspace", "library_path",
+    "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
+    "FD_ERR_CUDA", "FD_ERR_TIMEOUT", "FD_ERR_DEVICE_INPUT", "FD_FLAG_TEST_STARVE_FIRST_TILE",
+]
+
+FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
+FD_ERR_CUDA, FD_ERR_TIMEOUT, FD_ERR_DEVICE_INPUT = 4, 5, 6
+FD_FLAG_TEST_STARVE_FIRST_TILE = 0x1
+
+_P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class FdOptions(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int), ("flags", ctypes.c_uint),
+                ("wait_timeout_ns", ctypes.c_ulonglong),
+                ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _load():
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -m decode_attention_decoding_gb300.build`")
+    lib = ctypes.CDLL(path)
+    lib.fd_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
+    lib.fd_workspace_size.restype = _SZ
+    lib.fd_workspace_init.argtypes = [_P, _SZ, _P]
+    lib.fd_workspace_init.restype = _I
+    lib.fd_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _SZ,
+                              ctypes.POINTER(FdOptions), _P]
+    lib.fd_decode.restype = _I
+    lib.fd_decode_paged.argtypes = [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                                    _P, _SZ, ctypes.POINTER(FdOptions), _P]
+    lib.fd_decode_paged.restype = _I
+    lib.fd_get_device_error.argtypes = [_P, _P]
+    lib.fd_get_device_error.restype = _I
+    lib.fd_status_string.argtypes = [_I]
+    lib.fd_status_string.restype = ctypes.c_char_p
+    lib.fd_version.argtypes = []
+    lib.fd_version.restype = _I
+    return lib
+
+
+class _Lazy:
+    """Loads libfd.so on first use; raises ImportError if it has not been built."""
+    _lib = None
+
+    def __getattr__(self, name):
+        if _Lazy._lib is None:
+            _Lazy._lib = _load()
+        return getattr(_Lazy._lib, name)
+
+
+_lib = _Lazy()
+
+
+class FdError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fd_status_string(status)}")
+
+
+def fd_status_string(status: int) -> str:
+    return _lib.fd_status_string(int(status)).decode()
+
+
+def fd_version() -> int:
+    return _lib.fd_version()
+
+
+def fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim=128, max_kv_len=0, page_size=0) -> int:
+    return int(_lib.fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_kv_len, page_size))
+
+
+def _stream_ptr(stream, device=None):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def fd_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    st = _lib.fd_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream_ptr(stream, workspace.device))
+    if st != FD_OK:
+        raise FdError(st, "fd_workspace_init")
+
+
+def make_workspace(batch, num_q_heads, num_kv_heads, head_dim=128, max_kv_len=0, page_size=0,
+                   device="cuda") -> torch.Tensor:
+    """Allocate (with torch) and initialise a workspace for this shape."""
+    n = fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_kv_len, page_size)
+    if n == 0:
+        raise FdError(FD_ERR_INVALID_ARG, "fd_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    fd_workspace_init(ws)
+    return ws
+
+
+def _bits(t, name):
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must be bf16 (or its 16-bit pattern), got {t.dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t
+
+
+def _i32(t, name):
+    if t is None:
+        return None
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise TypeError(f"{name} must be contiguous int32")
+    return t
+
+
+def _options(num_ctas, flags, wait_timeout_ns, split_events):
+    ev0 = ev1 = None
+    if split_events is not None:
+        ev0 = ctypes.c_void_p(split_events[0].cuda_event)
+        ev1 = ctypes.c_void_p(split_events[1].cuda_event)
+    return FdOptions(int(num_ctas), int(flags), int(wait_timeout_ns), ev0, ev1)
+
+
+def _outputs(q, out, lse):
+    B, hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    if out.dtype != torch.float32 or not out.is_contiguous() or tuple(out.shape) != (B, hq, d):
+        raise ValueError("out must be contiguous fp32 [B, Hq, D]")
+    if lse is not False and (lse.dtype != torch.float32 or not lse.is_contiguous()
+                             or tuple(lse.shape) != (B, hq)):
+        raise ValueError("lse must be contiguous fp32 [B, Hq]")
+    return out, lse
+
+
+def fd_decode(q, k, v, seq_lens=None, seq_lens_host=None, scale=None, out=None, lse=None,
+              workspace=None, num_ctas=0, flags=0, wait_timeout_ns=0, split_events=None,
+              stream=None, check=True):
+    """Decode attention over a contiguous KV cache (see fd_decode in include/fd.h).
+
+    q [B, Hq, D], k/v [B, S_max, Hkv, D] bf16 CUDA tensors; seq_lens int32 [B]
+    on the device (None = every request has S_max tokens); seq_lens_host an
+    optional CPU int32 copy used only for host-side validation.  Pass
+    ``lse=False`` to skip the LSE output.  Returns (out, lse).
+    """
+    _bits(q, "q"); _bits(k, "k"); _bits(v, "v")
+    B, hq, d = q.shape
+    _, s_max, hkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out, lse = _outputs(q, out, lse)
+    if workspace is None:
+        workspace = make_workspace(B, hq, hkv, d, s_max, 0, q.device)
+    opts = _options(num_ctas, flags, wait_timeout_ns, split_events)
+    lh = None
+    if seq_lens_host is not None:
+        lh = seq_lens_host.to(torch.int32).contiguous().cpu()
+    st = _lib.fd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(_i32(seq_lens, "seq_lens")), _ptr(lh),
+                        B, hq, hkv, d, s_max, float(scale), _ptr(out),
+                        None if lse is False else _ptr(lse), _ptr(workspace),
+                        workspace.numel(), ctypes.byref(opts), _stream_ptr(stream, q.device))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_decode")
+    return out, (None if lse is False else lse)
+
+
+def fd_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=None, scale=None,
+                    out=None, lse=None, workspace=None, num_ctas=0, flags=0, wait_timeout_ns=0,
+                    split_events=None, stream=None, check=True):
+    """Decode attention over a paged KV cache (see fd_decode_paged in include/fd.h).
+
+    k_pages/v_pages [num_pages, P, Hkv, D] bf16; block_table int32 [B, max_blocks];
+    seq_lens int32 [B] on the device.
+    """
+    _bits(q, "q"); _bits(k_pages, "k_pages"); _bits(v_pages, "v_pages")
+    _i32(block_table, "block_table"); _i32(seq_lens, "seq_lens")
+    B, hq, d = q.shape
+    num_pages, page, hkv, _ = k_pages.shape
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out, lse = _outputs(q, out, lse)
+    if workspace is None:
+        workspace = make_workspace(B, hq, hkv, d, max_blocks * page, page, q.device)
+    opts = _options(num_ctas, flags, wait_timeout_ns, split_events)
+    lh = None
+    if seq_lens_host is not None:
+        lh = seq_lens_host.to(torch.int32).contiguous().cpu()
+    st = _lib.fd_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), max_blocks,
+                              _ptr(seq_lens), _ptr(lh), B, hq, hkv, d, page, num_pages, float(scale),
+                              _ptr(out), None if lse is False else _ptr(lse), _ptr(workspace),
+                              workspace.numel(), ctypes.byref(opts), _stream_ptr(stream, q.device))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_decode_paged")
+    return out, (None if lse is False else lse)
+
+
+def fd_get_device_error(workspace, stream=None) -> int:
+    """Read and clear the workspace's sticky device-error word (synchronises the stream)."""
+    return int(_lib.fd_get_device_error(_ptr(workspace), _stream_ptr(stream, workspace.device)))

@@ -1,0 +1,369 @@
+// fd_api.cu -- the C ABI of include/fd.h: argument checks, workspace layout,
+// split planning, TMA descriptors and the two launches.
+//
+// Host side of "纯手搓 flash decoding sm120" section 1 (binding and launch
+// code), re-planned for GB300: instead of a chunk size bucketed from a fixed
+// SM count, the grid is one persistent CTA per SM and the device divides the
+// KV tiles of all (request, kv head) pairs evenly among them (fd_sched.h),
+// so the plan needs no host copy of the lengths and no per-call allocation.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fd.h"
+#include "fd_launch.h"
+#include "fd_sched.h"
+
+namespace {
+
+using namespace fd;
+
+constexpr int kVersion = 10000;   // 1.0.0
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+// The one piece of state kept across calls: a cache of device properties.
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+bool g_dev_ok[64] = {};
+
+fd_status device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return FD_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_ok[dev]) {
+        DeviceInfo d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return FD_ERR_CUDA;
+        g_dev[dev] = d;
+        g_dev_ok[dev] = true;
+    }
+    *out = g_dev[dev];
+    return FD_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// A rank-3 view {head_dim, Hkv, rows} of a bf16 K or V tensor whose rows are
+// (token, kv head) pairs of 256 bytes; each load is a box of box_rows tokens
+// of one kv head.
+fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return FD_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)hkv * kRowBytes};
+    const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+// Checks shared by both entry points.  Returns FD_OK or the status to report.
+fd_status check_common(const void *q, const float *o, const void *ws, int batch, int hq, int hkv,
+                       int head_dim)
+{
+    if (batch < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0)
+        return FD_ERR_INVALID_ARG;
+    if (!q || !o || !ws)
+        return FD_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(o, 16) || !aligned(ws, 256))
+        return FD_ERR_INVALID_ARG;
+    if (head_dim != kHeadDim || !supported_group(hq / hkv) || batch > kMaxBatch)
+        return FD_ERR_UNSUPPORTED;
+    return FD_OK;
+}
+
+struct CallPlan {
+    SplitParams sp;
+    MergeParams mp;
+    SplitLaunch launch;
+    int group;
+};
+
+// Shared-memory plan of the split kernel for `group` and `batch`; fills the
+// offsets and stage count in sp and the byte size in launch.
+fd_status plan_smem(const DeviceInfo &dev, int group, int batch, SplitParams *sp, SplitLaunch *launch)
+{
+    const size_t red = align_up((size_t)kConsumerWarps * group * (kHeadDim + 2) * sizeof(float), 16);
+    const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
+    const size_t misc = 64;
+    const size_t per_stage_extra = 2 * 8 + kMetaInts * sizeof(int);   // 2 barriers + metadata
+    const size_t fixed = 1024 /* alignment slack */ + red + prefix + misc + 8 /* consumer barrier */;
+    const size_t avail = (size_t)dev.smem_optin;
+    if (avail <= fixed)
+        return FD_ERR_UNSUPPORTED;
+    int ns = (int)((avail - fixed) / (kStageBytes + per_stage_extra));
+    if (ns > kMaxStages)
+        ns = kMaxStages;
+    if (ns < 2)
+        return FD_ERR_UNSUPPORTED;
+    sp->num_stages = ns;
+    sp->off_red = (uint32_t)(ns * kStageBytes);
+    sp->off_prefix = (uint32_t)(sp->off_red + red);
+    sp->off_bar = (uint32_t)(sp->off_prefix + prefix);
+    sp->off_meta = (uint32_t)(sp->off_bar + (2 * ns + 1) * 8);
+    sp->off_misc = (uint32_t)(sp->off_meta + ns * kMetaInts * sizeof(int));
+    launch->smem_bytes = 1024 + sp->off_misc + misc;
+    launch->smem_optin = (size_t)dev.smem_optin;
+    return launch->smem_bytes <= avail ? FD_OK : FD_ERR_UNSUPPORTED;
+}
+
+fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const int32_t *seq_lens_dev,
+                    const int32_t *block_table, int batch, int hq, int hkv, int cap, int s_max,
+                    int page_size, int max_blocks, int num_pages, float scale, float *o, float *lse,
+                    void *workspace, const fd_options *opts, fd_stream_t stream)
+{
+    const int group = hq / hkv;
+    const WorkspaceLayout wl = workspace_layout(batch, hkv, group, kHeadDim);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int num_ctas = opts && opts->num_ctas > 0 ? opts->num_ctas : dev.sms;
+    if (num_ctas > kMaxCtas)
+        return FD_ERR_INVALID_ARG;
+
+    SplitParams &sp = cp->sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.q = static_cast<const uint16_t *>(q);
+    sp.seq_lens = seq_lens_dev;
+    sp.block_table = block_table;
+    sp.o = o;
+    sp.lse = lse;
+    sp.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+    sp.ws_lse = reinterpret_cast<float *>(ws + wl.lse_off);
+    sp.ws_prefix = reinterpret_cast<int32_t *>(ws + wl.prefix_off);
+    sp.ws_err = reinterpret_cast<unsigned int *>(ws + wl.err_off);
+    sp.batch = batch;
+    sp.hq = hq;
+    sp.hkv = hkv;
+    sp.cap = cap;
+    sp.s_max = s_max;
+    sp.page_size = page_size;
+    sp.max_blocks = max_blocks;
+    sp.num_pages = num_pages;
+    sp.scale_log2 = scale * 1.4426950408889634f;
+    sp.timeout_ns = opts && opts->wait_timeout_ns ? opts->wait_timeout_ns : kDefaultTimeoutNs;
+    sp.flags = opts ? opts->flags : 0u;
+
+    cp->launch.grid = num_ctas;
+    cp->launch.stream = reinterpret_cast<cudaStream_t>(stream);
+    fd_status st = plan_smem(dev, group, batch, &sp, &cp->launch);
+    if (st != FD_OK)
+        return st;
+
+    MergeParams &mp = cp->mp;
+    mp.o = o;
+    mp.lse = lse;
+    mp.ws_o = sp.ws_o;
+    mp.ws_lse = sp.ws_lse;
+    mp.ws_prefix = sp.ws_prefix;
+    mp.batch = batch;
+    mp.hq = hq;
+    mp.hkv = hkv;
+    mp.num_ctas = num_ctas;
+    cp->group = group;
+    return FD_OK;
+}
+
+fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUtensorMap &tmv,
+              const fd_options *opts)
+{
+    cudaStream_t stream = cp.launch.stream;
+    cudaEvent_t ev0 = opts ? static_cast<cudaEvent_t>(opts->split_start_event) : nullptr;
+    cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_end_event) : nullptr;
+    if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess)
+        return FD_ERR_CUDA;
+    cudaError_t e = paged ? launch_split_paged(cp.group, cp.sp, tmk, tmv, cp.launch)
+                          : launch_split_contig(cp.group, cp.sp, tmk, tmv, cp.launch);
+    if (e != cudaSuccess)
+        return FD_ERR_CUDA;
+    if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess)
+        return FD_ERR_CUDA;
+    e = launch_merge(cp.group, cp.mp, cp.sp.batch * cp.sp.hkv, stream);
+    if (e != cudaSuccess)
+        return FD_ERR_CUDA;
+    return FD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_kv_len,
+                         int page_size)
+{
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kv_len < 0 ||
+        page_size < 0 || num_q_heads % num_kv_heads != 0)
+        return 0;
+    return workspace_layout(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim).total;
+}
+
+fd_status fd_workspace_init(void *workspace, size_t workspace_bytes, fd_stream_t stream)
+{
+    if (!workspace || workspace_bytes < 256 || !aligned(workspace, 256))
+        return FD_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, 256, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FD_OK
+               : FD_ERR_CUDA;
+}
+
+fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *seq_lens_dev,
+                    const int32_t *seq_lens_host, int batch, int num_q_heads, int num_kv_heads,
+                    int head_dim, int s_max, float scale, float *o, float *lse, void *workspace,
+                    size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
+{
+    fd_status st = check_common(q, o, workspace, batch, num_q_heads, num_kv_heads, head_dim);
+    if (st != FD_OK)
+        return st;
+    if (s_max < 0 || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    if (seq_lens_host)
+        for (int b = 0; b < batch; ++b)
+            if (seq_lens_host[b] < 0 || seq_lens_host[b] > s_max)
+                return FD_ERR_INVALID_ARG;
+    if (opts && (opts->num_ctas < 0 || opts->num_ctas > kMaxCtas))
+        return FD_ERR_INVALID_ARG;
+    if ((long long)batch * s_max >= (1ll << 31) ||
+        (long long)num_kv_heads * batch * ceil_div(s_max, kTileTokens) >= (1ll << 31))
+        return FD_ERR_UNSUPPORTED;
+    if (workspace_bytes < fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, s_max, 0))
+        return FD_ERR_WORKSPACE_TOO_SMALL;
+    if (batch == 0)
+        return FD_OK;
+
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != FD_OK)
+        return st;
+    CallPlan cp;
+    st = fill_plan(&cp, dev, q, seq_lens_dev, nullptr, batch, num_q_heads, num_kv_heads, s_max, s_max,
+                   0, 0, 0, scale, o, lse, workspace, opts, stream);
+    if (st != FD_OK)
+        return st;
+    alignas(64) CUtensorMap tmk, tmv;
+    const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
+    if ((st = encode_kv_map(&tmk, k, num_kv_heads, rows, kTileTokens)) != FD_OK ||
+        (st = encode_kv_map(&tmv, v, num_kv_heads, rows, kTileTokens)) != FD_OK)
+        return st;
+    return run(cp, false, tmk, tmv, opts);
+}
+
+fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                          const int32_t *block_table, int max_blocks_per_seq,
+                          const int32_t *seq_lens_dev, const int32_t *seq_lens_host, int batch,
+                          int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                          int num_pages, float scale, float *o, float *lse, void *workspace,
+                          size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
+{
+    fd_status st = check_common(q, o, workspace, batch, num_q_heads, num_kv_heads, head_dim);
+    if (st != FD_OK)
+        return st;
+    if (!k_pages || !v_pages || !block_table || !seq_lens_dev || !aligned(k_pages, 16) ||
+        !aligned(v_pages, 16) || !aligned(block_table, 4) || (lse && !aligned(lse, 4)) ||
+        max_blocks_per_seq <= 0 || page_size <= 0 || num_pages <= 0)
+        return FD_ERR_INVALID_ARG;
+    if (!((page_size < kTileTokens && kTileTokens % page_size == 0) || page_size % kTileTokens == 0))
+        return FD_ERR_UNSUPPORTED;
+    const long long cap = (long long)max_blocks_per_seq * page_size;
+    if (cap >= (1ll << 31) || (long long)num_pages * page_size >= (1ll << 31) ||
+        (long long)num_kv_heads * batch * ((cap + kTileTokens - 1) / kTileTokens) >= (1ll << 31))
+        return FD_ERR_UNSUPPORTED;
+    if (seq_lens_host)
+        for (int b = 0; b < batch; ++b)
+            if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap)
+                return FD_ERR_INVALID_ARG;
+    if (opts && (opts->num_ctas < 0 || opts->num_ctas > kMaxCtas))
+        return FD_ERR_INVALID_ARG;
+    if (workspace_bytes <
+        fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, (int)cap, page_size))
+        return FD_ERR_WORKSPACE_TOO_SMALL;
+    if (batch == 0)
+        return FD_OK;
+
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != FD_OK)
+        return st;
+    CallPlan cp;
+    st = fill_plan(&cp, dev, q, seq_lens_dev, block_table, batch, num_q_heads, num_kv_heads, (int)cap, 0,
+                   page_size, max_blocks_per_seq, num_pages, scale, o, lse, workspace, opts, stream);
+    if (st != FD_OK)
+        return st;
+    alignas(64) CUtensorMap tmk, tmv;
+    const long long rows = (long long)num_pages * page_size;
+    const int box = page_size < kTileTokens ? page_size : kTileTokens;
+    if ((st = encode_kv_map(&tmk, k_pages, num_kv_heads, rows, box)) != FD_OK ||
+        (st = encode_kv_map(&tmv, v_pages, num_kv_heads, rows, box)) != FD_OK)
+        return st;
+    return run(cp, true, tmk, tmv, opts);
+}
+
+fd_status fd_get_device_error(void *workspace, fd_stream_t stream)
+{
+    if (!workspace || !aligned(workspace, 256))
+        return FD_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return FD_ERR_CUDA;
+    if (word != 0 && (cudaMemsetAsync(workspace, 0, sizeof word, s) != cudaSuccess ||
+                      cudaStreamSynchronize(s) != cudaSuccess))
+        return FD_ERR_CUDA;
+    if (word & kErrTimeout)
+        return FD_ERR_TIMEOUT;
+    if (word & (kErrLength | kErrPage))
+        return FD_ERR_DEVICE_INPUT;
+    return FD_OK;
+}
+
+const char *fd_status_string(fd_status status)
+{
+    switch (status) {
+    case FD_OK: return "FD_OK";
+    case FD_ERR_INVALID_ARG: return "FD_ERR_INVALID_ARG";
+    case FD_ERR_UNSUPPORTED: return "FD_ERR_UNSUPPORTED";
+    case FD_ERR_WORKSPACE_TOO_SMALL: return "FD_ERR_WORKSPACE_TOO_SMALL";
+    case FD_ERR_CUDA: return "FD_ERR_CUDA";
+    case FD_ERR_TIMEOUT: return "FD_ERR_TIMEOUT";
+    case FD_ERR_DEVICE_INPUT: return "FD_ERR_DEVICE_INPUT";
+    }
+    return "FD_ERR_UNKNOWN";
+}
+
+int fd_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,647 @@
+// fd_kernels.cuh -- split-KV decode attention kernels (sm_103a, CUDA cores).
+//
+// Split kernel ("pass 1" of 纯手搓 flash decoding sm120, section 1/2; the
+// Flash-Decoding section of the FlashAttention handbook page): a persistent
+// grid of P CTAs, each taking a contiguous run of 64-token KV tiles (see
+// fd_sched.h).  Per CTA:
+//   * warp 8 is the producer: it walks the CTA's tiles and, for each, waits
+//     for a free shared-memory stage, writes the tile's metadata, and issues
+//     TMA loads of the K and V tiles (paged: one load per page, addressed
+//     through the block table) that complete on the stage's "full" mbarrier;
+//   * warps 0..7 are consumers: warp w reads rows 8w..8w+7 of every tile, two
+//     rows at a time (one per half-warp; each lane holds 8 of the 128 head
+//     dimensions, read as one 16-byte shared load).  For every query head of
+//     the kv head's GQA group it forms the score q.k in fp32 (packed
+//     fp32x2 FMAs, a 16-lane shuffle reduction), keeps an online softmax in
+//     the log2 domain (running max m, running sum l, fp32 accumulator
+//     rescaled by 2^(m_old - m_new) every tile, as in the handbook's
+//     FlashAttention section), and accumulates p * V.  It then releases the
+//     stage on its "empty" mbarrier -- there is no CTA-wide barrier per tile.
+//   * At the last tile of a segment (request, kv head) within the CTA, the
+//     consumer warps merge their 16 half-warp states through shared memory
+//     and write either the final O and natural-log LSE (the CTA saw the whole
+//     segment) or a normalised partial O and its LSE (lse = m ln2 + ln l).
+// Merge kernel ("pass 2", section 2 of the sm120 article): one CTA per
+// segment combines its partials: LSE = max + ln sum exp(lse_i - max),
+// O = sum O_i exp(lse_i - LSE).
+#pragma once
+
+#include "fd_device.cuh"
+#include "fd_sched.h"
+
+namespace fd {
+
+constexpr int kHeadDim = 128;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kSplitThreads = kConsumerThreads + 32;
+constexpr int kRowBytes = kHeadDim * 2;                 // one bf16 K or V row
+constexpr int kTileBytes = kTileTokens * kRowBytes;     // 16 KB
+constexpr int kStageBytes = 2 * kTileBytes;             // K tile + V tile
+constexpr int kMaxStages = 6;
+constexpr int kMetaInts = 8;
+constexpr int kRowsPerWarp = kTileTokens / kConsumerWarps;   // 8
+constexpr int kRowsPerHalf = kRowsPerWarp / 2;               // 4
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+static_assert(kRowsPerWarp % 2 == 0, "two rows per warp step");
+
+// Per-tile metadata flags, written by the producer into shared memory.
+enum : int { kFirstInCta = 1, kLastInCta = 2, kOwnSegment = 4 };
+
+struct SplitParams {
+    const uint16_t *q;            // [B, Hq, D] bf16 bits
+    const int32_t *seq_lens;      // [B] device, or null (every length = cap)
+    const int32_t *block_table;   // [B, max_blocks] (paged only)
+    float *o;                     // [B, Hq, D]
+    float *lse;                   // [B, Hq] or null
+    float *ws_o;                  // [slots, G, D]
+    float *ws_lse;                // [slots, G]
+    int32_t *ws_prefix;           // [B + 1]
+    unsigned int *ws_err;
+    int batch, hq, hkv;
+    int cap;                      // largest valid length
+    int s_max;                    // contiguous: token rows per request
+    int page_size, max_blocks, num_pages;
+    float scale_log2;             // scale * log2(e)
+    int num_stages;
+    uint32_t off_red, off_prefix, off_bar, off_meta, off_misc;
+    unsigned long long timeout_ns;
+    unsigned int flags;
+};
+
+struct MergeParams {
+    float *o;
+    float *lse;
+    const float *ws_o;
+    const float *ws_lse;
+    const int32_t *ws_prefix;
+    int batch, hq, hkv, num_ctas;
+};
+
+__device__ __forceinline__ int load_len(const SplitParams &p, int b, bool report)
+{
+    int L = p.seq_lens ? p.seq_lens[b] : p.cap;
+    if (L < 0 || L > p.cap) {
+        if (report)
+            atomicOr(p.ws_err, kErrLength);
+        L = L < 0 ? 0 : p.cap;
+    }
+    return L;
+}
+
+// Every lane waits (so each acquires the barrier's phase); the outcome is
+// made warp-uniform so a wait that runs out exactly at the limit cannot split
+// the warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                          const volatile int *abort_flag)
+{
+    const bool ok = mbar_wait_bounded(bar, parity, timeout_ns, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Barrier among the consumer warps only, on an mbarrier with kConsumerWarps
+// arrivals per phase, so that it can give up (bounded) instead of hanging if
+// another warp has left.
+__device__ __forceinline__ bool consumer_sync(uint32_t cbar, uint32_t &cph, uint64_t timeout_ns,
+                                              const volatile int *abort_flag, int lane)
+{
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(cbar);
+    const bool ok = warp_wait(cbar, cph, timeout_ns, abort_flag);
+    cph ^= 1u;
+    return ok;
+}
+
+// prefix[b] = Hkv * (tiles of requests < b), prefix[B] = total tiles.
+// All kSplitThreads threads take part.  scan_tmp: kSplitThreads/32 ints.
+__device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, int *scan_tmp)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kWarps = kSplitThreads / 32;
+    const int B = p.batch;
+    const int per = ceil_div(B, kSplitThreads);
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    const bool report = blockIdx.x == 0;
+    int local = 0;
+    for (int b = b0; b < b1; ++b)
+        local += ceil_div(load_len(p, b, report), kTileTokens);
+    int x = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    if (lane == 31)
+        scan_tmp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < kWarps ? scan_tmp[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off)
+                w += y;
+        }
+        if (lane < kWarps)
+            scan_tmp[lane] = w;
+    }
+    __syncthreads();
+    int run = x - local + (warp > 0 ? scan_tmp[warp - 1] : 0);
+    for (int b = b0; b < b1; ++b) {
+        prefix[b] = run * p.hkv;
+        run += ceil_div(load_len(p, b, false), kTileTokens);
+    }
+    if (tid == kSplitThreads - 1)
+        prefix[B] = run * p.hkv;
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int b = tid; b <= B; b += kSplitThreads)
+            p.ws_prefix[b] = prefix[b];
+}
+
+// ------------------------------------------------------------------ producer
+
+template <bool PAGED>
+__device__ __forceinline__ void split_producer(const SplitParams &p, const CUtensorMap *tmk,
+                                               const CUtensorMap *tmv, uint32_t stage0,
+                                               const int *prefix, int *meta, uint32_t full0,
+                                               uint32_t empty0, volatile int *abort_flag,
+                                               int t_begin, int t_end, int lane)
+{
+    if (!PAGED && lane != 0)
+        return;
+    if (lane == 0) {
+        tma_prefetch_desc(tmk);
+        tma_prefetch_desc(tmv);
+    }
+    const uint64_t policy = l2_policy_evict_first();
+    const int NS = p.num_stages;
+    const bool starve = (p.flags & 1u) && blockIdx.x == 0;
+
+    int t = t_begin;
+    int b = request_of_tile(prefix, p.batch, t);
+    int nb = (prefix[b + 1] - prefix[b]) / p.hkv;
+    int h = (t - prefix[b]) / nb;
+    int j = (t - prefix[b]) - h * nb;
+    int L = load_len(p, b, false);
+
+    // Paged: a window of 32 block-table entries (one per lane) and the next
+    // window, loaded ahead so table reads stay off the issue path.
+    int win_b = -1, win_base = 0, nxt_base = 0;
+    int win_ent = 0, nxt_ent = 0;
+    auto table_load = [&](int bb, int idx) -> int {
+        return idx < p.max_blocks ? __ldg(p.block_table + (size_t)bb * p.max_blocks + idx) : 0;
+    };
+    auto table_entry = [&](int pg) -> int {   // warp-collective, same pg in every lane
+        if (b != win_b || pg < win_base || pg >= win_base + 32) {
+            if (b == win_b && pg >= nxt_base && pg < nxt_base + 32) {
+                win_base = nxt_base;
+                win_ent = nxt_ent;
+            } else {
+                win_b = b;
+                win_base = pg & ~31;
+                win_ent = table_load(b, win_base + lane);
+            }
+            nxt_base = win_base + 32;
+            nxt_ent = table_load(b, nxt_base + lane);
+        }
+        int e = __shfl_sync(0xffffffffu, win_ent, pg - win_base);
+        if (e < 0 || e >= p.num_pages) {
+            if (lane == 0)
+                atomicOr(p.ws_err, kErrPage);
+            e = 0;
+        }
+        return e;
+    };
+
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0;
+    for (; t < t_end; ++t) {
+        bool ok;
+        if (PAGED)
+            ok = warp_wait(empty0 + 8 * s, ph ^ 1u, p.timeout_ns, abort_flag);
+        else
+            ok = mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, p.timeout_ns, abort_flag);
+        if (!ok) {
+            if (lane == 0) {
+                atomicOr(p.ws_err, kErrTimeout);
+                *abort_flag = 1;
+            }
+            break;
+        }
+        const int seg_first = prefix[b] + h * nb;
+        const int token0 = j * kTileTokens;
+        const int nvalid = min(kTileTokens, L - token0);
+        int flags = 0;
+        if (j == 0 || t == t_begin)
+            flags |= kFirstInCta;
+        if (j == nb - 1 || t == t_end - 1)
+            flags |= kLastInCta;
+        if (seg_first >= t_begin && seg_first + nb <= t_end)
+            flags |= kOwnSegment;
+
+        const uint32_t full = full0 + 8 * s;
+        const uint32_t kdst = stage0 + s * kStageBytes;
+        const uint32_t vdst = kdst + kTileBytes;
+        if (lane == 0) {
+            int *m = meta + s * kMetaInts;
+            m[0] = b;
+            m[1] = h;
+            m[2] = j;
+            m[3] = nvalid;
+            m[4] = flags;
+            m[5] = b * p.hkv + h;
+        }
+        const uint32_t extra = (starve && issued == 0) ? 256u : 0u;
+        if constexpr (!PAGED) {
+            mbar_arrive_expect_tx(full, 2 * kTileBytes + extra);
+            const int row = b * p.s_max + token0;
+            tma_load_3d(kdst, tmk, full, 0, h, row, policy);
+            tma_load_3d(vdst, tmv, full, 0, h, row, policy);
+        } else {
+            const int P = p.page_size;
+            if (P >= kTileTokens) {
+                const int phys = table_entry(token0 / P);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full, 2 * kTileBytes + extra);
+                    const int row = phys * P + (token0 % P);
+                    tma_load_3d(kdst, tmk, full, 0, h, row, policy);
+                    tma_load_3d(vdst, tmv, full, 0, h, row, policy);
+                }
+            } else {
+                const int per_tile = kTileTokens / P;
+                const int pg0 = token0 / P;
+                const int need = min(per_tile, ceil_div(nvalid, P));
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full, 2u * need * P * kRowBytes + extra);
+                for (int k = 0; k < need; ++k) {
+                    const int phys = table_entry(pg0 + k);
+                    if (lane == 0) {
+                        const int row = phys * P;
+                        tma_load_3d(kdst + k * P * kRowBytes, tmk, full, 0, h, row, policy);
+                        tma_load_3d(vdst + k * P * kRowBytes, tmv, full, 0, h, row, policy);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        ++issued;
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+        if (t + 1 < t_end && ++j == nb) {
+            j = 0;
+            if (++h == p.hkv) {
+                h = 0;
+                do {
+                    ++b;
+                } while (b < p.batch && prefix[b + 1] == prefix[b]);
+                nb = (prefix[b + 1] - prefix[b]) / p.hkv;
+                L = load_len(p, b, false);
+            }
+        }
+    }
+    // Before leaving, wait (bounded) for every load still in flight so no
+    // asynchronous copy outlives the CTA's shared memory.
+    if (lane == 0) {
+        for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
+            mbar_wait_bounded(full0 + 8 * (k % NS), (uint32_t)((k / NS) & 1), p.timeout_ns, nullptr);
+    }
+}
+
+// ------------------------------------------------------------------ consumer
+
+template <int G>
+__device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *smem, uint32_t stage0,
+                                               const int *meta, uint32_t full0, uint32_t empty0,
+                                               uint32_t cbar, volatile int *abort_flag, int t_begin,
+                                               int t_end, int cw, int lane)
+{
+    const int NS = p.num_stages;
+    const int half = lane >> 4, li = lane & 15;
+    float *red_acc = reinterpret_cast<float *>(smem + p.off_red);   // [warps][G][D]
+    float *red_m = red_acc + kConsumerWarps * G * kHeadDim;          // [warps][G]
+    float *red_l = red_m + kConsumerWarps * G;                       // [warps][G]
+    const int ctid = cw * 32 + lane;
+    constexpr int kSub = G >= 8 ? 1 : (G >= 4 ? 2 : kRowsPerHalf);   // rows per online update
+
+    float2 qf[G][4];
+    float2 acc[G][4];
+    float m[G], l[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        m[g] = kNegInf;
+        l[g] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            acc[g][c] = make_float2(0.f, 0.f);
+            qf[g][c] = make_float2(0.f, 0.f);
+        }
+    }
+
+    int s = 0;
+    uint32_t ph = 0, cph = 0;
+    auto give_up = [&]() {
+        if (lane == 0) {
+            atomicOr(p.ws_err, kErrTimeout);
+            *abort_flag = 1;
+        }
+    };
+    for (int t = t_begin; t < t_end; ++t) {
+        if (!warp_wait(full0 + 8 * s, ph, p.timeout_ns, abort_flag)) {
+            if (lane == 0) {
+                atomicOr(p.ws_err, kErrTimeout);
+                *abort_flag = 1;
+            }
+            return;
+        }
+        const int *mt = meta + s * kMetaInts;
+        const int b = mt[0], h = mt[1], nvalid = mt[3], flags = mt[4], u = mt[5];
+
+        if (flags & kFirstInCta) {
+            const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint16_t *qp = p.q + ((size_t)b * p.hq + (size_t)h * G + g) * kHeadDim + li * 8;
+                const uint4 raw = ldg128_nc(qp);
+                qf[g][0] = mul2(bf16x2_to_float2(raw.x), c2);
+                qf[g][1] = mul2(bf16x2_to_float2(raw.y), c2);
+                qf[g][2] = mul2(bf16x2_to_float2(raw.z), c2);
+                qf[g][3] = mul2(bf16x2_to_float2(raw.w), c2);
+            }
+        }
+
+        const uint32_t kbase = stage0 + s * kStageBytes + li * 16;
+        const uint32_t vbase = kbase + kTileBytes;
+
+        // Rows of this half-warp, kSub at a time (fewer live scores for large G).
+#pragma unroll
+        for (int r0 = 0; r0 < kRowsPerHalf; r0 += kSub) {
+            // Scores (log2 units).
+            float sc[kSub][G];
+#pragma unroll
+            for (int r = 0; r < kSub; ++r) {
+                const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
+                const uint4 kw = lds128(kbase + row * kRowBytes);
+                const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
+                const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float2 a = mul2(qf[g][0], k0);
+                    a = fma2(qf[g][1], k1, a);
+                    a = fma2(qf[g][2], k2, a);
+                    a = fma2(qf[g][3], k3, a);
+                    sc[r][g] = a.x + a.y;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kSub; ++r)
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float x = sc[r][g];
+                    x += __shfl_xor_sync(0xffffffffu, x, 8);
+                    x += __shfl_xor_sync(0xffffffffu, x, 4);
+                    x += __shfl_xor_sync(0xffffffffu, x, 2);
+                    x += __shfl_xor_sync(0xffffffffu, x, 1);
+                    sc[r][g] = x;
+                }
+
+            // Online softmax update (rows past nvalid carry no weight).
+            float pr[kSub][G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float tile_max = kNegInf;
+#pragma unroll
+                for (int r = 0; r < kSub; ++r) {
+                    const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
+                    if (row < nvalid)
+                        tile_max = fmaxf(tile_max, sc[r][g]);
+                }
+                const float m_new = fmaxf(m[g], tile_max);
+                const float alpha = (m[g] == kNegInf) ? 0.f : exp2_approx(m[g] - m_new);
+                float psum = 0.f;
+#pragma unroll
+                for (int r = 0; r < kSub; ++r) {
+                    const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
+                    pr[r][g] = (row < nvalid) ? exp2_approx(sc[r][g] - m_new) : 0.f;
+                    psum += pr[r][g];
+                }
+                l[g] = l[g] * alpha + psum;
+                const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    acc[g][c] = mul2(acc[g][c], a2);
+                m[g] = m_new;
+            }
+
+            // acc += p * V
+#pragma unroll
+            for (int r = 0; r < kSub; ++r) {
+                const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
+                if (row < nvalid) {
+                    const uint4 vw = lds128(vbase + row * kRowBytes);
+                    const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
+                    const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float2 p2 = make_float2(pr[r][g], pr[r][g]);
+                        acc[g][0] = fma2(p2, v0, acc[g][0]);
+                        acc[g][1] = fma2(p2, v1, acc[g][1]);
+                        acc[g][2] = fma2(p2, v2, acc[g][2]);
+                        acc[g][3] = fma2(p2, v3, acc[g][3]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty0 + 8 * s);
+
+        if (flags & kLastInCta) {
+            // 1. merge the two half-warp states of this warp
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m[g], 16);
+                const float lo = __shfl_xor_sync(0xffffffffu, l[g], 16);
+                const float mn = fmaxf(m[g], mo);
+                const float a_self = (m[g] == kNegInf) ? 0.f : exp2_approx(m[g] - mn);
+                const float a_other = (mo == kNegInf) ? 0.f : exp2_approx(mo - mn);
+                l[g] = l[g] * a_self + lo * a_other;
+                const float2 s2 = make_float2(a_self, a_self), o2 = make_float2(a_other, a_other);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float2 other;
+                    other.x = __shfl_xor_sync(0xffffffffu, acc[g][c].x, 16);
+                    other.y = __shfl_xor_sync(0xffffffffu, acc[g][c].y, 16);
+                    acc[g][c] = fma2(acc[g][c], s2, mul2(other, o2));
+                }
+                m[g] = mn;
+            }
+            // 2. publish the warp state
+            if (half == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float4 *dst = reinterpret_cast<float4 *>(red_acc + (cw * G + g) * kHeadDim + li * 8);
+                    dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+                    dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+                }
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    red_m[cw * G + g] = m[g];
+                    red_l[cw * G + g] = l[g];
+                }
+            }
+            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
+                give_up();
+                return;
+            }
+            // 3. combine the warps and write the segment's result
+            const bool own = (flags & kOwnSegment) != 0;
+            const int slot = u + (int)blockIdx.x;
+            for (int idx = ctid; idx < G * kHeadDim; idx += kConsumerThreads) {
+                const int g = idx / kHeadDim, d = idx % kHeadDim;
+                float M = kNegInf;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    M = fmaxf(M, red_m[w * G + g]);
+                float lsum = 0.f, o = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float mw = red_m[w * G + g];
+                    const float wt = (mw == kNegInf) ? 0.f : exp2_approx(mw - M);
+                    lsum += wt * red_l[w * G + g];
+                    o += wt * red_acc[(w * G + g) * kHeadDim + d];
+                }
+                const float out = lsum > 0.f ? o / lsum : 0.f;
+                const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : kNegInf;
+                if (own) {
+                    const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
+                    p.o[row * kHeadDim + d] = out;
+                    if (d == 0 && p.lse)
+                        p.lse[row] = lse_v;
+                } else {
+                    p.ws_o[((size_t)slot * G + g) * kHeadDim + d] = out;
+                    if (d == 0)
+                        p.ws_lse[(size_t)slot * G + g] = lse_v;
+                }
+            }
+            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
+                give_up();
+                return;
+            }
+            // 4. fresh state for the next segment
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                m[g] = kNegInf;
+                l[g] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    acc[g][c] = make_float2(0.f, 0.f);
+            }
+        }
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernels
+
+template <int G, bool PAGED>
+__global__ void __launch_bounds__(kSplitThreads, 1)
+    split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
+                 const __grid_constant__ CUtensorMap tmv)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int *prefix = reinterpret_cast<int *>(smem + p.off_prefix);
+    int *meta = reinterpret_cast<int *>(smem + p.off_meta);
+    int *misc = reinterpret_cast<int *>(smem + p.off_misc);   // [0] abort flag, [1..] scan scratch
+    const uint32_t full0 = smem_addr(smem + p.off_bar);
+    const uint32_t empty0 = full0 + 8 * p.num_stages;
+    const uint32_t cbar = empty0 + 8 * p.num_stages;   // consumer-warp barrier
+    const uint32_t stage0 = smem_addr(smem);
+
+    // The merge kernel may launch now; it waits for this grid on its own.
+    pdl_launch_dependents();
+
+    if (tid == 0) {
+        for (int s = 0; s < p.num_stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kConsumerWarps);
+        }
+        mbar_init(cbar, kConsumerWarps);
+        misc[0] = 0;
+        mbar_init_fence();
+    }
+    build_prefix(p, prefix, misc + 1);   // ends with __syncthreads
+
+    const int T = prefix[p.batch];
+    int t_begin, t_end;
+    cta_tile_range(T, (int)gridDim.x, (int)blockIdx.x, &t_begin, &t_end);
+    if (t_begin >= t_end)
+        return;
+    volatile int *abort_flag = misc;
+    if (warp == kConsumerWarps)
+        split_producer<PAGED>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag, t_begin,
+                              t_end, lane);
+    else
+        split_consumer<G>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin, t_end, warp,
+                          lane);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__ MergeParams p)
+{
+    pdl_wait_prior_grid();
+    const int u = blockIdx.x;
+    const int b = u / p.hkv, h = u - b * p.hkv;
+    const int d = threadIdx.x;
+    const int pb = p.ws_prefix[b], pe = p.ws_prefix[b + 1], T = p.ws_prefix[p.batch];
+    const size_t row0 = (size_t)b * p.hq + (size_t)h * G;
+    if (pe == pb) {   // empty request: O = 0, LSE = -inf
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            p.o[(row0 + g) * kHeadDim + d] = 0.f;
+            if (d == 0 && p.lse)
+                p.lse[row0 + g] = kNegInf;
+        }
+        return;
+    }
+    const int nb = (pe - pb) / p.hkv;
+    const int first = pb + h * nb, last = first + nb - 1;
+    const int c0 = cta_of_tile(T, p.num_ctas, first), c1 = cta_of_tile(T, p.num_ctas, last);
+    if (c0 == c1)
+        return;   // one CTA saw the whole segment and wrote it
+#pragma unroll 1
+    for (int g = 0; g < G; ++g) {
+        float M = kNegInf;
+        for (int c = c0; c <= c1; ++c)
+            M = fmaxf(M, p.ws_lse[(size_t)(u + c) * G + g]);
+        float S = 0.f;
+        for (int c = c0; c <= c1; ++c)
+            S += expf(p.ws_lse[(size_t)(u + c) * G + g] - M);
+        const float lse = M + logf(S);
+        float acc = 0.f;
+        for (int c = c0; c <= c1; ++c) {
+            const size_t slot = (size_t)(u + c) * G + g;
+            acc += p.ws_o[slot * kHeadDim + d] * expf(p.ws_lse[slot] - lse);
+        }
+        p.o[(row0 + g) * kHeadDim + d] = acc;
+        if (d == 0 && p.lse)
+            p.lse[row0 + g] = lse;
+    }
+}
+
+}  // namespace fd

@@ -1,0 +1,177 @@
+/*
+ * fd.h -- split-KV ("Flash-Decoding") single-query decode attention for
+ * NVIDIA GB300 (sm_103a).  C ABI: plain pointers and sizes, no C++ or torch
+ * types.  Link against libfd.so.
+ *
+ * What one call computes, for every request b < batch and query head
+ * h < num_q_heads, over the first L_b = seq_lens[b] tokens of the KV cache:
+ *
+ *     s_t   = scale * sum_d q[b,h,d] * K_b[t, g, d]          g = h / (Hq/Hkv)
+ *     O     = sum_t softmax(s)_t * V_b[t, g, :]              (fp32)
+ *     LSE   = ln sum_t exp(s_t)                              (fp32, natural log)
+ *
+ * Sources (the pages this library follows):
+ *   - "纯手搓 flash decoding sm120" (wingedge777.com), section 1 (flash
+ *     decoding: split the KV sequence into chunks, one CTA per chunk writes a
+ *     partial output and its log-sum-exp) and section 2 (the pass-2 merge by
+ *     log-sum-exp; lse = m ln2 + ln d in the log2 domain).
+ *   - "FlashAttention 与推理算子" (anrans.github.io ai-infra-handbooks):
+ *     the online-softmax update of the FlashAttention section, the
+ *     PagedAttention section (token t of a request lives in physical block
+ *     block_table[t / page_size], slot t % page_size), the Flash-Decoding
+ *     section (merge of normalised split outputs), and exercise 3 (one CTA
+ *     serves every query head of a GQA group, so K/V are read once).
+ *
+ * Conventions shared by every entry point:
+ *   - Ownership: the caller owns every buffer.  The library allocates no
+ *     memory, keeps no per-call state, and never synchronises the stream
+ *     (except fd_get_device_error, which says so).
+ *   - Streams: all device work is ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  Calls with distinct workspaces may run
+ *     concurrently on different streams; calls sharing a workspace must be
+ *     ordered.
+ *   - Errors: arguments are checked on the host before any launch; a bad
+ *     argument returns a status and launches nothing.  Values that live only
+ *     on the device (lengths, block-table entries) are checked by the kernels,
+ *     which clamp them into range, never read out of bounds, and record the
+ *     problem in the workspace header; fd_get_device_error reports it.
+ *   - Alignment: q, k, v, k_pages, v_pages and o must be 16-byte aligned, and
+ *     the workspace 256-byte aligned; otherwise FD_ERR_INVALID_ARG.
+ *   - Supported shapes: head_dim 128; Hq/Hkv in {1, 2, 4, 8}; batch <= 4096.
+ *     Other shapes return FD_ERR_UNSUPPORTED.
+ *   - Precision: q, K and V are bf16; scores, softmax and accumulation are
+ *     fp32; outputs are fp32.
+ */
+#ifndef FD_H
+#define FD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st *fd_stream_t;
+
+typedef enum fd_status {
+    FD_OK = 0,
+    FD_ERR_INVALID_ARG = 1,         /* null pointer, bad size, misalignment, length > capacity */
+    FD_ERR_UNSUPPORTED = 2,         /* valid but not implemented: head_dim, group size, page size, batch */
+    FD_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < fd_workspace_size(...) */
+    FD_ERR_CUDA = 4,                /* a CUDA runtime or driver call failed (launch, tensor map) */
+    FD_ERR_TIMEOUT = 5,             /* a kernel's bounded wait ran out (reported by fd_get_device_error) */
+    FD_ERR_DEVICE_INPUT = 6         /* a device-side length or block-table entry was out of range */
+} fd_status;
+
+/* Optional knobs; pass NULL for the defaults. */
+typedef struct fd_options {
+    /* Number of persistent split CTAs that share the KV tiles (1..1024).
+     * 0 = one per SM of the current device.  Results do not depend on it
+     * beyond fp32 summation order. */
+    int num_ctas;
+    /* FD_FLAG_* bits; 0 for normal use. */
+    unsigned int flags;
+    /* Limit for every wait inside the kernels, in nanoseconds; 0 = 2 s.
+     * When a wait runs out the kernel stops, records FD_ERR_TIMEOUT in the
+     * workspace header and returns instead of hanging. */
+    unsigned long long wait_timeout_ns;
+    /* Optional cudaEvent_t handles recorded on `stream` immediately before
+     * and after the split kernel (for timing the kernel alone); NULL = none. */
+    void *split_start_event;
+    void *split_end_event;
+} fd_options;
+
+/* Test hook: CTA 0 announces more bytes for its first tile than it loads, so
+ * its consumers' wait can never complete and must run out.  Never set it in
+ * production; the outputs of such a call are undefined. */
+#define FD_FLAG_TEST_STARVE_FIRST_TILE 0x1u
+
+/*
+ * Bytes of workspace that fd_decode / fd_decode_paged need for this shape.
+ * Pure host function (no CUDA call).  The size does not depend on the
+ * lengths: it holds a 256-byte header, the per-request tile prefix and one
+ * fp32 partial (Hq/Hkv rows of head_dim outputs plus their log-sum-exp) per
+ * (request, kv head) plus one per possible split CTA.  max_kv_len and
+ * page_size are validated but do not change the size.
+ * Returns 0 for invalid arguments.
+ */
+size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                         int max_kv_len, int page_size);
+
+/*
+ * Clear the workspace header (the sticky device-error word).  Call once after
+ * allocating a workspace, before its first use.  Stream-ordered, asynchronous.
+ */
+fd_status fd_workspace_init(void *workspace, size_t workspace_bytes, fd_stream_t stream);
+
+/*
+ * Decode attention over a contiguous KV cache.
+ *   q            [batch, num_q_heads, head_dim] bf16, device.
+ *   k, v         [batch, s_max, num_kv_heads, head_dim] bf16, device, row-major.
+ *                Positions t >= seq_lens[b] of request b are never used
+ *                (they may hold anything, including NaN).
+ *   seq_lens_dev [batch] int32, device: L_b in [0, s_max].  NULL means every
+ *                request has length s_max.  A device value above s_max is
+ *                clamped to s_max and reported as FD_ERR_DEVICE_INPUT.
+ *   seq_lens_host [batch] int32, host copy of the lengths, or NULL.  Only used
+ *                to validate lengths on the host (FD_ERR_INVALID_ARG if any is
+ *                outside [0, s_max]); the kernels read seq_lens_dev.
+ *   scale        multiplies q.k (callers usually pass 1/sqrt(head_dim)).
+ *   o            [batch, num_q_heads, head_dim] fp32, device, written.
+ *   lse          [batch, num_q_heads] fp32, device, written, natural log; may
+ *                be NULL.  A request with L_b = 0 gets O = 0 and LSE = -inf.
+ *   workspace    device scratch of at least fd_workspace_size(batch,
+ *                num_q_heads, num_kv_heads, head_dim, s_max, 0) bytes,
+ *                initialised once with fd_workspace_init.
+ *   opts         NULL or options (see fd_options).
+ */
+fd_status fd_decode(const void *q, const void *k, const void *v,
+                    const int32_t *seq_lens_dev, const int32_t *seq_lens_host,
+                    int batch, int num_q_heads, int num_kv_heads, int head_dim, int s_max,
+                    float scale, float *o, float *lse,
+                    void *workspace, size_t workspace_bytes,
+                    const fd_options *opts, fd_stream_t stream);
+
+/*
+ * Decode attention over a paged KV cache.
+ *   k_pages, v_pages [num_pages, page_size, num_kv_heads, head_dim] bf16, device.
+ *   block_table  [batch, max_blocks_per_seq] int32, device, row-major: token t
+ *                of request b is in page block_table[b][t / page_size], slot
+ *                t % page_size.  Only the first ceil(L_b / page_size) entries of
+ *                a row are read; the rest may hold anything (e.g. -1).  An entry
+ *                outside [0, num_pages) is replaced by page 0 and reported as
+ *                FD_ERR_DEVICE_INPUT.
+ *   page_size    a divisor of 64 (1, 2, 4, ..., 32) or a multiple of 64.
+ *   seq_lens_dev [batch] int32, device, L_b in [0, max_blocks_per_seq * page_size];
+ *                must not be NULL.
+ *   Other arguments as for fd_decode.
+ */
+fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                          const int32_t *block_table, int max_blocks_per_seq,
+                          const int32_t *seq_lens_dev, const int32_t *seq_lens_host,
+                          int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                          int page_size, int num_pages, float scale,
+                          float *o, float *lse,
+                          void *workspace, size_t workspace_bytes,
+                          const fd_options *opts, fd_stream_t stream);
+
+/*
+ * Read and clear the sticky device-error word of a workspace: FD_OK,
+ * FD_ERR_TIMEOUT or FD_ERR_DEVICE_INPUT (timeout wins if both happened).
+ * SYNCHRONISES `stream` (it copies one word to the host).
+ */
+fd_status fd_get_device_error(void *workspace, fd_stream_t stream);
+
+/* Human-readable name of a status; never NULL. */
+const char *fd_status_string(fd_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int fd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_H */

@@ -1,0 +1,204 @@
+"""The C ABI on the host: exported symbols, argument checks, schedule invariants.
+
+None of these calls reaches the GPU: every case fails validation before the
+first CUDA call, or exercises pure host functions.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_attention_decoding_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+@pytest.fixture(scope="module")
+def fd():
+    import decode_attention_decoding_gb300 as fd
+    return fd
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fd_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert {"fd_workspace_size", "fd_decode", "fd_decode_paged"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", os.path.join(ROOT, "decode_attention_decoding_gb300", "libfd.so")],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r" T (fd_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        getattr(lib, n)
+
+
+def test_status_strings_and_version(fd):
+    for st in range(7):
+        assert fd.fd_status_string(st).startswith("FD_")
+    assert fd.fd_status_string(99) == "FD_ERR_UNKNOWN"
+    assert fd.fd_version() >= 10000
+
+
+def test_workspace_size_is_host_only_and_rejects_bad_shapes(fd):
+    assert fd.fd_workspace_size(1, 32, 32, 128, 4096, 0) > 0
+    assert fd.fd_workspace_size(1, 32, 5, 128, 4096, 0) == 0
+    assert fd.fd_workspace_size(-1, 32, 8, 128, 4096, 0) == 0
+    # independent of the lengths, growing with batch
+    assert fd.fd_workspace_size(4, 32, 8, 128, 10, 0) == fd.fd_workspace_size(4, 32, 8, 128, 10 ** 6, 16)
+    assert fd.fd_workspace_size(8, 32, 8, 128, 10, 0) > fd.fd_workspace_size(4, 32, 8, 128, 10, 0)
+    # room for one fp32 partial (G rows of D outputs + G LSEs) per slot
+    for B, hq, hkv in ((1, 32, 32), (64, 32, 8), (1, 64, 8)):
+        slots = B * hkv + 1024
+        assert fd.fd_workspace_size(B, hq, hkv, 128, 1, 0) >= slots * (hq // hkv) * 129 * 4
+
+
+ALIGNED = 1 << 20          # fake, 256-byte aligned device addresses (never dereferenced)
+
+
+def call_decode(lib, **over):
+    a = dict(q=ALIGNED, k=ALIGNED, v=ALIGNED, sl=None, slh=None, B=2, hq=8, hkv=2, d=128, smax=64,
+             scale=0.1, o=ALIGNED, lse=ALIGNED, ws=ALIGNED, wsb=1 << 30, opts=None, stream=None)
+    a.update(over)
+    f = lib.fd_decode
+    f.restype = ctypes.c_int
+    return f(ctypes.c_void_p(a["q"]), ctypes.c_void_p(a["k"]), ctypes.c_void_p(a["v"]), a["sl"], a["slh"],
+             a["B"], a["hq"], a["hkv"], a["d"], a["smax"], ctypes.c_float(a["scale"]),
+             ctypes.c_void_p(a["o"]), ctypes.c_void_p(a["lse"]), ctypes.c_void_p(a["ws"]),
+             ctypes.c_size_t(a["wsb"]), a["opts"], a["stream"])
+
+
+def test_decode_argument_checks(lib, fd):
+    E = fd
+    assert call_decode(lib, q=0) == E.FD_ERR_INVALID_ARG
+    assert call_decode(lib, o=0) == E.FD_ERR_INVALID_ARG
+    assert call_decode(lib, ws=0) == E.FD_ERR_INVALID_ARG
+    assert call_decode(lib, hq=6, hkv=4) == E.FD_ERR_INVALID_ARG
+    assert call_decode(lib, q=ALIGNED + 8) == E.FD_ERR_INVALID_ARG
+    assert call_decode(lib, k=ALIGNED + 2) == E.FD_ERR_INVALID_ARG
+    assert call_decode(lib, ws=ALIGNED + 16) == E.FD_ERR_INVALID_ARG
+    assert call_decode(lib, smax=-1) == E.FD_ERR_INVALID_ARG
+    assert call_decode(lib, d=64) == E.FD_ERR_UNSUPPORTED
+    assert call_decode(lib, hq=6, hkv=2) == E.FD_ERR_UNSUPPORTED       # group 3
+    assert call_decode(lib, hq=32, hkv=2) == E.FD_ERR_UNSUPPORTED      # group 16
+    assert call_decode(lib, B=5000) == E.FD_ERR_UNSUPPORTED
+    assert call_decode(lib, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
+    lens = (ctypes.c_int32 * 2)(10, 65)
+    assert call_decode(lib, slh=lens) == E.FD_ERR_INVALID_ARG
+    lens = (ctypes.c_int32 * 2)(10, -1)
+    assert call_decode(lib, slh=lens) == E.FD_ERR_INVALID_ARG
+    opts = fd.FdOptions(2000, 0, 0, None, None)
+    assert call_decode(lib, opts=ctypes.byref(opts)) == E.FD_ERR_INVALID_ARG
+    assert call_decode(lib, B=0) == E.FD_OK                           # nothing to do, no CUDA call
+
+
+def call_paged(lib, **over):
+    a = dict(q=ALIGNED, k=ALIGNED, v=ALIGNED, table=ALIGNED, mb=4, sl=ALIGNED, slh=None, B=2, hq=8,
+             hkv=2, d=128, page=16, npages=8, scale=0.1, o=ALIGNED, lse=ALIGNED, ws=ALIGNED,
+             wsb=1 << 30)
+    a.update(over)
+    f = lib.fd_decode_paged
+    f.restype = ctypes.c_int
+    return f(ctypes.c_void_p(a["q"]), ctypes.c_void_p(a["k"]), ctypes.c_void_p(a["v"]),
+             ctypes.c_void_p(a["table"]), a["mb"], ctypes.c_void_p(a["sl"]), a["slh"], a["B"], a["hq"],
+             a["hkv"], a["d"], a["page"], a["npages"], ctypes.c_float(a["scale"]), ctypes.c_void_p(a["o"]),
+             ctypes.c_void_p(a["lse"]), ctypes.c_void_p(a["ws"]), ctypes.c_size_t(a["wsb"]), None, None)
+
+
+def test_paged_argument_checks(lib, fd):
+    E = fd
+    assert call_paged(lib, table=0) == E.FD_ERR_INVALID_ARG
+    assert call_paged(lib, sl=0) == E.FD_ERR_INVALID_ARG
+    assert call_paged(lib, mb=0) == E.FD_ERR_INVALID_ARG
+    assert call_paged(lib, npages=0) == E.FD_ERR_INVALID_ARG
+    assert call_paged(lib, page=0) == E.FD_ERR_INVALID_ARG
+    assert call_paged(lib, page=24) == E.FD_ERR_UNSUPPORTED
+    assert call_paged(lib, page=96) == E.FD_ERR_UNSUPPORTED
+    lens = (ctypes.c_int32 * 2)(64, 65)                     # capacity 4 pages * 16
+    assert call_paged(lib, slh=lens) == E.FD_ERR_INVALID_ARG
+    assert call_paged(lib, wsb=100) == E.FD_ERR_WORKSPACE_TOO_SMALL
+    for ok_page in (1, 2, 8, 16, 32, 64, 128, 256):
+        assert call_paged(lib, page=ok_page, B=0) == E.FD_OK
+
+
+# ---------------------------------------------------------------------------
+# The split schedule (fd_sched.h), through a small g++-compiled shim
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def sched(tmp_path_factory):
+    d = tmp_path_factory.mktemp("shim")
+    so = str(d / "libshim.so")
+    subprocess.check_call(["g++", "-O1", "-std=c++17", "-shared", "-fPIC",
+                           "-I" + os.path.join(ROOT, "decode_attention_decoding_gb300", "csrc"),
+                           os.path.join(ROOT, "tests", "sched_shim.cpp"), "-o", so])
+    s = ctypes.CDLL(so)
+    s.shim_cta_of_tile.restype = ctypes.c_int
+    s.shim_request_of_tile.restype = ctypes.c_int
+    s.shim_slots.restype = ctypes.c_int
+    return s
+
+
+def ranges(sched, T, P):
+    out = []
+    b, e = ctypes.c_int(), ctypes.c_int()
+    for c in range(P):
+        sched.shim_cta_tile_range(T, P, c, ctypes.byref(b), ctypes.byref(e))
+        out.append((b.value, e.value))
+    return out
+
+
+@pytest.mark.parametrize("T,P", [(0, 5), (3, 8), (8, 8), (100, 7), (2048, 152), (32768, 152), (65537, 1024)])
+def test_cta_ranges_partition_tiles_evenly(sched, T, P):
+    r = ranges(sched, T, P)
+    assert r[0][0] == 0 and r[-1][1] == T
+    for (b0, e0), (b1, _) in zip(r, r[1:]):
+        assert e0 == b1
+    sizes = [e - b for b, e in r]
+    assert max(sizes) - min(sizes) <= 1
+    for t in sorted(set([0, T - 1, T // 2, *range(0, T, max(1, T // 97))])):
+        if 0 <= t < T:
+            c = sched.shim_cta_of_tile(T, P, t)
+            assert r[c][0] <= t < r[c][1]
+
+
+def test_partial_slots_are_unique_and_bounded(sched):
+    rng = np.random.default_rng(3)
+    tt = sched.shim_tile_tokens()
+    for trial in range(30):
+        B = int(rng.integers(1, 40))
+        hkv = int(rng.choice([1, 2, 8]))
+        lens = rng.integers(0, 3000, B)
+        lens[rng.random(B) < 0.2] = 0
+        ntiles = (lens + tt - 1) // tt
+        prefix = np.concatenate([[0], np.cumsum(ntiles * hkv)]).astype(np.int32)
+        T = int(prefix[-1])
+        P = int(rng.integers(1, 300))
+        r = ranges(sched, T, P)
+        seen = set()
+        pre = (ctypes.c_int * len(prefix))(*prefix.tolist())
+        for c, (b0, e0) in enumerate(r):
+            segs = set()
+            for t in range(b0, e0):
+                b = sched.shim_request_of_tile(pre, B, t)
+                assert prefix[b] <= t < prefix[b + 1]
+                h = (t - prefix[b]) // ntiles[b]
+                segs.add(b * hkv + h)
+            for u in segs:
+                slot = u + c
+                assert slot not in seen
+                seen.add(slot)
+                assert slot < sched.shim_slots(B, hkv)

@@ -1,0 +1,181 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Tolerances (the task's): O within 1e-2 + 1e-2 |ref| elementwise, LSE within
+1e-3 absolute.  Page gather and index selection are checked bit-exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fd_synth as syn
+import oracle
+from gpu_util import check, contig_to_paged, run, sample_items, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from decode_attention_decoding_gb300 import build
+    build.build()
+    oracle.build()
+
+
+RAGGED = [1000, 1, 0, 63, 64, 65, 129, 700]
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("num_ctas", [0, 1, 3, 7, 40])
+def test_contiguous_vs_oracle(group, num_ctas):
+    hkv = 4 if group <= 2 else 2
+    w = syn.make_contiguous(200 + group, len(RAGGED), hkv * group, hkv, 128, 1024, RAGGED)
+    o, l = run(w, num_ctas=num_ctas)
+    ro, rl = oracle.attend(w, threads=8)
+    check(o, l, ro, rl, f"G={group} ctas={num_ctas}")
+
+
+@pytest.mark.parametrize("page", [1, 8, 16, 32, 64, 128])
+@pytest.mark.parametrize("group", [1, 4, 8])
+def test_paged_vs_oracle_and_contiguous(page, group):
+    hkv = 2
+    w = syn.make_contiguous(300 + page, len(RAGGED), hkv * group, hkv, 128, 1024, RAGGED)
+    wp = contig_to_paged(w, page, perm_seed=page + group)
+    for ctas in (0, 5):
+        op, lp = run(wp, num_ctas=ctas)
+        ro, rl = oracle.attend(wp, threads=8)
+        check(op, lp, ro, rl, f"paged P={page} G={group}")
+        # identical logical data, identical tiles: bitwise identical results
+        oc, lc = run(w, num_ctas=ctas)
+        assert np.array_equal(op, oc) and np.array_equal(lp, lc)
+
+
+def test_poison_past_length_and_unused_pages_is_never_read():
+    lens = [5, 64, 65, 200, 0, 1023]
+    w = syn.make_contiguous(400, len(lens), 8, 2, 128, 1024, lens)
+    clean_o, clean_l = run(w, num_ctas=9)
+    wn = syn.Workload(w.name, w.q, w.k.copy(), w.v.copy(), w.seq_lens, 8, 2, 128, w.scale)
+    for b, L in enumerate(lens):
+        wn.k[b, L:] = syn.BF16_NAN
+        wn.v[b, L:] = syn.BF16_NAN
+    o, l = run(wn, num_ctas=9)
+    assert np.all(np.isfinite(o)) and np.array_equal(o, clean_o) and np.array_equal(l, clean_l)
+    for page in (16, 64):
+        wp = contig_to_paged(w, page, perm_seed=1, extra_pages=4, poison=True)
+        op, lp = run(wp, num_ctas=9)
+        assert np.all(np.isfinite(op)) and np.array_equal(op, clean_o) and np.array_equal(lp, clean_l)
+
+
+def test_empty_requests_and_all_empty_batch():
+    w = syn.make_contiguous(410, 3, 8, 8, 128, 256, [0, 256, 0])
+    o, l = run(w)
+    assert np.all(o[0] == 0) and np.all(o[2] == 0)
+    assert np.all(np.isneginf(l[0])) and np.all(np.isneginf(l[2]))
+    ro, rl = oracle.attend(w)
+    check(o, l, ro, rl, "mixed empty")
+    w0 = syn.make_contiguous(411, 2, 4, 4, 128, 64, [0, 0])
+    o, l = run(w0)
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+
+
+def test_lse_output_is_optional():
+    w = syn.make_contiguous(412, 2, 8, 2, 128, 300, [300, 17])
+    o, l = run(w, lse=False)
+    assert l is None
+    ro, rl = oracle.attend(w)
+    check(o, None, ro, rl, "no lse")
+
+
+@pytest.mark.parametrize("factor", [8.0, 32.0])
+def test_softmax_stress_scaled_keys(factor):
+    L = 4000
+    w = syn.make_contiguous(420 + int(factor), 1, 16, 2, 128, L, [L])
+    toks = syn.choose(5, L, L // 100)
+    syn.scale_keys(w, toks, factor)
+    o, l = run(w, num_ctas=13)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+    ro, rl = oracle.attend(w, threads=8)
+    check(o, l, ro, rl, f"keys x{factor}")
+
+
+def test_repeatable_bitwise():
+    w = syn.make_contiguous(430, 4, 32, 8, 128, 2000, [2000, 1500, 3, 999])
+    d = to_device(w)
+    a = run(w, d)
+    b = run(w, d)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------------------
+# Bit-exact gather probe: one dominating token selects its V row exactly
+# ---------------------------------------------------------------------------
+
+def gather_probe(L, group, hkv, t_star, seed):
+    """q heads equal within a group; K[t*] = 16 q so its score dominates by > 150
+    natural units in every split; V rows carry (t >> 8, t & 255, g, 1)."""
+    d = 128
+    w = syn.make_contiguous(seed, 1, hkv * group, hkv, d, L, [L])
+    qg = syn.bf16_bits_to_f64(w.q[0, ::group])              # one q per kv head
+    w.q[0] = np.repeat(w.q[0, ::group], group, axis=0)
+    for g in range(hkv):
+        w.k[0, t_star, g] = syn.f64_to_bf16_bits(16.0 * qg[g])
+    t = np.arange(L)
+    for g in range(hkv):
+        w.v[0, :, g, 0] = syn.f64_to_bf16_bits((t >> 8).astype(np.float64))
+        w.v[0, :, g, 1] = syn.f64_to_bf16_bits((t & 255).astype(np.float64))
+        w.v[0, :, g, 2] = syn.f64_to_bf16_bits(np.full(L, float(g)))
+        w.v[0, :, g, 3] = syn.f64_to_bf16_bits(np.ones(L))
+    # margin check on the host (exact scores in fp64)
+    K = syn.bf16_bits_to_f64(w.k[0])
+    s = w.scale * np.einsum("tgd,gd->tg", K, qg)
+    others = np.delete(s, t_star, axis=0).max(axis=0)
+    assert np.all(s[t_star] - others > 110), "probe margin too small"
+    return w
+
+
+@pytest.mark.parametrize("layout", ["contig", 16, 64])
+def test_bit_exact_gather(layout):
+    L, group, hkv = 3000, 4, 2
+    stars = [0, 1, 15, 16, 63, 64, 65, 1023, 1024, 2047, 2048, L - 1]
+    for ctas in (0, 7):
+        for t_star in stars:
+            w = gather_probe(L, group, hkv, t_star, seed=500)
+            if layout != "contig":
+                w = contig_to_paged(w, layout, perm_seed=t_star + 1)
+            o, l = run(w, num_ctas=ctas)
+            for h in range(hkv * group):
+                g = h // group
+                expect = syn.bf16_bits_to_f64(
+                    w.v[0, t_star, g] if layout == "contig"
+                    else w.v[w.block_table[0, t_star // layout], t_star % layout, g])
+                assert np.array_equal(o[0, h], expect), (layout, ctas, t_star, h)
+                assert o[0, h, 0] * 256 + o[0, h, 1] == t_star and o[0, h, 2] == g
+
+
+# ---------------------------------------------------------------------------
+# Device-side input errors are reported, clamped, and never fault
+# ---------------------------------------------------------------------------
+
+def test_device_length_above_capacity_is_reported():
+    import decode_attention_decoding_gb300 as fd
+    w = syn.make_contiguous(440, 2, 4, 4, 128, 128, [128, 50])
+    d = to_device(w)
+    d["seq_lens"][0] = 500                                    # > s_max on the device only
+    ws = fd.make_workspace(2, 4, 4, 128, 128)
+    o, l = fd.fd_decode(d["q"], d["k"], d["v"], d["seq_lens"], scale=w.scale, workspace=ws)
+    assert fd.fd_get_device_error(ws) == fd.FD_ERR_DEVICE_INPUT
+    ro, rl = oracle.attend(w)                                 # clamped to s_max = 128
+    check(o.cpu().numpy().astype(np.float64), l.cpu().numpy().astype(np.float64), ro, rl, "clamped")
+    assert fd.fd_get_device_error(ws) == fd.FD_OK             # the word was cleared
+
+
+def test_bad_block_table_entry_is_reported():
+    import decode_attention_decoding_gb300 as fd
+    w = contig_to_paged(syn.make_contiguous(441, 1, 4, 2, 128, 200, [200]), 16, perm_seed=2)
+    d = to_device(w)
+    d["block_table"][0, 3] = w.num_pages + 1000
+    ws = fd.make_workspace(1, 4, 2, 128, 200, 16)
+    o, l = fd.fd_decode_paged(d["q"], d["k"], d["v"], d["block_table"], d["seq_lens"], scale=w.scale,
+                              workspace=ws)
+    torch.cuda.synchronize()
+    assert np.all(np.isfinite(o.cpu().numpy()))
+    assert fd.fd_get_device_error(ws) == fd.FD_ERR_DEVICE_INPUT
