@@ -87,6 +87,21 @@ def byte_counts(w, P):
                 split=kv + q + ws + out)   # split reads K,V,q; writes partials or final O/LSE
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tbs(bytes_per_call: int, world: int, ms_per_call_max: float) -> float:
+    """Weak scaling: every rank processes one call per step; the slowest rank sets the time."""
+    return world * bytes_per_call / (ms_per_call_max * 1e-3) / 1e12
+
+
 def kernel_hash():
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -224,6 +239,9 @@ def run_ours(args, rank, world):
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:            # torch creates the CUDA event on first record
+        a.record(stream)
+        b.record(stream)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         if dist:
@@ -240,13 +258,10 @@ def run_ours(args, rank, world):
             dist.barrier()
     ms_total = e0.elapsed_time(e1)
     split_ms = [a.elapsed_time(b) for a, b in ev]
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / K
     bc = byte_counts(w, P)
-    value_tbs = world * bc["call"] / (ms_step * 1e-3) / 1e12
+    value_tbs = whole_job_tbs(bc["call"], world, ms_step)
     split_avg_ms = float(np.mean(split_ms))
     peaks, peak_src = measured_peaks()
     achieved_gbs = bc["split"] / (split_avg_ms * 1e-3) / 1e9
@@ -295,14 +310,10 @@ def run_ours(args, rank, world):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / K2
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / K2, dist, dev)
         h2d = hq_.nbytes + hk_.nbytes + hv_.nbytes + hl_.nbytes
         d2h = ho.numel() * 4 + hlse.numel() * 4
-        e2e = {"value": world * bc["call"] / (e2e_ms * 1e-3) / 1e12, "unit": "TB/s",
+        e2e = {"value": whole_job_tbs(bc["call"], world, e2e_ms), "unit": "TB/s",
                "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": K2}
 

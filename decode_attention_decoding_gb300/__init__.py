@@ -145,6 +145,9 @@ def _i32(t, name):
 def _options(num_ctas, flags, wait_timeout_ns, split_events):
     ev0 = ev1 = None
     if split_events is not None:
+        for e in split_events:
+            if not e.cuda_event:
+                raise ValueError("split_events must be created (recorded once) before use")
         ev0 = ctypes.c_void_p(split_events[0].cuda_event)
         ev1 = ctypes.c_void_p(split_events[1].cuda_event)
     return FdOptions(int(num_ctas), int(flags), int(wait_timeout_ns), ev0, ev1)

@@ -1,0 +1,81 @@
+"""The benchmark's multi-rank path on CPU (gloo, world size 2): the timed value
+is the slowest rank's, every rank agrees on it, and the whole-job throughput
+counts every rank's replica; the reference arm prints on rank 0 only."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = [1.5, 4.0][rank]
+    got = bench.max_over_ranks(ms, dist, "cpu")
+    tbs = bench.whole_job_tbs(10 ** 9, world, got)
+    dist.barrier()
+    q.put((rank, got, tbs))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_weak_scaling_value():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [4.0, 4.0]
+    for _, _, tbs in res:
+        assert tbs == pytest.approx(2 * 1e9 / 4e-3 / 1e12)
+
+
+def test_partial_count_matches_schedule_brute_force():
+    sys.path.insert(0, ROOT)
+    import bench
+    import numpy as np
+    rng = np.random.default_rng(5)
+    for _ in range(40):
+        B = int(rng.integers(1, 20)); hkv = int(rng.choice([1, 2, 8])); P = int(rng.integers(1, 200))
+        lens = rng.integers(0, 5000, B)
+        nt = (lens + 63) // 64
+        owner = []
+        for b in range(B):
+            for h in range(hkv):
+                owner += [(b, h)] * int(nt[b])
+        T = len(owner)
+        base, rem = divmod(T, P)
+        counts = {}
+        t = 0
+        for c in range(P):
+            n = base + (1 if c < rem else 0)
+            for seg in set(owner[t:t + n]):
+                counts.setdefault(seg, set()).add(c)
+            t += n
+        expect = sum(len(cs) for cs in counts.values() if len(cs) > 1)
+        assert bench.partial_count(lens, hkv, P) == expect
+
+
+def test_reference_arm_rank1_prints_nothing():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
