@@ -24,6 +24,7 @@ __all__ = [
     "fd_get_device_error", "fd_status_string", "fd_version", "make_workspace", "library_path",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
     "FD_ERR_CUDA", "FD_ERR_TIMEOUT", "FD_ERR_DEVICE_INPUT", "FD_FLAG_TEST_STARVE_FIRST_TILE",
+    "fd_decode_noalloc",
 ]
 
 FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
@@ -59,6 +60,8 @@ def _load():
     lib.fd_decode_paged.argtypes = [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                     _P, _SZ, ctypes.POINTER(FdOptions), _P]
     lib.fd_decode_paged.restype = _I
+    lib.fd_decode_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]
+    lib.fd_decode_noalloc.restype = _I
     lib.fd_get_device_error.argtypes = [_P, _P]
     lib.fd_get_device_error.restype = _I
     lib.fd_status_string.argtypes = [_I]
@@ -227,6 +230,27 @@ def fd_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=No
     if check and st != FD_OK:
         raise FdError(st, "fd_decode_paged")
     return out, (None if lse is False else lse)
+
+
+def fd_decode_noalloc(q, k, v, seq_lens, o, lse=None, device_status=None, scale=None, stream=None,
+                      check=True):
+    """fd_decode without a workspace (see fd_decode_noalloc in include/fd.h).
+
+    For callers that cannot allocate device memory where they run attention:
+    the scratch is a fixed array inside the library, and the caller passes
+    only inputs and preallocated outputs (o fp32 [B, Hq, D], optional lse fp32
+    [B, Hq] and device_status uint32/int32 [1]).  Returns the C status.
+    """
+    B, hq, d = q.shape
+    _, s_max, hkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = _lib.fd_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, hq, hkv, d, s_max,
+                                float(scale), _ptr(o), _ptr(lse), _ptr(device_status),
+                                _stream_ptr(stream, q.device))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_decode_noalloc")
+    return st
 
 
 def fd_get_device_error(workspace, stream=None) -> int:

@@ -1,0 +1,225 @@
+// fd_noalloc.cu -- fd_decode_noalloc: contiguous decode attention whose
+// split/merge scratch lives in a fixed device array inside this library, so
+// the call needs no workspace and performs no allocation of any kind.
+//
+// Who needs it: callers that cannot call cudaMalloc or any allocator at the
+// point where they run attention -- for example code running inside a
+// framework hook or plugin that forbids device allocation, a real-time path
+// that must not risk the latency or failure of an allocation, or a host
+// application that owns all device memory through its own pool and cannot
+// hand a pointer from it to this library.  They pass only inputs and
+// outputs.
+//
+// The scratch array (kNoallocScratchBytes) is reserved on every GPU that
+// loads this library and stays reserved until the process exits.  Every call
+// on a device uses the same array, and the array keeps whatever the previous
+// call left in it; the call clears the one word that must start at zero (the
+// device-error word) before its kernels run.  Two calls whose kernels overlap
+// on the GPU (different streams, no ordering between them) race on the array
+// and give undefined results.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fd.h"
+#include "fd_launch.h"
+#include "fd_sched.h"
+
+namespace {
+
+using namespace fd;
+
+constexpr size_t kNoallocScratchBytes = FD_NOALLOC_SCRATCH_BYTES;
+
+// The scratch: device-error word, tile prefix, partial LSEs and partial outputs.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+struct NoallocDevice {
+    unsigned char *scratch = nullptr;   // device address of g_noalloc_scratch
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+std::mutex g_mu;
+NoallocDevice g_devs[64];
+bool g_ready[64] = {};
+
+// Once per device, with that device current: resolve the array's device
+// address (in host code its name is only a host-side stand-in) and the
+// properties the launch needs.
+fd_status noalloc_setup(NoallocDevice *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return FD_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_ready[dev]) {
+        NoallocDevice d;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return FD_ERR_CUDA;
+        d.scratch = static_cast<unsigned char *>(p);
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return FD_ERR_CUDA;
+        g_devs[dev] = d;
+        g_ready[dev] = true;
+    }
+    *out = g_devs[dev];
+    return FD_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+fd_status encode_rows(CUtensorMap *map, const void *base, int hkv, long long rows)
+{
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    if (!fn)
+        return FD_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)hkv * kRowBytes};
+    const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1u, (cuuint32_t)kTileTokens};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? FD_OK
+               : FD_ERR_CUDA;
+}
+
+// Scratch layout for `slots` partials of `group` rows: the same regions as a
+// caller-provided workspace, but sized for the actual number of split CTAs.
+struct NoallocLayout {
+    size_t prefix_off, lse_off, o_off, total;
+};
+
+NoallocLayout noalloc_layout(int batch, int slots, int group)
+{
+    NoallocLayout l;
+    l.prefix_off = 256;
+    l.lse_off = align_up(l.prefix_off + sizeof(int) * (size_t)(batch + 1), 256);
+    l.o_off = align_up(l.lse_off + sizeof(float) * (size_t)slots * group, 256);
+    l.total = align_up(l.o_off + sizeof(float) * (size_t)slots * group * kHeadDim, 256);
+    return l;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void *v,
+                                       const int32_t *seq_lens_dev, int batch, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int s_max, float scale, float *o,
+                                       float *lse, unsigned int *device_status, fd_stream_t stream)
+{
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        s_max < 0 || !q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(o) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+        (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)))
+        return FD_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if (head_dim != kHeadDim || !(group == 1 || group == 2 || group == 4 || group == 8) ||
+        batch > kMaxBatch || (long long)batch * s_max >= (1ll << 31) ||
+        (long long)num_kv_heads * batch * ceil_div(s_max, kTileTokens) >= (1ll << 31))
+        return FD_ERR_UNSUPPORTED;
+    if (batch == 0)
+        return FD_OK;
+
+    NoallocDevice dev;
+    fd_status st = noalloc_setup(&dev);
+    if (st != FD_OK)
+        return st;
+    const int num_ctas = dev.sms;
+    const NoallocLayout wl = noalloc_layout(batch, batch * num_kv_heads + num_ctas, group);
+    if (wl.total > kNoallocScratchBytes)
+        return FD_ERR_WORKSPACE_TOO_SMALL;   // shape needs more scratch than the fixed array holds
+
+    // Split-kernel parameters, pointing into the fixed array.
+    SplitParams sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.q = static_cast<const uint16_t *>(q);
+    sp.seq_lens = seq_lens_dev;
+    sp.o = o;
+    sp.lse = lse;
+    sp.ws_err = reinterpret_cast<unsigned int *>(dev.scratch);
+    sp.ws_prefix = reinterpret_cast<int32_t *>(dev.scratch + wl.prefix_off);
+    sp.ws_lse = reinterpret_cast<float *>(dev.scratch + wl.lse_off);
+    sp.ws_o = reinterpret_cast<float *>(dev.scratch + wl.o_off);
+    sp.batch = batch;
+    sp.hq = num_q_heads;
+    sp.hkv = num_kv_heads;
+    sp.cap = s_max;
+    sp.s_max = s_max;
+    sp.scale_log2 = scale * 1.4426950408889634f;
+    sp.timeout_ns = 2000000000ull;
+
+    // Shared-memory plan (same rule as the workspace entry points).
+    const size_t red = align_up((size_t)kConsumerWarps * group * (kHeadDim + 2) * sizeof(float), 16);
+    const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
+    const size_t misc = 64;
+    const size_t fixed = 1024 + red + prefix + misc + 8;
+    if ((size_t)dev.smem_optin <= fixed)
+        return FD_ERR_UNSUPPORTED;
+    int ns = (int)(((size_t)dev.smem_optin - fixed) / (kStageBytes + 2 * 8 + kMetaInts * sizeof(int)));
+    if (ns > kMaxStages)
+        ns = kMaxStages;
+    if (ns < 2)
+        return FD_ERR_UNSUPPORTED;
+    sp.num_stages = ns;
+    sp.off_red = (uint32_t)(ns * kStageBytes);
+    sp.off_prefix = (uint32_t)(sp.off_red + red);
+    sp.off_bar = (uint32_t)(sp.off_prefix + prefix);
+    sp.off_meta = (uint32_t)(sp.off_bar + (2 * ns + 1) * 8);
+    sp.off_misc = (uint32_t)(sp.off_meta + ns * kMetaInts * sizeof(int));
+
+    SplitLaunch launch;
+    launch.grid = num_ctas;
+    launch.smem_bytes = 1024 + sp.off_misc + misc;
+    launch.smem_optin = (size_t)dev.smem_optin;
+    launch.stream = reinterpret_cast<cudaStream_t>(stream);
+
+    MergeParams mp;
+    mp.o = o;
+    mp.lse = lse;
+    mp.ws_o = sp.ws_o;
+    mp.ws_lse = sp.ws_lse;
+    mp.ws_prefix = sp.ws_prefix;
+    mp.batch = batch;
+    mp.hq = num_q_heads;
+    mp.hkv = num_kv_heads;
+    mp.num_ctas = num_ctas;
+
+    alignas(64) CUtensorMap tmk, tmv;
+    const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
+    if ((st = encode_rows(&tmk, k, num_kv_heads, rows)) != FD_OK ||
+        (st = encode_rows(&tmv, v, num_kv_heads, rows)) != FD_OK)
+        return st;
+
+    // The error word is the only part of the scratch that must start at zero.
+    if (cudaMemsetAsync(sp.ws_err, 0, sizeof(unsigned int), launch.stream) != cudaSuccess)
+        return FD_ERR_CUDA;
+    if (launch_split_contig(group, sp, tmk, tmv, launch) != cudaSuccess)
+        return FD_ERR_CUDA;
+    if (launch_merge(group, mp, batch * num_kv_heads, launch.stream) != cudaSuccess)
+        return FD_ERR_CUDA;
+    if (device_status &&
+        cudaMemcpyAsync(device_status, sp.ws_err, sizeof(unsigned int), cudaMemcpyDeviceToDevice,
+                        launch.stream) != cudaSuccess)
+        return FD_ERR_CUDA;
+    return FD_OK;
+}

@@ -157,6 +157,49 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
                           void *workspace, size_t workspace_bytes,
                           const fd_options *opts, fd_stream_t stream);
 
+/* Bytes of the fixed device scratch array used by fd_decode_noalloc. */
+#define FD_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Bits of the status word fd_decode_noalloc writes to *device_status. */
+#define FD_DEVICE_STATUS_TIMEOUT 0x1u     /* a bounded wait ran out */
+#define FD_DEVICE_STATUS_BAD_LENGTH 0x2u  /* a device length was outside [0, s_max] and was clamped */
+
+/*
+ * fd_decode without a workspace, for callers that cannot allocate device
+ * memory where they run attention: code inside a host framework or plugin
+ * that forbids device allocation at that point, latency-critical paths that
+ * must not risk an allocation stalling or failing, and applications whose
+ * device memory all belongs to their own pool.  The sources this library
+ * follows have no counterpart to this call; it exists only for such callers.
+ *
+ * It computes exactly what fd_decode computes (same kernels, contiguous
+ * layout, one split CTA per SM), with the split partials and the tile prefix
+ * held in a fixed device array of FD_NOALLOC_SCRATCH_BYTES (8 MiB) that is
+ * part of this library: every GPU that loads the library reserves it until
+ * the process exits.  Nothing is allocated -- no cudaMalloc, cudaFree or
+ * allocating library routine -- and no workspace is passed.  The caller still
+ * passes the inputs and the outputs.
+ *   q, k, v, seq_lens_dev, batch, num_q_heads, num_kv_heads, head_dim, s_max,
+ *   scale, o, lse: as for fd_decode (lse may be NULL).
+ *   device_status: NULL, or a device uint32 that receives this call's
+ *   FD_DEVICE_STATUS_* bits (0 when all went well), stream-ordered.
+ * Limits: the scratch must hold 256 bytes + 4 (batch + 1) bytes + (batch *
+ * num_kv_heads + number of SMs) partials of (Hq/Hkv) * (head_dim + 1) * 4
+ * bytes, each region rounded up to 256 bytes; a larger shape returns
+ * FD_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ * The first call on each device resolves the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.
+ * Every call on a device shares the one array, which keeps the previous
+ * call's contents; each call clears the part that must start at zero (the
+ * status word) itself.  Calls whose kernels can overlap on the GPU (for
+ * example on two unordered streams) race on the array: order them.
+ */
+fd_status fd_decode_noalloc(const void *q, const void *k, const void *v,
+                            const int32_t *seq_lens_dev, int batch, int num_q_heads,
+                            int num_kv_heads, int head_dim, int s_max, float scale, float *o,
+                            float *lse, unsigned int *device_status, fd_stream_t stream);
+
 /*
  * Read and clear the sticky device-error word of a workspace: FD_OK,
  * FD_ERR_TIMEOUT or FD_ERR_DEVICE_INPUT (timeout wins if both happened).
