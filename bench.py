@@ -223,14 +223,16 @@ def run_ours(args, rank, world):
     kvs = [(k, v)] + [(k.clone(), v.clone()) for _ in range(copies - 1)]
     stream = torch.cuda.current_stream(dev)
 
+    flags = fd.FD_FLAG_CUDA_CORES if args.cuda_cores else 0
+
     def step(i, events=None):
         kk, vv = kvs[i % copies]
         if w.paged:
             fd.fd_decode_paged(q, kk, vv, table, lens, scale=w.scale, out=out, lse=lse, workspace=ws,
-                               split_events=events)
+                               split_events=events, flags=flags)
         else:
             fd.fd_decode(q, kk, vv, lens, scale=w.scale, out=out, lse=lse, workspace=ws,
-                         split_events=events)
+                         split_events=events, flags=flags)
 
     for i in range(args.warmup):
         step(i)
@@ -238,26 +240,71 @@ def run_ours(args, rank, world):
     assert fd.fd_get_device_error(ws) == fd.FD_OK
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for a, b in ev:            # torch creates the CUDA event on first record
-        a.record(stream)
-        b.record(stream)
+    # Headline: replay a CUDA graph of `chunk` back-to-back calls (the way a
+    # serving loop issues decode steps); eager per-call time is reported too.
+    chunk = min(K, 50 if copies == 1 else copies * max(1, 50 // copies))
+    graph, graph_error = None, None
+    if not args.eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            cap_stream = torch.cuda.Stream(dev)
+            cap_stream.wait_stream(stream)
+            with torch.cuda.stream(cap_stream):
+                with torch.cuda.graph(graph, stream=cap_stream):
+                    for i in range(chunk):
+                        step(i)
+            stream.wait_stream(cap_stream)
+            for _ in range(2):
+                graph.replay()
+            torch.cuda.synchronize()
+        except Exception as exc:          # report it and time eager calls instead
+            graph, graph_error = None, f"{type(exc).__name__}: {exc}"[:200]
+            torch.cuda.synchronize()
+    reps = max(1, K // chunk) if graph else K
+    K = reps * chunk if graph else K
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        # Timed region 1 (the headline): K back-to-back calls, nothing between them.
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
         t_wall0 = time.time()
         e0.record(stream)
-        for i in range(K):
-            step(i, ev[i])
+        if graph:
+            for _ in range(reps):
+                graph.replay()
+        else:
+            for i in range(K):
+                step(i)
         e1.record(stream)
         torch.cuda.synchronize()
         t_wall1 = time.time()
         if dist:
             dist.barrier()
+        # Timed region 2 (the roofline): eager calls with CUDA events recorded
+        # on the stream around every split-kernel launch.
+        K2 = min(K, 2000)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K2)]
+        for a_, b_ in ev:          # torch creates the CUDA event on first record
+            a_.record(stream)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        for i in range(K2):
+            step(i, ev[i])
+        torch.cuda.synchronize()
     ms_total = e0.elapsed_time(e1)
-    split_ms = [a.elapsed_time(b) for a, b in ev]
+    split_ms = [a_.elapsed_time(b_) for a_, b_ in ev]
+    # eager calls without events (host marshalling + two launches per call)
+    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_eager = min(K, 500)
+    torch.cuda.synchronize()
+    a_.record(stream)
+    for i in range(n_eager):
+        step(i)
+    b_.record(stream)
+    torch.cuda.synchronize()
+    eager_us = a_.elapsed_time(b_) / n_eager * 1e3
     ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / K
     bc = byte_counts(w, P)
@@ -336,12 +383,16 @@ def run_ours(args, rank, world):
                        else f"ragged sum={int(w.seq_lens.sum())}",
                        "layout": f"paged P={w.page_size}" if w.paged else "contiguous",
                        "split_ctas": P, "parallelism": f"replicas x{world}",
+                       "launch": f"cuda graph of {chunk} calls" if graph else "eager",
+                       "graph_error": graph_error, "eager_us_per_call": eager_us,
                        "l2": (f"rotating {copies} K/V copies (> 2x L2)" if copies > 1
                               else f"inputs {kv_alloc / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB, no flush")},
             "bytes_per_call": bc["call"], "bytes_detail": bc,
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": "fd::split_kernel", "split_us": split_avg_ms * 1e3,
+                         "consumers": ("cuda cores" if (args.cuda_cores or w.num_q_heads == w.num_kv_heads)
+                                       else "tensor cores (mma.sync bf16)"),
                          "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"},
             "gpu_launches": 2 * K,
             "clocks": clk.summary(t_wall0, t_wall1),
@@ -386,11 +437,15 @@ def cpu_baseline(w, seconds):
     dt = time_oracle(w, items, threads)
     n = int(min(total_rows, max(n, n * seconds / max(dt, 1e-3))))
     items, by = oracle_sample(w, n)
-    dt = time_oracle(w, items, threads)
-    return {"value": by / dt / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
-            "seconds": dt,
-            "sample": f"{n} of {total_rows} query rows (whole kv length each), fp64 C oracle, "
-                      f"{threads} threads; bytes = K+V rows streamed per query row"}
+    reps, total, t = 0, 0, 0.0
+    while t < seconds and reps < 1000:
+        t += time_oracle(w, items, threads)
+        total += by
+        reps += 1
+    return {"value": total / t / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
+            "seconds": t,
+            "sample": f"{n} of {total_rows} query rows (whole kv length each) x {reps} repetitions, "
+                      f"fp64 C oracle, {threads} threads; bytes = K+V rows streamed per query row"}
 
 
 def run_reference(args, rank, world):
@@ -434,6 +489,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager calls instead of a CUDA graph")
+    ap.add_argument("--cuda-cores", action="store_true",
+                    help="force the CUDA-core consumers for GQA groups (comparison runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)

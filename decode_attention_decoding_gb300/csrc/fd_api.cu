@@ -74,20 +74,23 @@ EncodeTiledFn encode_fn()
 
 // A rank-3 view {head_dim, Hkv, rows} of a bf16 K or V tensor whose rows are
 // (token, kv head) pairs of 256 bytes; each load is a box of box_rows tokens
-// of one kv head.
-fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows)
+// of one kv head: the whole 128-dim row, or (swizzled) 64 dims of it with the
+// 128-byte swizzle that the tensor-core consumers read.
+fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
+                        bool swizzled)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return FD_ERR_CUDA;
     const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)rows};
     const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)hkv * kRowBytes};
-    const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1u, (cuuint32_t)box_rows};
+    const cuuint32_t box[3] = {(cuuint32_t)(swizzled ? kHeadDim / 2 : kHeadDim), 1u,
+                               (cuuint32_t)box_rows};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
 }
 
@@ -115,7 +118,17 @@ struct CallPlan {
     MergeParams mp;
     SplitLaunch launch;
     int group;
+    bool mma;   // tensor-core consumers (GQA groups) instead of CUDA cores
 };
+
+// Tensor-core consumers serve GQA groups; paged pools need pages of at least
+// 8 tokens so every page box starts on a 1 KB swizzle boundary.
+bool use_mma(int group, int page_size, const fd_options *opts)
+{
+    if (opts && (opts->flags & FD_FLAG_CUDA_CORES))
+        return false;
+    return group >= 2 && (page_size == 0 || page_size >= 8);
+}
 
 // Shared-memory plan of the split kernel for `group` and `batch`; fills the
 // offsets and stage count in sp and the byte size in launch.
@@ -197,6 +210,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     mp.hkv = hkv;
     mp.num_ctas = num_ctas;
     cp->group = group;
+    cp->mma = use_mma(group, page_size, opts);
     return FD_OK;
 }
 
@@ -208,8 +222,13 @@ fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUte
     cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_end_event) : nullptr;
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    cudaError_t e = paged ? launch_split_paged(cp.group, cp.sp, tmk, tmv, cp.launch)
-                          : launch_split_contig(cp.group, cp.sp, tmk, tmv, cp.launch);
+    cudaError_t e;
+    if (cp.mma)
+        e = paged ? launch_split_paged_mma(cp.group, cp.sp, tmk, tmv, cp.launch)
+                  : launch_split_contig_mma(cp.group, cp.sp, tmk, tmv, cp.launch);
+    else
+        e = paged ? launch_split_paged(cp.group, cp.sp, tmk, tmv, cp.launch)
+                  : launch_split_contig(cp.group, cp.sp, tmk, tmv, cp.launch);
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess)
@@ -276,8 +295,8 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
         return st;
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
-    if ((st = encode_kv_map(&tmk, k, num_kv_heads, rows, kTileTokens)) != FD_OK ||
-        (st = encode_kv_map(&tmv, v, num_kv_heads, rows, kTileTokens)) != FD_OK)
+    if ((st = encode_kv_map(&tmk, k, num_kv_heads, rows, kTileTokens, cp.mma)) != FD_OK ||
+        (st = encode_kv_map(&tmv, v, num_kv_heads, rows, kTileTokens, cp.mma)) != FD_OK)
         return st;
     return run(cp, false, tmk, tmv, opts);
 }
@@ -325,8 +344,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)num_pages * page_size;
     const int box = page_size < kTileTokens ? page_size : kTileTokens;
-    if ((st = encode_kv_map(&tmk, k_pages, num_kv_heads, rows, box)) != FD_OK ||
-        (st = encode_kv_map(&tmv, v_pages, num_kv_heads, rows, box)) != FD_OK)
+    if ((st = encode_kv_map(&tmk, k_pages, num_kv_heads, rows, box, cp.mma)) != FD_OK ||
+        (st = encode_kv_map(&tmv, v_pages, num_kv_heads, rows, box, cp.mma)) != FD_OK)
         return st;
     return run(cp, true, tmk, tmv, opts);
 }

@@ -1,4 +1,4 @@
-// fd_kernels.cuh -- split-KV decode attention kernels (sm_103a, CUDA cores).
+// fd_kernels.cuh -- split-KV decode attention kernels (sm_103a).
 //
 // Split kernel ("pass 1" of 纯手搓 flash decoding sm120, section 1/2; the
 // Flash-Decoding section of the FlashAttention handbook page): a persistent
@@ -8,7 +8,9 @@
 //     for a free shared-memory stage, writes the tile's metadata, and issues
 //     TMA loads of the K and V tiles (paged: one load per page, addressed
 //     through the block table) that complete on the stage's "full" mbarrier;
-//   * warps 0..7 are consumers: warp w reads rows 8w..8w+7 of every tile, two
+//   * warps 0..7 are consumers (CUDA-core variant shown here; the
+//     tensor-core variant for GQA groups is described at split_consumer_mma):
+//     warp w reads rows 8w..8w+7 of every tile, two
 //     rows at a time (one per half-warp; each lane holds 8 of the 128 head
 //     dimensions, read as one 16-byte shared load).  For every query head of
 //     the kv head's GQA group it forms the score q.k in fp32 (packed
@@ -38,6 +40,7 @@ constexpr int kSplitThreads = kConsumerThreads + 32;
 constexpr int kRowBytes = kHeadDim * 2;                 // one bf16 K or V row
 constexpr int kTileBytes = kTileTokens * kRowBytes;     // 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;             // K tile + V tile
+constexpr int kHalfBytes = kTileBytes / 2;              // 64 tokens x 64 dims (swizzled layout)
 constexpr int kMaxStages = 6;
 constexpr int kMetaInts = 8;
 constexpr int kRowsPerWarp = kTileTokens / kConsumerWarps;   // 8
@@ -165,7 +168,7 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
 
 // ------------------------------------------------------------------ producer
 
-template <bool PAGED>
+template <bool PAGED, bool SW128>
 __device__ __forceinline__ void split_producer(const SplitParams &p, const CUtensorMap *tmk,
                                                const CUtensorMap *tmv, uint32_t stage0,
                                                const int *prefix, int *meta, uint32_t full0,
@@ -258,20 +261,30 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             m[5] = b * p.hkv + h;
         }
         const uint32_t extra = (starve && issued == 0) ? 256u : 0u;
+        // One K and one V box per tile (or per page); with the 128-byte
+        // swizzle each box is split into two half-rows of 64 dims that land
+        // in separate 8 KB regions of the tile.
+        auto load_kv = [&](uint32_t koff, int row) {
+            if constexpr (SW128) {
+                tma_load_3d(kdst + koff, tmk, full, 0, h, row, policy);
+                tma_load_3d(kdst + kHalfBytes + koff, tmk, full, kHeadDim / 2, h, row, policy);
+                tma_load_3d(vdst + koff, tmv, full, 0, h, row, policy);
+                tma_load_3d(vdst + kHalfBytes + koff, tmv, full, kHeadDim / 2, h, row, policy);
+            } else {
+                tma_load_3d(kdst + 2 * koff, tmk, full, 0, h, row, policy);
+                tma_load_3d(vdst + 2 * koff, tmv, full, 0, h, row, policy);
+            }
+        };
         if constexpr (!PAGED) {
             mbar_arrive_expect_tx(full, 2 * kTileBytes + extra);
-            const int row = b * p.s_max + token0;
-            tma_load_3d(kdst, tmk, full, 0, h, row, policy);
-            tma_load_3d(vdst, tmv, full, 0, h, row, policy);
+            load_kv(0, b * p.s_max + token0);
         } else {
             const int P = p.page_size;
             if (P >= kTileTokens) {
                 const int phys = table_entry(token0 / P);
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full, 2 * kTileBytes + extra);
-                    const int row = phys * P + (token0 % P);
-                    tma_load_3d(kdst, tmk, full, 0, h, row, policy);
-                    tma_load_3d(vdst, tmv, full, 0, h, row, policy);
+                    load_kv(0, phys * P + (token0 % P));
                 }
             } else {
                 const int per_tile = kTileTokens / P;
@@ -281,11 +294,8 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
                     mbar_arrive_expect_tx(full, 2u * need * P * kRowBytes + extra);
                 for (int k = 0; k < need; ++k) {
                     const int phys = table_entry(pg0 + k);
-                    if (lane == 0) {
-                        const int row = phys * P;
-                        tma_load_3d(kdst + k * P * kRowBytes, tmk, full, 0, h, row, policy);
-                        tma_load_3d(vdst + k * P * kRowBytes, tmv, full, 0, h, row, policy);
-                    }
+                    if (lane == 0)
+                        load_kv(k * P * (kRowBytes / 2), phys * P);
                 }
             }
             __syncwarp();
@@ -316,6 +326,44 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
 }
 
 // ------------------------------------------------------------------ consumer
+
+// Combine NSTATE partial softmax states (m, l, acc[G][D]) published in shared
+// memory and write the segment's result: final O/LSE when the CTA saw the
+// whole segment, otherwise a normalised partial and its LSE.
+template <int G, int NSTATE>
+__device__ __forceinline__ void combine_and_write(const SplitParams &p, const float *red_acc,
+                                                  const float *red_m, const float *red_l, int ctid,
+                                                  int b, int h, int u, bool own)
+{
+    const int slot = u + (int)blockIdx.x;
+    for (int idx = ctid; idx < G * kHeadDim; idx += kConsumerThreads) {
+        const int g = idx / kHeadDim, d = idx % kHeadDim;
+        float M = kNegInf;
+#pragma unroll
+        for (int w = 0; w < NSTATE; ++w)
+            M = fmaxf(M, red_m[w * G + g]);
+        float lsum = 0.f, o = 0.f;
+#pragma unroll
+        for (int w = 0; w < NSTATE; ++w) {
+            const float mw = red_m[w * G + g];
+            const float wt = (mw == kNegInf) ? 0.f : exp2_approx(mw - M);
+            lsum += wt * red_l[w * G + g];
+            o += wt * red_acc[(w * G + g) * kHeadDim + d];
+        }
+        const float out = lsum > 0.f ? o / lsum : 0.f;
+        const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : kNegInf;
+        if (own) {
+            const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
+            p.o[row * kHeadDim + d] = out;
+            if (d == 0 && p.lse)
+                p.lse[row] = lse_v;
+        } else {
+            p.ws_o[((size_t)slot * G + g) * kHeadDim + d] = out;
+            if (d == 0)
+                p.ws_lse[(size_t)slot * G + g] = lse_v;
+        }
+    }
+}
 
 template <int G>
 __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *smem, uint32_t stage0,
@@ -504,35 +552,8 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                 return;
             }
             // 3. combine the warps and write the segment's result
-            const bool own = (flags & kOwnSegment) != 0;
-            const int slot = u + (int)blockIdx.x;
-            for (int idx = ctid; idx < G * kHeadDim; idx += kConsumerThreads) {
-                const int g = idx / kHeadDim, d = idx % kHeadDim;
-                float M = kNegInf;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    M = fmaxf(M, red_m[w * G + g]);
-                float lsum = 0.f, o = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float mw = red_m[w * G + g];
-                    const float wt = (mw == kNegInf) ? 0.f : exp2_approx(mw - M);
-                    lsum += wt * red_l[w * G + g];
-                    o += wt * red_acc[(w * G + g) * kHeadDim + d];
-                }
-                const float out = lsum > 0.f ? o / lsum : 0.f;
-                const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : kNegInf;
-                if (own) {
-                    const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
-                    p.o[row * kHeadDim + d] = out;
-                    if (d == 0 && p.lse)
-                        p.lse[row] = lse_v;
-                } else {
-                    p.ws_o[((size_t)slot * G + g) * kHeadDim + d] = out;
-                    if (d == 0)
-                        p.ws_lse[(size_t)slot * G + g] = lse_v;
-                }
-            }
+            combine_and_write<G, kConsumerWarps>(p, red_acc, red_m, red_l, ctid, b, h, u,
+                                                 (flags & kOwnSegment) != 0);
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
@@ -554,9 +575,221 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
     }
 }
 
+
+// ------------------------------------------------------------------ tensor-core consumer
+//
+// GQA groups (G = Hq/Hkv >= 2) make q.K^T a small dense contraction: for a
+// 16-token slice of a tile, S^T[16 x 8] = K[16 x 128] . Q^T[128 x 8] with the
+// group's query heads as the 8 columns (padded with zero heads when G < 8),
+// and O^T[128 x 8] += V^T[128 x 16] . P^T[16 x 8].  Both are warp-level
+// m16n8k16 bf16 MMAs with fp32 accumulation.  The tile arrives with the
+// 128-byte TMA swizzle (two 8 KB halves of 64 dims each), so the ldmatrix
+// row reads are free of bank conflicts.  P is rounded to bf16 for the second
+// product and the running sum l adds up exactly those rounded weights.
+//
+// Warps 2i and 2i+1 take tokens 16i..16i+15 of every tile; both form the
+// scores (so each holds the softmax state), and for P.V warp 2i covers dims
+// 0..63 and warp 2i+1 dims 64..127.
+
+// Byte address of 16-byte chunk `chunk` (0..15) of `row` in a swizzled tile.
+__device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk)
+{
+    return tile + (chunk >> 3) * kHalfBytes + row * (kRowBytes / 2) + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+template <int G>
+__device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t *smem, uint32_t stage0,
+                                                   const int *meta, uint32_t full0, uint32_t empty0,
+                                                   uint32_t cbar, volatile int *abort_flag, int t_begin,
+                                                   int t_end, int cw, int lane)
+{
+    static_assert(G >= 1 && G <= 8, "one n8 tile of query heads");
+    constexpr int kPairs = kConsumerWarps / 2;
+    const int NS = p.num_stages;
+    const int pair = cw >> 1, dhalf = cw & 1;
+    const int grp = lane >> 2, qd = lane & 3;   // mma fragment coordinates
+    const int tok0 = pair * 16;
+    float *red_acc = reinterpret_cast<float *>(smem + p.off_red);   // [pairs][G][D]
+    float *red_m = red_acc + kConsumerWarps * G * kHeadDim;          // [pairs][G]
+    float *red_l = red_m + kConsumerWarps * G;                       // [pairs][G]
+    const int ctid = cw * 32 + lane;
+
+    uint32_t qb[8][2];         // Q^T B-fragments, one pair per 16-dim k-step
+    float acc[4][4];           // O^T fragments of this warp's 4 dim tiles
+    float m[2], l[2];          // heads 2 qd and 2 qd + 1 (l: this lane's tokens only)
+    auto reset = [&]() {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            m[j] = kNegInf;
+            l[j] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                acc[i][c] = 0.f;
+    };
+    auto give_up = [&]() {
+        if (lane == 0) {
+            atomicOr(p.ws_err, kErrTimeout);
+            *abort_flag = 1;
+        }
+    };
+    reset();
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+        qb[ks][0] = qb[ks][1] = 0u;
+
+    int s = 0;
+    uint32_t ph = 0, cph = 0;
+    for (int t = t_begin; t < t_end; ++t) {
+        if (!warp_wait(full0 + 8 * s, ph, p.timeout_ns, abort_flag)) {
+            give_up();
+            return;
+        }
+        const int *mt = meta + s * kMetaInts;
+        const int b = mt[0], h = mt[1], nvalid = mt[3], flags = mt[4], u = mt[5];
+
+        if (flags & kFirstInCta) {
+            // B[k = d][n = head]: lane holds head `grp`, dims 16 ks + 2 qd (+1) and (+8, +9).
+            if (grp < G) {
+                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                    p.q + ((size_t)b * p.hq + (size_t)h * G + grp) * kHeadDim);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    qb[ks][0] = __ldg(qrow + ks * 8 + qd);
+                    qb[ks][1] = __ldg(qrow + ks * 8 + 4 + qd);
+                }
+            }
+        }
+
+        const uint32_t ktile = stage0 + s * kStageBytes;
+        const uint32_t vtile = ktile + kTileBytes;
+
+        // S^T = K . Q^T for tokens tok0 .. tok0 + 15 (fragment rows grp and grp + 8).
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int row = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(sw128_addr(ktile, row, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+                mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            }
+        }
+        const bool v0 = tok0 + grp < nvalid, v1 = tok0 + grp + 8 < nvalid;
+        // sc[0]: (token grp, head 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1)
+        float x[4];
+        x[0] = v0 ? sc[0] * p.scale_log2 : kNegInf;
+        x[1] = v0 ? sc[1] * p.scale_log2 : kNegInf;
+        x[2] = v1 ? sc[2] * p.scale_log2 : kNegInf;
+        x[3] = v1 ? sc[3] * p.scale_log2 : kNegInf;
+
+        // Online softmax over this warp's 16 tokens, per head.
+        float alpha[2], pw[4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = fmaxf(x[j], x[j + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m[j], mx);
+            alpha[j] = (m[j] == kNegInf) ? 0.f : exp2_approx(m[j] - m_new);
+            pw[j] = (x[j] == kNegInf) ? 0.f : exp2_approx(x[j] - m_new);
+            pw[j + 2] = (x[j + 2] == kNegInf) ? 0.f : exp2_approx(x[j + 2] - m_new);
+            m[j] = m_new;
+        }
+        const uint32_t p_lo = pack_bf16x2(pw[0], pw[1]);   // token grp, heads 2qd, 2qd+1
+        const uint32_t p_hi = pack_bf16x2(pw[2], pw[3]);   // token grp + 8
+        {
+            const float2 r_lo = bf16x2_to_float2(p_lo), r_hi = bf16x2_to_float2(p_hi);
+            l[0] = l[0] * alpha[0] + (r_lo.x + r_hi.x);
+            l[1] = l[1] * alpha[1] + (r_lo.y + r_hi.y);
+        }
+        // P^T as the B operand (k = token, n = head): transpose the 8x8 blocks.
+        const uint32_t pb0 = movmatrix_trans(p_lo);
+        const uint32_t pb1 = movmatrix_trans(p_hi);
+
+        // Rows past the request's end may hold anything (even NaN), and the
+        // tensor core would form 0 * NaN: zero this warp's half of them.
+        const bool ragged = nvalid < tok0 + 16;
+        if (ragged) {
+            const int first = nvalid > tok0 ? nvalid : tok0;
+            const uint32_t base = vtile + dhalf * kHalfBytes;
+            for (int idx = lane; idx < (tok0 + 16 - first) * 8; idx += 32) {
+                const uint32_t a = base + (first + (idx >> 3)) * (kRowBytes / 2) + ((idx & 7) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+            }
+            __syncwarp();
+        }
+
+        // O^T = alpha O^T + V^T . P^T over this warp's 64 dims.
+        {
+            const int vrow = tok0 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[i][0] *= alpha[0];
+                acc[i][1] *= alpha[1];
+                acc[i][2] *= alpha[0];
+                acc[i][3] *= alpha[1];
+                const int dt = dhalf * 4 + i;   // 16-dim tile index
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4_trans(sw128_addr(vtile, vrow, 2 * dt + ((lane >> 3) & 1)), a0, a1, a2, a3);
+                mma_bf16_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
+            }
+        }
+        if (ragged)   // order the zeroing stores before the next TMA write to this stage
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty0 + 8 * s);
+
+        if (flags & kLastInCta) {
+            // l over the warp's 16 tokens (lanes sharing qd hold the same heads)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
+                l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
+                l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int head = 2 * qd + j;
+                if (head < G) {
+                    if (dhalf == 0 && grp == 0) {
+                        red_m[pair * G + head] = m[j];
+                        red_l[pair * G + head] = l[j];
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int d = (dhalf * 4 + i) * 16 + grp;
+                        red_acc[(pair * G + head) * kHeadDim + d] = acc[i][j];
+                        red_acc[(pair * G + head) * kHeadDim + d + 8] = acc[i][j + 2];
+                    }
+                }
+            }
+            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
+                give_up();
+                return;
+            }
+            combine_and_write<G, kPairs>(p, red_acc, red_m, red_l, ctid, b, h, u,
+                                         (flags & kOwnSegment) != 0);
+            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
+                give_up();
+                return;
+            }
+            reset();
+        }
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ kernels
 
-template <int G, bool PAGED>
+template <int G, bool PAGED, bool MMA>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv)
@@ -594,8 +827,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         return;
     volatile int *abort_flag = misc;
     if (warp == kConsumerWarps)
-        split_producer<PAGED>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag, t_begin,
-                              t_end, lane);
+        split_producer<PAGED, MMA>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
+                                   t_begin, t_end, lane);
+    else if constexpr (MMA)
+        split_consumer_mma<G>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin, t_end,
+                              warp, lane);
     else
         split_consumer<G>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin, t_end, warp,
                           lane);

@@ -1,6 +1,8 @@
 // fd_launch.h -- host-side launch wrappers, one per kernel translation unit.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -15,31 +17,46 @@ struct SplitLaunch {
     cudaStream_t stream;
 };
 
+// Split kernel with CUDA-core consumers; K/V tensor maps without swizzle.
 // Returns cudaErrorInvalidValue for an unsupported group size.
 cudaError_t launch_split_contig(int group, const SplitParams &p, const CUtensorMap &tmk,
                                 const CUtensorMap &tmv, const SplitLaunch &cfg);
 cudaError_t launch_split_paged(int group, const SplitParams &p, const CUtensorMap &tmk,
                                const CUtensorMap &tmv, const SplitLaunch &cfg);
+// Split kernel with tensor-core consumers (group 2, 4 or 8); K/V tensor maps
+// with 64-dim boxes and the 128-byte swizzle.
+cudaError_t launch_split_contig_mma(int group, const SplitParams &p, const CUtensorMap &tmk,
+                                    const CUtensorMap &tmv, const SplitLaunch &cfg);
+cudaError_t launch_split_paged_mma(int group, const SplitParams &p, const CUtensorMap &tmk,
+                                   const CUtensorMap &tmv, const SplitLaunch &cfg);
 cudaError_t launch_merge(int group, const MergeParams &p, int grid, cudaStream_t stream);
 
 // Shared by the two split translation units.
-template <int G, bool PAGED>
+template <int G, bool PAGED, bool MMA>
 cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const SplitLaunch &c)
 {
-    // cudaFuncSetAttribute is idempotent and cheap; it raises the kernel's
-    // dynamic shared-memory limit to the device's opt-in maximum.
-    cudaError_t e = cudaFuncSetAttribute(split_kernel<G, PAGED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)c.smem_optin);
+    // Raise the kernel's dynamic shared-memory limit to the device's opt-in
+    // maximum, once per device (so later calls may be captured in a graph).
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(split_kernel<G, PAGED, MMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)c.smem_optin);
+        if (e != cudaSuccess)
+            return e;
+        configured.fetch_or(bit, std::memory_order_release);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)c.grid);
     cfg.blockDim = dim3(kSplitThreads);
     cfg.dynamicSmemBytes = c.smem_bytes;
     cfg.stream = c.stream;
-    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED>, p, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, MMA>, p, tmk, tmv);
 }
 
 }  // namespace fd

@@ -7,10 +7,21 @@ cudaError_t launch_split_paged(int group, const SplitParams &p, const CUtensorMa
                                const CUtensorMap &tmv, const SplitLaunch &cfg)
 {
     switch (group) {
-    case 1: return launch_split_t<1, true>(p, tmk, tmv, cfg);
-    case 2: return launch_split_t<2, true>(p, tmk, tmv, cfg);
-    case 4: return launch_split_t<4, true>(p, tmk, tmv, cfg);
-    case 8: return launch_split_t<8, true>(p, tmk, tmv, cfg);
+    case 1: return launch_split_t<1, true, false>(p, tmk, tmv, cfg);
+    case 2: return launch_split_t<2, true, false>(p, tmk, tmv, cfg);
+    case 4: return launch_split_t<4, true, false>(p, tmk, tmv, cfg);
+    case 8: return launch_split_t<8, true, false>(p, tmk, tmv, cfg);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_split_paged_mma(int group, const SplitParams &p, const CUtensorMap &tmk,
+                                   const CUtensorMap &tmv, const SplitLaunch &cfg)
+{
+    switch (group) {
+    case 2: return launch_split_t<2, true, true>(p, tmk, tmv, cfg);
+    case 4: return launch_split_t<4, true, true>(p, tmk, tmv, cfg);
+    case 8: return launch_split_t<8, true, true>(p, tmk, tmv, cfg);
     default: return cudaErrorInvalidValue;
     }
 }

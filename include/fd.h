@@ -88,6 +88,13 @@ typedef struct fd_options {
  * production; the outputs of such a call are undefined. */
 #define FD_FLAG_TEST_STARVE_FIRST_TILE 0x1u
 
+/* Use the CUDA-core consumers for every group size.  By default GQA groups
+ * (Hq/Hkv >= 2, and paged pools with pages of at least 8 tokens) run q.K^T
+ * and P.V on the tensor cores (bf16 MMA, fp32 accumulation, softmax weights
+ * rounded to bf16 for P.V); this flag selects the all-fp32 CUDA-core
+ * arithmetic instead. */
+#define FD_FLAG_CUDA_CORES 0x2u
+
 /*
  * Bytes of workspace that fd_decode / fd_decode_paged need for this shape.
  * Pure host function (no CUDA call).  The size does not depend on the

@@ -11,12 +11,23 @@ from gpu_util import check, run, sample_items
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("config_id", [1, 2, 3, 4, 5])
-def test_full_size_config_sampled(config_id):
+_CACHE = {}
+
+
+def workload(config_id):
+    if config_id not in _CACHE:
+        _CACHE.clear()
+        _CACHE[config_id] = syn.make_config(config_id)
+    return _CACHE[config_id]
+
+
+# flags 2 = FD_FLAG_CUDA_CORES: the GQA workloads are checked on both consumer paths
+@pytest.mark.parametrize("config_id,flags", [(1, 0), (2, 0), (3, 0), (3, 2), (4, 0), (4, 2), (5, 0), (5, 2)])
+def test_full_size_config_sampled(config_id, flags):
     from decode_attention_decoding_gb300 import build
     build.build()
-    w = syn.make_config(config_id)
-    o, l = run(w)
+    w = workload(config_id)
+    o, l = run(w, flags=flags)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
     items = sample_items(w, 24, seed=config_id)
     if config_id == 1:          # small enough for every row
@@ -27,5 +38,5 @@ def test_full_size_config_sampled(config_id):
     else:
         b, h = items[:, 0], items[:, 1]
         stats = check(o[b, h], l[b, h], ro, rl, f"config {config_id}")
-    print(f"config {config_id}: max|dO|={stats[0]:.3g} max rel(|r|>=1e-2)={stats[1]:.3g} "
+    print(f"config {config_id} flags={flags}: max|dO|={stats[0]:.3g} max rel(|r|>=1e-2)={stats[1]:.3g} "
           f"max|dLSE|={stats[2]:.3g}")

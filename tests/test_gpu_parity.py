@@ -24,14 +24,18 @@ def built():
 RAGGED = [1000, 1, 0, 63, 64, 65, 129, 700]
 
 
+CUDA_CORES = 0x2      # FD_FLAG_CUDA_CORES: all-fp32 CUDA-core consumers for every group
+
+
+@pytest.mark.parametrize("cores", ["default", "cuda_cores"])
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
 @pytest.mark.parametrize("num_ctas", [0, 1, 3, 7, 40])
-def test_contiguous_vs_oracle(group, num_ctas):
+def test_contiguous_vs_oracle(group, num_ctas, cores):
     hkv = 4 if group <= 2 else 2
     w = syn.make_contiguous(200 + group, len(RAGGED), hkv * group, hkv, 128, 1024, RAGGED)
-    o, l = run(w, num_ctas=num_ctas)
+    o, l = run(w, num_ctas=num_ctas, flags=CUDA_CORES if cores == "cuda_cores" else 0)
     ro, rl = oracle.attend(w, threads=8)
-    check(o, l, ro, rl, f"G={group} ctas={num_ctas}")
+    check(o, l, ro, rl, f"G={group} ctas={num_ctas} {cores}")
 
 
 @pytest.mark.parametrize("page", [1, 8, 16, 32, 64, 128])
@@ -40,28 +44,31 @@ def test_paged_vs_oracle_and_contiguous(page, group):
     hkv = 2
     w = syn.make_contiguous(300 + page, len(RAGGED), hkv * group, hkv, 128, 1024, RAGGED)
     wp = contig_to_paged(w, page, perm_seed=page + group)
+    # pages under 8 tokens always take the CUDA-core consumers
+    flags = CUDA_CORES if (page < 8 and group >= 2) else 0
     for ctas in (0, 5):
         op, lp = run(wp, num_ctas=ctas)
         ro, rl = oracle.attend(wp, threads=8)
         check(op, lp, ro, rl, f"paged P={page} G={group}")
-        # identical logical data, identical tiles: bitwise identical results
-        oc, lc = run(w, num_ctas=ctas)
+        # identical logical data, identical tiles and consumers: bitwise identical results
+        oc, lc = run(w, num_ctas=ctas, flags=flags)
         assert np.array_equal(op, oc) and np.array_equal(lp, lc)
 
 
-def test_poison_past_length_and_unused_pages_is_never_read():
+@pytest.mark.parametrize("group,flags", [(4, 0), (4, CUDA_CORES), (1, 0), (8, 0)])
+def test_poison_past_length_and_unused_pages_is_never_read(group, flags):
     lens = [5, 64, 65, 200, 0, 1023]
-    w = syn.make_contiguous(400, len(lens), 8, 2, 128, 1024, lens)
-    clean_o, clean_l = run(w, num_ctas=9)
-    wn = syn.Workload(w.name, w.q, w.k.copy(), w.v.copy(), w.seq_lens, 8, 2, 128, w.scale)
+    w = syn.make_contiguous(400, len(lens), 2 * group, 2, 128, 1024, lens)
+    clean_o, clean_l = run(w, num_ctas=9, flags=flags)
+    wn = syn.Workload(w.name, w.q, w.k.copy(), w.v.copy(), w.seq_lens, 2 * group, 2, 128, w.scale)
     for b, L in enumerate(lens):
         wn.k[b, L:] = syn.BF16_NAN
         wn.v[b, L:] = syn.BF16_NAN
-    o, l = run(wn, num_ctas=9)
+    o, l = run(wn, num_ctas=9, flags=flags)
     assert np.all(np.isfinite(o)) and np.array_equal(o, clean_o) and np.array_equal(l, clean_l)
     for page in (16, 64):
         wp = contig_to_paged(w, page, perm_seed=1, extra_pages=4, poison=True)
-        op, lp = run(wp, num_ctas=9)
+        op, lp = run(wp, num_ctas=9, flags=flags)
         assert np.all(np.isfinite(op)) and np.array_equal(op, clean_o) and np.array_equal(lp, clean_l)
 
 
@@ -85,13 +92,14 @@ def test_lse_output_is_optional():
     check(o, None, ro, rl, "no lse")
 
 
+@pytest.mark.parametrize("flags", [0, CUDA_CORES])
 @pytest.mark.parametrize("factor", [8.0, 32.0])
-def test_softmax_stress_scaled_keys(factor):
+def test_softmax_stress_scaled_keys(factor, flags):
     L = 4000
     w = syn.make_contiguous(420 + int(factor), 1, 16, 2, 128, L, [L])
     toks = syn.choose(5, L, L // 100)
     syn.scale_keys(w, toks, factor)
-    o, l = run(w, num_ctas=13)
+    o, l = run(w, num_ctas=13, flags=flags)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
     ro, rl = oracle.attend(w, threads=8)
     check(o, l, ro, rl, f"keys x{factor}")
@@ -132,8 +140,9 @@ def gather_probe(L, group, hkv, t_star, seed):
     return w
 
 
+@pytest.mark.parametrize("flags", [0, CUDA_CORES])
 @pytest.mark.parametrize("layout", ["contig", 16, 64])
-def test_bit_exact_gather(layout):
+def test_bit_exact_gather(layout, flags):
     L, group, hkv = 3000, 4, 2
     stars = [0, 1, 15, 16, 63, 64, 65, 1023, 1024, 2047, 2048, L - 1]
     for ctas in (0, 7):
@@ -141,7 +150,7 @@ def test_bit_exact_gather(layout):
             w = gather_probe(L, group, hkv, t_star, seed=500)
             if layout != "contig":
                 w = contig_to_paged(w, layout, perm_seed=t_star + 1)
-            o, l = run(w, num_ctas=ctas)
+            o, l = run(w, num_ctas=ctas, flags=flags)
             for h in range(hkv * group):
                 g = h // group
                 expect = syn.bf16_bits_to_f64(
