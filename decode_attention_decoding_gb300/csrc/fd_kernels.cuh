@@ -24,8 +24,8 @@
 //     and write either the final O and natural-log LSE (the CTA saw the whole
 //     segment) or a normalised partial O and its LSE (lse = m ln2 + ln l).
 // Merge kernel ("pass 2", section 2 of the sm120 article): one CTA per
-// segment combines its partials: LSE = max + ln sum exp(lse_i - max),
-// O = sum O_i exp(lse_i - LSE).
+// (segment, query head) combines that head's partials:
+// LSE = max + ln sum exp(lse_i - max), O = sum O_i exp(lse_i - LSE).
 #pragma once
 
 #include "fd_device.cuh"
@@ -175,8 +175,9 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
                                                uint32_t empty0, volatile int *abort_flag,
                                                int t_begin, int t_end, int lane)
 {
-    if (!PAGED && lane != 0)
-        return;
+    // The whole warp walks the tiles; lane 0 arms the barriers and the TMA
+    // loads of a tile are spread over lanes (one box per lane, or one page
+    // per lane for small pages) so they issue together.
     if (lane == 0) {
         tma_prefetch_desc(tmk);
         tma_prefetch_desc(tmv);
@@ -184,6 +185,8 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     const uint64_t policy = l2_policy_evict_first();
     const int NS = p.num_stages;
     const bool starve = (p.flags & 1u) && blockIdx.x == 0;
+    // Boxes per (tile or page): K and V, each whole or as two swizzled halves.
+    constexpr int kBoxes = SW128 ? 4 : 2;
 
     int t = t_begin;
     int b = request_of_tile(prefix, p.batch, t);
@@ -199,7 +202,8 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     auto table_load = [&](int bb, int idx) -> int {
         return idx < p.max_blocks ? __ldg(p.block_table + (size_t)bb * p.max_blocks + idx) : 0;
     };
-    auto table_entry = [&](int pg) -> int {   // warp-collective, same pg in every lane
+    // Warp-collective: make the window hold page index pg (a 32-aligned window).
+    auto ensure_window = [&](int pg) {
         if (b != win_b || pg < win_base || pg >= win_base + 32) {
             if (b == win_b && pg >= nxt_base && pg < nxt_base + 32) {
                 win_base = nxt_base;
@@ -212,25 +216,33 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             nxt_base = win_base + 32;
             nxt_ent = table_load(b, nxt_base + lane);
         }
-        int e = __shfl_sync(0xffffffffu, win_ent, pg - win_base);
+    };
+    // Warp-collective: entry of page pg_lane (each lane its own, inside the window).
+    auto window_entry = [&](int pg_lane) -> int {
+        int e = __shfl_sync(0xffffffffu, win_ent, (pg_lane - win_base) & 31);
         if (e < 0 || e >= p.num_pages) {
-            if (lane == 0)
-                atomicOr(p.ws_err, kErrPage);
+            atomicOr(p.ws_err, kErrPage);
             e = 0;
         }
         return e;
+    };
+    // Box `box` (0..kBoxes-1) of the tile's K/V, `koff` bytes into each half
+    // (swizzled layout) or `2 koff` bytes into each tile (plain layout).
+    auto load_box = [&](int box, uint32_t kdst, uint32_t vdst, uint32_t full, uint32_t koff, int row) {
+        if constexpr (SW128) {
+            const uint32_t dst = ((box & 2) ? vdst : kdst) + (box & 1) * kHalfBytes + koff;
+            tma_load_3d(dst, (box & 2) ? tmv : tmk, full, (box & 1) * (kHeadDim / 2), h, row, policy);
+        } else {
+            const uint32_t dst = ((box & 1) ? vdst : kdst) + 2 * koff;
+            tma_load_3d(dst, (box & 1) ? tmv : tmk, full, 0, h, row, policy);
+        }
     };
 
     int s = 0;
     uint32_t ph = 0;
     int issued = 0;
     for (; t < t_end; ++t) {
-        bool ok;
-        if (PAGED)
-            ok = warp_wait(empty0 + 8 * s, ph ^ 1u, p.timeout_ns, abort_flag);
-        else
-            ok = mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, p.timeout_ns, abort_flag);
-        if (!ok) {
+        if (!warp_wait(empty0 + 8 * s, ph ^ 1u, p.timeout_ns, abort_flag)) {
             if (lane == 0) {
                 atomicOr(p.ws_err, kErrTimeout);
                 *abort_flag = 1;
@@ -251,6 +263,10 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
         const uint32_t full = full0 + 8 * s;
         const uint32_t kdst = stage0 + s * kStageBytes;
         const uint32_t vdst = kdst + kTileBytes;
+        const uint32_t extra = (starve && issued == 0) ? 256u : 0u;
+        const int P = p.page_size;
+        // pages of this tile that hold valid tokens (paged, P < 64)
+        const int need = (PAGED && P < kTileTokens) ? min(kTileTokens / P, ceil_div(nvalid, P)) : 1;
         if (lane == 0) {
             int *m = meta + s * kMetaInts;
             m[0] = b;
@@ -259,47 +275,33 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             m[3] = nvalid;
             m[4] = flags;
             m[5] = b * p.hkv + h;
+            const uint32_t bytes = (PAGED && P < kTileTokens) ? 2u * need * P * kRowBytes
+                                                              : (uint32_t)(2 * kTileBytes);
+            mbar_arrive_expect_tx(full, bytes + extra);
         }
-        const uint32_t extra = (starve && issued == 0) ? 256u : 0u;
-        // One K and one V box per tile (or per page); with the 128-byte
-        // swizzle each box is split into two half-rows of 64 dims that land
-        // in separate 8 KB regions of the tile.
-        auto load_kv = [&](uint32_t koff, int row) {
-            if constexpr (SW128) {
-                tma_load_3d(kdst + koff, tmk, full, 0, h, row, policy);
-                tma_load_3d(kdst + kHalfBytes + koff, tmk, full, kHeadDim / 2, h, row, policy);
-                tma_load_3d(vdst + koff, tmv, full, 0, h, row, policy);
-                tma_load_3d(vdst + kHalfBytes + koff, tmv, full, kHeadDim / 2, h, row, policy);
-            } else {
-                tma_load_3d(kdst + 2 * koff, tmk, full, 0, h, row, policy);
-                tma_load_3d(vdst + 2 * koff, tmv, full, 0, h, row, policy);
-            }
-        };
+        __syncwarp();
         if constexpr (!PAGED) {
-            mbar_arrive_expect_tx(full, 2 * kTileBytes + extra);
-            load_kv(0, b * p.s_max + token0);
+            if (lane < kBoxes)
+                load_box(lane, kdst, vdst, full, 0, b * p.s_max + token0);
+        } else if (P >= kTileTokens) {
+            ensure_window(token0 / P);
+            const int phys = window_entry(token0 / P);
+            if (lane < kBoxes)
+                load_box(lane, kdst, vdst, full, 0, phys * P + (token0 % P));
         } else {
-            const int P = p.page_size;
-            if (P >= kTileTokens) {
-                const int phys = table_entry(token0 / P);
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(full, 2 * kTileBytes + extra);
-                    load_kv(0, phys * P + (token0 % P));
-                }
-            } else {
-                const int per_tile = kTileTokens / P;
-                const int pg0 = token0 / P;
-                const int need = min(per_tile, ceil_div(nvalid, P));
-                if (lane == 0)
-                    mbar_arrive_expect_tx(full, 2u * need * P * kRowBytes + extra);
-                for (int k = 0; k < need; ++k) {
-                    const int phys = table_entry(pg0 + k);
-                    if (lane == 0)
-                        load_kv(k * P * (kRowBytes / 2), phys * P);
+            const int pg0 = token0 / P;
+            for (int k0 = 0; k0 < need; k0 += 32) {
+                ensure_window(pg0 + k0);
+                const int k = k0 + lane;
+                const int phys = window_entry(pg0 + (k < need ? k : k0));
+                if (k < need) {
+#pragma unroll
+                    for (int box = 0; box < kBoxes; ++box)
+                        load_box(box, kdst, vdst, full, k * P * (kRowBytes / 2), phys * P);
                 }
             }
-            __syncwarp();
         }
+        __syncwarp();
         ++issued;
         if (++s == NS) {
             s = 0;
@@ -837,22 +839,24 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                           lane);
 }
 
+// One CTA per (segment, query head of its group); thread d owns output dim d.
+// The partials' log-sum-exps and merge weights are staged in shared memory
+// so each output needs only one pass over the partial rows.
 template <int G>
 __global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__ MergeParams p)
 {
+    __shared__ float s_w[kMaxCtas];
+    __shared__ float s_lse;
     pdl_wait_prior_grid();
-    const int u = blockIdx.x;
+    const int u = blockIdx.x, g = blockIdx.y;
     const int b = u / p.hkv, h = u - b * p.hkv;
     const int d = threadIdx.x;
     const int pb = p.ws_prefix[b], pe = p.ws_prefix[b + 1], T = p.ws_prefix[p.batch];
-    const size_t row0 = (size_t)b * p.hq + (size_t)h * G;
+    const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
     if (pe == pb) {   // empty request: O = 0, LSE = -inf
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            p.o[(row0 + g) * kHeadDim + d] = 0.f;
-            if (d == 0 && p.lse)
-                p.lse[row0 + g] = kNegInf;
-        }
+        p.o[row * kHeadDim + d] = 0.f;
+        if (d == 0 && p.lse)
+            p.lse[row] = kNegInf;
         return;
     }
     const int nb = (pe - pb) / p.hkv;
@@ -860,24 +864,54 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__
     const int c0 = cta_of_tile(T, p.num_ctas, first), c1 = cta_of_tile(T, p.num_ctas, last);
     if (c0 == c1)
         return;   // one CTA saw the whole segment and wrote it
-#pragma unroll 1
-    for (int g = 0; g < G; ++g) {
-        float M = kNegInf;
-        for (int c = c0; c <= c1; ++c)
-            M = fmaxf(M, p.ws_lse[(size_t)(u + c) * G + g]);
-        float S = 0.f;
-        for (int c = c0; c <= c1; ++c)
-            S += expf(p.ws_lse[(size_t)(u + c) * G + g] - M);
-        const float lse = M + logf(S);
-        float acc = 0.f;
-        for (int c = c0; c <= c1; ++c) {
-            const size_t slot = (size_t)(u + c) * G + g;
-            acc += p.ws_o[slot * kHeadDim + d] * expf(p.ws_lse[slot] - lse);
-        }
-        p.o[(row0 + g) * kHeadDim + d] = acc;
-        if (d == 0 && p.lse)
-            p.lse[row0 + g] = lse;
+    const int n = c1 - c0 + 1;
+    float lmax = kNegInf;
+    for (int i = d; i < n; i += kHeadDim) {
+        const float v = p.ws_lse[(size_t)(u + c0 + i) * G + g];
+        s_w[i] = v;
+        lmax = fmaxf(lmax, v);
     }
+    // block max, then block sum of exp(lse_i - max): warp shuffles + shared memory
+    __shared__ float s_red[kHeadDim / 32];
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+    if ((d & 31) == 0)
+        s_red[d >> 5] = lmax;
+    __syncthreads();
+    float M = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kHeadDim / 32; ++w)
+        M = fmaxf(M, s_red[w]);
+    __syncthreads();
+    float sum = 0.f;
+    for (int i = d; i < n; i += kHeadDim)
+        sum += expf(s_w[i] - M);
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if ((d & 31) == 0)
+        s_red[d >> 5] = sum;
+    __syncthreads();
+    if (d == 0) {
+        float S = 0.f;
+#pragma unroll
+        for (int w = 0; w < kHeadDim / 32; ++w)
+            S += s_red[w];
+        s_lse = M + logf(S);
+    }
+    __syncthreads();
+    const float lse = s_lse;
+    for (int i = d; i < n; i += kHeadDim)
+        s_w[i] = expf(s_w[i] - lse);
+    __syncthreads();
+    float acc = 0.f;
+    const float *src = p.ws_o + ((size_t)(u + c0) * G + g) * kHeadDim + d;
+    for (int i = 0; i < n; ++i)
+        acc += src[(size_t)i * G * kHeadDim] * s_w[i];
+    p.o[row * kHeadDim + d] = acc;
+    if (d == 0 && p.lse)
+        p.lse[row] = lse;
 }
 
 }  // namespace fd

@@ -5,13 +5,14 @@
 namespace fd {
 
 template <int G>
+// grid = number of segments (requests x kv heads); one CTA per (segment, query head).
 static cudaError_t launch_merge_t(const MergeParams &p, int grid, cudaStream_t stream)
 {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
+    cfg.gridDim = dim3((unsigned)grid, (unsigned)G);   // (segment, query head of its group)
     cfg.blockDim = dim3(kHeadDim);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
