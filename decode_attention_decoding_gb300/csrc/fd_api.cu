@@ -94,6 +94,49 @@ fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long r
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
 }
 
+// A rank-4 view {64 dims, rows, 2 halves, Hkv} of the same tensor, so that
+// one box {64, box_rows, 2, 1} carries both 128-byte-swizzled 64-dim halves
+// of box_rows rows of one kv head (laid out half by half in shared memory).
+fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return FD_ERR_CUDA;
+    const cuuint64_t dims[4] = {(cuuint64_t)(kHeadDim / 2), (cuuint64_t)rows, 2u, (cuuint64_t)hkv};
+    const cuuint64_t strides[3] = {(cuuint64_t)hkv * kRowBytes, (cuuint64_t)kRowBytes / 2,
+                                   (cuuint64_t)kRowBytes};
+    const cuuint32_t box[4] = {(cuuint32_t)(kHeadDim / 2), (cuuint32_t)box_rows, 2u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
+}
+
+// K and V maps for a call: the tensor-core consumers prefer 4-D maps (one
+// box per tile or page carries both swizzled halves) and fall back to 3-D
+// maps with one box per half if the driver rejects the 4-D view.
+fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, const void *v, int hkv,
+                         long long rows, int box_rows, bool mma, SplitParams *sp)
+{
+    int rl = 0;
+    while ((1 << rl) < box_rows)
+        ++rl;
+    sp->box4d = 0;
+    sp->box_rows_log2 = 6;
+    if (mma && !(sp->flags & FD_FLAG_NO_4D_BOXES) && encode_kv_map_4d(tmk, k, hkv, rows, box_rows) == FD_OK &&
+        encode_kv_map_4d(tmv, v, hkv, rows, box_rows) == FD_OK) {
+        sp->box4d = 1;
+        sp->box_rows_log2 = rl;
+        return FD_OK;
+    }
+    fd_status st;
+    if ((st = encode_kv_map(tmk, k, hkv, rows, box_rows, mma)) != FD_OK ||
+        (st = encode_kv_map(tmv, v, hkv, rows, box_rows, mma)) != FD_OK)
+        return st;
+    return FD_OK;
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
@@ -295,8 +338,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
         return st;
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
-    if ((st = encode_kv_map(&tmk, k, num_kv_heads, rows, kTileTokens, cp.mma)) != FD_OK ||
-        (st = encode_kv_map(&tmv, v, num_kv_heads, rows, kTileTokens, cp.mma)) != FD_OK)
+    if ((st = encode_kv_maps(&tmk, &tmv, k, v, num_kv_heads, rows, kTileTokens, cp.mma, &cp.sp)) != FD_OK)
         return st;
     return run(cp, false, tmk, tmv, opts);
 }
@@ -344,8 +386,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)num_pages * page_size;
     const int box = page_size < kTileTokens ? page_size : kTileTokens;
-    if ((st = encode_kv_map(&tmk, k_pages, num_kv_heads, rows, box, cp.mma)) != FD_OK ||
-        (st = encode_kv_map(&tmv, v_pages, num_kv_heads, rows, box, cp.mma)) != FD_OK)
+    if ((st = encode_kv_maps(&tmk, &tmv, k_pages, v_pages, num_kv_heads, rows, box, cp.mma, &cp.sp)) !=
+        FD_OK)
         return st;
     return run(cp, true, tmk, tmv, opts);
 }

@@ -108,6 +108,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, uint
         : "memory");
 }
 
+// 4-D tiled bulk tensor load global -> shared, completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *desc, uint32_t bar, int c0, int c1,
+                                            int c2, int c3, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // L2 policy for data read exactly once (the KV cache stream).
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {

@@ -72,6 +72,11 @@ struct SplitParams {
     uint32_t off_red, off_prefix, off_bar, off_meta, off_misc;
     unsigned long long timeout_ns;
     unsigned int flags;
+    // Tensor-core path only: 1 when the K/V tensor maps are 4-D views
+    // {64 dims, rows, 2 halves, Hkv} so one box carries both swizzled halves
+    // of box_rows rows; 0 for 3-D maps with one box per 64-dim half.
+    int box4d;
+    int box_rows_log2;   // log2 of the rows in one box: 6 (64) or log2(page size)
 };
 
 struct MergeParams {
@@ -185,8 +190,9 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     const uint64_t policy = l2_policy_evict_first();
     const int NS = p.num_stages;
     const bool starve = (p.flags & 1u) && blockIdx.x == 0;
-    // Boxes per (tile or page): K and V, each whole or as two swizzled halves.
-    constexpr int kBoxes = SW128 ? 4 : 2;
+    // Boxes per (tile or page): K and V, each whole (plain or 4-D swizzled)
+    // or as two swizzled 64-dim halves.
+    const int kBoxes = (SW128 && !p.box4d) ? 4 : 2;
 
     int t = t_begin;
     int b = request_of_tile(prefix, p.batch, t);
@@ -195,31 +201,35 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     int j = (t - prefix[b]) - h * nb;
     int L = load_len(p, b, false);
 
-    // Paged: a window of 32 block-table entries (one per lane) and the next
-    // window, loaded ahead so table reads stay off the issue path.
-    int win_b = -1, win_base = 0, nxt_base = 0;
-    int win_ent = 0, nxt_ent = 0;
+    // Paged: block-table entries in a ring of four 32-entry windows (one
+    // entry per lane per window).  The current window is e0; e1..e3 are the
+    // next three, loaded ahead so table reads stay far off the issue path.
+    int win_b = -1, win_base = 0;
+    int e0 = 0, e1 = 0, e2 = 0, e3 = 0;
     auto table_load = [&](int bb, int idx) -> int {
         return idx < p.max_blocks ? __ldg(p.block_table + (size_t)bb * p.max_blocks + idx) : 0;
     };
-    // Warp-collective: make the window hold page index pg (a 32-aligned window).
+    // Warp-collective: make the current window hold page index pg.
     auto ensure_window = [&](int pg) {
-        if (b != win_b || pg < win_base || pg >= win_base + 32) {
-            if (b == win_b && pg >= nxt_base && pg < nxt_base + 32) {
-                win_base = nxt_base;
-                win_ent = nxt_ent;
-            } else {
-                win_b = b;
-                win_base = pg & ~31;
-                win_ent = table_load(b, win_base + lane);
-            }
-            nxt_base = win_base + 32;
-            nxt_ent = table_load(b, nxt_base + lane);
+        if (b != win_b || pg < win_base || pg >= win_base + 128) {
+            win_b = b;
+            win_base = pg & ~31;
+            e0 = table_load(b, win_base + lane);
+            e1 = table_load(b, win_base + 32 + lane);
+            e2 = table_load(b, win_base + 64 + lane);
+            e3 = table_load(b, win_base + 96 + lane);
+        }
+        while (pg >= win_base + 32) {   // advance one window, prefetch the fourth ahead
+            e0 = e1;
+            e1 = e2;
+            e2 = e3;
+            win_base += 32;
+            e3 = table_load(b, win_base + 96 + lane);
         }
     };
     // Warp-collective: entry of page pg_lane (each lane its own, inside the window).
     auto window_entry = [&](int pg_lane) -> int {
-        int e = __shfl_sync(0xffffffffu, win_ent, (pg_lane - win_base) & 31);
+        int e = __shfl_sync(0xffffffffu, e0, (pg_lane - win_base) & 31);
         if (e < 0 || e >= p.num_pages) {
             atomicOr(p.ws_err, kErrPage);
             e = 0;
@@ -229,7 +239,10 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     // Box `box` (0..kBoxes-1) of the tile's K/V, `koff` bytes into each half
     // (swizzled layout) or `2 koff` bytes into each tile (plain layout).
     auto load_box = [&](int box, uint32_t kdst, uint32_t vdst, uint32_t full, uint32_t koff, int row) {
-        if constexpr (SW128) {
+        if (SW128 && p.box4d) {   // box 0: K, box 1: V; both halves in one box
+            tma_load_4d(((box & 1) ? vdst : kdst) + 2 * koff, (box & 1) ? tmv : tmk, full, 0, row, 0, h,
+                        policy);
+        } else if constexpr (SW128) {
             const uint32_t dst = ((box & 2) ? vdst : kdst) + (box & 1) * kHalfBytes + koff;
             tma_load_3d(dst, (box & 2) ? tmv : tmk, full, (box & 1) * (kHeadDim / 2), h, row, policy);
         } else {
@@ -295,7 +308,6 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
                 const int k = k0 + lane;
                 const int phys = window_entry(pg0 + (k < need ? k : k0));
                 if (k < need) {
-#pragma unroll
                     for (int box = 0; box < kBoxes; ++box)
                         load_box(box, kdst, vdst, full, k * P * (kRowBytes / 2), phys * P);
                 }
@@ -593,10 +605,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 // scores (so each holds the softmax state), and for P.V warp 2i covers dims
 // 0..63 and warp 2i+1 dims 64..127.
 
-// Byte address of 16-byte chunk `chunk` (0..15) of `row` in a swizzled tile.
-__device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk)
+// Byte address of 16-byte chunk `chunk` (0..15) of `row` in a swizzled tile
+// made of boxes of 2^rl rows, each box laid out [64-dim half][row][128 B].
+// With rl = 6 (one 64-row box per half) this is two 8 KB halves.
+__device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk, int rl)
 {
-    return tile + (chunk >> 3) * kHalfBytes + row * (kRowBytes / 2) + (((chunk & 7) ^ (row & 7)) << 4);
+    const int rb = row >> rl, rr = row & ((1 << rl) - 1);
+    return tile + ((rb << (rl + 1)) + ((chunk >> 3) << rl) + rr) * (kRowBytes / 2) +
+           (((chunk & 7) ^ (row & 7)) << 4);
 }
 
 template <int G>
@@ -611,6 +627,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
     const int pair = cw >> 1, dhalf = cw & 1;
     const int grp = lane >> 2, qd = lane & 3;   // mma fragment coordinates
     const int tok0 = pair * 16;
+    const int rl = p.box_rows_log2;
     float *red_acc = reinterpret_cast<float *>(smem + p.off_red);   // [pairs][G][D]
     float *red_m = red_acc + kConsumerWarps * G * kHeadDim;          // [pairs][G]
     float *red_l = red_m + kConsumerWarps * G;                       // [pairs][G]
@@ -675,7 +692,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(sw128_addr(ktile, row, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+                ldmatrix_x4(sw128_addr(ktile, row, 2 * ks + (lane >> 4), rl), a0, a1, a2, a3);
                 mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
         }
@@ -717,9 +734,9 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         const bool ragged = nvalid < tok0 + 16;
         if (ragged) {
             const int first = nvalid > tok0 ? nvalid : tok0;
-            const uint32_t base = vtile + dhalf * kHalfBytes;
             for (int idx = lane; idx < (tok0 + 16 - first) * 8; idx += 32) {
-                const uint32_t a = base + (first + (idx >> 3)) * (kRowBytes / 2) + ((idx & 7) << 4);
+                // whole 128-byte half-row: the chunk order inside it does not matter
+                const uint32_t a = sw128_addr(vtile, first + (idx >> 3), dhalf * 8 + (idx & 7), rl);
                 asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
             }
             __syncwarp();
@@ -736,7 +753,8 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                 acc[i][3] *= alpha[1];
                 const int dt = dhalf * 4 + i;   // 16-dim tile index
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(sw128_addr(vtile, vrow, 2 * dt + ((lane >> 3) & 1)), a0, a1, a2, a3);
+                ldmatrix_x4_trans(sw128_addr(vtile, vrow, 2 * dt + ((lane >> 3) & 1), rl), a0, a1, a2,
+                                  a3);
                 mma_bf16_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
             }
         }

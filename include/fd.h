@@ -95,6 +95,11 @@ typedef struct fd_options {
  * arithmetic instead. */
 #define FD_FLAG_CUDA_CORES 0x2u
 
+/* Tensor-core consumers: load each 64-dim half of a K/V tile as its own TMA
+ * box (3-D tensor maps) instead of one box carrying both halves (4-D maps).
+ * Results are identical; for comparisons only. */
+#define FD_FLAG_NO_4D_BOXES 0x4u
+
 /*
  * Bytes of workspace that fd_decode / fd_decode_paged need for this shape.
  * Pure host function (no CUDA call).  The size does not depend on the

@@ -188,3 +188,19 @@ def test_bad_block_table_entry_is_reported():
     torch.cuda.synchronize()
     assert np.all(np.isfinite(o.cpu().numpy()))
     assert fd.fd_get_device_error(ws) == fd.FD_ERR_DEVICE_INPUT
+
+
+NO_4D = 0x4   # FD_FLAG_NO_4D_BOXES: one TMA box per 64-dim half (3-D tensor maps)
+
+
+@pytest.mark.parametrize("page", [0, 8, 16, 32, 64, 128])
+def test_tensor_core_box_layouts_agree(page):
+    """4-D boxes (both halves per box) and 3-D half boxes give bitwise equal results."""
+    w = syn.make_contiguous(450 + page, len(RAGGED), 16, 2, 128, 1024, RAGGED)
+    if page:
+        w = contig_to_paged(w, page, perm_seed=page, poison=True)
+    a = run(w, num_ctas=11)
+    b = run(w, num_ctas=11, flags=NO_4D)
+    ro, rl = oracle.attend(w, threads=8)
+    check(a[0], a[1], ro, rl, f"4-D boxes P={page}")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
