@@ -230,6 +230,9 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     sp.cap = cap;
     sp.s_max = s_max;
     sp.page_size = page_size;
+    sp.page_log2 = 0;
+    while (page_size > 0 && page_size < kTileTokens && (1 << sp.page_log2) < page_size)
+        ++sp.page_log2;
     sp.max_blocks = max_blocks;
     sp.num_pages = num_pages;
     sp.scale_log2 = scale * 1.4426950408889634f;

@@ -77,6 +77,7 @@ struct SplitParams {
     // of box_rows rows; 0 for 3-D maps with one box per 64-dim half.
     int box4d;
     int box_rows_log2;   // log2 of the rows in one box: 6 (64) or log2(page size)
+    int page_log2;       // paged, page size under 64: log2 of the page size
 };
 
 struct MergeParams {
@@ -192,7 +193,9 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     const bool starve = (p.flags & 1u) && blockIdx.x == 0;
     // Boxes per (tile or page): K and V, each whole (plain or 4-D swizzled)
     // or as two swizzled 64-dim halves.
-    const int kBoxes = (SW128 && !p.box4d) ? 4 : 2;
+    const int box_log2 = (SW128 && !p.box4d) ? 2 : 1;
+    const int kBoxes = 1 << box_log2;
+    const int page_log2 = p.page_log2;   // pages under 64 tokens are powers of two
 
     int t = t_begin;
     int b = request_of_tile(prefix, p.batch, t);
@@ -278,18 +281,17 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
         const uint32_t vdst = kdst + kTileBytes;
         const uint32_t extra = (starve && issued == 0) ? 256u : 0u;
         const int P = p.page_size;
+        const bool small_pages = PAGED && P < kTileTokens;
         // pages of this tile that hold valid tokens (paged, P < 64)
-        const int need = (PAGED && P < kTileTokens) ? min(kTileTokens / P, ceil_div(nvalid, P)) : 1;
+        const int need = small_pages ? min(kTileTokens >> page_log2, (nvalid + P - 1) >> page_log2) : 1;
         if (lane == 0) {
             int *m = meta + s * kMetaInts;
             m[0] = b;
             m[1] = h;
-            m[2] = j;
             m[3] = nvalid;
             m[4] = flags;
             m[5] = b * p.hkv + h;
-            const uint32_t bytes = (PAGED && P < kTileTokens) ? 2u * need * P * kRowBytes
-                                                              : (uint32_t)(2 * kTileBytes);
+            const uint32_t bytes = small_pages ? 2u * need * P * kRowBytes : (uint32_t)(2 * kTileBytes);
             mbar_arrive_expect_tx(full, bytes + extra);
         }
         __syncwarp();
@@ -302,15 +304,16 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             if (lane < kBoxes)
                 load_box(lane, kdst, vdst, full, 0, phys * P + (token0 % P));
         } else {
-            const int pg0 = token0 / P;
-            for (int k0 = 0; k0 < need; k0 += 32) {
-                ensure_window(pg0 + k0);
-                const int k = k0 + lane;
-                const int phys = window_entry(pg0 + (k < need ? k : k0));
-                if (k < need) {
-                    for (int box = 0; box < kBoxes; ++box)
-                        load_box(box, kdst, vdst, full, k * P * (kRowBytes / 2), phys * P);
-                }
+            // One (page, box) pair per lane, so a tile's boxes issue together.
+            const int pg0 = token0 >> page_log2;
+            const int items = need << box_log2;
+            for (int i0 = 0; i0 < items; i0 += 32) {
+                ensure_window(pg0 + (i0 >> box_log2));
+                const int item = i0 + lane;
+                const int k = item >> box_log2;
+                const int phys = window_entry(pg0 + (item < items ? k : (i0 >> box_log2)));
+                if (item < items)
+                    load_box(item & (kBoxes - 1), kdst, vdst, full, (k * P) * (kRowBytes / 2), phys * P);
             }
         }
         __syncwarp();
@@ -838,6 +841,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         misc[0] = 0;
         mbar_init_fence();
     }
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: everything above overlapped its tail; inputs and the workspace
+    // are touched only after it has completed.
+    pdl_wait_prior_grid();
     build_prefix(p, prefix, misc + 1);   // ends with __syncthreads
 
     const int T = prefix[p.batch];
@@ -865,6 +872,7 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__
 {
     __shared__ float s_w[kMaxCtas];
     __shared__ float s_lse;
+    pdl_launch_dependents();   // the next call's split kernel may start its prologue
     pdl_wait_prior_grid();
     const int u = blockIdx.x, g = blockIdx.y;
     const int b = u / p.hkv, h = u - b * p.hkv;

@@ -51,11 +51,18 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
             return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
+    // Programmatic dependent launch: the kernel's prologue may overlap the
+    // previous kernel in the stream; it waits for it before reading inputs.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)c.grid);
     cfg.blockDim = dim3(kSplitThreads);
     cfg.dynamicSmemBytes = c.smem_bytes;
     cfg.stream = c.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, MMA>, p, tmk, tmv);
 }
 

@@ -17,6 +17,8 @@ Recipe (the same on every machine):
   computed in fp64.
 * bf16: one round-to-nearest-even from fp64 straight to bf16 (no detour
   through fp32, which would round twice).
+* fp16: one round-to-nearest-even from fp64 straight to fp16 (NumPy's direct
+  double-to-half conversion, subnormals included).
 * Integers in [lo, hi]: ``lo + z % (hi - lo + 1)``.
 * Permutations: Fisher-Yates driven by the same integer draws.
 
@@ -83,6 +85,28 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return b.view(np.float32).astype(np.float64)
 
 
+def f64_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to fp16 bit patterns, nearest-even, in one step."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    if not np.all(np.isfinite(x)) or np.any(np.abs(x) > 65504.0):
+        raise ValueError("f64_to_f16_bits: non-finite or out-of-range input")
+    return x.astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen fp16 bit patterns exactly to fp64."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def round_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    """fp64 -> 16-bit patterns of `dtype` ('bf16' or 'f16')."""
+    return f64_to_bf16_bits(x) if dtype == "bf16" else f64_to_f16_bits(x)
+
+
+def widen_bits(bits: np.ndarray, dtype: str) -> np.ndarray:
+    return bf16_bits_to_f64(bits) if dtype == "bf16" else f16_bits_to_f64(bits)
+
+
 def _normal_chunk(seed: int, start: int, n: int) -> np.ndarray:
     # element e uses the Box-Muller pair (2*(e//2), 2*(e//2)+1)
     p0 = start // 2
@@ -99,14 +123,14 @@ def _normal_chunk(seed: int, start: int, n: int) -> np.ndarray:
     return out[off:off + n]
 
 
-def normal_bf16(seed: int, shape, workers: int | None = None) -> np.ndarray:
-    """i.i.d. N(0,1) values rounded to bf16, returned as uint16 bit patterns."""
+def normal_bf16(seed: int, shape, workers: int | None = None, dtype: str = "bf16") -> np.ndarray:
+    """i.i.d. N(0,1) values rounded to bf16 (or fp16), returned as uint16 bit patterns."""
     n = int(np.prod(shape)) if len(shape) else 1
     out = np.empty(n, dtype=np.uint16)
 
     def work(start):
         m = min(_CHUNK, n - start)
-        out[start:start + m] = f64_to_bf16_bits(_normal_chunk(seed, start, m))
+        out[start:start + m] = round_bits(_normal_chunk(seed, start, m), dtype)
 
     starts = range(0, n, _CHUNK)
     if n <= _CHUNK:
@@ -155,9 +179,13 @@ def choose(seed: int, n: int, k: int) -> np.ndarray:
 BF16_NAN = np.uint16(0x7FC0)
 
 
-def scale_bf16_bits(bits: np.ndarray, factor: float) -> np.ndarray:
-    """Multiply bf16 values by a power of two (exact in bf16 for normal values)."""
+def scale_bf16_bits(bits: np.ndarray, factor: float, dtype: str = "bf16") -> np.ndarray:
+    """Multiply bf16 (or fp16) values by a power of two (exact unless it overflows)."""
     assert factor > 0 and math.log2(factor).is_integer()
+    if dtype == "f16":
+        f = np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32) * np.float32(factor)
+        assert np.all(np.abs(f) <= 65504.0)
+        return f.astype(np.float16).view(np.uint16)
     f = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32) * np.float32(factor)
     return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
 
@@ -186,6 +214,7 @@ class Workload:
     page_size: int = 0                 # 0 = contiguous
     block_table: np.ndarray | None = None
     meta: dict = field(default_factory=dict)
+    dtype: str = "bf16"                # element type of q, K, V: 'bf16' or 'f16'
 
     @property
     def batch(self) -> int:
@@ -218,12 +247,13 @@ def default_scale(head_dim: int) -> float:
 
 
 def make_contiguous(config_id: int, batch: int, hq: int, hkv: int, d: int, s_max: int,
-                    lens, name: str = "") -> Workload:
-    q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d))
-    k = normal_bf16(seed_for(config_id, TENSOR_K), (batch, s_max, hkv, d))
-    v = normal_bf16(seed_for(config_id, TENSOR_V), (batch, s_max, hkv, d))
+                    lens, name: str = "", dtype: str = "bf16") -> Workload:
+    q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d), dtype=dtype)
+    k = normal_bf16(seed_for(config_id, TENSOR_K), (batch, s_max, hkv, d), dtype=dtype)
+    v = normal_bf16(seed_for(config_id, TENSOR_V), (batch, s_max, hkv, d), dtype=dtype)
     lens = np.asarray(lens, dtype=np.int32).reshape(batch)
-    return Workload(name or f"contig{config_id}", q, k, v, lens, hq, hkv, d, default_scale(d))
+    return Workload(name or f"contig{config_id}", q, k, v, lens, hq, hkv, d, default_scale(d),
+                    dtype=dtype)
 
 
 def build_block_table(lens, page: int, max_blocks: int, perm: np.ndarray) -> np.ndarray:
@@ -238,17 +268,18 @@ def build_block_table(lens, page: int, max_blocks: int, perm: np.ndarray) -> np.
 
 
 def make_paged(config_id: int, batch: int, hq: int, hkv: int, d: int, page: int,
-               lens, max_blocks: int, name: str = "", extra_pages: int = 0) -> Workload:
+               lens, max_blocks: int, name: str = "", extra_pages: int = 0,
+               dtype: str = "bf16") -> Workload:
     lens = np.asarray(lens, dtype=np.int32).reshape(batch)
     used = int(sum((int(L) + page - 1) // page for L in lens))
     num_pages = max(1, used + extra_pages)
     perm = permutation(seed_for(config_id, TENSOR_PERM), num_pages)
     table = build_block_table(lens, page, max_blocks, perm)
-    q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d))
-    k = normal_bf16(seed_for(config_id, TENSOR_K), (num_pages, page, hkv, d))
-    v = normal_bf16(seed_for(config_id, TENSOR_V), (num_pages, page, hkv, d))
+    q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d), dtype=dtype)
+    k = normal_bf16(seed_for(config_id, TENSOR_K), (num_pages, page, hkv, d), dtype=dtype)
+    v = normal_bf16(seed_for(config_id, TENSOR_V), (num_pages, page, hkv, d), dtype=dtype)
     return Workload(name or f"paged{config_id}", q, k, v, lens, hq, hkv, d, default_scale(d),
-                    page_size=page, block_table=table)
+                    page_size=page, block_table=table, dtype=dtype)
 
 
 def scale_keys(w: Workload, tokens: np.ndarray, factor: float) -> None:
@@ -261,15 +292,15 @@ def scale_keys(w: Workload, tokens: np.ndarray, factor: float) -> None:
                 continue
             if w.paged:
                 pg = int(w.block_table[b, t // w.page_size])
-                w.k[pg, t % w.page_size] = scale_bf16_bits(w.k[pg, t % w.page_size], factor)
+                w.k[pg, t % w.page_size] = scale_bf16_bits(w.k[pg, t % w.page_size], factor, w.dtype)
             else:
-                w.k[b, t] = scale_bf16_bits(w.k[b, t], factor)
+                w.k[b, t] = scale_bf16_bits(w.k[b, t], factor, w.dtype)
 
 
 def _scale_keys_paged_fast(w: Workload, b: int, tokens: np.ndarray, factor: float) -> None:
     pg = w.block_table[b, tokens // w.page_size].astype(np.int64)
     sl = tokens % w.page_size
-    w.k[pg, sl] = scale_bf16_bits(w.k[pg, sl], factor)
+    w.k[pg, sl] = scale_bf16_bits(w.k[pg, sl], factor, w.dtype)
 
 
 # The five benchmark workloads (sizes from the task's configuration list).

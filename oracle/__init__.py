@@ -54,7 +54,7 @@ def _load():
         if _lib is None:
             build()
             lib = ctypes.CDLL(_LIB)
-            lib.oracle_attend.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _D,
+            lib.oracle_attend.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _D, _I,
                                           _P, _I, _P, _P, _P]
             lib.oracle_attend.restype = _I
             lib.oracle_lse_merge.argtypes = [_P, _P, _I, _I, _P, _P]
@@ -70,10 +70,10 @@ def _ptr(a):
 
 
 def attend_raw(q, k, v, seq_lens, num_q_heads, num_kv_heads, scale, *,
-               page_size=0, block_table=None, items=None, threads=1):
+               page_size=0, block_table=None, items=None, threads=1, dtype="bf16"):
     """Oracle attention on raw arrays.
 
-    q: uint16 bf16 bits [B, Hq, D]; k, v: uint16 [B, S_max, Hkv, D] (contiguous)
+    q: uint16 bf16 (or fp16, dtype='f16') bits [B, Hq, D]; k, v: uint16 [B, S_max, Hkv, D] (contiguous)
     or [num_pages, P, Hkv, D] (paged, with block_table int32 [B, max_blocks]).
     items: int32 [n, 4] rows (b, h, t0, t1), t1 < 0 meaning "to L_b"; default
     is every (b, h) over its whole length.  Returns (o [n, D], lse [n]) in
@@ -107,7 +107,8 @@ def attend_raw(q, k, v, seq_lens, num_q_heads, num_kv_heads, scale, *,
         scratch = np.empty(maxlen, dtype=np.float64)
         rc = lib.oracle_attend(_ptr(q), _ptr(k), _ptr(v), _ptr(lens), B, hq, num_kv_heads, d,
                                s_max, page_size, _ptr(table), max_blocks, num_pages,
-                               float(scale), _ptr(items[lo:hi]), hi - lo, _ptr(scratch),
+                               float(scale), 1 if dtype == "f16" else 0, _ptr(items[lo:hi]), hi - lo,
+                               _ptr(scratch),
                                _ptr(o[lo:hi]), _ptr(lse[lo:hi]))
         if rc != 0:
             raise ValueError("oracle_attend: invalid arguments (bad page, head or length)")
@@ -128,7 +129,7 @@ def attend(w, items=None, threads=1):
     """Oracle attention for a workload object (see ``fd_synth.Workload``)."""
     return attend_raw(w.q, w.k, w.v, w.seq_lens, w.num_q_heads, w.num_kv_heads, w.scale,
                       page_size=w.page_size, block_table=w.block_table, items=items,
-                      threads=threads)
+                      threads=threads, dtype=getattr(w, "dtype", "bf16"))
 
 
 def lse_merge(o_parts, lse_parts):

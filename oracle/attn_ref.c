@@ -32,6 +32,9 @@
  *                          by block, O divided by l at the end), for one
  *                          query row with a vector value of width dv.
  *
+ * Inputs are bf16 or IEEE fp16 bit patterns (the first page's tensor-map
+ * helper accepts either), widened exactly to fp64.
+ *
  * GQA head mapping: query head h reads kv head h / (Hq / Hkv) (consecutive
  * query heads share a kv head).  Paged layout: token t of request b lives
  * in physical page block_table[b][t / P], slot t % P.
@@ -46,6 +49,26 @@ static double bf16_to_f64(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+static double f16_to_f64(uint16_t bits)
+{
+    const int sign = bits >> 15, e = (bits >> 10) & 31, m = bits & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);              /* zero or subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m + 1024), e - 25);  /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* Element type of q, K and V: 0 = bf16, 1 = fp16. */
+static double elem_to_f64(uint16_t bits, int dtype)
+{
+    return dtype ? f16_to_f64(bits) : bf16_to_f64(bits);
 }
 
 /* Where the K (or V) row of logical token t of request b, kv head g lives. */
@@ -84,7 +107,7 @@ static const uint16_t *kv_row(const kv_view *w, int b, int t, int g)
  * Returns 0, or -1 when a referenced page is out of range.
  */
 static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
-                      int b, int h, int hq, int t0, int t1, double scale,
+                      int b, int h, int hq, int t0, int t1, double scale, int dtype,
                       double *s /* scratch, >= t1 - t0 */, double *o, double *lse)
 {
     const int d = kw->d;
@@ -108,7 +131,7 @@ static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
             return -1;
         double dot = 0.0;
         for (int j = 0; j < d; ++j)
-            dot += bf16_to_f64(qrow[j]) * bf16_to_f64(krow[j]);
+            dot += elem_to_f64(qrow[j], dtype) * elem_to_f64(krow[j], dtype);
         s[i] = scale * dot;
         if (s[i] > mx)
             mx = s[i];
@@ -129,12 +152,13 @@ static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
             return -1;
         const double p = s[i] / z;
         for (int j = 0; j < d; ++j)
-            o[j] += p * bf16_to_f64(vrow[j]);
+            o[j] += p * elem_to_f64(vrow[j], dtype);
     }
     return 0;
 }
 
 /*
+ * dtype: 0 when q, K and V hold bf16 bit patterns, 1 for IEEE fp16.
  * For each of npairs items (b, h, t0, t1) in `items` (int32, 4 per item;
  * t1 < 0 means "to the request's length"), compute the attention of query
  * (b, h) over tokens [t0, min(t1, L_b)).  o is [npairs][d], lse [npairs].
@@ -146,7 +170,7 @@ static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
 int oracle_attend(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   const int32_t *seq_lens, int batch, int hq, int hkv, int d,
                   int s_max, int page_size, const int32_t *block_table,
-                  int max_blocks, int num_pages, double scale,
+                  int max_blocks, int num_pages, double scale, int dtype,
                   const int32_t *items, int npairs, double *scratch,
                   double *o, double *lse)
 {
@@ -171,7 +195,7 @@ int oracle_attend(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             t1 = L;
         if (t0 < 0)
             t0 = 0;
-        if (attend_one(q, &kw, &vw, b, h, hq, t0, t1, scale, scratch,
+        if (attend_one(q, &kw, &vw, b, h, hq, t0, t1, scale, dtype, scratch,
                        o + (int64_t)i * d, lse + i) != 0)
             return -1;
     }

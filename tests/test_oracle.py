@@ -321,3 +321,47 @@ def test_softmax_stress_scaled_keys(factor):
         ro, rl = mp_attention(wide(w.q[0, h]), wide(w.k[0, :, 0]), wide(w.v[0, :, 0]), w.scale)
         np.testing.assert_allclose(o[0, h], ro, rtol=1e-12, atol=1e-14)
         assert lse[0, h] == pytest.approx(rl, rel=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# fp16 inputs (the first page's tensor-map helper takes fp16 as well as bf16)
+# ---------------------------------------------------------------------------
+
+def f16(x):
+    return syn.f64_to_f16_bits(np.asarray(x, dtype=np.float64))
+
+
+def test_f16_single_token_gives_v0_exactly_including_subnormals():
+    d = 128
+    q = f16(np.linspace(-1, 1, d).reshape(1, 1, d))
+    k = f16(np.linspace(2, -2, d).reshape(1, 1, 1, d))
+    vals = np.concatenate([[2 ** -24, 3 * 2 ** -24, -(2 ** -20), 6.1e-5, 65504.0, -2.5],
+                           np.linspace(-3, 3, d - 6)])
+    v = f16(vals.reshape(1, 1, 1, d))
+    w = syn.Workload("f16", q, k, v, np.array([1], np.int32), 1, 1, d, 0.25, dtype="f16")
+    o, lse = oracle.attend(w)
+    # reference widening by numpy's float16 (independent of the C oracle)
+    assert np.array_equal(o[0, 0], v.view(np.float16).astype(np.float64)[0, 0, 0])
+    s = 0.25 * math.fsum(q.view(np.float16).astype(np.float64)[0, 0] * k.view(np.float16).astype(np.float64)[0, 0, 0])
+    assert lse[0, 0] == pytest.approx(s, rel=1e-14, abs=1e-15)
+
+
+@pytest.mark.parametrize("L", [17, 65])
+def test_f16_brute_force(L):
+    w = syn.make_contiguous(120 + L, 1, 2, 1, 128, L, [L], dtype="f16")
+    o, lse = oracle.attend(w)
+    wd = lambda a: syn.f16_bits_to_f64(a)
+    for h in range(2):
+        ro, rl = mp_attention(wd(w.q[0, h]), wd(w.k[0, :L, 0]), wd(w.v[0, :L, 0]), w.scale)
+        np.testing.assert_allclose(o[0, h], ro, rtol=1e-12, atol=1e-14)
+        assert lse[0, h] == pytest.approx(rl, rel=1e-13, abs=1e-13)
+
+
+def test_f16_paged_equals_contiguous():
+    lens = [1, 40, 0, 129]
+    w = syn.make_contiguous(131, len(lens), 4, 2, 128, 200, lens, dtype="f16")
+    o, lse = oracle.attend(w)
+    wp = to_paged(w, 16, perm_seed=4)
+    wp.dtype = "f16"
+    op, lp = oracle.attend(wp)
+    assert np.array_equal(o, op) and np.array_equal(lse, lp)

@@ -29,6 +29,8 @@ MUTANTS = {
     "query row indexed by kv head": ("const uint16_t *qrow = q + ((int64_t)b * hq + h) * d;",
                                      "const uint16_t *qrow = q + ((int64_t)b * hq + g) * d;"),
     "last token dropped": ("const int n = t1 - t0;", "const int n = t1 - t0 - (t1 - t0 > 1);"),
+    "fp16 exponent bias off by one": ("v = ldexp((double)(m + 1024), e - 25);", "v = ldexp((double)(m + 1024), e - 24);"),
+    "fp16 subnormals flushed": ("v = ldexp((double)m, -24);", "v = 0.0;"),
 }
 
 

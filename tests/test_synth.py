@@ -102,3 +102,39 @@ def test_block_table_assigns_each_page_once():
 
 def test_default_scale_is_fp32_inverse_sqrt():
     assert syn.default_scale(128) == float(np.float32(1) / np.sqrt(np.float32(128)))
+
+
+def f16_round_exact(x: float) -> float:
+    """Nearest IEEE fp16 (11 significant bits, subnormal quantum 2^-24), ties to even."""
+    if x == 0:
+        return 0.0
+    f = abs(Fraction(x))
+    sign = -1 if x < 0 else 1
+    e = 0
+    while f >= 2:
+        f /= 2; e += 1
+    while f < 1:
+        f *= 2; e -= 1
+    if e < -14:
+        q = abs(Fraction(x)) / Fraction(2) ** -24
+        lo = int(q); rem = q - lo
+        if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2):
+            lo += 1
+        return sign * float(lo * Fraction(2) ** -24)
+    scaled = f * 1024
+    lo = int(scaled); rem = scaled - lo
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2):
+        lo += 1
+    return sign * float(Fraction(lo, 1024) * Fraction(2) ** e)
+
+
+def test_f16_rounding_is_nearest_even_from_fp64():
+    rng = np.random.default_rng(2)
+    xs = np.concatenate([rng.standard_normal(3000) * 10.0 ** rng.integers(-8, 4, 3000),
+                         [1 + 2 ** -11, 1 + 3 * 2 ** -11, 1 + 2 ** -11 + 2 ** -40, 2 ** -25, 3 * 2 ** -26,
+                          1.5 * 2 ** -24, 65504.0, 0.0]])
+    got = syn.f16_bits_to_f64(syn.f64_to_f16_bits(xs))
+    ref = np.array([f16_round_exact(float(x)) for x in xs])
+    assert np.array_equal(got, ref)
+    with pytest.raises(ValueError):
+        syn.f64_to_f16_bits(np.array([70000.0]))
