@@ -4,7 +4,8 @@
 Default workload: MHA long-KV decode -- batch 1, 32 query heads = 32 kv heads,
 head_dim 128, kv_len 65536, contiguous [S, H, D] bf16 K/V, scale 1/sqrt(128)
 (1 GiB of K+V, larger than the 129 MB L2, so no flush is needed between
-steps).  A step is one fd_decode call: the split kernel plus the LSE merge.
+steps).  A step is one fd_decode call: one kernel, whose CTAs also merge the
+split partials by LSE.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
 
@@ -394,7 +395,7 @@ def run_ours(args, rank, world):
                          "consumers": ("cuda cores" if (args.cuda_cores or w.num_q_heads == w.num_kv_heads)
                                        else "tensor cores (mma.sync bf16)"),
                          "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"},
-            "gpu_launches": 2 * K,
+            "gpu_launches": K,            # one split kernel per call (the merge is fused)
             "clocks": clk.summary(t_wall0, t_wall1),
             "e2e": e2e,
             "cpu_baseline": cpu,

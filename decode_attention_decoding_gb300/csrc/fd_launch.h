@@ -29,7 +29,6 @@ cudaError_t launch_split_contig_mma(int group, const SplitParams &p, const CUten
                                     const CUtensorMap &tmv, const SplitLaunch &cfg);
 cudaError_t launch_split_paged_mma(int group, const SplitParams &p, const CUtensorMap &tmk,
                                    const CUtensorMap &tmv, const SplitLaunch &cfg);
-cudaError_t launch_merge(int group, const MergeParams &p, int grid, cudaStream_t stream);
 
 // Shared by the two split translation units.
 template <int G, bool PAGED, bool MMA>

@@ -204,3 +204,20 @@ def test_tensor_core_box_layouts_agree(page):
     ro, rl = oracle.attend(w, threads=8)
     check(a[0], a[1], ro, rl, f"4-D boxes P={page}")
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_one_workspace_across_many_calls_and_split_patterns():
+    """The merge tickets reset themselves: one workspace serves calls with
+    different lengths, groups of CTAs and layouts back to back."""
+    import decode_attention_decoding_gb300 as fd
+    ws = fd.make_workspace(8, 16, 4, 128, 2048, 16)
+    cases = [([2048, 5, 700, 0, 64, 65, 1999, 1], 7), ([100, 2000, 33, 1024, 0, 0, 9, 2048], 152),
+             ([2048] * 8, 3), ([1, 2, 3, 4, 5, 6, 7, 8], 40), ([1500, 0, 0, 0, 0, 0, 0, 2047], 1)]
+    for i, (lens, ctas) in enumerate(cases * 2):
+        w = syn.make_contiguous(470 + i, 8, 16, 4, 128, 2048, lens)
+        if i % 2:
+            w = contig_to_paged(w, 16, perm_seed=i)
+        o, l = run(w, workspace=ws, num_ctas=ctas)
+        ro, rl = oracle.attend(w, threads=8)
+        check(o, l, ro, rl, f"call {i}")
+    assert fd.fd_get_device_error(ws) == fd.FD_OK

@@ -27,7 +27,8 @@ def test_starved_wait_times_out_and_context_survives(paged):
     else:
         fd.fd_decode(d["q"], d["k"], d["v"], d["seq_lens"], **kw)
     assert fd.fd_get_device_error(ws) == fd.FD_ERR_TIMEOUT
-    # the same workspace and context still give correct results afterwards
+    # after re-initialising the workspace, the same context gives correct results
+    fd.fd_workspace_init(ws)
     o, l = run(w, d, workspace=ws)
     ro, rl = oracle.attend(w)
     check(o, l, ro, rl, "after timeout")
