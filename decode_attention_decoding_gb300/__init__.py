@@ -40,7 +40,8 @@ _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 class FdOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("flags", ctypes.c_uint),
                 ("wait_timeout_ns", ctypes.c_ulonglong),
-                ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p)]
+                ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p),
+                ("dtype", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -133,8 +134,8 @@ def make_workspace(batch, num_q_heads, num_kv_heads, head_dim=128, max_kv_len=0,
 
 
 def _bits(t, name):
-    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-        raise TypeError(f"{name} must be bf16 (or its 16-bit pattern), got {t.dtype}")
+    if t.dtype not in (torch.bfloat16, torch.float16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must be bf16 or fp16 (or its 16-bit pattern), got {t.dtype}")
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
     return t
@@ -148,7 +149,16 @@ def _i32(t, name):
     return t
 
 
-def _options(num_ctas, flags, wait_timeout_ns, split_events):
+FD_DTYPE_BF16, FD_DTYPE_F16 = 0, 1
+
+
+def _dtype_code(t, dtype):
+    if dtype is not None:
+        return {"bf16": FD_DTYPE_BF16, "f16": FD_DTYPE_F16}[dtype]
+    return FD_DTYPE_F16 if t.dtype == torch.float16 else FD_DTYPE_BF16
+
+
+def _options(num_ctas, flags, wait_timeout_ns, split_events, dtype_code=FD_DTYPE_BF16):
     ev0 = ev1 = None
     if split_events is not None:
         for e in split_events:
@@ -156,7 +166,7 @@ def _options(num_ctas, flags, wait_timeout_ns, split_events):
                 raise ValueError("split_events must be created (recorded once) before use")
         ev0 = ctypes.c_void_p(split_events[0].cuda_event)
         ev1 = ctypes.c_void_p(split_events[1].cuda_event)
-    return FdOptions(int(num_ctas), int(flags), int(wait_timeout_ns), ev0, ev1)
+    return FdOptions(int(num_ctas), int(flags), int(wait_timeout_ns), ev0, ev1, int(dtype_code))
 
 
 def _outputs(q, out, lse):
@@ -175,10 +185,11 @@ def _outputs(q, out, lse):
 
 def fd_decode(q, k, v, seq_lens=None, seq_lens_host=None, scale=None, out=None, lse=None,
               workspace=None, num_ctas=0, flags=0, wait_timeout_ns=0, split_events=None,
-              stream=None, check=True):
+              stream=None, check=True, dtype=None):
     """Decode attention over a contiguous KV cache (see fd_decode in include/fd.h).
 
-    q [B, Hq, D], k/v [B, S_max, Hkv, D] bf16 CUDA tensors; seq_lens int32 [B]
+    q [B, Hq, D], k/v [B, S_max, Hkv, D] bf16 or fp16 CUDA tensors (``dtype``
+    'bf16'/'f16' overrides the tensors' own type, e.g. for int16 views); seq_lens int32 [B]
     on the device (None = every request has S_max tokens); seq_lens_host an
     optional CPU int32 copy used only for host-side validation.  Pass
     ``lse=False`` to skip the LSE output.  Returns (out, lse).
@@ -191,7 +202,7 @@ def fd_decode(q, k, v, seq_lens=None, seq_lens_host=None, scale=None, out=None, 
     out, lse = _outputs(q, out, lse)
     if workspace is None:
         workspace = make_workspace(B, hq, hkv, d, s_max, 0, q.device)
-    opts = _options(num_ctas, flags, wait_timeout_ns, split_events)
+    opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype))
     lh = None
     if seq_lens_host is not None:
         lh = seq_lens_host.to(torch.int32).contiguous().cpu()
@@ -206,7 +217,7 @@ def fd_decode(q, k, v, seq_lens=None, seq_lens_host=None, scale=None, out=None, 
 
 def fd_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=None, scale=None,
                     out=None, lse=None, workspace=None, num_ctas=0, flags=0, wait_timeout_ns=0,
-                    split_events=None, stream=None, check=True):
+                    split_events=None, stream=None, check=True, dtype=None):
     """Decode attention over a paged KV cache (see fd_decode_paged in include/fd.h).
 
     k_pages/v_pages [num_pages, P, Hkv, D] bf16; block_table int32 [B, max_blocks];
@@ -222,7 +233,7 @@ def fd_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=No
     out, lse = _outputs(q, out, lse)
     if workspace is None:
         workspace = make_workspace(B, hq, hkv, d, max_blocks * page, page, q.device)
-    opts = _options(num_ctas, flags, wait_timeout_ns, split_events)
+    opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype))
     lh = None
     if seq_lens_host is not None:
         lh = seq_lens_host.to(torch.int32).contiguous().cpu()

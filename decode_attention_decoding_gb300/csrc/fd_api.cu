@@ -21,7 +21,7 @@ namespace {
 
 using namespace fd;
 
-constexpr int kVersion = 10000;   // 1.0.0
+constexpr int kVersion = 10100;   // 1.1.0
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
 struct DeviceInfo {
@@ -77,7 +77,7 @@ EncodeTiledFn encode_fn()
 // of one kv head: the whole 128-dim row, or (swizzled) 64 dims of it with the
 // 128-byte swizzle that the tensor-core consumers read.
 fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
-                        bool swizzled)
+                        bool swizzled, bool f16)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -87,7 +87,8 @@ fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long r
     const cuuint32_t box[3] = {(cuuint32_t)(swizzled ? kHeadDim / 2 : kHeadDim), 1u,
                                (cuuint32_t)box_rows};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+    const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -97,7 +98,8 @@ fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long r
 // A rank-4 view {64 dims, rows, 2 halves, Hkv} of the same tensor, so that
 // one box {64, box_rows, 2, 1} carries both 128-byte-swizzled 64-dim halves
 // of box_rows rows of one kv head (laid out half by half in shared memory).
-fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows)
+fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
+                           bool f16)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -107,7 +109,8 @@ fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long lon
                                    (cuuint64_t)kRowBytes};
     const cuuint32_t box[4] = {(cuuint32_t)(kHeadDim / 2), (cuuint32_t)box_rows, 2u, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+    const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                          const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
@@ -117,22 +120,23 @@ fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long lon
 // box per tile or page carries both swizzled halves) and fall back to 3-D
 // maps with one box per half if the driver rejects the 4-D view.
 fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, const void *v, int hkv,
-                         long long rows, int box_rows, bool mma, SplitParams *sp)
+                         long long rows, int box_rows, bool mma, bool f16, SplitParams *sp)
 {
     int rl = 0;
     while ((1 << rl) < box_rows)
         ++rl;
     sp->box4d = 0;
     sp->box_rows_log2 = 6;
-    if (mma && !(sp->flags & FD_FLAG_NO_4D_BOXES) && encode_kv_map_4d(tmk, k, hkv, rows, box_rows) == FD_OK &&
-        encode_kv_map_4d(tmv, v, hkv, rows, box_rows) == FD_OK) {
+    if (mma && !(sp->flags & FD_FLAG_NO_4D_BOXES) &&
+        encode_kv_map_4d(tmk, k, hkv, rows, box_rows, f16) == FD_OK &&
+        encode_kv_map_4d(tmv, v, hkv, rows, box_rows, f16) == FD_OK) {
         sp->box4d = 1;
         sp->box_rows_log2 = rl;
         return FD_OK;
     }
     fd_status st;
-    if ((st = encode_kv_map(tmk, k, hkv, rows, box_rows, mma)) != FD_OK ||
-        (st = encode_kv_map(tmv, v, hkv, rows, box_rows, mma)) != FD_OK)
+    if ((st = encode_kv_map(tmk, k, hkv, rows, box_rows, mma, f16)) != FD_OK ||
+        (st = encode_kv_map(tmv, v, hkv, rows, box_rows, mma, f16)) != FD_OK)
         return st;
     return FD_OK;
 }
@@ -161,6 +165,7 @@ struct CallPlan {
     SplitLaunch launch;
     int group;
     bool mma;   // tensor-core consumers (GQA groups) instead of CUDA cores
+    bool f16;   // IEEE fp16 inputs instead of bf16
 };
 
 // Tensor-core consumers serve GQA groups; paged pools need pages of at least
@@ -247,6 +252,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
 
     cp->group = group;
     cp->mma = use_mma(group, page_size, opts);
+    cp->f16 = opts && opts->dtype == FD_DTYPE_F16;
     return FD_OK;
 }
 
@@ -259,12 +265,12 @@ fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUte
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess)
         return FD_ERR_CUDA;
     cudaError_t e;
-    if (cp.mma)
-        e = paged ? launch_split_paged_mma(cp.group, cp.sp, tmk, tmv, cp.launch)
-                  : launch_split_contig_mma(cp.group, cp.sp, tmk, tmv, cp.launch);
+    if (paged)
+        e = cp.f16 ? launch_split_paged_f16(cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch)
+                   : launch_split_paged_bf16(cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch);
     else
-        e = paged ? launch_split_paged(cp.group, cp.sp, tmk, tmv, cp.launch)
-                  : launch_split_contig(cp.group, cp.sp, tmk, tmv, cp.launch);
+        e = cp.f16 ? launch_split_contig_f16(cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch)
+                   : launch_split_contig_bf16(cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch);
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess)
@@ -309,7 +315,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
         for (int b = 0; b < batch; ++b)
             if (seq_lens_host[b] < 0 || seq_lens_host[b] > s_max)
                 return FD_ERR_INVALID_ARG;
-    if (opts && (opts->num_ctas < 0 || opts->num_ctas > kMaxCtas))
+    if (opts && (opts->num_ctas < 0 || opts->num_ctas > kMaxCtas || opts->dtype < 0 || opts->dtype > 1))
         return FD_ERR_INVALID_ARG;
     if ((long long)batch * s_max >= (1ll << 31) ||
         (long long)num_kv_heads * batch * ceil_div(s_max, kTileTokens) >= (1ll << 31))
@@ -329,7 +335,8 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
         return st;
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
-    if ((st = encode_kv_maps(&tmk, &tmv, k, v, num_kv_heads, rows, kTileTokens, cp.mma, &cp.sp)) != FD_OK)
+    if ((st = encode_kv_maps(&tmk, &tmv, k, v, num_kv_heads, rows, kTileTokens, cp.mma, cp.f16, &cp.sp)) !=
+        FD_OK)
         return st;
     return run(cp, false, tmk, tmv, opts);
 }
@@ -358,7 +365,7 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
         for (int b = 0; b < batch; ++b)
             if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap)
                 return FD_ERR_INVALID_ARG;
-    if (opts && (opts->num_ctas < 0 || opts->num_ctas > kMaxCtas))
+    if (opts && (opts->num_ctas < 0 || opts->num_ctas > kMaxCtas || opts->dtype < 0 || opts->dtype > 1))
         return FD_ERR_INVALID_ARG;
     if (workspace_bytes <
         fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, (int)cap, page_size))
@@ -377,8 +384,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)num_pages * page_size;
     const int box = page_size < kTileTokens ? page_size : kTileTokens;
-    if ((st = encode_kv_maps(&tmk, &tmv, k_pages, v_pages, num_kv_heads, rows, box, cp.mma, &cp.sp)) !=
-        FD_OK)
+    if ((st = encode_kv_maps(&tmk, &tmv, k_pages, v_pages, num_kv_heads, rows, box, cp.mma, cp.f16,
+                             &cp.sp)) != FD_OK)
         return st;
     return run(cp, true, tmk, tmv, opts);
 }

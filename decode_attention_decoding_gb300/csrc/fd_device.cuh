@@ -186,6 +186,27 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// Two IEEE fp16 values packed in a 32-bit word (element 0 low) to fp32.
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w)
+{
+    float2 r;
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(w));
+    return r;
+}
+
+// Packed 16-bit pair to fp32 for the input element type (bf16 or fp16).
+template <bool F16>
+__device__ __forceinline__ float2 x2_to_float2(uint32_t w)
+{
+    if constexpr (F16)
+        return f16x2_to_float2(w);
+    else
+        return bf16x2_to_float2(w);
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
     uint4 v;
@@ -255,6 +276,45 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Two fp32 values rounded to fp16 (nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// D = A (16x16 fp16, row) * B (16x8 fp16, col) + C, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The 16-bit MMA for the input element type.
+template <bool F16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1)
+{
+    if constexpr (F16)
+        mma_f16_16816(d, a0, a1, a2, a3, b0, b1);
+    else
+        mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_x2(float lo, float hi)
+{
+    if constexpr (F16)
+        return pack_f16x2(lo, hi);
+    else
+        return pack_bf16x2(lo, hi);
 }
 
 }  // namespace fd

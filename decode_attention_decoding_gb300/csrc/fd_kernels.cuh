@@ -339,11 +339,15 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
 
 // Combine NSTATE partial softmax states (m, l, acc[G][D]) published in shared
 // memory and write the segment's result: final O/LSE when the CTA saw the
-// whole segment, otherwise a normalised partial and its LSE.
+// whole segment, otherwise a normalised partial and its LSE.  O is divided by
+// the sum of the weights that multiplied V (red_l); the LSE uses the sum of
+// the exact fp32 weights (red_lt), which differs only when P was rounded to a
+// 16-bit type for the tensor-core product.
 template <int G, int NSTATE>
 __device__ __forceinline__ void combine_and_write(const SplitParams &p, const float *red_acc,
-                                                  const float *red_m, const float *red_l, int ctid,
-                                                  int b, int h, int u, bool own)
+                                                  const float *red_m, const float *red_l,
+                                                  const float *red_lt, int ctid, int b, int h, int u,
+                                                  bool own)
 {
     const int slot = u + (int)blockIdx.x;
     for (int idx = ctid; idx < G * kHeadDim; idx += kConsumerThreads) {
@@ -352,16 +356,17 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
 #pragma unroll
         for (int w = 0; w < NSTATE; ++w)
             M = fmaxf(M, red_m[w * G + g]);
-        float lsum = 0.f, o = 0.f;
+        float lsum = 0.f, ltrue = 0.f, o = 0.f;
 #pragma unroll
         for (int w = 0; w < NSTATE; ++w) {
             const float mw = red_m[w * G + g];
             const float wt = (mw == kNegInf) ? 0.f : exp2_approx(mw - M);
             lsum += wt * red_l[w * G + g];
+            ltrue += wt * red_lt[w * G + g];
             o += wt * red_acc[(w * G + g) * kHeadDim + d];
         }
         const float out = lsum > 0.f ? o / lsum : 0.f;
-        const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : kNegInf;
+        const float lse_v = ltrue > 0.f ? (M + log2f(ltrue)) * kLn2 : kNegInf;
         if (own) {
             const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
             p.o[row * kHeadDim + d] = out;
@@ -450,7 +455,7 @@ __device__ __forceinline__ bool merge_if_last(const SplitParams &p, float *scrat
     return consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane);
 }
 
-template <int G>
+template <int G, bool F16>
 __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *smem, uint32_t stage0,
                                                const int *prefix, int *merge_flag,
                                                const int *meta, uint32_t full0, uint32_t empty0,
@@ -504,10 +509,10 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             for (int g = 0; g < G; ++g) {
                 const uint16_t *qp = p.q + ((size_t)b * p.hq + (size_t)h * G + g) * kHeadDim + li * 8;
                 const uint4 raw = ldg128_nc(qp);
-                qf[g][0] = mul2(bf16x2_to_float2(raw.x), c2);
-                qf[g][1] = mul2(bf16x2_to_float2(raw.y), c2);
-                qf[g][2] = mul2(bf16x2_to_float2(raw.z), c2);
-                qf[g][3] = mul2(bf16x2_to_float2(raw.w), c2);
+                qf[g][0] = mul2(x2_to_float2<F16>(raw.x), c2);
+                qf[g][1] = mul2(x2_to_float2<F16>(raw.y), c2);
+                qf[g][2] = mul2(x2_to_float2<F16>(raw.z), c2);
+                qf[g][3] = mul2(x2_to_float2<F16>(raw.w), c2);
             }
         }
 
@@ -523,8 +528,8 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             for (int r = 0; r < kSub; ++r) {
                 const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
                 const uint4 kw = lds128(kbase + row * kRowBytes);
-                const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
-                const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
+                const float2 k0 = x2_to_float2<F16>(kw.x), k1 = x2_to_float2<F16>(kw.y);
+                const float2 k2 = x2_to_float2<F16>(kw.z), k3 = x2_to_float2<F16>(kw.w);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     float2 a = mul2(qf[g][0], k0);
@@ -580,8 +585,8 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                 const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
                 if (row < nvalid) {
                     const uint4 vw = lds128(vbase + row * kRowBytes);
-                    const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
-                    const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
+                    const float2 v0 = x2_to_float2<F16>(vw.x), v1 = x2_to_float2<F16>(vw.y);
+                    const float2 v2 = x2_to_float2<F16>(vw.z), v3 = x2_to_float2<F16>(vw.w);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         const float2 p2 = make_float2(pr[r][g], pr[r][g]);
@@ -638,7 +643,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                 return;
             }
             // 3. combine the warps and write the segment's result
-            combine_and_write<G, kConsumerWarps>(p, red_acc, red_m, red_l, ctid, b, h, u,
+            combine_and_write<G, kConsumerWarps>(p, red_acc, red_m, red_l, red_l, ctid, b, h, u,
                                                  (flags & kOwnSegment) != 0);
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane) ||
                 (!(flags & kOwnSegment) &&
@@ -670,9 +675,9 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 // 16-token slice of a tile, S^T[16 x 8] = K[16 x 128] . Q^T[128 x 8] with the
 // group's query heads as the 8 columns (padded with zero heads when G < 8),
 // and O^T[128 x 8] += V^T[128 x 16] . P^T[16 x 8].  Both are warp-level
-// m16n8k16 bf16 MMAs with fp32 accumulation.  The tile arrives with the
-// 128-byte TMA swizzle (two 8 KB halves of 64 dims each), so the ldmatrix
-// row reads are free of bank conflicts.  P is rounded to bf16 for the second
+// m16n8k16 MMAs on the input type (bf16 or fp16) with fp32 accumulation.
+// The tile arrives with the 128-byte TMA swizzle, so the ldmatrix row reads
+// are free of bank conflicts.  P is rounded to the input type for the second
 // product and the running sum l adds up exactly those rounded weights.
 //
 // Warps 2i and 2i+1 take tokens 16i..16i+15 of every tile; both form the
@@ -689,7 +694,7 @@ __device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk
            (((chunk & 7) ^ (row & 7)) << 4);
 }
 
-template <int G>
+template <int G, bool F16>
 __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t *smem, uint32_t stage0,
                                                const int *prefix, int *merge_flag,
                                                    const int *meta, uint32_t full0, uint32_t empty0,
@@ -710,12 +715,15 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 
     uint32_t qb[8][2];         // Q^T B-fragments, one pair per 16-dim k-step
     float acc[4][4];           // O^T fragments of this warp's 4 dim tiles
-    float m[2], l[2];          // heads 2 qd and 2 qd + 1 (l: this lane's tokens only)
+    // heads 2 qd and 2 qd + 1, this lane's tokens only: l sums the 16-bit
+    // rounded weights that multiply V, lt the exact fp32 weights (for the LSE)
+    float m[2], l[2], lt[2];
     auto reset = [&]() {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             m[j] = kNegInf;
             l[j] = 0.f;
+            lt[j] = 0.f;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -768,7 +776,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             for (int ks = 0; ks < 8; ++ks) {
                 uint32_t a0, a1, a2, a3;
                 ldmatrix_x4(sw128_addr(ktile, row, 2 * ks + (lane >> 4), rl), a0, a1, a2, a3);
-                mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                mma_16816<F16>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
         }
         const bool v0 = tok0 + grp < nvalid, v1 = tok0 + grp + 8 < nvalid;
@@ -793,12 +801,14 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             pw[j + 2] = (x[j + 2] == kNegInf) ? 0.f : exp2_approx(x[j + 2] - m_new);
             m[j] = m_new;
         }
-        const uint32_t p_lo = pack_bf16x2(pw[0], pw[1]);   // token grp, heads 2qd, 2qd+1
-        const uint32_t p_hi = pack_bf16x2(pw[2], pw[3]);   // token grp + 8
+        const uint32_t p_lo = pack_x2<F16>(pw[0], pw[1]);   // token grp, heads 2qd, 2qd+1
+        const uint32_t p_hi = pack_x2<F16>(pw[2], pw[3]);   // token grp + 8
         {
-            const float2 r_lo = bf16x2_to_float2(p_lo), r_hi = bf16x2_to_float2(p_hi);
+            const float2 r_lo = x2_to_float2<F16>(p_lo), r_hi = x2_to_float2<F16>(p_hi);
             l[0] = l[0] * alpha[0] + (r_lo.x + r_hi.x);
             l[1] = l[1] * alpha[1] + (r_lo.y + r_hi.y);
+            lt[0] = lt[0] * alpha[0] + (pw[0] + pw[2]);
+            lt[1] = lt[1] * alpha[1] + (pw[1] + pw[3]);
         }
         // P^T as the B operand (k = token, n = head): transpose the 8x8 blocks.
         const uint32_t pb0 = movmatrix_trans(p_lo);
@@ -830,7 +840,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                 uint32_t a0, a1, a2, a3;
                 ldmatrix_x4_trans(sw128_addr(vtile, vrow, 2 * dt + ((lane >> 3) & 1), rl), a0, a1, a2,
                                   a3);
-                mma_bf16_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
+                mma_16816<F16>(acc[i], a0, a1, a2, a3, pb0, pb1);
             }
         }
         if (ragged)   // order the zeroing stores before the next TMA write to this stage
@@ -846,6 +856,9 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                 l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
                 l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
                 l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
+                lt[j] += __shfl_xor_sync(0xffffffffu, lt[j], 4);
+                lt[j] += __shfl_xor_sync(0xffffffffu, lt[j], 8);
+                lt[j] += __shfl_xor_sync(0xffffffffu, lt[j], 16);
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -854,6 +867,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                     if (dhalf == 0 && grp == 0) {
                         red_m[pair * G + head] = m[j];
                         red_l[pair * G + head] = l[j];
+                        red_l[(kPairs + pair) * G + head] = lt[j];   // exact sums after the pairs' slots
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -867,7 +881,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                 give_up();
                 return;
             }
-            combine_and_write<G, kPairs>(p, red_acc, red_m, red_l, ctid, b, h, u,
+            combine_and_write<G, kPairs>(p, red_acc, red_m, red_l, red_l + kPairs * G, ctid, b, h, u,
                                          (flags & kOwnSegment) != 0);
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane) ||
                 (!(flags & kOwnSegment) &&
@@ -886,7 +900,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 
 // ------------------------------------------------------------------ kernels
 
-template <int G, bool PAGED, bool MMA>
+template <int G, bool PAGED, bool MMA, bool F16>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv)
@@ -941,10 +955,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         split_producer<PAGED, MMA>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
                                    t_begin, t_end, lane);
     else if constexpr (MMA)
-        split_consumer_mma<G>(p, smem, stage0, prefix, misc + 12, meta, full0, empty0, cbar, abort_flag,
+        split_consumer_mma<G, F16>(p, smem, stage0, prefix, misc + 12, meta, full0, empty0, cbar, abort_flag,
                               t_begin, t_end, warp, lane);
     else
-        split_consumer<G>(p, smem, stage0, prefix, misc + 12, meta, full0, empty0, cbar, abort_flag,
+        split_consumer<G, F16>(p, smem, stage0, prefix, misc + 12, meta, full0, empty0, cbar, abort_flag,
                           t_begin, t_end, warp, lane);
 }
 

@@ -17,21 +17,26 @@ struct SplitLaunch {
     cudaStream_t stream;
 };
 
-// Split kernel with CUDA-core consumers; K/V tensor maps without swizzle.
-// Returns cudaErrorInvalidValue for an unsupported group size.
+// Split kernel with CUDA-core consumers on bf16 inputs; K/V tensor maps
+// without swizzle (used by the no-workspace entry point).  Returns
+// cudaErrorInvalidValue for an unsupported group size.
 cudaError_t launch_split_contig(int group, const SplitParams &p, const CUtensorMap &tmk,
                                 const CUtensorMap &tmv, const SplitLaunch &cfg);
-cudaError_t launch_split_paged(int group, const SplitParams &p, const CUtensorMap &tmk,
-                               const CUtensorMap &tmv, const SplitLaunch &cfg);
-// Split kernel with tensor-core consumers (group 2, 4 or 8); K/V tensor maps
-// with 64-dim boxes and the 128-byte swizzle.
-cudaError_t launch_split_contig_mma(int group, const SplitParams &p, const CUtensorMap &tmk,
+
+// Any variant: layout (paged), consumers (mma: tensor cores for group 2, 4
+// or 8, with swizzled K/V maps), input element type (f16: IEEE fp16, else
+// bf16).  One translation unit per (layout, element type) defines it.
+cudaError_t launch_split_contig_bf16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
+                                     const CUtensorMap &tmv, const SplitLaunch &cfg);
+cudaError_t launch_split_contig_f16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
                                     const CUtensorMap &tmv, const SplitLaunch &cfg);
-cudaError_t launch_split_paged_mma(int group, const SplitParams &p, const CUtensorMap &tmk,
+cudaError_t launch_split_paged_bf16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
+                                    const CUtensorMap &tmv, const SplitLaunch &cfg);
+cudaError_t launch_split_paged_f16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
                                    const CUtensorMap &tmv, const SplitLaunch &cfg);
 
-// Shared by the two split translation units.
-template <int G, bool PAGED, bool MMA>
+// Shared by the split translation units.
+template <int G, bool PAGED, bool MMA, bool F16>
 cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const SplitLaunch &c)
 {
@@ -44,7 +49,7 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
         return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(split_kernel<G, PAGED, MMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(split_kernel<G, PAGED, MMA, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)c.smem_optin);
         if (e != cudaSuccess)
             return e;
@@ -62,7 +67,28 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
     cfg.stream = c.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, MMA>, p, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, MMA, F16>, p, tmk, tmv);
+}
+
+template <bool PAGED, bool F16>
+cudaError_t launch_split_group(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
+                               const CUtensorMap &tmv, const SplitLaunch &c)
+{
+    if (mma) {
+        switch (group) {
+        case 2: return launch_split_t<2, PAGED, true, F16>(p, tmk, tmv, c);
+        case 4: return launch_split_t<4, PAGED, true, F16>(p, tmk, tmv, c);
+        case 8: return launch_split_t<8, PAGED, true, F16>(p, tmk, tmv, c);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (group) {
+    case 1: return launch_split_t<1, PAGED, false, F16>(p, tmk, tmv, c);
+    case 2: return launch_split_t<2, PAGED, false, F16>(p, tmk, tmv, c);
+    case 4: return launch_split_t<4, PAGED, false, F16>(p, tmk, tmv, c);
+    case 8: return launch_split_t<8, PAGED, false, F16>(p, tmk, tmv, c);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace fd

@@ -1,0 +1,12 @@
+// Split kernel instances: paged KV layout [num_pages, P, Hkv, D], fp16.
+#include "fd_launch.h"
+
+namespace fd {
+
+cudaError_t launch_split_paged_f16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
+                                   const CUtensorMap &tmv, const SplitLaunch &cfg)
+{
+    return launch_split_group<true, true>(mma, group, p, tmk, tmv, cfg);
+}
+
+}  // namespace fd

@@ -39,8 +39,9 @@
  *     the workspace 256-byte aligned; otherwise FD_ERR_INVALID_ARG.
  *   - Supported shapes: head_dim 128; Hq/Hkv in {1, 2, 4, 8}; batch <= 4096.
  *     Other shapes return FD_ERR_UNSUPPORTED.
- *   - Precision: q, K and V are bf16; scores, softmax and accumulation are
- *     fp32; outputs are fp32.
+ *   - Precision: q, K and V are bf16 (default) or IEEE fp16
+ *     (fd_options.dtype); scores, softmax and accumulation are fp32; outputs
+ *     are fp32.
  */
 #ifndef FD_H
 #define FD_H
@@ -65,6 +66,12 @@ typedef enum fd_status {
     FD_ERR_DEVICE_INPUT = 6         /* a device-side length or block-table entry was out of range */
 } fd_status;
 
+/* Element type of q, K and V. */
+typedef enum fd_dtype {
+    FD_DTYPE_BF16 = 0,   /* bfloat16 (default) */
+    FD_DTYPE_F16 = 1     /* IEEE binary16 */
+} fd_dtype;
+
 /* Optional knobs; pass NULL for the defaults. */
 typedef struct fd_options {
     /* Number of persistent split CTAs that share the KV tiles (1..1024).
@@ -81,6 +88,8 @@ typedef struct fd_options {
      * and after the split kernel (for timing the kernel alone); NULL = none. */
     void *split_start_event;
     void *split_end_event;
+    /* Element type of q, K and V (fd_dtype); 0 = bf16. */
+    int dtype;
 } fd_options;
 
 /* Test hook: CTA 0 announces more bytes for its first tile than it loads, so

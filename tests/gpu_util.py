@@ -9,12 +9,14 @@ import fd_synth as syn
 O_ATOL, O_RTOL, LSE_ATOL = 1e-2, 1e-2, 1e-3
 
 
-def dev_bf16(bits, device="cuda"):
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+def dev_bf16(bits, device="cuda", dtype="bf16"):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+    return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
 
 
 def to_device(w, device="cuda"):
-    d = dict(q=dev_bf16(w.q, device), k=dev_bf16(w.k, device), v=dev_bf16(w.v, device),
+    dt = getattr(w, "dtype", "bf16")
+    d = dict(q=dev_bf16(w.q, device, dt), k=dev_bf16(w.k, device, dt), v=dev_bf16(w.v, device, dt),
              seq_lens=torch.from_numpy(np.ascontiguousarray(w.seq_lens, dtype=np.int32)).to(device))
     if w.paged:
         d["block_table"] = torch.from_numpy(np.ascontiguousarray(w.block_table, dtype=np.int32)).to(device)
@@ -73,7 +75,7 @@ def contig_to_paged(w, page, perm_seed, extra_pages=3, poison=False):
             kp[table[b, i], :n] = w.k[b, i * page:i * page + n]
             vp[table[b, i], :n] = w.v[b, i * page:i * page + n]
     return syn.Workload(w.name + f"_p{page}", w.q, kp, vp, lens.copy(), w.num_q_heads, w.num_kv_heads,
-                        d, w.scale, page_size=page, block_table=table)
+                        d, w.scale, page_size=page, block_table=table, dtype=getattr(w, "dtype", "bf16"))
 
 
 def sample_items(w, n, seed=0):
