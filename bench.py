@@ -4,8 +4,7 @@
 Default workload: MHA long-KV decode -- batch 1, 32 query heads = 32 kv heads,
 head_dim 128, kv_len 65536, contiguous [S, H, D] bf16 K/V, scale 1/sqrt(128)
 (1 GiB of K+V, larger than the 129 MB L2, so no flush is needed between
-steps).  A step is one fd_decode call: one kernel, whose CTAs also merge the
-split partials by LSE.
+steps).  A step is one fd_decode call: the split kernel plus the LSE merge.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
 
@@ -334,11 +333,28 @@ def run_ours(args, rank, world):
         dl = torch.empty_like(lens)
         K2 = max(3, min(K, args.e2e_steps))
 
+        # Host->device copies of the step's inputs, split into chunks spread
+        # over several streams so that more than one copy engine moves them.
+        n_cs = max(1, args.copy_streams)
+        cstreams = [torch.cuda.Stream(dev) for _ in range(n_cs)]
+        pieces = []
+        for hsrc, ddst in ((hk_, dk), (hv_, dv)):
+            hf, df = hsrc.view(-1), ddst.view(-1)
+            step_ = (hf.numel() + 2 * n_cs - 1) // (2 * n_cs)
+            for i0 in range(0, hf.numel(), step_):
+                pieces.append((hf[i0:i0 + step_], df[i0:i0 + step_]))
+
         def e2e_step():
+            cur = torch.cuda.current_stream(dev)
+            for cs in cstreams:
+                cs.wait_stream(cur)
+            for i, (hsrc, ddst) in enumerate(pieces):
+                with torch.cuda.stream(cstreams[i % n_cs]):
+                    ddst.copy_(hsrc, non_blocking=True)
             dq.copy_(hq_, non_blocking=True)
-            dk.copy_(hk_, non_blocking=True)
-            dv.copy_(hv_, non_blocking=True)
             dl.copy_(hl_, non_blocking=True)
+            for cs in cstreams:
+                cur.wait_stream(cs)
             qb, kb, vb = dq.view(torch.bfloat16), dk.view(torch.bfloat16), dv.view(torch.bfloat16)
             if w.paged:
                 fd.fd_decode_paged(qb, kb, vb, table, dl, scale=w.scale, out=out, lse=lse, workspace=ws)
@@ -363,6 +379,7 @@ def run_ours(args, rank, world):
         d2h = ho.numel() * 4 + hlse.numel() * 4
         e2e = {"value": whole_job_tbs(bc["call"], world, e2e_ms), "unit": "TB/s",
                "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": int(h2d),
+               "copy_streams": n_cs,
                "d2h_bytes_per_step": int(d2h), "steps": K2}
 
     err = fd.fd_get_device_error(ws)
@@ -395,7 +412,7 @@ def run_ours(args, rank, world):
                          "consumers": ("cuda cores" if (args.cuda_cores or w.num_q_heads == w.num_kv_heads)
                                        else "tensor cores (mma.sync bf16)"),
                          "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"},
-            "gpu_launches": K,            # one split kernel per call (the merge is fused)
+            "gpu_launches": 2 * K,        # split kernel + merge kernel per call
             "clocks": clk.summary(t_wall0, t_wall1),
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -489,6 +506,8 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--copy-streams", type=int, default=4,
+                    help="streams the e2e leg spreads its host->device copies over")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of a CUDA graph")
     ap.add_argument("--cuda-cores", action="store_true",

@@ -1,5 +1,5 @@
 // fd_api.cu -- the C ABI of include/fd.h: argument checks, workspace layout,
-// split planning, TMA descriptors and the launch (one kernel per call).
+// split planning, TMA descriptors and the two launches (split, then merge).
 //
 // Host side of "纯手搓 flash decoding sm120" section 1 (binding and launch
 // code), re-planned for GB300: instead of a chunk size bucketed from a fixed
@@ -162,6 +162,7 @@ fd_status check_common(const void *q, const float *o, const void *ws, int batch,
 
 struct CallPlan {
     SplitParams sp;
+    MergeParams mp;
     SplitLaunch launch;
     int group;
     bool mma;   // tensor-core consumers (GQA groups) instead of CUDA cores
@@ -227,7 +228,6 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     sp.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
     sp.ws_lse = reinterpret_cast<float *>(ws + wl.lse_off);
     sp.ws_prefix = reinterpret_cast<int32_t *>(ws + wl.prefix_off);
-    sp.ws_cnt = reinterpret_cast<int32_t *>(ws + wl.cnt_off);
     sp.ws_err = reinterpret_cast<unsigned int *>(ws + wl.err_off);
     sp.batch = batch;
     sp.hq = hq;
@@ -250,6 +250,16 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     if (st != FD_OK)
         return st;
 
+    MergeParams &mp = cp->mp;
+    mp.o = o;
+    mp.lse = lse;
+    mp.ws_o = sp.ws_o;
+    mp.ws_lse = sp.ws_lse;
+    mp.ws_prefix = sp.ws_prefix;
+    mp.batch = batch;
+    mp.hq = hq;
+    mp.hkv = hkv;
+    mp.num_ctas = num_ctas;
     cp->group = group;
     cp->mma = use_mma(group, page_size, opts);
     cp->f16 = opts && opts->dtype == FD_DTYPE_F16;
@@ -274,6 +284,9 @@ fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUte
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess)
+        return FD_ERR_CUDA;
+    e = launch_merge(cp.group, cp.mp, cp.sp.batch * cp.sp.hkv, stream);
+    if (e != cudaSuccess)
         return FD_ERR_CUDA;
     return FD_OK;
 }

@@ -23,9 +23,8 @@
 //     consumer warps merge their 16 half-warp states through shared memory
 //     and write either the final O and natural-log LSE (the CTA saw the whole
 //     segment) or a normalised partial O and its LSE (lse = m ln2 + ln l).
-// Merge ("pass 2", section 2 of the sm120 article), fused into the split
-// kernel: for a segment several CTAs shared, the CTA that finishes it last
-// (an atomic ticket, nothing waits) combines the partials:
+// Merge kernel ("pass 2", section 2 of the sm120 article): one CTA per
+// (segment, query head) combines that head's partials:
 // LSE = max + ln sum exp(lse_i - max), O = sum O_i exp(lse_i - LSE).
 #pragma once
 
@@ -63,7 +62,6 @@ struct SplitParams {
     float *ws_o;                  // [slots, G, D]
     float *ws_lse;                // [slots, G]
     int32_t *ws_prefix;           // [B + 1]
-    int32_t *ws_cnt;              // [B * Hkv] merge tickets, zero between calls
     unsigned int *ws_err;
     int batch, hq, hkv;
     int cap;                      // largest valid length
@@ -80,6 +78,15 @@ struct SplitParams {
     int box4d;
     int box_rows_log2;   // log2 of the rows in one box: 6 (64) or log2(page size)
     int page_log2;       // paged, page size under 64: log2 of the page size
+};
+
+struct MergeParams {
+    float *o;
+    float *lse;
+    const float *ws_o;
+    const float *ws_lse;
+    const int32_t *ws_prefix;
+    int batch, hq, hkv, num_ctas;
 };
 
 __device__ __forceinline__ int load_len(const SplitParams &p, int b, bool report)
@@ -380,84 +387,8 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
     }
 }
 
-// Called by the consumer warps after they wrote a partial of segment u (the
-// CTA saw only part of it).  Each CTA that touched u takes a ticket; the one
-// that draws the last ticket merges the segment's partials by log-sum-exp
-// ("pass 2" of the sm120 article, section 2: LSE = max + ln sum e^(lse_i -
-// max), O = sum O_i e^(lse_i - LSE)) and writes O and LSE.  No CTA waits for
-// another.  `scratch` (the free shared-memory reduction region) holds the
-// partials' LSEs and weights.  Returns false if a consumer barrier ran out.
-template <int G>
-__device__ __forceinline__ bool merge_if_last(const SplitParams &p, float *scratch, int *flag,
-                                              const int *prefix, int b, int h, int u, int cw, int lane,
-                                              uint32_t cbar, uint32_t &cph, const volatile int *abort_flag)
-{
-    const int ctid = cw * 32 + lane;
-    const int T = prefix[p.batch];
-    const int nb = (prefix[b + 1] - prefix[b]) / p.hkv;
-    const int first = prefix[b] + h * nb;
-    const int c0 = cta_of_tile(T, (int)gridDim.x, first);
-    const int n = cta_of_tile(T, (int)gridDim.x, first + nb - 1) - c0 + 1;
-    if (ctid == 0) {
-        __threadfence();   // this CTA's partial is visible before its ticket
-        const int last = atomicAdd(p.ws_cnt + u, 1) == n - 1;
-        if (last) {
-            __threadfence();        // every other partial is visible to this CTA
-            p.ws_cnt[u] = 0;        // all n tickets are in: ready for the next call
-        }
-        *flag = last;
-    }
-    if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane))
-        return false;
-    if (!*flag)
-        return true;
-    float *w = scratch;            // [n][G] partial LSEs, then merge weights
-    float *seg_lse = scratch + n * G;
-    const float *lse_src = p.ws_lse + (size_t)(u + c0) * G;   // slots u+c0 .. u+c0+n-1
-    for (int i = ctid; i < n * G; i += kConsumerThreads)
-        w[i] = __ldcg(lse_src + i);
-    if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane))
-        return false;
-    if (cw < G) {                  // warp g: LSE of head g over the n partials
-        float mx = kNegInf;
-        for (int c = lane; c < n; c += 32)
-            mx = fmaxf(mx, w[c * G + cw]);
-#pragma unroll
-        for (int off = 16; off; off >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        float sum = 0.f;
-        for (int c = lane; c < n; c += 32)
-            sum += expf(w[c * G + cw] - mx);
-#pragma unroll
-        for (int off = 16; off; off >>= 1)
-            sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        if (lane == 0)
-            seg_lse[cw] = mx + logf(sum);
-    }
-    if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane))
-        return false;
-    for (int i = ctid; i < n * G; i += kConsumerThreads)
-        w[i] = expf(w[i] - seg_lse[i % G]);
-    if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane))
-        return false;
-    const float *o_src = p.ws_o + (size_t)(u + c0) * G * kHeadDim;
-    for (int idx = ctid; idx < G * kHeadDim; idx += kConsumerThreads) {
-        const int g = idx / kHeadDim;
-        float acc = 0.f;
-        for (int c = 0; c < n; ++c)
-            acc += __ldcg(o_src + (size_t)c * G * kHeadDim + idx) * w[c * G + g];
-        const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
-        p.o[row * kHeadDim + (idx % kHeadDim)] = acc;
-        if (idx % kHeadDim == 0 && p.lse)
-            p.lse[row] = seg_lse[g];
-    }
-    // the scratch is reused by the next flush
-    return consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane);
-}
-
 template <int G, bool F16>
 __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *smem, uint32_t stage0,
-                                               const int *prefix, int *merge_flag,
                                                const int *meta, uint32_t full0, uint32_t empty0,
                                                uint32_t cbar, volatile int *abort_flag, int t_begin,
                                                int t_end, int cw, int lane)
@@ -645,9 +576,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             // 3. combine the warps and write the segment's result
             combine_and_write<G, kConsumerWarps>(p, red_acc, red_m, red_l, red_l, ctid, b, h, u,
                                                  (flags & kOwnSegment) != 0);
-            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane) ||
-                (!(flags & kOwnSegment) &&
-                 !merge_if_last<G>(p, red_acc, merge_flag, prefix, b, h, u, cw, lane, cbar, cph, abort_flag))) {
+            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
             }
@@ -696,7 +625,6 @@ __device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk
 
 template <int G, bool F16>
 __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t *smem, uint32_t stage0,
-                                               const int *prefix, int *merge_flag,
                                                    const int *meta, uint32_t full0, uint32_t empty0,
                                                    uint32_t cbar, volatile int *abort_flag, int t_begin,
                                                    int t_end, int cw, int lane)
@@ -883,9 +811,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             }
             combine_and_write<G, kPairs>(p, red_acc, red_m, red_l, red_l + kPairs * G, ctid, b, h, u,
                                          (flags & kOwnSegment) != 0);
-            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane) ||
-                (!(flags & kOwnSegment) &&
-                 !merge_if_last<G>(p, red_acc, merge_flag, prefix, b, h, u, cw, lane, cbar, cph, abort_flag))) {
+            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
             }
@@ -935,16 +861,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     pdl_wait_prior_grid();
     build_prefix(p, prefix, misc + 1);   // ends with __syncthreads
 
-    // Requests with no tokens get no tile: O = 0 and LSE = -inf, written here.
-    for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
-        if (prefix[b + 1] == prefix[b]) {
-            for (int i = tid; i < p.hq * kHeadDim; i += kSplitThreads)
-                p.o[(size_t)b * p.hq * kHeadDim + i] = 0.f;
-            if (p.lse)
-                for (int i = tid; i < p.hq; i += kSplitThreads)
-                    p.lse[(size_t)b * p.hq + i] = kNegInf;
-        }
-    }
     const int T = prefix[p.batch];
     int t_begin, t_end;
     cta_tile_range(T, (int)gridDim.x, (int)blockIdx.x, &t_begin, &t_end);
@@ -955,11 +871,95 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         split_producer<PAGED, MMA>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
                                    t_begin, t_end, lane);
     else if constexpr (MMA)
-        split_consumer_mma<G, F16>(p, smem, stage0, prefix, misc + 12, meta, full0, empty0, cbar, abort_flag,
+        split_consumer_mma<G, F16>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag,
                               t_begin, t_end, warp, lane);
     else
-        split_consumer<G, F16>(p, smem, stage0, prefix, misc + 12, meta, full0, empty0, cbar, abort_flag,
+        split_consumer<G, F16>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag,
                           t_begin, t_end, warp, lane);
+}
+
+// One CTA per (segment, query head of its group); thread d owns output dim d.
+// The partials' log-sum-exps and merge weights are staged in shared memory
+// so each output needs only one pass over the partial rows.
+template <int G>
+__global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__ MergeParams p)
+{
+    __shared__ float s_w[kMaxCtas];
+    __shared__ float s_lse;
+    pdl_launch_dependents();   // the next call's split kernel may start its prologue
+    pdl_wait_prior_grid();
+    const int u = blockIdx.x, g = blockIdx.y;
+    const int b = u / p.hkv, h = u - b * p.hkv;
+    const int d = threadIdx.x;
+    const int pb = p.ws_prefix[b], pe = p.ws_prefix[b + 1], T = p.ws_prefix[p.batch];
+    const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
+    if (pe == pb) {   // empty request: O = 0, LSE = -inf
+        p.o[row * kHeadDim + d] = 0.f;
+        if (d == 0 && p.lse)
+            p.lse[row] = kNegInf;
+        return;
+    }
+    const int nb = (pe - pb) / p.hkv;
+    const int first = pb + h * nb, last = first + nb - 1;
+    const int c0 = cta_of_tile(T, p.num_ctas, first), c1 = cta_of_tile(T, p.num_ctas, last);
+    if (c0 == c1)
+        return;   // one CTA saw the whole segment and wrote it
+    const int n = c1 - c0 + 1;
+    float lmax = kNegInf;
+    for (int i = d; i < n; i += kHeadDim) {
+        const float v = p.ws_lse[(size_t)(u + c0 + i) * G + g];
+        s_w[i] = v;
+        lmax = fmaxf(lmax, v);
+    }
+    // block max, then block sum of exp(lse_i - max): warp shuffles + shared memory
+    __shared__ float s_red[kHeadDim / 32];
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+    if ((d & 31) == 0)
+        s_red[d >> 5] = lmax;
+    __syncthreads();
+    float M = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kHeadDim / 32; ++w)
+        M = fmaxf(M, s_red[w]);
+    __syncthreads();
+    float sum = 0.f;
+    for (int i = d; i < n; i += kHeadDim)
+        sum += expf(s_w[i] - M);
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if ((d & 31) == 0)
+        s_red[d >> 5] = sum;
+    __syncthreads();
+    if (d == 0) {
+        float S = 0.f;
+#pragma unroll
+        for (int w = 0; w < kHeadDim / 32; ++w)
+            S += s_red[w];
+        s_lse = M + logf(S);
+    }
+    __syncthreads();
+    const float lse = s_lse;
+    for (int i = d; i < n; i += kHeadDim)
+        s_w[i] = expf(s_w[i] - lse);
+    __syncthreads();
+    // several partial rows in flight per thread: the loop is latency-bound
+    float acc = 0.f;
+    const float *src = p.ws_o + ((size_t)(u + c0) * G + g) * kHeadDim + d;
+    const size_t stride = (size_t)G * kHeadDim;
+    int i = 0;
+    for (; i + 4 <= n; i += 4) {
+        const float x0 = src[(size_t)i * stride], x1 = src[(size_t)(i + 1) * stride];
+        const float x2 = src[(size_t)(i + 2) * stride], x3 = src[(size_t)(i + 3) * stride];
+        acc += x0 * s_w[i] + x1 * s_w[i + 1] + x2 * s_w[i + 2] + x3 * s_w[i + 3];
+    }
+    for (; i < n; ++i)
+        acc += src[(size_t)i * stride] * s_w[i];
+    p.o[row * kHeadDim + d] = acc;
+    if (d == 0 && p.lse)
+        p.lse[row] = lse;
 }
 
 }  // namespace fd

@@ -35,6 +35,10 @@ cudaError_t launch_split_paged_bf16(bool mma, int group, const SplitParams &p, c
 cudaError_t launch_split_paged_f16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
                                    const CUtensorMap &tmv, const SplitLaunch &cfg);
 
+// LSE merge of the split partials; grid = number of segments (requests x kv
+// heads).  Launched as a programmatic dependent of the split kernel.
+cudaError_t launch_merge(int group, const MergeParams &p, int grid, cudaStream_t stream);
+
 // Shared by the split translation units.
 template <int G, bool PAGED, bool MMA, bool F16>
 cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,

@@ -1,0 +1,35 @@
+// LSE merge kernel instances, launched with programmatic dependent launch so
+// their launch overlaps the split kernel's tail.
+#include "fd_launch.h"
+
+namespace fd {
+
+template <int G>
+// grid = number of segments (requests x kv heads); one CTA per (segment, query head).
+static cudaError_t launch_merge_t(const MergeParams &p, int grid, cudaStream_t stream)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, (unsigned)G);   // (segment, query head of its group)
+    cfg.blockDim = dim3(kHeadDim);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel<G>, p);
+}
+
+cudaError_t launch_merge(int group, const MergeParams &p, int grid, cudaStream_t stream)
+{
+    switch (group) {
+    case 1: return launch_merge_t<1>(p, grid, stream);
+    case 2: return launch_merge_t<2>(p, grid, stream);
+    case 4: return launch_merge_t<4>(p, grid, stream);
+    case 8: return launch_merge_t<8>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fd

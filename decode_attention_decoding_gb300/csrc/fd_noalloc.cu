@@ -13,10 +13,10 @@
 // The scratch array (kNoallocScratchBytes) is reserved on every GPU that
 // loads this library and stays reserved until the process exits.  Every call
 // on a device uses the same array, and the array keeps whatever the previous
-// call left in it; the call clears what must start at zero (the device-error
-// word and the per-segment merge tickets) before its kernel runs.  Two calls
-// whose kernels overlap on the GPU (different streams, no ordering between
-// them) race on the array and give undefined results.
+// call left in it; the call clears the one word that must start at zero (the
+// device-error word) before its kernels run.  Two calls whose kernels
+// overlap on the GPU (different streams, no ordering between them) race on
+// the array and give undefined results.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -103,19 +103,15 @@ fd_status encode_rows(CUtensorMap *map, const void *base, int hkv, long long row
 }
 
 // Scratch layout for `slots` partials of `group` rows: the same regions as a
-// caller-provided workspace, but sized for the actual number of split CTAs,
-// with the merge tickets right after the status word so one memset clears
-// everything that must start at zero.
+// caller-provided workspace, but sized for the actual number of split CTAs.
 struct NoallocLayout {
-    size_t cnt_off, zero_bytes, prefix_off, lse_off, o_off, total;
+    size_t prefix_off, lse_off, o_off, total;
 };
 
-NoallocLayout noalloc_layout(int batch, int segments, int slots, int group)
+NoallocLayout noalloc_layout(int batch, int slots, int group)
 {
     NoallocLayout l;
-    l.cnt_off = 256;
-    l.zero_bytes = l.cnt_off + sizeof(int) * (size_t)segments;
-    l.prefix_off = align_up(l.zero_bytes, 256);
+    l.prefix_off = 256;
     l.lse_off = align_up(l.prefix_off + sizeof(int) * (size_t)(batch + 1), 256);
     l.o_off = align_up(l.lse_off + sizeof(float) * (size_t)slots * group, 256);
     l.total = align_up(l.o_off + sizeof(float) * (size_t)slots * group * kHeadDim, 256);
@@ -149,8 +145,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     if (st != FD_OK)
         return st;
     const int num_ctas = dev.sms;
-    const NoallocLayout wl =
-        noalloc_layout(batch, batch * num_kv_heads, batch * num_kv_heads + num_ctas, group);
+    const NoallocLayout wl = noalloc_layout(batch, batch * num_kv_heads + num_ctas, group);
     if (wl.total > kNoallocScratchBytes)
         return FD_ERR_WORKSPACE_TOO_SMALL;   // shape needs more scratch than the fixed array holds
 
@@ -163,7 +158,6 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     sp.lse = lse;
     sp.ws_err = reinterpret_cast<unsigned int *>(dev.scratch);
     sp.ws_prefix = reinterpret_cast<int32_t *>(dev.scratch + wl.prefix_off);
-    sp.ws_cnt = reinterpret_cast<int32_t *>(dev.scratch + wl.cnt_off);
     sp.ws_lse = reinterpret_cast<float *>(dev.scratch + wl.lse_off);
     sp.ws_o = reinterpret_cast<float *>(dev.scratch + wl.o_off);
     sp.batch = batch;
@@ -199,16 +193,29 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     launch.smem_optin = (size_t)dev.smem_optin;
     launch.stream = reinterpret_cast<cudaStream_t>(stream);
 
+    MergeParams mp;
+    mp.o = o;
+    mp.lse = lse;
+    mp.ws_o = sp.ws_o;
+    mp.ws_lse = sp.ws_lse;
+    mp.ws_prefix = sp.ws_prefix;
+    mp.batch = batch;
+    mp.hq = num_q_heads;
+    mp.hkv = num_kv_heads;
+    mp.num_ctas = num_ctas;
+
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
     if ((st = encode_rows(&tmk, k, num_kv_heads, rows)) != FD_OK ||
         (st = encode_rows(&tmv, v, num_kv_heads, rows)) != FD_OK)
         return st;
 
-    // The status word and the merge tickets must start at zero.
-    if (cudaMemsetAsync(dev.scratch, 0, wl.zero_bytes, launch.stream) != cudaSuccess)
+    // The status word is the only part of the scratch that must start at zero.
+    if (cudaMemsetAsync(sp.ws_err, 0, sizeof(unsigned int), launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;
     if (launch_split_contig(group, sp, tmk, tmv, launch) != cudaSuccess)
+        return FD_ERR_CUDA;
+    if (launch_merge(group, mp, batch * num_kv_heads, launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;
     if (device_status &&
         cudaMemcpyAsync(device_status, sp.ws_err, sizeof(unsigned int), cudaMemcpyDeviceToDevice,

@@ -13,11 +13,10 @@
 // length: CTA c gets floor(T/P) tiles, plus one if c < T mod P.  A CTA that
 // covers a whole segment writes that segment's final output; otherwise it
 // writes a partial (normalised output + log-sum-exp) for every segment it
-// touches, into slot u + c, and takes a ticket on the segment's counter; the
-// CTA drawing the last ticket merges the segment.  That slot is unique: CTAs and segments are both
+// touches, into slot u + c.  That slot is unique: CTAs and segments are both
 // visited in increasing order, so two CTAs c < c' that share a slot would
 // need u > u' while c' only sees segments >= the last one of c.  There are
-// at most B*Hkv + P - 1 slots.  The merging CTA finds the CTAs of segment u
+// at most B*Hkv + P - 1 slots.  The merge step finds the CTAs of segment u
 // from its first and last tile with cta_of_tile().
 //
 // Shared by the host (tests, sizing) and the kernels.
@@ -77,7 +76,6 @@ FD_HD int request_of_tile(const int *prefix, int batch, int t)
 struct WorkspaceLayout {
     size_t err_off;      // uint32 sticky error word
     size_t prefix_off;   // int32 [batch + 1]
-    size_t cnt_off;      // int32 [batch * Hkv] merge tickets (zero between calls)
     size_t lse_off;      // fp32 [slots][group]
     size_t o_off;        // fp32 [slots][group][head_dim]
     size_t total;
@@ -92,8 +90,7 @@ FD_HD WorkspaceLayout workspace_layout(int batch, int num_kv_heads, int group, i
     w.slots = batch * num_kv_heads + kMaxCtas;
     w.err_off = 0;
     w.prefix_off = 256;
-    w.cnt_off = align_up(w.prefix_off + sizeof(int) * (size_t)(batch + 1), 256);
-    w.lse_off = align_up(w.cnt_off + sizeof(int) * (size_t)batch * num_kv_heads, 256);
+    w.lse_off = align_up(w.prefix_off + sizeof(int) * (size_t)(batch + 1), 256);
     w.o_off = align_up(w.lse_off + sizeof(float) * (size_t)w.slots * group, 256);
     w.total = align_up(w.o_off + sizeof(float) * (size_t)w.slots * group * head_dim, 256);
     return w;

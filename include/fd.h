@@ -112,10 +112,9 @@ typedef struct fd_options {
 /*
  * Bytes of workspace that fd_decode / fd_decode_paged need for this shape.
  * Pure host function (no CUDA call).  The size does not depend on the
- * lengths: it holds a 256-byte header, the per-request tile prefix, one
- * merge ticket per (request, kv head), and one fp32 partial (Hq/Hkv rows of
- * head_dim outputs plus their log-sum-exp) per (request, kv head) plus one
- * per possible split CTA.  max_kv_len and page_size are validated but do not
+ * lengths: it holds a 256-byte header, the per-request tile prefix and one
+ * fp32 partial (Hq/Hkv rows of head_dim outputs plus their log-sum-exp) per
+ * (request, kv head) plus one per possible split CTA.  max_kv_len and page_size are validated but do not
  * change the size.
  * Returns 0 for invalid arguments.
  */
@@ -123,11 +122,9 @@ size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_
                          int max_kv_len, int page_size);
 
 /*
- * Zero-fill a workspace (its sticky device-error word and the per-segment
- * merge tickets must start at zero; the calls leave them at zero).  Call once
- * after allocating a workspace, before its first use, and again after
- * fd_get_device_error has reported FD_ERR_TIMEOUT.  Stream-ordered,
- * asynchronous.
+ * Zero-fill a workspace (its sticky device-error word must start at zero).
+ * Call once after allocating a workspace, before its first use.
+ * Stream-ordered, asynchronous.
  */
 fd_status fd_workspace_init(void *workspace, size_t workspace_bytes, fd_stream_t stream);
 
@@ -208,17 +205,16 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  *   scale, o, lse: as for fd_decode (lse may be NULL).
  *   device_status: NULL, or a device uint32 that receives this call's
  *   FD_DEVICE_STATUS_* bits (0 when all went well), stream-ordered.
- * Limits: the scratch must hold 256 bytes + 4 (batch * num_kv_heads) bytes
- * of merge tickets + 4 (batch + 1) bytes + (batch * num_kv_heads + number of
- * SMs) partials of (Hq/Hkv) * (head_dim + 1) * 4 bytes, each region rounded
- * up to 256 bytes; a larger shape returns FD_ERR_WORKSPACE_TOO_SMALL before
- * anything is launched.
+ * Limits: the scratch must hold 256 bytes + 4 (batch + 1) bytes + (batch *
+ * num_kv_heads + number of SMs) partials of (Hq/Hkv) * (head_dim + 1) * 4
+ * bytes, each region rounded up to 256 bytes; a larger shape returns
+ * FD_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  * The first call on each device resolves the array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call before any
  * stream capture.
  * Every call on a device shares the one array, which keeps the previous
- * call's contents; each call clears the parts that must start at zero (the
- * status word and the merge tickets) itself.  Calls whose kernels can overlap on the GPU (for
+ * call's contents; each call clears the part that must start at zero (the
+ * status word) itself.  Calls whose kernels can overlap on the GPU (for
  * example on two unordered streams) race on the array: order them.
  */
 fd_status fd_decode_noalloc(const void *q, const void *k, const void *v,
@@ -229,9 +225,8 @@ fd_status fd_decode_noalloc(const void *q, const void *k, const void *v,
 /*
  * Read and clear the sticky device-error word of a workspace: FD_OK,
  * FD_ERR_TIMEOUT or FD_ERR_DEVICE_INPUT (timeout wins if both happened).
- * After FD_ERR_TIMEOUT the outputs of the failed call are undefined and the
- * workspace must be re-initialised with fd_workspace_init before reuse (a
- * call cut short can leave merge tickets behind).
+ * After FD_ERR_TIMEOUT the outputs of the failed call are undefined; the
+ * workspace can be reused as it is.
  * SYNCHRONISES `stream` (it copies one word to the host).
  */
 fd_status fd_get_device_error(void *workspace, fd_stream_t stream);
