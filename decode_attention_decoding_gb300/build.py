@@ -2,8 +2,9 @@
 
 Usage: ``python -m decode_attention_decoding_gb300.build`` or call :func:`build`.
 Each translation unit is compiled by its own nvcc process, in parallel, then
-linked into ``decode_attention_decoding_gb300/libfd.so``.  Objects go to
-``decode_attention_decoding_gb300/_build/``.
+linked into ``decode_attention_decoding_gb300/libfd.so``.  ``fd_split_inst.cu``
+is compiled once per split-kernel variant (layout x element type x head_dim),
+each with its own defines.  Objects go to ``decode_attention_decoding_gb300/_build/``.
 """
 from __future__ import annotations
 
@@ -33,8 +34,28 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found (set NVCC or put the CUDA toolkit on PATH)")
 
 
+SPLIT_INST = "fd_split_inst.cu"
+SPLIT_VARIANTS = [(paged, f16, d) for paged in (0, 1) for f16 in (0, 1) for d in (64, 128, 256)]
+
+
 def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def _units():
+    """(source, object name, extra defines) for every translation unit."""
+    units = []
+    for src in _sources():
+        stem = os.path.basename(src)[:-3]
+        if os.path.basename(src) == SPLIT_INST:
+            for paged, f16, d in SPLIT_VARIANTS:
+                defs = [f"-DFD_INST_PAGED={'true' if paged else 'false'}",
+                        f"-DFD_INST_F16={'true' if f16 else 'false'}", f"-DFD_INST_D={d}"]
+                units.append((src, f"{stem}_{'paged' if paged else 'contig'}_{'f16' if f16 else 'bf16'}_d{d}",
+                              defs))
+        else:
+            units.append((src, stem, []))
+    return units
 
 
 def _deps():
@@ -57,9 +78,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     flags = NVCC_FLAGS + list(extra_flags) + (["-Xptxas", "-v"] if verbose else [])
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc] + flags + ["-c", src, "-o", obj]
+    def compile_one(unit):
+        src, stem, defs = unit
+        obj = os.path.join(BUILD, stem + ".o")
+        cmd = [nvcc] + flags + defs + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
@@ -67,8 +89,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             sys.stderr.write(r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        objs = list(ex.map(compile_one, _sources()))
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        objs = list(ex.map(compile_one, _units()))
     tmp = LIB + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs, capture_output=True, text=True)
     if r.returncode != 0:

@@ -21,7 +21,7 @@ namespace {
 
 using namespace fd;
 
-constexpr int kVersion = 10100;   // 1.1.0
+constexpr int kVersion = 10200;   // 1.2.0
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
 struct DeviceInfo {
@@ -72,20 +72,20 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// A rank-3 view {head_dim, Hkv, rows} of a bf16 K or V tensor whose rows are
-// (token, kv head) pairs of 256 bytes; each load is a box of box_rows tokens
-// of one kv head: the whole 128-dim row, or (swizzled) 64 dims of it with the
-// 128-byte swizzle that the tensor-core consumers read.
+// A rank-3 view {head_dim, Hkv, rows} of a 16-bit K or V tensor whose rows
+// are (token, kv head) pairs of 2 head_dim bytes; each load is a box of
+// box_rows tokens of one kv head: the whole row, or (swizzled) one 64-dim
+// part of it with the 128-byte swizzle that the tensor-core consumers read.
 fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
-                        bool swizzled, bool f16)
+                        bool swizzled, bool f16, int d)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return FD_ERR_CUDA;
-    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)hkv * kRowBytes};
-    const cuuint32_t box[3] = {(cuuint32_t)(swizzled ? kHeadDim / 2 : kHeadDim), 1u,
-                               (cuuint32_t)box_rows};
+    const cuuint64_t row_bytes = 2u * (cuuint64_t)d;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {row_bytes, (cuuint64_t)hkv * row_bytes};
+    const cuuint32_t box[3] = {(cuuint32_t)(swizzled ? 64 : d), 1u, (cuuint32_t)box_rows};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                           const_cast<void *>(base), dims,
@@ -95,19 +95,20 @@ fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long r
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
 }
 
-// A rank-4 view {64 dims, rows, 2 halves, Hkv} of the same tensor, so that
-// one box {64, box_rows, 2, 1} carries both 128-byte-swizzled 64-dim halves
-// of box_rows rows of one kv head (laid out half by half in shared memory).
+// A rank-4 view {64 dims, rows, head_dim/64 parts, Hkv} of the same tensor,
+// so that one box {64, box_rows, head_dim/64, 1} carries every
+// 128-byte-swizzled 64-dim part of box_rows rows of one kv head (laid out
+// part by part in shared memory).
 fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
-                           bool f16)
+                           bool f16, int d)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return FD_ERR_CUDA;
-    const cuuint64_t dims[4] = {(cuuint64_t)(kHeadDim / 2), (cuuint64_t)rows, 2u, (cuuint64_t)hkv};
-    const cuuint64_t strides[3] = {(cuuint64_t)hkv * kRowBytes, (cuuint64_t)kRowBytes / 2,
-                                   (cuuint64_t)kRowBytes};
-    const cuuint32_t box[4] = {(cuuint32_t)(kHeadDim / 2), (cuuint32_t)box_rows, 2u, 1u};
+    const cuuint64_t row_bytes = 2u * (cuuint64_t)d;
+    const cuuint64_t dims[4] = {64u, (cuuint64_t)rows, (cuuint64_t)(d / 64), (cuuint64_t)hkv};
+    const cuuint64_t strides[3] = {(cuuint64_t)hkv * row_bytes, 128u, row_bytes};
+    const cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, (cuuint32_t)(d / 64), 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                           const_cast<void *>(base), dims,
@@ -117,10 +118,10 @@ fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long lon
 }
 
 // K and V maps for a call: the tensor-core consumers prefer 4-D maps (one
-// box per tile or page carries both swizzled halves) and fall back to 3-D
-// maps with one box per half if the driver rejects the 4-D view.
+// box per tile or page carries every swizzled part) and fall back to 3-D
+// maps with one box per 64-dim part if the driver rejects the 4-D view.
 fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, const void *v, int hkv,
-                         long long rows, int box_rows, bool mma, bool f16, SplitParams *sp)
+                         long long rows, int box_rows, bool mma, bool f16, int d, SplitParams *sp)
 {
     int rl = 0;
     while ((1 << rl) < box_rows)
@@ -128,15 +129,15 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
     sp->box4d = 0;
     sp->box_rows_log2 = 6;
     if (mma && !(sp->flags & FD_FLAG_NO_4D_BOXES) &&
-        encode_kv_map_4d(tmk, k, hkv, rows, box_rows, f16) == FD_OK &&
-        encode_kv_map_4d(tmv, v, hkv, rows, box_rows, f16) == FD_OK) {
+        encode_kv_map_4d(tmk, k, hkv, rows, box_rows, f16, d) == FD_OK &&
+        encode_kv_map_4d(tmv, v, hkv, rows, box_rows, f16, d) == FD_OK) {
         sp->box4d = 1;
         sp->box_rows_log2 = rl;
         return FD_OK;
     }
     fd_status st;
-    if ((st = encode_kv_map(tmk, k, hkv, rows, box_rows, mma, f16)) != FD_OK ||
-        (st = encode_kv_map(tmv, v, hkv, rows, box_rows, mma, f16)) != FD_OK)
+    if ((st = encode_kv_map(tmk, k, hkv, rows, box_rows, mma, f16, d)) != FD_OK ||
+        (st = encode_kv_map(tmv, v, hkv, rows, box_rows, mma, f16, d)) != FD_OK)
         return st;
     return FD_OK;
 }
@@ -144,6 +145,8 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
 // Checks shared by both entry points.  Returns FD_OK or the status to report.
 fd_status check_common(const void *q, const float *o, const void *ws, int batch, int hq, int hkv,
@@ -155,7 +158,7 @@ fd_status check_common(const void *q, const float *o, const void *ws, int batch,
         return FD_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(o, 16) || !aligned(ws, 256))
         return FD_ERR_INVALID_ARG;
-    if (head_dim != kHeadDim || !supported_group(hq / hkv) || batch > kMaxBatch)
+    if (!supported_head_dim(head_dim) || !supported_group(hq / hkv) || batch > kMaxBatch)
         return FD_ERR_UNSUPPORTED;
     return FD_OK;
 }
@@ -165,6 +168,7 @@ struct CallPlan {
     MergeParams mp;
     SplitLaunch launch;
     int group;
+    int head_dim;
     bool mma;   // tensor-core consumers (GQA groups) instead of CUDA cores
     bool f16;   // IEEE fp16 inputs instead of bf16
 };
@@ -178,11 +182,14 @@ bool use_mma(int group, int page_size, const fd_options *opts)
     return group >= 2 && (page_size == 0 || page_size >= 8);
 }
 
-// Shared-memory plan of the split kernel for `group` and `batch`; fills the
-// offsets and stage count in sp and the byte size in launch.
-fd_status plan_smem(const DeviceInfo &dev, int group, int batch, SplitParams *sp, SplitLaunch *launch)
+// Shared-memory plan of the split kernel for the call's consumers, group,
+// head_dim and batch; fills the offsets and stage count in sp and the byte
+// size in launch.
+fd_status plan_smem(const DeviceInfo &dev, bool mma, int group, int d, int batch, SplitParams *sp,
+                    SplitLaunch *launch)
 {
-    const size_t red = align_up((size_t)kConsumerWarps * group * (kHeadDim + 2) * sizeof(float), 16);
+    const size_t stage_bytes = 2u * kTileTokens * 2u * (size_t)d;   // K and V tiles
+    const size_t red = align_up((size_t)reduction_floats(mma, group, d) * sizeof(float), 16);
     const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
     const size_t misc = 64;
     const size_t per_stage_extra = 2 * 8 + kMetaInts * sizeof(int);   // 2 barriers + metadata
@@ -190,13 +197,13 @@ fd_status plan_smem(const DeviceInfo &dev, int group, int batch, SplitParams *sp
     const size_t avail = (size_t)dev.smem_optin;
     if (avail <= fixed)
         return FD_ERR_UNSUPPORTED;
-    int ns = (int)((avail - fixed) / (kStageBytes + per_stage_extra));
+    int ns = (int)((avail - fixed) / (stage_bytes + per_stage_extra));
     if (ns > kMaxStages)
         ns = kMaxStages;
     if (ns < 2)
         return FD_ERR_UNSUPPORTED;
     sp->num_stages = ns;
-    sp->off_red = (uint32_t)(ns * kStageBytes);
+    sp->off_red = (uint32_t)(ns * stage_bytes);
     sp->off_prefix = (uint32_t)(sp->off_red + red);
     sp->off_bar = (uint32_t)(sp->off_prefix + prefix);
     sp->off_meta = (uint32_t)(sp->off_bar + (2 * ns + 1) * 8);
@@ -208,11 +215,11 @@ fd_status plan_smem(const DeviceInfo &dev, int group, int batch, SplitParams *sp
 
 fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const int32_t *seq_lens_dev,
                     const int32_t *block_table, int batch, int hq, int hkv, int cap, int s_max,
-                    int page_size, int max_blocks, int num_pages, float scale, float *o, float *lse,
-                    void *workspace, const fd_options *opts, fd_stream_t stream)
+                    int head_dim, int page_size, int max_blocks, int num_pages, float scale, float *o,
+                    float *lse, void *workspace, const fd_options *opts, fd_stream_t stream)
 {
     const int group = hq / hkv;
-    const WorkspaceLayout wl = workspace_layout(batch, hkv, group, kHeadDim);
+    const WorkspaceLayout wl = workspace_layout(batch, hkv, group, head_dim);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int num_ctas = opts && opts->num_ctas > 0 ? opts->num_ctas : dev.sms;
     if (num_ctas > kMaxCtas)
@@ -244,9 +251,13 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     sp.timeout_ns = opts && opts->wait_timeout_ns ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     sp.flags = opts ? opts->flags : 0u;
 
+    cp->group = group;
+    cp->head_dim = head_dim;
+    cp->mma = use_mma(group, page_size, opts);
+    cp->f16 = opts && opts->dtype == FD_DTYPE_F16;
     cp->launch.grid = num_ctas;
     cp->launch.stream = reinterpret_cast<cudaStream_t>(stream);
-    fd_status st = plan_smem(dev, group, batch, &sp, &cp->launch);
+    fd_status st = plan_smem(dev, cp->mma, group, head_dim, batch, &sp, &cp->launch);
     if (st != FD_OK)
         return st;
 
@@ -260,9 +271,6 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     mp.hq = hq;
     mp.hkv = hkv;
     mp.num_ctas = num_ctas;
-    cp->group = group;
-    cp->mma = use_mma(group, page_size, opts);
-    cp->f16 = opts && opts->dtype == FD_DTYPE_F16;
     return FD_OK;
 }
 
@@ -274,18 +282,12 @@ fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUte
     cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_end_event) : nullptr;
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    cudaError_t e;
-    if (paged)
-        e = cp.f16 ? launch_split_paged_f16(cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch)
-                   : launch_split_paged_bf16(cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch);
-    else
-        e = cp.f16 ? launch_split_contig_f16(cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch)
-                   : launch_split_contig_bf16(cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch);
+    cudaError_t e = launch_split(paged, cp.f16, cp.head_dim, cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch);
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    e = launch_merge(cp.group, cp.mp, cp.sp.batch * cp.sp.hkv, stream);
+    e = launch_merge(cp.group, cp.head_dim, cp.mp, cp.sp.batch * cp.sp.hkv, stream);
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
     return FD_OK;
@@ -343,13 +345,13 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
         return st;
     CallPlan cp;
     st = fill_plan(&cp, dev, q, seq_lens_dev, nullptr, batch, num_q_heads, num_kv_heads, s_max, s_max,
-                   0, 0, 0, scale, o, lse, workspace, opts, stream);
+                   head_dim, 0, 0, 0, scale, o, lse, workspace, opts, stream);
     if (st != FD_OK)
         return st;
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
-    if ((st = encode_kv_maps(&tmk, &tmv, k, v, num_kv_heads, rows, kTileTokens, cp.mma, cp.f16, &cp.sp)) !=
-        FD_OK)
+    if ((st = encode_kv_maps(&tmk, &tmv, k, v, num_kv_heads, rows, kTileTokens, cp.mma, cp.f16, head_dim,
+                             &cp.sp)) != FD_OK)
         return st;
     return run(cp, false, tmk, tmv, opts);
 }
@@ -391,14 +393,15 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
         return st;
     CallPlan cp;
     st = fill_plan(&cp, dev, q, seq_lens_dev, block_table, batch, num_q_heads, num_kv_heads, (int)cap, 0,
-                   page_size, max_blocks_per_seq, num_pages, scale, o, lse, workspace, opts, stream);
+                   head_dim, page_size, max_blocks_per_seq, num_pages, scale, o, lse, workspace, opts,
+                   stream);
     if (st != FD_OK)
         return st;
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)num_pages * page_size;
     const int box = page_size < kTileTokens ? page_size : kTileTokens;
     if ((st = encode_kv_maps(&tmk, &tmv, k_pages, v_pages, num_kv_heads, rows, box, cp.mma, cp.f16,
-                             &cp.sp)) != FD_OK)
+                             head_dim, &cp.sp)) != FD_OK)
         return st;
     return run(cp, true, tmk, tmv, opts);
 }

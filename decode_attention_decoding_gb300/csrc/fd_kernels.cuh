@@ -10,17 +10,17 @@
 //     through the block table) that complete on the stage's "full" mbarrier;
 //   * warps 0..7 are consumers (CUDA-core variant shown here; the
 //     tensor-core variant for GQA groups is described at split_consumer_mma):
-//     warp w reads rows 8w..8w+7 of every tile, two
-//     rows at a time (one per half-warp; each lane holds 8 of the 128 head
-//     dimensions, read as one 16-byte shared load).  For every query head of
-//     the kv head's GQA group it forms the score q.k in fp32 (packed
-//     fp32x2 FMAs, a 16-lane shuffle reduction), keeps an online softmax in
+//     warp w reads rows 8w..8w+7 of every tile, 32/(D/8) rows at a time (a
+//     row spans D/8 lanes; each lane holds 8 of the D head dimensions, read
+//     as one 16-byte shared load).  For every query head of the kv head's
+//     GQA group it forms the score q.k in fp32 (packed fp32x2 FMAs, a
+//     shuffle reduction over the row's lanes), keeps an online softmax in
 //     the log2 domain (running max m, running sum l, fp32 accumulator
 //     rescaled by 2^(m_old - m_new) every tile, as in the handbook's
 //     FlashAttention section), and accumulates p * V.  It then releases the
 //     stage on its "empty" mbarrier -- there is no CTA-wide barrier per tile.
 //   * At the last tile of a segment (request, kv head) within the CTA, the
-//     consumer warps merge their 16 half-warp states through shared memory
+//     consumer warps merge their per-row-group states through shared memory
 //     and write either the final O and natural-log LSE (the CTA saw the whole
 //     segment) or a normalised partial O and its LSE (lse = m ln2 + ln l).
 // Merge kernel ("pass 2", section 2 of the sm120 article): one CTA per
@@ -33,28 +33,45 @@
 
 namespace fd {
 
-constexpr int kHeadDim = 128;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kSplitThreads = kConsumerThreads + 32;
-constexpr int kRowBytes = kHeadDim * 2;                 // one bf16 K or V row
-constexpr int kTileBytes = kTileTokens * kRowBytes;     // 16 KB
-constexpr int kStageBytes = 2 * kTileBytes;             // K tile + V tile
-constexpr int kHalfBytes = kTileBytes / 2;              // 64 tokens x 64 dims (swizzled layout)
-constexpr int kMaxStages = 6;
+constexpr int kPairs = kConsumerWarps / 2;
+constexpr int kPartBytes = kTileTokens * 128;           // 64 rows x 64 dims: one swizzled part
+constexpr int kMaxStages = 8;
 constexpr int kMetaInts = 8;
 constexpr int kRowsPerWarp = kTileTokens / kConsumerWarps;   // 8
-constexpr int kRowsPerHalf = kRowsPerWarp / 2;               // 4
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
-static_assert(kRowsPerWarp % 2 == 0, "two rows per warp step");
+// Sizes that follow from the head dimension D (64, 128 or 256).
+template <int D>
+struct HeadDim {
+    static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
+    static constexpr int kRowBytes = D * 2;                   // one 16-bit K or V row
+    static constexpr int kTileBytes = kTileTokens * kRowBytes;
+    static constexpr int kStageBytes = 2 * kTileBytes;        // K tile + V tile
+    static constexpr int kParts = D / 64;                     // 128-byte swizzled parts of a row
+    static constexpr int kLanesPerRow = D / 8;                // CUDA cores: 8 dims per lane
+    static constexpr int kRowsPerStep = 32 / kLanesPerRow;    // rows a warp reads at once
+    static constexpr int kRowsPerGroup = kRowsPerWarp / kRowsPerStep;
+    static constexpr int kKSteps = D / 16;                    // tensor cores: k-steps of q.K^T
+    static constexpr int kDimTilesPerWarp = D / 32;           // P.V dim tiles per warp of a pair
+};
+
+// Floats of the shared reduction region (partial O, m, and the weight sums)
+// for one segment: one state per warp on CUDA cores, one per warp pair (with
+// two weight sums) on tensor cores.
+__host__ __device__ constexpr int reduction_floats(bool mma, int group, int d)
+{
+    return mma ? kPairs * group * (d + 3) : kConsumerWarps * group * (d + 2);
+}
 
 // Per-tile metadata flags, written by the producer into shared memory.
 enum : int { kFirstInCta = 1, kLastInCta = 2, kOwnSegment = 4 };
 
 struct SplitParams {
-    const uint16_t *q;            // [B, Hq, D] bf16 bits
+    const uint16_t *q;            // [B, Hq, D] bf16 or fp16 bits
     const int32_t *seq_lens;      // [B] device, or null (every length = cap)
     const int32_t *block_table;   // [B, max_blocks] (paged only)
     float *o;                     // [B, Hq, D]
@@ -174,7 +191,7 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
 
 // ------------------------------------------------------------------ producer
 
-template <bool PAGED, bool SW128>
+template <bool PAGED, bool SW128, int D>
 __device__ __forceinline__ void split_producer(const SplitParams &p, const CUtensorMap *tmk,
                                                const CUtensorMap *tmv, uint32_t stage0,
                                                const int *prefix, int *meta, uint32_t full0,
@@ -191,9 +208,10 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     const uint64_t policy = l2_policy_evict_first();
     const int NS = p.num_stages;
     const bool starve = (p.flags & 1u) && blockIdx.x == 0;
+    using HD = HeadDim<D>;
     // Boxes per (tile or page): K and V, each whole (plain or 4-D swizzled)
-    // or as two swizzled 64-dim halves.
-    const int box_log2 = (SW128 && !p.box4d) ? 2 : 1;
+    // or as D/64 swizzled 64-dim parts.
+    const int box_log2 = (SW128 && !p.box4d) ? 1 + (HD::kParts == 4 ? 2 : HD::kParts - 1) : 1;
     const int kBoxes = 1 << box_log2;
     const int page_log2 = p.page_log2;   // pages under 64 tokens are powers of two
 
@@ -239,17 +257,19 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
         }
         return e;
     };
-    // Box `box` (0..kBoxes-1) of the tile's K/V, `koff` bytes into each half
-    // (swizzled layout) or `2 koff` bytes into each tile (plain layout).
-    auto load_box = [&](int box, uint32_t kdst, uint32_t vdst, uint32_t full, uint32_t koff, int row) {
-        if (SW128 && p.box4d) {   // box 0: K, box 1: V; both halves in one box
-            tma_load_4d(((box & 1) ? vdst : kdst) + 2 * koff, (box & 1) ? tmv : tmk, full, 0, row, 0, h,
-                        policy);
-        } else if constexpr (SW128) {
-            const uint32_t dst = ((box & 2) ? vdst : kdst) + (box & 1) * kHalfBytes + koff;
-            tma_load_3d(dst, (box & 2) ? tmv : tmk, full, (box & 1) * (kHeadDim / 2), h, row, policy);
+    // Box `box` (0..kBoxes-1) of the tile's K/V for the rows starting at tile
+    // row r0 (a page's first row, or 0).
+    auto load_box = [&](int box, uint32_t kdst, uint32_t vdst, uint32_t full, int r0, int row) {
+        if (SW128 && p.box4d) {   // box 0: K, box 1: V; all parts in one box
+            tma_load_4d(((box & 1) ? vdst : kdst) + r0 * HD::kRowBytes, (box & 1) ? tmv : tmk, full, 0, row,
+                        0, h, policy);
+        } else if constexpr (SW128) {   // one box per 64-dim part
+            const int part = box & (HD::kParts - 1);
+            const bool is_v = box >= HD::kParts;
+            const uint32_t dst = (is_v ? vdst : kdst) + part * kPartBytes + r0 * 128;
+            tma_load_3d(dst, is_v ? tmv : tmk, full, part * 64, h, row, policy);
         } else {
-            const uint32_t dst = ((box & 1) ? vdst : kdst) + 2 * koff;
+            const uint32_t dst = ((box & 1) ? vdst : kdst) + r0 * HD::kRowBytes;
             tma_load_3d(dst, (box & 1) ? tmv : tmk, full, 0, h, row, policy);
         }
     };
@@ -277,8 +297,8 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             flags |= kOwnSegment;
 
         const uint32_t full = full0 + 8 * s;
-        const uint32_t kdst = stage0 + s * kStageBytes;
-        const uint32_t vdst = kdst + kTileBytes;
+        const uint32_t kdst = stage0 + s * HD::kStageBytes;
+        const uint32_t vdst = kdst + HD::kTileBytes;
         const uint32_t extra = (starve && issued == 0) ? 256u : 0u;
         const int P = p.page_size;
         const bool small_pages = PAGED && P < kTileTokens;
@@ -291,7 +311,7 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             m[3] = nvalid;
             m[4] = flags;
             m[5] = b * p.hkv + h;
-            const uint32_t bytes = small_pages ? 2u * need * P * kRowBytes : (uint32_t)(2 * kTileBytes);
+            const uint32_t bytes = small_pages ? 2u * need * P * HD::kRowBytes : (uint32_t)(2 * HD::kTileBytes);
             mbar_arrive_expect_tx(full, bytes + extra);
         }
         __syncwarp();
@@ -313,7 +333,7 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
                 const int k = item >> box_log2;
                 const int phys = window_entry(pg0 + (item < items ? k : (i0 >> box_log2)));
                 if (item < items)
-                    load_box(item & (kBoxes - 1), kdst, vdst, full, (k * P) * (kRowBytes / 2), phys * P);
+                    load_box(item & (kBoxes - 1), kdst, vdst, full, k * P, phys * P);
             }
         }
         __syncwarp();
@@ -350,15 +370,15 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
 // the sum of the weights that multiplied V (red_l); the LSE uses the sum of
 // the exact fp32 weights (red_lt), which differs only when P was rounded to a
 // 16-bit type for the tensor-core product.
-template <int G, int NSTATE>
+template <int G, int NSTATE, int D>
 __device__ __forceinline__ void combine_and_write(const SplitParams &p, const float *red_acc,
                                                   const float *red_m, const float *red_l,
                                                   const float *red_lt, int ctid, int b, int h, int u,
                                                   bool own)
 {
     const int slot = u + (int)blockIdx.x;
-    for (int idx = ctid; idx < G * kHeadDim; idx += kConsumerThreads) {
-        const int g = idx / kHeadDim, d = idx % kHeadDim;
+    for (int idx = ctid; idx < G * D; idx += kConsumerThreads) {
+        const int g = idx / D, d = idx % D;
         float M = kNegInf;
 #pragma unroll
         for (int w = 0; w < NSTATE; ++w)
@@ -370,36 +390,40 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
             const float wt = (mw == kNegInf) ? 0.f : exp2_approx(mw - M);
             lsum += wt * red_l[w * G + g];
             ltrue += wt * red_lt[w * G + g];
-            o += wt * red_acc[(w * G + g) * kHeadDim + d];
+            o += wt * red_acc[(w * G + g) * D + d];
         }
         const float out = lsum > 0.f ? o / lsum : 0.f;
         const float lse_v = ltrue > 0.f ? (M + log2f(ltrue)) * kLn2 : kNegInf;
         if (own) {
             const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
-            p.o[row * kHeadDim + d] = out;
+            p.o[row * D + d] = out;
             if (d == 0 && p.lse)
                 p.lse[row] = lse_v;
         } else {
-            p.ws_o[((size_t)slot * G + g) * kHeadDim + d] = out;
+            p.ws_o[((size_t)slot * G + g) * D + d] = out;
             if (d == 0)
                 p.ws_lse[(size_t)slot * G + g] = lse_v;
         }
     }
 }
 
-template <int G, bool F16>
+template <int G, bool F16, int D>
 __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *smem, uint32_t stage0,
                                                const int *meta, uint32_t full0, uint32_t empty0,
                                                uint32_t cbar, volatile int *abort_flag, int t_begin,
                                                int t_end, int cw, int lane)
 {
+    using HD = HeadDim<D>;
+    constexpr int LPR = HD::kLanesPerRow, RPS = HD::kRowsPerStep, RPG = HD::kRowsPerGroup;
     const int NS = p.num_stages;
-    const int half = lane >> 4, li = lane & 15;
+    const int sub = lane / LPR, li = lane % LPR;   // row slot within a warp step, lane within the row
     float *red_acc = reinterpret_cast<float *>(smem + p.off_red);   // [warps][G][D]
-    float *red_m = red_acc + kConsumerWarps * G * kHeadDim;          // [warps][G]
+    float *red_m = red_acc + kConsumerWarps * G * D;                 // [warps][G]
     float *red_l = red_m + kConsumerWarps * G;                       // [warps][G]
     const int ctid = cw * 32 + lane;
-    constexpr int kSub = G >= 8 ? 1 : (G >= 4 ? 2 : kRowsPerHalf);   // rows per online update
+    // rows per online update (fewer live scores for large G)
+    constexpr int kSub0 = G >= 8 ? 1 : (G >= 4 ? 2 : RPG);
+    constexpr int kSub = kSub0 < RPG ? kSub0 : RPG;
 
     float2 qf[G][4];
     float2 acc[G][4];
@@ -438,7 +462,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const uint16_t *qp = p.q + ((size_t)b * p.hq + (size_t)h * G + g) * kHeadDim + li * 8;
+                const uint16_t *qp = p.q + ((size_t)b * p.hq + (size_t)h * G + g) * D + li * 8;
                 const uint4 raw = ldg128_nc(qp);
                 qf[g][0] = mul2(x2_to_float2<F16>(raw.x), c2);
                 qf[g][1] = mul2(x2_to_float2<F16>(raw.y), c2);
@@ -447,18 +471,18 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             }
         }
 
-        const uint32_t kbase = stage0 + s * kStageBytes + li * 16;
-        const uint32_t vbase = kbase + kTileBytes;
+        const uint32_t kbase = stage0 + s * HD::kStageBytes + li * 16;
+        const uint32_t vbase = kbase + HD::kTileBytes;
 
-        // Rows of this half-warp, kSub at a time (fewer live scores for large G).
+        // Rows of this lane group, kSub at a time.
 #pragma unroll
-        for (int r0 = 0; r0 < kRowsPerHalf; r0 += kSub) {
+        for (int r0 = 0; r0 < RPG; r0 += kSub) {
             // Scores (log2 units).
             float sc[kSub][G];
 #pragma unroll
             for (int r = 0; r < kSub; ++r) {
-                const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
-                const uint4 kw = lds128(kbase + row * kRowBytes);
+                const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
+                const uint4 kw = lds128(kbase + row * HD::kRowBytes);
                 const float2 k0 = x2_to_float2<F16>(kw.x), k1 = x2_to_float2<F16>(kw.y);
                 const float2 k2 = x2_to_float2<F16>(kw.z), k3 = x2_to_float2<F16>(kw.w);
 #pragma unroll
@@ -475,10 +499,9 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     float x = sc[r][g];
-                    x += __shfl_xor_sync(0xffffffffu, x, 8);
-                    x += __shfl_xor_sync(0xffffffffu, x, 4);
-                    x += __shfl_xor_sync(0xffffffffu, x, 2);
-                    x += __shfl_xor_sync(0xffffffffu, x, 1);
+#pragma unroll
+                    for (int off = LPR / 2; off; off >>= 1)
+                        x += __shfl_xor_sync(0xffffffffu, x, off);
                     sc[r][g] = x;
                 }
 
@@ -489,7 +512,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                 float tile_max = kNegInf;
 #pragma unroll
                 for (int r = 0; r < kSub; ++r) {
-                    const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
+                    const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
                     if (row < nvalid)
                         tile_max = fmaxf(tile_max, sc[r][g]);
                 }
@@ -498,7 +521,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                 float psum = 0.f;
 #pragma unroll
                 for (int r = 0; r < kSub; ++r) {
-                    const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
+                    const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
                     pr[r][g] = (row < nvalid) ? exp2_approx(sc[r][g] - m_new) : 0.f;
                     psum += pr[r][g];
                 }
@@ -513,9 +536,9 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             // acc += p * V
 #pragma unroll
             for (int r = 0; r < kSub; ++r) {
-                const int row = cw * kRowsPerWarp + 2 * (r0 + r) + half;
+                const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
                 if (row < nvalid) {
-                    const uint4 vw = lds128(vbase + row * kRowBytes);
+                    const uint4 vw = lds128(vbase + row * HD::kRowBytes);
                     const float2 v0 = x2_to_float2<F16>(vw.x), v1 = x2_to_float2<F16>(vw.y);
                     const float2 v2 = x2_to_float2<F16>(vw.z), v3 = x2_to_float2<F16>(vw.w);
 #pragma unroll
@@ -534,30 +557,33 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             mbar_arrive(empty0 + 8 * s);
 
         if (flags & kLastInCta) {
-            // 1. merge the two half-warp states of this warp
+            // 1. merge the states of the warp's lane groups (rows of one step)
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float mo = __shfl_xor_sync(0xffffffffu, m[g], 16);
-                const float lo = __shfl_xor_sync(0xffffffffu, l[g], 16);
-                const float mn = fmaxf(m[g], mo);
-                const float a_self = (m[g] == kNegInf) ? 0.f : exp2_approx(m[g] - mn);
-                const float a_other = (mo == kNegInf) ? 0.f : exp2_approx(mo - mn);
-                l[g] = l[g] * a_self + lo * a_other;
-                const float2 s2 = make_float2(a_self, a_self), o2 = make_float2(a_other, a_other);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float2 other;
-                    other.x = __shfl_xor_sync(0xffffffffu, acc[g][c].x, 16);
-                    other.y = __shfl_xor_sync(0xffffffffu, acc[g][c].y, 16);
-                    acc[g][c] = fma2(acc[g][c], s2, mul2(other, o2));
-                }
-                m[g] = mn;
-            }
-            // 2. publish the warp state
-            if (half == 0) {
+            for (int off = LPR; off < 32; off <<= 1) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    float4 *dst = reinterpret_cast<float4 *>(red_acc + (cw * G + g) * kHeadDim + li * 8);
+                    const float mo = __shfl_xor_sync(0xffffffffu, m[g], off);
+                    const float lo = __shfl_xor_sync(0xffffffffu, l[g], off);
+                    const float mn = fmaxf(m[g], mo);
+                    const float a_self = (m[g] == kNegInf) ? 0.f : exp2_approx(m[g] - mn);
+                    const float a_other = (mo == kNegInf) ? 0.f : exp2_approx(mo - mn);
+                    l[g] = l[g] * a_self + lo * a_other;
+                    const float2 s2 = make_float2(a_self, a_self), o2 = make_float2(a_other, a_other);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float2 other;
+                        other.x = __shfl_xor_sync(0xffffffffu, acc[g][c].x, off);
+                        other.y = __shfl_xor_sync(0xffffffffu, acc[g][c].y, off);
+                        acc[g][c] = fma2(acc[g][c], s2, mul2(other, o2));
+                    }
+                    m[g] = mn;
+                }
+            }
+            // 2. publish the warp state
+            if (sub == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float4 *dst = reinterpret_cast<float4 *>(red_acc + (cw * G + g) * D + li * 8);
                     dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
                     dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
                 }
@@ -574,8 +600,8 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                 return;
             }
             // 3. combine the warps and write the segment's result
-            combine_and_write<G, kConsumerWarps>(p, red_acc, red_m, red_l, red_l, ctid, b, h, u,
-                                                 (flags & kOwnSegment) != 0);
+            combine_and_write<G, kConsumerWarps, D>(p, red_acc, red_m, red_l, red_l, ctid, b, h, u,
+                                                    (flags & kOwnSegment) != 0);
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
@@ -610,39 +636,41 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 // product and the running sum l adds up exactly those rounded weights.
 //
 // Warps 2i and 2i+1 take tokens 16i..16i+15 of every tile; both form the
-// scores (so each holds the softmax state), and for P.V warp 2i covers dims
-// 0..63 and warp 2i+1 dims 64..127.
+// scores (so each holds the softmax state), and for P.V warp 2i covers the
+// first half of the head dimension and warp 2i+1 the second.
 
-// Byte address of 16-byte chunk `chunk` (0..15) of `row` in a swizzled tile
-// made of boxes of 2^rl rows, each box laid out [64-dim half][row][128 B].
-// With rl = 6 (one 64-row box per half) this is two 8 KB halves.
+// Byte address of 16-byte chunk `chunk` (0 .. D/8-1) of `row` in a swizzled
+// tile made of boxes of 2^rl rows, each box laid out [64-dim part][row][128 B].
+// With rl = 6 (one 64-row box per part) the tile is D/64 parts of 8 KB.
+template <int D>
 __device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk, int rl)
 {
     const int rb = row >> rl, rr = row & ((1 << rl) - 1);
-    return tile + ((rb << (rl + 1)) + ((chunk >> 3) << rl) + rr) * (kRowBytes / 2) +
+    return tile + ((((rb * HeadDim<D>::kParts) + (chunk >> 3)) << rl) + rr) * 128 +
            (((chunk & 7) ^ (row & 7)) << 4);
 }
 
-template <int G, bool F16>
+template <int G, bool F16, int D>
 __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t *smem, uint32_t stage0,
                                                    const int *meta, uint32_t full0, uint32_t empty0,
                                                    uint32_t cbar, volatile int *abort_flag, int t_begin,
                                                    int t_end, int cw, int lane)
 {
     static_assert(G >= 1 && G <= 8, "one n8 tile of query heads");
-    constexpr int kPairs = kConsumerWarps / 2;
+    using HD = HeadDim<D>;
+    constexpr int KS = HD::kKSteps, DT = HD::kDimTilesPerWarp;
     const int NS = p.num_stages;
     const int pair = cw >> 1, dhalf = cw & 1;
     const int grp = lane >> 2, qd = lane & 3;   // mma fragment coordinates
     const int tok0 = pair * 16;
     const int rl = p.box_rows_log2;
     float *red_acc = reinterpret_cast<float *>(smem + p.off_red);   // [pairs][G][D]
-    float *red_m = red_acc + kConsumerWarps * G * kHeadDim;          // [pairs][G]
-    float *red_l = red_m + kConsumerWarps * G;                       // [pairs][G]
+    float *red_m = red_acc + kPairs * G * D;                         // [pairs][G]
+    float *red_l = red_m + kPairs * G;                               // [2 pairs][G]: l, then lt
     const int ctid = cw * 32 + lane;
 
-    uint32_t qb[8][2];         // Q^T B-fragments, one pair per 16-dim k-step
-    float acc[4][4];           // O^T fragments of this warp's 4 dim tiles
+    uint32_t qb[KS][2];        // Q^T B-fragments, one pair per 16-dim k-step
+    float acc[DT][4];          // O^T fragments of this warp's D/32 dim tiles
     // heads 2 qd and 2 qd + 1, this lane's tokens only: l sums the 16-bit
     // rounded weights that multiply V, lt the exact fp32 weights (for the LSE)
     float m[2], l[2], lt[2];
@@ -654,7 +682,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             lt[j] = 0.f;
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < DT; ++i)
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 acc[i][c] = 0.f;
@@ -667,7 +695,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
     };
     reset();
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
+    for (int ks = 0; ks < KS; ++ks)
         qb[ks][0] = qb[ks][1] = 0u;
 
     int s = 0;
@@ -684,26 +712,26 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             // B[k = d][n = head]: lane holds head `grp`, dims 16 ks + 2 qd (+1) and (+8, +9).
             if (grp < G) {
                 const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                    p.q + ((size_t)b * p.hq + (size_t)h * G + grp) * kHeadDim);
+                    p.q + ((size_t)b * p.hq + (size_t)h * G + grp) * D);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
+                for (int ks = 0; ks < KS; ++ks) {
                     qb[ks][0] = __ldg(qrow + ks * 8 + qd);
                     qb[ks][1] = __ldg(qrow + ks * 8 + 4 + qd);
                 }
             }
         }
 
-        const uint32_t ktile = stage0 + s * kStageBytes;
-        const uint32_t vtile = ktile + kTileBytes;
+        const uint32_t ktile = stage0 + s * HD::kStageBytes;
+        const uint32_t vtile = ktile + HD::kTileBytes;
 
         // S^T = K . Q^T for tokens tok0 .. tok0 + 15 (fragment rows grp and grp + 8).
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
         {
             const int row = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
+            for (int ks = 0; ks < KS; ++ks) {
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(sw128_addr(ktile, row, 2 * ks + (lane >> 4), rl), a0, a1, a2, a3);
+                ldmatrix_x4(sw128_addr<D>(ktile, row, 2 * ks + (lane >> 4), rl), a0, a1, a2, a3);
                 mma_16816<F16>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
         }
@@ -746,27 +774,28 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         // tensor core would form 0 * NaN: zero this warp's half of them.
         const bool ragged = nvalid < tok0 + 16;
         if (ragged) {
+            constexpr int kChunks = D / 16;   // 16-byte chunks in half a row
             const int first = nvalid > tok0 ? nvalid : tok0;
-            for (int idx = lane; idx < (tok0 + 16 - first) * 8; idx += 32) {
-                // whole 128-byte half-row: the chunk order inside it does not matter
-                const uint32_t a = sw128_addr(vtile, first + (idx >> 3), dhalf * 8 + (idx & 7), rl);
+            for (int idx = lane; idx < (tok0 + 16 - first) * kChunks; idx += 32) {
+                const uint32_t a = sw128_addr<D>(vtile, first + idx / kChunks,
+                                                 dhalf * kChunks + idx % kChunks, rl);
                 asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
             }
             __syncwarp();
         }
 
-        // O^T = alpha O^T + V^T . P^T over this warp's 64 dims.
+        // O^T = alpha O^T + V^T . P^T over this warp's D/2 dims.
         {
             const int vrow = tok0 + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < DT; ++i) {
                 acc[i][0] *= alpha[0];
                 acc[i][1] *= alpha[1];
                 acc[i][2] *= alpha[0];
                 acc[i][3] *= alpha[1];
-                const int dt = dhalf * 4 + i;   // 16-dim tile index
+                const int dt = dhalf * DT + i;   // 16-dim tile index
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(sw128_addr(vtile, vrow, 2 * dt + ((lane >> 3) & 1), rl), a0, a1, a2,
+                ldmatrix_x4_trans(sw128_addr<D>(vtile, vrow, 2 * dt + ((lane >> 3) & 1), rl), a0, a1, a2,
                                   a3);
                 mma_16816<F16>(acc[i], a0, a1, a2, a3, pb0, pb1);
             }
@@ -798,10 +827,10 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                         red_l[(kPairs + pair) * G + head] = lt[j];   // exact sums after the pairs' slots
                     }
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int d = (dhalf * 4 + i) * 16 + grp;
-                        red_acc[(pair * G + head) * kHeadDim + d] = acc[i][j];
-                        red_acc[(pair * G + head) * kHeadDim + d + 8] = acc[i][j + 2];
+                    for (int i = 0; i < DT; ++i) {
+                        const int d = (dhalf * DT + i) * 16 + grp;
+                        red_acc[(pair * G + head) * D + d] = acc[i][j];
+                        red_acc[(pair * G + head) * D + d + 8] = acc[i][j + 2];
                     }
                 }
             }
@@ -809,8 +838,8 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                 give_up();
                 return;
             }
-            combine_and_write<G, kPairs>(p, red_acc, red_m, red_l, red_l + kPairs * G, ctid, b, h, u,
-                                         (flags & kOwnSegment) != 0);
+            combine_and_write<G, kPairs, D>(p, red_acc, red_m, red_l, red_l + kPairs * G, ctid, b, h, u,
+                                            (flags & kOwnSegment) != 0);
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
@@ -826,7 +855,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 
 // ------------------------------------------------------------------ kernels
 
-template <int G, bool PAGED, bool MMA, bool F16>
+template <int G, bool PAGED, bool MMA, bool F16, int D>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv)
@@ -868,21 +897,21 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         return;
     volatile int *abort_flag = misc;
     if (warp == kConsumerWarps)
-        split_producer<PAGED, MMA>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
-                                   t_begin, t_end, lane);
+        split_producer<PAGED, MMA, D>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
+                                      t_begin, t_end, lane);
     else if constexpr (MMA)
-        split_consumer_mma<G, F16>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag,
-                              t_begin, t_end, warp, lane);
+        split_consumer_mma<G, F16, D>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin,
+                                      t_end, warp, lane);
     else
-        split_consumer<G, F16>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag,
-                          t_begin, t_end, warp, lane);
+        split_consumer<G, F16, D>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin, t_end,
+                                  warp, lane);
 }
 
 // One CTA per (segment, query head of its group); thread d owns output dim d.
 // The partials' log-sum-exps and merge weights are staged in shared memory
 // so each output needs only one pass over the partial rows.
-template <int G>
-__global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__ MergeParams p)
+template <int G, int D>
+__global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeParams p)
 {
     __shared__ float s_w[kMaxCtas];
     __shared__ float s_lse;
@@ -894,7 +923,7 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__
     const int pb = p.ws_prefix[b], pe = p.ws_prefix[b + 1], T = p.ws_prefix[p.batch];
     const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
     if (pe == pb) {   // empty request: O = 0, LSE = -inf
-        p.o[row * kHeadDim + d] = 0.f;
+        p.o[row * D + d] = 0.f;
         if (d == 0 && p.lse)
             p.lse[row] = kNegInf;
         return;
@@ -906,13 +935,13 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__
         return;   // one CTA saw the whole segment and wrote it
     const int n = c1 - c0 + 1;
     float lmax = kNegInf;
-    for (int i = d; i < n; i += kHeadDim) {
+    for (int i = d; i < n; i += D) {
         const float v = p.ws_lse[(size_t)(u + c0 + i) * G + g];
         s_w[i] = v;
         lmax = fmaxf(lmax, v);
     }
     // block max, then block sum of exp(lse_i - max): warp shuffles + shared memory
-    __shared__ float s_red[kHeadDim / 32];
+    __shared__ float s_red[D / 32];
 #pragma unroll
     for (int off = 16; off; off >>= 1)
         lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
@@ -921,11 +950,11 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__
     __syncthreads();
     float M = s_red[0];
 #pragma unroll
-    for (int w = 1; w < kHeadDim / 32; ++w)
+    for (int w = 1; w < D / 32; ++w)
         M = fmaxf(M, s_red[w]);
     __syncthreads();
     float sum = 0.f;
-    for (int i = d; i < n; i += kHeadDim)
+    for (int i = d; i < n; i += D)
         sum += expf(s_w[i] - M);
 #pragma unroll
     for (int off = 16; off; off >>= 1)
@@ -936,19 +965,19 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__
     if (d == 0) {
         float S = 0.f;
 #pragma unroll
-        for (int w = 0; w < kHeadDim / 32; ++w)
+        for (int w = 0; w < D / 32; ++w)
             S += s_red[w];
         s_lse = M + logf(S);
     }
     __syncthreads();
     const float lse = s_lse;
-    for (int i = d; i < n; i += kHeadDim)
+    for (int i = d; i < n; i += D)
         s_w[i] = expf(s_w[i] - lse);
     __syncthreads();
     // several partial rows in flight per thread: the loop is latency-bound
     float acc = 0.f;
-    const float *src = p.ws_o + ((size_t)(u + c0) * G + g) * kHeadDim + d;
-    const size_t stride = (size_t)G * kHeadDim;
+    const float *src = p.ws_o + ((size_t)(u + c0) * G + g) * D + d;
+    const size_t stride = (size_t)G * D;
     int i = 0;
     for (; i + 4 <= n; i += 4) {
         const float x0 = src[(size_t)i * stride], x1 = src[(size_t)(i + 1) * stride];
@@ -957,7 +986,7 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(const __grid_constant__
     }
     for (; i < n; ++i)
         acc += src[(size_t)i * stride] * s_w[i];
-    p.o[row * kHeadDim + d] = acc;
+    p.o[row * D + d] = acc;
     if (d == 0 && p.lse)
         p.lse[row] = lse;
 }

@@ -17,30 +17,13 @@ struct SplitLaunch {
     cudaStream_t stream;
 };
 
-// Split kernel with CUDA-core consumers on bf16 inputs; K/V tensor maps
-// without swizzle (used by the no-workspace entry point).  Returns
-// cudaErrorInvalidValue for an unsupported group size.
-cudaError_t launch_split_contig(int group, const SplitParams &p, const CUtensorMap &tmk,
-                                const CUtensorMap &tmv, const SplitLaunch &cfg);
-
-// Any variant: layout (paged), consumers (mma: tensor cores for group 2, 4
-// or 8, with swizzled K/V maps), input element type (f16: IEEE fp16, else
-// bf16).  One translation unit per (layout, element type) defines it.
-cudaError_t launch_split_contig_bf16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
-                                     const CUtensorMap &tmv, const SplitLaunch &cfg);
-cudaError_t launch_split_contig_f16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
-                                    const CUtensorMap &tmv, const SplitLaunch &cfg);
-cudaError_t launch_split_paged_bf16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
-                                    const CUtensorMap &tmv, const SplitLaunch &cfg);
-cudaError_t launch_split_paged_f16(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
-                                   const CUtensorMap &tmv, const SplitLaunch &cfg);
-
 // LSE merge of the split partials; grid = number of segments (requests x kv
 // heads).  Launched as a programmatic dependent of the split kernel.
-cudaError_t launch_merge(int group, const MergeParams &p, int grid, cudaStream_t stream);
+// Returns cudaErrorInvalidValue for an unsupported group size or head_dim.
+cudaError_t launch_merge(int group, int head_dim, const MergeParams &p, int grid, cudaStream_t stream);
 
 // Shared by the split translation units.
-template <int G, bool PAGED, bool MMA, bool F16>
+template <int G, bool PAGED, bool MMA, bool F16, int D>
 cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const SplitLaunch &c)
 {
@@ -53,7 +36,7 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
         return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(split_kernel<G, PAGED, MMA, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(split_kernel<G, PAGED, MMA, F16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)c.smem_optin);
         if (e != cudaSuccess)
             return e;
@@ -71,28 +54,59 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
     cfg.stream = c.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, MMA, F16>, p, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, MMA, F16, D>, p, tmk, tmv);
 }
 
-template <bool PAGED, bool F16>
-cudaError_t launch_split_group(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
-                               const CUtensorMap &tmv, const SplitLaunch &c)
+// One split-kernel variant per (layout, element type, head_dim): consumers
+// on tensor cores (mma: group 2, 4 or 8, swizzled K/V maps) or CUDA cores
+// (any group).  Returns cudaErrorInvalidValue for an unsupported group.
+template <bool PAGED, bool F16, int D>
+cudaError_t launch_split_variant(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
+                                 const CUtensorMap &tmv, const SplitLaunch &c)
 {
     if (mma) {
         switch (group) {
-        case 2: return launch_split_t<2, PAGED, true, F16>(p, tmk, tmv, c);
-        case 4: return launch_split_t<4, PAGED, true, F16>(p, tmk, tmv, c);
-        case 8: return launch_split_t<8, PAGED, true, F16>(p, tmk, tmv, c);
+        case 2: return launch_split_t<2, PAGED, true, F16, D>(p, tmk, tmv, c);
+        case 4: return launch_split_t<4, PAGED, true, F16, D>(p, tmk, tmv, c);
+        case 8: return launch_split_t<8, PAGED, true, F16, D>(p, tmk, tmv, c);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (group) {
-    case 1: return launch_split_t<1, PAGED, false, F16>(p, tmk, tmv, c);
-    case 2: return launch_split_t<2, PAGED, false, F16>(p, tmk, tmv, c);
-    case 4: return launch_split_t<4, PAGED, false, F16>(p, tmk, tmv, c);
-    case 8: return launch_split_t<8, PAGED, false, F16>(p, tmk, tmv, c);
+    case 1: return launch_split_t<1, PAGED, false, F16, D>(p, tmk, tmv, c);
+    case 2: return launch_split_t<2, PAGED, false, F16, D>(p, tmk, tmv, c);
+    case 4: return launch_split_t<4, PAGED, false, F16, D>(p, tmk, tmv, c);
+    case 8: return launch_split_t<8, PAGED, false, F16, D>(p, tmk, tmv, c);
     default: return cudaErrorInvalidValue;
     }
+}
+
+// Each variant is compiled in its own translation unit (fd_split_inst.cu,
+// built once per combination), so the twelve compile in parallel.
+#define FD_SPLIT_VARIANTS(X) \
+    X(false, false, 64) X(false, false, 128) X(false, false, 256) \
+    X(false, true, 64) X(false, true, 128) X(false, true, 256) \
+    X(true, false, 64) X(true, false, 128) X(true, false, 256) \
+    X(true, true, 64) X(true, true, 128) X(true, true, 256)
+#define FD_EXTERN_SPLIT(P, F, D)                                                                \
+    extern template cudaError_t launch_split_variant<P, F, D>(bool, int, const SplitParams &, \
+                                                              const CUtensorMap &,             \
+                                                              const CUtensorMap &, const SplitLaunch &);
+FD_SPLIT_VARIANTS(FD_EXTERN_SPLIT)
+#undef FD_EXTERN_SPLIT
+
+// Split launch for a call: layout, element type and head_dim pick the
+// variant.  Returns cudaErrorInvalidValue for an unsupported head_dim.
+inline cudaError_t launch_split(bool paged, bool f16, int head_dim, bool mma, int group,
+                                const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                const SplitLaunch &c)
+{
+#define FD_PICK_SPLIT(P, F, D)                                                  \
+    if (paged == P && f16 == F && head_dim == D)                              \
+        return launch_split_variant<P, F, D>(mma, group, p, tmk, tmv, c);
+    FD_SPLIT_VARIANTS(FD_PICK_SPLIT)
+#undef FD_PICK_SPLIT
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace fd

@@ -4,8 +4,8 @@
 
 namespace fd {
 
-template <int G>
 // grid = number of segments (requests x kv heads); one CTA per (segment, query head).
+template <int G, int D>
 static cudaError_t launch_merge_t(const MergeParams &p, int grid, cudaStream_t stream)
 {
     cudaLaunchAttribute attr[1];
@@ -13,21 +13,32 @@ static cudaError_t launch_merge_t(const MergeParams &p, int grid, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, (unsigned)G);   // (segment, query head of its group)
-    cfg.blockDim = dim3(kHeadDim);
+    cfg.blockDim = dim3(D);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, merge_kernel<G>, p);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<G, D>, p);
 }
 
-cudaError_t launch_merge(int group, const MergeParams &p, int grid, cudaStream_t stream)
+template <int D>
+static cudaError_t launch_merge_d(int group, const MergeParams &p, int grid, cudaStream_t stream)
 {
     switch (group) {
-    case 1: return launch_merge_t<1>(p, grid, stream);
-    case 2: return launch_merge_t<2>(p, grid, stream);
-    case 4: return launch_merge_t<4>(p, grid, stream);
-    case 8: return launch_merge_t<8>(p, grid, stream);
+    case 1: return launch_merge_t<1, D>(p, grid, stream);
+    case 2: return launch_merge_t<2, D>(p, grid, stream);
+    case 4: return launch_merge_t<4, D>(p, grid, stream);
+    case 8: return launch_merge_t<8, D>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_merge(int group, int head_dim, const MergeParams &p, int grid, cudaStream_t stream)
+{
+    switch (head_dim) {
+    case 64: return launch_merge_d<64>(group, p, grid, stream);
+    case 128: return launch_merge_d<128>(group, p, grid, stream);
+    case 256: return launch_merge_d<256>(group, p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

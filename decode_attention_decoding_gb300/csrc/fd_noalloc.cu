@@ -33,6 +33,8 @@ namespace {
 using namespace fd;
 
 constexpr size_t kNoallocScratchBytes = FD_NOALLOC_SCRATCH_BYTES;
+constexpr int kD = 128;   // the one head_dim this entry point serves
+using HD = HeadDim<kD>;
 
 // The scratch: device-error word, tile prefix, partial LSEs and partial outputs.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
@@ -91,9 +93,9 @@ fd_status encode_rows(CUtensorMap *map, const void *base, int hkv, long long row
     }();
     if (!fn)
         return FD_ERR_CUDA;
-    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)hkv * kRowBytes};
-    const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1u, (cuuint32_t)kTileTokens};
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)hkv, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)HD::kRowBytes, (cuuint64_t)hkv * HD::kRowBytes};
+    const cuuint32_t box[3] = {(cuuint32_t)kD, 1u, (cuuint32_t)kTileTokens};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -114,7 +116,7 @@ NoallocLayout noalloc_layout(int batch, int slots, int group)
     l.prefix_off = 256;
     l.lse_off = align_up(l.prefix_off + sizeof(int) * (size_t)(batch + 1), 256);
     l.o_off = align_up(l.lse_off + sizeof(float) * (size_t)slots * group, 256);
-    l.total = align_up(l.o_off + sizeof(float) * (size_t)slots * group * kHeadDim, 256);
+    l.total = align_up(l.o_off + sizeof(float) * (size_t)slots * group * kD, 256);
     return l;
 }
 
@@ -133,7 +135,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
         (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)))
         return FD_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    if (head_dim != kHeadDim || !(group == 1 || group == 2 || group == 4 || group == 8) ||
+    if (head_dim != kD || !(group == 1 || group == 2 || group == 4 || group == 8) ||
         batch > kMaxBatch || (long long)batch * s_max >= (1ll << 31) ||
         (long long)num_kv_heads * batch * ceil_div(s_max, kTileTokens) >= (1ll << 31))
         return FD_ERR_UNSUPPORTED;
@@ -169,19 +171,19 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     sp.timeout_ns = 2000000000ull;
 
     // Shared-memory plan (same rule as the workspace entry points).
-    const size_t red = align_up((size_t)kConsumerWarps * group * (kHeadDim + 2) * sizeof(float), 16);
+    const size_t red = align_up((size_t)reduction_floats(false, group, kD) * sizeof(float), 16);
     const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
     const size_t misc = 64;
     const size_t fixed = 1024 + red + prefix + misc + 8;
     if ((size_t)dev.smem_optin <= fixed)
         return FD_ERR_UNSUPPORTED;
-    int ns = (int)(((size_t)dev.smem_optin - fixed) / (kStageBytes + 2 * 8 + kMetaInts * sizeof(int)));
+    int ns = (int)(((size_t)dev.smem_optin - fixed) / (HD::kStageBytes + 2 * 8 + kMetaInts * sizeof(int)));
     if (ns > kMaxStages)
         ns = kMaxStages;
     if (ns < 2)
         return FD_ERR_UNSUPPORTED;
     sp.num_stages = ns;
-    sp.off_red = (uint32_t)(ns * kStageBytes);
+    sp.off_red = (uint32_t)(ns * HD::kStageBytes);
     sp.off_prefix = (uint32_t)(sp.off_red + red);
     sp.off_bar = (uint32_t)(sp.off_prefix + prefix);
     sp.off_meta = (uint32_t)(sp.off_bar + (2 * ns + 1) * 8);
@@ -213,9 +215,9 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     // The status word is the only part of the scratch that must start at zero.
     if (cudaMemsetAsync(sp.ws_err, 0, sizeof(unsigned int), launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    if (launch_split_contig(group, sp, tmk, tmv, launch) != cudaSuccess)
+    if (launch_split_variant<false, false, kD>(false, group, sp, tmk, tmv, launch) != cudaSuccess)
         return FD_ERR_CUDA;
-    if (launch_merge(group, mp, batch * num_kv_heads, launch.stream) != cudaSuccess)
+    if (launch_merge(group, kD, mp, batch * num_kv_heads, launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;
     if (device_status &&
         cudaMemcpyAsync(device_status, sp.ws_err, sizeof(unsigned int), cudaMemcpyDeviceToDevice,

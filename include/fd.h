@@ -37,8 +37,8 @@
  *     problem in the workspace header; fd_get_device_error reports it.
  *   - Alignment: q, k, v, k_pages, v_pages and o must be 16-byte aligned, and
  *     the workspace 256-byte aligned; otherwise FD_ERR_INVALID_ARG.
- *   - Supported shapes: head_dim 128; Hq/Hkv in {1, 2, 4, 8}; batch <= 4096.
- *     Other shapes return FD_ERR_UNSUPPORTED.
+ *   - Supported shapes: head_dim 64, 128 or 256; Hq/Hkv in {1, 2, 4, 8};
+ *     batch <= 4096.  Other shapes return FD_ERR_UNSUPPORTED.
  *   - Precision: q, K and V are bf16 (default) or IEEE fp16
  *     (fd_options.dtype); scores, softmax and accumulation are fp32; outputs
  *     are fp32.
@@ -194,8 +194,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  * device memory all belongs to their own pool.  The sources this library
  * follows have no counterpart to this call; it exists only for such callers.
  *
- * It computes exactly what fd_decode computes (same kernels, contiguous
- * layout, one split CTA per SM), with the split partials and the tile prefix
+ * It computes what fd_decode computes (the CUDA-core split kernel and the
+ * same merge, contiguous layout, one split CTA per SM), with the split partials and the tile prefix
  * held in a fixed device array of FD_NOALLOC_SCRATCH_BYTES (8 MiB) that is
  * part of this library: every GPU that loads the library reserves it until
  * the process exits.  Nothing is allocated -- no cudaMalloc, cudaFree or
@@ -205,7 +205,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  *   scale, o, lse: as for fd_decode (lse may be NULL).
  *   device_status: NULL, or a device uint32 that receives this call's
  *   FD_DEVICE_STATUS_* bits (0 when all went well), stream-ordered.
- * Limits: the scratch must hold 256 bytes + 4 (batch + 1) bytes + (batch *
+ * Limits: bf16 inputs and head_dim 128 only (other head dims return
+ * FD_ERR_UNSUPPORTED); the scratch must hold 256 bytes + 4 (batch + 1) bytes + (batch *
  * num_kv_heads + number of SMs) partials of (Hq/Hkv) * (head_dim + 1) * 4
  * bytes, each region rounded up to 256 bytes; a larger shape returns
  * FD_ERR_WORKSPACE_TOO_SMALL before anything is launched.

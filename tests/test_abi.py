@@ -91,7 +91,10 @@ def test_decode_argument_checks(lib, fd):
     assert call_decode(lib, k=ALIGNED + 2) == E.FD_ERR_INVALID_ARG
     assert call_decode(lib, ws=ALIGNED + 16) == E.FD_ERR_INVALID_ARG
     assert call_decode(lib, smax=-1) == E.FD_ERR_INVALID_ARG
-    assert call_decode(lib, d=64) == E.FD_ERR_UNSUPPORTED
+    for d in (32, 96, 192, 512):
+        assert call_decode(lib, d=d) == E.FD_ERR_UNSUPPORTED
+    for d in (64, 128, 256):   # accepted head dims reach the workspace check
+        assert call_decode(lib, d=d, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
     assert call_decode(lib, hq=6, hkv=2) == E.FD_ERR_UNSUPPORTED       # group 3
     assert call_decode(lib, hq=32, hkv=2) == E.FD_ERR_UNSUPPORTED      # group 16
     assert call_decode(lib, B=5000) == E.FD_ERR_UNSUPPORTED
