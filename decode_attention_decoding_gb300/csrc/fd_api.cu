@@ -182,6 +182,34 @@ bool use_mma(int group, int page_size, const fd_options *opts)
     return group >= 2 && (page_size == 0 || page_size >= 8);
 }
 
+// Kv heads fused into one launch head: the largest F in {4, 2} with
+// F * head_dim <= 256, F * group <= 8 and F dividing Hkv, on the tensor-core
+// path only (F * group >= 2 always selects it); 1 = no fusion.
+int fuse_factor(int group, int hkv, int head_dim, int page_size, const fd_options *opts)
+{
+    if (opts && (opts->flags & (FD_FLAG_CUDA_CORES | FD_FLAG_NO_HEAD_FUSION)))
+        return 1;
+    if (page_size != 0 && page_size < 8)
+        return 1;
+    for (int f = 4; f >= 2; f /= 2)
+        if (f * head_dim <= 256 && f * group <= 8 && hkv % f == 0)
+            return f;
+    return 1;
+}
+
+// Workspace for every launch shape a call of this shape may take (fused or not).
+size_t workspace_bytes_needed(int batch, int hq, int hkv, int head_dim)
+{
+    const int group = hq / hkv;
+    size_t need = workspace_layout(batch, hkv, group, head_dim).total;
+    for (int f = 2; f <= 4; f *= 2)
+        if (f * head_dim <= 256 && f * group <= 8 && hkv % f == 0) {
+            const size_t t = workspace_layout(batch, hkv / f, f * group, f * head_dim).total;
+            need = t > need ? t : need;
+        }
+    return need;
+}
+
 // Shared-memory plan of the split kernel for the call's consumers, group,
 // head_dim and batch; fills the offsets and stage count in sp and the byte
 // size in launch.
@@ -218,8 +246,14 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
                     int head_dim, int page_size, int max_blocks, int num_pages, float scale, float *o,
                     float *lse, void *workspace, const fd_options *opts, fd_stream_t stream)
 {
-    const int group = hq / hkv;
-    const WorkspaceLayout wl = workspace_layout(batch, hkv, group, head_dim);
+    // Launch shape: F fused kv heads of head_dim dims become one head of
+    // F * head_dim dims with F * group query heads.
+    const int real_group = hq / hkv;
+    const int fuse = fuse_factor(real_group, hkv, head_dim, page_size, opts);
+    const int group = fuse * real_group;
+    const int d = fuse * head_dim;
+    hkv /= fuse;
+    const WorkspaceLayout wl = workspace_layout(batch, hkv, group, d);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int num_ctas = opts && opts->num_ctas > 0 ? opts->num_ctas : dev.sms;
     if (num_ctas > kMaxCtas)
@@ -250,14 +284,18 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     sp.scale_log2 = scale * 1.4426950408889634f;
     sp.timeout_ns = opts && opts->wait_timeout_ns ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     sp.flags = opts ? opts->flags : 0u;
+    sp.fuse_dh = fuse > 1 ? head_dim : 0;
+    sp.fuse_g = real_group;
 
     cp->group = group;
-    cp->head_dim = head_dim;
+    cp->head_dim = d;
     cp->mma = use_mma(group, page_size, opts);
     cp->f16 = opts && opts->dtype == FD_DTYPE_F16;
+    if (fuse > 1 && !cp->mma)
+        return FD_ERR_UNSUPPORTED;   // fusion is defined for the tensor-core consumers only
     cp->launch.grid = num_ctas;
     cp->launch.stream = reinterpret_cast<cudaStream_t>(stream);
-    fd_status st = plan_smem(dev, cp->mma, group, head_dim, batch, &sp, &cp->launch);
+    fd_status st = plan_smem(dev, cp->mma, group, d, batch, &sp, &cp->launch);
     if (st != FD_OK)
         return st;
 
@@ -271,6 +309,8 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     mp.hq = hq;
     mp.hkv = hkv;
     mp.num_ctas = num_ctas;
+    mp.fuse_dh = sp.fuse_dh;
+    mp.fuse_g = sp.fuse_g;
     return FD_OK;
 }
 
@@ -303,7 +343,7 @@ size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_
     if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kv_len < 0 ||
         page_size < 0 || num_q_heads % num_kv_heads != 0)
         return 0;
-    return workspace_layout(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim).total;
+    return workspace_bytes_needed(batch, num_q_heads, num_kv_heads, head_dim);
 }
 
 fd_status fd_workspace_init(void *workspace, size_t workspace_bytes, fd_stream_t stream)
@@ -350,7 +390,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
         return st;
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
-    if ((st = encode_kv_maps(&tmk, &tmv, k, v, num_kv_heads, rows, kTileTokens, cp.mma, cp.f16, head_dim,
+    if ((st = encode_kv_maps(&tmk, &tmv, k, v, cp.sp.hkv, rows, kTileTokens, cp.mma, cp.f16, cp.head_dim,
                              &cp.sp)) != FD_OK)
         return st;
     return run(cp, false, tmk, tmv, opts);
@@ -400,8 +440,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)num_pages * page_size;
     const int box = page_size < kTileTokens ? page_size : kTileTokens;
-    if ((st = encode_kv_maps(&tmk, &tmv, k_pages, v_pages, num_kv_heads, rows, box, cp.mma, cp.f16,
-                             head_dim, &cp.sp)) != FD_OK)
+    if ((st = encode_kv_maps(&tmk, &tmv, k_pages, v_pages, cp.sp.hkv, rows, box, cp.mma, cp.f16,
+                             cp.head_dim, &cp.sp)) != FD_OK)
         return st;
     return run(cp, true, tmk, tmv, opts);
 }

@@ -38,7 +38,7 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kSplitThreads = kConsumerThreads + 32;
 constexpr int kPairs = kConsumerWarps / 2;
 constexpr int kPartBytes = kTileTokens * 128;           // 64 rows x 64 dims: one swizzled part
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 16;
 constexpr int kMetaInts = 8;
 constexpr int kRowsPerWarp = kTileTokens / kConsumerWarps;   // 8
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -95,6 +95,14 @@ struct SplitParams {
     int box4d;
     int box_rows_log2;   // log2 of the rows in one box: 6 (64) or log2(page size)
     int page_log2;       // paged, page size under 64: log2 of the page size
+    // Fused heads (tensor-core path only).  When fuse_dh > 0, each kv head of
+    // the launch is F = D / fuse_dh adjacent kv heads of the caller, side by
+    // side (the same bytes), and its G query heads are their F groups of
+    // fuse_g = G / F query heads: query head g owns dims
+    // [part(g), part(g) + fuse_dh) with part(g) = (g / fuse_g) fuse_dh, takes
+    // zeros for q elsewhere and writes only its own dims.  q and o rows then
+    // hold fuse_dh values.  0: no fusion (q and o rows hold D values).
+    int fuse_dh, fuse_g;
 };
 
 struct MergeParams {
@@ -104,7 +112,25 @@ struct MergeParams {
     const float *ws_lse;
     const int32_t *ws_prefix;
     int batch, hq, hkv, num_ctas;
+    int fuse_dh, fuse_g;   // as in SplitParams
 };
+
+// First dim of query head g's part of a fused head (0 without fusion).
+__device__ __forceinline__ int fused_part(int fuse_dh, int fuse_g, int g)
+{
+    return fuse_dh ? (g / fuse_g) * fuse_dh : 0;
+}
+
+// Store output element d (of D) of query row `row`: unfused rows hold D
+// values; a fused head's query rows hold only their own fuse_dh dims.
+template <int D>
+__device__ __forceinline__ void store_o(float *o, size_t row, int d, int fuse_dh, int part, float v)
+{
+    if (!fuse_dh)
+        o[row * D + d] = v;
+    else if (d >= part && d < part + fuse_dh)
+        o[row * fuse_dh + (d - part)] = v;
+}
 
 __device__ __forceinline__ int load_len(const SplitParams &p, int b, bool report)
 {
@@ -396,7 +422,7 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
         const float lse_v = ltrue > 0.f ? (M + log2f(ltrue)) * kLn2 : kNegInf;
         if (own) {
             const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
-            p.o[row * D + d] = out;
+            store_o<D>(p.o, row, d, p.fuse_dh, fused_part(p.fuse_dh, p.fuse_g, g), out);
             if (d == 0 && p.lse)
                 p.lse[row] = lse_v;
         } else {
@@ -710,13 +736,18 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 
         if (flags & kFirstInCta) {
             // B[k = d][n = head]: lane holds head `grp`, dims 16 ks + 2 qd (+1) and (+8, +9).
+            // A fused head's query reads its own fuse_dh dims; zeros elsewhere.
             if (grp < G) {
+                const int qdim = p.fuse_dh ? p.fuse_dh : D;
+                const int part = fused_part(p.fuse_dh, p.fuse_g, grp);
                 const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                    p.q + ((size_t)b * p.hq + (size_t)h * G + grp) * D);
+                    p.q + ((size_t)b * p.hq + (size_t)h * G + grp) * qdim);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    qb[ks][0] = __ldg(qrow + ks * 8 + qd);
-                    qb[ks][1] = __ldg(qrow + ks * 8 + 4 + qd);
+                    const int d0 = ks * 16 - part;   // first dim of this k-step in the q row
+                    const bool in = d0 >= 0 && d0 < qdim;
+                    qb[ks][0] = in ? __ldg(qrow + d0 / 2 + qd) : 0u;
+                    qb[ks][1] = in ? __ldg(qrow + d0 / 2 + 4 + qd) : 0u;
                 }
             }
         }
@@ -922,8 +953,9 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
     const int d = threadIdx.x;
     const int pb = p.ws_prefix[b], pe = p.ws_prefix[b + 1], T = p.ws_prefix[p.batch];
     const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
+    const int part = fused_part(p.fuse_dh, p.fuse_g, g);
     if (pe == pb) {   // empty request: O = 0, LSE = -inf
-        p.o[row * D + d] = 0.f;
+        store_o<D>(p.o, row, d, p.fuse_dh, part, 0.f);
         if (d == 0 && p.lse)
             p.lse[row] = kNegInf;
         return;
@@ -986,7 +1018,7 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
     }
     for (; i < n; ++i)
         acc += src[(size_t)i * stride] * s_w[i];
-    p.o[row * D + d] = acc;
+    store_o<D>(p.o, row, d, p.fuse_dh, part, acc);
     if (d == 0 && p.lse)
         p.lse[row] = lse;
 }

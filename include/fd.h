@@ -104,18 +104,30 @@ typedef struct fd_options {
  * arithmetic instead. */
 #define FD_FLAG_CUDA_CORES 0x2u
 
-/* Tensor-core consumers: load each 64-dim half of a K/V tile as its own TMA
- * box (3-D tensor maps) instead of one box carrying both halves (4-D maps).
+/* Tensor-core consumers: load each 64-dim part of a K/V tile as its own TMA
+ * box (3-D tensor maps) instead of one box carrying every part (4-D maps).
  * Results are identical; for comparisons only. */
 #define FD_FLAG_NO_4D_BOXES 0x4u
+
+/* Do not fuse kv heads.  By default, when the tensor-core consumers apply
+ * (contiguous KV, or pages of at least 8 tokens, and no FD_FLAG_CUDA_CORES),
+ * F adjacent kv heads (F = 4 or 2, the largest with F * head_dim <= 256,
+ * F * (Hq/Hkv) <= 8 and F dividing Hkv) are read as one head of F * head_dim
+ * dims: [.., Hkv, D] and [.., Hkv/F, F*D] are the same bytes, so each TMA row
+ * is F times longer, and the F query groups share one tensor-core tile with
+ * zeros for the dims of the other heads.  Every query head still attends only
+ * to its own kv head.  This flag keeps one kv head per segment. */
+#define FD_FLAG_NO_HEAD_FUSION 0x8u
 
 /*
  * Bytes of workspace that fd_decode / fd_decode_paged need for this shape.
  * Pure host function (no CUDA call).  The size does not depend on the
  * lengths: it holds a 256-byte header, the per-request tile prefix and one
  * fp32 partial (Hq/Hkv rows of head_dim outputs plus their log-sum-exp) per
- * (request, kv head) plus one per possible split CTA.  max_kv_len and page_size are validated but do not
- * change the size.
+ * (request, kv head) plus one per possible split CTA -- sized for whichever
+ * launch shape the call takes, with or without fused kv heads (see
+ * FD_FLAG_NO_HEAD_FUSION).  max_kv_len and page_size are validated but do
+ * not change the size.
  * Returns 0 for invalid arguments.
  */
 size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,

@@ -44,7 +44,8 @@ def test_contiguous_vs_oracle(d, group, flags):
 def test_paged_vs_oracle_and_contiguous(d, page, group):
     w = syn.make_contiguous(950 + d + page, len(RAGGED), 2 * group, 2, d, 1024, RAGGED)
     wp = contig_to_paged(w, page, perm_seed=page + d, poison=True)
-    flags = CUDA_CORES if (page < 8 and group >= 2) else 0
+    # pages under 8 tokens always take the unfused CUDA-core consumers
+    flags = CUDA_CORES if page < 8 else 0
     ro, rl = oracle.attend(wp, threads=8)
     for ctas in (0, 5):
         op, lp = run(wp, num_ctas=ctas)

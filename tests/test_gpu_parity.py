@@ -44,8 +44,8 @@ def test_paged_vs_oracle_and_contiguous(page, group):
     hkv = 2
     w = syn.make_contiguous(300 + page, len(RAGGED), hkv * group, hkv, 128, 1024, RAGGED)
     wp = contig_to_paged(w, page, perm_seed=page + group)
-    # pages under 8 tokens always take the CUDA-core consumers
-    flags = CUDA_CORES if (page < 8 and group >= 2) else 0
+    # pages under 8 tokens always take the unfused CUDA-core consumers
+    flags = CUDA_CORES if page < 8 else 0
     for ctas in (0, 5):
         op, lp = run(wp, num_ctas=ctas)
         ro, rl = oracle.attend(wp, threads=8)
