@@ -300,6 +300,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
         return st;
 
     MergeParams &mp = cp->mp;
+    std::memset(&mp, 0, sizeof mp);
     mp.o = o;
     mp.lse = lse;
     mp.ws_o = sp.ws_o;

@@ -196,6 +196,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     launch.stream = reinterpret_cast<cudaStream_t>(stream);
 
     MergeParams mp;
+    std::memset(&mp, 0, sizeof mp);   // no fused heads; every field defined
     mp.o = o;
     mp.lse = lse;
     mp.ws_o = sp.ws_o;
