@@ -25,6 +25,7 @@ __all__ = [
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
     "FD_ERR_CUDA", "FD_ERR_TIMEOUT", "FD_ERR_DEVICE_INPUT", "FD_FLAG_TEST_STARVE_FIRST_TILE",
     "FD_FLAG_CUDA_CORES", "FD_FLAG_NO_4D_BOXES", "FD_FLAG_NO_HEAD_FUSION",
+    "FD_FLAG_FUSE_HEADS",
     "fd_decode_noalloc",
 ]
 
@@ -34,6 +35,7 @@ FD_FLAG_TEST_STARVE_FIRST_TILE = 0x1
 FD_FLAG_CUDA_CORES = 0x2
 FD_FLAG_NO_4D_BOXES = 0x4
 FD_FLAG_NO_HEAD_FUSION = 0x8
+FD_FLAG_FUSE_HEADS = 0x10
 
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 

@@ -182,19 +182,46 @@ bool use_mma(int group, int page_size, const fd_options *opts)
     return group >= 2 && (page_size == 0 || page_size >= 8);
 }
 
+// Fusion pays where a kv head's TMA rows are short (128-byte rows of 64
+// dims, or page boxes under 64 tokens) and the call is long enough for the
+// wider tiles: measured on GB300, it lost up to a quarter of the time on
+// calls of under ~24 tiles per CTA (larger tiles, fewer of them per CTA,
+// twice the merge width) and gained 10-85% above that on such rows.
+constexpr double kFuseMinTilesPerCta = 24.0;
+
 // Kv heads fused into one launch head: the largest F in {4, 2} with
 // F * head_dim <= 256, F * group <= 8 and F dividing Hkv, on the tensor-core
-// path only (F * group >= 2 always selects it); 1 = no fusion.
-int fuse_factor(int group, int hkv, int head_dim, int page_size, const fd_options *opts)
+// path only (F * group >= 2 always selects it), for short rows and at least
+// kFuseMinTilesPerCta (estimated) tiles per CTA unless FD_FLAG_FUSE_HEADS
+// forces it; 1 = no fusion.
+int fuse_factor(int group, int hkv, int head_dim, int page_size, double tiles_per_cta,
+                const fd_options *opts)
 {
     if (opts && (opts->flags & (FD_FLAG_CUDA_CORES | FD_FLAG_NO_HEAD_FUSION)))
         return 1;
     if (page_size != 0 && page_size < 8)
         return 1;
+    const bool short_rows = head_dim == 64 || (page_size > 0 && page_size < kTileTokens);
+    const bool forced = opts && (opts->flags & FD_FLAG_FUSE_HEADS);
+    if (!forced && (!short_rows || tiles_per_cta < kFuseMinTilesPerCta))
+        return 1;
     for (int f = 4; f >= 2; f /= 2)
         if (f * head_dim <= 256 && f * group <= 8 && hkv % f == 0)
             return f;
     return 1;
+}
+
+// KV tiles of a call (unfused): from the host copy of the lengths when the
+// caller passes one, else every request at the capacity `span`.
+long long estimate_tiles(const int32_t *seq_lens_host, int batch, int hkv, long long span)
+{
+    long long tiles = 0;
+    if (seq_lens_host)
+        for (int b = 0; b < batch; ++b)
+            tiles += ceil_div((long long)seq_lens_host[b], (long long)kTileTokens);
+    else
+        tiles = (long long)batch * ceil_div(span, (long long)kTileTokens);
+    return tiles * hkv;
 }
 
 // Workspace for every launch shape a call of this shape may take (fused or not).
@@ -244,20 +271,21 @@ fd_status plan_smem(const DeviceInfo &dev, bool mma, int group, int d, int batch
 fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const int32_t *seq_lens_dev,
                     const int32_t *block_table, int batch, int hq, int hkv, int cap, int s_max,
                     int head_dim, int page_size, int max_blocks, int num_pages, float scale, float *o,
-                    float *lse, void *workspace, const fd_options *opts, fd_stream_t stream)
+                    float *lse, void *workspace, long long est_tiles, const fd_options *opts,
+                    fd_stream_t stream)
 {
+    int num_ctas = opts && opts->num_ctas > 0 ? opts->num_ctas : dev.sms;
+    if (num_ctas > kMaxCtas)
+        return FD_ERR_INVALID_ARG;
     // Launch shape: F fused kv heads of head_dim dims become one head of
     // F * head_dim dims with F * group query heads.
     const int real_group = hq / hkv;
-    const int fuse = fuse_factor(real_group, hkv, head_dim, page_size, opts);
+    const int fuse = fuse_factor(real_group, hkv, head_dim, page_size, (double)est_tiles / num_ctas, opts);
     const int group = fuse * real_group;
     const int d = fuse * head_dim;
     hkv /= fuse;
     const WorkspaceLayout wl = workspace_layout(batch, hkv, group, d);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    int num_ctas = opts && opts->num_ctas > 0 ? opts->num_ctas : dev.sms;
-    if (num_ctas > kMaxCtas)
-        return FD_ERR_INVALID_ARG;
 
     SplitParams &sp = cp->sp;
     std::memset(&sp, 0, sizeof sp);
@@ -386,7 +414,8 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
         return st;
     CallPlan cp;
     st = fill_plan(&cp, dev, q, seq_lens_dev, nullptr, batch, num_q_heads, num_kv_heads, s_max, s_max,
-                   head_dim, 0, 0, 0, scale, o, lse, workspace, opts, stream);
+                   head_dim, 0, 0, 0, scale, o, lse, workspace,
+                   estimate_tiles(seq_lens_host, batch, num_kv_heads, s_max), opts, stream);
     if (st != FD_OK)
         return st;
     alignas(64) CUtensorMap tmk, tmv;
@@ -434,8 +463,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
         return st;
     CallPlan cp;
     st = fill_plan(&cp, dev, q, seq_lens_dev, block_table, batch, num_q_heads, num_kv_heads, (int)cap, 0,
-                   head_dim, page_size, max_blocks_per_seq, num_pages, scale, o, lse, workspace, opts,
-                   stream);
+                   head_dim, page_size, max_blocks_per_seq, num_pages, scale, o, lse, workspace,
+                   estimate_tiles(seq_lens_host, batch, num_kv_heads, cap), opts, stream);
     if (st != FD_OK)
         return st;
     alignas(64) CUtensorMap tmk, tmv;

@@ -111,13 +111,21 @@ typedef struct fd_options {
 
 /* Do not fuse kv heads.  By default, when the tensor-core consumers apply
  * (contiguous KV, or pages of at least 8 tokens, and no FD_FLAG_CUDA_CORES),
- * F adjacent kv heads (F = 4 or 2, the largest with F * head_dim <= 256,
- * F * (Hq/Hkv) <= 8 and F dividing Hkv) are read as one head of F * head_dim
- * dims: [.., Hkv, D] and [.., Hkv/F, F*D] are the same bytes, so each TMA row
- * is F times longer, and the F query groups share one tensor-core tile with
- * zeros for the dims of the other heads.  Every query head still attends only
- * to its own kv head.  This flag keeps one kv head per segment. */
+ * a kv head's rows are short (head_dim 64, or pages under 64 tokens) and the
+ * call has at least 24 KV tiles of 64 tokens per split CTA (counted from
+ * seq_lens_host when given, else from the capacity), F adjacent kv heads
+ * (F = 4 or 2, the largest with F * head_dim <= 256, F * (Hq/Hkv) <= 8 and F
+ * dividing Hkv) are read as one head of F * head_dim dims: [.., Hkv, D] and
+ * [.., Hkv/F, F*D] are the same bytes, so each TMA row is F times longer, and
+ * the F query groups share one tensor-core tile with zeros for the dims of
+ * the other heads.  Every query head still attends only to its own kv head.
+ * This flag keeps one kv head per segment. */
 #define FD_FLAG_NO_HEAD_FUSION 0x8u
+
+/* Fuse kv heads whenever the shape and consumers allow it (the F rule
+ * above), whatever the row length and the call's size.  FD_FLAG_NO_HEAD_FUSION
+ * wins if both are set. */
+#define FD_FLAG_FUSE_HEADS 0x10u
 
 /*
  * Bytes of workspace that fd_decode / fd_decode_paged need for this shape.

@@ -15,6 +15,7 @@ pytestmark = pytest.mark.gpu
 
 CUDA_CORES = 0x2
 NO_FUSION = 0x8       # FD_FLAG_NO_HEAD_FUSION
+FUSE = 0x10           # FD_FLAG_FUSE_HEADS: fuse whenever the shape allows it
 RAGGED = [1000, 1, 0, 63, 64, 65, 129, 700]
 
 
@@ -42,7 +43,7 @@ def test_fused_and_unfused_match_the_oracle(d, group, hkv):
     w = syn.make_contiguous(1100 + d + 10 * group + hkv, len(RAGGED), hkv * group, hkv, d, 1024, RAGGED)
     ro, rl = oracle.attend(w, threads=8)
     dev = to_device(w)
-    for flags in (0, NO_FUSION):
+    for flags in (0, FUSE, NO_FUSION):
         for ctas in (0, 7):
             # NaN-filled outputs: every element must be written exactly by its own head
             out = torch.full((w.batch, w.num_q_heads, d), float("nan"), device="cuda")
@@ -59,9 +60,9 @@ def test_fused_paged_matches_oracle_and_contiguous(d, group, hkv, page):
     wp = contig_to_paged(w, page, perm_seed=page + group, poison=True)
     ro, rl = oracle.attend(wp, threads=8)
     for ctas in (0, 5):
-        op, lp = run(wp, num_ctas=ctas)
+        op, lp = run(wp, num_ctas=ctas, flags=FUSE)
         check(op, lp, ro, rl, f"d={d} G={group} P={page} ctas={ctas}")
-        oc, lc = run(w, num_ctas=ctas)
+        oc, lc = run(w, num_ctas=ctas, flags=FUSE)
         assert np.array_equal(op, oc) and np.array_equal(lp, lc)
 
 
@@ -85,7 +86,7 @@ def test_fused_heads_never_mix(d, group, hkv):
     for g in range(hkv):
         assert s[stars[g], g] - np.delete(s[:, g], stars[g]).max() > 110, "probe margin too small"
     for ctas in (0, 7):
-        o, _ = run(w, num_ctas=ctas)
+        o, _ = run(w, num_ctas=ctas, flags=FUSE)
         for h in range(hkv * group):
             g = h // group
             assert np.array_equal(o[0, h], syn.bf16_bits_to_f64(w.v[0, stars[g], g])), (ctas, h)
@@ -95,6 +96,21 @@ def test_fused_heads_never_mix(d, group, hkv):
 def test_fused_f16_inputs():
     w = syn.make_contiguous(1400, len(RAGGED), 8, 4, 128, 1024, RAGGED, dtype="f16")
     ro, rl = oracle.attend(w, threads=8)
-    for flags in (0, NO_FUSION):
+    for flags in (FUSE, NO_FUSION):
         o, l = run(w, num_ctas=7, flags=flags)
         check(o, l, ro, rl, f"f16 flags={flags}")
+
+
+@pytest.mark.parametrize("d,page", [(64, 0), (128, 16), (64, 16)])
+def test_default_fuses_long_calls_with_short_rows(d, page):
+    """The default picks fusion for a long call with short rows; the result
+    equals the forced-fusion launch bit for bit and matches the oracle."""
+    lens = [6000, 4000, 5000, 3000]
+    w = syn.make_contiguous(1500 + d + page, len(lens), 8, 4, d, 6000, lens)
+    if page:
+        w = contig_to_paged(w, page, perm_seed=page)
+    ro, rl = oracle.attend(w, threads=8)
+    o, l = run(w, num_ctas=8)          # (sum of tiles) x Hkv / 8 CTAs >= 24 per CTA
+    of, lf = run(w, num_ctas=8, flags=FUSE)
+    assert np.array_equal(o, of) and np.array_equal(l, lf)
+    check(o, l, ro, rl, f"d={d} P={page} default")
