@@ -19,6 +19,10 @@ Recipe (the same on every machine):
   through fp32, which would round twice).
 * fp16: one round-to-nearest-even from fp64 straight to fp16 (NumPy's direct
   double-to-half conversion, subnormals included).
+* FP8 KV caches (OCP E4M3 / E5M2): the fp64 normal divided by the tensor's
+  dequantisation scale, rounded once to nearest-even on the format's grid,
+  saturating at its largest finite value (448 / 57344); NaN and infinity
+  codes are never produced.
 * Integers in [lo, hi]: ``lo + z % (hi - lo + 1)``.
 * Permutations: Fisher-Yates driven by the same integer draws.
 
@@ -107,6 +111,43 @@ def widen_bits(bits: np.ndarray, dtype: str) -> np.ndarray:
     return bf16_bits_to_f64(bits) if dtype == "bf16" else f16_bits_to_f64(bits)
 
 
+# (exponent bits, fraction bits, bias, largest finite value)
+FP8_FORMATS = {"e4m3": (4, 3, 7, 448.0), "e5m2": (5, 2, 15, 57344.0)}
+
+
+def f64_to_fp8_bits(x: np.ndarray, fmt: str) -> np.ndarray:
+    """Round fp64 values to FP8 codes ('e4m3' or 'e5m2'), nearest-even in one
+    step, saturating at the largest finite magnitude."""
+    ebits, mbits, bias, vmax = FP8_FORMATS[fmt]
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    if not np.all(np.isfinite(x)):
+        raise ValueError("f64_to_fp8_bits: non-finite input")
+    sign = (x < 0) | ((x == 0) & np.signbit(x))
+    a = np.minimum(np.abs(x), vmax)
+    emin = 1 - bias                                   # exponent of the smallest normal
+    e = np.full(a.shape, emin, dtype=np.int64)
+    nz = a > 0
+    e[nz] = np.maximum(np.floor(np.log2(a[nz])).astype(np.int64), emin)
+    # log2 rounding can be off by one at binade edges: fix so 2^e <= a < 2^(e+1) (or e = emin)
+    e = np.where((a >= np.ldexp(1.0, e + 1)) & nz, e + 1, e)
+    e = np.where((a < np.ldexp(1.0, e)) & (e > emin), e - 1, e)
+    quantum = np.ldexp(1.0, e - mbits)
+    qv = np.rint(a / quantum) * quantum               # exact scaling; rint is half-even
+    qv = np.minimum(qv, vmax)
+    # encode the (now representable) magnitude
+    code = np.zeros(a.shape, dtype=np.int64)
+    normal = qv >= np.ldexp(1.0, emin)
+    sub = ~normal
+    code[sub] = np.rint(qv[sub] / np.ldexp(1.0, emin - mbits)).astype(np.int64)
+    if normal.any():
+        en = np.floor(np.log2(qv[normal])).astype(np.int64)
+        en = np.where(qv[normal] >= np.ldexp(1.0, en + 1), en + 1, en)
+        en = np.where(qv[normal] < np.ldexp(1.0, en), en - 1, en)
+        frac = np.rint(qv[normal] / np.ldexp(1.0, en - mbits)).astype(np.int64) - (1 << mbits)
+        code[normal] = ((en + bias) << mbits) | frac
+    return (code | (sign.astype(np.int64) << 7)).astype(np.uint8)
+
+
 def _normal_chunk(seed: int, start: int, n: int) -> np.ndarray:
     # element e uses the Box-Muller pair (2*(e//2), 2*(e//2)+1)
     p0 = start // 2
@@ -131,6 +172,26 @@ def normal_bf16(seed: int, shape, workers: int | None = None, dtype: str = "bf16
     def work(start):
         m = min(_CHUNK, n - start)
         out[start:start + m] = round_bits(_normal_chunk(seed, start, m), dtype)
+
+    starts = range(0, n, _CHUNK)
+    if n <= _CHUNK:
+        for s in starts:
+            work(s)
+    else:
+        with ThreadPoolExecutor(max_workers=workers or min(32, os.cpu_count() or 1)) as ex:
+            list(ex.map(work, starts))
+    return out.reshape(shape)
+
+
+def normal_fp8(seed: int, shape, fmt: str, scale: float, workers: int | None = None) -> np.ndarray:
+    """i.i.d. N(0,1) values stored as FP8 codes with dequantisation scale
+    `scale` (code = fp8(x / scale)), returned as uint8."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.uint8)
+
+    def work(start):
+        m = min(_CHUNK, n - start)
+        out[start:start + m] = f64_to_fp8_bits(_normal_chunk(seed, start, m) / scale, fmt)
 
     starts = range(0, n, _CHUNK)
     if n <= _CHUNK:
@@ -214,7 +275,10 @@ class Workload:
     page_size: int = 0                 # 0 = contiguous
     block_table: np.ndarray | None = None
     meta: dict = field(default_factory=dict)
-    dtype: str = "bf16"                # element type of q, K, V: 'bf16' or 'f16'
+    dtype: str = "bf16"                # element type of q (and of K, V unless kv_dtype is set)
+    kv_dtype: str | None = None        # None: K/V as q; 'e4m3' / 'e5m2': uint8 FP8 codes
+    k_scale: float = 1.0               # dequantisation scales of an FP8 cache (fp32 values)
+    v_scale: float = 1.0
 
     @property
     def batch(self) -> int:
@@ -236,9 +300,14 @@ class Workload:
     def max_blocks(self) -> int:
         return self.block_table.shape[1] if self.paged else 0
 
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.kv_dtype in ("e4m3", "e5m2") else 2
+
     def kv_bytes(self) -> int:
         """K+V bytes of the valid tokens, read once each."""
-        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 2 * 2
+        return (int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 2
+                * self.kv_elem_bytes)
 
 
 def default_scale(head_dim: int) -> float:
@@ -246,14 +315,30 @@ def default_scale(head_dim: int) -> float:
     return float(np.float32(1.0) / np.sqrt(np.float32(head_dim)))
 
 
+def _kv(config_id: int, shape, dtype: str, kv_dtype, k_scale: float, v_scale: float):
+    if kv_dtype in ("e4m3", "e5m2"):
+        return (normal_fp8(seed_for(config_id, TENSOR_K), shape, kv_dtype, k_scale),
+                normal_fp8(seed_for(config_id, TENSOR_V), shape, kv_dtype, v_scale))
+    return (normal_bf16(seed_for(config_id, TENSOR_K), shape, dtype=dtype),
+            normal_bf16(seed_for(config_id, TENSOR_V), shape, dtype=dtype))
+
+
+def fp32(x: float) -> float:
+    """The fp32 value nearest x (scales are passed to the library as fp32)."""
+    return float(np.float32(x))
+
+
 def make_contiguous(config_id: int, batch: int, hq: int, hkv: int, d: int, s_max: int,
-                    lens, name: str = "", dtype: str = "bf16") -> Workload:
+                    lens, name: str = "", dtype: str = "bf16", kv_dtype: str | None = None,
+                    k_scale: float = 1.0, v_scale: float = 1.0) -> Workload:
+    """Contiguous workload; with kv_dtype 'e4m3'/'e5m2' K and V are FP8 codes
+    whose dequantised values (code * scale) approximate N(0,1)."""
+    k_scale, v_scale = fp32(k_scale), fp32(v_scale)
     q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d), dtype=dtype)
-    k = normal_bf16(seed_for(config_id, TENSOR_K), (batch, s_max, hkv, d), dtype=dtype)
-    v = normal_bf16(seed_for(config_id, TENSOR_V), (batch, s_max, hkv, d), dtype=dtype)
+    k, v = _kv(config_id, (batch, s_max, hkv, d), dtype, kv_dtype, k_scale, v_scale)
     lens = np.asarray(lens, dtype=np.int32).reshape(batch)
     return Workload(name or f"contig{config_id}", q, k, v, lens, hq, hkv, d, default_scale(d),
-                    dtype=dtype)
+                    dtype=dtype, kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale)
 
 
 def build_block_table(lens, page: int, max_blocks: int, perm: np.ndarray) -> np.ndarray:
@@ -269,17 +354,19 @@ def build_block_table(lens, page: int, max_blocks: int, perm: np.ndarray) -> np.
 
 def make_paged(config_id: int, batch: int, hq: int, hkv: int, d: int, page: int,
                lens, max_blocks: int, name: str = "", extra_pages: int = 0,
-               dtype: str = "bf16") -> Workload:
+               dtype: str = "bf16", kv_dtype: str | None = None, k_scale: float = 1.0,
+               v_scale: float = 1.0) -> Workload:
     lens = np.asarray(lens, dtype=np.int32).reshape(batch)
     used = int(sum((int(L) + page - 1) // page for L in lens))
     num_pages = max(1, used + extra_pages)
     perm = permutation(seed_for(config_id, TENSOR_PERM), num_pages)
     table = build_block_table(lens, page, max_blocks, perm)
+    k_scale, v_scale = fp32(k_scale), fp32(v_scale)
     q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d), dtype=dtype)
-    k = normal_bf16(seed_for(config_id, TENSOR_K), (num_pages, page, hkv, d), dtype=dtype)
-    v = normal_bf16(seed_for(config_id, TENSOR_V), (num_pages, page, hkv, d), dtype=dtype)
+    k, v = _kv(config_id, (num_pages, page, hkv, d), dtype, kv_dtype, k_scale, v_scale)
     return Workload(name or f"paged{config_id}", q, k, v, lens, hq, hkv, d, default_scale(d),
-                    page_size=page, block_table=table, dtype=dtype)
+                    page_size=page, block_table=table, dtype=dtype, kv_dtype=kv_dtype,
+                    k_scale=k_scale, v_scale=v_scale)
 
 
 def scale_keys(w: Workload, tokens: np.ndarray, factor: float) -> None:

@@ -55,7 +55,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB)
             lib.oracle_attend.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _D, _I,
-                                          _P, _I, _P, _P, _P]
+                                          _I, _D, _D, _P, _I, _P, _P, _P]
             lib.oracle_attend.restype = _I
             lib.oracle_lse_merge.argtypes = [_P, _P, _I, _I, _P, _P]
             lib.oracle_lse_merge.restype = None
@@ -69,20 +69,28 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+_KV_CODES = {"bf16": 0, "f16": 1, "e4m3": 2, "e5m2": 3}
+
+
 def attend_raw(q, k, v, seq_lens, num_q_heads, num_kv_heads, scale, *,
-               page_size=0, block_table=None, items=None, threads=1, dtype="bf16"):
+               page_size=0, block_table=None, items=None, threads=1, dtype="bf16",
+               kv_dtype=None, k_scale=1.0, v_scale=1.0):
     """Oracle attention on raw arrays.
 
-    q: uint16 bf16 (or fp16, dtype='f16') bits [B, Hq, D]; k, v: uint16 [B, S_max, Hkv, D] (contiguous)
-    or [num_pages, P, Hkv, D] (paged, with block_table int32 [B, max_blocks]).
+    q: uint16 bf16 (or fp16, dtype='f16') bits [B, Hq, D]; k, v: [B, S_max, Hkv, D] (contiguous)
+    or [num_pages, P, Hkv, D] (paged, with block_table int32 [B, max_blocks]), uint16 bits of
+    q's type, or (kv_dtype 'e4m3' / 'e5m2') uint8 FP8 codes dequantised by k_scale / v_scale.
     items: int32 [n, 4] rows (b, h, t0, t1), t1 < 0 meaning "to L_b"; default
     is every (b, h) over its whole length.  Returns (o [n, D], lse [n]) in
     fp64; with items=None they are reshaped to [B, Hq, D] and [B, Hq].
     """
     lib = _load()
+    kv_dtype = kv_dtype or dtype
+    kvcode = _KV_CODES[kv_dtype]
+    kv_np = np.uint8 if kvcode >= 2 else np.uint16
     q = np.ascontiguousarray(q, dtype=np.uint16)
-    k = np.ascontiguousarray(k, dtype=np.uint16)
-    v = np.ascontiguousarray(v, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=kv_np)
+    v = np.ascontiguousarray(v, dtype=kv_np)
     lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
     B, hq, d = q.shape
     if page_size:
@@ -107,7 +115,8 @@ def attend_raw(q, k, v, seq_lens, num_q_heads, num_kv_heads, scale, *,
         scratch = np.empty(maxlen, dtype=np.float64)
         rc = lib.oracle_attend(_ptr(q), _ptr(k), _ptr(v), _ptr(lens), B, hq, num_kv_heads, d,
                                s_max, page_size, _ptr(table), max_blocks, num_pages,
-                               float(scale), 1 if dtype == "f16" else 0, _ptr(items[lo:hi]), hi - lo,
+                               float(scale), 1 if dtype == "f16" else 0, kvcode, float(k_scale),
+                               float(v_scale), _ptr(items[lo:hi]), hi - lo,
                                _ptr(scratch),
                                _ptr(o[lo:hi]), _ptr(lse[lo:hi]))
         if rc != 0:
@@ -129,7 +138,9 @@ def attend(w, items=None, threads=1):
     """Oracle attention for a workload object (see ``fd_synth.Workload``)."""
     return attend_raw(w.q, w.k, w.v, w.seq_lens, w.num_q_heads, w.num_kv_heads, w.scale,
                       page_size=w.page_size, block_table=w.block_table, items=items,
-                      threads=threads, dtype=getattr(w, "dtype", "bf16"))
+                      threads=threads, dtype=getattr(w, "dtype", "bf16"),
+                      kv_dtype=getattr(w, "kv_dtype", None), k_scale=getattr(w, "k_scale", 1.0),
+                      v_scale=getattr(w, "v_scale", 1.0))
 
 
 def lse_merge(o_parts, lse_parts):

@@ -32,8 +32,12 @@
  *                          by block, O divided by l at the end), for one
  *                          query row with a vector value of width dv.
  *
- * Inputs are bf16 or IEEE fp16 bit patterns (the first page's tensor-map
- * helper accepts either), widened exactly to fp64.
+ * q is bf16 or IEEE fp16 bit patterns (the first page's tensor-map helper
+ * accepts either), widened exactly to fp64.  K and V hold the same 16-bit
+ * type, or an 8-bit FP8 KV cache ("FlashAttention 与推理算子", the decode
+ * kernel checklist: the KV cache is BF16 or FP8, converted to fp32 in
+ * registers): OCP FP8 E4M3 or E5M2 codes, each tensor with one
+ * dequantisation scale, K_t = k_scale * decode(k8_t) and likewise V.
  *
  * GQA head mapping: query head h reads kv head h / (Hq / Hkv) (consecutive
  * query heads share a kv head).  Paged layout: token t of request b lives
@@ -65,15 +69,63 @@ static double f16_to_f64(uint16_t bits)
     return sign ? -v : v;
 }
 
-/* Element type of q, K and V: 0 = bf16, 1 = fp16. */
+/* Element type of q: 0 = bf16, 1 = fp16. */
 static double elem_to_f64(uint16_t bits, int dtype)
 {
     return dtype ? f16_to_f64(bits) : bf16_to_f64(bits);
 }
 
+/* OCP 8-bit floating point, E4M3 ("fn" form): 1 sign, 4 exponent (bias 7),
+ * 3 fraction bits; exponent 0 holds zero and the subnormals m * 2^-9; there
+ * is no infinity, and S.1111.111 is NaN, so the largest value is 448. */
+static double e4m3_to_f64(uint8_t bits)
+{
+    const int sign = bits >> 7, e = (bits >> 3) & 15, m = bits & 7;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else if (e == 15 && m == 7)
+        v = NAN;
+    else
+        v = ldexp((double)(m + 8), e - 10);   /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* OCP 8-bit floating point, E5M2: 1 sign, 5 exponent (bias 15), 2 fraction
+ * bits, IEEE-style: subnormals m * 2^-16, infinities and NaNs at
+ * exponent 31. */
+static double e5m2_to_f64(uint8_t bits)
+{
+    const int sign = bits >> 7, e = (bits >> 2) & 31, m = bits & 3;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -16);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m + 4), e - 17);   /* (1 + m/4) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* K/V element type: 0 = bf16, 1 = fp16, 2 = FP8 E4M3, 3 = FP8 E5M2. */
+static int kv_elem_bytes(int kvtype) { return kvtype >= 2 ? 1 : 2; }
+
+/* Element j of a K or V row, before its tensor's dequantisation scale. */
+static double kv_elem(const uint8_t *row, int j, int kvtype)
+{
+    if (kvtype == 2)
+        return e4m3_to_f64(row[j]);
+    if (kvtype == 3)
+        return e5m2_to_f64(row[j]);
+    uint16_t bits;
+    memcpy(&bits, row + 2 * (int64_t)j, sizeof bits);
+    return elem_to_f64(bits, kvtype);
+}
+
 /* Where the K (or V) row of logical token t of request b, kv head g lives. */
 typedef struct {
-    const uint16_t *base;     /* K or V */
+    const uint8_t *base;      /* K or V */
+    int esize;                /* bytes per element */
     int paged;
     /* contiguous [B, S_max, Hkv, D] */
     int s_max;
@@ -87,7 +139,7 @@ typedef struct {
 } kv_view;
 
 /* Returns NULL if the token's page is not a valid physical page. */
-static const uint16_t *kv_row(const kv_view *w, int b, int t, int g)
+static const uint8_t *kv_row(const kv_view *w, int b, int t, int g)
 {
     int64_t row;
     if (!w->paged) {
@@ -98,7 +150,7 @@ static const uint16_t *kv_row(const kv_view *w, int b, int t, int g)
             return NULL;
         row = ((int64_t)phys * w->page + t % w->page) * w->hkv + g;
     }
-    return w->base + row * w->d;
+    return w->base + row * w->d * w->esize;
 }
 
 /*
@@ -108,6 +160,7 @@ static const uint16_t *kv_row(const kv_view *w, int b, int t, int g)
  */
 static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
                       int b, int h, int hq, int t0, int t1, double scale, int dtype,
+                      int kvtype, double k_scale, double v_scale,
                       double *s /* scratch, >= t1 - t0 */, double *o, double *lse)
 {
     const int d = kw->d;
@@ -123,15 +176,15 @@ static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
         return 0;
     }
 
-    /* S = scale * q . K_t */
+    /* S = scale * q . K_t, K_t = k_scale * (stored row) */
     double mx = -INFINITY;
     for (int i = 0; i < n; ++i) {
-        const uint16_t *krow = kv_row(kw, b, t0 + i, g);
+        const uint8_t *krow = kv_row(kw, b, t0 + i, g);
         if (!krow)
             return -1;
         double dot = 0.0;
         for (int j = 0; j < d; ++j)
-            dot += elem_to_f64(qrow[j], dtype) * elem_to_f64(krow[j], dtype);
+            dot += elem_to_f64(qrow[j], dtype) * (k_scale * kv_elem(krow, j, kvtype));
         s[i] = scale * dot;
         if (s[i] > mx)
             mx = s[i];
@@ -147,18 +200,20 @@ static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
 
     /* O = sum_t P_t V_t */
     for (int i = 0; i < n; ++i) {
-        const uint16_t *vrow = kv_row(vw, b, t0 + i, g);
+        const uint8_t *vrow = kv_row(vw, b, t0 + i, g);
         if (!vrow)
             return -1;
         const double p = s[i] / z;
         for (int j = 0; j < d; ++j)
-            o[j] += p * elem_to_f64(vrow[j], dtype);
+            o[j] += p * (v_scale * kv_elem(vrow, j, kvtype));
     }
     return 0;
 }
 
 /*
- * dtype: 0 when q, K and V hold bf16 bit patterns, 1 for IEEE fp16.
+ * dtype: 0 when q holds bf16 bit patterns, 1 for IEEE fp16.  kvtype: the
+ * K/V element type (0 bf16, 1 fp16, 2 FP8 E4M3, 3 FP8 E5M2); k_scale and
+ * v_scale multiply every decoded K and V element (1 for 16-bit caches).
  * For each of npairs items (b, h, t0, t1) in `items` (int32, 4 per item;
  * t1 < 0 means "to the request's length"), compute the attention of query
  * (b, h) over tokens [t0, min(t1, L_b)).  o is [npairs][d], lse [npairs].
@@ -167,18 +222,20 @@ static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
  * scratch must hold max token count doubles.  Returns 0, or -1 on a bad page
  * or a length outside the layout.
  */
-int oracle_attend(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+int oracle_attend(const uint16_t *q, const void *k, const void *v,
                   const int32_t *seq_lens, int batch, int hq, int hkv, int d,
                   int s_max, int page_size, const int32_t *block_table,
                   int max_blocks, int num_pages, double scale, int dtype,
+                  int kvtype, double k_scale, double v_scale,
                   const int32_t *items, int npairs, double *scratch,
                   double *o, double *lse)
 {
-    if (hkv <= 0 || hq % hkv != 0)
+    if (hkv <= 0 || hq % hkv != 0 || kvtype < 0 || kvtype > 3)
         return -1;
-    kv_view kw = {k, page_size > 0, s_max, block_table, max_blocks, page_size, num_pages, hkv, d};
+    kv_view kw = {(const uint8_t *)k, kv_elem_bytes(kvtype), page_size > 0, s_max, block_table,
+                  max_blocks, page_size, num_pages, hkv, d};
     kv_view vw = kw;
-    vw.base = v;
+    vw.base = (const uint8_t *)v;
     for (int i = 0; i < npairs; ++i) {
         const int b = items[4 * i + 0], h = items[4 * i + 1];
         int t0 = items[4 * i + 2], t1 = items[4 * i + 3];
@@ -195,8 +252,8 @@ int oracle_attend(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             t1 = L;
         if (t0 < 0)
             t0 = 0;
-        if (attend_one(q, &kw, &vw, b, h, hq, t0, t1, scale, dtype, scratch,
-                       o + (int64_t)i * d, lse + i) != 0)
+        if (attend_one(q, &kw, &vw, b, h, hq, t0, t1, scale, dtype, kvtype, k_scale, v_scale,
+                       scratch, o + (int64_t)i * d, lse + i) != 0)
             return -1;
     }
     return 0;

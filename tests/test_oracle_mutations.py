@@ -1,8 +1,8 @@
 """Plant plausible mistakes in a copy of the oracle and check the pins catch each.
 
 Every mutant is compiled from a modified copy of ``oracle/attn_ref.c`` in a
-temporary directory, on the CPU, and the pin suite ``tests/test_oracle.py``
-must fail (or crash) against it.  The committed oracle is never modified.
+temporary directory, on the CPU, and the pin suites ``tests/test_oracle.py``
+and ``tests/test_oracle_fp8.py`` must fail (or crash) against it.  The committed oracle is never modified.
 """
 import os
 import shutil
@@ -20,8 +20,8 @@ MUTANTS = {
     "page slot and page index swapped": (
         "row = ((int64_t)phys * w->page + t % w->page) * w->hkv + g;",
         "row = ((int64_t)phys * w->page + t / w->page) * w->hkv + g;"),
-    "K read in place of V": ("const uint16_t *vrow = kv_row(vw, b, t0 + i, g);",
-                             "const uint16_t *vrow = kv_row(kw, b, t0 + i, g);"),
+    "K read in place of V": ("const uint8_t *vrow = kv_row(vw, b, t0 + i, g);",
+                             "const uint8_t *vrow = kv_row(kw, b, t0 + i, g);"),
     "ln Z dropped from LSE": ("*lse = mx + log(z);", "*lse = mx;"),
     "merge weight not normalised": ("const double w = exp(lse_parts[i] - g);",
                                     "const double w = exp(lse_parts[i] - lse_max);"),
@@ -31,6 +31,18 @@ MUTANTS = {
     "last token dropped": ("const int n = t1 - t0;", "const int n = t1 - t0 - (t1 - t0 > 1);"),
     "fp16 exponent bias off by one": ("v = ldexp((double)(m + 1024), e - 25);", "v = ldexp((double)(m + 1024), e - 24);"),
     "fp16 subnormals flushed": ("v = ldexp((double)m, -24);", "v = 0.0;"),
+    "e4m3 exponent bias off by one": ("v = ldexp((double)(m + 8), e - 10);",
+                                      "v = ldexp((double)(m + 8), e - 9);"),
+    "e4m3 subnormals flushed": ("v = ldexp((double)m, -9);", "v = 0.0;"),
+    "e4m3 top exponent taken as NaN": ("else if (e == 15 && m == 7)", "else if (e == 15)"),
+    "e5m2 decoded as e4m3": ("        return e5m2_to_f64(row[j]);", "        return e4m3_to_f64(row[j]);"),
+    "e5m2 exponent bias off by one": ("v = ldexp((double)(m + 4), e - 17);",
+                                      "v = ldexp((double)(m + 4), e - 16);"),
+    "k_scale applied to V": ("o[j] += p * (v_scale * kv_elem(vrow, j, kvtype));",
+                             "o[j] += p * (k_scale * kv_elem(vrow, j, kvtype));"),
+    "k_scale dropped": ("(k_scale * kv_elem(krow, j, kvtype))", "(kv_elem(krow, j, kvtype))"),
+    "FP8 row stride taken as 2 bytes": ("return w->base + row * w->d * w->esize;",
+                                        "return w->base + row * w->d * 2;"),
 }
 
 
@@ -43,7 +55,7 @@ def test_mutant_is_caught(name, tmp_path):
         shutil.copytree(os.path.join(ROOT, sub), tmp_path / sub,
                         ignore=shutil.ignore_patterns("*.so", "__pycache__", "test_oracle_mutations.py"))
     (tmp_path / "oracle" / "attn_ref.c").write_text(src.replace(before, after))
-    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle.py", "-q", "-x",
-                        "-p", "no:cacheprovider"], cwd=tmp_path, capture_output=True, text=True,
-                       timeout=300)
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle.py",
+                        "tests/test_oracle_fp8.py", "-q", "-x", "-p", "no:cacheprovider"],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant '{name}' passed every pin:\n{r.stdout[-2000:]}"

@@ -138,3 +138,37 @@ def test_f16_rounding_is_nearest_even_from_fp64():
     assert np.array_equal(got, ref)
     with pytest.raises(ValueError):
         syn.f64_to_f16_bits(np.array([70000.0]))
+
+
+# ---------------------------------------------------------------------------
+# FP8 codes (OCP E4M3 / E5M2)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,tdt,vmax", [("e4m3", "float8_e4m3fn", 448.0), ("e5m2", "float8_e5m2", 57344.0)])
+def test_fp8_rounding_matches_torch_and_saturates(fmt, tdt, vmax):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    # fp32-exact inputs: torch converts through fp32, so only those are rounded once there
+    x = (rng.standard_normal(100000) * 10 ** rng.uniform(-5, 3, 100000)).astype(np.float32)
+    x = np.concatenate([x, np.linspace(-vmax, vmax, 20001, dtype=np.float32)]).astype(np.float64)
+    x = x[np.abs(x) <= vmax]
+    ref = torch.from_numpy(x).to(getattr(torch, tdt)).view(torch.uint8).numpy()
+    assert np.array_equal(syn.f64_to_fp8_bits(x, fmt), ref)
+    top = syn.f64_to_fp8_bits(np.array([vmax * 1.2, -1e30, vmax]), fmt)
+    assert top[0] == top[2] and top[1] == (top[0] | 0x80)   # saturate, never NaN or inf
+
+
+def test_fp8_single_rounding_at_halfway_points():
+    """x just above a halfway point rounds up (a detour through fp32 would round to even)."""
+    assert syn.f64_to_fp8_bits(np.array([84.00000000000006]), "e4m3")[0] == 0x6B   # 88 = 1.375 * 2^6
+    assert syn.f64_to_fp8_bits(np.array([84.0]), "e4m3")[0] == 0x6A                # 80 (even fraction)
+    assert syn.f64_to_fp8_bits(np.array([4.500000088419607]), "e5m2")[0] == 0x45   # 5
+
+
+def test_fp8_workload_is_seeded_and_scaled():
+    w = syn.make_contiguous(5, 2, 4, 2, 64, 16, [16, 3], kv_dtype="e4m3", k_scale=0.05, v_scale=0.5)
+    w2 = syn.make_contiguous(5, 2, 4, 2, 64, 16, [16, 3], kv_dtype="e4m3", k_scale=0.05, v_scale=0.5)
+    assert w.k.dtype == np.uint8 and np.array_equal(w.k, w2.k) and np.array_equal(w.v, w2.v)
+    assert w.k_scale == float(np.float32(0.05)) and w.kv_bytes() == 19 * 2 * 64 * 2
+    # codes are x / scale: with k_scale 0.05, |code value| ~ 20 |x|
+    assert 5 < np.median(np.abs(w.k.view(np.int8).astype(np.int64) & 0x7F)) < 127
