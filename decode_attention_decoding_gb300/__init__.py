@@ -25,7 +25,7 @@ __all__ = [
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
     "FD_ERR_CUDA", "FD_ERR_TIMEOUT", "FD_ERR_DEVICE_INPUT", "FD_FLAG_TEST_STARVE_FIRST_TILE",
     "FD_FLAG_CUDA_CORES", "FD_FLAG_NO_4D_BOXES", "FD_FLAG_NO_HEAD_FUSION",
-    "FD_FLAG_FUSE_HEADS",
+    "FD_FLAG_FUSE_HEADS", "FD_KV_AS_Q", "FD_KV_FP8_E4M3", "FD_KV_FP8_E5M2",
     "fd_decode_noalloc",
 ]
 
@@ -36,6 +36,7 @@ FD_FLAG_CUDA_CORES = 0x2
 FD_FLAG_NO_4D_BOXES = 0x4
 FD_FLAG_NO_HEAD_FUSION = 0x8
 FD_FLAG_FUSE_HEADS = 0x10
+FD_KV_AS_Q, FD_KV_FP8_E4M3, FD_KV_FP8_E5M2 = 0, 1, 2
 
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 
@@ -44,7 +45,8 @@ class FdOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("flags", ctypes.c_uint),
                 ("wait_timeout_ns", ctypes.c_ulonglong),
                 ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
 
 
 def library_path() -> str:
@@ -144,6 +146,30 @@ def _bits(t, name):
     return t
 
 
+_FP8_TORCH = {getattr(torch, n): c for n, c in (("float8_e4m3fn", 1), ("float8_e5m2", 2))
+              if hasattr(torch, n)}
+_KV_NAMES = {"e4m3": FD_KV_FP8_E4M3, "e5m2": FD_KV_FP8_E5M2}
+
+
+def _kv_code(k, v, kv_dtype):
+    """FD_KV_* for the cache tensors: FP8 from their torch float8 type or, for
+    uint8 / int8 codes, from kv_dtype ('e4m3' / 'e5m2'); else the type of q."""
+    for t, name in ((k, "k"), (v, "v")):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if kv_dtype is not None:
+        code = _KV_NAMES[kv_dtype]
+        if k.element_size() != 1 or v.element_size() != 1:
+            raise TypeError("an FP8 cache holds one byte per element")
+        return code
+    if k.dtype in _FP8_TORCH:
+        if v.dtype != k.dtype:
+            raise TypeError("k and v must have the same FP8 type")
+        return _FP8_TORCH[k.dtype]
+    _bits(k, "k"); _bits(v, "v")
+    return FD_KV_AS_Q
+
+
 def _i32(t, name):
     if t is None:
         return None
@@ -161,7 +187,8 @@ def _dtype_code(t, dtype):
     return FD_DTYPE_F16 if t.dtype == torch.float16 else FD_DTYPE_BF16
 
 
-def _options(num_ctas, flags, wait_timeout_ns, split_events, dtype_code=FD_DTYPE_BF16):
+def _options(num_ctas, flags, wait_timeout_ns, split_events, dtype_code=FD_DTYPE_BF16,
+             kv_code=FD_KV_AS_Q, k_scale=1.0, v_scale=1.0):
     ev0 = ev1 = None
     if split_events is not None:
         for e in split_events:
@@ -169,7 +196,8 @@ def _options(num_ctas, flags, wait_timeout_ns, split_events, dtype_code=FD_DTYPE
                 raise ValueError("split_events must be created (recorded once) before use")
         ev0 = ctypes.c_void_p(split_events[0].cuda_event)
         ev1 = ctypes.c_void_p(split_events[1].cuda_event)
-    return FdOptions(int(num_ctas), int(flags), int(wait_timeout_ns), ev0, ev1, int(dtype_code))
+    return FdOptions(int(num_ctas), int(flags), int(wait_timeout_ns), ev0, ev1, int(dtype_code),
+                     int(kv_code), float(k_scale), float(v_scale))
 
 
 def _outputs(q, out, lse):
@@ -188,16 +216,20 @@ def _outputs(q, out, lse):
 
 def fd_decode(q, k, v, seq_lens=None, seq_lens_host=None, scale=None, out=None, lse=None,
               workspace=None, num_ctas=0, flags=0, wait_timeout_ns=0, split_events=None,
-              stream=None, check=True, dtype=None):
+              stream=None, check=True, dtype=None, kv_dtype=None, k_scale=1.0, v_scale=1.0):
     """Decode attention over a contiguous KV cache (see fd_decode in include/fd.h).
 
-    q [B, Hq, D], k/v [B, S_max, Hkv, D] bf16 or fp16 CUDA tensors (``dtype``
-    'bf16'/'f16' overrides the tensors' own type, e.g. for int16 views); seq_lens int32 [B]
-    on the device (None = every request has S_max tokens); seq_lens_host an
-    optional CPU int32 copy used only for host-side validation.  Pass
-    ``lse=False`` to skip the LSE output.  Returns (out, lse).
+    q [B, Hq, D] bf16 or fp16 (``dtype`` 'bf16'/'f16' overrides the tensor's
+    own type, e.g. for int16 views); k/v [B, S_max, Hkv, D] of q's type, or an
+    FP8 cache: torch float8_e4m3fn / float8_e5m2 tensors, or uint8 codes with
+    ``kv_dtype`` 'e4m3' / 'e5m2', dequantised by ``k_scale`` / ``v_scale``.
+    seq_lens int32 [B] on the device (None = every request has S_max tokens);
+    seq_lens_host an optional CPU int32 copy used for host-side validation
+    (and to size the launch).  Pass ``lse=False`` to skip the LSE output.
+    Returns (out, lse).
     """
-    _bits(q, "q"); _bits(k, "k"); _bits(v, "v")
+    _bits(q, "q")
+    kv_code = _kv_code(k, v, kv_dtype)
     B, hq, d = q.shape
     _, s_max, hkv, _ = k.shape
     if scale is None:
@@ -205,7 +237,8 @@ def fd_decode(q, k, v, seq_lens=None, seq_lens_host=None, scale=None, out=None, 
     out, lse = _outputs(q, out, lse)
     if workspace is None:
         workspace = make_workspace(B, hq, hkv, d, s_max, 0, q.device)
-    opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype))
+    opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype), kv_code,
+                    k_scale, v_scale)
     lh = None
     if seq_lens_host is not None:
         lh = seq_lens_host.to(torch.int32).contiguous().cpu()
@@ -220,13 +253,15 @@ def fd_decode(q, k, v, seq_lens=None, seq_lens_host=None, scale=None, out=None, 
 
 def fd_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=None, scale=None,
                     out=None, lse=None, workspace=None, num_ctas=0, flags=0, wait_timeout_ns=0,
-                    split_events=None, stream=None, check=True, dtype=None):
+                    split_events=None, stream=None, check=True, dtype=None, kv_dtype=None,
+                    k_scale=1.0, v_scale=1.0):
     """Decode attention over a paged KV cache (see fd_decode_paged in include/fd.h).
 
-    k_pages/v_pages [num_pages, P, Hkv, D] bf16; block_table int32 [B, max_blocks];
-    seq_lens int32 [B] on the device.
+    k_pages/v_pages [num_pages, P, Hkv, D] of q's type or an FP8 cache (as for
+    fd_decode); block_table int32 [B, max_blocks]; seq_lens int32 [B] on the device.
     """
-    _bits(q, "q"); _bits(k_pages, "k_pages"); _bits(v_pages, "v_pages")
+    _bits(q, "q")
+    kv_code = _kv_code(k_pages, v_pages, kv_dtype)
     _i32(block_table, "block_table"); _i32(seq_lens, "seq_lens")
     B, hq, d = q.shape
     num_pages, page, hkv, _ = k_pages.shape
@@ -236,7 +271,8 @@ def fd_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=No
     out, lse = _outputs(q, out, lse)
     if workspace is None:
         workspace = make_workspace(B, hq, hkv, d, max_blocks * page, page, q.device)
-    opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype))
+    opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype), kv_code,
+                    k_scale, v_scale)
     lh = None
     if seq_lens_host is not None:
         lh = seq_lens_host.to(torch.int32).contiguous().cpu()

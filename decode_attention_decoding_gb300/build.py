@@ -3,7 +3,7 @@
 Usage: ``python -m decode_attention_decoding_gb300.build`` or call :func:`build`.
 Each translation unit is compiled by its own nvcc process, in parallel, then
 linked into ``decode_attention_decoding_gb300/libfd.so``.  ``fd_split_inst.cu``
-is compiled once per split-kernel variant (layout x element type x head_dim),
+is compiled once per split-kernel variant (layout x K/V element type x head_dim),
 each with its own defines.  Objects go to ``decode_attention_decoding_gb300/_build/``.
 """
 from __future__ import annotations
@@ -35,7 +35,8 @@ def _nvcc() -> str:
 
 
 SPLIT_INST = "fd_split_inst.cu"
-SPLIT_VARIANTS = [(paged, f16, d) for paged in (0, 1) for f16 in (0, 1) for d in (64, 128, 256)]
+KV_NAMES = ("bf16", "f16", "e4m3", "e5m2")
+SPLIT_VARIANTS = [(paged, kv, d) for paged in (0, 1) for kv in range(4) for d in (64, 128, 256)]
 
 
 def _sources():
@@ -48,11 +49,10 @@ def _units():
     for src in _sources():
         stem = os.path.basename(src)[:-3]
         if os.path.basename(src) == SPLIT_INST:
-            for paged, f16, d in SPLIT_VARIANTS:
-                defs = [f"-DFD_INST_PAGED={'true' if paged else 'false'}",
-                        f"-DFD_INST_F16={'true' if f16 else 'false'}", f"-DFD_INST_D={d}"]
-                units.append((src, f"{stem}_{'paged' if paged else 'contig'}_{'f16' if f16 else 'bf16'}_d{d}",
-                              defs))
+            for paged, kv, d in SPLIT_VARIANTS:
+                defs = [f"-DFD_INST_PAGED={'true' if paged else 'false'}", f"-DFD_INST_KV={kv}",
+                        f"-DFD_INST_D={d}"]
+                units.append((src, f"{stem}_{'paged' if paged else 'contig'}_{KV_NAMES[kv]}_d{d}", defs))
         else:
             units.append((src, stem, []))
     return units

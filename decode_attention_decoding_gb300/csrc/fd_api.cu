@@ -21,7 +21,7 @@ namespace {
 
 using namespace fd;
 
-constexpr int kVersion = 10200;   // 1.2.0
+constexpr int kVersion = 10300;   // 1.3.0
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
 struct DeviceInfo {
@@ -72,22 +72,31 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// A rank-3 view {head_dim, Hkv, rows} of a 16-bit K or V tensor whose rows
-// are (token, kv head) pairs of 2 head_dim bytes; each load is a box of
-// box_rows tokens of one kv head: the whole row, or (swizzled) one 64-dim
+// Tensor-map element type and size of a K/V element type (kKv*).
+CUtensorMapDataType kv_map_type(int kv)
+{
+    return kv == kKvBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                         : (kv == kKvF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+int kv_elem_bytes(int kv) { return kv_is_fp8(kv) ? 1 : 2; }
+
+// A rank-3 view {head_dim, Hkv, rows} of a K or V tensor whose rows are
+// (token, kv head) pairs of head_dim elements; each load is a box of
+// box_rows tokens of one kv head: the whole row, or (swizzled) one 128-byte
 // part of it with the 128-byte swizzle that the tensor-core consumers read.
 fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
-                        bool swizzled, bool f16, int d)
+                        bool swizzled, int kv, int d)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return FD_ERR_CUDA;
-    const cuuint64_t row_bytes = 2u * (cuuint64_t)d;
+    const int eb = kv_elem_bytes(kv);
+    const cuuint64_t row_bytes = (cuuint64_t)eb * (cuuint64_t)d;
     const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)rows};
     const cuuint64_t strides[2] = {row_bytes, (cuuint64_t)hkv * row_bytes};
-    const cuuint32_t box[3] = {(cuuint32_t)(swizzled ? 64 : d), 1u, (cuuint32_t)box_rows};
+    const cuuint32_t box[3] = {(cuuint32_t)(swizzled ? 128 / eb : d), 1u, (cuuint32_t)box_rows};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    const CUresult r = fn(map, kv_map_type(kv), 3,
                           const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -95,22 +104,24 @@ fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long r
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
 }
 
-// A rank-4 view {64 dims, rows, head_dim/64 parts, Hkv} of the same tensor,
-// so that one box {64, box_rows, head_dim/64, 1} carries every
-// 128-byte-swizzled 64-dim part of box_rows rows of one kv head (laid out
-// part by part in shared memory).
+// A rank-4 view {128-byte part, rows, parts, Hkv} of the same tensor (a part
+// is 64 16-bit elements or 128 FP8 codes), so that one box {part, box_rows,
+// parts, 1} carries every 128-byte-swizzled part of box_rows rows of one kv
+// head (laid out part by part in shared memory).
 fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
-                           bool f16, int d)
+                           int kv, int d)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return FD_ERR_CUDA;
-    const cuuint64_t row_bytes = 2u * (cuuint64_t)d;
-    const cuuint64_t dims[4] = {64u, (cuuint64_t)rows, (cuuint64_t)(d / 64), (cuuint64_t)hkv};
+    const int eb = kv_elem_bytes(kv);
+    const cuuint64_t row_bytes = (cuuint64_t)eb * (cuuint64_t)d;
+    const cuuint32_t part = (cuuint32_t)(128 / eb), parts = (cuuint32_t)(row_bytes / 128);
+    const cuuint64_t dims[4] = {part, (cuuint64_t)rows, parts, (cuuint64_t)hkv};
     const cuuint64_t strides[3] = {(cuuint64_t)hkv * row_bytes, 128u, row_bytes};
-    const cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, (cuuint32_t)(d / 64), 1u};
+    const cuuint32_t box[4] = {part, (cuuint32_t)box_rows, parts, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+    const CUresult r = fn(map, kv_map_type(kv), 4,
                           const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -121,7 +132,7 @@ fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long lon
 // box per tile or page carries every swizzled part) and fall back to 3-D
 // maps with one box per 64-dim part if the driver rejects the 4-D view.
 fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, const void *v, int hkv,
-                         long long rows, int box_rows, bool mma, bool f16, int d, SplitParams *sp)
+                         long long rows, int box_rows, bool mma, int kv, int d, SplitParams *sp)
 {
     int rl = 0;
     while ((1 << rl) < box_rows)
@@ -129,15 +140,15 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
     sp->box4d = 0;
     sp->box_rows_log2 = 6;
     if (mma && !(sp->flags & FD_FLAG_NO_4D_BOXES) &&
-        encode_kv_map_4d(tmk, k, hkv, rows, box_rows, f16, d) == FD_OK &&
-        encode_kv_map_4d(tmv, v, hkv, rows, box_rows, f16, d) == FD_OK) {
+        encode_kv_map_4d(tmk, k, hkv, rows, box_rows, kv, d) == FD_OK &&
+        encode_kv_map_4d(tmv, v, hkv, rows, box_rows, kv, d) == FD_OK) {
         sp->box4d = 1;
         sp->box_rows_log2 = rl;
         return FD_OK;
     }
     fd_status st;
-    if ((st = encode_kv_map(tmk, k, hkv, rows, box_rows, mma, f16, d)) != FD_OK ||
-        (st = encode_kv_map(tmv, v, hkv, rows, box_rows, mma, f16, d)) != FD_OK)
+    if ((st = encode_kv_map(tmk, k, hkv, rows, box_rows, mma, kv, d)) != FD_OK ||
+        (st = encode_kv_map(tmv, v, hkv, rows, box_rows, mma, kv, d)) != FD_OK)
         return st;
     return FD_OK;
 }
@@ -147,6 +158,17 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
 bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+
+// fd_options fields in range; FP8 scales must be finite and positive (0 = 1).
+bool options_valid(const fd_options *opts)
+{
+    if (!opts)
+        return true;
+    auto scale_ok = [](float x) { return x == 0.f || (x > 0.f && x < __builtin_huge_valf()); };
+    return opts->num_ctas >= 0 && opts->num_ctas <= kMaxCtas && opts->dtype >= 0 && opts->dtype <= 1 &&
+           opts->kv_dtype >= FD_KV_AS_Q && opts->kv_dtype <= FD_KV_FP8_E5M2 && scale_ok(opts->k_scale) &&
+           scale_ok(opts->v_scale);
+}
 
 // Checks shared by both entry points.  Returns FD_OK or the status to report.
 fd_status check_common(const void *q, const float *o, const void *ws, int batch, int hq, int hkv,
@@ -170,20 +192,22 @@ struct CallPlan {
     int group;
     int head_dim;
     bool mma;   // tensor-core consumers (GQA groups) instead of CUDA cores
-    bool f16;   // IEEE fp16 inputs instead of bf16
+    int kv;     // K/V element type (kKv*): bf16, fp16 (q of the same type) or FP8
 };
 
 // Tensor-core consumers serve GQA groups; paged pools need pages of at least
-// 8 tokens so every page box starts on a 1 KB swizzle boundary.
-bool use_mma(int group, int page_size, const fd_options *opts)
+// 8 tokens so every page box starts on a 1 KB swizzle boundary, and a row
+// must fill at least one 128-byte swizzled part.
+bool use_mma(int group, int page_size, int row_bytes, const fd_options *opts)
 {
     if (opts && (opts->flags & FD_FLAG_CUDA_CORES))
         return false;
-    return group >= 2 && (page_size == 0 || page_size >= 8);
+    return group >= 2 && (page_size == 0 || page_size >= 8) && row_bytes >= 128;
 }
 
-// Fusion pays where a kv head's TMA rows are short (128-byte rows of 64
-// dims, or page boxes under 64 tokens) and the call is long enough for the
+// Fusion pays where a kv head's TMA rows are short (under 256 bytes: 64
+// 16-bit dims or an FP8 row of up to 128 dims, or page boxes under 64
+// tokens) and the call is long enough for the
 // wider tiles: measured on GB300, it lost up to a quarter of the time on
 // calls of under ~24 tiles per CTA (larger tiles, fewer of them per CTA,
 // twice the merge width) and gained 10-85% above that on such rows.
@@ -194,14 +218,14 @@ constexpr double kFuseMinTilesPerCta = 24.0;
 // path only (F * group >= 2 always selects it), for short rows and at least
 // kFuseMinTilesPerCta (estimated) tiles per CTA unless FD_FLAG_FUSE_HEADS
 // forces it; 1 = no fusion.
-int fuse_factor(int group, int hkv, int head_dim, int page_size, double tiles_per_cta,
+int fuse_factor(int group, int hkv, int head_dim, int elem_bytes, int page_size, double tiles_per_cta,
                 const fd_options *opts)
 {
     if (opts && (opts->flags & (FD_FLAG_CUDA_CORES | FD_FLAG_NO_HEAD_FUSION)))
         return 1;
     if (page_size != 0 && page_size < 8)
         return 1;
-    const bool short_rows = head_dim == 64 || (page_size > 0 && page_size < kTileTokens);
+    const bool short_rows = head_dim * elem_bytes < 256 || (page_size > 0 && page_size < kTileTokens);
     const bool forced = opts && (opts->flags & FD_FLAG_FUSE_HEADS);
     if (!forced && (!short_rows || tiles_per_cta < kFuseMinTilesPerCta))
         return 1;
@@ -238,12 +262,12 @@ size_t workspace_bytes_needed(int batch, int hq, int hkv, int head_dim)
 }
 
 // Shared-memory plan of the split kernel for the call's consumers, group,
-// head_dim and batch; fills the offsets and stage count in sp and the byte
-// size in launch.
-fd_status plan_smem(const DeviceInfo &dev, bool mma, int group, int d, int batch, SplitParams *sp,
-                    SplitLaunch *launch)
+// head_dim, K/V element size and batch; fills the offsets and stage count in
+// sp and the byte size in launch.
+fd_status plan_smem(const DeviceInfo &dev, bool mma, int group, int d, int elem_bytes, int batch,
+                    SplitParams *sp, SplitLaunch *launch)
 {
-    const size_t stage_bytes = 2u * kTileTokens * 2u * (size_t)d;   // K and V tiles
+    const size_t stage_bytes = 2u * kTileTokens * (size_t)elem_bytes * (size_t)d;   // K and V tiles
     const size_t red = align_up((size_t)reduction_floats(mma, group, d) * sizeof(float), 16);
     const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
     const size_t misc = 64;
@@ -277,10 +301,16 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     int num_ctas = opts && opts->num_ctas > 0 ? opts->num_ctas : dev.sms;
     if (num_ctas > kMaxCtas)
         return FD_ERR_INVALID_ARG;
+    const bool q_f16 = opts && opts->dtype == FD_DTYPE_F16;
+    const int kv_dtype = opts ? opts->kv_dtype : FD_KV_AS_Q;
+    const int kv = kv_dtype == FD_KV_FP8_E4M3 ? kKvE4m3
+                   : kv_dtype == FD_KV_FP8_E5M2 ? kKvE5m2 : (q_f16 ? kKvF16 : kKvBf16);
+    const int eb = kv_elem_bytes(kv);
     // Launch shape: F fused kv heads of head_dim dims become one head of
     // F * head_dim dims with F * group query heads.
     const int real_group = hq / hkv;
-    const int fuse = fuse_factor(real_group, hkv, head_dim, page_size, (double)est_tiles / num_ctas, opts);
+    const int fuse =
+        fuse_factor(real_group, hkv, head_dim, eb, page_size, (double)est_tiles / num_ctas, opts);
     const int group = fuse * real_group;
     const int d = fuse * head_dim;
     hkv /= fuse;
@@ -309,7 +339,12 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
         ++sp.page_log2;
     sp.max_blocks = max_blocks;
     sp.num_pages = num_pages;
-    sp.scale_log2 = scale * 1.4426950408889634f;
+    // An FP8 cache's k_scale multiplies every score: fold it into the scale.
+    const float k_scale = kv_is_fp8(kv) && opts && opts->k_scale != 0.f ? opts->k_scale : 1.f;
+    const float v_scale = kv_is_fp8(kv) && opts && opts->v_scale != 0.f ? opts->v_scale : 1.f;
+    sp.scale_log2 = scale * k_scale * 1.4426950408889634f;
+    sp.v_scale = v_scale;
+    sp.q_f16 = q_f16 ? 1 : 0;
     sp.timeout_ns = opts && opts->wait_timeout_ns ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     sp.flags = opts ? opts->flags : 0u;
     sp.fuse_dh = fuse > 1 ? head_dim : 0;
@@ -317,13 +352,13 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
 
     cp->group = group;
     cp->head_dim = d;
-    cp->mma = use_mma(group, page_size, opts);
-    cp->f16 = opts && opts->dtype == FD_DTYPE_F16;
+    cp->kv = kv;
+    cp->mma = use_mma(group, page_size, eb * d, opts);
     if (fuse > 1 && !cp->mma)
         return FD_ERR_UNSUPPORTED;   // fusion is defined for the tensor-core consumers only
     cp->launch.grid = num_ctas;
     cp->launch.stream = reinterpret_cast<cudaStream_t>(stream);
-    fd_status st = plan_smem(dev, cp->mma, group, d, batch, &sp, &cp->launch);
+    fd_status st = plan_smem(dev, cp->mma, group, d, eb, batch, &sp, &cp->launch);
     if (st != FD_OK)
         return st;
 
@@ -351,7 +386,7 @@ fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUte
     cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_end_event) : nullptr;
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    cudaError_t e = launch_split(paged, cp.f16, cp.head_dim, cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch);
+    cudaError_t e = launch_split(paged, cp.kv, cp.head_dim, cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch);
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess)
@@ -399,7 +434,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
         for (int b = 0; b < batch; ++b)
             if (seq_lens_host[b] < 0 || seq_lens_host[b] > s_max)
                 return FD_ERR_INVALID_ARG;
-    if (opts && (opts->num_ctas < 0 || opts->num_ctas > kMaxCtas || opts->dtype < 0 || opts->dtype > 1))
+    if (!options_valid(opts))
         return FD_ERR_INVALID_ARG;
     if ((long long)batch * s_max >= (1ll << 31) ||
         (long long)num_kv_heads * batch * ceil_div(s_max, kTileTokens) >= (1ll << 31))
@@ -420,7 +455,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
         return st;
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
-    if ((st = encode_kv_maps(&tmk, &tmv, k, v, cp.sp.hkv, rows, kTileTokens, cp.mma, cp.f16, cp.head_dim,
+    if ((st = encode_kv_maps(&tmk, &tmv, k, v, cp.sp.hkv, rows, kTileTokens, cp.mma, cp.kv, cp.head_dim,
                              &cp.sp)) != FD_OK)
         return st;
     return run(cp, false, tmk, tmv, opts);
@@ -450,7 +485,7 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
         for (int b = 0; b < batch; ++b)
             if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap)
                 return FD_ERR_INVALID_ARG;
-    if (opts && (opts->num_ctas < 0 || opts->num_ctas > kMaxCtas || opts->dtype < 0 || opts->dtype > 1))
+    if (!options_valid(opts))
         return FD_ERR_INVALID_ARG;
     if (workspace_bytes <
         fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, (int)cap, page_size))
@@ -470,7 +505,7 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)num_pages * page_size;
     const int box = page_size < kTileTokens ? page_size : kTileTokens;
-    if ((st = encode_kv_maps(&tmk, &tmv, k_pages, v_pages, cp.sp.hkv, rows, box, cp.mma, cp.f16,
+    if ((st = encode_kv_maps(&tmk, &tmv, k_pages, v_pages, cp.sp.hkv, rows, box, cp.mma, cp.kv,
                              cp.head_dim, &cp.sp)) != FD_OK)
         return st;
     return run(cp, true, tmk, tmv, opts);

@@ -207,6 +207,53 @@ __device__ __forceinline__ float2 x2_to_float2(uint32_t w)
         return bf16x2_to_float2(w);
 }
 
+// Element types of the K/V cache.  bf16 and fp16 caches come with a query of
+// the same type; an FP8 cache (OCP E4M3 or E5M2 codes) with a bf16 or fp16
+// query chosen at run time.
+enum : int { kKvBf16 = 0, kKvF16 = 1, kKvE4m3 = 2, kKvE5m2 = 3 };
+
+__host__ __device__ constexpr bool kv_is_fp8(int kv) { return kv >= kKvE4m3; }
+
+// Two FP8 codes (element 0 in the low byte) to two fp16 values (element 0 in
+// the low half).  Every E4M3 and E5M2 value is an fp16 value, so the
+// conversion is exact.
+template <int KV>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t w)
+{
+    uint32_t r;
+    if constexpr (KV == kKvE4m3)
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(w));
+    else
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(w));
+    return r;
+}
+
+// Low and high 16-bit halves of a word.
+__device__ __forceinline__ uint16_t lo16(uint32_t w) { return (uint16_t)(w & 0xFFFFu); }
+__device__ __forceinline__ uint16_t hi16(uint32_t w) { return (uint16_t)(w >> 16); }
+
+// Byte permute: result byte i = byte sel_i of {b, a} (a holds bytes 0..3).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// Two FP8 codes to fp32.
+template <int KV>
+__device__ __forceinline__ float2 fp8x2_to_float2(uint16_t w)
+{
+    return f16x2_to_float2(fp8x2_to_f16x2<KV>(w));
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
     uint4 v;

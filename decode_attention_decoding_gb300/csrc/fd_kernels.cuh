@@ -37,22 +37,26 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kSplitThreads = kConsumerThreads + 32;
 constexpr int kPairs = kConsumerWarps / 2;
-constexpr int kPartBytes = kTileTokens * 128;           // 64 rows x 64 dims: one swizzled part
+constexpr int kPartBytes = kTileTokens * 128;           // 64 rows x 128 bytes: one swizzled part
 constexpr int kMaxStages = 16;
 constexpr int kMetaInts = 8;
 constexpr int kRowsPerWarp = kTileTokens / kConsumerWarps;   // 8
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
-// Sizes that follow from the head dimension D (64, 128 or 256).
-template <int D>
-struct HeadDim {
+// Sizes that follow from the head dimension D (64, 128 or 256) and the K/V
+// element type KV (16-bit, or 8-bit FP8 codes).
+template <int D, int KV>
+struct Shape {
     static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
-    static constexpr int kRowBytes = D * 2;                   // one 16-bit K or V row
+    static constexpr int kElemBytes = kv_is_fp8(KV) ? 1 : 2;
+    static constexpr int kRowBytes = D * kElemBytes;          // one K or V row
     static constexpr int kTileBytes = kTileTokens * kRowBytes;
     static constexpr int kStageBytes = 2 * kTileBytes;        // K tile + V tile
-    static constexpr int kParts = D / 64;                     // 128-byte swizzled parts of a row
-    static constexpr int kLanesPerRow = D / 8;                // CUDA cores: 8 dims per lane
+    static constexpr int kParts = kRowBytes / 128;            // 128-byte swizzled parts of a row
+    static constexpr int kPartElems = 128 / kElemBytes;       // elements of one part
+    static constexpr int kLanesPerRow = D / 8;                // CUDA cores: 8 elements per lane
+    static constexpr int kLaneBytes = 8 * kElemBytes;
     static constexpr int kRowsPerStep = 32 / kLanesPerRow;    // rows a warp reads at once
     static constexpr int kRowsPerGroup = kRowsPerWarp / kRowsPerStep;
     static constexpr int kKSteps = D / 16;                    // tensor cores: k-steps of q.K^T
@@ -103,6 +107,8 @@ struct SplitParams {
     // zeros for q elsewhere and writes only its own dims.  q and o rows then
     // hold fuse_dh values.  0: no fusion (q and o rows hold D values).
     int fuse_dh, fuse_g;
+    int q_f16;        // FP8 caches: 1 when q is fp16, 0 when bf16
+    float v_scale;    // multiplies O (an FP8 cache's V dequantisation scale; 1 otherwise)
 };
 
 struct MergeParams {
@@ -217,7 +223,7 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
 
 // ------------------------------------------------------------------ producer
 
-template <bool PAGED, bool SW128, int D>
+template <bool PAGED, bool SW128, int D, int KV>
 __device__ __forceinline__ void split_producer(const SplitParams &p, const CUtensorMap *tmk,
                                                const CUtensorMap *tmv, uint32_t stage0,
                                                const int *prefix, int *meta, uint32_t full0,
@@ -234,9 +240,9 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     const uint64_t policy = l2_policy_evict_first();
     const int NS = p.num_stages;
     const bool starve = (p.flags & 1u) && blockIdx.x == 0;
-    using HD = HeadDim<D>;
+    using HD = Shape<D, KV>;
     // Boxes per (tile or page): K and V, each whole (plain or 4-D swizzled)
-    // or as D/64 swizzled 64-dim parts.
+    // or as one box per 128-byte swizzled part.
     const int box_log2 = (SW128 && !p.box4d) ? 1 + (HD::kParts == 4 ? 2 : HD::kParts - 1) : 1;
     const int kBoxes = 1 << box_log2;
     const int page_log2 = p.page_log2;   // pages under 64 tokens are powers of two
@@ -289,11 +295,11 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
         if (SW128 && p.box4d) {   // box 0: K, box 1: V; all parts in one box
             tma_load_4d(((box & 1) ? vdst : kdst) + r0 * HD::kRowBytes, (box & 1) ? tmv : tmk, full, 0, row,
                         0, h, policy);
-        } else if constexpr (SW128) {   // one box per 64-dim part
+        } else if constexpr (SW128) {   // one box per 128-byte part
             const int part = box & (HD::kParts - 1);
             const bool is_v = box >= HD::kParts;
             const uint32_t dst = (is_v ? vdst : kdst) + part * kPartBytes + r0 * 128;
-            tma_load_3d(dst, is_v ? tmv : tmk, full, part * 64, h, row, policy);
+            tma_load_3d(dst, is_v ? tmv : tmk, full, part * HD::kPartElems, h, row, policy);
         } else {
             const uint32_t dst = ((box & 1) ? vdst : kdst) + r0 * HD::kRowBytes;
             tma_load_3d(dst, (box & 1) ? tmv : tmk, full, 0, h, row, policy);
@@ -418,7 +424,7 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
             ltrue += wt * red_lt[w * G + g];
             o += wt * red_acc[(w * G + g) * D + d];
         }
-        const float out = lsum > 0.f ? o / lsum : 0.f;
+        const float out = lsum > 0.f ? (o / lsum) * p.v_scale : 0.f;
         const float lse_v = ltrue > 0.f ? (M + log2f(ltrue)) * kLn2 : kNegInf;
         if (own) {
             const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
@@ -433,15 +439,47 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
     }
 }
 
-template <int G, bool F16, int D>
+// Eight consecutive K or V elements of a shared-memory row, widened to fp32:
+// one 16-byte load of 16-bit values, or one 8-byte load of FP8 codes.
+template <int KV>
+__device__ __forceinline__ void load_row8(uint32_t addr, float2 (&x)[4])
+{
+    if constexpr (kv_is_fp8(KV)) {
+        const uint2 w = lds64(addr);
+        x[0] = fp8x2_to_float2<KV>(lo16(w.x));
+        x[1] = fp8x2_to_float2<KV>(hi16(w.x));
+        x[2] = fp8x2_to_float2<KV>(lo16(w.y));
+        x[3] = fp8x2_to_float2<KV>(hi16(w.y));
+    } else {
+        const uint4 w = lds128(addr);
+        x[0] = x2_to_float2<KV == kKvF16>(w.x);
+        x[1] = x2_to_float2<KV == kKvF16>(w.y);
+        x[2] = x2_to_float2<KV == kKvF16>(w.z);
+        x[3] = x2_to_float2<KV == kKvF16>(w.w);
+    }
+}
+
+// The query's element type: that of a 16-bit cache, chosen at run time for
+// an FP8 cache.
+template <int KV>
+__device__ __forceinline__ bool q_is_f16(const SplitParams &p)
+{
+    if constexpr (kv_is_fp8(KV))
+        return p.q_f16 != 0;
+    else
+        return KV == kKvF16;
+}
+
+template <int G, int KV, int D>
 __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *smem, uint32_t stage0,
                                                const int *meta, uint32_t full0, uint32_t empty0,
                                                uint32_t cbar, volatile int *abort_flag, int t_begin,
                                                int t_end, int cw, int lane)
 {
-    using HD = HeadDim<D>;
+    using HD = Shape<D, KV>;
     constexpr int LPR = HD::kLanesPerRow, RPS = HD::kRowsPerStep, RPG = HD::kRowsPerGroup;
     const int NS = p.num_stages;
+    const bool qf16 = q_is_f16<KV>(p);
     const int sub = lane / LPR, li = lane % LPR;   // row slot within a warp step, lane within the row
     float *red_acc = reinterpret_cast<float *>(smem + p.off_red);   // [warps][G][D]
     float *red_m = red_acc + kConsumerWarps * G * D;                 // [warps][G]
@@ -490,14 +528,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             for (int g = 0; g < G; ++g) {
                 const uint16_t *qp = p.q + ((size_t)b * p.hq + (size_t)h * G + g) * D + li * 8;
                 const uint4 raw = ldg128_nc(qp);
-                qf[g][0] = mul2(x2_to_float2<F16>(raw.x), c2);
-                qf[g][1] = mul2(x2_to_float2<F16>(raw.y), c2);
-                qf[g][2] = mul2(x2_to_float2<F16>(raw.z), c2);
-                qf[g][3] = mul2(x2_to_float2<F16>(raw.w), c2);
+                const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    qf[g][c] = mul2(qf16 ? f16x2_to_float2(rw[c]) : bf16x2_to_float2(rw[c]), c2);
             }
         }
 
-        const uint32_t kbase = stage0 + s * HD::kStageBytes + li * 16;
+        const uint32_t kbase = stage0 + s * HD::kStageBytes + li * HD::kLaneBytes;
         const uint32_t vbase = kbase + HD::kTileBytes;
 
         // Rows of this lane group, kSub at a time.
@@ -508,15 +546,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 #pragma unroll
             for (int r = 0; r < kSub; ++r) {
                 const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
-                const uint4 kw = lds128(kbase + row * HD::kRowBytes);
-                const float2 k0 = x2_to_float2<F16>(kw.x), k1 = x2_to_float2<F16>(kw.y);
-                const float2 k2 = x2_to_float2<F16>(kw.z), k3 = x2_to_float2<F16>(kw.w);
+                float2 kx[4];
+                load_row8<KV>(kbase + row * HD::kRowBytes, kx);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    float2 a = mul2(qf[g][0], k0);
-                    a = fma2(qf[g][1], k1, a);
-                    a = fma2(qf[g][2], k2, a);
-                    a = fma2(qf[g][3], k3, a);
+                    float2 a = mul2(qf[g][0], kx[0]);
+                    a = fma2(qf[g][1], kx[1], a);
+                    a = fma2(qf[g][2], kx[2], a);
+                    a = fma2(qf[g][3], kx[3], a);
                     sc[r][g] = a.x + a.y;
                 }
             }
@@ -564,16 +601,15 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             for (int r = 0; r < kSub; ++r) {
                 const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
                 if (row < nvalid) {
-                    const uint4 vw = lds128(vbase + row * HD::kRowBytes);
-                    const float2 v0 = x2_to_float2<F16>(vw.x), v1 = x2_to_float2<F16>(vw.y);
-                    const float2 v2 = x2_to_float2<F16>(vw.z), v3 = x2_to_float2<F16>(vw.w);
+                    float2 vx[4];
+                    load_row8<KV>(vbase + row * HD::kRowBytes, vx);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         const float2 p2 = make_float2(pr[r][g], pr[r][g]);
-                        acc[g][0] = fma2(p2, v0, acc[g][0]);
-                        acc[g][1] = fma2(p2, v1, acc[g][1]);
-                        acc[g][2] = fma2(p2, v2, acc[g][2]);
-                        acc[g][3] = fma2(p2, v3, acc[g][3]);
+                        acc[g][0] = fma2(p2, vx[0], acc[g][0]);
+                        acc[g][1] = fma2(p2, vx[1], acc[g][1]);
+                        acc[g][2] = fma2(p2, vx[2], acc[g][2]);
+                        acc[g][3] = fma2(p2, vx[3], acc[g][3]);
                     }
                 }
             }
@@ -665,26 +701,46 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 // scores (so each holds the softmax state), and for P.V warp 2i covers the
 // first half of the head dimension and warp 2i+1 the second.
 
-// Byte address of 16-byte chunk `chunk` (0 .. D/8-1) of `row` in a swizzled
-// tile made of boxes of 2^rl rows, each box laid out [64-dim part][row][128 B].
-// With rl = 6 (one 64-row box per part) the tile is D/64 parts of 8 KB.
-template <int D>
+// Byte address of 16-byte chunk `chunk` (0 .. row bytes / 16 - 1) of `row`
+// in a swizzled tile made of boxes of 2^rl rows, each box laid out
+// [128-byte part][row][128 B].  With rl = 6 (one 64-row box per part) the
+// tile is PARTS parts of 8 KB.
+template <int PARTS>
 __device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk, int rl)
 {
     const int rb = row >> rl, rr = row & ((1 << rl) - 1);
-    return tile + ((((rb * HeadDim<D>::kParts) + (chunk >> 3)) << rl) + rr) * 128 +
-           (((chunk & 7) ^ (row & 7)) << 4);
+    return tile + ((((rb * PARTS) + (chunk >> 3)) << rl) + rr) * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
-template <int G, bool F16, int D>
+// FP8 caches on the tensor cores.  K and V stay FP8 codes in shared memory
+// and are converted to fp16 pairs in registers (exactly), so the products run
+// as fp16 MMAs:
+//   * K: an ldmatrix of b16 units over a 16-byte chunk gives each lane four
+//     consecutive codes, dims 4 qd .. 4 qd + 3 of the chunk.  The MMA's k
+//     order is free as long as A and B agree, so k-step positions 2 qd, 2qd+1
+//     take dims 4 qd, 4 qd + 1 and positions 2 qd + 8, + 9 take 4 qd + 2, + 3;
+//     the query's B fragment is loaded in the same order.
+//   * V^T: an ldmatrix.trans of b16 units gives each lane, for tokens 2 qd
+//     and 2 qd + 1, the codes of dims 2 grp and 2 grp + 1; one byte permute
+//     pairs the two tokens per dim.  So output row grp of a 16-dim tile is dim
+//     2 grp and row grp + 8 is dim 2 grp + 1.
+//   * q: fp16 has a narrower range than bf16, so each query head is scaled by
+//     a power of two that puts its largest |element| in [2^14, 2^15) before
+//     the conversion (exact for every element that stays an fp16 normal), and
+//     the score is multiplied back by the same power of two.
+
+template <int G, int KV, int D>
 __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t *smem, uint32_t stage0,
                                                    const int *meta, uint32_t full0, uint32_t empty0,
                                                    uint32_t cbar, volatile int *abort_flag, int t_begin,
                                                    int t_end, int cw, int lane)
 {
     static_assert(G >= 1 && G <= 8, "one n8 tile of query heads");
-    using HD = HeadDim<D>;
+    using HD = Shape<D, KV>;
     constexpr int KS = HD::kKSteps, DT = HD::kDimTilesPerWarp;
+    constexpr bool FP8 = kv_is_fp8(KV);
+    constexpr bool MMA_F16 = KV != kKvBf16;   // fp16 MMAs for fp16 and FP8 caches
+    static_assert(HD::kParts >= 1, "tensor-core rows span at least one 128-byte part");
     const int NS = p.num_stages;
     const int pair = cw >> 1, dhalf = cw & 1;
     const int grp = lane >> 2, qd = lane & 3;   // mma fragment coordinates
@@ -696,6 +752,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
     const int ctid = cw * 32 + lane;
 
     uint32_t qb[KS][2];        // Q^T B-fragments, one pair per 16-dim k-step
+    float smul[2];             // score multipliers of heads 2 qd, 2 qd + 1 (log2 units)
     float acc[DT][4];          // O^T fragments of this warp's D/32 dim tiles
     // heads 2 qd and 2 qd + 1, this lane's tokens only: l sums the 16-bit
     // rounded weights that multiply V, lt the exact fp32 weights (for the LSE)
@@ -723,6 +780,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
         qb[ks][0] = qb[ks][1] = 0u;
+    smul[0] = smul[1] = p.scale_log2;
 
     int s = 0;
     uint32_t ph = 0, cph = 0;
@@ -735,19 +793,60 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         const int b = mt[0], h = mt[1], nvalid = mt[3], flags = mt[4], u = mt[5];
 
         if (flags & kFirstInCta) {
-            // B[k = d][n = head]: lane holds head `grp`, dims 16 ks + 2 qd (+1) and (+8, +9).
             // A fused head's query reads its own fuse_dh dims; zeros elsewhere.
-            if (grp < G) {
-                const int qdim = p.fuse_dh ? p.fuse_dh : D;
-                const int part = fused_part(p.fuse_dh, p.fuse_g, grp);
-                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                    p.q + ((size_t)b * p.hq + (size_t)h * G + grp) * qdim);
+            const int qdim = p.fuse_dh ? p.fuse_dh : D;
+            const int part = fused_part(p.fuse_dh, p.fuse_g, grp);
+            const uint16_t *qrow = p.q + ((size_t)b * p.hq + (size_t)h * G + (grp < G ? grp : 0)) * qdim;
+            if constexpr (!FP8) {
+                // B[k = d][n = head]: lane holds head `grp`, dims 16 ks + 2 qd (+1) and (+8, +9).
+                const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     const int d0 = ks * 16 - part;   // first dim of this k-step in the q row
-                    const bool in = d0 >= 0 && d0 < qdim;
-                    qb[ks][0] = in ? __ldg(qrow + d0 / 2 + qd) : 0u;
-                    qb[ks][1] = in ? __ldg(qrow + d0 / 2 + 4 + qd) : 0u;
+                    const bool in = grp < G && d0 >= 0 && d0 < qdim;
+                    qb[ks][0] = in ? __ldg(q32 + d0 / 2 + qd) : 0u;
+                    qb[ks][1] = in ? __ldg(q32 + d0 / 2 + 4 + qd) : 0u;
+                }
+            } else {
+                // lane holds head `grp`, dims 16 ks + 4 qd .. + 3 (see above)
+                const bool qf16 = p.q_f16 != 0;
+                float qv[KS][4];
+                float amax = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int d0 = ks * 16 - part;
+                    const bool in = grp < G && d0 >= 0 && d0 < qdim;
+                    uint2 w = make_uint2(0u, 0u);
+                    if (in)
+                        w = __ldg(reinterpret_cast<const uint2 *>(qrow + d0 + 4 * qd));
+                    const float2 lo = qf16 ? f16x2_to_float2(w.x) : bf16x2_to_float2(w.x);
+                    const float2 hi = qf16 ? f16x2_to_float2(w.y) : bf16x2_to_float2(w.y);
+                    qv[ks][0] = lo.x;
+                    qv[ks][1] = lo.y;
+                    qv[ks][2] = hi.x;
+                    qv[ks][3] = hi.y;
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(hi.x), fabsf(hi.y))));
+                }
+                // the head's max over its four lanes (same grp)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                // power of two sh with amax * 2^-sh in [2^14, 2^15); zero heads keep sh = 0
+                int sh = 0;
+                if (amax > 0.f) {
+                    const int e = ((__float_as_int(amax) >> 23) & 255) - 127;   // floor(log2 amax), normals
+                    sh = min(max(e - 14, -120), 126);
+                }
+                const float down = __int_as_float((127 - sh) << 23);   // 2^-sh
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    qb[ks][0] = pack_f16x2(qv[ks][0] * down, qv[ks][1] * down);
+                    qb[ks][1] = pack_f16x2(qv[ks][2] * down, qv[ks][3] * down);
+                }
+                // this lane's score columns are heads 2 qd and 2 qd + 1 (held by lanes 4 head)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int shj = __shfl_sync(0xffffffffu, sh, (2 * qd + j) * 4);
+                    smul[j] = p.scale_log2 * __int_as_float((127 + shj) << 23);
                 }
             }
         }
@@ -759,20 +858,35 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
         {
             const int row = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            if constexpr (!FP8) {
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(sw128_addr<D>(ktile, row, 2 * ks + (lane >> 4), rl), a0, a1, a2, a3);
-                mma_16816<F16>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(sw128_addr<HD::kParts>(ktile, row, 2 * ks + (lane >> 4), rl), a0, a1, a2, a3);
+                    mma_16816<MMA_F16>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
+            } else {
+                // one ldmatrix covers two 16-dim chunks: k-steps 2 kk and 2 kk + 1
+#pragma unroll
+                for (int kk = 0; kk < KS / 2; ++kk) {
+                    uint32_t r0, r1, r2, r3;
+                    ldmatrix_x4(sw128_addr<HD::kParts>(ktile, row, 2 * kk + (lane >> 4), rl), r0, r1, r2, r3);
+                    mma_16816<true>(sc, fp8x2_to_f16x2<KV>(lo16(r0)), fp8x2_to_f16x2<KV>(lo16(r1)),
+                                    fp8x2_to_f16x2<KV>(hi16(r0)), fp8x2_to_f16x2<KV>(hi16(r1)), qb[2 * kk][0],
+                                    qb[2 * kk][1]);
+                    mma_16816<true>(sc, fp8x2_to_f16x2<KV>(lo16(r2)), fp8x2_to_f16x2<KV>(lo16(r3)),
+                                    fp8x2_to_f16x2<KV>(hi16(r2)), fp8x2_to_f16x2<KV>(hi16(r3)),
+                                    qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
+                }
             }
         }
         const bool v0 = tok0 + grp < nvalid, v1 = tok0 + grp + 8 < nvalid;
         // sc[0]: (token grp, head 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1)
         float x[4];
-        x[0] = v0 ? sc[0] * p.scale_log2 : kNegInf;
-        x[1] = v0 ? sc[1] * p.scale_log2 : kNegInf;
-        x[2] = v1 ? sc[2] * p.scale_log2 : kNegInf;
-        x[3] = v1 ? sc[3] * p.scale_log2 : kNegInf;
+        x[0] = v0 ? sc[0] * smul[0] : kNegInf;
+        x[1] = v0 ? sc[1] * smul[1] : kNegInf;
+        x[2] = v1 ? sc[2] * smul[0] : kNegInf;
+        x[3] = v1 ? sc[3] * smul[1] : kNegInf;
 
         // Online softmax over this warp's 16 tokens, per head.
         float alpha[2], pw[4];
@@ -788,10 +902,10 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             pw[j + 2] = (x[j + 2] == kNegInf) ? 0.f : exp2_approx(x[j + 2] - m_new);
             m[j] = m_new;
         }
-        const uint32_t p_lo = pack_x2<F16>(pw[0], pw[1]);   // token grp, heads 2qd, 2qd+1
-        const uint32_t p_hi = pack_x2<F16>(pw[2], pw[3]);   // token grp + 8
+        const uint32_t p_lo = pack_x2<MMA_F16>(pw[0], pw[1]);   // token grp, heads 2qd, 2qd+1
+        const uint32_t p_hi = pack_x2<MMA_F16>(pw[2], pw[3]);   // token grp + 8
         {
-            const float2 r_lo = x2_to_float2<F16>(p_lo), r_hi = x2_to_float2<F16>(p_hi);
+            const float2 r_lo = x2_to_float2<MMA_F16>(p_lo), r_hi = x2_to_float2<MMA_F16>(p_hi);
             l[0] = l[0] * alpha[0] + (r_lo.x + r_hi.x);
             l[1] = l[1] * alpha[1] + (r_lo.y + r_hi.y);
             lt[0] = lt[0] * alpha[0] + (pw[0] + pw[2]);
@@ -805,30 +919,49 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         // tensor core would form 0 * NaN: zero this warp's half of them.
         const bool ragged = nvalid < tok0 + 16;
         if (ragged) {
-            constexpr int kChunks = D / 16;   // 16-byte chunks in half a row
+            constexpr int kChunks = HD::kRowBytes / 32;   // 16-byte chunks in half a row
             const int first = nvalid > tok0 ? nvalid : tok0;
             for (int idx = lane; idx < (tok0 + 16 - first) * kChunks; idx += 32) {
-                const uint32_t a = sw128_addr<D>(vtile, first + idx / kChunks,
-                                                 dhalf * kChunks + idx % kChunks, rl);
+                const uint32_t a = sw128_addr<HD::kParts>(vtile, first + idx / kChunks,
+                                                          dhalf * kChunks + idx % kChunks, rl);
                 asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
             }
             __syncwarp();
         }
 
         // O^T = alpha O^T + V^T . P^T over this warp's D/2 dims.
-        {
+#pragma unroll
+        for (int i = 0; i < DT; ++i) {
+            acc[i][0] *= alpha[0];
+            acc[i][1] *= alpha[1];
+            acc[i][2] *= alpha[0];
+            acc[i][3] *= alpha[1];
+        }
+        if constexpr (!FP8) {
             const int vrow = tok0 + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
             for (int i = 0; i < DT; ++i) {
-                acc[i][0] *= alpha[0];
-                acc[i][1] *= alpha[1];
-                acc[i][2] *= alpha[0];
-                acc[i][3] *= alpha[1];
                 const int dt = dhalf * DT + i;   // 16-dim tile index
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(sw128_addr<D>(vtile, vrow, 2 * dt + ((lane >> 3) & 1), rl), a0, a1, a2,
-                                  a3);
-                mma_16816<F16>(acc[i], a0, a1, a2, a3, pb0, pb1);
+                ldmatrix_x4_trans(sw128_addr<HD::kParts>(vtile, vrow, 2 * dt + ((lane >> 3) & 1), rl), a0, a1,
+                                  a2, a3);
+                mma_16816<MMA_F16>(acc[i], a0, a1, a2, a3, pb0, pb1);
+            }
+        } else {
+            // matrices (tokens 0-7 | 8-15) x (chunk c | c + 1): two 16-dim tiles per ldmatrix
+            const int vrow = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+            for (int ii = 0; ii < DT / 2; ++ii) {
+                const int c = dhalf * DT + 2 * ii;   // chunk = 16-dim tile index
+                uint32_t r0, r1, r2, r3;
+                ldmatrix_x4_trans(sw128_addr<HD::kParts>(vtile, vrow, c + (lane >> 4), rl), r0, r1, r2, r3);
+                // bytes (t, 2grp), (t, 2grp+1), (t+1, 2grp), (t+1, 2grp+1) -> dim pairs over tokens
+                const uint32_t s0 = prmt(r0, 0u, 0x3120u), s1 = prmt(r1, 0u, 0x3120u);
+                const uint32_t s2 = prmt(r2, 0u, 0x3120u), s3 = prmt(r3, 0u, 0x3120u);
+                mma_16816<true>(acc[2 * ii], fp8x2_to_f16x2<KV>(lo16(s0)), fp8x2_to_f16x2<KV>(hi16(s0)),
+                                fp8x2_to_f16x2<KV>(lo16(s1)), fp8x2_to_f16x2<KV>(hi16(s1)), pb0, pb1);
+                mma_16816<true>(acc[2 * ii + 1], fp8x2_to_f16x2<KV>(lo16(s2)), fp8x2_to_f16x2<KV>(hi16(s2)),
+                                fp8x2_to_f16x2<KV>(lo16(s3)), fp8x2_to_f16x2<KV>(hi16(s3)), pb0, pb1);
             }
         }
         if (ragged)   // order the zeroing stores before the next TMA write to this stage
@@ -859,9 +992,12 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                     }
 #pragma unroll
                     for (int i = 0; i < DT; ++i) {
-                        const int d = (dhalf * DT + i) * 16 + grp;
-                        red_acc[(pair * G + head) * D + d] = acc[i][j];
-                        red_acc[(pair * G + head) * D + d + 8] = acc[i][j + 2];
+                        // output rows grp and grp + 8 of the tile: dims grp and grp + 8, or for
+                        // FP8 caches 2 grp and 2 grp + 1 (see above)
+                        const int d0 = (dhalf * DT + i) * 16;
+                        const int dlo = d0 + (FP8 ? 2 * grp : grp), dhi = d0 + (FP8 ? 2 * grp + 1 : grp + 8);
+                        red_acc[(pair * G + head) * D + dlo] = acc[i][j];
+                        red_acc[(pair * G + head) * D + dhi] = acc[i][j + 2];
                     }
                 }
             }
@@ -886,7 +1022,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 
 // ------------------------------------------------------------------ kernels
 
-template <int G, bool PAGED, bool MMA, bool F16, int D>
+template <int G, bool PAGED, bool MMA, int KV, int D>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv)
@@ -928,14 +1064,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         return;
     volatile int *abort_flag = misc;
     if (warp == kConsumerWarps)
-        split_producer<PAGED, MMA, D>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
-                                      t_begin, t_end, lane);
+        split_producer<PAGED, MMA, D, KV>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
+                                          t_begin, t_end, lane);
     else if constexpr (MMA)
-        split_consumer_mma<G, F16, D>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin,
-                                      t_end, warp, lane);
+        split_consumer_mma<G, KV, D>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin,
+                                     t_end, warp, lane);
     else
-        split_consumer<G, F16, D>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin, t_end,
-                                  warp, lane);
+        split_consumer<G, KV, D>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin, t_end,
+                                 warp, lane);
 }
 
 // One CTA per (segment, query head of its group); thread d owns output dim d.

@@ -23,7 +23,7 @@ struct SplitLaunch {
 cudaError_t launch_merge(int group, int head_dim, const MergeParams &p, int grid, cudaStream_t stream);
 
 // Shared by the split translation units.
-template <int G, bool PAGED, bool MMA, bool F16, int D>
+template <int G, bool PAGED, bool MMA, int KV, int D>
 cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const SplitLaunch &c)
 {
@@ -36,7 +36,7 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
         return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(split_kernel<G, PAGED, MMA, F16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(split_kernel<G, PAGED, MMA, KV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)c.smem_optin);
         if (e != cudaSuccess)
             return e;
@@ -54,56 +54,60 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
     cfg.stream = c.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, MMA, F16, D>, p, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, MMA, KV, D>, p, tmk, tmv);
 }
 
-// One split-kernel variant per (layout, element type, head_dim): consumers
-// on tensor cores (mma: group 2, 4 or 8, swizzled K/V maps) or CUDA cores
-// (any group).  Returns cudaErrorInvalidValue for an unsupported group.
-template <bool PAGED, bool F16, int D>
+// One split-kernel variant per (layout, K/V element type, head_dim):
+// consumers on tensor cores (mma: group 2, 4 or 8, swizzled K/V maps, rows of
+// at least 128 bytes) or CUDA cores (any group).  Returns
+// cudaErrorInvalidValue for an unsupported group or consumer choice.
+template <bool PAGED, int KV, int D>
 cudaError_t launch_split_variant(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
                                  const CUtensorMap &tmv, const SplitLaunch &c)
 {
     if (mma) {
-        switch (group) {
-        case 2: return launch_split_t<2, PAGED, true, F16, D>(p, tmk, tmv, c);
-        case 4: return launch_split_t<4, PAGED, true, F16, D>(p, tmk, tmv, c);
-        case 8: return launch_split_t<8, PAGED, true, F16, D>(p, tmk, tmv, c);
-        default: return cudaErrorInvalidValue;
+        if constexpr (Shape<D, KV>::kParts >= 1) {
+            switch (group) {
+            case 2: return launch_split_t<2, PAGED, true, KV, D>(p, tmk, tmv, c);
+            case 4: return launch_split_t<4, PAGED, true, KV, D>(p, tmk, tmv, c);
+            case 8: return launch_split_t<8, PAGED, true, KV, D>(p, tmk, tmv, c);
+            default: return cudaErrorInvalidValue;
+            }
         }
+        return cudaErrorInvalidValue;
     }
     switch (group) {
-    case 1: return launch_split_t<1, PAGED, false, F16, D>(p, tmk, tmv, c);
-    case 2: return launch_split_t<2, PAGED, false, F16, D>(p, tmk, tmv, c);
-    case 4: return launch_split_t<4, PAGED, false, F16, D>(p, tmk, tmv, c);
-    case 8: return launch_split_t<8, PAGED, false, F16, D>(p, tmk, tmv, c);
+    case 1: return launch_split_t<1, PAGED, false, KV, D>(p, tmk, tmv, c);
+    case 2: return launch_split_t<2, PAGED, false, KV, D>(p, tmk, tmv, c);
+    case 4: return launch_split_t<4, PAGED, false, KV, D>(p, tmk, tmv, c);
+    case 8: return launch_split_t<8, PAGED, false, KV, D>(p, tmk, tmv, c);
     default: return cudaErrorInvalidValue;
     }
 }
 
 // Each variant is compiled in its own translation unit (fd_split_inst.cu,
-// built once per combination), so the twelve compile in parallel.
-#define FD_SPLIT_VARIANTS(X) \
-    X(false, false, 64) X(false, false, 128) X(false, false, 256) \
-    X(false, true, 64) X(false, true, 128) X(false, true, 256) \
-    X(true, false, 64) X(true, false, 128) X(true, false, 256) \
-    X(true, true, 64) X(true, true, 128) X(true, true, 256)
-#define FD_EXTERN_SPLIT(P, F, D)                                                                \
-    extern template cudaError_t launch_split_variant<P, F, D>(bool, int, const SplitParams &, \
+// built once per combination), so they compile in parallel.
+#define FD_SPLIT_VARIANTS_KV(X, P, KV) X(P, KV, 64) X(P, KV, 128) X(P, KV, 256)
+#define FD_SPLIT_VARIANTS_P(X, P)                                                          \
+    FD_SPLIT_VARIANTS_KV(X, P, kKvBf16) FD_SPLIT_VARIANTS_KV(X, P, kKvF16)                   \
+    FD_SPLIT_VARIANTS_KV(X, P, kKvE4m3) FD_SPLIT_VARIANTS_KV(X, P, kKvE5m2)
+#define FD_SPLIT_VARIANTS(X) FD_SPLIT_VARIANTS_P(X, false) FD_SPLIT_VARIANTS_P(X, true)
+#define FD_EXTERN_SPLIT(P, KV, D)                                                                \
+    extern template cudaError_t launch_split_variant<P, KV, D>(bool, int, const SplitParams &, \
                                                               const CUtensorMap &,             \
                                                               const CUtensorMap &, const SplitLaunch &);
 FD_SPLIT_VARIANTS(FD_EXTERN_SPLIT)
 #undef FD_EXTERN_SPLIT
 
-// Split launch for a call: layout, element type and head_dim pick the
-// variant.  Returns cudaErrorInvalidValue for an unsupported head_dim.
-inline cudaError_t launch_split(bool paged, bool f16, int head_dim, bool mma, int group,
+// Split launch for a call: layout, K/V element type (kKv*) and head_dim pick
+// the variant.  Returns cudaErrorInvalidValue for an unsupported head_dim.
+inline cudaError_t launch_split(bool paged, int kv, int head_dim, bool mma, int group,
                                 const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 const SplitLaunch &c)
 {
-#define FD_PICK_SPLIT(P, F, D)                                                  \
-    if (paged == P && f16 == F && head_dim == D)                              \
-        return launch_split_variant<P, F, D>(mma, group, p, tmk, tmv, c);
+#define FD_PICK_SPLIT(P, KV, D)                                                 \
+    if (paged == P && kv == KV && head_dim == D)                              \
+        return launch_split_variant<P, KV, D>(mma, group, p, tmk, tmv, c);
     FD_SPLIT_VARIANTS(FD_PICK_SPLIT)
 #undef FD_PICK_SPLIT
     return cudaErrorInvalidValue;

@@ -34,7 +34,7 @@ using namespace fd;
 
 constexpr size_t kNoallocScratchBytes = FD_NOALLOC_SCRATCH_BYTES;
 constexpr int kD = 128;   // the one head_dim this entry point serves
-using HD = HeadDim<kD>;
+using HD = Shape<kD, kKvBf16>;
 
 // The scratch: device-error word, tile prefix, partial LSEs and partial outputs.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
@@ -168,6 +168,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     sp.cap = s_max;
     sp.s_max = s_max;
     sp.scale_log2 = scale * 1.4426950408889634f;
+    sp.v_scale = 1.f;
     sp.timeout_ns = 2000000000ull;
 
     // Shared-memory plan (same rule as the workspace entry points).
@@ -216,7 +217,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     // The status word is the only part of the scratch that must start at zero.
     if (cudaMemsetAsync(sp.ws_err, 0, sizeof(unsigned int), launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    if (launch_split_variant<false, false, kD>(false, group, sp, tmk, tmv, launch) != cudaSuccess)
+    if (launch_split_variant<false, kKvBf16, kD>(false, group, sp, tmk, tmv, launch) != cudaSuccess)
         return FD_ERR_CUDA;
     if (launch_merge(group, kD, mp, batch * num_kv_heads, launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;

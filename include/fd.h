@@ -40,8 +40,10 @@
  *   - Supported shapes: head_dim 64, 128 or 256; Hq/Hkv in {1, 2, 4, 8};
  *     batch <= 4096.  Other shapes return FD_ERR_UNSUPPORTED.
  *   - Precision: q, K and V are bf16 (default) or IEEE fp16
- *     (fd_options.dtype); scores, softmax and accumulation are fp32; outputs
- *     are fp32.
+ *     (fd_options.dtype); K and V may instead be an FP8 cache
+ *     (fd_options.kv_dtype: OCP E4M3 or E5M2 codes, one byte per element, with
+ *     per-tensor dequantisation scales k_scale and v_scale).  Scores, softmax
+ *     and accumulation are fp32; outputs are fp32.
  */
 #ifndef FD_H
 #define FD_H
@@ -72,6 +74,15 @@ typedef enum fd_dtype {
     FD_DTYPE_F16 = 1     /* IEEE binary16 */
 } fd_dtype;
 
+/* Element type of the K/V cache.  An FP8 cache holds one code per element,
+ * [.., head_dim] bytes per (token, kv head) row, and represents
+ * K = k_scale * decode(code) and V = v_scale * decode(code). */
+typedef enum fd_kv_dtype {
+    FD_KV_AS_Q = 0,       /* the type of q (fd_options.dtype) */
+    FD_KV_FP8_E4M3 = 1,   /* OCP FP8 E4M3 ("fn": no infinities, max 448) */
+    FD_KV_FP8_E5M2 = 2    /* OCP FP8 E5M2 */
+} fd_kv_dtype;
+
 /* Optional knobs; pass NULL for the defaults. */
 typedef struct fd_options {
     /* Number of persistent split CTAs that share the KV tiles (1..1024).
@@ -90,6 +101,13 @@ typedef struct fd_options {
     void *split_end_event;
     /* Element type of q, K and V (fd_dtype); 0 = bf16. */
     int dtype;
+    /* Element type of K and V (fd_kv_dtype); 0 = that of q. */
+    int kv_dtype;
+    /* Dequantisation scales of an FP8 cache; 0 means 1.  k_scale multiplies
+     * every K element (it enters the scores), v_scale every V element (it
+     * multiplies O).  Ignored for 16-bit caches. */
+    float k_scale;
+    float v_scale;
 } fd_options;
 
 /* Test hook: CTA 0 announces more bytes for its first tile than it loads, so
@@ -111,7 +129,8 @@ typedef struct fd_options {
 
 /* Do not fuse kv heads.  By default, when the tensor-core consumers apply
  * (contiguous KV, or pages of at least 8 tokens, and no FD_FLAG_CUDA_CORES),
- * a kv head's rows are short (head_dim 64, or pages under 64 tokens) and the
+ * a kv head's rows are short (under 256 bytes: head_dim 64, or an FP8 cache
+ * with head_dim up to 128, or pages under 64 tokens) and the
  * call has at least 24 KV tiles of 64 tokens per split CTA (counted from
  * seq_lens_host when given, else from the capacity), F adjacent kv heads
  * (F = 4 or 2, the largest with F * head_dim <= 256, F * (Hq/Hkv) <= 8 and F
@@ -150,8 +169,9 @@ fd_status fd_workspace_init(void *workspace, size_t workspace_bytes, fd_stream_t
 
 /*
  * Decode attention over a contiguous KV cache.
- *   q            [batch, num_q_heads, head_dim] bf16, device.
- *   k, v         [batch, s_max, num_kv_heads, head_dim] bf16, device, row-major.
+ *   q            [batch, num_q_heads, head_dim] bf16 or fp16, device.
+ *   k, v         [batch, s_max, num_kv_heads, head_dim] device, row-major, of
+ *                q's type or FP8 codes (fd_options.kv_dtype).
  *                Positions t >= seq_lens[b] of request b are never used
  *                (they may hold anything, including NaN).
  *   seq_lens_dev [batch] int32, device: L_b in [0, s_max].  NULL means every
@@ -178,7 +198,8 @@ fd_status fd_decode(const void *q, const void *k, const void *v,
 
 /*
  * Decode attention over a paged KV cache.
- *   k_pages, v_pages [num_pages, page_size, num_kv_heads, head_dim] bf16, device.
+ *   k_pages, v_pages [num_pages, page_size, num_kv_heads, head_dim] device, of
+ *                q's type or FP8 codes (fd_options.kv_dtype).
  *   block_table  [batch, max_blocks_per_seq] int32, device, row-major: token t
  *                of request b is in page block_table[b][t / page_size], slot
  *                t % page_size.  Only the first ceil(L_b / page_size) entries of

@@ -1,5 +1,7 @@
 """Helpers for the GPU tests: move a workload to the device, run the library
 through its C ABI binding, and compare with the oracle."""
+import dataclasses
+
 import numpy as np
 import torch
 
@@ -14,9 +16,18 @@ def dev_bf16(bits, device="cuda", dtype="bf16"):
     return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
 
 
+def dev_fp8(codes, device="cuda"):
+    """FP8 codes as a uint8 CUDA tensor (the binding takes kv_dtype with it)."""
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).to(device)
+
+
 def to_device(w, device="cuda"):
     dt = getattr(w, "dtype", "bf16")
-    d = dict(q=dev_bf16(w.q, device, dt), k=dev_bf16(w.k, device, dt), v=dev_bf16(w.v, device, dt),
+    if getattr(w, "kv_dtype", None) in ("e4m3", "e5m2"):
+        k, v = dev_fp8(w.k, device), dev_fp8(w.v, device)
+    else:
+        k, v = dev_bf16(w.k, device, dt), dev_bf16(w.v, device, dt)
+    d = dict(q=dev_bf16(w.q, device, dt), k=k, v=v,
              seq_lens=torch.from_numpy(np.ascontiguousarray(w.seq_lens, dtype=np.int32)).to(device))
     if w.paged:
         d["block_table"] = torch.from_numpy(np.ascontiguousarray(w.block_table, dtype=np.int32)).to(device)
@@ -27,6 +38,8 @@ def run(w, dev=None, **kw):
     """Run fd_decode / fd_decode_paged on workload w; returns fp64 numpy (O, LSE)."""
     import decode_attention_decoding_gb300 as fd
     dev = dev or to_device(w)
+    if getattr(w, "kv_dtype", None) in ("e4m3", "e5m2"):
+        kw = dict(kw, kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale)
     if w.paged:
         o, l = fd.fd_decode_paged(dev["q"], dev["k"], dev["v"], dev["block_table"], dev["seq_lens"],
                                   seq_lens_host=torch.from_numpy(w.seq_lens), scale=w.scale, **kw)
@@ -64,9 +77,11 @@ def contig_to_paged(w, page, perm_seed, extra_pages=3, poison=False):
     perm = syn.permutation(perm_seed, n_pages)
     max_blocks = max(1, (S + page - 1) // page)
     table = syn.build_block_table(lens, page, max_blocks, perm)
-    fill = syn.BF16_NAN if poison else np.uint16(0)
-    kp = np.full((n_pages, page, hkv, d), fill, np.uint16)
-    vp = np.full((n_pages, page, hkv, d), fill, np.uint16)
+    fp8 = getattr(w, "kv_dtype", None) in ("e4m3", "e5m2")
+    nan = np.uint8(0x7F) if fp8 else syn.BF16_NAN          # a NaN code in both FP8 formats
+    fill = nan if poison else w.k.dtype.type(0)
+    kp = np.full((n_pages, page, hkv, d), fill, w.k.dtype)
+    vp = np.full((n_pages, page, hkv, d), fill, w.v.dtype)
     for b in range(B):
         L = int(lens[b])
         nb = (L + page - 1) // page
@@ -74,8 +89,8 @@ def contig_to_paged(w, page, perm_seed, extra_pages=3, poison=False):
             n = min(page, L - i * page)
             kp[table[b, i], :n] = w.k[b, i * page:i * page + n]
             vp[table[b, i], :n] = w.v[b, i * page:i * page + n]
-    return syn.Workload(w.name + f"_p{page}", w.q, kp, vp, lens.copy(), w.num_q_heads, w.num_kv_heads,
-                        d, w.scale, page_size=page, block_table=table, dtype=getattr(w, "dtype", "bf16"))
+    return dataclasses.replace(w, name=w.name + f"_p{page}", k=kp, v=vp, seq_lens=lens.copy(),
+                               page_size=page, block_table=table)
 
 
 def sample_items(w, n, seed=0):

@@ -105,6 +105,14 @@ def test_decode_argument_checks(lib, fd):
     assert call_decode(lib, slh=lens) == E.FD_ERR_INVALID_ARG
     opts = fd.FdOptions(2000, 0, 0, None, None)
     assert call_decode(lib, opts=ctypes.byref(opts)) == E.FD_ERR_INVALID_ARG
+    # FP8 cache options: type code and scales are checked on the host
+    for kv, ks, vs in ((3, 0.0, 0.0), (-1, 0.0, 0.0), (1, -1.0, 1.0), (2, 1.0, float("nan")),
+                       (1, float("inf"), 1.0)):
+        opts = fd.FdOptions(0, 0, 0, None, None, 0, kv, ks, vs)
+        assert call_decode(lib, opts=ctypes.byref(opts)) == E.FD_ERR_INVALID_ARG, (kv, ks, vs)
+    for kv in (1, 2):   # valid FP8 options reach the workspace check
+        opts = fd.FdOptions(0, 0, 0, None, None, 0, kv, 0.5, 2.0)
+        assert call_decode(lib, opts=ctypes.byref(opts), wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
     assert call_decode(lib, B=0) == E.FD_OK                           # nothing to do, no CUDA call
 
 
