@@ -477,6 +477,18 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
         return FD_ERR_INVALID_ARG;
     if (!((page_size < kTileTokens && kTileTokens % page_size == 0) || page_size % kTileTokens == 0))
         return FD_ERR_UNSUPPORTED;
+    if (!options_valid(opts))
+        return FD_ERR_INVALID_ARG;
+    // A page's TMA box lands at a multiple of its own size in shared memory,
+    // and tensor copies need 128-byte aligned destinations: pages under 64
+    // tokens must hold at least 128 bytes per kv head (only an FP8 cache with
+    // head_dim 64 and one-token pages falls short).
+    {
+        const int kvd = opts ? opts->kv_dtype : FD_KV_AS_Q;
+        const int eb = (kvd == FD_KV_FP8_E4M3 || kvd == FD_KV_FP8_E5M2) ? 1 : 2;
+        if (page_size < kTileTokens && page_size * head_dim * eb < 128)
+            return FD_ERR_UNSUPPORTED;
+    }
     const long long cap = (long long)max_blocks_per_seq * page_size;
     if (cap >= (1ll << 31) || (long long)num_pages * page_size >= (1ll << 31) ||
         (long long)num_kv_heads * batch * ((cap + kTileTokens - 1) / kTileTokens) >= (1ll << 31))

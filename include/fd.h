@@ -206,7 +206,10 @@ fd_status fd_decode(const void *q, const void *k, const void *v,
  *                a row are read; the rest may hold anything (e.g. -1).  An entry
  *                outside [0, num_pages) is replaced by page 0 and reported as
  *                FD_ERR_DEVICE_INPUT.
- *   page_size    a divisor of 64 (1, 2, 4, ..., 32) or a multiple of 64.
+ *   page_size    a divisor of 64 (1, 2, 4, ..., 32) or a multiple of 64; a
+ *                page under 64 tokens must hold at least 128 bytes per kv head
+ *                (an FP8 cache with head_dim 64 needs pages of 2 or more).
+ *                Other sizes return FD_ERR_UNSUPPORTED.
  *   seq_lens_dev [batch] int32, device, L_b in [0, max_blocks_per_seq * page_size];
  *                must not be NULL.
  *   Other arguments as for fd_decode.

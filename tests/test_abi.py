@@ -119,14 +119,14 @@ def test_decode_argument_checks(lib, fd):
 def call_paged(lib, **over):
     a = dict(q=ALIGNED, k=ALIGNED, v=ALIGNED, table=ALIGNED, mb=4, sl=ALIGNED, slh=None, B=2, hq=8,
              hkv=2, d=128, page=16, npages=8, scale=0.1, o=ALIGNED, lse=ALIGNED, ws=ALIGNED,
-             wsb=1 << 30)
+             wsb=1 << 30, opts=None)
     a.update(over)
     f = lib.fd_decode_paged
     f.restype = ctypes.c_int
     return f(ctypes.c_void_p(a["q"]), ctypes.c_void_p(a["k"]), ctypes.c_void_p(a["v"]),
              ctypes.c_void_p(a["table"]), a["mb"], ctypes.c_void_p(a["sl"]), a["slh"], a["B"], a["hq"],
              a["hkv"], a["d"], a["page"], a["npages"], ctypes.c_float(a["scale"]), ctypes.c_void_p(a["o"]),
-             ctypes.c_void_p(a["lse"]), ctypes.c_void_p(a["ws"]), ctypes.c_size_t(a["wsb"]), None, None)
+             ctypes.c_void_p(a["lse"]), ctypes.c_void_p(a["ws"]), ctypes.c_size_t(a["wsb"]), a["opts"], None)
 
 
 def test_paged_argument_checks(lib, fd):
@@ -137,6 +137,11 @@ def test_paged_argument_checks(lib, fd):
     assert call_paged(lib, npages=0) == E.FD_ERR_INVALID_ARG
     assert call_paged(lib, page=0) == E.FD_ERR_INVALID_ARG
     assert call_paged(lib, page=24) == E.FD_ERR_UNSUPPORTED
+    # one-token FP8 pages of head_dim 64 are 64-byte TMA boxes: below the 128-byte alignment
+    fp8 = fd.FdOptions(0, 0, 0, None, None, 0, 1, 1.0, 1.0)
+    assert call_paged(lib, page=1, d=64, opts=ctypes.byref(fp8)) == E.FD_ERR_UNSUPPORTED
+    assert call_paged(lib, page=2, d=64, opts=ctypes.byref(fp8), wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
+    assert call_paged(lib, page=1, d=64, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL   # bf16: 128 bytes
     assert call_paged(lib, page=96) == E.FD_ERR_UNSUPPORTED
     lens = (ctypes.c_int32 * 2)(64, 65)                     # capacity 4 pages * 16
     assert call_paged(lib, slh=lens) == E.FD_ERR_INVALID_ARG

@@ -48,7 +48,7 @@ def test_contiguous_vs_oracle(fmt, d, group, flags):
         check(o, l, ro, rl, f"{fmt} d={d} G={group} flags={flags} ctas={ctas}")
 
 
-@pytest.mark.parametrize("page", [1, 8, 16, 64])
+@pytest.mark.parametrize("page", [2, 8, 16, 64])
 @pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("fmt", FMTS)
@@ -133,3 +133,18 @@ def test_bit_exact_gather(fmt, d, flags):
             g = h // group
             assert np.array_equal(o[0, h], v_scale * decode(v[0, t_star, g], fmt)), (t_star, h)
             assert sum(int(o[0, h, j] / v_scale) << (3 * j) for j in range(4)) == t_star
+
+
+def test_one_token_fp8_pages_of_head_dim_64_are_rejected_before_launch():
+    """64-byte page boxes would miss the 128-byte TMA alignment: the host refuses them."""
+    import decode_attention_decoding_gb300 as fd
+    w = syn.make_contiguous(2000, 2, 4, 2, 64, 64, [10, 64], kv_dtype="e4m3")
+    wp = contig_to_paged(w, 1, perm_seed=1)
+    with pytest.raises(fd.FdError) as e:
+        run(wp)
+    assert e.value.status == fd.FD_ERR_UNSUPPORTED
+    w128 = syn.make_contiguous(2001, 2, 4, 2, 128, 64, [10, 64], kv_dtype="e4m3")
+    wp = contig_to_paged(w128, 1, perm_seed=1)
+    ro, rl = oracle.attend(wp)
+    o, l = run(wp)
+    check(o, l, ro, rl, "e4m3 d=128 P=1")
