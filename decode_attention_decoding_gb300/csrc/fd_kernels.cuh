@@ -855,15 +855,18 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         const uint32_t vtile = ktile + HD::kTileBytes;
 
         // S^T = K . Q^T for tokens tok0 .. tok0 + 15 (fragment rows grp and grp + 8).
+        // Even and odd k-steps accumulate separately: two dependent MMA chains
+        // of KS/2 instead of one of KS (the chain's latency bounds the tile).
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
         {
+            float sc2[4] = {0.f, 0.f, 0.f, 0.f};
             const int row = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);
             if constexpr (!FP8) {
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     uint32_t a0, a1, a2, a3;
                     ldmatrix_x4(sw128_addr<HD::kParts>(ktile, row, 2 * ks + (lane >> 4), rl), a0, a1, a2, a3);
-                    mma_16816<MMA_F16>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                    mma_16816<MMA_F16>((ks & 1) ? sc2 : sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
                 }
             } else {
                 // one ldmatrix covers two 16-dim chunks: k-steps 2 kk and 2 kk + 1
@@ -874,11 +877,14 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                     mma_16816<true>(sc, fp8x2_to_f16x2<KV>(lo16(r0)), fp8x2_to_f16x2<KV>(lo16(r1)),
                                     fp8x2_to_f16x2<KV>(hi16(r0)), fp8x2_to_f16x2<KV>(hi16(r1)), qb[2 * kk][0],
                                     qb[2 * kk][1]);
-                    mma_16816<true>(sc, fp8x2_to_f16x2<KV>(lo16(r2)), fp8x2_to_f16x2<KV>(lo16(r3)),
+                    mma_16816<true>(sc2, fp8x2_to_f16x2<KV>(lo16(r2)), fp8x2_to_f16x2<KV>(lo16(r3)),
                                     fp8x2_to_f16x2<KV>(hi16(r2)), fp8x2_to_f16x2<KV>(hi16(r3)),
                                     qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
                 }
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                sc[i] += sc2[i];
         }
         const bool v0 = tok0 + grp < nvalid, v1 = tok0 + grp + 8 < nvalid;
         // sc[0]: (token grp, head 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1)
