@@ -87,6 +87,24 @@ def byte_counts(w, P):
                 split=kv + q + ws + out)   # split reads K,V,q; writes partials or final O/LSE
 
 
+def consumers_label(args, w) -> str:
+    """Which consumers the library's default choice runs for this workload."""
+    G = w.num_q_heads // w.num_kv_heads
+    fp8 = w.kv_dtype is not None
+    row = w.head_dim * (1 if fp8 else 2)
+    if args.cuda_cores or (w.paged and w.page_size < 8):
+        return "cuda cores"
+    short = row < 256 or (w.paged and w.page_size < 64)
+    tiles = sum((int(L) + 63) // 64 for L in w.seq_lens) * w.num_kv_heads
+    long_call = tiles / 152 >= 24
+    fused = short and long_call and any(f * w.head_dim <= 256 and f * G <= 8 and w.num_kv_heads % f == 0
+                                        for f in (2, 4))
+    if G == 1 and not fused:
+        return "cuda cores"
+    mma = "mma.sync fp16 on FP8 codes" if fp8 else "mma.sync bf16"
+    return f"tensor cores ({mma})" + (", fused kv heads" if fused else "")
+
+
 def max_over_ranks(x: float, dist, device) -> float:
     """The largest value of x over all ranks (x itself without a process group)."""
     if dist is None:
@@ -195,14 +213,21 @@ def run_ours(args, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    w = syn.make_config(args.config)
+    w = syn.make_config(args.config, kv_dtype=args.kv if args.kv != "bf16" else None)
     B, hq, d = w.q.shape
     hkv = w.num_kv_heads
+    fp8 = w.kv_dtype is not None
+    kv_opts = dict(kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale) if fp8 else {}
 
     def todev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
 
-    q, k, v = todev(w.q), todev(w.k), todev(w.v)
+    def todev_kv(codes):
+        if fp8:
+            return torch.from_numpy(np.ascontiguousarray(codes)).to(dev)
+        return todev(codes)
+
+    q, k, v = todev(w.q), todev_kv(w.k), todev_kv(w.v)
     lens = torch.from_numpy(w.seq_lens.astype(np.int32)).to(dev)
     lens_h = torch.from_numpy(w.seq_lens.astype(np.int32))
     table = torch.from_numpy(w.block_table.astype(np.int32)).to(dev) if w.paged else None
@@ -228,11 +253,11 @@ def run_ours(args, rank, world):
     def step(i, events=None):
         kk, vv = kvs[i % copies]
         if w.paged:
-            fd.fd_decode_paged(q, kk, vv, table, lens, scale=w.scale, out=out, lse=lse, workspace=ws,
-                               split_events=events, flags=flags)
+            fd.fd_decode_paged(q, kk, vv, table, lens, lens_h, scale=w.scale, out=out, lse=lse, workspace=ws,
+                               split_events=events, flags=flags, **kv_opts)
         else:
-            fd.fd_decode(q, kk, vv, lens, scale=w.scale, out=out, lse=lse, workspace=ws,
-                         split_events=events, flags=flags)
+            fd.fd_decode(q, kk, vv, lens, lens_h, scale=w.scale, out=out, lse=lse, workspace=ws,
+                         split_events=events, flags=flags, **kv_opts)
 
     for i in range(args.warmup):
         step(i)
@@ -324,12 +349,13 @@ def run_ours(args, rank, world):
     # result -> host, every step.
     e2e = None
     if not args.no_e2e:
-        hq_, hk_, hv_ = (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
-                         for x in (w.q, w.k, w.v))
+        hq_ = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory()
+        hk_, hv_ = (torch.from_numpy(np.ascontiguousarray(x).view(np.uint8 if fp8 else np.int16)).pin_memory()
+                    for x in (w.k, w.v))
         hl_ = lens_h.pin_memory()
         ho = torch.empty((B, hq, d), dtype=torch.float32).pin_memory()
         hlse = torch.empty((B, hq), dtype=torch.float32).pin_memory()
-        dq, dk, dv = (torch.empty(x.shape, dtype=torch.int16, device=dev) for x in (hq_, hk_, hv_))
+        dq, dk, dv = (torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (hq_, hk_, hv_))
         dl = torch.empty_like(lens)
         K2 = max(3, min(K, args.e2e_steps))
 
@@ -355,11 +381,13 @@ def run_ours(args, rank, world):
             dl.copy_(hl_, non_blocking=True)
             for cs in cstreams:
                 cur.wait_stream(cs)
-            qb, kb, vb = dq.view(torch.bfloat16), dk.view(torch.bfloat16), dv.view(torch.bfloat16)
+            qb = dq.view(torch.bfloat16)
+            kb, vb = (dk, dv) if fp8 else (dk.view(torch.bfloat16), dv.view(torch.bfloat16))
             if w.paged:
-                fd.fd_decode_paged(qb, kb, vb, table, dl, scale=w.scale, out=out, lse=lse, workspace=ws)
+                fd.fd_decode_paged(qb, kb, vb, table, dl, lens_h, scale=w.scale, out=out, lse=lse, workspace=ws,
+                                   **kv_opts)
             else:
-                fd.fd_decode(qb, kb, vb, dl, scale=w.scale, out=out, lse=lse, workspace=ws)
+                fd.fd_decode(qb, kb, vb, dl, lens_h, scale=w.scale, out=out, lse=lse, workspace=ws, **kv_opts)
             ho.copy_(out, non_blocking=True)
             hlse.copy_(lse, non_blocking=True)
 
@@ -393,7 +421,9 @@ def run_ours(args, rank, world):
             "warmup": args.warmup, "ms_per_step": ms_step, "us_per_call": ms_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "frac_of_peak_hbm": value_tbs * 1e3 / world / peaks["hbm_gbs"],
-            "dtype": "f32", "input_dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
+            "dtype": "f32", "input_dtype": (f"bf16 q, FP8 {w.kv_dtype} K/V (scale {w.k_scale})" if fp8
+                                            else "bf16"),
+            "data": "synthetic (seeded N(0,1) bf16" + (", quantised once to FP8)" if fp8 else ")"),
             "impl": "ours",
             "config": {"workload": syn.CONFIG_NAMES[args.config], "batch": B, "num_q_heads": hq,
                        "num_kv_heads": hkv, "head_dim": d,
@@ -409,8 +439,7 @@ def run_ours(args, rank, world):
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": "fd::split_kernel", "split_us": split_avg_ms * 1e3,
-                         "consumers": ("cuda cores" if (args.cuda_cores or w.num_q_heads == w.num_kv_heads)
-                                       else "tensor cores (mma.sync bf16)"),
+                         "consumers": consumers_label(args, w),
                          "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"},
             "gpu_launches": 2 * K,        # split kernel + merge kernel per call
             "clocks": clk.summary(t_wall0, t_wall1),
@@ -434,7 +463,7 @@ def oracle_sample(w, n_rows):
     items = np.array([[b, h, 0, -1] for b, h in rows], dtype=np.int32)
     toks = sum(int(w.seq_lens[b]) for b, _ in rows)
     # bytes the oracle streams for these rows: K+V row per token (per query head)
-    return items, toks * w.head_dim * 2 * 2
+    return items, toks * w.head_dim * 2 * w.kv_elem_bytes
 
 
 def time_oracle(w, items, threads):
@@ -471,7 +500,7 @@ def run_reference(args, rank, world):
         return
     import oracle
     oracle.build()
-    w = syn.make_config(args.config)
+    w = syn.make_config(args.config, kv_dtype=args.kv if args.kv != "bf16" else None)
     threads = os.cpu_count() or 1
     total_rows = w.batch * w.num_q_heads
     budget = max(1.0, args.reference_budget_s / max(1, args.steps + args.warmup))
@@ -489,7 +518,8 @@ def run_reference(args, rank, world):
               f"{threads} threads")
     line = {"metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "input_dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "input_dtype": f"bf16 q, FP8 {w.kv_dtype} K/V" if w.kv_dtype else "bf16",
             "data": "synthetic (seeded N(0,1) bf16)", "impl": "reference",
             "config": {"workload": syn.CONFIG_NAMES[args.config], "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": "TB/s", "cores": threads, "kind": "oracle",
@@ -504,6 +534,8 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3", "e5m2"],
+                    help="K/V cache element type (FP8 caches are quantised from the same values)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--copy-streams", type=int, default=4,
