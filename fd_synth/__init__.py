@@ -285,6 +285,11 @@ class Workload:
         return self.q.shape[0]
 
     @property
+    def q_len(self) -> int:
+        """New query tokens per request: q is [B, Hq, D] (1) or [B, q_len, Hq, D]."""
+        return self.q.shape[1] if self.q.ndim == 4 else 1
+
+    @property
     def paged(self) -> bool:
         return self.page_size > 0
 
@@ -330,11 +335,13 @@ def fp32(x: float) -> float:
 
 def make_contiguous(config_id: int, batch: int, hq: int, hkv: int, d: int, s_max: int,
                     lens, name: str = "", dtype: str = "bf16", kv_dtype: str | None = None,
-                    k_scale: float = 1.0, v_scale: float = 1.0) -> Workload:
+                    k_scale: float = 1.0, v_scale: float = 1.0, q_len: int = 1) -> Workload:
     """Contiguous workload; with kv_dtype 'e4m3'/'e5m2' K and V are FP8 codes
-    whose dequantised values (code * scale) approximate N(0,1)."""
+    whose dequantised values (code * scale) approximate N(0,1); with q_len > 1
+    q is [B, q_len, Hq, D] (the last q_len cached tokens are the new ones)."""
     k_scale, v_scale = fp32(k_scale), fp32(v_scale)
-    q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d), dtype=dtype)
+    qshape = (batch, hq, d) if q_len == 1 else (batch, q_len, hq, d)
+    q = normal_bf16(seed_for(config_id, TENSOR_Q), qshape, dtype=dtype)
     k, v = _kv(config_id, (batch, s_max, hkv, d), dtype, kv_dtype, k_scale, v_scale)
     lens = np.asarray(lens, dtype=np.int32).reshape(batch)
     return Workload(name or f"contig{config_id}", q, k, v, lens, hq, hkv, d, default_scale(d),

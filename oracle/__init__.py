@@ -55,7 +55,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB)
             lib.oracle_attend.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _D, _I,
-                                          _I, _D, _D, _P, _I, _P, _P, _P]
+                                          _I, _D, _D, _I, _P, _I, _P, _P, _P]
             lib.oracle_attend.restype = _I
             lib.oracle_lse_merge.argtypes = [_P, _P, _I, _I, _P, _P]
             lib.oracle_lse_merge.restype = None
@@ -77,12 +77,16 @@ def attend_raw(q, k, v, seq_lens, num_q_heads, num_kv_heads, scale, *,
                kv_dtype=None, k_scale=1.0, v_scale=1.0):
     """Oracle attention on raw arrays.
 
-    q: uint16 bf16 (or fp16, dtype='f16') bits [B, Hq, D]; k, v: [B, S_max, Hkv, D] (contiguous)
+    q: uint16 bf16 (or fp16, dtype='f16') bits [B, Hq, D], or [B, q_len, Hq, D] for several
+    new query tokens per request (new token i sees tokens 0 .. L - q_len + i);
+    k, v: [B, S_max, Hkv, D] (contiguous)
     or [num_pages, P, Hkv, D] (paged, with block_table int32 [B, max_blocks]), uint16 bits of
     q's type, or (kv_dtype 'e4m3' / 'e5m2') uint8 FP8 codes dequantised by k_scale / v_scale.
-    items: int32 [n, 4] rows (b, h, t0, t1), t1 < 0 meaning "to L_b"; default
-    is every (b, h) over its whole length.  Returns (o [n, D], lse [n]) in
-    fp64; with items=None they are reshaped to [B, Hq, D] and [B, Hq].
+    items: int32 [n, 4] rows (b, r, t0, t1) with query row r = i * Hq + h, t1 < 0
+    meaning "to the row's causal end" (L_b when q_len = 1); default is every
+    row over its whole visible length.  Returns (o [n, D], lse [n]) in fp64;
+    with items=None they are reshaped like q ([B, Hq, D] / [B, q_len, Hq, D])
+    and [B, Hq] / [B, q_len, Hq].
     """
     lib = _load()
     kv_dtype = kv_dtype or dtype
@@ -92,7 +96,10 @@ def attend_raw(q, k, v, seq_lens, num_q_heads, num_kv_heads, scale, *,
     k = np.ascontiguousarray(k, dtype=kv_np)
     v = np.ascontiguousarray(v, dtype=kv_np)
     lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
-    B, hq, d = q.shape
+    if q.ndim == 4:
+        B, q_len, hq, d = q.shape
+    else:
+        (B, hq, d), q_len = q.shape, 1
     if page_size:
         table = np.ascontiguousarray(block_table, dtype=np.int32)
         s_max, max_blocks, num_pages = 0, table.shape[1], k.shape[0]
@@ -102,8 +109,8 @@ def attend_raw(q, k, v, seq_lens, num_q_heads, num_kv_heads, scale, *,
         cap = s_max
     full = items is None
     if full:
-        bb, hh = np.meshgrid(np.arange(B), np.arange(hq), indexing="ij")
-        items = np.stack([bb.ravel(), hh.ravel(), np.zeros(B * hq), -np.ones(B * hq)], 1)
+        bb, hh = np.meshgrid(np.arange(B), np.arange(q_len * hq), indexing="ij")
+        items = np.stack([bb.ravel(), hh.ravel(), np.zeros(bb.size), -np.ones(bb.size)], 1)
     items = np.ascontiguousarray(items, dtype=np.int32).reshape(-1, 4)
     n = items.shape[0]
     o = np.zeros((n, d), dtype=np.float64)
@@ -116,7 +123,7 @@ def attend_raw(q, k, v, seq_lens, num_q_heads, num_kv_heads, scale, *,
         rc = lib.oracle_attend(_ptr(q), _ptr(k), _ptr(v), _ptr(lens), B, hq, num_kv_heads, d,
                                s_max, page_size, _ptr(table), max_blocks, num_pages,
                                float(scale), 1 if dtype == "f16" else 0, kvcode, float(k_scale),
-                               float(v_scale), _ptr(items[lo:hi]), hi - lo,
+                               float(v_scale), q_len, _ptr(items[lo:hi]), hi - lo,
                                _ptr(scratch),
                                _ptr(o[lo:hi]), _ptr(lse[lo:hi]))
         if rc != 0:
@@ -130,6 +137,8 @@ def attend_raw(q, k, v, seq_lens, num_q_heads, num_kv_heads, scale, *,
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda i: run(bounds[i], bounds[i + 1]), range(len(bounds) - 1)))
     if full:
+        if q.ndim == 4:
+            return o.reshape(B, q_len, hq, d), lse.reshape(B, q_len, hq)
         return o.reshape(B, hq, d), lse.reshape(B, hq)
     return o, lse
 

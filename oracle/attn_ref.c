@@ -42,6 +42,12 @@
  * GQA head mapping: query head h reads kv head h / (Hq / Hkv) (consecutive
  * query heads share a kv head).  Paged layout: token t of request b lives
  * in physical page block_table[b][t / P], slot t % P.
+ *
+ * Several new query tokens per request (q_len > 1): the cache of length L
+ * already holds them, and new token i (0-based) sits at position
+ * L - q_len + i, so under the causal mask of the handbook's FlashAttention
+ * section (query i sees only the keys up to its own position) it attends to
+ * tokens [0, L - q_len + i].  q and O are [B, q_len, Hq, D].
  */
 #include <math.h>
 #include <stdint.h>
@@ -159,14 +165,14 @@ static const uint8_t *kv_row(const kv_view *w, int b, int t, int g)
  * Returns 0, or -1 when a referenced page is out of range.
  */
 static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
-                      int b, int h, int hq, int t0, int t1, double scale, int dtype,
-                      int kvtype, double k_scale, double v_scale,
+                      int b, int i_tok, int q_len, int h, int hq, int t0, int t1, double scale,
+                      int dtype, int kvtype, double k_scale, double v_scale,
                       double *s /* scratch, >= t1 - t0 */, double *o, double *lse)
 {
     const int d = kw->d;
     const int group = hq / kw->hkv;
     const int g = h / group;
-    const uint16_t *qrow = q + ((int64_t)b * hq + h) * d;
+    const uint16_t *qrow = q + (((int64_t)b * q_len + i_tok) * hq + h) * d;
     const int n = t1 - t0;
 
     for (int j = 0; j < d; ++j)
@@ -214,9 +220,12 @@ static int attend_one(const uint16_t *q, const kv_view *kw, const kv_view *vw,
  * dtype: 0 when q holds bf16 bit patterns, 1 for IEEE fp16.  kvtype: the
  * K/V element type (0 bf16, 1 fp16, 2 FP8 E4M3, 3 FP8 E5M2); k_scale and
  * v_scale multiply every decoded K and V element (1 for 16-bit caches).
- * For each of npairs items (b, h, t0, t1) in `items` (int32, 4 per item;
- * t1 < 0 means "to the request's length"), compute the attention of query
- * (b, h) over tokens [t0, min(t1, L_b)).  o is [npairs][d], lse [npairs].
+ * q_len: new query tokens per request (q is [B, q_len, Hq, D]).
+ * For each of npairs items (b, r, t0, t1) in `items` (int32, 4 per item),
+ * query row r = i * Hq + h is new token i, query head h; t1 < 0 means "to
+ * the causal end", the row's visible length max(0, L_b - q_len + i + 1).
+ * It computes the attention of that query over tokens [t0, min(t1, L_b)).
+ * o is [npairs][d], lse [npairs].
  * page_size == 0 selects the contiguous layout (k, v are [B, S_max, Hkv, D]);
  * otherwise k, v are pages [num_pages, P, Hkv, D] behind block_table.
  * scratch must hold max token count doubles.  Returns 0, or -1 on a bad page
@@ -226,21 +235,22 @@ int oracle_attend(const uint16_t *q, const void *k, const void *v,
                   const int32_t *seq_lens, int batch, int hq, int hkv, int d,
                   int s_max, int page_size, const int32_t *block_table,
                   int max_blocks, int num_pages, double scale, int dtype,
-                  int kvtype, double k_scale, double v_scale,
+                  int kvtype, double k_scale, double v_scale, int q_len,
                   const int32_t *items, int npairs, double *scratch,
                   double *o, double *lse)
 {
-    if (hkv <= 0 || hq % hkv != 0 || kvtype < 0 || kvtype > 3)
+    if (hkv <= 0 || hq % hkv != 0 || kvtype < 0 || kvtype > 3 || q_len < 1)
         return -1;
     kv_view kw = {(const uint8_t *)k, kv_elem_bytes(kvtype), page_size > 0, s_max, block_table,
                   max_blocks, page_size, num_pages, hkv, d};
     kv_view vw = kw;
     vw.base = (const uint8_t *)v;
     for (int i = 0; i < npairs; ++i) {
-        const int b = items[4 * i + 0], h = items[4 * i + 1];
+        const int b = items[4 * i + 0], r = items[4 * i + 1];
         int t0 = items[4 * i + 2], t1 = items[4 * i + 3];
-        if (b < 0 || b >= batch || h < 0 || h >= hq)
+        if (b < 0 || b >= batch || r < 0 || r >= q_len * hq)
             return -1;
+        const int i_tok = r / hq, h = r % hq;
         const int L = seq_lens[b];
         if (L < 0)
             return -1;
@@ -248,12 +258,16 @@ int oracle_attend(const uint16_t *q, const void *k, const void *v,
             return -1;
         if (page_size > 0 && L > (int64_t)max_blocks * page_size)
             return -1;
-        if (t1 < 0 || t1 > L)
-            t1 = L;
+        /* causal end of new token i_tok: it sees positions 0 .. L - q_len + i_tok */
+        int end = L - q_len + i_tok + 1;
+        if (end < 0)
+            end = 0;
+        if (t1 < 0 || t1 > end)
+            t1 = end;
         if (t0 < 0)
             t0 = 0;
-        if (attend_one(q, &kw, &vw, b, h, hq, t0, t1, scale, dtype, kvtype, k_scale, v_scale,
-                       scratch, o + (int64_t)i * d, lse + i) != 0)
+        if (attend_one(q, &kw, &vw, b, i_tok, q_len, h, hq, t0, t1, scale, dtype, kvtype, k_scale,
+                       v_scale, scratch, o + (int64_t)i * d, lse + i) != 0)
             return -1;
     }
     return 0;

@@ -1,8 +1,9 @@
 """Plant plausible mistakes in a copy of the oracle and check the pins catch each.
 
 Every mutant is compiled from a modified copy of ``oracle/attn_ref.c`` in a
-temporary directory, on the CPU, and the pin suites ``tests/test_oracle.py``
-and ``tests/test_oracle_fp8.py`` must fail (or crash) against it.  The committed oracle is never modified.
+temporary directory, on the CPU, and the pin suites ``tests/test_oracle.py``,
+``tests/test_oracle_fp8.py`` and ``tests/test_oracle_qlen.py`` must fail (or
+crash) against it.  The committed oracle is never modified.
 """
 import os
 import shutil
@@ -26,8 +27,15 @@ MUTANTS = {
     "merge weight not normalised": ("const double w = exp(lse_parts[i] - g);",
                                     "const double w = exp(lse_parts[i] - lse_max);"),
     "online correction inverted": ("exp(m - m_new);", "exp(m_new - m);"),
-    "query row indexed by kv head": ("const uint16_t *qrow = q + ((int64_t)b * hq + h) * d;",
-                                     "const uint16_t *qrow = q + ((int64_t)b * hq + g) * d;"),
+    "query row indexed by kv head": ("const uint16_t *qrow = q + (((int64_t)b * q_len + i_tok) * hq + h) * d;",
+                                     "const uint16_t *qrow = q + (((int64_t)b * q_len + i_tok) * hq + g) * d;"),
+    "causal end off by one": ("int end = L - q_len + i_tok + 1;", "int end = L - q_len + i_tok;"),
+    "new tokens see the whole cache": ("int end = L - q_len + i_tok + 1;", "int end = L;"),
+    "query rows of a request not strided by q_len": (
+        "const uint16_t *qrow = q + (((int64_t)b * q_len + i_tok) * hq + h) * d;",
+        "const uint16_t *qrow = q + (((int64_t)b + i_tok) * hq + h) * d;"),
+    "token and head of a query row swapped": ("const int i_tok = r / hq, h = r % hq;",
+                                              "const int i_tok = r % q_len, h = r / q_len;"),
     "last token dropped": ("const int n = t1 - t0;", "const int n = t1 - t0 - (t1 - t0 > 1);"),
     "fp16 exponent bias off by one": ("v = ldexp((double)(m + 1024), e - 25);", "v = ldexp((double)(m + 1024), e - 24);"),
     "fp16 subnormals flushed": ("v = ldexp((double)m, -24);", "v = 0.0;"),
@@ -56,6 +64,7 @@ def test_mutant_is_caught(name, tmp_path):
                         ignore=shutil.ignore_patterns("*.so", "__pycache__", "test_oracle_mutations.py"))
     (tmp_path / "oracle" / "attn_ref.c").write_text(src.replace(before, after))
     r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle.py",
-                        "tests/test_oracle_fp8.py", "-q", "-x", "-p", "no:cacheprovider"],
+                        "tests/test_oracle_fp8.py", "tests/test_oracle_qlen.py", "-q", "-x",
+                        "-p", "no:cacheprovider"],
                        cwd=tmp_path, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant '{name}' passed every pin:\n{r.stdout[-2000:]}"
