@@ -46,7 +46,7 @@ class FdOptions(ctypes.Structure):
                 ("wait_timeout_ns", ctypes.c_ulonglong),
                 ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p),
                 ("dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float),
-                ("v_scale", ctypes.c_float)]
+                ("v_scale", ctypes.c_float), ("q_len", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -61,6 +61,8 @@ def _load():
     lib = ctypes.CDLL(path)
     lib.fd_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
     lib.fd_workspace_size.restype = _SZ
+    lib.fd_workspace_size_q.argtypes = [_I, _I, _I, _I, _I, _I, _I]
+    lib.fd_workspace_size_q.restype = _SZ
     lib.fd_workspace_init.argtypes = [_P, _SZ, _P]
     lib.fd_workspace_init.restype = _I
     lib.fd_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _SZ,
@@ -107,8 +109,10 @@ def fd_version() -> int:
     return _lib.fd_version()
 
 
-def fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim=128, max_kv_len=0, page_size=0) -> int:
-    return int(_lib.fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_kv_len, page_size))
+def fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim=128, max_kv_len=0, page_size=0,
+                      q_len=1) -> int:
+    return int(_lib.fd_workspace_size_q(batch, num_q_heads, num_kv_heads, head_dim, max_kv_len, page_size,
+                                        q_len))
 
 
 def _stream_ptr(stream, device=None):
@@ -128,9 +132,9 @@ def fd_workspace_init(workspace: torch.Tensor, stream=None) -> None:
 
 
 def make_workspace(batch, num_q_heads, num_kv_heads, head_dim=128, max_kv_len=0, page_size=0,
-                   device="cuda") -> torch.Tensor:
+                   device="cuda", q_len=1) -> torch.Tensor:
     """Allocate (with torch) and initialise a workspace for this shape."""
-    n = fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_kv_len, page_size)
+    n = fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_kv_len, page_size, q_len)
     if n == 0:
         raise FdError(FD_ERR_INVALID_ARG, "fd_workspace_size")
     ws = torch.empty(n, dtype=torch.uint8, device=device)
@@ -188,7 +192,7 @@ def _dtype_code(t, dtype):
 
 
 def _options(num_ctas, flags, wait_timeout_ns, split_events, dtype_code=FD_DTYPE_BF16,
-             kv_code=FD_KV_AS_Q, k_scale=1.0, v_scale=1.0):
+             kv_code=FD_KV_AS_Q, k_scale=1.0, v_scale=1.0, q_len=1):
     ev0 = ev1 = None
     if split_events is not None:
         for e in split_events:
@@ -197,20 +201,28 @@ def _options(num_ctas, flags, wait_timeout_ns, split_events, dtype_code=FD_DTYPE
         ev0 = ctypes.c_void_p(split_events[0].cuda_event)
         ev1 = ctypes.c_void_p(split_events[1].cuda_event)
     return FdOptions(int(num_ctas), int(flags), int(wait_timeout_ns), ev0, ev1, int(dtype_code),
-                     int(kv_code), float(k_scale), float(v_scale))
+                     int(kv_code), float(k_scale), float(v_scale), int(q_len))
+
+
+def _q_shape(q):
+    """(B, q_len, Hq, D) of q: [B, Hq, D] (one new token) or [B, q_len, Hq, D]."""
+    if q.dim() == 4:
+        return tuple(q.shape)
+    B, hq, d = q.shape
+    return B, 1, hq, d
 
 
 def _outputs(q, out, lse):
-    B, hq, d = q.shape
+    shape_o, shape_l = tuple(q.shape), tuple(q.shape[:-1])
     if out is None:
-        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+        out = torch.empty(shape_o, dtype=torch.float32, device=q.device)
     if lse is None:
-        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
-    if out.dtype != torch.float32 or not out.is_contiguous() or tuple(out.shape) != (B, hq, d):
-        raise ValueError("out must be contiguous fp32 [B, Hq, D]")
+        lse = torch.empty(shape_l, dtype=torch.float32, device=q.device)
+    if out.dtype != torch.float32 or not out.is_contiguous() or tuple(out.shape) != shape_o:
+        raise ValueError(f"out must be contiguous fp32 {list(shape_o)}")
     if lse is not False and (lse.dtype != torch.float32 or not lse.is_contiguous()
-                             or tuple(lse.shape) != (B, hq)):
-        raise ValueError("lse must be contiguous fp32 [B, Hq]")
+                             or tuple(lse.shape) != shape_l):
+        raise ValueError(f"lse must be contiguous fp32 {list(shape_l)}")
     return out, lse
 
 
@@ -220,7 +232,9 @@ def fd_decode(q, k, v, seq_lens=None, seq_lens_host=None, scale=None, out=None, 
     """Decode attention over a contiguous KV cache (see fd_decode in include/fd.h).
 
     q [B, Hq, D] bf16 or fp16 (``dtype`` 'bf16'/'f16' overrides the tensor's
-    own type, e.g. for int16 views); k/v [B, S_max, Hkv, D] of q's type, or an
+    own type, e.g. for int16 views), or [B, q_len, Hq, D] for q_len new tokens
+    per request (token i sees cache positions 0 .. L - q_len + i; out and lse
+    then carry the q_len axis too); k/v [B, S_max, Hkv, D] of q's type, or an
     FP8 cache: torch float8_e4m3fn / float8_e5m2 tensors, or uint8 codes with
     ``kv_dtype`` 'e4m3' / 'e5m2', dequantised by ``k_scale`` / ``v_scale``.
     seq_lens int32 [B] on the device (None = every request has S_max tokens);
@@ -230,15 +244,15 @@ def fd_decode(q, k, v, seq_lens=None, seq_lens_host=None, scale=None, out=None, 
     """
     _bits(q, "q")
     kv_code = _kv_code(k, v, kv_dtype)
-    B, hq, d = q.shape
+    B, q_len, hq, d = _q_shape(q)
     _, s_max, hkv, _ = k.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     out, lse = _outputs(q, out, lse)
     if workspace is None:
-        workspace = make_workspace(B, hq, hkv, d, s_max, 0, q.device)
+        workspace = make_workspace(B, hq, hkv, d, s_max, 0, q.device, q_len=q_len)
     opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype), kv_code,
-                    k_scale, v_scale)
+                    k_scale, v_scale, q_len)
     lh = None
     if seq_lens_host is not None:
         lh = seq_lens_host.to(torch.int32).contiguous().cpu()
@@ -263,16 +277,16 @@ def fd_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=No
     _bits(q, "q")
     kv_code = _kv_code(k_pages, v_pages, kv_dtype)
     _i32(block_table, "block_table"); _i32(seq_lens, "seq_lens")
-    B, hq, d = q.shape
+    B, q_len, hq, d = _q_shape(q)
     num_pages, page, hkv, _ = k_pages.shape
     max_blocks = block_table.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     out, lse = _outputs(q, out, lse)
     if workspace is None:
-        workspace = make_workspace(B, hq, hkv, d, max_blocks * page, page, q.device)
+        workspace = make_workspace(B, hq, hkv, d, max_blocks * page, page, q.device, q_len=q_len)
     opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype), kv_code,
-                    k_scale, v_scale)
+                    k_scale, v_scale, q_len)
     lh = None
     if seq_lens_host is not None:
         lh = seq_lens_host.to(torch.int32).contiguous().cpu()

@@ -155,7 +155,13 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+// Query columns of a kv head (group x new tokens) fit one n8 tile; the
+// kernels are built for 1, 2, 4 or 8 columns and pad the rest.
+bool supported_columns(int cols) { return cols >= 1 && cols <= 8; }
+
+int pow2_columns(int cols) { return cols <= 1 ? 1 : cols <= 2 ? 2 : cols <= 4 ? 4 : 8; }
+
+int q_len_of(const fd_options *opts) { return opts && opts->q_len > 0 ? opts->q_len : 1; }
 
 bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
@@ -167,12 +173,12 @@ bool options_valid(const fd_options *opts)
     auto scale_ok = [](float x) { return x == 0.f || (x > 0.f && x < __builtin_huge_valf()); };
     return opts->num_ctas >= 0 && opts->num_ctas <= kMaxCtas && opts->dtype >= 0 && opts->dtype <= 1 &&
            opts->kv_dtype >= FD_KV_AS_Q && opts->kv_dtype <= FD_KV_FP8_E5M2 && scale_ok(opts->k_scale) &&
-           scale_ok(opts->v_scale);
+           scale_ok(opts->v_scale) && opts->q_len >= 0;
 }
 
 // Checks shared by both entry points.  Returns FD_OK or the status to report.
 fd_status check_common(const void *q, const float *o, const void *ws, int batch, int hq, int hkv,
-                       int head_dim)
+                       int head_dim, const fd_options *opts)
 {
     if (batch < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0)
         return FD_ERR_INVALID_ARG;
@@ -180,7 +186,9 @@ fd_status check_common(const void *q, const float *o, const void *ws, int batch,
         return FD_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(o, 16) || !aligned(ws, 256))
         return FD_ERR_INVALID_ARG;
-    if (!supported_head_dim(head_dim) || !supported_group(hq / hkv) || batch > kMaxBatch)
+    if (!options_valid(opts))
+        return FD_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim) || (long long)(hq / hkv) * q_len_of(opts) > 8 || batch > kMaxBatch)
         return FD_ERR_UNSUPPORTED;
     return FD_OK;
 }
@@ -214,11 +222,12 @@ bool use_mma(int group, int page_size, int row_bytes, const fd_options *opts)
 constexpr double kFuseMinTilesPerCta = 24.0;
 
 // Kv heads fused into one launch head: the largest F in {4, 2} with
-// F * head_dim <= 256, F * group <= 8 and F dividing Hkv, on the tensor-core
+// F * head_dim <= 256, F * columns <= 8 (columns = group x new tokens) and F
+// dividing Hkv, on the tensor-core
 // path only (F * group >= 2 always selects it), for short rows and at least
 // kFuseMinTilesPerCta (estimated) tiles per CTA unless FD_FLAG_FUSE_HEADS
 // forces it; 1 = no fusion.
-int fuse_factor(int group, int hkv, int head_dim, int elem_bytes, int page_size, double tiles_per_cta,
+int fuse_factor(int cols, int hkv, int head_dim, int elem_bytes, int page_size, double tiles_per_cta,
                 const fd_options *opts)
 {
     if (opts && (opts->flags & (FD_FLAG_CUDA_CORES | FD_FLAG_NO_HEAD_FUSION)))
@@ -230,7 +239,7 @@ int fuse_factor(int group, int hkv, int head_dim, int elem_bytes, int page_size,
     if (!forced && (!short_rows || tiles_per_cta < kFuseMinTilesPerCta))
         return 1;
     for (int f = 4; f >= 2; f /= 2)
-        if (f * head_dim <= 256 && f * group <= 8 && hkv % f == 0)
+        if (f * head_dim <= 256 && f * cols <= 8 && hkv % f == 0)
             return f;
     return 1;
 }
@@ -248,14 +257,15 @@ long long estimate_tiles(const int32_t *seq_lens_host, int batch, int hkv, long 
     return tiles * hkv;
 }
 
-// Workspace for every launch shape a call of this shape may take (fused or not).
-size_t workspace_bytes_needed(int batch, int hq, int hkv, int head_dim)
+// Workspace for every launch shape a call of this shape may take (fused or
+// not), with the launch's column count rounded up as the kernels pad it.
+size_t workspace_bytes_needed(int batch, int hq, int hkv, int head_dim, int q_len)
 {
-    const int group = hq / hkv;
-    size_t need = workspace_layout(batch, hkv, group, head_dim).total;
+    const int cols = (hq / hkv) * q_len;
+    size_t need = workspace_layout(batch, hkv, pow2_columns(cols), head_dim).total;
     for (int f = 2; f <= 4; f *= 2)
-        if (f * head_dim <= 256 && f * group <= 8 && hkv % f == 0) {
-            const size_t t = workspace_layout(batch, hkv / f, f * group, f * head_dim).total;
+        if (f * head_dim <= 256 && f * cols <= 8 && hkv % f == 0) {
+            const size_t t = workspace_layout(batch, hkv / f, pow2_columns(f * cols), f * head_dim).total;
             need = t > need ? t : need;
         }
     return need;
@@ -307,11 +317,14 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
                    : kv_dtype == FD_KV_FP8_E5M2 ? kKvE5m2 : (q_f16 ? kKvF16 : kKvBf16);
     const int eb = kv_elem_bytes(kv);
     // Launch shape: F fused kv heads of head_dim dims become one head of
-    // F * head_dim dims with F * group query heads.
+    // F * head_dim dims whose query columns are F x q_len x group (padded to
+    // 1, 2, 4 or 8 for the kernel's template).
     const int real_group = hq / hkv;
-    const int fuse =
-        fuse_factor(real_group, hkv, head_dim, eb, page_size, (double)est_tiles / num_ctas, opts);
-    const int group = fuse * real_group;
+    const int q_len = q_len_of(opts);
+    const int cols = real_group * q_len;
+    const int fuse = fuse_factor(cols, hkv, head_dim, eb, page_size, (double)est_tiles / num_ctas, opts);
+    const int n_cols = fuse * cols;
+    const int group = pow2_columns(n_cols);
     const int d = fuse * head_dim;
     hkv /= fuse;
     const WorkspaceLayout wl = workspace_layout(batch, hkv, group, d);
@@ -348,7 +361,10 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     sp.timeout_ns = opts && opts->wait_timeout_ns ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     sp.flags = opts ? opts->flags : 0u;
     sp.fuse_dh = fuse > 1 ? head_dim : 0;
-    sp.fuse_g = real_group;
+    sp.fuse_f = fuse;
+    sp.q_len = q_len;
+    sp.g_real = real_group;
+    sp.n_cols = n_cols;
 
     cp->group = group;
     cp->head_dim = d;
@@ -374,7 +390,10 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     mp.hkv = hkv;
     mp.num_ctas = num_ctas;
     mp.fuse_dh = sp.fuse_dh;
-    mp.fuse_g = sp.fuse_g;
+    mp.fuse_f = sp.fuse_f;
+    mp.q_len = sp.q_len;
+    mp.g_real = sp.g_real;
+    mp.n_cols = sp.n_cols;
     return FD_OK;
 }
 
@@ -404,10 +423,16 @@ extern "C" {
 size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_kv_len,
                          int page_size)
 {
+    return fd_workspace_size_q(batch, num_q_heads, num_kv_heads, head_dim, max_kv_len, page_size, 1);
+}
+
+size_t fd_workspace_size_q(int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_kv_len,
+                           int page_size, int q_len)
+{
     if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kv_len < 0 ||
-        page_size < 0 || num_q_heads % num_kv_heads != 0)
+        page_size < 0 || num_q_heads % num_kv_heads != 0 || q_len < 1)
         return 0;
-    return workspace_bytes_needed(batch, num_q_heads, num_kv_heads, head_dim);
+    return workspace_bytes_needed(batch, num_q_heads, num_kv_heads, head_dim, q_len);
 }
 
 fd_status fd_workspace_init(void *workspace, size_t workspace_bytes, fd_stream_t stream)
@@ -425,7 +450,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
                     int head_dim, int s_max, float scale, float *o, float *lse, void *workspace,
                     size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
 {
-    fd_status st = check_common(q, o, workspace, batch, num_q_heads, num_kv_heads, head_dim);
+    fd_status st = check_common(q, o, workspace, batch, num_q_heads, num_kv_heads, head_dim, opts);
     if (st != FD_OK)
         return st;
     if (s_max < 0 || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (lse && !aligned(lse, 4)))
@@ -439,7 +464,8 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
     if ((long long)batch * s_max >= (1ll << 31) ||
         (long long)num_kv_heads * batch * ceil_div(s_max, kTileTokens) >= (1ll << 31))
         return FD_ERR_UNSUPPORTED;
-    if (workspace_bytes < fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, s_max, 0))
+    if (workspace_bytes <
+        fd_workspace_size_q(batch, num_q_heads, num_kv_heads, head_dim, s_max, 0, q_len_of(opts)))
         return FD_ERR_WORKSPACE_TOO_SMALL;
     if (batch == 0)
         return FD_OK;
@@ -468,7 +494,7 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
                           int num_pages, float scale, float *o, float *lse, void *workspace,
                           size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
 {
-    fd_status st = check_common(q, o, workspace, batch, num_q_heads, num_kv_heads, head_dim);
+    fd_status st = check_common(q, o, workspace, batch, num_q_heads, num_kv_heads, head_dim, opts);
     if (st != FD_OK)
         return st;
     if (!k_pages || !v_pages || !block_table || !seq_lens_dev || !aligned(k_pages, 16) ||
@@ -499,8 +525,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
                 return FD_ERR_INVALID_ARG;
     if (!options_valid(opts))
         return FD_ERR_INVALID_ARG;
-    if (workspace_bytes <
-        fd_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, (int)cap, page_size))
+    if (workspace_bytes < fd_workspace_size_q(batch, num_q_heads, num_kv_heads, head_dim, (int)cap,
+                                              page_size, q_len_of(opts)))
         return FD_ERR_WORKSPACE_TOO_SMALL;
     if (batch == 0)
         return FD_OK;

@@ -99,14 +99,14 @@ struct SplitParams {
     int box4d;
     int box_rows_log2;   // log2 of the rows in one box: 6 (64) or log2(page size)
     int page_log2;       // paged, page size under 64: log2 of the page size
-    // Fused heads (tensor-core path only).  When fuse_dh > 0, each kv head of
-    // the launch is F = D / fuse_dh adjacent kv heads of the caller, side by
-    // side (the same bytes), and its G query heads are their F groups of
-    // fuse_g = G / F query heads: query head g owns dims
-    // [part(g), part(g) + fuse_dh) with part(g) = (g / fuse_g) fuse_dh, takes
-    // zeros for q elsewhere and writes only its own dims.  q and o rows then
-    // hold fuse_dh values.  0: no fusion (q and o rows hold D values).
-    int fuse_dh, fuse_g;
+    // Query columns of a launch head (see col_info): the caller's q is
+    // [B, q_len, Hq, dh] with dh = D / fuse_f, and a launch head is fuse_f
+    // adjacent kv heads of the caller read as one row of D elements (fused
+    // heads, tensor-core path only; fuse_f = 1 otherwise).  Its n_cols <= G
+    // columns are (part, new token i, query head g) in that order; columns
+    // n_cols .. G-1 are padding (zero query, never written).
+    int q_len, g_real, n_cols, fuse_f;
+    int fuse_dh;      // dh when fuse_f > 1, else 0 (q and o rows hold D values)
     int q_f16;        // FP8 caches: 1 when q is fp16, 0 when bf16
     float v_scale;    // multiplies O (an FP8 cache's V dequantisation scale; 1 otherwise)
 };
@@ -118,13 +118,39 @@ struct MergeParams {
     const float *ws_lse;
     const int32_t *ws_prefix;
     int batch, hq, hkv, num_ctas;
-    int fuse_dh, fuse_g;   // as in SplitParams
+    int q_len, g_real, n_cols, fuse_f, fuse_dh;   // as in SplitParams
 };
 
-// First dim of query head g's part of a fused head (0 without fusion).
-__device__ __forceinline__ int fused_part(int fuse_dh, int fuse_g, int g)
+// Where launch column n of launch head h of request b reads q and writes O:
+// part (which fused kv head), new token i (causal limit), the caller's query
+// row, and the first of the D dims that belong to it (0 without fusion).
+struct ColInfo {
+    int i;
+    int dim0;
+    size_t row;
+    bool valid;
+};
+
+__device__ __forceinline__ ColInfo col_info(int q_len, int g_real, int n_cols, int fuse_f, int fuse_dh,
+                                            int hq, int b, int h, int n)
 {
-    return fuse_dh ? (g / fuse_g) * fuse_dh : 0;
+    ColInfo c;
+    c.valid = n < n_cols;
+    const int per = q_len * g_real;   // columns of one caller kv head
+    const int nn = c.valid ? n : 0;
+    const int part = nn / per;
+    const int n2 = nn - part * per;
+    c.i = n2 / g_real;
+    const int g = n2 - c.i * g_real;
+    c.row = ((size_t)b * q_len + c.i) * hq + (size_t)(h * fuse_f + part) * g_real + g;
+    c.dim0 = part * fuse_dh;
+    return c;
+}
+
+template <class P>
+__device__ __forceinline__ ColInfo col_info(const P &p, int b, int h, int n)
+{
+    return col_info(p.q_len, p.g_real, p.n_cols, p.fuse_f, p.fuse_dh, p.hq, b, h, n);
 }
 
 // Store output element d (of D) of query row `row`: unfused rows hold D
@@ -411,6 +437,8 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
     const int slot = u + (int)blockIdx.x;
     for (int idx = ctid; idx < G * D; idx += kConsumerThreads) {
         const int g = idx / D, d = idx % D;
+        if (g >= p.n_cols)
+            continue;   // padding column
         float M = kNegInf;
 #pragma unroll
         for (int w = 0; w < NSTATE; ++w)
@@ -427,10 +455,10 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
         const float out = lsum > 0.f ? (o / lsum) * p.v_scale : 0.f;
         const float lse_v = ltrue > 0.f ? (M + log2f(ltrue)) * kLn2 : kNegInf;
         if (own) {
-            const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
-            store_o<D>(p.o, row, d, p.fuse_dh, fused_part(p.fuse_dh, p.fuse_g, g), out);
+            const ColInfo c = col_info(p, b, h, g);
+            store_o<D>(p.o, c.row, d, p.fuse_dh, c.dim0, out);
             if (d == 0 && p.lse)
-                p.lse[row] = lse_v;
+                p.lse[c.row] = lse_v;
         } else {
             p.ws_o[((size_t)slot * G + g) * D + d] = out;
             if (d == 0)
@@ -488,6 +516,11 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
     // rows per online update (fewer live scores for large G)
     constexpr int kSub0 = G >= 8 ? 1 : (G >= 4 ? 2 : RPG);
     constexpr int kSub = kSub0 < RPG ? kSub0 : RPG;
+    // causal lag of each column: new token i sees q_len - 1 - i fewer tokens
+    int lag[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+        lag[g] = p.q_len - 1 - col_info(p, 0, 0, g).i;
 
     float2 qf[G][4];
     float2 acc[G][4];
@@ -526,8 +559,10 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const uint16_t *qp = p.q + ((size_t)b * p.hq + (size_t)h * G + g) * D + li * 8;
-                const uint4 raw = ldg128_nc(qp);
+                const ColInfo c = col_info(p, b, h, g);
+                uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+                if (c.valid)
+                    raw = ldg128_nc(p.q + c.row * D + li * 8);
                 const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -568,15 +603,17 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                     sc[r][g] = x;
                 }
 
-            // Online softmax update (rows past nvalid carry no weight).
+            // Online softmax update (rows past the column's causal end, or past
+            // the request's end, carry no weight).
             float pr[kSub][G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
+                const int lim = nvalid - lag[g];
                 float tile_max = kNegInf;
 #pragma unroll
                 for (int r = 0; r < kSub; ++r) {
                     const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
-                    if (row < nvalid)
+                    if (row < lim)
                         tile_max = fmaxf(tile_max, sc[r][g]);
                 }
                 const float m_new = fmaxf(m[g], tile_max);
@@ -585,7 +622,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 #pragma unroll
                 for (int r = 0; r < kSub; ++r) {
                     const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
-                    pr[r][g] = (row < nvalid) ? exp2_approx(sc[r][g] - m_new) : 0.f;
+                    pr[r][g] = (row < lim) ? exp2_approx(sc[r][g] - m_new) : 0.f;
                     psum += pr[r][g];
                 }
                 l[g] = l[g] * alpha + psum;
@@ -781,6 +818,9 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
     for (int ks = 0; ks < KS; ++ks)
         qb[ks][0] = qb[ks][1] = 0u;
     smul[0] = smul[1] = p.scale_log2;
+    // causal lag of this lane's score columns 2 qd and 2 qd + 1
+    const int lag0 = p.q_len - 1 - col_info(p, 0, 0, 2 * qd).i;
+    const int lag1 = p.q_len - 1 - col_info(p, 0, 0, 2 * qd + 1).i;
 
     int s = 0;
     uint32_t ph = 0, cph = 0;
@@ -794,16 +834,19 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 
         if (flags & kFirstInCta) {
             // A fused head's query reads its own fuse_dh dims; zeros elsewhere.
+            // Padding columns (grp >= n_cols) keep a zero query.
             const int qdim = p.fuse_dh ? p.fuse_dh : D;
-            const int part = fused_part(p.fuse_dh, p.fuse_g, grp);
-            const uint16_t *qrow = p.q + ((size_t)b * p.hq + (size_t)h * G + (grp < G ? grp : 0)) * qdim;
+            const ColInfo col = col_info(p, b, h, grp);
+            const int part = col.dim0;
+            const bool colv = col.valid && grp < G;
+            const uint16_t *qrow = p.q + col.row * qdim;
             if constexpr (!FP8) {
                 // B[k = d][n = head]: lane holds head `grp`, dims 16 ks + 2 qd (+1) and (+8, +9).
                 const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     const int d0 = ks * 16 - part;   // first dim of this k-step in the q row
-                    const bool in = grp < G && d0 >= 0 && d0 < qdim;
+                    const bool in = colv && d0 >= 0 && d0 < qdim;
                     qb[ks][0] = in ? __ldg(q32 + d0 / 2 + qd) : 0u;
                     qb[ks][1] = in ? __ldg(q32 + d0 / 2 + 4 + qd) : 0u;
                 }
@@ -815,7 +858,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     const int d0 = ks * 16 - part;
-                    const bool in = grp < G && d0 >= 0 && d0 < qdim;
+                    const bool in = colv && d0 >= 0 && d0 < qdim;
                     uint2 w = make_uint2(0u, 0u);
                     if (in)
                         w = __ldg(reinterpret_cast<const uint2 *>(qrow + d0 + 4 * qd));
@@ -886,13 +929,14 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             for (int i = 0; i < 4; ++i)
                 sc[i] += sc2[i];
         }
-        const bool v0 = tok0 + grp < nvalid, v1 = tok0 + grp + 8 < nvalid;
-        // sc[0]: (token grp, head 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1)
+        // sc[0]: (token grp, head 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1);
+        // a token counts for a column if it is inside the column's causal end
+        const int lim0 = nvalid - lag0, lim1 = nvalid - lag1;
         float x[4];
-        x[0] = v0 ? sc[0] * smul[0] : kNegInf;
-        x[1] = v0 ? sc[1] * smul[1] : kNegInf;
-        x[2] = v1 ? sc[2] * smul[0] : kNegInf;
-        x[3] = v1 ? sc[3] * smul[1] : kNegInf;
+        x[0] = tok0 + grp < lim0 ? sc[0] * smul[0] : kNegInf;
+        x[1] = tok0 + grp < lim1 ? sc[1] * smul[1] : kNegInf;
+        x[2] = tok0 + grp + 8 < lim0 ? sc[2] * smul[0] : kNegInf;
+        x[3] = tok0 + grp + 8 < lim1 ? sc[3] * smul[1] : kNegInf;
 
         // Online softmax over this warp's 16 tokens, per head.
         float alpha[2], pw[4];
@@ -990,7 +1034,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int head = 2 * qd + j;
-                if (head < G) {
+                if (head < G && head < p.n_cols) {
                     if (dhalf == 0 && grp == 0) {
                         red_m[pair * G + head] = m[j];
                         red_l[pair * G + head] = l[j];
@@ -1094,8 +1138,9 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
     const int b = u / p.hkv, h = u - b * p.hkv;
     const int d = threadIdx.x;
     const int pb = p.ws_prefix[b], pe = p.ws_prefix[b + 1], T = p.ws_prefix[p.batch];
-    const size_t row = (size_t)b * p.hq + (size_t)h * G + g;
-    const int part = fused_part(p.fuse_dh, p.fuse_g, g);
+    const ColInfo col = col_info(p, b, h, g);   // g < n_cols (the grid's y extent)
+    const size_t row = col.row;
+    const int part = col.dim0;
     if (pe == pb) {   // empty request: O = 0, LSE = -inf
         store_o<D>(p.o, row, d, p.fuse_dh, part, 0.f);
         if (d == 0 && p.lse)
@@ -1126,6 +1171,12 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
 #pragma unroll
     for (int w = 1; w < D / 32; ++w)
         M = fmaxf(M, s_red[w]);
+    if (M == kNegInf) {   // no partial saw a visible token (a new token before the cache's start)
+        store_o<D>(p.o, row, d, p.fuse_dh, part, 0.f);
+        if (d == 0 && p.lse)
+            p.lse[row] = kNegInf;
+        return;           // M is the same in every thread: the whole block leaves
+    }
     __syncthreads();
     float sum = 0.f;
     for (int i = d; i < n; i += D)

@@ -12,7 +12,7 @@ static cudaError_t launch_merge_t(const MergeParams &p, int grid, cudaStream_t s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid, (unsigned)G);   // (segment, query head of its group)
+    cfg.gridDim = dim3((unsigned)grid, (unsigned)p.n_cols);   // (segment, query column of its head)
     cfg.blockDim = dim3(D);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

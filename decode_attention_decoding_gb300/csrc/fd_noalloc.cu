@@ -169,6 +169,10 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     sp.s_max = s_max;
     sp.scale_log2 = scale * 1.4426950408889634f;
     sp.v_scale = 1.f;
+    sp.q_len = 1;   // one query token per request, no fused heads
+    sp.g_real = group;
+    sp.n_cols = group;
+    sp.fuse_f = 1;
     sp.timeout_ns = 2000000000ull;
 
     // Shared-memory plan (same rule as the workspace entry points).
@@ -207,6 +211,10 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     mp.hq = num_q_heads;
     mp.hkv = num_kv_heads;
     mp.num_ctas = num_ctas;
+    mp.q_len = 1;
+    mp.g_real = group;
+    mp.n_cols = group;
+    mp.fuse_f = 1;
 
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);

@@ -37,8 +37,14 @@
  *     problem in the workspace header; fd_get_device_error reports it.
  *   - Alignment: q, k, v, k_pages, v_pages and o must be 16-byte aligned, and
  *     the workspace 256-byte aligned; otherwise FD_ERR_INVALID_ARG.
- *   - Supported shapes: head_dim 64, 128 or 256; Hq/Hkv in {1, 2, 4, 8};
+ *   - Supported shapes: head_dim 64, 128 or 256; G = Hq/Hkv and the new query
+ *     tokens per request q_len (fd_options.q_len) with G * q_len <= 8;
  *     batch <= 4096.  Other shapes return FD_ERR_UNSUPPORTED.
+ *   - Several new tokens (q_len > 1, e.g. checking draft tokens): the cache
+ *     of length L already holds them, q is [batch, q_len, Hq, head_dim], and
+ *     new token i (0-based) attends causally to positions 0 .. L - q_len + i.
+ *     O is [batch, q_len, Hq, head_dim] and LSE [batch, q_len, Hq]; a row that
+ *     sees no position (L < q_len - i) gets O = 0 and LSE = -inf.
  *   - Precision: q, K and V are bf16 (default) or IEEE fp16
  *     (fd_options.dtype); K and V may instead be an FP8 cache
  *     (fd_options.kv_dtype: OCP E4M3 or E5M2 codes, one byte per element, with
@@ -108,6 +114,8 @@ typedef struct fd_options {
      * multiplies O).  Ignored for 16-bit caches. */
     float k_scale;
     float v_scale;
+    /* New query tokens per request (0 means 1); see the note on q_len above. */
+    int q_len;
 } fd_options;
 
 /* Test hook: CTA 0 announces more bytes for its first tile than it loads, so
@@ -159,6 +167,12 @@ typedef struct fd_options {
  */
 size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                          int max_kv_len, int page_size);
+
+/* fd_workspace_size for calls with q_len new query tokens per request
+ * (fd_options.q_len); q_len = 1 gives fd_workspace_size.  Returns 0 for
+ * invalid arguments. */
+size_t fd_workspace_size_q(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                           int max_kv_len, int page_size, int q_len);
 
 /*
  * Zero-fill a workspace (its sticky device-error word must start at zero).

@@ -64,6 +64,9 @@ def test_workspace_size_is_host_only_and_rejects_bad_shapes(fd):
     for B, hq, hkv in ((1, 32, 32), (64, 32, 8), (1, 64, 8)):
         slots = B * hkv + 1024
         assert fd.fd_workspace_size(B, hq, hkv, 128, 1, 0) >= slots * (hq // hkv) * 129 * 4
+    # q_len new tokens: G x q_len partial rows per slot
+    assert fd.fd_workspace_size(4, 8, 2, 128, 1, 0, q_len=2) >= (4 * 2 + 1024) * 8 * 129 * 4
+    assert fd.fd_workspace_size(4, 8, 2, 128, 1, 0, q_len=1) == fd.fd_workspace_size(4, 8, 2, 128, 1, 0)
 
 
 ALIGNED = 1 << 20          # fake, 256-byte aligned device addresses (never dereferenced)
@@ -95,8 +98,15 @@ def test_decode_argument_checks(lib, fd):
         assert call_decode(lib, d=d) == E.FD_ERR_UNSUPPORTED
     for d in (64, 128, 256):   # accepted head dims reach the workspace check
         assert call_decode(lib, d=d, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
-    assert call_decode(lib, hq=6, hkv=2) == E.FD_ERR_UNSUPPORTED       # group 3
+    assert call_decode(lib, hq=6, hkv=2, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL   # group 3: padded to 4
     assert call_decode(lib, hq=32, hkv=2) == E.FD_ERR_UNSUPPORTED      # group 16
+    # several new tokens: group x q_len query columns must fit 8
+    for g, ql, ok in ((4, 2, True), (1, 8, True), (2, 3, True), (4, 3, False), (8, 2, False), (1, 9, False)):
+        opts = fd.FdOptions(0, 0, 0, None, None, 0, 0, 0.0, 0.0, ql)
+        st = call_decode(lib, hq=2 * g, hkv=2, opts=ctypes.byref(opts), wsb=1024)
+        assert st == (E.FD_ERR_WORKSPACE_TOO_SMALL if ok else E.FD_ERR_UNSUPPORTED), (g, ql)
+    opts = fd.FdOptions(0, 0, 0, None, None, 0, 0, 0.0, 0.0, -1)
+    assert call_decode(lib, opts=ctypes.byref(opts)) == E.FD_ERR_INVALID_ARG
     assert call_decode(lib, B=5000) == E.FD_ERR_UNSUPPORTED
     assert call_decode(lib, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
     lens = (ctypes.c_int32 * 2)(10, 65)
