@@ -366,6 +366,7 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             int *m = meta + s * kMetaInts;
             m[0] = b;
             m[1] = h;
+            m[2] = L - token0;   // tokens of the request from this tile on (causal limits)
             m[3] = nvalid;
             m[4] = flags;
             m[5] = b * p.hkv + h;
@@ -553,7 +554,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             return;
         }
         const int *mt = meta + s * kMetaInts;
-        const int b = mt[0], h = mt[1], nvalid = mt[3], flags = mt[4], u = mt[5];
+        const int b = mt[0], h = mt[1], rem = mt[2], nvalid = mt[3], flags = mt[4], u = mt[5];
 
         if (flags & kFirstInCta) {
             const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
@@ -608,7 +609,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             float pr[kSub][G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const int lim = nvalid - lag[g];
+                const int lim = min(nvalid, rem - lag[g]);   // the column's causal end in this tile
                 float tile_max = kNegInf;
 #pragma unroll
                 for (int r = 0; r < kSub; ++r) {
@@ -830,7 +831,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             return;
         }
         const int *mt = meta + s * kMetaInts;
-        const int b = mt[0], h = mt[1], nvalid = mt[3], flags = mt[4], u = mt[5];
+        const int b = mt[0], h = mt[1], rem = mt[2], nvalid = mt[3], flags = mt[4], u = mt[5];
 
         if (flags & kFirstInCta) {
             // A fused head's query reads its own fuse_dh dims; zeros elsewhere.
@@ -931,7 +932,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         }
         // sc[0]: (token grp, head 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1);
         // a token counts for a column if it is inside the column's causal end
-        const int lim0 = nvalid - lag0, lim1 = nvalid - lag1;
+        const int lim0 = min(nvalid, rem - lag0), lim1 = min(nvalid, rem - lag1);
         float x[4];
         x[0] = tok0 + grp < lim0 ? sc[0] * smul[0] : kNegInf;
         x[1] = tok0 + grp < lim1 ? sc[1] * smul[1] : kNegInf;
