@@ -365,6 +365,11 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     sp.q_len = q_len;
     sp.g_real = real_group;
     sp.n_cols = n_cols;
+    // launch column n = (part, new token i, query head g), part-major
+    for (int n = 0; n < n_cols; ++n) {
+        const int part = n / cols, n2 = n % cols;
+        sp.col_code[n] = (n2 / real_group) | (part << 4) | ((n2 % real_group) << 8);
+    }
 
     cp->group = group;
     cp->head_dim = d;
@@ -394,6 +399,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     mp.q_len = sp.q_len;
     mp.g_real = sp.g_real;
     mp.n_cols = sp.n_cols;
+    std::memcpy(mp.col_code, sp.col_code, sizeof mp.col_code);
     return FD_OK;
 }
 

@@ -107,6 +107,7 @@ struct SplitParams {
     // n_cols .. G-1 are padding (zero query, never written).
     int q_len, g_real, n_cols, fuse_f;
     int fuse_dh;      // dh when fuse_f > 1, else 0 (q and o rows hold D values)
+    int col_code[8];  // column n: new token i | part << 4 | head g << 8 (host-computed)
     int q_f16;        // FP8 caches: 1 when q is fp16, 0 when bf16
     float v_scale;    // multiplies O (an FP8 cache's V dequantisation scale; 1 otherwise)
 };
@@ -119,6 +120,7 @@ struct MergeParams {
     const int32_t *ws_prefix;
     int batch, hq, hkv, num_ctas;
     int q_len, g_real, n_cols, fuse_f, fuse_dh;   // as in SplitParams
+    int col_code[8];
 };
 
 // Where launch column n of launch head h of request b reads q and writes O:
@@ -131,26 +133,19 @@ struct ColInfo {
     bool valid;
 };
 
-__device__ __forceinline__ ColInfo col_info(int q_len, int g_real, int n_cols, int fuse_f, int fuse_dh,
-                                            int hq, int b, int h, int n)
-{
-    ColInfo c;
-    c.valid = n < n_cols;
-    const int per = q_len * g_real;   // columns of one caller kv head
-    const int nn = c.valid ? n : 0;
-    const int part = nn / per;
-    const int n2 = nn - part * per;
-    c.i = n2 / g_real;
-    const int g = n2 - c.i * g_real;
-    c.row = ((size_t)b * q_len + c.i) * hq + (size_t)(h * fuse_f + part) * g_real + g;
-    c.dim0 = part * fuse_dh;
-    return c;
-}
-
+// The host lays the columns out as (part, new token i, query head g) and
+// passes each column's (i, part, g) in col_code, so no division runs here.
 template <class P>
 __device__ __forceinline__ ColInfo col_info(const P &p, int b, int h, int n)
 {
-    return col_info(p.q_len, p.g_real, p.n_cols, p.fuse_f, p.fuse_dh, p.hq, b, h, n);
+    ColInfo c;
+    c.valid = n < p.n_cols;
+    const int code = p.col_code[c.valid ? n : 0];
+    c.i = code & 15;
+    const int part = (code >> 4) & 15, g = code >> 8;
+    c.row = ((size_t)b * p.q_len + c.i) * p.hq + (size_t)(h * p.fuse_f + part) * p.g_real + g;
+    c.dim0 = part * p.fuse_dh;
+    return c;
 }
 
 // Store output element d (of D) of query row `row`: unfused rows hold D
@@ -932,12 +927,21 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         }
         // sc[0]: (token grp, head 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1);
         // a token counts for a column if it is inside the column's causal end
-        const int lim0 = min(nvalid, rem - lag0), lim1 = min(nvalid, rem - lag1);
+        // (the request's end when there is one new token)
         float x[4];
-        x[0] = tok0 + grp < lim0 ? sc[0] * smul[0] : kNegInf;
-        x[1] = tok0 + grp < lim1 ? sc[1] * smul[1] : kNegInf;
-        x[2] = tok0 + grp + 8 < lim0 ? sc[2] * smul[0] : kNegInf;
-        x[3] = tok0 + grp + 8 < lim1 ? sc[3] * smul[1] : kNegInf;
+        if (p.q_len == 1) {
+            const bool v0 = tok0 + grp < nvalid, v1 = tok0 + grp + 8 < nvalid;
+            x[0] = v0 ? sc[0] * smul[0] : kNegInf;
+            x[1] = v0 ? sc[1] * smul[1] : kNegInf;
+            x[2] = v1 ? sc[2] * smul[0] : kNegInf;
+            x[3] = v1 ? sc[3] * smul[1] : kNegInf;
+        } else {
+            const int lim0 = min(nvalid, rem - lag0), lim1 = min(nvalid, rem - lag1);
+            x[0] = tok0 + grp < lim0 ? sc[0] * smul[0] : kNegInf;
+            x[1] = tok0 + grp < lim1 ? sc[1] * smul[1] : kNegInf;
+            x[2] = tok0 + grp + 8 < lim0 ? sc[2] * smul[0] : kNegInf;
+            x[3] = tok0 + grp + 8 < lim1 ? sc[3] * smul[1] : kNegInf;
+        }
 
         // Online softmax over this warp's 16 tokens, per head.
         float alpha[2], pw[4];

@@ -173,6 +173,8 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     sp.g_real = group;
     sp.n_cols = group;
     sp.fuse_f = 1;
+    for (int n = 0; n < group; ++n)
+        sp.col_code[n] = n << 8;   // token 0, part 0, query head n
     sp.timeout_ns = 2000000000ull;
 
     // Shared-memory plan (same rule as the workspace entry points).
@@ -215,6 +217,8 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     mp.g_real = group;
     mp.n_cols = group;
     mp.fuse_f = 1;
+    for (int n = 0; n < group; ++n)
+        mp.col_code[n] = n << 8;
 
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
