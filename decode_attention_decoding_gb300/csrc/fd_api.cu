@@ -198,10 +198,13 @@ struct CallPlan {
     SplitParams sp;
     MergeParams mp;
     SplitLaunch launch;
-    int group;
-    int head_dim;
-    bool mma;   // tensor-core consumers (GQA groups) instead of CUDA cores
-    int kv;     // K/V element type (kKv*): bf16, fp16 (q of the same type) or FP8
+    int group;        // split kernel's columns per warp group (template G)
+    int head_dim;     // split kernel's row dims (template D)
+    int cons;         // consumer kind (kCons*)
+    bool mma;         // tensor-core consumers (either kind)
+    int merge_group;  // merge kernel's columns per launch head
+    int merge_dim;    // merge kernel's dims per column
+    int kv;           // K/V element type (kKv*): bf16, fp16 (q of the same type) or FP8
 };
 
 // Tensor-core consumers serve GQA groups; paged pools need pages of at least
@@ -222,12 +225,14 @@ bool use_mma(int group, int page_size, int row_bytes, const fd_options *opts)
 // twice the merge width) and gained 10-85% above that on such rows.
 constexpr double kFuseMinTilesPerCta = 24.0;
 
-// Kv heads fused into one launch head: the largest F in {4, 2} with
-// F * head_dim <= 256, F * columns <= 8 (columns = group x new tokens) and F
-// dividing Hkv, on the tensor-core
-// path only (F * group >= 2 always selects it), for short rows and at least
-// kFuseMinTilesPerCta (estimated) tiles per CTA unless FD_FLAG_FUSE_HEADS
-// forces it; 1 = no fusion.
+// Kv heads fused into one launch head, on the tensor-core path only, for
+// short rows and at least kFuseMinTilesPerCta (estimated) tiles per CTA
+// unless FD_FLAG_FUSE_HEADS forces it:
+//   * 2 (paired heads: each warp of a pair takes one of the two heads, up to
+//     8 query columns each) when 2 x head_dim <= 256 and Hkv is even --
+//     unless the paired row is still under 256 bytes and 4 heads fit: then
+//   * 4 (one shared 256-dim row; 4 x columns <= 8, 4 | Hkv);
+//   * 1 otherwise.
 int fuse_factor(int cols, int hkv, int head_dim, int elem_bytes, int page_size, double tiles_per_cta,
                 const fd_options *opts)
 {
@@ -239,10 +244,11 @@ int fuse_factor(int cols, int hkv, int head_dim, int elem_bytes, int page_size, 
     const bool forced = opts && (opts->flags & FD_FLAG_FUSE_HEADS);
     if (!forced && (!short_rows || tiles_per_cta < kFuseMinTilesPerCta))
         return 1;
-    for (int f = 4; f >= 2; f /= 2)
-        if (f * head_dim <= 256 && f * cols <= 8 && hkv % f == 0)
-            return f;
-    return 1;
+    const bool four = 4 * head_dim <= 256 && 4 * cols <= 8 && hkv % 4 == 0;
+    const bool two = 2 * head_dim <= 256 && cols <= 8 && hkv % 2 == 0;
+    if (two && (2 * head_dim * elem_bytes >= 256 || !four))
+        return 2;
+    return four ? 4 : 1;
 }
 
 // KV tiles of a call (unfused): from the host copy of the lengths when the
@@ -264,22 +270,22 @@ size_t workspace_bytes_needed(int batch, int hq, int hkv, int head_dim, int q_le
 {
     const int cols = (hq / hkv) * q_len;
     size_t need = workspace_layout(batch, hkv, pow2_columns(cols), head_dim).total;
-    for (int f = 2; f <= 4; f *= 2)
-        if (f * head_dim <= 256 && f * cols <= 8 && hkv % f == 0) {
-            const size_t t = workspace_layout(batch, hkv / f, pow2_columns(f * cols), f * head_dim).total;
-            need = t > need ? t : need;
-        }
+    auto take = [&](size_t t) { need = t > need ? t : need; };
+    if (2 * head_dim <= 256 && cols <= 8 && hkv % 2 == 0)   // paired heads: both heads' columns
+        take(workspace_layout(batch, hkv / 2, 2 * pow2_columns(cols), head_dim).total);
+    if (4 * head_dim <= 256 && 4 * cols <= 8 && hkv % 4 == 0)   // four heads in one row
+        take(workspace_layout(batch, hkv / 4, pow2_columns(4 * cols), 4 * head_dim).total);
     return need;
 }
 
 // Shared-memory plan of the split kernel for the call's consumers, group,
 // head_dim, K/V element size and batch; fills the offsets and stage count in
 // sp and the byte size in launch.
-fd_status plan_smem(const DeviceInfo &dev, bool mma, int group, int d, int elem_bytes, int batch,
+fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_bytes, int batch,
                     SplitParams *sp, SplitLaunch *launch)
 {
     const size_t stage_bytes = 2u * kTileTokens * (size_t)elem_bytes * (size_t)d;   // K and V tiles
-    const size_t red = align_up((size_t)reduction_floats(mma, group, d) * sizeof(float), 16);
+    const size_t red = align_up((size_t)reduction_floats(cons, group, d) * sizeof(float), 16);
     const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
     const size_t misc = 64;
     const size_t per_stage_extra = 2 * 8 + kMetaInts * sizeof(int);   // 2 barriers + metadata
@@ -331,17 +337,21 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
                    : kv_dtype == FD_KV_FP8_E5M2 ? kKvE5m2 : (q_f16 ? kKvF16 : kKvBf16);
     const int eb = kv_elem_bytes(kv);
     // Launch shape: F fused kv heads of head_dim dims become one head of
-    // F * head_dim dims whose query columns are F x q_len x group (padded to
-    // 1, 2, 4 or 8 for the kernel's template).
+    // F * head_dim dims.  A kv head's query columns (q_len x group) are padded
+    // to 1, 2, 4 or 8.  Paired heads (F = 2) keep each head's columns in its
+    // own warp of a pair (2 x padded columns in all, head_dim dims each); four
+    // fused heads share one set of 4 x columns over 4 x head_dim dims.
     const int real_group = hq / hkv;
     const int q_len = q_len_of(opts);
     const int cols = real_group * q_len;
     const int fuse = fuse_factor(cols, hkv, head_dim, eb, page_size, (double)est_tiles / num_ctas, opts);
-    const int n_cols = fuse * cols;
-    const int group = pow2_columns(n_cols);
+    const bool paired = fuse == 2;
+    const int group = paired ? pow2_columns(cols) : pow2_columns(fuse * cols);
+    const int slots = paired ? 2 * group : group;        // column slots of a launch head
     const int d = fuse * head_dim;
+    const int merge_dim = paired ? head_dim : d;
     hkv /= fuse;
-    const WorkspaceLayout wl = workspace_layout(batch, hkv, group, d);
+    const WorkspaceLayout wl = workspace_layout(batch, hkv, slots, merge_dim);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
 
     SplitParams &sp = cp->sp;
@@ -374,26 +384,32 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     sp.q_f16 = q_f16 ? 1 : 0;
     sp.timeout_ns = opts && opts->wait_timeout_ns ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     sp.flags = opts ? opts->flags : 0u;
-    sp.fuse_dh = fuse > 1 ? head_dim : 0;
+    sp.fuse_dh = fuse == 4 ? head_dim : 0;   // only a shared 4-head row splits a column's dims
     sp.fuse_f = fuse;
     sp.q_len = q_len;
     sp.g_real = real_group;
-    sp.n_cols = n_cols;
-    // launch column n = (part, new token i, query head g), part-major
-    for (int n = 0; n < n_cols; ++n) {
-        const int part = n / cols, n2 = n % cols;
-        sp.col_code[n] = (n2 / real_group) | (part << 4) | ((n2 % real_group) << 8);
+    sp.n_cols = slots;
+    // column slot n = (part, new token i, query head g), part-major; each part
+    // holds `cols` real columns, in a block of `group` slots when paired
+    const int per_part = paired ? group : cols;
+    for (int n = 0; n < 16; ++n) {
+        const int part = n / per_part, c = n % per_part;
+        const bool real = n < slots && part < fuse && c < cols;
+        sp.col_code[n] = real ? (c / real_group) | (part << 4) | ((c % real_group) << 8) : -1;
     }
 
     cp->group = group;
     cp->head_dim = d;
     cp->kv = kv;
-    cp->mma = use_mma(group, page_size, eb * d, opts);
-    if (fuse > 1 && !cp->mma)
+    cp->merge_group = slots;
+    cp->merge_dim = merge_dim;
+    cp->mma = paired || use_mma(group, page_size, eb * d, opts);
+    cp->cons = paired ? kConsMmaPair : (cp->mma ? kConsMma : kConsCudaCores);
+    if (fuse > 1 && !use_mma(2, page_size, eb * d, opts))
         return FD_ERR_UNSUPPORTED;   // fusion is defined for the tensor-core consumers only
     cp->launch.grid = num_ctas;
     cp->launch.stream = reinterpret_cast<cudaStream_t>(stream);
-    fd_status st = plan_smem(dev, cp->mma, group, d, eb, batch, &sp, &cp->launch);
+    fd_status st = plan_smem(dev, cp->cons, group, d, eb, batch, &sp, &cp->launch);
     if (st != FD_OK)
         return st;
 
@@ -425,12 +441,12 @@ fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUte
     cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_end_event) : nullptr;
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    cudaError_t e = launch_split(paged, cp.kv, cp.head_dim, cp.mma, cp.group, cp.sp, tmk, tmv, cp.launch);
+    cudaError_t e = launch_split(paged, cp.kv, cp.head_dim, cp.cons, cp.group, cp.sp, tmk, tmv, cp.launch);
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    e = launch_merge(cp.group, cp.head_dim, cp.mp, cp.sp.batch * cp.sp.hkv, stream);
+    e = launch_merge(cp.merge_group, cp.merge_dim, cp.mp, cp.sp.batch * cp.sp.hkv, stream);
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
     return FD_OK;

@@ -63,12 +63,22 @@ struct Shape {
     static constexpr int kDimTilesPerWarp = D / 32;           // P.V dim tiles per warp of a pair
 };
 
+// Consumer kinds of the split kernel.
+enum : int {
+    kConsCudaCores = 0,   // CUDA cores, any group
+    kConsMma = 1,         // tensor cores: a warp pair shares the columns, splits the dims
+    kConsMmaPair = 2      // tensor cores on two fused kv heads: each warp of a pair takes one
+};
+
 // Floats of the shared reduction region (partial O, m, and the weight sums)
 // for one segment: one state per warp on CUDA cores, one per warp pair (with
-// two weight sums) on tensor cores.
-__host__ __device__ constexpr int reduction_floats(bool mma, int group, int d)
+// two weight sums) on tensor cores; with paired heads a pair holds both
+// heads' columns, d/2 dims each.
+__host__ __device__ constexpr int reduction_floats(int cons, int group, int d)
 {
-    return mma ? kPairs * group * (d + 3) : kConsumerWarps * group * (d + 2);
+    return cons == kConsMmaPair ? kPairs * 2 * group * (d / 2 + 3)
+           : cons == kConsMma   ? kPairs * group * (d + 3)
+                                : kConsumerWarps * group * (d + 2);
 }
 
 // Per-tile metadata flags, written by the producer into shared memory.
@@ -100,14 +110,14 @@ struct SplitParams {
     int box_rows_log2;   // log2 of the rows in one box: 6 (64) or log2(page size)
     int page_log2;       // paged, page size under 64: log2 of the page size
     // Query columns of a launch head (see col_info): the caller's q is
-    // [B, q_len, Hq, dh] with dh = D / fuse_f, and a launch head is fuse_f
-    // adjacent kv heads of the caller read as one row of D elements (fused
-    // heads, tensor-core path only; fuse_f = 1 otherwise).  Its n_cols <= G
-    // columns are (part, new token i, query head g) in that order; columns
-    // n_cols .. G-1 are padding (zero query, never written).
+    // [B, q_len, Hq, dh], and a launch head is fuse_f adjacent kv heads of
+    // the caller read as one row of D elements (fused heads, tensor-core path
+    // only; fuse_f = 1 otherwise).  Column n is (part, new token i, query
+    // head g), given by col_code[n]; a negative code marks a padding column
+    // (zero query, never written).  n_cols: the column slots of a head.
     int q_len, g_real, n_cols, fuse_f;
-    int fuse_dh;      // dh when fuse_f > 1, else 0 (q and o rows hold D values)
-    int col_code[8];  // column n: new token i | part << 4 | head g << 8 (host-computed)
+    int fuse_dh;       // dh when a fused row's parts share each column's dims, else 0
+    int col_code[16];  // new token i | part << 4 | head g << 8, or -1 (host-computed)
     int q_f16;        // FP8 caches: 1 when q is fp16, 0 when bf16
     float v_scale;    // multiplies O (an FP8 cache's V dequantisation scale; 1 otherwise)
 };
@@ -120,7 +130,7 @@ struct MergeParams {
     const int32_t *ws_prefix;
     int batch, hq, hkv, num_ctas;
     int q_len, g_real, n_cols, fuse_f, fuse_dh;   // as in SplitParams
-    int col_code[8];
+    int col_code[16];
 };
 
 // Where launch column n of launch head h of request b reads q and writes O:
@@ -139,8 +149,9 @@ template <class P>
 __device__ __forceinline__ ColInfo col_info(const P &p, int b, int h, int n)
 {
     ColInfo c;
-    c.valid = n < p.n_cols;
-    const int code = p.col_code[c.valid ? n : 0];
+    const int raw = p.col_code[n];
+    c.valid = raw >= 0;
+    const int code = c.valid ? raw : 0;
     c.i = code & 15;
     const int part = (code >> 4) & 15, g = code >> 8;
     c.row = ((size_t)b * p.q_len + c.i) * p.hq + (size_t)(h * p.fuse_f + part) * p.g_real + g;
@@ -433,7 +444,7 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
     const int slot = u + (int)blockIdx.x;
     for (int idx = ctid; idx < G * D; idx += kConsumerThreads) {
         const int g = idx / D, d = idx % D;
-        if (g >= p.n_cols)
+        if (p.col_code[g] < 0)
             continue;   // padding column
         float M = kNegInf;
 #pragma unroll
@@ -762,7 +773,7 @@ __device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk
 //     the conversion (exact for every element that stays an fp16 normal), and
 //     the score is multiplied back by the same power of two.
 
-template <int G, int KV, int D>
+template <int G, int KV, int D, bool PAIR>
 __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t *smem, uint32_t stage0,
                                                    const int *meta, uint32_t full0, uint32_t empty0,
                                                    uint32_t cbar, volatile int *abort_flag, int t_begin,
@@ -770,7 +781,14 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 {
     static_assert(G >= 1 && G <= 8, "one n8 tile of query heads");
     using HD = Shape<D, KV>;
-    constexpr int KS = HD::kKSteps, DT = HD::kDimTilesPerWarp;
+    // PAIR: the row holds two kv heads of D/2 dims; warp dhalf of a pair owns
+    // head dhalf entirely (its G columns, its D/2 dims for q.K^T and for P.V).
+    // Otherwise both warps of a pair share the G columns and split the dims.
+    constexpr int DW = PAIR ? D / 2 : D;         // dims of one column's q row
+    constexpr int KS = DW / 16;                  // k-steps of q.K^T
+    constexpr int DT = HD::kDimTilesPerWarp;     // 16-dim tiles of P.V per warp
+    constexpr int GT = PAIR ? 2 * G : G;         // columns of the launch head
+    constexpr int DR = PAIR ? D / 2 : D;         // dims kept per column in the reduction
     constexpr bool FP8 = kv_is_fp8(KV);
     constexpr bool MMA_F16 = KV != kKvBf16;   // fp16 MMAs for fp16 and FP8 caches
     static_assert(HD::kParts >= 1, "tensor-core rows span at least one 128-byte part");
@@ -779,10 +797,12 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
     const int grp = lane >> 2, qd = lane & 3;   // mma fragment coordinates
     const int tok0 = pair * 16;
     const int rl = p.box_rows_log2;
-    float *red_acc = reinterpret_cast<float *>(smem + p.off_red);   // [pairs][G][D]
-    float *red_m = red_acc + kPairs * G * D;                         // [pairs][G]
-    float *red_l = red_m + kPairs * G;                               // [2 pairs][G]: l, then lt
+    float *red_acc = reinterpret_cast<float *>(smem + p.off_red);   // [pairs][GT][DR]
+    float *red_m = red_acc + kPairs * GT * DR;                       // [pairs][GT]
+    float *red_l = red_m + kPairs * GT;                              // [2 pairs][GT]: l, then lt
     const int ctid = cw * 32 + lane;
+    const int cbase = PAIR ? dhalf * G : 0;                          // this warp's first column
+    const int koff = PAIR ? dhalf * (HD::kRowBytes / 32) : 0;        // its first 16-byte chunk of K
 
     uint32_t qb[KS][2];        // Q^T B-fragments, one pair per 16-dim k-step
     float smul[2];             // score multipliers of heads 2 qd, 2 qd + 1 (log2 units)
@@ -815,8 +835,8 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         qb[ks][0] = qb[ks][1] = 0u;
     smul[0] = smul[1] = p.scale_log2;
     // causal lag of this lane's score columns 2 qd and 2 qd + 1
-    const int lag0 = p.q_len - 1 - col_info(p, 0, 0, 2 * qd).i;
-    const int lag1 = p.q_len - 1 - col_info(p, 0, 0, 2 * qd + 1).i;
+    const int lag0 = p.q_len - 1 - col_info(p, 0, 0, cbase + 2 * qd).i;
+    const int lag1 = p.q_len - 1 - col_info(p, 0, 0, cbase + 2 * qd + 1).i;
 
     int s = 0;
     uint32_t ph = 0, cph = 0;
@@ -830,9 +850,9 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 
         if (flags & kFirstInCta) {
             // A fused head's query reads its own fuse_dh dims; zeros elsewhere.
-            // Padding columns (grp >= n_cols) keep a zero query.
-            const int qdim = p.fuse_dh ? p.fuse_dh : D;
-            const ColInfo col = col_info(p, b, h, grp);
+            // Padding columns keep a zero query.
+            const int qdim = PAIR ? DW : (p.fuse_dh ? p.fuse_dh : D);
+            const ColInfo col = col_info(p, b, h, cbase + grp);
             const int part = col.dim0;
             const bool colv = col.valid && grp < G;
             const uint16_t *qrow = p.q + col.row * qdim;
@@ -904,7 +924,8 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     uint32_t a0, a1, a2, a3;
-                    ldmatrix_x4(sw128_addr<HD::kParts>(ktile, row, 2 * ks + (lane >> 4), rl), a0, a1, a2, a3);
+                    ldmatrix_x4(sw128_addr<HD::kParts>(ktile, row, koff + 2 * ks + (lane >> 4), rl), a0, a1, a2,
+                                a3);
                     mma_16816<MMA_F16>((ks & 1) ? sc2 : sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
                 }
             } else {
@@ -912,7 +933,8 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 #pragma unroll
                 for (int kk = 0; kk < KS / 2; ++kk) {
                     uint32_t r0, r1, r2, r3;
-                    ldmatrix_x4(sw128_addr<HD::kParts>(ktile, row, 2 * kk + (lane >> 4), rl), r0, r1, r2, r3);
+                    ldmatrix_x4(sw128_addr<HD::kParts>(ktile, row, koff + 2 * kk + (lane >> 4), rl), r0, r1, r2,
+                                r3);
                     mma_16816<true>(sc, fp8x2_to_f16x2<KV>(lo16(r0)), fp8x2_to_f16x2<KV>(lo16(r1)),
                                     fp8x2_to_f16x2<KV>(hi16(r0)), fp8x2_to_f16x2<KV>(hi16(r1)), qb[2 * kk][0],
                                     qb[2 * kk][1]);
@@ -1038,21 +1060,22 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int head = 2 * qd + j;
-                if (head < G && head < p.n_cols) {
-                    if (dhalf == 0 && grp == 0) {
-                        red_m[pair * G + head] = m[j];
-                        red_l[pair * G + head] = l[j];
-                        red_l[(kPairs + pair) * G + head] = lt[j];   // exact sums after the pairs' slots
+                const int head = 2 * qd + j;              // this warp's column
+                const int gcol = cbase + head;            // the launch head's column
+                if (head < G && p.col_code[gcol] >= 0) {
+                    if ((PAIR || dhalf == 0) && grp == 0) {
+                        red_m[pair * GT + gcol] = m[j];
+                        red_l[pair * GT + gcol] = l[j];
+                        red_l[(kPairs + pair) * GT + gcol] = lt[j];   // exact sums after the pairs' slots
                     }
 #pragma unroll
                     for (int i = 0; i < DT; ++i) {
                         // output rows grp and grp + 8 of the tile: dims grp and grp + 8, or for
-                        // FP8 caches 2 grp and 2 grp + 1 (see above)
-                        const int d0 = (dhalf * DT + i) * 16;
+                        // FP8 caches 2 grp and 2 grp + 1 (see above); paired heads keep their own dims
+                        const int d0 = (dhalf * DT + i) * 16 - (PAIR ? dhalf * DR : 0);
                         const int dlo = d0 + (FP8 ? 2 * grp : grp), dhi = d0 + (FP8 ? 2 * grp + 1 : grp + 8);
-                        red_acc[(pair * G + head) * D + dlo] = acc[i][j];
-                        red_acc[(pair * G + head) * D + dhi] = acc[i][j + 2];
+                        red_acc[(pair * GT + gcol) * DR + dlo] = acc[i][j];
+                        red_acc[(pair * GT + gcol) * DR + dhi] = acc[i][j + 2];
                     }
                 }
             }
@@ -1060,8 +1083,8 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                 give_up();
                 return;
             }
-            combine_and_write<G, kPairs, D>(p, red_acc, red_m, red_l, red_l + kPairs * G, ctid, b, h, u,
-                                            (flags & kOwnSegment) != 0);
+            combine_and_write<GT, kPairs, DR>(p, red_acc, red_m, red_l, red_l + kPairs * GT, ctid, b, h, u,
+                                              (flags & kOwnSegment) != 0);
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
@@ -1077,7 +1100,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 
 // ------------------------------------------------------------------ kernels
 
-template <int G, bool PAGED, bool MMA, int KV, int D>
+template <int G, bool PAGED, int CONS, int KV, int D>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv)
@@ -1119,11 +1142,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         return;
     volatile int *abort_flag = misc;
     if (warp == kConsumerWarps)
-        split_producer<PAGED, MMA, D, KV>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
-                                          t_begin, t_end, lane);
-    else if constexpr (MMA)
-        split_consumer_mma<G, KV, D>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin,
-                                     t_end, warp, lane);
+        split_producer<PAGED, CONS != kConsCudaCores, D, KV>(p, &tmk, &tmv, stage0, prefix, meta, full0,
+                                                             empty0, abort_flag, t_begin, t_end, lane);
+    else if constexpr (CONS != kConsCudaCores)
+        split_consumer_mma<G, KV, D, CONS == kConsMmaPair>(p, smem, stage0, meta, full0, empty0, cbar,
+                                                           abort_flag, t_begin, t_end, warp, lane);
     else
         split_consumer<G, KV, D>(p, smem, stage0, meta, full0, empty0, cbar, abort_flag, t_begin, t_end,
                                  warp, lane);
@@ -1144,6 +1167,8 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
     const int d = threadIdx.x;
     const int pb = p.ws_prefix[b], pe = p.ws_prefix[b + 1], T = p.ws_prefix[p.batch];
     const ColInfo col = col_info(p, b, h, g);   // g < n_cols (the grid's y extent)
+    if (!col.valid)
+        return;   // padding column: nothing to write
     const size_t row = col.row;
     const int part = col.dim0;
     if (pe == pb) {   // empty request: O = 0, LSE = -inf

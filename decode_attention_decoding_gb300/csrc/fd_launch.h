@@ -23,7 +23,7 @@ struct SplitLaunch {
 cudaError_t launch_merge(int group, int head_dim, const MergeParams &p, int grid, cudaStream_t stream);
 
 // Shared by the split translation units.
-template <int G, bool PAGED, bool MMA, int KV, int D>
+template <int G, bool PAGED, int CONS, int KV, int D>
 cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const SplitLaunch &c)
 {
@@ -36,7 +36,7 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
         return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(split_kernel<G, PAGED, MMA, KV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(split_kernel<G, PAGED, CONS, KV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)c.smem_optin);
         if (e != cudaSuccess)
             return e;
@@ -54,33 +54,46 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
     cfg.stream = c.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, MMA, KV, D>, p, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, CONS, KV, D>, p, tmk, tmv);
 }
 
-// One split-kernel variant per (layout, K/V element type, head_dim):
-// consumers on tensor cores (mma: group 2, 4 or 8, swizzled K/V maps, rows of
-// at least 128 bytes) or CUDA cores (any group).  Returns
-// cudaErrorInvalidValue for an unsupported group or consumer choice.
+// One split-kernel variant per (layout, K/V element type, row dims D):
+// consumers on CUDA cores (any group), on tensor cores (group 2, 4 or 8,
+// swizzled K/V maps, rows of at least 128 bytes), or on tensor cores with two
+// fused kv heads per row (group = columns per head, 1 to 8; D = 2 x head_dim).
+// Returns cudaErrorInvalidValue for an unsupported combination.
 template <bool PAGED, int KV, int D>
-cudaError_t launch_split_variant(bool mma, int group, const SplitParams &p, const CUtensorMap &tmk,
+cudaError_t launch_split_variant(int cons, int group, const SplitParams &p, const CUtensorMap &tmk,
                                  const CUtensorMap &tmv, const SplitLaunch &c)
 {
-    if (mma) {
+    if (cons == kConsMma) {
         if constexpr (Shape<D, KV>::kParts >= 1) {
             switch (group) {
-            case 2: return launch_split_t<2, PAGED, true, KV, D>(p, tmk, tmv, c);
-            case 4: return launch_split_t<4, PAGED, true, KV, D>(p, tmk, tmv, c);
-            case 8: return launch_split_t<8, PAGED, true, KV, D>(p, tmk, tmv, c);
+            case 2: return launch_split_t<2, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
+            case 4: return launch_split_t<4, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
+            case 8: return launch_split_t<8, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
+            default: return cudaErrorInvalidValue;
+            }
+        }
+        return cudaErrorInvalidValue;
+    }
+    if (cons == kConsMmaPair) {
+        if constexpr (Shape<D, KV>::kParts >= 1 && D >= 128) {
+            switch (group) {
+            case 1: return launch_split_t<1, PAGED, kConsMmaPair, KV, D>(p, tmk, tmv, c);
+            case 2: return launch_split_t<2, PAGED, kConsMmaPair, KV, D>(p, tmk, tmv, c);
+            case 4: return launch_split_t<4, PAGED, kConsMmaPair, KV, D>(p, tmk, tmv, c);
+            case 8: return launch_split_t<8, PAGED, kConsMmaPair, KV, D>(p, tmk, tmv, c);
             default: return cudaErrorInvalidValue;
             }
         }
         return cudaErrorInvalidValue;
     }
     switch (group) {
-    case 1: return launch_split_t<1, PAGED, false, KV, D>(p, tmk, tmv, c);
-    case 2: return launch_split_t<2, PAGED, false, KV, D>(p, tmk, tmv, c);
-    case 4: return launch_split_t<4, PAGED, false, KV, D>(p, tmk, tmv, c);
-    case 8: return launch_split_t<8, PAGED, false, KV, D>(p, tmk, tmv, c);
+    case 1: return launch_split_t<1, PAGED, kConsCudaCores, KV, D>(p, tmk, tmv, c);
+    case 2: return launch_split_t<2, PAGED, kConsCudaCores, KV, D>(p, tmk, tmv, c);
+    case 4: return launch_split_t<4, PAGED, kConsCudaCores, KV, D>(p, tmk, tmv, c);
+    case 8: return launch_split_t<8, PAGED, kConsCudaCores, KV, D>(p, tmk, tmv, c);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -93,7 +106,7 @@ cudaError_t launch_split_variant(bool mma, int group, const SplitParams &p, cons
     FD_SPLIT_VARIANTS_KV(X, P, kKvE4m3) FD_SPLIT_VARIANTS_KV(X, P, kKvE5m2)
 #define FD_SPLIT_VARIANTS(X) FD_SPLIT_VARIANTS_P(X, false) FD_SPLIT_VARIANTS_P(X, true)
 #define FD_EXTERN_SPLIT(P, KV, D)                                                                \
-    extern template cudaError_t launch_split_variant<P, KV, D>(bool, int, const SplitParams &, \
+    extern template cudaError_t launch_split_variant<P, KV, D>(int, int, const SplitParams &, \
                                                               const CUtensorMap &,             \
                                                               const CUtensorMap &, const SplitLaunch &);
 FD_SPLIT_VARIANTS(FD_EXTERN_SPLIT)
@@ -101,13 +114,13 @@ FD_SPLIT_VARIANTS(FD_EXTERN_SPLIT)
 
 // Split launch for a call: layout, K/V element type (kKv*) and head_dim pick
 // the variant.  Returns cudaErrorInvalidValue for an unsupported head_dim.
-inline cudaError_t launch_split(bool paged, int kv, int head_dim, bool mma, int group,
+inline cudaError_t launch_split(bool paged, int kv, int head_dim, int cons, int group,
                                 const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 const SplitLaunch &c)
 {
 #define FD_PICK_SPLIT(P, KV, D)                                                 \
     if (paged == P && kv == KV && head_dim == D)                              \
-        return launch_split_variant<P, KV, D>(mma, group, p, tmk, tmv, c);
+        return launch_split_variant<P, KV, D>(cons, group, p, tmk, tmv, c);
     FD_SPLIT_VARIANTS(FD_PICK_SPLIT)
 #undef FD_PICK_SPLIT
     return cudaErrorInvalidValue;

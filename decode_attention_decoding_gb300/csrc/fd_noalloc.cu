@@ -173,12 +173,12 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     sp.g_real = group;
     sp.n_cols = group;
     sp.fuse_f = 1;
-    for (int n = 0; n < group; ++n)
-        sp.col_code[n] = n << 8;   // token 0, part 0, query head n
+    for (int n = 0; n < 16; ++n)
+        sp.col_code[n] = n < group ? n << 8 : -1;   // token 0, part 0, query head n
     sp.timeout_ns = 2000000000ull;
 
     // Shared-memory plan (same rule as the workspace entry points).
-    const size_t red = align_up((size_t)reduction_floats(false, group, kD) * sizeof(float), 16);
+    const size_t red = align_up((size_t)reduction_floats(kConsCudaCores, group, kD) * sizeof(float), 16);
     const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
     const size_t misc = 64;
     const size_t fixed = 1024 + red + prefix + misc + 8;
@@ -217,8 +217,8 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     mp.g_real = group;
     mp.n_cols = group;
     mp.fuse_f = 1;
-    for (int n = 0; n < group; ++n)
-        mp.col_code[n] = n << 8;
+    for (int n = 0; n < 16; ++n)
+        mp.col_code[n] = n < group ? n << 8 : -1;
 
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
@@ -229,7 +229,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     // The status word is the only part of the scratch that must start at zero.
     if (cudaMemsetAsync(sp.ws_err, 0, sizeof(unsigned int), launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    if (launch_split_variant<false, kKvBf16, kD>(false, group, sp, tmk, tmv, launch) != cudaSuccess)
+    if (launch_split_variant<false, kKvBf16, kD>(kConsCudaCores, group, sp, tmk, tmv, launch) != cudaSuccess)
         return FD_ERR_CUDA;
     if (launch_merge(group, kD, mp, batch * num_kv_heads, launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;

@@ -65,7 +65,10 @@ def test_paged_vs_oracle_and_contiguous(fmt, d, group, page):
         assert np.array_equal(op, oc) and np.array_equal(lp, lc)
 
 
-@pytest.mark.parametrize("d,group,hkv", [(64, 1, 4), (64, 2, 4), (128, 1, 4), (128, 4, 2), (64, 4, 2)])
+# (64, 1, 4) and (64, 2, 4) fuse four 64-code heads into one shared 256-byte row;
+# the others pair two heads (one per warp of a pair), (128, 8, 2) included
+@pytest.mark.parametrize("d,group,hkv", [(64, 1, 4), (64, 2, 4), (128, 1, 4), (128, 4, 2), (64, 4, 2),
+                                         (128, 8, 2)])
 @pytest.mark.parametrize("fmt", FMTS)
 def test_fused_heads(fmt, d, group, hkv):
     w = syn.make_contiguous(1800 + d + group, len(RAGGED), hkv * group, hkv, d, 1024, RAGGED,

@@ -1,8 +1,9 @@
-"""Fused kv heads: F adjacent kv heads read as one head of F * head_dim dims
-(the same bytes), their query groups sharing one tensor-core tile with zeros
-for the other heads' dims.  The fused launch must give what the unfused one
-gives: each query head attends to its own kv head only, and writes only its
-own head_dim outputs."""
+"""Fused kv heads: F adjacent kv heads read as one row of F * head_dim dims
+(the same bytes).  Two heads are paired (each warp of a pair takes one head);
+four share one tensor-core tile with zeros for the other heads' dims (the
+FP8 tests cover that launch).  The fused launch must give what the unfused
+one gives: each query head attends to its own kv head only, and writes only
+its own head_dim outputs."""
 import numpy as np
 import pytest
 import torch
@@ -26,16 +27,16 @@ def built():
     oracle.build()
 
 
-# (head_dim, group, hkv): the fusion factor the library picks is in the comment
-SHAPES = [(64, 1, 4),    # F = 4: one 256-dim head, 4 query heads
-          (64, 2, 4),    # F = 4: 8 query heads
-          (64, 4, 2),    # F = 2
-          (64, 2, 6),    # F = 2 (6 is not a multiple of 4)
-          (128, 1, 4),   # F = 2: 256 dims
-          (128, 2, 2),   # F = 2
-          (128, 4, 2),   # F = 2: 8 query heads
-          (128, 8, 2),   # F = 1: 16 query heads would not fit one tile
-          (64, 1, 3)]    # F = 1: odd Hkv
+# (head_dim, group, hkv): the launch the library picks is in the comment
+SHAPES = [(64, 1, 4),    # paired heads (two 64-dim heads per 256-byte row)
+          (64, 2, 4),    # paired
+          (64, 4, 2),    # paired
+          (64, 2, 6),    # paired
+          (128, 1, 4),   # paired: 256 dims per row
+          (128, 2, 2),   # paired
+          (128, 4, 2),   # paired
+          (128, 8, 2),   # paired: 8 query heads per warp, 16 per launch head
+          (64, 1, 3)]    # no fusion: odd Hkv
 
 
 @pytest.mark.parametrize("d,group,hkv", SHAPES)
@@ -66,7 +67,8 @@ def test_fused_paged_matches_oracle_and_contiguous(d, group, hkv, page):
         assert np.array_equal(op, oc) and np.array_equal(lp, lc)
 
 
-@pytest.mark.parametrize("d,group,hkv", [(64, 1, 4), (64, 2, 4), (128, 2, 2), (128, 4, 2)])
+@pytest.mark.parametrize("d,group,hkv", [(64, 1, 4), (64, 2, 4), (128, 2, 2), (128, 4, 2), (128, 8, 2),
+                                         (64, 8, 4)])
 def test_fused_heads_never_mix(d, group, hkv):
     """Each kv head gets its own dominating token; a query head that saw
     another head's keys or values would pick the wrong token."""
