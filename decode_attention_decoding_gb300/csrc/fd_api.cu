@@ -430,6 +430,8 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     mp.g_real = sp.g_real;
     mp.n_cols = sp.n_cols;
     std::memcpy(mp.col_code, sp.col_code, sizeof mp.col_code);
+    mp.seq_lens = seq_lens_dev;
+    mp.cap = cap;
     return FD_OK;
 }
 

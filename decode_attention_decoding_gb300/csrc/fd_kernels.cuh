@@ -131,7 +131,12 @@ struct MergeParams {
     int batch, hq, hkv, num_ctas;
     int q_len, g_real, n_cols, fuse_f, fuse_dh;   // as in SplitParams
     int col_code[16];
+    const int32_t *seq_lens;   // as in SplitParams (small batches: segment geometry)
+    int cap;
 };
+
+constexpr int kMergeDirectBatch = 32;   // batches this small: segment geometry from the lengths
+constexpr int kMergeDirectParts = 16;   // segments split this few ways: one load round trip
 
 // Where launch column n of launch head h of request b reads q and writes O:
 // part (which fused kv head), new token i (causal limit), the caller's query
@@ -1117,9 +1122,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const uint32_t cbar = empty0 + 8 * p.num_stages;   // consumer-warp barrier
     const uint32_t stage0 = smem_addr(smem);
 
-    // The merge kernel may launch now; it waits for this grid on its own.
-    pdl_launch_dependents();
-
     if (tid == 0) {
         for (int s = 0; s < p.num_stages; ++s) {
             mbar_init(full0 + 8 * s, 1);
@@ -1133,6 +1135,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     // stream: everything above overlapped its tail; inputs and the workspace
     // are touched only after it has completed.
     pdl_wait_prior_grid();
+    // The merge kernel may launch now; it waits for this grid on its own.  Its
+    // early part reads the lengths, which the kernels before this one (now
+    // complete) may have written.
+    pdl_launch_dependents();
     build_prefix(p, prefix, misc + 1);   // ends with __syncthreads
 
     const int T = prefix[p.batch];
@@ -1153,19 +1159,56 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 }
 
 // One CTA per (segment, query head of its group); thread d owns output dim d.
-// The partials' log-sum-exps and merge weights are staged in shared memory
-// so each output needs only one pass over the partial rows.
+// After the split grid completes, the merge is a chain of dependent loads, so
+// it keeps the chain short: for small batches the segment's tile range comes
+// from the lengths before the wait (as the split kernel derives it), and a
+// segment split n <= kMergeDirectParts ways is merged with one round trip of
+// loads and no block reductions.  Larger cases stage the partials' LSEs and
+// merge weights in shared memory.
 template <int G, int D>
 __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeParams p)
 {
     __shared__ float s_w[kMaxCtas];
     __shared__ float s_lse;
-    pdl_launch_dependents();   // the next call's split kernel may start its prologue
-    pdl_wait_prior_grid();
+    __shared__ int s_geo[3];   // small batches: first tile of request b, its end, total tiles
     const int u = blockIdx.x, g = blockIdx.y;
     const int b = u / p.hkv, h = u - b * p.hkv;
     const int d = threadIdx.x;
-    const int pb = p.ws_prefix[b], pe = p.ws_prefix[b + 1], T = p.ws_prefix[p.batch];
+    const bool small = p.batch <= kMergeDirectBatch;
+    if (small && d < 32) {
+        int L = 0;
+        if (d < p.batch) {
+            L = p.seq_lens ? p.seq_lens[d] : p.cap;
+            L = L < 0 ? 0 : (L > p.cap ? p.cap : L);   // clamped as the split kernel clamps
+        }
+        const int t = ceil_div(L, kTileTokens);
+        int x = t;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (d >= off)
+                x += y;
+        }
+        if (d == b) {
+            s_geo[0] = (x - t) * p.hkv;
+            s_geo[1] = x * p.hkv;
+        }
+        if (d == 31)
+            s_geo[2] = x * p.hkv;
+    }
+    __syncthreads();
+    pdl_launch_dependents();   // the next call's split kernel may start its prologue
+    pdl_wait_prior_grid();
+    int pb, pe, T;
+    if (small) {
+        pb = s_geo[0];
+        pe = s_geo[1];
+        T = s_geo[2];
+    } else {
+        pb = p.ws_prefix[b];
+        pe = p.ws_prefix[b + 1];
+        T = p.ws_prefix[p.batch];
+    }
     const ColInfo col = col_info(p, b, h, g);   // g < n_cols (the grid's y extent)
     if (!col.valid)
         return;   // padding column: nothing to write
@@ -1183,6 +1226,50 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
     if (c0 == c1)
         return;   // one CTA saw the whole segment and wrote it
     const int n = c1 - c0 + 1;
+    if (n <= kMergeDirectParts) {
+        // every thread loads the n partial LSEs (the same addresses) and its own
+        // n partial outputs together, then combines them itself
+        float lv[kMergeDirectParts], ov[kMergeDirectParts];
+        const float *lsrc = p.ws_lse + (size_t)(u + c0) * G + g;
+        const float *osrc = p.ws_o + ((size_t)(u + c0) * G + g) * D + d;
+#pragma unroll
+        for (int i = 0; i < kMergeDirectParts; ++i) {
+            lv[i] = i < n ? lsrc[(size_t)i * G] : kNegInf;
+            ov[i] = i < n ? osrc[(size_t)i * G * D] : 0.f;
+        }
+        float M = kNegInf;
+#pragma unroll
+        for (int i = 0; i < kMergeDirectParts; ++i) {
+            if (i >= n)
+                break;
+            M = fmaxf(M, lv[i]);
+        }
+        if (M == kNegInf) {   // no partial saw a visible token
+            store_o<D>(p.o, row, d, p.fuse_dh, part, 0.f);
+            if (d == 0 && p.lse)
+                p.lse[row] = kNegInf;
+            return;
+        }
+        float S = 0.f;
+#pragma unroll
+        for (int i = 0; i < kMergeDirectParts; ++i) {
+            if (i >= n)
+                break;
+            S += expf(lv[i] - M);
+        }
+        const float lse = M + logf(S);
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < kMergeDirectParts; ++i) {
+            if (i >= n)
+                break;
+            acc += ov[i] * expf(lv[i] - lse);
+        }
+        store_o<D>(p.o, row, d, p.fuse_dh, part, acc);
+        if (d == 0 && p.lse)
+            p.lse[row] = lse;
+        return;
+    }
     float lmax = kNegInf;
     for (int i = d; i < n; i += D) {
         const float v = p.ws_lse[(size_t)(u + c0 + i) * G + g];

@@ -213,6 +213,8 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     mp.hq = num_q_heads;
     mp.hkv = num_kv_heads;
     mp.num_ctas = num_ctas;
+    mp.seq_lens = seq_lens_dev;
+    mp.cap = s_max;
     mp.q_len = 1;
     mp.g_real = group;
     mp.n_cols = group;
