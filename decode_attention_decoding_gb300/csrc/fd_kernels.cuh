@@ -8,23 +8,26 @@
 //     for a free shared-memory stage, writes the tile's metadata, and issues
 //     TMA loads of the K and V tiles (paged: one load per page, addressed
 //     through the block table) that complete on the stage's "full" mbarrier;
-//   * warps 0..7 are consumers (CUDA-core variant shown here; the
-//     tensor-core variant for GQA groups is described at split_consumer_mma):
-//     warp w reads rows 8w..8w+7 of every tile, 32/(D/8) rows at a time (a
-//     row spans D/8 lanes; each lane holds 8 of the D head dimensions, read
-//     as one 16-byte shared load).  For every query head of the kv head's
-//     GQA group it forms the score q.k in fp32 (packed fp32x2 FMAs, a
-//     shuffle reduction over the row's lanes), keeps an online softmax in
-//     the log2 domain (running max m, running sum l, fp32 accumulator
-//     rescaled by 2^(m_old - m_new) every tile, as in the handbook's
-//     FlashAttention section), and accumulates p * V.  It then releases the
-//     stage on its "empty" mbarrier -- there is no CTA-wide barrier per tile.
+//   * warps 0..7 are consumers, of one of three kinds (kCons*):
+//       - CUDA cores (shown here): warp w reads rows 8w..8w+7 of every tile,
+//         32/(D/8) rows at a time (a row spans D/8 lanes; each lane holds 8 of
+//         the D head dimensions, one 16-byte shared load, or 8 bytes of FP8
+//         codes).  For every query column of the kv head (its GQA group, times
+//         the new tokens of the step) it forms the score q.k in fp32 (packed
+//         fp32x2 FMAs, a shuffle reduction over the row's lanes), keeps an
+//         online softmax in the log2 domain (running max m, running sum l,
+//         fp32 accumulator rescaled by 2^(m_old - m_new) every tile, as in the
+//         handbook's FlashAttention section), and accumulates p * V;
+//       - tensor cores, a warp pair sharing the columns (split_consumer_mma);
+//       - tensor cores on two fused kv heads, one per warp of a pair.
+//     Each consumer warp then releases the stage on its "empty" mbarrier --
+//     there is no CTA-wide barrier per tile.
 //   * At the last tile of a segment (request, kv head) within the CTA, the
-//     consumer warps merge their per-row-group states through shared memory
-//     and write either the final O and natural-log LSE (the CTA saw the whole
-//     segment) or a normalised partial O and its LSE (lse = m ln2 + ln l).
+//     consumer warps merge their states through shared memory and write
+//     either the final O and natural-log LSE (the CTA saw the whole segment)
+//     or a normalised partial O and its LSE (lse = m ln2 + ln l).
 // Merge kernel ("pass 2", section 2 of the sm120 article): one CTA per
-// (segment, query head) combines that head's partials:
+// (segment, query column) combines that column's partials:
 // LSE = max + ln sum exp(lse_i - max), O = sum O_i exp(lse_i - LSE).
 #pragma once
 
@@ -104,8 +107,8 @@ struct SplitParams {
     unsigned long long timeout_ns;
     unsigned int flags;
     // Tensor-core path only: 1 when the K/V tensor maps are 4-D views
-    // {64 dims, rows, 2 halves, Hkv} so one box carries both swizzled halves
-    // of box_rows rows; 0 for 3-D maps with one box per 64-dim half.
+    // {128-byte part, rows, parts, Hkv} so one box carries every swizzled
+    // part of box_rows rows; 0 for 3-D maps with one box per part.
     int box4d;
     int box_rows_log2;   // log2 of the rows in one box: 6 (64) or log2(page size)
     int page_log2;       // paged, page size under 64: log2 of the page size
@@ -737,18 +740,21 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 
 // ------------------------------------------------------------------ tensor-core consumer
 //
-// GQA groups (G = Hq/Hkv >= 2) make q.K^T a small dense contraction: for a
-// 16-token slice of a tile, S^T[16 x 8] = K[16 x 128] . Q^T[128 x 8] with the
-// group's query heads as the 8 columns (padded with zero heads when G < 8),
-// and O^T[128 x 8] += V^T[128 x 16] . P^T[16 x 8].  Both are warp-level
-// m16n8k16 MMAs on the input type (bf16 or fp16) with fp32 accumulation.
-// The tile arrives with the 128-byte TMA swizzle, so the ldmatrix row reads
-// are free of bank conflicts.  P is rounded to the input type for the second
-// product and the running sum l adds up exactly those rounded weights.
+// GQA groups (and several new tokens) make q.K^T a small dense contraction:
+// for a 16-token slice of a tile, S^T[16 x 8] = K[16 x D] . Q^T[D x 8] with the
+// kv head's query columns as the 8 columns (padded with zero columns), and
+// O^T[D x 8] += V^T[D x 16] . P^T[16 x 8].  Both are warp-level m16n8k16 MMAs
+// (bf16, or fp16 for fp16 and FP8 caches) with fp32 accumulation.  The tile
+// arrives with the 128-byte TMA swizzle, so the ldmatrix row reads are free
+// of bank conflicts.  P is rounded to the MMA type for the second product
+// and the running sum l adds up exactly those rounded weights (a second sum
+// of the exact weights gives the LSE).
 //
-// Warps 2i and 2i+1 take tokens 16i..16i+15 of every tile; both form the
-// scores (so each holds the softmax state), and for P.V warp 2i covers the
-// first half of the head dimension and warp 2i+1 the second.
+// Warps 2i and 2i+1 take tokens 16i..16i+15 of every tile.  Sharing the
+// columns, both form the scores (so each holds the softmax state), and for
+// P.V warp 2i covers the first half of the row's dims and warp 2i+1 the
+// second.  On two paired kv heads, warp 2i + j owns head j outright: its
+// columns, its half of the row for q.K^T and for P.V.
 
 // Byte address of 16-byte chunk `chunk` (0 .. row bytes / 16 - 1) of `row`
 // in a swizzled tile made of boxes of 2^rl rows, each box laid out
