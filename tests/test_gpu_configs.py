@@ -14,19 +14,24 @@ pytestmark = pytest.mark.gpu
 _CACHE = {}
 
 
-def workload(config_id):
-    if config_id not in _CACHE:
+def workload(config_id, kv=None):
+    key = (config_id, kv)
+    if key not in _CACHE:
         _CACHE.clear()
-        _CACHE[config_id] = syn.make_config(config_id)
-    return _CACHE[config_id]
+        _CACHE[key] = syn.make_config(config_id, kv_dtype=kv)
+    return _CACHE[key]
 
 
-# flags 2 = FD_FLAG_CUDA_CORES: the GQA workloads are checked on both consumer paths
-@pytest.mark.parametrize("config_id,flags", [(1, 0), (2, 0), (3, 0), (3, 2), (4, 0), (4, 2), (5, 0), (5, 2)])
-def test_full_size_config_sampled(config_id, flags):
+# flags 2 = FD_FLAG_CUDA_CORES: the GQA workloads are checked on both consumer paths;
+# kv: the benchmark's FP8 variants of the workloads (bench.py --kv)
+@pytest.mark.parametrize("config_id,flags,kv", [(1, 0, None), (2, 0, None), (3, 0, None), (3, 2, None),
+                                                (4, 0, None), (4, 2, None), (5, 0, None), (5, 2, None),
+                                                (2, 0, "e4m3"), (3, 0, "e5m2"), (4, 0, "e4m3"),
+                                                (5, 0, "e4m3"), (5, 2, "e4m3")])
+def test_full_size_config_sampled(config_id, flags, kv):
     from decode_attention_decoding_gb300 import build
     build.build()
-    w = workload(config_id)
+    w = workload(config_id, kv)
     o, l = run(w, flags=flags)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
     items = sample_items(w, 24, seed=config_id)
@@ -34,9 +39,9 @@ def test_full_size_config_sampled(config_id, flags):
         items = None
     ro, rl = oracle.attend(w, items=items, threads=16)
     if items is None:
-        stats = check(o, l, ro, rl, f"config {config_id}")
+        stats = check(o, l, ro, rl, f"config {config_id} kv={kv}")
     else:
         b, h = items[:, 0], items[:, 1]
-        stats = check(o[b, h], l[b, h], ro, rl, f"config {config_id}")
-    print(f"config {config_id} flags={flags}: max|dO|={stats[0]:.3g} max rel(|r|>=1e-2)={stats[1]:.3g} "
+        stats = check(o[b, h], l[b, h], ro, rl, f"config {config_id} kv={kv}")
+    print(f"config {config_id} flags={flags} kv={kv}: max|dO|={stats[0]:.3g} max rel(|r|>=1e-2)={stats[1]:.3g} "
           f"max|dLSE|={stats[2]:.3g}")
