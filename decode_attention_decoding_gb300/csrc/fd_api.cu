@@ -157,11 +157,9 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Query columns of a kv head (group x new tokens) fit one n8 tile; the
-// kernels are built for 1, 2, 4 or 8 columns and pad the rest.
-bool supported_columns(int cols) { return cols >= 1 && cols <= 8; }
-
-int pow2_columns(int cols) { return cols <= 1 ? 1 : cols <= 2 ? 2 : cols <= 4 ? 4 : 8; }
+// Query columns of a kv head (group x new tokens): the kernels are built for
+// 1, 2, 4, 8 or 16 columns and pad the rest.
+int pow2_columns(int cols) { return cols <= 1 ? 1 : cols <= 2 ? 2 : cols <= 4 ? 4 : cols <= 8 ? 8 : 16; }
 
 int q_len_of(const fd_options *opts) { return opts && opts->q_len > 0 ? opts->q_len : 1; }
 
@@ -190,9 +188,34 @@ fd_status check_common(const void *q, const float *o, const void *ws, int batch,
         return FD_ERR_INVALID_ARG;
     if (!options_valid(opts))
         return FD_ERR_INVALID_ARG;
-    if (!supported_head_dim(head_dim) || (long long)(hq / hkv) * q_len_of(opts) > 8 || batch > kMaxBatch)
+    if (!supported_head_dim(head_dim) || (long long)(hq / hkv) * q_len_of(opts) > kMaxColumns ||
+        batch > kMaxBatch)
         return FD_ERR_UNSUPPORTED;
     return FD_OK;
+}
+
+// Bytes of one K/V element under these options.
+int kv_elem_bytes_of(const fd_options *opts)
+{
+    const int kvd = opts ? opts->kv_dtype : FD_KV_AS_Q;
+    return (kvd == FD_KV_FP8_E4M3 || kvd == FD_KV_FP8_E5M2) ? 1 : 2;
+}
+
+// More than 8 query columns per kv head run on the tensor-core consumers only:
+// no FD_FLAG_CUDA_CORES, pages of at least 8 tokens, and a row of at least
+// 128 bytes -- directly, or by pairing two kv heads (an FP8 head of 64 dims).
+// Host-only; FD_OK or FD_ERR_UNSUPPORTED.
+fd_status check_columns(int hq, int hkv, int head_dim, int page_size, const fd_options *opts)
+{
+    if ((long long)(hq / hkv) * q_len_of(opts) <= kMaxColumnsCudaCores)
+        return FD_OK;
+    const unsigned flags = opts ? opts->flags : 0u;
+    if ((flags & FD_FLAG_CUDA_CORES) || (page_size != 0 && page_size < 8))
+        return FD_ERR_UNSUPPORTED;
+    if (head_dim * kv_elem_bytes_of(opts) >= 128)
+        return FD_OK;
+    const bool pairable = 2 * head_dim <= 256 && hkv % 2 == 0 && !(flags & FD_FLAG_NO_HEAD_FUSION);
+    return pairable ? FD_OK : FD_ERR_UNSUPPORTED;
 }
 
 struct CallPlan {
@@ -230,7 +253,7 @@ constexpr double kFuseMinTilesPerCta = 24.0;
 // short rows and at least kFuseMinTilesPerCta (estimated) tiles per CTA
 // unless FD_FLAG_FUSE_HEADS forces it:
 //   * 2 (paired heads: each warp of a pair takes one of the two heads, up to
-//     8 query columns each) when 2 x head_dim <= 256 and Hkv is even --
+//     16 query columns each) when 2 x head_dim <= 256 and Hkv is even --
 //     unless the paired row is still under 256 bytes and 4 heads fit: then
 //   * 4 (one shared 256-dim row; 4 x columns <= 8, 4 | Hkv);
 //   * 1 otherwise.
@@ -242,11 +265,14 @@ int fuse_factor(int cols, int hkv, int head_dim, int elem_bytes, int page_size, 
     if (page_size != 0 && page_size < 8)
         return 1;
     const bool short_rows = head_dim * elem_bytes < 256 || (page_size > 0 && page_size < kTileTokens);
-    const bool forced = opts && (opts->flags & FD_FLAG_FUSE_HEADS);
+    // over 8 columns need the tensor-core consumers, whose rows span at least
+    // 128 bytes: a shorter row (an FP8 head of 64 dims) is paired whenever it can be
+    const bool needed = cols > kMaxColumnsCudaCores && head_dim * elem_bytes < 128;
+    const bool forced = (opts && (opts->flags & FD_FLAG_FUSE_HEADS)) || needed;
     if (!forced && (!short_rows || tiles_per_cta < kFuseMinTilesPerCta))
         return 1;
     const bool four = 4 * head_dim <= 256 && 4 * cols <= 8 && hkv % 4 == 0;
-    const bool two = 2 * head_dim <= 256 && cols <= 8 && hkv % 2 == 0;
+    const bool two = 2 * head_dim <= 256 && cols <= kMaxColumns && hkv % 2 == 0;
     if (two && (2 * head_dim * elem_bytes >= 256 || !four))
         return 2;
     return four ? 4 : 1;
@@ -272,7 +298,7 @@ size_t workspace_bytes_needed(int batch, int hq, int hkv, int head_dim, int q_le
     const int cols = (hq / hkv) * q_len;
     size_t need = workspace_layout(batch, hkv, pow2_columns(cols), head_dim).total;
     auto take = [&](size_t t) { need = t > need ? t : need; };
-    if (2 * head_dim <= 256 && cols <= 8 && hkv % 2 == 0)   // paired heads: both heads' columns
+    if (2 * head_dim <= 256 && hkv % 2 == 0)   // paired heads: both heads' columns
         take(workspace_layout(batch, hkv / 2, 2 * pow2_columns(cols), head_dim).total);
     if (4 * head_dim <= 256 && 4 * cols <= 8 && hkv % 4 == 0)   // four heads in one row
         take(workspace_layout(batch, hkv / 4, pow2_columns(4 * cols), 4 * head_dim).total);
@@ -349,7 +375,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     const int eb = kv_elem_bytes(kv);
     // Launch shape: F fused kv heads of head_dim dims become one head of
     // F * head_dim dims.  A kv head's query columns (q_len x group) are padded
-    // to 1, 2, 4 or 8.  Paired heads (F = 2) keep each head's columns in its
+    // to 1, 2, 4, 8 or 16.  Paired heads (F = 2) keep each head's columns in its
     // own warp of a pair (2 x padded columns in all, head_dim dims each); four
     // fused heads share one set of 4 x columns over 4 x head_dim dims.
     const int real_group = hq / hkv;
@@ -403,7 +429,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     // column slot n = (part, new token i, query head g), part-major; each part
     // holds `cols` real columns, in a block of `group` slots when paired
     const int per_part = paired ? group : cols;
-    for (int n = 0; n < 16; ++n) {
+    for (int n = 0; n < kMaxColumnSlots; ++n) {
         const int part = n / per_part, c = n % per_part;
         const bool real = n < slots && part < fuse && c < cols;
         sp.col_code[n] = real ? (c / real_group) | (part << 4) | ((c % real_group) << 8) : -1;
@@ -418,6 +444,8 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     cp->cons = paired ? kConsMmaPair : (cp->mma ? kConsMma : kConsCudaCores);
     if (fuse > 1 && !use_mma(2, page_size, eb * d, opts))
         return FD_ERR_UNSUPPORTED;   // fusion is defined for the tensor-core consumers only
+    if (!cp->mma && group > kMaxColumnsCudaCores)
+        return FD_ERR_UNSUPPORTED;   // over 8 columns need the tensor-core consumers
     cp->launch.grid = num_ctas;
     cp->launch.stream = reinterpret_cast<cudaStream_t>(stream);
     fd_status st = plan_smem(dev, cp->cons, group, d, eb, batch, (double)est_tiles / num_ctas, &sp,
@@ -480,7 +508,8 @@ size_t fd_workspace_size_q(int batch, int num_q_heads, int num_kv_heads, int hea
                            int page_size, int q_len)
 {
     if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kv_len < 0 ||
-        page_size < 0 || num_q_heads % num_kv_heads != 0 || q_len < 1)
+        page_size < 0 || num_q_heads % num_kv_heads != 0 || q_len < 1 ||
+        (long long)(num_q_heads / num_kv_heads) * q_len > kMaxColumns)
         return 0;
     return workspace_bytes_needed(batch, num_q_heads, num_kv_heads, head_dim, q_len);
 }
@@ -511,6 +540,8 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
                 return FD_ERR_INVALID_ARG;
     if (!options_valid(opts))
         return FD_ERR_INVALID_ARG;
+    if ((st = check_columns(num_q_heads, num_kv_heads, head_dim, 0, opts)) != FD_OK)
+        return st;
     if ((long long)batch * s_max >= (1ll << 31) ||
         (long long)num_kv_heads * batch * ceil_div(s_max, kTileTokens) >= (1ll << 31))
         return FD_ERR_UNSUPPORTED;
@@ -559,12 +590,10 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     // and tensor copies need 128-byte aligned destinations: pages under 64
     // tokens must hold at least 128 bytes per kv head (only an FP8 cache with
     // head_dim 64 and one-token pages falls short).
-    {
-        const int kvd = opts ? opts->kv_dtype : FD_KV_AS_Q;
-        const int eb = (kvd == FD_KV_FP8_E4M3 || kvd == FD_KV_FP8_E5M2) ? 1 : 2;
-        if (page_size < kTileTokens && page_size * head_dim * eb < 128)
-            return FD_ERR_UNSUPPORTED;
-    }
+    if (page_size < kTileTokens && page_size * head_dim * kv_elem_bytes_of(opts) < 128)
+        return FD_ERR_UNSUPPORTED;
+    if ((st = check_columns(num_q_heads, num_kv_heads, head_dim, page_size, opts)) != FD_OK)
+        return st;
     const long long cap = (long long)max_blocks_per_seq * page_size;
     if (cap >= (1ll << 31) || (long long)num_pages * page_size >= (1ll << 31) ||
         (long long)num_kv_heads * batch * ((cap + kTileTokens - 1) / kTileTokens) >= (1ll << 31))

@@ -87,6 +87,13 @@ __host__ __device__ constexpr int reduction_floats(int cons, int group, int d)
 // Per-tile metadata flags, written by the producer into shared memory.
 enum : int { kFirstInCta = 1, kLastInCta = 2, kOwnSegment = 4 };
 
+// Query columns of one kv head (group x new tokens): up to two n8 tiles on
+// the tensor-core consumers, one on CUDA cores; a launch head of two paired
+// kv heads has twice as many column slots.
+constexpr int kMaxColumns = 16;
+constexpr int kMaxColumnsCudaCores = 8;
+constexpr int kMaxColumnSlots = 2 * kMaxColumns;
+
 struct SplitParams {
     const uint16_t *q;            // [B, Hq, D] bf16 or fp16 bits
     const int32_t *seq_lens;      // [B] device, or null (every length = cap)
@@ -120,7 +127,7 @@ struct SplitParams {
     // (zero query, never written).  n_cols: the column slots of a head.
     int q_len, g_real, n_cols, fuse_f;
     int fuse_dh;       // dh when a fused row's parts share each column's dims, else 0
-    int col_code[16];  // new token i | part << 4 | head g << 8, or -1 (host-computed)
+    int col_code[kMaxColumnSlots];   // new token i | part << 4 | head g << 8, or -1 (host-computed)
     int q_f16;        // FP8 caches: 1 when q is fp16, 0 when bf16
     float v_scale;    // multiplies O (an FP8 cache's V dequantisation scale; 1 otherwise)
 };
@@ -133,7 +140,7 @@ struct MergeParams {
     const int32_t *ws_prefix;
     int batch, hq, hkv, num_ctas;
     int q_len, g_real, n_cols, fuse_f, fuse_dh;   // as in SplitParams
-    int col_code[16];
+    int col_code[kMaxColumnSlots];
     const int32_t *seq_lens;   // as in SplitParams (small batches: segment geometry)
     int cap;
 };
@@ -790,14 +797,22 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                                                    uint32_t cbar, volatile int *abort_flag, int t_begin,
                                                    int t_end, int cw, int lane)
 {
-    static_assert(G >= 1 && G <= 8, "one n8 tile of query heads");
+    static_assert(G >= 1 && G <= 16, "one or two n8 tiles of query columns");
     using HD = Shape<D, KV>;
-    // PAIR: the row holds two kv heads of D/2 dims; warp dhalf of a pair owns
-    // head dhalf entirely (its G columns, its D/2 dims for q.K^T and for P.V).
-    // Otherwise both warps of a pair share the G columns and split the dims.
+    // How the two warps of a pair (the same 16 tokens) share the work:
+    //   PAIR:   the row holds two kv heads of D/2 dims; warp dhalf owns head
+    //           dhalf entirely (its G columns, its D/2 dims for q.K^T and P.V);
+    //   CSPLIT: over 8 columns of one head; warp dhalf owns columns
+    //           8 dhalf .. 8 dhalf + 7 over all D dims (each warp one n8 tile);
+    //   else:   both warps take all G columns and split the D dims of P.V.
+    // A paired head of over 8 columns takes two n8 tiles in its warp: each K
+    // and V fragment feeds both.
+    constexpr bool CSPLIT = !PAIR && G > 8;
+    constexpr int GW = CSPLIT ? G / 2 : G;       // columns of this warp
+    constexpr int NT = GW > 8 ? 2 : 1;           // n8 tiles of columns per warp
     constexpr int DW = PAIR ? D / 2 : D;         // dims of one column's q row
     constexpr int KS = DW / 16;                  // k-steps of q.K^T
-    constexpr int DT = HD::kDimTilesPerWarp;     // 16-dim tiles of P.V per warp
+    constexpr int DT = CSPLIT ? D / 16 : HD::kDimTilesPerWarp;   // 16-dim tiles of P.V per warp
     constexpr int GT = PAIR ? 2 * G : G;         // columns of the launch head
     constexpr int DR = PAIR ? D / 2 : D;         // dims kept per column in the reduction
     constexpr bool FP8 = kv_is_fp8(KV);
@@ -812,27 +827,33 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
     float *red_m = red_acc + kPairs * GT * DR;                       // [pairs][GT]
     float *red_l = red_m + kPairs * GT;                              // [2 pairs][GT]: l, then lt
     const int ctid = cw * 32 + lane;
-    const int cbase = PAIR ? dhalf * G : 0;                          // this warp's first column
+    const int cbase = PAIR ? dhalf * G : (CSPLIT ? dhalf * GW : 0);  // this warp's first column
+    const int dtb = CSPLIT ? 0 : dhalf * DT;                         // its first 16-dim tile of P.V
     const int koff = PAIR ? dhalf * (HD::kRowBytes / 32) : 0;        // its first 16-byte chunk of K
 
-    uint32_t qb[KS][2];        // Q^T B-fragments, one pair per 16-dim k-step
-    float smul[2];             // score multipliers of heads 2 qd, 2 qd + 1 (log2 units)
-    float acc[DT][4];          // O^T fragments of this warp's D/32 dim tiles
-    // heads 2 qd and 2 qd + 1, this lane's tokens only: l sums the 16-bit
-    // rounded weights that multiply V, lt the exact fp32 weights (for the LSE)
-    float m[2], l[2], lt[2];
+    uint32_t qb[NT][KS][2];    // Q^T B-fragments, one pair per 16-dim k-step
+    float smul[NT][2];         // score multipliers of columns 2 qd, 2 qd + 1 (log2 units)
+    float acc[NT][DT][4];      // O^T fragments of this warp's D/32 dim tiles
+    // columns 2 qd and 2 qd + 1 of each tile, this lane's tokens only: l sums
+    // the 16-bit rounded weights that multiply V, lt the exact fp32 weights
+    // (for the LSE)
+    float m[NT][2], l[NT][2], lt[NT][2];
+    int lag[NT][2];            // causal lag of those columns
     auto reset = [&]() {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            m[j] = kNegInf;
-            l[j] = 0.f;
-            lt[j] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                m[nt][j] = kNegInf;
+                l[nt][j] = 0.f;
+                lt[nt][j] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < DT; ++i)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    acc[nt][i][c] = 0.f;
         }
-#pragma unroll
-        for (int i = 0; i < DT; ++i)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                acc[i][c] = 0.f;
     };
     auto give_up = [&]() {
         if (lane == 0) {
@@ -842,12 +863,14 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
     };
     reset();
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
-        qb[ks][0] = qb[ks][1] = 0u;
-    smul[0] = smul[1] = p.scale_log2;
-    // causal lag of this lane's score columns 2 qd and 2 qd + 1
-    const int lag0 = p.q_len - 1 - col_info(p, 0, 0, cbase + 2 * qd).i;
-    const int lag1 = p.q_len - 1 - col_info(p, 0, 0, cbase + 2 * qd + 1).i;
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+            qb[nt][ks][0] = qb[nt][ks][1] = 0u;
+        smul[nt][0] = smul[nt][1] = p.scale_log2;
+        lag[nt][0] = p.q_len - 1 - col_info(p, 0, 0, cbase + nt * 8 + 2 * qd).i;
+        lag[nt][1] = p.q_len - 1 - col_info(p, 0, 0, cbase + nt * 8 + 2 * qd + 1).i;
+    }
 
     int s = 0;
     uint32_t ph = 0, cph = 0;
@@ -860,63 +883,67 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         const int b = mt[0], h = mt[1], rem = mt[2], nvalid = mt[3], flags = mt[4], u = mt[5];
 
         if (flags & kFirstInCta) {
-            // A fused head's query reads its own fuse_dh dims; zeros elsewhere.
-            // Padding columns keep a zero query.
-            const int qdim = PAIR ? DW : (p.fuse_dh ? p.fuse_dh : D);
-            const ColInfo col = col_info(p, b, h, cbase + grp);
-            const int part = col.dim0;
-            const bool colv = col.valid && grp < G;
-            const uint16_t *qrow = p.q + col.row * qdim;
-            if constexpr (!FP8) {
-                // B[k = d][n = head]: lane holds head `grp`, dims 16 ks + 2 qd (+1) and (+8, +9).
-                const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int d0 = ks * 16 - part;   // first dim of this k-step in the q row
-                    const bool in = colv && d0 >= 0 && d0 < qdim;
-                    qb[ks][0] = in ? __ldg(q32 + d0 / 2 + qd) : 0u;
-                    qb[ks][1] = in ? __ldg(q32 + d0 / 2 + 4 + qd) : 0u;
-                }
-            } else {
-                // lane holds head `grp`, dims 16 ks + 4 qd .. + 3 (see above)
-                const bool qf16 = p.q_f16 != 0;
-                float qv[KS][4];
-                float amax = 0.f;
+            for (int nt = 0; nt < NT; ++nt) {
+                // A fused head's query reads its own fuse_dh dims; zeros elsewhere.
+                // Padding columns keep a zero query.
+                const int qdim = PAIR ? DW : (p.fuse_dh ? p.fuse_dh : D);
+                const int lc = nt * 8 + grp;   // this lane's column within the warp's columns
+                const ColInfo col = col_info(p, b, h, cbase + (lc < GW ? lc : 0));
+                const int part = col.dim0;
+                const bool colv = col.valid && lc < GW;
+                const uint16_t *qrow = p.q + col.row * qdim;
+                if constexpr (!FP8) {
+                    // B[k = d][n = column]: lane holds column grp, dims 16 ks + 2 qd (+1) and (+8, +9).
+                    const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int d0 = ks * 16 - part;
-                    const bool in = colv && d0 >= 0 && d0 < qdim;
-                    uint2 w = make_uint2(0u, 0u);
-                    if (in)
-                        w = __ldg(reinterpret_cast<const uint2 *>(qrow + d0 + 4 * qd));
-                    const float2 lo = qf16 ? f16x2_to_float2(w.x) : bf16x2_to_float2(w.x);
-                    const float2 hi = qf16 ? f16x2_to_float2(w.y) : bf16x2_to_float2(w.y);
-                    qv[ks][0] = lo.x;
-                    qv[ks][1] = lo.y;
-                    qv[ks][2] = hi.x;
-                    qv[ks][3] = hi.y;
-                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(hi.x), fabsf(hi.y))));
-                }
-                // the head's max over its four lanes (same grp)
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                // power of two sh with amax * 2^-sh in [2^14, 2^15); zero heads keep sh = 0
-                int sh = 0;
-                if (amax > 0.f) {
-                    const int e = ((__float_as_int(amax) >> 23) & 255) - 127;   // floor(log2 amax), normals
-                    sh = min(max(e - 14, -120), 126);
-                }
-                const float down = __int_as_float((127 - sh) << 23);   // 2^-sh
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int d0 = ks * 16 - part;   // first dim of this k-step in the q row
+                        const bool in = colv && d0 >= 0 && d0 < qdim;
+                        qb[nt][ks][0] = in ? __ldg(q32 + d0 / 2 + qd) : 0u;
+                        qb[nt][ks][1] = in ? __ldg(q32 + d0 / 2 + 4 + qd) : 0u;
+                    }
+                } else {
+                    // lane holds column grp, dims 16 ks + 4 qd .. + 3 (see above)
+                    const bool qf16 = p.q_f16 != 0;
+                    float qv[KS][4];
+                    float amax = 0.f;
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    qb[ks][0] = pack_f16x2(qv[ks][0] * down, qv[ks][1] * down);
-                    qb[ks][1] = pack_f16x2(qv[ks][2] * down, qv[ks][3] * down);
-                }
-                // this lane's score columns are heads 2 qd and 2 qd + 1 (held by lanes 4 head)
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int d0 = ks * 16 - part;
+                        const bool in = colv && d0 >= 0 && d0 < qdim;
+                        uint2 w = make_uint2(0u, 0u);
+                        if (in)
+                            w = __ldg(reinterpret_cast<const uint2 *>(qrow + d0 + 4 * qd));
+                        const float2 lo = qf16 ? f16x2_to_float2(w.x) : bf16x2_to_float2(w.x);
+                        const float2 hi = qf16 ? f16x2_to_float2(w.y) : bf16x2_to_float2(w.y);
+                        qv[ks][0] = lo.x;
+                        qv[ks][1] = lo.y;
+                        qv[ks][2] = hi.x;
+                        qv[ks][3] = hi.y;
+                        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(hi.x), fabsf(hi.y))));
+                    }
+                    // the column's max over its four lanes (same grp)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                    // power of two sh with amax * 2^-sh in [2^14, 2^15); zero columns keep sh = 0
+                    int sh = 0;
+                    if (amax > 0.f) {
+                        const int e = ((__float_as_int(amax) >> 23) & 255) - 127;   // floor(log2 amax), normals
+                        sh = min(max(e - 14, -120), 126);
+                    }
+                    const float down = __int_as_float((127 - sh) << 23);   // 2^-sh
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int shj = __shfl_sync(0xffffffffu, sh, (2 * qd + j) * 4);
-                    smul[j] = p.scale_log2 * __int_as_float((127 + shj) << 23);
+                    for (int ks = 0; ks < KS; ++ks) {
+                        qb[nt][ks][0] = pack_f16x2(qv[ks][0] * down, qv[ks][1] * down);
+                        qb[nt][ks][1] = pack_f16x2(qv[ks][2] * down, qv[ks][3] * down);
+                    }
+                    // this lane's score columns are 2 qd and 2 qd + 1 (held by lanes 4 column)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int shj = __shfl_sync(0xffffffffu, sh, (2 * qd + j) * 4);
+                        smul[nt][j] = p.scale_log2 * __int_as_float((127 + shj) << 23);
+                    }
                 }
             }
         }
@@ -927,9 +954,13 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         // S^T = K . Q^T for tokens tok0 .. tok0 + 15 (fragment rows grp and grp + 8).
         // Even and odd k-steps accumulate separately: two dependent MMA chains
         // of KS/2 instead of one of KS (the chain's latency bounds the tile).
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        float sc[NT][4], sc2[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                sc[nt][i] = sc2[nt][i] = 0.f;
         {
-            float sc2[4] = {0.f, 0.f, 0.f, 0.f};
             const int row = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);
             if constexpr (!FP8) {
 #pragma unroll
@@ -937,7 +968,10 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                     uint32_t a0, a1, a2, a3;
                     ldmatrix_x4(sw128_addr<HD::kParts>(ktile, row, koff + 2 * ks + (lane >> 4), rl), a0, a1, a2,
                                 a3);
-                    mma_16816<MMA_F16>((ks & 1) ? sc2 : sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_16816<MMA_F16>((ks & 1) ? sc2[nt] : sc[nt], a0, a1, a2, a3, qb[nt][ks][0],
+                                           qb[nt][ks][1]);
                 }
             } else {
                 // one ldmatrix covers two 16-dim chunks: k-steps 2 kk and 2 kk + 1
@@ -946,110 +980,132 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                     uint32_t r0, r1, r2, r3;
                     ldmatrix_x4(sw128_addr<HD::kParts>(ktile, row, koff + 2 * kk + (lane >> 4), rl), r0, r1, r2,
                                 r3);
-                    mma_16816<true>(sc, fp8x2_to_f16x2<KV>(lo16(r0)), fp8x2_to_f16x2<KV>(lo16(r1)),
-                                    fp8x2_to_f16x2<KV>(hi16(r0)), fp8x2_to_f16x2<KV>(hi16(r1)), qb[2 * kk][0],
-                                    qb[2 * kk][1]);
-                    mma_16816<true>(sc2, fp8x2_to_f16x2<KV>(lo16(r2)), fp8x2_to_f16x2<KV>(lo16(r3)),
-                                    fp8x2_to_f16x2<KV>(hi16(r2)), fp8x2_to_f16x2<KV>(hi16(r3)),
-                                    qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
+                    const uint32_t e0 = fp8x2_to_f16x2<KV>(lo16(r0)), e1 = fp8x2_to_f16x2<KV>(lo16(r1));
+                    const uint32_t e2 = fp8x2_to_f16x2<KV>(hi16(r0)), e3 = fp8x2_to_f16x2<KV>(hi16(r1));
+                    const uint32_t o0 = fp8x2_to_f16x2<KV>(lo16(r2)), o1 = fp8x2_to_f16x2<KV>(lo16(r3));
+                    const uint32_t o2 = fp8x2_to_f16x2<KV>(hi16(r2)), o3 = fp8x2_to_f16x2<KV>(hi16(r3));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_16816<true>(sc[nt], e0, e1, e2, e3, qb[nt][2 * kk][0], qb[nt][2 * kk][1]);
+                        mma_16816<true>(sc2[nt], o0, o1, o2, o3, qb[nt][2 * kk + 1][0], qb[nt][2 * kk + 1][1]);
+                    }
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                sc[i] += sc2[i];
-        }
-        // sc[0]: (token grp, head 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1);
-        // a token counts for a column if it is inside the column's causal end
-        // (the request's end when there is one new token)
-        float x[4];
-        if (p.q_len == 1) {
-            const bool v0 = tok0 + grp < nvalid, v1 = tok0 + grp + 8 < nvalid;
-            x[0] = v0 ? sc[0] * smul[0] : kNegInf;
-            x[1] = v0 ? sc[1] * smul[1] : kNegInf;
-            x[2] = v1 ? sc[2] * smul[0] : kNegInf;
-            x[3] = v1 ? sc[3] * smul[1] : kNegInf;
-        } else {
-            const int lim0 = min(nvalid, rem - lag0), lim1 = min(nvalid, rem - lag1);
-            x[0] = tok0 + grp < lim0 ? sc[0] * smul[0] : kNegInf;
-            x[1] = tok0 + grp < lim1 ? sc[1] * smul[1] : kNegInf;
-            x[2] = tok0 + grp + 8 < lim0 ? sc[2] * smul[0] : kNegInf;
-            x[3] = tok0 + grp + 8 < lim1 ? sc[3] * smul[1] : kNegInf;
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    sc[nt][i] += sc2[nt][i];
         }
 
-        // Online softmax over this warp's 16 tokens, per head.
-        float alpha[2], pw[4];
+        // Per n8 tile: mask, online softmax over this warp's 16 tokens, P.
+        float alpha[NT][2];
+        uint32_t pb0[NT], pb1[NT];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float mx = fmaxf(x[j], x[j + 2]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m[j], mx);
-            alpha[j] = (m[j] == kNegInf) ? 0.f : exp2_approx(m[j] - m_new);
-            pw[j] = (x[j] == kNegInf) ? 0.f : exp2_approx(x[j] - m_new);
-            pw[j + 2] = (x[j + 2] == kNegInf) ? 0.f : exp2_approx(x[j + 2] - m_new);
-            m[j] = m_new;
+        for (int nt = 0; nt < NT; ++nt) {
+            // sc[0]: (token grp, column 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1);
+            // a token counts for a column if it is inside the column's causal end
+            // (the request's end when there is one new token)
+            float x[4];
+            if (p.q_len == 1) {
+                const bool v0 = tok0 + grp < nvalid, v1 = tok0 + grp + 8 < nvalid;
+                x[0] = v0 ? sc[nt][0] * smul[nt][0] : kNegInf;
+                x[1] = v0 ? sc[nt][1] * smul[nt][1] : kNegInf;
+                x[2] = v1 ? sc[nt][2] * smul[nt][0] : kNegInf;
+                x[3] = v1 ? sc[nt][3] * smul[nt][1] : kNegInf;
+            } else {
+                const int lim0 = min(nvalid, rem - lag[nt][0]), lim1 = min(nvalid, rem - lag[nt][1]);
+                x[0] = tok0 + grp < lim0 ? sc[nt][0] * smul[nt][0] : kNegInf;
+                x[1] = tok0 + grp < lim1 ? sc[nt][1] * smul[nt][1] : kNegInf;
+                x[2] = tok0 + grp + 8 < lim0 ? sc[nt][2] * smul[nt][0] : kNegInf;
+                x[3] = tok0 + grp + 8 < lim1 ? sc[nt][3] * smul[nt][1] : kNegInf;
+            }
+            float pw[4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float mx = fmaxf(x[j], x[j + 2]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m[nt][j], mx);
+                alpha[nt][j] = (m[nt][j] == kNegInf) ? 0.f : exp2_approx(m[nt][j] - m_new);
+                pw[j] = (x[j] == kNegInf) ? 0.f : exp2_approx(x[j] - m_new);
+                pw[j + 2] = (x[j + 2] == kNegInf) ? 0.f : exp2_approx(x[j + 2] - m_new);
+                m[nt][j] = m_new;
+            }
+            const uint32_t p_lo = pack_x2<MMA_F16>(pw[0], pw[1]);   // token grp, columns 2qd, 2qd+1
+            const uint32_t p_hi = pack_x2<MMA_F16>(pw[2], pw[3]);   // token grp + 8
+            {
+                const float2 r_lo = x2_to_float2<MMA_F16>(p_lo), r_hi = x2_to_float2<MMA_F16>(p_hi);
+                l[nt][0] = l[nt][0] * alpha[nt][0] + (r_lo.x + r_hi.x);
+                l[nt][1] = l[nt][1] * alpha[nt][1] + (r_lo.y + r_hi.y);
+                lt[nt][0] = lt[nt][0] * alpha[nt][0] + (pw[0] + pw[2]);
+                lt[nt][1] = lt[nt][1] * alpha[nt][1] + (pw[1] + pw[3]);
+            }
+            // P^T as the B operand (k = token, n = column): transpose the 8x8 blocks.
+            pb0[nt] = movmatrix_trans(p_lo);
+            pb1[nt] = movmatrix_trans(p_hi);
         }
-        const uint32_t p_lo = pack_x2<MMA_F16>(pw[0], pw[1]);   // token grp, heads 2qd, 2qd+1
-        const uint32_t p_hi = pack_x2<MMA_F16>(pw[2], pw[3]);   // token grp + 8
-        {
-            const float2 r_lo = x2_to_float2<MMA_F16>(p_lo), r_hi = x2_to_float2<MMA_F16>(p_hi);
-            l[0] = l[0] * alpha[0] + (r_lo.x + r_hi.x);
-            l[1] = l[1] * alpha[1] + (r_lo.y + r_hi.y);
-            lt[0] = lt[0] * alpha[0] + (pw[0] + pw[2]);
-            lt[1] = lt[1] * alpha[1] + (pw[1] + pw[3]);
-        }
-        // P^T as the B operand (k = token, n = head): transpose the 8x8 blocks.
-        const uint32_t pb0 = movmatrix_trans(p_lo);
-        const uint32_t pb1 = movmatrix_trans(p_hi);
 
         // Rows past the request's end may hold anything (even NaN), and the
-        // tensor core would form 0 * NaN: zero this warp's half of them.
+        // tensor core would form 0 * NaN: zero the part of them this warp
+        // reads (its half of the dims; every dim under CSPLIT, where both
+        // warps of the pair store the same zeros).
         const bool ragged = nvalid < tok0 + 16;
         if (ragged) {
-            constexpr int kChunks = HD::kRowBytes / 32;   // 16-byte chunks in half a row
+            constexpr int kChunks = HD::kRowBytes / (CSPLIT ? 16 : 32);   // 16-byte chunks this warp reads
+            const int c0 = CSPLIT ? 0 : dhalf * kChunks;
             const int first = nvalid > tok0 ? nvalid : tok0;
             for (int idx = lane; idx < (tok0 + 16 - first) * kChunks; idx += 32) {
                 const uint32_t a = sw128_addr<HD::kParts>(vtile, first + idx / kChunks,
-                                                          dhalf * kChunks + idx % kChunks, rl);
+                                                          c0 + idx % kChunks, rl);
                 asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
             }
             __syncwarp();
         }
 
-        // O^T = alpha O^T + V^T . P^T over this warp's D/2 dims.
+        // O^T = alpha O^T + V^T . P^T over this warp's dims (tiles dtb .. dtb + DT - 1).
 #pragma unroll
-        for (int i = 0; i < DT; ++i) {
-            acc[i][0] *= alpha[0];
-            acc[i][1] *= alpha[1];
-            acc[i][2] *= alpha[0];
-            acc[i][3] *= alpha[1];
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < DT; ++i) {
+                acc[nt][i][0] *= alpha[nt][0];
+                acc[nt][i][1] *= alpha[nt][1];
+                acc[nt][i][2] *= alpha[nt][0];
+                acc[nt][i][3] *= alpha[nt][1];
+            }
         if constexpr (!FP8) {
             const int vrow = tok0 + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
             for (int i = 0; i < DT; ++i) {
-                const int dt = dhalf * DT + i;   // 16-dim tile index
+                const int dt = dtb + i;   // 16-dim tile index
                 uint32_t a0, a1, a2, a3;
                 ldmatrix_x4_trans(sw128_addr<HD::kParts>(vtile, vrow, 2 * dt + ((lane >> 3) & 1), rl), a0, a1,
                                   a2, a3);
-                mma_16816<MMA_F16>(acc[i], a0, a1, a2, a3, pb0, pb1);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_16816<MMA_F16>(acc[nt][i], a0, a1, a2, a3, pb0[nt], pb1[nt]);
             }
         } else {
             // matrices (tokens 0-7 | 8-15) x (chunk c | c + 1): two 16-dim tiles per ldmatrix
             const int vrow = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
             for (int ii = 0; ii < DT / 2; ++ii) {
-                const int c = dhalf * DT + 2 * ii;   // chunk = 16-dim tile index
+                const int c = dtb + 2 * ii;   // chunk = 16-dim tile index
                 uint32_t r0, r1, r2, r3;
                 ldmatrix_x4_trans(sw128_addr<HD::kParts>(vtile, vrow, c + (lane >> 4), rl), r0, r1, r2, r3);
                 // bytes (t, 2grp), (t, 2grp+1), (t+1, 2grp), (t+1, 2grp+1) -> dim pairs over tokens
                 const uint32_t s0 = prmt(r0, 0u, 0x3120u), s1 = prmt(r1, 0u, 0x3120u);
                 const uint32_t s2 = prmt(r2, 0u, 0x3120u), s3 = prmt(r3, 0u, 0x3120u);
-                mma_16816<true>(acc[2 * ii], fp8x2_to_f16x2<KV>(lo16(s0)), fp8x2_to_f16x2<KV>(hi16(s0)),
-                                fp8x2_to_f16x2<KV>(lo16(s1)), fp8x2_to_f16x2<KV>(hi16(s1)), pb0, pb1);
-                mma_16816<true>(acc[2 * ii + 1], fp8x2_to_f16x2<KV>(lo16(s2)), fp8x2_to_f16x2<KV>(hi16(s2)),
-                                fp8x2_to_f16x2<KV>(lo16(s3)), fp8x2_to_f16x2<KV>(hi16(s3)), pb0, pb1);
+                const uint32_t a0 = fp8x2_to_f16x2<KV>(lo16(s0)), a1 = fp8x2_to_f16x2<KV>(hi16(s0));
+                const uint32_t a2 = fp8x2_to_f16x2<KV>(lo16(s1)), a3 = fp8x2_to_f16x2<KV>(hi16(s1));
+                const uint32_t b0 = fp8x2_to_f16x2<KV>(lo16(s2)), b1 = fp8x2_to_f16x2<KV>(hi16(s2));
+                const uint32_t b2 = fp8x2_to_f16x2<KV>(lo16(s3)), b3 = fp8x2_to_f16x2<KV>(hi16(s3));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_16816<true>(acc[nt][2 * ii], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+                    mma_16816<true>(acc[nt][2 * ii + 1], b0, b1, b2, b3, pb0[nt], pb1[nt]);
+                }
             }
         }
         if (ragged)   // order the zeroing stores before the next TMA write to this stage
@@ -1059,34 +1115,37 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             mbar_arrive(empty0 + 8 * s);
 
         if (flags & kLastInCta) {
-            // l over the warp's 16 tokens (lanes sharing qd hold the same heads)
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
-                l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
-                l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
-                lt[j] += __shfl_xor_sync(0xffffffffu, lt[j], 4);
-                lt[j] += __shfl_xor_sync(0xffffffffu, lt[j], 8);
-                lt[j] += __shfl_xor_sync(0xffffffffu, lt[j], 16);
-            }
+            for (int nt = 0; nt < NT; ++nt) {
+                // l over the warp's 16 tokens (lanes sharing qd hold the same columns)
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int head = 2 * qd + j;              // this warp's column
-                const int gcol = cbase + head;            // the launch head's column
-                if (head < G && p.col_code[gcol] >= 0) {
-                    if ((PAIR || dhalf == 0) && grp == 0) {
-                        red_m[pair * GT + gcol] = m[j];
-                        red_l[pair * GT + gcol] = l[j];
-                        red_l[(kPairs + pair) * GT + gcol] = lt[j];   // exact sums after the pairs' slots
-                    }
+                for (int j = 0; j < 2; ++j) {
+                    l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 4);
+                    l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 8);
+                    l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 16);
+                    lt[nt][j] += __shfl_xor_sync(0xffffffffu, lt[nt][j], 4);
+                    lt[nt][j] += __shfl_xor_sync(0xffffffffu, lt[nt][j], 8);
+                    lt[nt][j] += __shfl_xor_sync(0xffffffffu, lt[nt][j], 16);
+                }
 #pragma unroll
-                    for (int i = 0; i < DT; ++i) {
-                        // output rows grp and grp + 8 of the tile: dims grp and grp + 8, or for
-                        // FP8 caches 2 grp and 2 grp + 1 (see above); paired heads keep their own dims
-                        const int d0 = (dhalf * DT + i) * 16 - (PAIR ? dhalf * DR : 0);
-                        const int dlo = d0 + (FP8 ? 2 * grp : grp), dhi = d0 + (FP8 ? 2 * grp + 1 : grp + 8);
-                        red_acc[(pair * GT + gcol) * DR + dlo] = acc[i][j];
-                        red_acc[(pair * GT + gcol) * DR + dhi] = acc[i][j + 2];
+                for (int j = 0; j < 2; ++j) {
+                    const int head = nt * 8 + 2 * qd + j;     // this warp's column
+                    const int gcol = cbase + head;            // the launch head's column
+                    if (head < GW && p.col_code[gcol] >= 0) {
+                        if ((PAIR || CSPLIT || dhalf == 0) && grp == 0) {
+                            red_m[pair * GT + gcol] = m[nt][j];
+                            red_l[pair * GT + gcol] = l[nt][j];
+                            red_l[(kPairs + pair) * GT + gcol] = lt[nt][j];   // exact sums after the pairs' slots
+                        }
+#pragma unroll
+                        for (int i = 0; i < DT; ++i) {
+                            // output rows grp and grp + 8 of the tile: dims grp and grp + 8, or for
+                            // FP8 caches 2 grp and 2 grp + 1 (see above); paired heads keep their own dims
+                            const int d0 = (dtb + i) * 16 - (PAIR ? dhalf * DR : 0);
+                            const int dlo = d0 + (FP8 ? 2 * grp : grp), dhi = d0 + (FP8 ? 2 * grp + 1 : grp + 8);
+                            red_acc[(pair * GT + gcol) * DR + dlo] = acc[nt][i][j];
+                            red_acc[(pair * GT + gcol) * DR + dhi] = acc[nt][i][j + 2];
+                        }
                     }
                 }
             }

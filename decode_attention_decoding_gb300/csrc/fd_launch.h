@@ -58,9 +58,9 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
 }
 
 // One split-kernel variant per (layout, K/V element type, row dims D):
-// consumers on CUDA cores (any group), on tensor cores (group 2, 4 or 8,
+// consumers on CUDA cores (group 1 to 8), on tensor cores (group 2 to 16,
 // swizzled K/V maps, rows of at least 128 bytes), or on tensor cores with two
-// fused kv heads per row (group = columns per head, 1 to 8; D = 2 x head_dim).
+// fused kv heads per row (group = columns per head, 1 to 16; D = 2 x head_dim).
 // Returns cudaErrorInvalidValue for an unsupported combination.
 template <bool PAGED, int KV, int D>
 cudaError_t launch_split_variant(int cons, int group, const SplitParams &p, const CUtensorMap &tmk,
@@ -72,6 +72,7 @@ cudaError_t launch_split_variant(int cons, int group, const SplitParams &p, cons
             case 2: return launch_split_t<2, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
             case 4: return launch_split_t<4, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
             case 8: return launch_split_t<8, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
+            case 16: return launch_split_t<16, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
             default: return cudaErrorInvalidValue;
             }
         }
@@ -84,6 +85,7 @@ cudaError_t launch_split_variant(int cons, int group, const SplitParams &p, cons
             case 2: return launch_split_t<2, PAGED, kConsMmaPair, KV, D>(p, tmk, tmv, c);
             case 4: return launch_split_t<4, PAGED, kConsMmaPair, KV, D>(p, tmk, tmv, c);
             case 8: return launch_split_t<8, PAGED, kConsMmaPair, KV, D>(p, tmk, tmv, c);
+            case 16: return launch_split_t<16, PAGED, kConsMmaPair, KV, D>(p, tmk, tmv, c);
             default: return cudaErrorInvalidValue;
             }
         }

@@ -30,6 +30,7 @@ static cudaError_t launch_merge_d(int group, const MergeParams &p, int grid, cud
     case 4: return launch_merge_t<4, D>(p, grid, stream);
     case 8: return launch_merge_t<8, D>(p, grid, stream);
     case 16: return launch_merge_t<16, D>(p, grid, stream);
+    case 32: return launch_merge_t<32, D>(p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

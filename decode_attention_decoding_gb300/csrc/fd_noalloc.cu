@@ -173,7 +173,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     sp.g_real = group;
     sp.n_cols = group;
     sp.fuse_f = 1;
-    for (int n = 0; n < 16; ++n)
+    for (int n = 0; n < kMaxColumnSlots; ++n)
         sp.col_code[n] = n < group ? n << 8 : -1;   // token 0, part 0, query head n
     sp.timeout_ns = 2000000000ull;
 
@@ -219,7 +219,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     mp.g_real = group;
     mp.n_cols = group;
     mp.fuse_f = 1;
-    for (int n = 0; n < 16; ++n)
+    for (int n = 0; n < kMaxColumnSlots; ++n)
         mp.col_code[n] = n < group ? n << 8 : -1;
 
     alignas(64) CUtensorMap tmk, tmv;

@@ -38,8 +38,12 @@
  *   - Alignment: q, k, v, k_pages, v_pages and o must be 16-byte aligned, and
  *     the workspace 256-byte aligned; otherwise FD_ERR_INVALID_ARG.
  *   - Supported shapes: head_dim 64, 128 or 256; G = Hq/Hkv and the new query
- *     tokens per request q_len (fd_options.q_len) with G * q_len <= 8;
- *     batch <= 4096.  Other shapes return FD_ERR_UNSUPPORTED.
+ *     tokens per request q_len (fd_options.q_len) with G * q_len <= 16;
+ *     batch <= 4096.  Other shapes return FD_ERR_UNSUPPORTED.  Over 8 query
+ *     columns (G * q_len > 8) run on the tensor-core consumers only, so they
+ *     also return FD_ERR_UNSUPPORTED with FD_FLAG_CUDA_CORES, with pages of
+ *     under 8 tokens, and for an FP8 cache with head_dim 64 when the kv heads
+ *     cannot be paired (odd Hkv, or FD_FLAG_NO_HEAD_FUSION).
  *   - Several new tokens (q_len > 1, e.g. checking draft tokens): the cache
  *     of length L already holds them, q is [batch, q_len, Hq, head_dim], and
  *     new token i (0-based) attends causally to positions 0 .. L - q_len + i.
@@ -138,15 +142,19 @@ typedef struct fd_options {
 /* Do not fuse kv heads.  By default, when the tensor-core consumers apply
  * (contiguous KV, or pages of at least 8 tokens, and no FD_FLAG_CUDA_CORES),
  * a kv head's rows are short (under 256 bytes: head_dim 64, or an FP8 cache
- * with head_dim up to 128, or pages under 64 tokens) and the
- * call has at least 24 KV tiles of 64 tokens per split CTA (counted from
- * seq_lens_host when given, else from the capacity), F adjacent kv heads
- * (F = 4 or 2, the largest with F * head_dim <= 256, F * (Hq/Hkv) <= 8 and F
- * dividing Hkv) are read as one head of F * head_dim dims: [.., Hkv, D] and
- * [.., Hkv/F, F*D] are the same bytes, so each TMA row is F times longer, and
- * the F query groups share one tensor-core tile with zeros for the dims of
- * the other heads.  Every query head still attends only to its own kv head.
- * This flag keeps one kv head per segment. */
+ * with head_dim up to 128, or pages under 64 tokens) and the call has at
+ * least 24 KV tiles of 64 tokens per split CTA (counted from seq_lens_host
+ * when given, else from the capacity), F adjacent kv heads are read as one
+ * head of F * head_dim dims: [.., Hkv, D] and [.., Hkv/F, F*D] are the same
+ * bytes, so each TMA row is F times longer.
+ *   F = 4 when 4 * head_dim <= 256, 4 * G * q_len <= 8 and 4 divides Hkv: the
+ *         four query groups share one tensor-core tile, with zeros for the
+ *         dims of the other heads;
+ *   F = 2 otherwise, when 2 * head_dim <= 256 and 2 divides Hkv: each warp of
+ *         a pair takes one of the two heads.
+ * Over 8 query columns with an FP8 head_dim of 64 always pair.  Every query
+ * head still attends only to its own kv head.  This flag keeps one kv head
+ * per segment. */
 #define FD_FLAG_NO_HEAD_FUSION 0x8u
 
 /* Fuse kv heads whenever the shape and consumers allow it (the F rule
@@ -163,7 +171,8 @@ typedef struct fd_options {
  * launch shape the call takes, with or without fused kv heads (see
  * FD_FLAG_NO_HEAD_FUSION).  max_kv_len and page_size are validated but do
  * not change the size.
- * Returns 0 for invalid arguments.
+ * Returns 0 for invalid arguments and for more than 16 query columns per kv
+ * head (Hq/Hkv x q_len), which no call accepts.
  */
 size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                          int max_kv_len, int page_size);

@@ -67,6 +67,10 @@ def test_workspace_size_is_host_only_and_rejects_bad_shapes(fd):
     # q_len new tokens: G x q_len partial rows per slot
     assert fd.fd_workspace_size(4, 8, 2, 128, 1, 0, q_len=2) >= (4 * 2 + 1024) * 8 * 129 * 4
     assert fd.fd_workspace_size(4, 8, 2, 128, 1, 0, q_len=1) == fd.fd_workspace_size(4, 8, 2, 128, 1, 0)
+    # 16 columns (GQA-8 with two new tokens), and paired heads of 64 dims with 2 x 16 slots
+    assert fd.fd_workspace_size(4, 16, 2, 128, 1, 0, q_len=2) >= (4 * 2 + 1024) * 16 * 129 * 4
+    assert fd.fd_workspace_size(4, 32, 4, 64, 1, 0, q_len=2) >= (4 * 2 + 1024) * 32 * 65 * 4
+    assert fd.fd_workspace_size(4, 16, 2, 128, 1, 0, q_len=3) == 0
 
 
 ALIGNED = 1 << 20          # fake, 256-byte aligned device addresses (never dereferenced)
@@ -99,12 +103,24 @@ def test_decode_argument_checks(lib, fd):
     for d in (64, 128, 256):   # accepted head dims reach the workspace check
         assert call_decode(lib, d=d, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
     assert call_decode(lib, hq=6, hkv=2, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL   # group 3: padded to 4
-    assert call_decode(lib, hq=32, hkv=2) == E.FD_ERR_UNSUPPORTED      # group 16
-    # several new tokens: group x q_len query columns must fit 8
-    for g, ql, ok in ((4, 2, True), (1, 8, True), (2, 3, True), (4, 3, False), (8, 2, False), (1, 9, False)):
+    assert call_decode(lib, hq=32, hkv=2, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL   # group 16
+    assert call_decode(lib, hq=64, hkv=2) == E.FD_ERR_UNSUPPORTED      # group 32
+    # several new tokens: group x q_len query columns must fit 16
+    for g, ql, ok in ((4, 2, True), (1, 8, True), (2, 3, True), (4, 3, True), (8, 2, True), (1, 9, True),
+                      (1, 16, True), (16, 1, True), (8, 3, False), (1, 17, False), (16, 2, False)):
         opts = fd.FdOptions(0, 0, 0, None, None, 0, 0, 0.0, 0.0, ql)
         st = call_decode(lib, hq=2 * g, hkv=2, opts=ctypes.byref(opts), wsb=1024)
         assert st == (E.FD_ERR_WORKSPACE_TOO_SMALL if ok else E.FD_ERR_UNSUPPORTED), (g, ql)
+    # over 8 columns run on the tensor-core consumers only: rejected on the
+    # host with FD_FLAG_CUDA_CORES, and for an FP8 head of 64 dims that cannot
+    # pair (odd Hkv, or FD_FLAG_NO_HEAD_FUSION)
+    for g, ql, flags, kv, d, hkv, ok in ((8, 2, 0x2, 0, 128, 2, False), (8, 1, 0x2, 0, 128, 2, True),
+                                         (4, 3, 0x2, 0, 128, 2, False), (8, 2, 0, 1, 64, 2, True),
+                                         (8, 2, 0, 1, 64, 3, False), (8, 2, 0x8, 2, 64, 2, False),
+                                         (8, 2, 0x8, 1, 128, 2, True), (8, 2, 0x8, 0, 64, 2, True)):
+        opts = fd.FdOptions(0, flags, 0, None, None, 0, kv, 0.0, 0.0, ql)
+        st = call_decode(lib, hq=hkv * g, hkv=hkv, d=d, opts=ctypes.byref(opts), wsb=1024)
+        assert st == (E.FD_ERR_WORKSPACE_TOO_SMALL if ok else E.FD_ERR_UNSUPPORTED), (g, ql, flags, kv, d)
     opts = fd.FdOptions(0, 0, 0, None, None, 0, 0, 0.0, 0.0, -1)
     assert call_decode(lib, opts=ctypes.byref(opts)) == E.FD_ERR_INVALID_ARG
     assert call_decode(lib, B=5000) == E.FD_ERR_UNSUPPORTED
@@ -153,6 +169,10 @@ def test_paged_argument_checks(lib, fd):
     assert call_paged(lib, page=2, d=64, opts=ctypes.byref(fp8), wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
     assert call_paged(lib, page=1, d=64, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL   # bf16: 128 bytes
     assert call_paged(lib, page=96) == E.FD_ERR_UNSUPPORTED
+    # over 8 columns need the tensor-core consumers, which need pages of at least 8 tokens
+    many = fd.FdOptions(0, 0, 0, None, None, 0, 0, 0.0, 0.0, 2)
+    assert call_paged(lib, page=4, hq=16, opts=ctypes.byref(many)) == E.FD_ERR_UNSUPPORTED
+    assert call_paged(lib, page=8, hq=16, opts=ctypes.byref(many), wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
     lens = (ctypes.c_int32 * 2)(64, 65)                     # capacity 4 pages * 16
     assert call_paged(lib, slh=lens) == E.FD_ERR_INVALID_ARG
     assert call_paged(lib, wsb=100) == E.FD_ERR_WORKSPACE_TOO_SMALL

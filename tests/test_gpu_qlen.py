@@ -42,6 +42,52 @@ def test_contiguous_vs_oracle(group, q_len, flags):
         check(o, l, ro, rl, f"G={group} q_len={q_len} flags={flags} ctas={ctas}")
 
 
+# over 8 query columns per kv head: two n8 tiles on the tensor-core consumers
+# (GQA-8 with two new tokens, MHA with up to 16, GQA-16 with one, padded counts)
+@pytest.mark.parametrize("d,group,q_len", [(128, 8, 2), (128, 1, 16), (128, 1, 9), (128, 4, 3), (128, 16, 1),
+                                           (64, 8, 2), (64, 1, 16), (256, 8, 2), (256, 1, 12)])
+def test_sixteen_columns(d, group, q_len):
+    w = syn.make_contiguous(2150 + d + 10 * group + q_len, len(LENS), 2 * group, 2, d, 1024, LENS, q_len=q_len)
+    ro, rl = oracle.attend(w, threads=8)
+    for flags, ctas in ((0, 0), (0, 7), (NO_FUSION, 7), (FUSE, 7)):
+        out = torch.full(w.q.shape, float("nan"), device="cuda")
+        o, l = run(w, num_ctas=ctas, flags=flags, out=out)
+        assert not np.isnan(o).any()
+        check(o, l, ro, rl, f"d={d} G={group} q_len={q_len} flags={flags} ctas={ctas}")
+
+
+@pytest.mark.parametrize("page", [8, 16, 128])
+def test_sixteen_columns_paged(page):
+    w = syn.make_contiguous(2170 + page, len(LENS), 16, 2, 128, 1024, LENS, q_len=2)
+    wp = contig_to_paged(w, page, perm_seed=page, poison=True)
+    ro, rl = oracle.attend(wp, threads=8)
+    for ctas in (0, 5):
+        op, lp = run(wp, num_ctas=ctas)
+        check(op, lp, ro, rl, f"P={page} G=8 q_len=2 ctas={ctas}")
+        oc, lc = run(w, num_ctas=ctas)
+        assert np.array_equal(op, oc) and np.array_equal(lp, lc)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_sixteen_columns_fp8(fmt, d):
+    """FP8 heads of 64 dims are paired so their rows reach 128 bytes."""
+    w = syn.make_contiguous(2180 + d, len(LENS), 16, 2, d, 1024, LENS, q_len=2, kv_dtype=fmt, k_scale=0.05,
+                            v_scale=0.7)
+    ro, rl = oracle.attend(w, threads=8)
+    for flags in ((0, FUSE) if d == 64 else (0, NO_FUSION, FUSE)):
+        o, l = run(w, num_ctas=7, flags=flags)
+        check(o, l, ro, rl, f"{fmt} d={d} G=8 q_len=2 flags={flags}")
+
+
+def test_sixteen_columns_need_tensor_cores():
+    import decode_attention_decoding_gb300 as fd
+    w = syn.make_contiguous(2190, 2, 16, 2, 128, 64, [10, 64], q_len=2)
+    with pytest.raises(fd.FdError) as e:
+        run(w, flags=CUDA_CORES)
+    assert e.value.status == fd.FD_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("d", [64, 256])
 @pytest.mark.parametrize("group,q_len", [(1, 4), (4, 2)])
 def test_head_dims(d, group, q_len):
@@ -88,12 +134,14 @@ def test_fp8_cache(fmt):
 
 
 @pytest.mark.parametrize("flags", [0, CUDA_CORES])
-@pytest.mark.parametrize("group,q_len", [(1, 8), (2, 4), (4, 2)])
+@pytest.mark.parametrize("group,q_len", [(1, 8), (2, 4), (4, 2), (8, 2), (1, 16), (4, 3)])
 def test_causal_gather_probe(group, q_len, flags):
     """Key at position L - q_len + j is 2^(4+j) q (q = +-1): every new token's
     largest visible score is its own position by more than 110 natural
     units, and V rows encode their position, so new token i must return
     exactly V[L - q_len + i]; seeing a later position would return another."""
+    if flags == CUDA_CORES and group * q_len > 8:
+        pytest.skip("over 8 columns run on the tensor-core consumers only")
     L, hkv, d = 1500, 2, 128
     w = syn.make_contiguous(2600 + group, 1, hkv * group, hkv, d, L, [L], q_len=q_len)
     signs = np.where(syn.normal_bf16(9, (hkv, d)).view(np.int16) < 0, -1.0, 1.0)
