@@ -17,50 +17,14 @@
 #include "fd_launch.h"
 #include "fd_sched.h"
 
-namespace {
-
-using namespace fd;
-
-constexpr int kVersion = 10300;   // 1.3.0
-constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
-constexpr size_t kMergeRoomBytes = 32u * 1024u;   // shared memory left beside a split CTA
-constexpr size_t kShortCallInFlightBytes = 96u * 1024u;   // K/V in flight per CTA on short calls
-
-struct DeviceInfo {
-    int sms = 0;
-    int smem_optin = 0;
-};
-
-// The one piece of state kept across calls: a cache of device properties.
-std::mutex g_dev_mu;
-DeviceInfo g_dev[64];
-bool g_dev_ok[64] = {};
-
-fd_status device_info(DeviceInfo *out)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return FD_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev_ok[dev]) {
-        DeviceInfo d;
-        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-                cudaSuccess)
-            return FD_ERR_CUDA;
-        g_dev[dev] = d;
-        g_dev_ok[dev] = true;
-    }
-    *out = g_dev[dev];
-    return FD_OK;
-}
+namespace fd {
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn()
+static EncodeTiledFn encode_fn()
 {
     static EncodeTiledFn fn = []() -> EncodeTiledFn {
         void *p = nullptr;
@@ -75,18 +39,18 @@ EncodeTiledFn encode_fn()
 }
 
 // Tensor-map element type and size of a K/V element type (kKv*).
-CUtensorMapDataType kv_map_type(int kv)
+static CUtensorMapDataType kv_map_type(int kv)
 {
     return kv == kKvBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                          : (kv == kKvF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
-int kv_elem_bytes(int kv) { return kv_is_fp8(kv) ? 1 : 2; }
+static int kv_elem_bytes(int kv) { return kv_is_fp8(kv) ? 1 : 2; }
 
 // A rank-3 view {head_dim, Hkv, rows} of a K or V tensor whose rows are
 // (token, kv head) pairs of head_dim elements; each load is a box of
 // box_rows tokens of one kv head: the whole row, or (swizzled) one 128-byte
 // part of it with the 128-byte swizzle that the tensor-core consumers read.
-fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
+static fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
                         bool swizzled, int kv, int d)
 {
     EncodeTiledFn fn = encode_fn();
@@ -110,7 +74,7 @@ fd_status encode_kv_map(CUtensorMap *map, const void *base, int hkv, long long r
 // is 64 16-bit elements or 128 FP8 codes), so that one box {part, box_rows,
 // parts, 1} carries every 128-byte-swizzled part of box_rows rows of one kv
 // head (laid out part by part in shared memory).
-fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
+static fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, long long rows, int box_rows,
                            int kv, int d)
 {
     EncodeTiledFn fn = encode_fn();
@@ -152,6 +116,46 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
     if ((st = encode_kv_map(tmk, k, hkv, rows, box_rows, mma, kv, d)) != FD_OK ||
         (st = encode_kv_map(tmv, v, hkv, rows, box_rows, mma, kv, d)) != FD_OK)
         return st;
+    return FD_OK;
+}
+
+}  // namespace fd
+
+namespace {
+
+using namespace fd;
+
+constexpr int kVersion = 10300;   // 1.3.0
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+constexpr size_t kMergeRoomBytes = 32u * 1024u;   // shared memory left beside a split CTA
+constexpr size_t kShortCallInFlightBytes = 96u * 1024u;   // K/V in flight per CTA on short calls
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+// The one piece of state kept across calls: a cache of device properties.
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+bool g_dev_ok[64] = {};
+
+fd_status device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return FD_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_ok[dev]) {
+        DeviceInfo d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return FD_ERR_CUDA;
+        g_dev[dev] = d;
+        g_dev_ok[dev] = true;
+    }
+    *out = g_dev[dev];
     return FD_OK;
 }
 

@@ -61,7 +61,6 @@ struct Shape {
     static constexpr int kLanesPerRow = D / 8;                // CUDA cores: 8 elements per lane
     static constexpr int kLaneBytes = 8 * kElemBytes;
     static constexpr int kRowsPerStep = 32 / kLanesPerRow;    // rows a warp reads at once
-    static constexpr int kRowsPerGroup = kRowsPerWarp / kRowsPerStep;
     static constexpr int kKSteps = D / 16;                    // tensor cores: k-steps of q.K^T
     static constexpr int kDimTilesPerWarp = D / 32;           // P.V dim tiles per warp of a pair
 };
@@ -527,7 +526,20 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                                                int t_end, int cw, int lane)
 {
     using HD = Shape<D, KV>;
-    constexpr int LPR = HD::kLanesPerRow, RPS = HD::kRowsPerStep, RPG = HD::kRowsPerGroup;
+    constexpr int LPR = HD::kLanesPerRow, RPS = HD::kRowsPerStep;
+    // Eight columns split the warps in two halves (warps 0-3 take columns 0-3,
+    // warps 4-7 columns 4-7), each half covering every row of the tile, 16 per
+    // warp: a thread then holds the q, O and softmax state of 4 columns, as
+    // for G = 4, where 8 columns would spill.  Each K/V row is read from
+    // shared memory by two warps.
+    constexpr int CS = G == 8 ? 2 : 1;            // column sets
+    constexpr int GW = G / CS;                    // columns of this warp
+    constexpr int WR = kConsumerWarps / CS;       // warps over the rows of a tile (states per column)
+    constexpr int RPW = kTileTokens / WR;         // rows of this warp
+    constexpr int RPG = RPW / RPS;                // row steps of this warp
+    const int cbase = (cw / WR) * GW;             // first column of this warp
+    const int row0 = (cw % WR) * RPW;             // first row of this warp
+    const int slot = cw % WR;                     // its state slot in the reduction
     const int NS = p.num_stages;
     const bool qf16 = q_is_f16<KV>(p);
     const int sub = lane / LPR, li = lane % LPR;   // row slot within a warp step, lane within the row
@@ -536,19 +548,19 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
     float *red_l = red_m + kConsumerWarps * G;                       // [warps][G]
     const int ctid = cw * 32 + lane;
     // rows per online update (fewer live scores for large G)
-    constexpr int kSub0 = G >= 8 ? 1 : (G >= 4 ? 2 : RPG);
+    constexpr int kSub0 = GW >= 8 ? 1 : (GW >= 4 ? 2 : RPG);
     constexpr int kSub = kSub0 < RPG ? kSub0 : RPG;
     // causal lag of each column: new token i sees q_len - 1 - i fewer tokens
-    int lag[G];
+    int lag[GW];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-        lag[g] = p.q_len - 1 - col_info(p, 0, 0, g).i;
+    for (int g = 0; g < GW; ++g)
+        lag[g] = p.q_len - 1 - col_info(p, 0, 0, cbase + g).i;
 
-    float2 qf[G][4];
-    float2 acc[G][4];
-    float m[G], l[G];
+    float2 qf[GW][4];
+    float2 acc[GW][4];
+    float m[GW], l[GW];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int g = 0; g < GW; ++g) {
         m[g] = kNegInf;
         l[g] = 0.f;
 #pragma unroll
@@ -580,8 +592,8 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
         if (flags & kFirstInCta) {
             const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const ColInfo c = col_info(p, b, h, g);
+            for (int g = 0; g < GW; ++g) {
+                const ColInfo c = col_info(p, b, h, cbase + g);
                 uint4 raw = make_uint4(0u, 0u, 0u, 0u);
                 if (c.valid)
                     raw = ldg128_nc(p.q + c.row * D + li * 8);
@@ -599,14 +611,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 #pragma unroll
         for (int r0 = 0; r0 < RPG; r0 += kSub) {
             // Scores (log2 units).
-            float sc[kSub][G];
+            float sc[kSub][GW];
 #pragma unroll
             for (int r = 0; r < kSub; ++r) {
-                const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
+                const int row = row0 + RPS * (r0 + r) + sub;
                 float2 kx[4];
                 load_row8<KV>(kbase + row * HD::kRowBytes, kx);
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < GW; ++g) {
                     float2 a = mul2(qf[g][0], kx[0]);
                     a = fma2(qf[g][1], kx[1], a);
                     a = fma2(qf[g][2], kx[2], a);
@@ -617,7 +629,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 #pragma unroll
             for (int r = 0; r < kSub; ++r)
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < GW; ++g) {
                     float x = sc[r][g];
 #pragma unroll
                     for (int off = LPR / 2; off; off >>= 1)
@@ -627,14 +639,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 
             // Online softmax update (rows past the column's causal end, or past
             // the request's end, carry no weight).
-            float pr[kSub][G];
+            float pr[kSub][GW];
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < GW; ++g) {
                 const int lim = min(nvalid, rem - lag[g]);   // the column's causal end in this tile
                 float tile_max = kNegInf;
 #pragma unroll
                 for (int r = 0; r < kSub; ++r) {
-                    const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
+                    const int row = row0 + RPS * (r0 + r) + sub;
                     if (row < lim)
                         tile_max = fmaxf(tile_max, sc[r][g]);
                 }
@@ -643,7 +655,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                 float psum = 0.f;
 #pragma unroll
                 for (int r = 0; r < kSub; ++r) {
-                    const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
+                    const int row = row0 + RPS * (r0 + r) + sub;
                     pr[r][g] = (row < lim) ? exp2_approx(sc[r][g] - m_new) : 0.f;
                     psum += pr[r][g];
                 }
@@ -658,12 +670,12 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             // acc += p * V
 #pragma unroll
             for (int r = 0; r < kSub; ++r) {
-                const int row = cw * kRowsPerWarp + RPS * (r0 + r) + sub;
+                const int row = row0 + RPS * (r0 + r) + sub;
                 if (row < nvalid) {
                     float2 vx[4];
                     load_row8<KV>(vbase + row * HD::kRowBytes, vx);
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
+                    for (int g = 0; g < GW; ++g) {
                         const float2 p2 = make_float2(pr[r][g], pr[r][g]);
                         acc[g][0] = fma2(p2, vx[0], acc[g][0]);
                         acc[g][1] = fma2(p2, vx[1], acc[g][1]);
@@ -682,7 +694,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 #pragma unroll
             for (int off = LPR; off < 32; off <<= 1) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < GW; ++g) {
                     const float mo = __shfl_xor_sync(0xffffffffu, m[g], off);
                     const float lo = __shfl_xor_sync(0xffffffffu, l[g], off);
                     const float mn = fmaxf(m[g], mo);
@@ -700,20 +712,20 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                     m[g] = mn;
                 }
             }
-            // 2. publish the warp state
+            // 2. publish the warp state (its columns, in its slot)
             if (sub == 0) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float4 *dst = reinterpret_cast<float4 *>(red_acc + (cw * G + g) * D + li * 8);
+                for (int g = 0; g < GW; ++g) {
+                    float4 *dst = reinterpret_cast<float4 *>(red_acc + (slot * G + cbase + g) * D + li * 8);
                     dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
                     dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
                 }
             }
             if (lane == 0) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    red_m[cw * G + g] = m[g];
-                    red_l[cw * G + g] = l[g];
+                for (int g = 0; g < GW; ++g) {
+                    red_m[slot * G + cbase + g] = m[g];
+                    red_l[slot * G + cbase + g] = l[g];
                 }
             }
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
@@ -721,15 +733,15 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
                 return;
             }
             // 3. combine the warps and write the segment's result
-            combine_and_write<G, kConsumerWarps, D>(p, red_acc, red_m, red_l, red_l, ctid, b, h, u,
-                                                    (flags & kOwnSegment) != 0);
+            combine_and_write<G, WR, D>(p, red_acc, red_m, red_l, red_l, ctid, b, h, u,
+                                        (flags & kOwnSegment) != 0);
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
             }
             // 4. fresh state for the next segment
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < GW; ++g) {
                 m[g] = kNegInf;
                 l[g] = 0.f;
 #pragma unroll

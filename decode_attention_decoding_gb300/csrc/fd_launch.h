@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fd.h"
 #include "fd_kernels.cuh"
 
 namespace fd {
@@ -16,6 +17,15 @@ struct SplitLaunch {
     size_t smem_optin;     // the device's opt-in maximum (set once per kernel)
     cudaStream_t stream;
 };
+
+// K and V tensor maps of a call (fd_api.cu): rows are (token, kv head)
+// pairs of d elements of type kv (kKv*), loaded box_rows tokens at a time.
+// The tensor-core consumers (mma) take 128-byte swizzled boxes, as one 4-D
+// box per load when the driver accepts the view (sets sp->box4d and
+// sp->box_rows_log2); the CUDA-core consumers take whole rows.  Returns
+// FD_ERR_CUDA if the driver rejects the maps.
+fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, const void *v, int hkv,
+                         long long rows, int box_rows, bool mma, int kv, int d, SplitParams *sp);
 
 // LSE merge of the split partials; grid = number of segments (requests x kv
 // heads).  Launched as a programmatic dependent of the split kernel.

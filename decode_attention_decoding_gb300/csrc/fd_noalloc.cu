@@ -75,35 +75,6 @@ fd_status noalloc_setup(NoallocDevice *out)
     return FD_OK;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-fd_status encode_rows(CUtensorMap *map, const void *base, int hkv, long long rows)
-{
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    if (!fn)
-        return FD_ERR_CUDA;
-    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)hkv, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)HD::kRowBytes, (cuuint64_t)hkv * HD::kRowBytes};
-    const cuuint32_t box[3] = {(cuuint32_t)kD, 1u, (cuuint32_t)kTileTokens};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
-               ? FD_OK
-               : FD_ERR_CUDA;
-}
-
 // Scratch layout for `slots` partials of `group` rows: the same regions as a
 // caller-provided workspace, but sized for the actual number of split CTAs.
 struct NoallocLayout {
@@ -177,8 +148,12 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
         sp.col_code[n] = n < group ? n << 8 : -1;   // token 0, part 0, query head n
     sp.timeout_ns = 2000000000ull;
 
+    // Consumers as fd_decode picks them for an unfused call: CUDA cores for
+    // one query head per kv head, tensor cores for GQA groups.
+    const int cons = group >= 2 ? kConsMma : kConsCudaCores;
+
     // Shared-memory plan (same rule as the workspace entry points).
-    const size_t red = align_up((size_t)reduction_floats(kConsCudaCores, group, kD) * sizeof(float), 16);
+    const size_t red = align_up((size_t)reduction_floats(cons, group, kD) * sizeof(float), 16);
     const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
     const size_t misc = 64;
     const size_t fixed = 1024 + red + prefix + misc + 8;
@@ -224,14 +199,14 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
 
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)batch * (s_max > 0 ? s_max : 1);
-    if ((st = encode_rows(&tmk, k, num_kv_heads, rows)) != FD_OK ||
-        (st = encode_rows(&tmv, v, num_kv_heads, rows)) != FD_OK)
+    if ((st = encode_kv_maps(&tmk, &tmv, k, v, num_kv_heads, rows, kTileTokens, cons != kConsCudaCores, kKvBf16,
+                             kD, &sp)) != FD_OK)
         return st;
 
     // The status word is the only part of the scratch that must start at zero.
     if (cudaMemsetAsync(sp.ws_err, 0, sizeof(unsigned int), launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    if (launch_split_variant<false, kKvBf16, kD>(kConsCudaCores, group, sp, tmk, tmv, launch) != cudaSuccess)
+    if (launch_split_variant<false, kKvBf16, kD>(cons, group, sp, tmk, tmv, launch) != cudaSuccess)
         return FD_ERR_CUDA;
     if (launch_merge(group, kD, mp, batch * num_kv_heads, launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;

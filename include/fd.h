@@ -261,9 +261,10 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  * device memory all belongs to their own pool.  The sources this library
  * follows have no counterpart to this call; it exists only for such callers.
  *
- * It computes what fd_decode computes (the CUDA-core split kernel and the
- * same merge, contiguous layout, one split CTA per SM), with the split partials and the tile prefix
- * held in a fixed device array of FD_NOALLOC_SCRATCH_BYTES (8 MiB) that is
+ * It computes what fd_decode computes for a contiguous, unfused call (the
+ * same split kernel -- CUDA-core consumers for Hq = Hkv, tensor-core
+ * consumers for GQA groups -- and the same merge, one split CTA per SM), with
+ * the split partials and the tile prefix held in a fixed device array of FD_NOALLOC_SCRATCH_BYTES (8 MiB) that is
  * part of this library: every GPU that loads the library reserves it until
  * the process exits.  Nothing is allocated -- no cudaMalloc, cudaFree or
  * allocating library routine -- and no workspace is passed.  The caller still
@@ -272,8 +273,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  *   scale, o, lse: as for fd_decode (lse may be NULL).
  *   device_status: NULL, or a device uint32 that receives this call's
  *   FD_DEVICE_STATUS_* bits (0 when all went well), stream-ordered.
- * Limits: bf16 inputs and head_dim 128 only (other head dims return
- * FD_ERR_UNSUPPORTED); the scratch must hold 256 bytes + 4 (batch + 1) bytes + (batch *
+ * Limits: bf16 inputs, head_dim 128 and Hq/Hkv in {1, 2, 4, 8} only (other
+ * shapes return FD_ERR_UNSUPPORTED); the scratch must hold 256 bytes + 4 (batch + 1) bytes + (batch *
  * num_kv_heads + number of SMs) partials of (Hq/Hkv) * (head_dim + 1) * 4
  * bytes, each region rounded up to 256 bytes; a larger shape returns
  * FD_ERR_WORKSPACE_TOO_SMALL before anything is launched.

@@ -3,7 +3,8 @@ memory where they run attention (it keeps its scratch in a fixed array inside
 the library instead of a caller workspace).
 
 Called through the C ABI with ctypes, twice in a row on different inputs, and
-compared with fd_decode on the same inputs within the GPU tests' tolerance.
+compared with the fp64 oracle within the GPU tests' tolerance, for each group
+size it serves (CUDA-core consumers for MHA, tensor-core consumers for GQA).
 This file is collected last so that a stop-at-first-failure run has already
 run every other test.
 """
@@ -14,7 +15,8 @@ import pytest
 import torch
 
 import fd_synth as syn
-from gpu_util import LSE_ATOL, O_ATOL, O_RTOL, to_device
+import oracle
+from gpu_util import check, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -37,28 +39,24 @@ def call_noalloc(lib, d, w, o, lse, status):
                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def assert_close(o, lse, ro, rl):
-    o, lse, ro, rl = (x.cpu().numpy().astype(np.float64) for x in (o, lse, ro, rl))
-    assert np.all(np.abs(o - ro) <= O_ATOL + O_RTOL * np.abs(ro))
-    fin = np.isfinite(rl)
-    assert np.array_equal(fin, np.isfinite(lse)) and np.all(lse[~fin] == rl[~fin])
-    assert np.all(np.abs(lse[fin] - rl[fin]) <= LSE_ATOL)
-
-
-def test_noalloc_matches_fd_decode_on_two_calls_in_a_row(lib):
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_noalloc_matches_the_oracle_on_two_calls_in_a_row(lib, group):
     import decode_attention_decoding_gb300 as fd
-    cases = [syn.make_contiguous(700, 4, 16, 4, 128, 1500, [1500, 3, 0, 777]),
-             syn.make_contiguous(701, 4, 16, 4, 128, 1500, [64, 1499, 1000, 1])]
-    o = torch.full((4, 16, 128), float("nan"), dtype=torch.float32, device="cuda")
-    lse = torch.full((4, 16), float("nan"), dtype=torch.float32, device="cuda")
+    oracle.build()
+    hkv = 4
+    cases = [syn.make_contiguous(700 + group, 4, hkv * group, hkv, 128, 1500, [1500, 3, 0, 777]),
+             syn.make_contiguous(710 + group, 4, hkv * group, hkv, 128, 1500, [64, 1499, 1000, 1])]
+    o = torch.full((4, hkv * group, 128), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((4, hkv * group), float("nan"), dtype=torch.float32, device="cuda")
     status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
     for w in cases:                       # consecutive calls share the fixed scratch
         d = to_device(w)
         assert call_noalloc(lib, d, w, o, lse, status) == fd.FD_OK
-        ro, rl = fd.fd_decode(d["q"], d["k"], d["v"], d["seq_lens"], scale=w.scale)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        assert_close(o, lse, ro, rl)
+        ro, rl = oracle.attend(w, threads=8)
+        check(o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rl,
+              f"noalloc G={group}")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
