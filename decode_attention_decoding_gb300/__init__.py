@@ -24,7 +24,7 @@ __all__ = [
     "fd_get_device_error", "fd_status_string", "fd_version", "make_workspace", "library_path",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
     "FD_ERR_CUDA", "FD_ERR_TIMEOUT", "FD_ERR_DEVICE_INPUT", "FD_FLAG_TEST_STARVE_FIRST_TILE",
-    "FD_FLAG_CUDA_CORES", "FD_FLAG_NO_4D_BOXES", "FD_FLAG_NO_HEAD_FUSION",
+    "FD_FLAG_CUDA_CORES", "FD_FLAG_NO_4D_BOXES", "FD_FLAG_NO_HEAD_FUSION", "FD_FLAG_NO_GATHER",
     "FD_FLAG_FUSE_HEADS", "FD_KV_AS_Q", "FD_KV_FP8_E4M3", "FD_KV_FP8_E5M2",
     "fd_decode_noalloc",
 ]
@@ -35,6 +35,7 @@ FD_FLAG_TEST_STARVE_FIRST_TILE = 0x1
 FD_FLAG_CUDA_CORES = 0x2
 FD_FLAG_NO_4D_BOXES = 0x4
 FD_FLAG_NO_HEAD_FUSION = 0x8
+FD_FLAG_NO_GATHER = 0x20
 FD_FLAG_FUSE_HEADS = 0x10
 FD_KV_AS_Q, FD_KV_FP8_E4M3, FD_KV_FP8_E5M2 = 0, 1, 2
 

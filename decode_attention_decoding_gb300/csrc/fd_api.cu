@@ -94,6 +94,25 @@ static fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, l
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
 }
 
+// A rank-2 view {d, rows} of a paged K or V pool whose rows are (page, token,
+// kv head) triples of d elements, with one-row boxes and no swizzle: the
+// CUDA-core consumers gather pages under 8 tokens four rows per load.
+static fd_status encode_kv_rows_2d(CUtensorMap *map, const void *base, long long rows, int kv, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return FD_ERR_CUDA;
+    const cuuint64_t row_bytes = (cuuint64_t)kv_elem_bytes(kv) * (cuuint64_t)d;
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)d, 1u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(map, kv_map_type(kv), 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
+}
+
 // K and V maps for a call: the tensor-core consumers prefer 4-D maps (one
 // box per tile or page carries every swizzled part) and fall back to 3-D
 // maps with one box per 64-dim part if the driver rejects the 4-D view.
@@ -625,6 +644,19 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
         return st;
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)num_pages * page_size;
+    // Pages of 1 or 2 tokens (CUDA-core consumers): gather a tile's rows four
+    // per load when the (page, token, kv head) row index fits int32; one box
+    // per page otherwise, with FD_FLAG_NO_GATHER, or if the driver rejects the
+    // view.  The TMA unit's cost per load, not its size, bounds these pages:
+    // measured on GB300, gathering ran one-token pages 2.2-2.5x and two-token
+    // pages 1.4x faster; four-token pages carry four rows per box already.
+    cp.sp.gather4 = 0;
+    if (!cp.mma && page_size <= 2 && rows * cp.sp.hkv < (1ll << 31) && !(cp.sp.flags & FD_FLAG_NO_GATHER) &&
+        encode_kv_rows_2d(&tmk, k_pages, rows * cp.sp.hkv, cp.kv, cp.head_dim) == FD_OK &&
+        encode_kv_rows_2d(&tmv, v_pages, rows * cp.sp.hkv, cp.kv, cp.head_dim) == FD_OK) {
+        cp.sp.gather4 = 1;
+        return run(cp, true, tmk, tmv, opts);
+    }
     const int box = page_size < kTileTokens ? page_size : kTileTokens;
     if ((st = encode_kv_maps(&tmk, &tmv, k_pages, v_pages, cp.sp.hkv, rows, box, cp.mma, cp.kv,
                              cp.head_dim, &cp.sp)) != FD_OK)

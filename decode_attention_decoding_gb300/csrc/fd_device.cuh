@@ -108,6 +108,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, uint
         : "memory");
 }
 
+// Four rows of a 2-D tensor map (rows r0..r3, columns from c0, one box
+// {columns, 1} each) gathered into four consecutive box-sized slots at dst,
+// completing on `bar`.
+__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const void *desc, uint32_t bar, int c0, int r0,
+                                               int r1, int r2, int r3, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar),
+        "l"(policy)
+        : "memory");
+}
+
 // 4-D tiled bulk tensor load global -> shared, completing on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *desc, uint32_t bar, int c0, int c1,
                                             int c2, int c3, uint64_t policy)

@@ -118,6 +118,11 @@ struct SplitParams {
     int box4d;
     int box_rows_log2;   // log2 of the rows in one box: 6 (64) or log2(page size)
     int page_log2;       // paged, page size under 64: log2 of the page size
+    // Paged with pages of 1 or 2 tokens (CUDA-core consumers): 1 when the K/V
+    // maps are 2-D {head_dim, num_pages * P * Hkv rows} with one-row boxes and
+    // a tile's rows are gathered four per load (row of token o of page e for
+    // kv head h: (e * P + o) * Hkv + h); 0 for one box per page.
+    int gather4;
     // Query columns of a launch head (see col_info): the caller's q is
     // [B, q_len, Hq, dh], and a launch head is fuse_f adjacent kv heads of
     // the caller read as one row of D elements (fused heads, tensor-core path
@@ -335,6 +340,20 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
         }
         return e;
     };
+    // Warp-collective: entry of page pg_lane anywhere in the window's 128
+    // entries (each lane its own).
+    auto window_entry_any = [&](int pg_lane) -> int {
+        const int idx = pg_lane - win_base;
+        const int src = idx & 31;
+        const int a = __shfl_sync(0xffffffffu, e0, src), bq = __shfl_sync(0xffffffffu, e1, src);
+        const int c = __shfl_sync(0xffffffffu, e2, src), d = __shfl_sync(0xffffffffu, e3, src);
+        int e = idx < 32 ? a : (idx < 64 ? bq : (idx < 96 ? c : d));
+        if (idx < 0 || idx >= 128 || e < 0 || e >= p.num_pages) {
+            atomicOr(p.ws_err, kErrPage);
+            e = 0;
+        }
+        return e;
+    };
     // Box `box` (0..kBoxes-1) of the tile's K/V for the rows starting at tile
     // row r0 (a page's first row, or 0).
     auto load_box = [&](int box, uint32_t kdst, uint32_t vdst, uint32_t full, int r0, int row) {
@@ -380,6 +399,7 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
         const uint32_t extra = (starve && issued == 0) ? 256u : 0u;
         const int P = p.page_size;
         const bool small_pages = PAGED && P < kTileTokens;
+        const bool gather = !SW128 && PAGED && p.gather4 != 0;
         // pages of this tile that hold valid tokens (paged, P < 64)
         const int need = small_pages ? min(kTileTokens >> page_log2, (nvalid + P - 1) >> page_log2) : 1;
         if (lane == 0) {
@@ -390,7 +410,9 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             m[3] = nvalid;
             m[4] = flags;
             m[5] = b * p.hkv + h;
-            const uint32_t bytes = small_pages ? 2u * need * P * HD::kRowBytes : (uint32_t)(2 * HD::kTileBytes);
+            const uint32_t bytes = gather ? 2u * (uint32_t)(((nvalid + 3) >> 2) * 4 * HD::kRowBytes)
+                                   : small_pages ? 2u * need * P * HD::kRowBytes
+                                                 : (uint32_t)(2 * HD::kTileBytes);
             mbar_arrive_expect_tx(full, bytes + extra);
         }
         __syncwarp();
@@ -402,6 +424,25 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             const int phys = window_entry(token0 / P);
             if (lane < kBoxes)
                 load_box(lane, kdst, vdst, full, 0, phys * P + (token0 % P));
+        } else if (gather) {
+            if constexpr (!SW128) {
+                // Four rows per load: lane l < 16 gathers K rows 4l .. 4l + 3 of
+                // the tile, lane 16 + l the same V rows.  Rows past the request's
+                // end repeat its last token (never read by the consumers).  The
+                // tile's pages (at most 64) lie in the window's 128 entries.
+                ensure_window(token0 >> page_log2);
+                const int grp = lane & 15;
+                int rowc[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int tok = token0 + min(4 * grp + k, nvalid - 1);
+                    const int e = window_entry_any(tok >> page_log2);
+                    rowc[k] = (e * P + (tok & (P - 1))) * p.hkv + h;
+                }
+                if (grp < ((nvalid + 3) >> 2))
+                    tma_gather4_2d((lane < 16 ? kdst : vdst) + 4 * grp * HD::kRowBytes, lane < 16 ? tmk : tmv,
+                                   full, 0, rowc[0], rowc[1], rowc[2], rowc[3], policy);
+            }
         } else {
             // One (page, box) pair per lane, so a tile's boxes issue together.
             const int pg0 = token0 >> page_log2;

@@ -157,6 +157,11 @@ typedef struct fd_options {
  * per segment. */
 #define FD_FLAG_NO_HEAD_FUSION 0x8u
 
+/* Do not gather pages of 1 or 2 tokens four rows per TMA load
+ * (tile::gather4); load one box per page instead.  Results are identical; for
+ * comparisons only. */
+#define FD_FLAG_NO_GATHER 0x20u
+
 /* Fuse kv heads whenever the shape and consumers allow it (the F rule
  * above), whatever the row length and the call's size.  FD_FLAG_NO_HEAD_FUSION
  * wins if both are set. */

@@ -177,17 +177,41 @@ def test_device_length_above_capacity_is_reported():
     assert fd.fd_get_device_error(ws) == fd.FD_OK             # the word was cleared
 
 
-def test_bad_block_table_entry_is_reported():
+@pytest.mark.parametrize("page", [16, 1])
+def test_bad_block_table_entry_is_reported(page):
     import decode_attention_decoding_gb300 as fd
-    w = contig_to_paged(syn.make_contiguous(441, 1, 4, 2, 128, 200, [200]), 16, perm_seed=2)
+    w = contig_to_paged(syn.make_contiguous(441, 1, 4, 2, 128, 200, [200]), page, perm_seed=2)
     d = to_device(w)
     d["block_table"][0, 3] = w.num_pages + 1000
-    ws = fd.make_workspace(1, 4, 2, 128, 200, 16)
+    ws = fd.make_workspace(1, 4, 2, 128, 200, page)
     o, l = fd.fd_decode_paged(d["q"], d["k"], d["v"], d["block_table"], d["seq_lens"], scale=w.scale,
                               workspace=ws)
     torch.cuda.synchronize()
     assert np.all(np.isfinite(o.cpu().numpy()))
     assert fd.fd_get_device_error(ws) == fd.FD_ERR_DEVICE_INPUT
+
+
+NO_GATHER = 0x20   # FD_FLAG_NO_GATHER: one TMA box per small page instead of four-row gathers
+
+
+@pytest.mark.parametrize("page", [1, 2])
+@pytest.mark.parametrize("d,kv,group", [(64, None, 4), (128, None, 1), (128, None, 8), (256, None, 2),
+                                        (128, "e4m3", 4), (64, "e5m2", 8)])
+def test_small_pages_gathered_four_rows_per_load(page, d, kv, group):
+    """Pages of 1 or 2 tokens: a tile's rows gathered four per TMA load
+    (tile::gather4) give results bitwise equal to one box per page, and match
+    the oracle, with ragged lengths and poisoned unused pages."""
+    if kv and page * d < 128:
+        pytest.skip("one-token FP8 pages of 64 dims are refused (64-byte page boxes)")
+    extra = dict(kv_dtype=kv, k_scale=0.05, v_scale=0.7) if kv else {}
+    w = syn.make_contiguous(460 + page + d + group, len(RAGGED), 2 * group, 2, d, 1024, RAGGED, **extra)
+    wp = contig_to_paged(w, page, perm_seed=page + d, poison=True)
+    ro, rl = oracle.attend(wp, threads=8)
+    for ctas in (0, 5):
+        a = run(wp, num_ctas=ctas)
+        b = run(wp, num_ctas=ctas, flags=NO_GATHER)
+        check(a[0], a[1], ro, rl, f"gathered P={page} d={d} kv={kv} G={group} ctas={ctas}")
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
 NO_4D = 0x4   # FD_FLAG_NO_4D_BOXES: one TMA box per 64-dim half (3-D tensor maps)
