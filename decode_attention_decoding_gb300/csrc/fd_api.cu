@@ -225,19 +225,20 @@ int kv_elem_bytes_of(const fd_options *opts)
 }
 
 // More than 8 query columns per kv head run on the tensor-core consumers only:
-// no FD_FLAG_CUDA_CORES, pages of at least 8 tokens, and a row of at least
-// 128 bytes -- directly, or by pairing two kv heads (an FP8 head of 64 dims).
-// Host-only; FD_OK or FD_ERR_UNSUPPORTED.
+// no FD_FLAG_CUDA_CORES, and a row of at least 128 bytes -- directly, or by
+// pairing two kv heads (an FP8 head of 64 dims; pairing needs pages of at
+// least 8 tokens).  Host-only; FD_OK or FD_ERR_UNSUPPORTED.
 fd_status check_columns(int hq, int hkv, int head_dim, int page_size, const fd_options *opts)
 {
     if ((long long)(hq / hkv) * q_len_of(opts) <= kMaxColumnsCudaCores)
         return FD_OK;
     const unsigned flags = opts ? opts->flags : 0u;
-    if ((flags & FD_FLAG_CUDA_CORES) || (page_size != 0 && page_size < 8))
+    if (flags & FD_FLAG_CUDA_CORES)
         return FD_ERR_UNSUPPORTED;
     if (head_dim * kv_elem_bytes_of(opts) >= 128)
         return FD_OK;
-    const bool pairable = 2 * head_dim <= 256 && hkv % 2 == 0 && !(flags & FD_FLAG_NO_HEAD_FUSION);
+    const bool pairable = 2 * head_dim <= 256 && hkv % 2 == 0 && !(flags & FD_FLAG_NO_HEAD_FUSION) &&
+                          (page_size == 0 || page_size >= 8);
     return pairable ? FD_OK : FD_ERR_UNSUPPORTED;
 }
 
@@ -254,14 +255,16 @@ struct CallPlan {
     int kv;           // K/V element type (kKv*): bf16, fp16 (q of the same type) or FP8
 };
 
-// Tensor-core consumers serve GQA groups; paged pools need pages of at least
-// 8 tokens so every page box starts on a 1 KB swizzle boundary, and a row
-// must fill at least one 128-byte swizzled part.
+// Tensor-core consumers serve GQA groups; a row must fill at least one
+// 128-byte swizzled part.  Pages of 8 tokens or more arrive by TMA (every
+// page box starts on a 1 KB swizzle boundary); smaller pages are copied row
+// by row with cp.async into the same swizzled layout.
 bool use_mma(int group, int page_size, int row_bytes, const fd_options *opts)
 {
+    (void)page_size;
     if (opts && (opts->flags & FD_FLAG_CUDA_CORES))
         return false;
-    return group >= 2 && (page_size == 0 || page_size >= 8) && row_bytes >= 128;
+    return group >= 2 && row_bytes >= 128;
 }
 
 // Fusion pays where a kv head's TMA rows are short (under 256 bytes: 64
@@ -644,6 +647,21 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
         return st;
     alignas(64) CUtensorMap tmk, tmv;
     const long long rows = (long long)num_pages * page_size;
+    // Pages under 8 tokens on the tensor-core consumers: the producer copies
+    // rows with cp.async into the swizzled layout; no tensor maps.
+    cp.sp.cp_async = 0;
+    if (cp.mma && page_size < 8) {
+        if (rows * cp.sp.hkv >= (1ll << 32))   // pool rows must fit the producer's 32-bit row index
+            return FD_ERR_UNSUPPORTED;
+        std::memset(&tmk, 0, sizeof tmk);
+        std::memset(&tmv, 0, sizeof tmv);
+        cp.sp.cp_async = 1;
+        cp.sp.k_pool = static_cast<const uint8_t *>(k_pages);
+        cp.sp.v_pool = static_cast<const uint8_t *>(v_pages);
+        cp.sp.box4d = 0;
+        cp.sp.box_rows_log2 = 6;   // the consumers' layout: one 64-row box per 128-byte part
+        return run(cp, true, tmk, tmv, opts);
+    }
     // Pages of 1 or 2 tokens (CUDA-core consumers): gather a tile's rows four
     // per load when the (page, token, kv head) row index fits int32; one box
     // per page otherwise, with FD_FLAG_NO_GATHER, or if the driver rejects the

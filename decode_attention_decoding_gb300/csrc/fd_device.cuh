@@ -108,6 +108,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, uint
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), with an L2 policy.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "l"(policy)
+                 : "memory");
+}
+
+// One arrive on `bar` once every cp.async this thread issued before has
+// landed; the barrier's expected count already includes it (no increment).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Four rows of a 2-D tensor map (rows r0..r3, columns from c0, one box
 // {columns, 1} each) gathered into four consecutive box-sized slots at dst,
 // completing on `bar`.

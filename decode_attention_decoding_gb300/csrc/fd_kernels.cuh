@@ -38,7 +38,14 @@ namespace fd {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kSplitThreads = kConsumerThreads + 32;
+// Producer warps: one issues TMA loads; copying small pages with cp.async
+// (the split kernel's CPA instances) takes four.  Twelve warps still put at
+// most 3 on each SM sub-partition, so the consumers keep 168 registers a
+// thread; the other instances keep the smaller block, which leaves registers
+// for the merge CTAs that launch early beside it.
+constexpr int kProducerWarps = 4;
+constexpr int kSplitThreads = kConsumerThreads + 32;                       // one producer warp
+constexpr int kSplitThreadsCpAsync = kConsumerThreads + 32 * kProducerWarps;
 constexpr int kPairs = kConsumerWarps / 2;
 constexpr int kPartBytes = kTileTokens * 128;           // 64 rows x 128 bytes: one swizzled part
 constexpr int kMaxStages = 16;
@@ -83,6 +90,11 @@ __host__ __device__ constexpr int reduction_floats(int cons, int group, int d)
                                 : kConsumerWarps * group * (d + 2);
 }
 
+// Full-barrier arrivals per tile when the producers use cp.async: one
+// (asynchronous) per producer lane, plus the first producer's lane 0 after it
+// writes the tile's metadata.
+constexpr int kCpAsyncArrivals = 32 * kProducerWarps + 1;
+
 // Per-tile metadata flags, written by the producer into shared memory.
 enum : int { kFirstInCta = 1, kLastInCta = 2, kOwnSegment = 4 };
 
@@ -123,6 +135,12 @@ struct SplitParams {
     // a tile's rows are gathered four per load (row of token o of page e for
     // kv head h: (e * P + o) * Hkv + h); 0 for one box per page.
     int gather4;
+    // Paged with pages under 8 tokens on the tensor-core consumers: 1 when the
+    // producers copy each valid row of a tile with per-thread 16-byte cp.async
+    // straight into the swizzled layout (no tensor maps), from the pools
+    // below.  The full barriers then expect kCpAsyncArrivals arrivals.
+    int cp_async;
+    const uint8_t *k_pool, *v_pool;   // [num_pages, P, Hkv, D] (cp_async only)
     // Query columns of a launch head (see col_info): the caller's q is
     // [B, q_len, Hq, dh], and a launch head is fuse_f adjacent kv heads of
     // the caller read as one row of D elements (fused heads, tensor-core path
@@ -225,13 +243,14 @@ __device__ __forceinline__ bool consumer_sync(uint32_t cbar, uint32_t &cph, uint
 }
 
 // prefix[b] = Hkv * (tiles of requests < b), prefix[B] = total tiles.
-// All kSplitThreads threads take part.  scan_tmp: kSplitThreads/32 ints.
+// All NTHREADS threads of the block take part.  scan_tmp: NTHREADS / 32 ints.
+template <int NTHREADS>
 __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, int *scan_tmp)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kWarps = kSplitThreads / 32;
+    constexpr int nthreads = NTHREADS, kWarps = nthreads / 32;
     const int B = p.batch;
-    const int per = ceil_div(B, kSplitThreads);
+    const int per = ceil_div(B, nthreads);
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
     const bool report = blockIdx.x == 0;
     int local = 0;
@@ -264,15 +283,26 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
         prefix[b] = run * p.hkv;
         run += ceil_div(load_len(p, b, false), kTileTokens);
     }
-    if (tid == kSplitThreads - 1)
+    if (tid == nthreads - 1)
         prefix[B] = run * p.hkv;
     __syncthreads();
     if (blockIdx.x == 0)
-        for (int b = tid; b <= B; b += kSplitThreads)
+        for (int b = tid; b <= B; b += nthreads)
             p.ws_prefix[b] = prefix[b];
 }
 
 // ------------------------------------------------------------------ producer
+
+// Byte address of 16-byte chunk `chunk` (0 .. row bytes / 16 - 1) of `row`
+// in a swizzled tile made of boxes of 2^rl rows, each box laid out
+// [128-byte part][row][128 B].  With rl = 6 (one 64-row box per part) the
+// tile is PARTS parts of 8 KB.
+template <int PARTS>
+__device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk, int rl)
+{
+    const int rb = row >> rl, rr = row & ((1 << rl) - 1);
+    return tile + ((((rb * PARTS) + (chunk >> 3)) << rl) + rr) * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
 
 template <bool PAGED, bool SW128, int D, int KV>
 __device__ __forceinline__ void split_producer(const SplitParams &p, const CUtensorMap *tmk,
@@ -477,6 +507,160 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     // Before leaving, wait (bounded) for every load still in flight so no
     // asynchronous copy outlives the CTA's shared memory.
     if (lane == 0) {
+        for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
+            mbar_wait_bounded(full0 + 8 * (k % NS), (uint32_t)((k / NS) & 1), p.timeout_ns, nullptr);
+    }
+}
+
+// Producer for pages under 8 tokens on the tensor-core consumers: no TMA.
+// All kProducerWarps warps walk the CTA's tiles in the order split_producer
+// does; warp pw copies tile rows 16 pw .. 16 pw + 15 that hold valid tokens
+// with per-thread 16-byte cp.async, straight into the 128-byte swizzled
+// layout the consumers read (TMA page boxes of fewer than 8 rows cannot land
+// on the swizzle's 1 KB boundaries).  For each row, lanes 0-15 copy its K
+// chunks and lanes 16-31 its V chunks.  The full barrier of a stage expects
+// kCpAsyncArrivals arrivals: one per producer lane once its copies have
+// landed, and warp 0's lane 0 after it writes the tile's metadata.
+template <bool SW128, int D, int KV>
+__device__ __forceinline__ void split_producer_cpa(const SplitParams &p, uint32_t stage0, const int *prefix,
+                                                   int *meta, uint32_t full0, uint32_t empty0,
+                                                   volatile int *abort_flag, int t_begin, int t_end, int lane,
+                                                   int pw)
+{
+    using HD = Shape<D, KV>;
+    constexpr int kChunks = HD::kRowBytes / 16;
+    constexpr int kRowsPerProducer = kTileTokens / kProducerWarps;   // 16
+    const uint64_t policy = l2_policy_evict_first();
+    const int NS = p.num_stages;
+    const int P = p.page_size, page_log2 = p.page_log2;   // P = 1, 2 or 4
+    const bool lead = pw == 0 && lane == 0;
+    const bool starve = (p.flags & 1u) && blockIdx.x == 0;   // test hook: the first tile never completes
+    const int r_begin = pw * kRowsPerProducer;
+
+    int t = t_begin;
+    int b = request_of_tile(prefix, p.batch, t);
+    int nb = (prefix[b + 1] - prefix[b]) / p.hkv;
+    int h = (t - prefix[b]) / nb;
+    int j = (t - prefix[b]) - h * nb;
+    int L = load_len(p, b, false);
+
+    // Block-table entries of request b, pages win_base .. win_base + 127: lane
+    // l holds entry win_base + l + 32 k in e[k].  The window advances 32
+    // entries at a time and loads the fourth block ahead, so a tile's (at most
+    // 64) pages, which start in block 0, are read from blocks 0-2 only.
+    int win_b = -1, win_base = 0;
+    int e[4] = {0, 0, 0, 0};
+    auto table_load = [&](int idx) -> int {
+        return idx < p.max_blocks ? __ldg(p.block_table + (size_t)b * p.max_blocks + idx) : 0;
+    };
+
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0;
+    for (; t < t_end; ++t) {
+        if (!warp_wait(empty0 + 8 * s, ph ^ 1u, p.timeout_ns, abort_flag)) {
+            if (lead) {
+                atomicOr(p.ws_err, kErrTimeout);
+                *abort_flag = 1;
+            }
+            break;
+        }
+        const int seg_first = prefix[b] + h * nb;
+        const int token0 = j * kTileTokens;
+        const int nvalid = min(kTileTokens, L - token0);
+        const uint32_t full = full0 + 8 * s;
+        const uint32_t kdst = stage0 + s * HD::kStageBytes;
+        const uint32_t vdst = kdst + HD::kTileBytes;
+        if (lead) {
+            int flags = 0;
+            if (j == 0 || t == t_begin)
+                flags |= kFirstInCta;
+            if (j == nb - 1 || t == t_end - 1)
+                flags |= kLastInCta;
+            if (seg_first >= t_begin && seg_first + nb <= t_end)
+                flags |= kOwnSegment;
+            int *m = meta + s * kMetaInts;
+            m[0] = b;
+            m[1] = h;
+            m[2] = L - token0;
+            m[3] = nvalid;
+            m[4] = flags;
+            m[5] = b * p.hkv + h;
+            if (!(starve && issued == 0))
+                mbar_arrive(full);
+        }
+
+        const int pg0 = token0 >> page_log2;
+        if (b != win_b || pg0 < win_base || pg0 >= win_base + 128) {
+            win_b = b;
+            win_base = pg0 & ~31;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                e[k] = table_load(win_base + 32 * k + lane);
+        }
+        while (pg0 >= win_base + 32) {
+            e[0] = e[1];
+            e[1] = e[2];
+            e[2] = e[3];
+            win_base += 32;
+            e[3] = table_load(win_base + 96 + lane);
+        }
+        // lane l: the pool row of tile row r_begin + (l & 15) (rows past the
+        // request's end stand in for its last row; never copied)
+        uint32_t prow;
+        {
+            const int tok = token0 + min(r_begin + (lane & 15), nvalid - 1);
+            const int idx = (tok >> page_log2) - win_base;   // 0 .. 94
+            const int src = idx & 31;
+            const int x0 = __shfl_sync(0xffffffffu, e[0], src), x1 = __shfl_sync(0xffffffffu, e[1], src);
+            const int x2 = __shfl_sync(0xffffffffu, e[2], src);
+            int pe = idx < 32 ? x0 : (idx < 64 ? x1 : x2);
+            if (idx < 0 || idx >= 96 || pe < 0 || pe >= p.num_pages) {
+                atomicOr(p.ws_err, kErrPage);
+                pe = 0;
+            }
+            prow = (uint32_t)(((size_t)pe * P + (tok & (P - 1))) * p.hkv + h);   // < 2^32: checked on the host
+        }
+        const uint8_t *pool = lane < 16 ? p.k_pool : p.v_pool;
+        const uint32_t dst0 = lane < 16 ? kdst : vdst;
+        const int r_end = min(nvalid, r_begin + kRowsPerProducer);
+#pragma unroll 8
+        for (int r = r_begin; r < r_end; ++r) {
+            const uint32_t row = __shfl_sync(0xffffffffu, prow, r - r_begin);
+            const uint8_t *src = pool + (size_t)row * HD::kRowBytes;
+#pragma unroll
+            for (int c = lane & 15; c < kChunks; c += 16) {
+                uint32_t dst;
+                if constexpr (SW128)
+                    dst = sw128_addr<HD::kParts>(dst0, r, c, 6);
+                else
+                    dst = dst0 + r * HD::kRowBytes + c * 16;
+                cp_async_16(dst, src + c * 16, policy);
+            }
+        }
+        cp_async_mbar_arrive_noinc(full);
+
+        ++issued;
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+        if (t + 1 < t_end && ++j == nb) {
+            j = 0;
+            if (++h == p.hkv) {
+                h = 0;
+                do {
+                    ++b;
+                } while (b < p.batch && prefix[b + 1] == prefix[b]);
+                nb = (prefix[b + 1] - prefix[b]) / p.hkv;
+                L = load_len(p, b, false);
+            }
+        }
+    }
+    // Before leaving: this lane's own copies, then (bounded) every stage still
+    // in flight, so no copy outlives the CTA's shared memory.
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (lead) {
         for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
             mbar_wait_bounded(full0 + 8 * (k % NS), (uint32_t)((k / NS) & 1), p.timeout_ns, nullptr);
     }
@@ -816,16 +1000,6 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 // second.  On two paired kv heads, warp 2i + j owns head j outright: its
 // columns, its half of the row for q.K^T and for P.V.
 
-// Byte address of 16-byte chunk `chunk` (0 .. row bytes / 16 - 1) of `row`
-// in a swizzled tile made of boxes of 2^rl rows, each box laid out
-// [128-byte part][row][128 B].  With rl = 6 (one 64-row box per part) the
-// tile is PARTS parts of 8 KB.
-template <int PARTS>
-__device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int row, int chunk, int rl)
-{
-    const int rb = row >> rl, rr = row & ((1 << rl) - 1);
-    return tile + ((((rb * PARTS) + (chunk >> 3)) << rl) + rr) * 128 + (((chunk & 7) ^ (row & 7)) << 4);
-}
 
 // FP8 caches on the tensor cores.  K and V stay FP8 codes in shared memory
 // and are converted to fp16 pairs in registers (exactly), so the products run
@@ -1223,11 +1397,15 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 
 // ------------------------------------------------------------------ kernels
 
-template <int G, bool PAGED, int CONS, int KV, int D>
-__global__ void __launch_bounds__(kSplitThreads, 1)
+// CPA: paged with pages under 8 tokens on the tensor-core consumers, rows
+// copied by kProducerWarps warps with cp.async (split_producer_cpa).
+template <int G, bool PAGED, int CONS, int KV, int D, bool CPA>
+__global__ void __launch_bounds__(CPA ? kSplitThreadsCpAsync : kSplitThreads, 1)
     split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv)
 {
+    static_assert(!CPA || (PAGED && CONS != kConsCudaCores), "cp.async copies feed paged tensor-core launches");
+    constexpr int kThreads = CPA ? kSplitThreadsCpAsync : kSplitThreads;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -1242,7 +1420,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < p.num_stages; ++s) {
-            mbar_init(full0 + 8 * s, 1);
+            mbar_init(full0 + 8 * s, CPA ? kCpAsyncArrivals : 1);
             mbar_init(empty0 + 8 * s, kConsumerWarps);
         }
         mbar_init(cbar, kConsumerWarps);
@@ -1257,7 +1435,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     // early part reads the lengths, which the kernels before this one (now
     // complete) may have written.
     pdl_launch_dependents();
-    build_prefix(p, prefix, misc + 1);   // ends with __syncthreads
+    build_prefix<kThreads>(p, prefix, misc + 1);   // ends with __syncthreads
 
     const int T = prefix[p.batch];
     int t_begin, t_end;
@@ -1265,9 +1443,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     if (t_begin >= t_end)
         return;
     volatile int *abort_flag = misc;
-    if (warp == kConsumerWarps)
-        split_producer<PAGED, CONS != kConsCudaCores, D, KV>(p, &tmk, &tmv, stage0, prefix, meta, full0,
-                                                             empty0, abort_flag, t_begin, t_end, lane);
+    if (warp >= kConsumerWarps) {
+        if constexpr (CPA)
+            split_producer_cpa<true, D, KV>(p, stage0, prefix, meta, full0, empty0, abort_flag, t_begin, t_end,
+                                            lane, warp - kConsumerWarps);
+        else
+            split_producer<PAGED, CONS != kConsCudaCores, D, KV>(p, &tmk, &tmv, stage0, prefix, meta, full0,
+                                                                 empty0, abort_flag, t_begin, t_end, lane);
+    }
     else if constexpr (CONS != kConsCudaCores)
         split_consumer_mma<G, KV, D, CONS == kConsMmaPair>(p, smem, stage0, meta, full0, empty0, cbar,
                                                            abort_flag, t_begin, t_end, warp, lane);

@@ -33,7 +33,7 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
 cudaError_t launch_merge(int group, int head_dim, const MergeParams &p, int grid, cudaStream_t stream);
 
 // Shared by the split translation units.
-template <int G, bool PAGED, int CONS, int KV, int D>
+template <int G, bool PAGED, int CONS, int KV, int D, bool CPA = false>
 cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const SplitLaunch &c)
 {
@@ -46,7 +46,7 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
         return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(split_kernel<G, PAGED, CONS, KV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(split_kernel<G, PAGED, CONS, KV, D, CPA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)c.smem_optin);
         if (e != cudaSuccess)
             return e;
@@ -59,12 +59,12 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)c.grid);
-    cfg.blockDim = dim3(kSplitThreads);
+    cfg.blockDim = dim3(CPA ? kSplitThreadsCpAsync : kSplitThreads);
     cfg.dynamicSmemBytes = c.smem_bytes;
     cfg.stream = c.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, CONS, KV, D>, p, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, CONS, KV, D, CPA>, p, tmk, tmv);
 }
 
 // One split-kernel variant per (layout, K/V element type, row dims D):
@@ -76,6 +76,18 @@ template <bool PAGED, int KV, int D>
 cudaError_t launch_split_variant(int cons, int group, const SplitParams &p, const CUtensorMap &tmk,
                                  const CUtensorMap &tmv, const SplitLaunch &c)
 {
+    if (cons == kConsMma && p.cp_async) {   // pages under 8 tokens: rows copied with cp.async
+        if constexpr (PAGED && Shape<D, KV>::kParts >= 1) {
+            switch (group) {
+            case 2: return launch_split_t<2, PAGED, kConsMma, KV, D, true>(p, tmk, tmv, c);
+            case 4: return launch_split_t<4, PAGED, kConsMma, KV, D, true>(p, tmk, tmv, c);
+            case 8: return launch_split_t<8, PAGED, kConsMma, KV, D, true>(p, tmk, tmv, c);
+            case 16: return launch_split_t<16, PAGED, kConsMma, KV, D, true>(p, tmk, tmv, c);
+            default: return cudaErrorInvalidValue;
+            }
+        }
+        return cudaErrorInvalidValue;
+    }
     if (cons == kConsMma) {
         if constexpr (Shape<D, KV>::kParts >= 1) {
             switch (group) {

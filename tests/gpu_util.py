@@ -101,3 +101,13 @@ def sample_items(w, n, seed=0):
     while len(pairs) < min(n, B * hq):
         pairs.add((int(rng.integers(B)), int(rng.integers(hq))))
     return np.array([[b, h, 0, -1] for b, h in sorted(pairs)], dtype=np.int32)
+
+
+def small_page_twin_flags(w):
+    """Flags that make a contiguous run of w take the consumers that a paged
+    run with pages under 8 tokens takes, so the two agree bitwise: the
+    unfused tensor-core consumers when a kv head has 2 or more query columns
+    (G x q_len) and a row holds at least 128 bytes, else CUDA cores."""
+    cols = (w.num_q_heads // w.num_kv_heads) * w.q_len
+    row_bytes = w.head_dim * w.kv_elem_bytes
+    return 0x8 if cols >= 2 and row_bytes >= 128 else 0x2   # FD_FLAG_NO_HEAD_FUSION / FD_FLAG_CUDA_CORES

@@ -169,10 +169,17 @@ def test_paged_argument_checks(lib, fd):
     assert call_paged(lib, page=2, d=64, opts=ctypes.byref(fp8), wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
     assert call_paged(lib, page=1, d=64, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL   # bf16: 128 bytes
     assert call_paged(lib, page=96) == E.FD_ERR_UNSUPPORTED
-    # over 8 columns need the tensor-core consumers, which need pages of at least 8 tokens
+    # over 8 columns need the tensor-core consumers (any page size; pages under 8
+    # tokens are copied with cp.async), which a 64-dim FP8 head reaches only by
+    # pairing kv heads, and pairing needs pages of at least 8 tokens
     many = fd.FdOptions(0, 0, 0, None, None, 0, 0, 0.0, 0.0, 2)
-    assert call_paged(lib, page=4, hq=16, opts=ctypes.byref(many)) == E.FD_ERR_UNSUPPORTED
+    assert call_paged(lib, page=4, hq=16, opts=ctypes.byref(many), wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
     assert call_paged(lib, page=8, hq=16, opts=ctypes.byref(many), wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
+    many_cc = fd.FdOptions(0, 0x2, 0, None, None, 0, 0, 0.0, 0.0, 2)
+    assert call_paged(lib, page=8, hq=16, opts=ctypes.byref(many_cc)) == E.FD_ERR_UNSUPPORTED
+    many_fp8 = fd.FdOptions(0, 0, 0, None, None, 0, 1, 0.0, 0.0, 2)
+    assert call_paged(lib, page=4, hq=16, d=64, opts=ctypes.byref(many_fp8)) == E.FD_ERR_UNSUPPORTED
+    assert call_paged(lib, page=8, hq=16, d=64, opts=ctypes.byref(many_fp8), wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
     lens = (ctypes.c_int32 * 2)(64, 65)                     # capacity 4 pages * 16
     assert call_paged(lib, slh=lens) == E.FD_ERR_INVALID_ARG
     assert call_paged(lib, wsb=100) == E.FD_ERR_WORKSPACE_TOO_SMALL

@@ -6,7 +6,7 @@ import pytest
 
 import fd_synth as syn
 import oracle
-from gpu_util import check, contig_to_paged, run
+from gpu_util import check, contig_to_paged, run, small_page_twin_flags
 
 pytestmark = pytest.mark.gpu
 
@@ -37,8 +37,8 @@ def test_f16_contiguous_vs_oracle(group, flags):
 def test_f16_paged_vs_oracle_and_contiguous(page, group):
     w = syn.make_contiguous(820 + page, len(RAGGED), 2 * group, 2, 128, 1024, RAGGED, dtype="f16")
     wp = contig_to_paged(w, page, perm_seed=page, poison=True)
-    # pages under 8 tokens always take the unfused CUDA-core consumers
-    flags = CUDA_CORES if page < 8 else 0
+    # pages under 8 tokens take unfused consumers (tensor cores for GQA)
+    flags = small_page_twin_flags(w) if page < 8 else 0
     op, lp = run(wp, num_ctas=5)
     ro, rl = oracle.attend(wp, threads=8)
     check(op, lp, ro, rl, f"f16 paged P={page} G={group}")

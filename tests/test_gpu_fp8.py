@@ -10,7 +10,7 @@ import torch
 
 import fd_synth as syn
 import oracle
-from gpu_util import check, contig_to_paged, run
+from gpu_util import check, contig_to_paged, run, small_page_twin_flags
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +56,7 @@ def test_paged_vs_oracle_and_contiguous(fmt, d, group, page):
     w = syn.make_contiguous(1700 + d + page, len(RAGGED), 2 * group, 2, d, 1024, RAGGED, kv_dtype=fmt,
                             k_scale=SCALES[0], v_scale=SCALES[1])
     wp = contig_to_paged(w, page, perm_seed=page + d, poison=True)
-    flags = CUDA_CORES if page < 8 else 0
+    flags = small_page_twin_flags(w) if page < 8 else 0
     ro, rl = oracle.attend(wp, threads=8)
     for ctas in (0, 5):
         op, lp = run(wp, num_ctas=ctas)

@@ -10,7 +10,7 @@ import pytest
 
 import fd_synth as syn
 import oracle
-from gpu_util import check, contig_to_paged, run
+from gpu_util import check, contig_to_paged, run, small_page_twin_flags
 
 pytestmark = pytest.mark.gpu
 
@@ -44,8 +44,8 @@ def test_contiguous_vs_oracle(d, group, flags):
 def test_paged_vs_oracle_and_contiguous(d, page, group):
     w = syn.make_contiguous(950 + d + page, len(RAGGED), 2 * group, 2, d, 1024, RAGGED)
     wp = contig_to_paged(w, page, perm_seed=page + d, poison=True)
-    # pages under 8 tokens always take the unfused CUDA-core consumers
-    flags = CUDA_CORES if page < 8 else 0
+    # pages under 8 tokens take unfused consumers (tensor cores for GQA)
+    flags = small_page_twin_flags(w) if page < 8 else 0
     ro, rl = oracle.attend(wp, threads=8)
     for ctas in (0, 5):
         op, lp = run(wp, num_ctas=ctas)

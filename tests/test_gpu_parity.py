@@ -9,7 +9,7 @@ import torch
 
 import fd_synth as syn
 import oracle
-from gpu_util import check, contig_to_paged, run, sample_items, to_device
+from gpu_util import check, contig_to_paged, run, sample_items, to_device, small_page_twin_flags
 
 pytestmark = pytest.mark.gpu
 
@@ -44,8 +44,8 @@ def test_paged_vs_oracle_and_contiguous(page, group):
     hkv = 2
     w = syn.make_contiguous(300 + page, len(RAGGED), hkv * group, hkv, 128, 1024, RAGGED)
     wp = contig_to_paged(w, page, perm_seed=page + group)
-    # pages under 8 tokens always take the unfused CUDA-core consumers
-    flags = CUDA_CORES if page < 8 else 0
+    # pages under 8 tokens take unfused consumers (tensor cores for GQA)
+    flags = small_page_twin_flags(w) if page < 8 else 0
     for ctas in (0, 5):
         op, lp = run(wp, num_ctas=ctas)
         ro, rl = oracle.attend(wp, threads=8)

@@ -10,7 +10,7 @@ import torch
 
 import fd_synth as syn
 import oracle
-from gpu_util import check, contig_to_paged, run
+from gpu_util import check, contig_to_paged, run, small_page_twin_flags
 
 pytestmark = pytest.mark.gpu
 
@@ -103,7 +103,7 @@ def test_head_dims(d, group, q_len):
 def test_paged_vs_oracle_and_contiguous(group, q_len, page):
     w = syn.make_contiguous(2300 + page + q_len, len(LENS), 2 * group, 2, 128, 1024, LENS, q_len=q_len)
     wp = contig_to_paged(w, page, perm_seed=page, poison=True)
-    flags = CUDA_CORES if page < 8 else 0
+    flags = small_page_twin_flags(w) if page < 8 else 0
     ro, rl = oracle.attend(wp, threads=8)
     for ctas in (0, 5):
         op, lp = run(wp, num_ctas=ctas)

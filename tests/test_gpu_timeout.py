@@ -11,15 +11,18 @@ from gpu_util import check, run, to_device
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("paged", [False, True])
-def test_starved_wait_times_out_and_context_survives(paged):
+# page 0: contiguous (TMA); 16: page boxes (TMA); 4: rows copied with cp.async
+# on the tensor-core consumers; 1 with one query head per kv head: gathered rows
+@pytest.mark.parametrize("page,group", [(0, 4), (16, 4), (4, 4), (1, 1)])
+def test_starved_wait_times_out_and_context_survives(page, group):
     import decode_attention_decoding_gb300 as fd
     from gpu_util import contig_to_paged
-    w = syn.make_contiguous(600, 2, 8, 2, 128, 2000, [2000, 777])
+    paged = page > 0
+    w = syn.make_contiguous(600, 2, 2 * group, 2, 128, 2000, [2000, 777])
     if paged:
-        w = contig_to_paged(w, 16, perm_seed=3)
+        w = contig_to_paged(w, page, perm_seed=3)
     d = to_device(w)
-    ws = fd.make_workspace(2, 8, 2, 128, 2000, 16 if paged else 0)
+    ws = fd.make_workspace(2, 2 * group, 2, 128, 2000, page)
     kw = dict(scale=w.scale, workspace=ws, num_ctas=4, flags=fd.FD_FLAG_TEST_STARVE_FIRST_TILE,
               wait_timeout_ns=50_000_000)
     if paged:
