@@ -41,9 +41,9 @@
  *     tokens per request q_len (fd_options.q_len) with G * q_len <= 16;
  *     batch <= 4096.  Other shapes return FD_ERR_UNSUPPORTED.  Over 8 query
  *     columns (G * q_len > 8) run on the tensor-core consumers only, so they
- *     also return FD_ERR_UNSUPPORTED with FD_FLAG_CUDA_CORES, with pages of
- *     under 8 tokens, and for an FP8 cache with head_dim 64 when the kv heads
- *     cannot be paired (odd Hkv, or FD_FLAG_NO_HEAD_FUSION).
+ *     also return FD_ERR_UNSUPPORTED with FD_FLAG_CUDA_CORES, and for an FP8
+ *     cache with head_dim 64 when the kv heads cannot be paired (odd Hkv,
+ *     FD_FLAG_NO_HEAD_FUSION, or pages under 8 tokens).
  *   - Several new tokens (q_len > 1, e.g. checking draft tokens): the cache
  *     of length L already holds them, q is [batch, q_len, Hq, head_dim], and
  *     new token i (0-based) attends causally to positions 0 .. L - q_len + i.
