@@ -259,9 +259,8 @@ struct CallPlan {
 // 128-byte swizzled part.  Pages of 8 tokens or more arrive by TMA (every
 // page box starts on a 1 KB swizzle boundary); smaller pages are copied row
 // by row with cp.async into the same swizzled layout.
-bool use_mma(int group, int page_size, int row_bytes, const fd_options *opts)
+bool use_mma(int group, int row_bytes, const fd_options *opts)
 {
-    (void)page_size;
     if (opts && (opts->flags & FD_FLAG_CUDA_CORES))
         return false;
     return group >= 2 && row_bytes >= 128;
@@ -466,9 +465,9 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     cp->kv = kv;
     cp->merge_group = slots;
     cp->merge_dim = merge_dim;
-    cp->mma = paired || use_mma(group, page_size, eb * d, opts);
+    cp->mma = paired || use_mma(group, eb * d, opts);
     cp->cons = paired ? kConsMmaPair : (cp->mma ? kConsMma : kConsCudaCores);
-    if (fuse > 1 && !use_mma(2, page_size, eb * d, opts))
+    if (fuse > 1 && !use_mma(2, eb * d, opts))
         return FD_ERR_UNSUPPORTED;   // fusion is defined for the tensor-core consumers only
     if (!cp->mma && group > kMaxColumnsCudaCores)
         return FD_ERR_UNSUPPORTED;   // over 8 columns need the tensor-core consumers
