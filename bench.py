@@ -92,16 +92,20 @@ def consumers_label(args, w) -> str:
     G = w.num_q_heads // w.num_kv_heads
     fp8 = w.kv_dtype is not None
     row = w.head_dim * (1 if fp8 else 2)
-    if args.cuda_cores or (w.paged and w.page_size < 8):
+    mma = "mma.sync fp16 on FP8 codes" if fp8 else "mma.sync bf16"
+    if args.cuda_cores:
         return "cuda cores"
+    if w.paged and w.page_size < 8:   # no fusion; rows copied or gathered
+        if G >= 2 and row >= 128:
+            return f"tensor cores ({mma}), rows copied with cp.async"
+        return "cuda cores" + (", rows gathered four per TMA load" if w.page_size <= 2 else "")
     short = row < 256 or (w.paged and w.page_size < 64)
     tiles = sum((int(L) + 63) // 64 for L in w.seq_lens) * w.num_kv_heads
     long_call = tiles / 152 >= 24
-    fused = short and long_call and any(f * w.head_dim <= 256 and f * G <= 8 and w.num_kv_heads % f == 0
-                                        for f in (2, 4))
-    if G == 1 and not fused:
+    fused = short and long_call and any(f * w.head_dim <= 256 and w.num_kv_heads % f == 0 and
+                                        (G <= 16 if f == 2 else 4 * G <= 8) for f in (2, 4))
+    if (G == 1 or row < 128) and not fused:
         return "cuda cores"
-    mma = "mma.sync fp16 on FP8 codes" if fp8 else "mma.sync bf16"
     return f"tensor cores ({mma})" + (", fused kv heads" if fused else "")
 
 
@@ -125,6 +129,15 @@ def kernel_hash():
     for f in KERNEL_SOURCES:
         h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def bench_workload(args):
+    """The workload the arguments name: one of the five configurations, with
+    an FP8 cache (--kv) and re-paged into pages of --page tokens when asked."""
+    w = syn.make_config(args.config, kv_dtype=args.kv if args.kv != "bf16" else None)
+    if args.page:
+        w = syn.repage(w, args.page, perm_seed=syn.seed_for(args.config, syn.TENSOR_PERM) + args.page)
+    return w
 
 
 def measured_peaks():
@@ -213,7 +226,7 @@ def run_ours(args, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    w = syn.make_config(args.config, kv_dtype=args.kv if args.kv != "bf16" else None)
+    w = bench_workload(args)
     B, hq, d = w.q.shape
     hkv = w.num_kv_heads
     fp8 = w.kv_dtype is not None
@@ -340,7 +353,8 @@ def run_ours(args, rank, world):
     traffic = None
     try:
         tj = json.load(open(TRAFFIC_FILE))
-        if tj.get("kernel_hash") == kernel_hash() and tj.get("workload") == syn.CONFIG_NAMES[args.config]:
+        if (tj.get("kernel_hash") == kernel_hash() and tj.get("workload") == syn.CONFIG_NAMES[args.config]
+                and not args.page and args.kv == "bf16"):
             traffic = tj.get("traffic_bytes_per_launch")
     except Exception:
         pass
@@ -487,7 +501,7 @@ def run_reference(args, rank, world):
         return
     import oracle
     oracle.build()
-    w = syn.make_config(args.config, kv_dtype=args.kv if args.kv != "bf16" else None)
+    w = bench_workload(args)
     threads = os.cpu_count() or 1
     total_rows = w.batch * w.num_q_heads
     budget = max(1.0, args.reference_budget_s / max(1, args.steps + args.warmup))
@@ -523,6 +537,9 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3", "e5m2"],
                     help="K/V cache element type (FP8 caches are quantised from the same values)")
+    ap.add_argument("--page", type=int, default=0,
+                    help="re-page the workload's K/V into shuffled pages of this many tokens "
+                         "(a divisor of 64 or a multiple of 64; 0 keeps its own layout)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-e2e", action="store_true")

@@ -33,7 +33,7 @@ from __future__ import annotations
 
 import os
 from concurrent.futures import ThreadPoolExecutor
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace as dc_replace
 import math
 
 import numpy as np
@@ -472,3 +472,31 @@ def make_config(config_id: int, kv_dtype: str | None = None) -> Workload:
         w.meta["scaled_tokens"] = toks
         return w
     raise ValueError(config_id)
+
+
+def repage(w: Workload, page: int, perm_seed: int, extra_pages: int = 3) -> Workload:
+    """The same logical K/V (contiguous or paged) in pages of `page` tokens,
+    shuffled by the seeded permutation; unreferenced pages are zero.  Pure
+    layout (no attention arithmetic); vectorised, for full-size workloads."""
+    lens = np.asarray(w.seq_lens, dtype=np.int64)
+    B = len(lens)
+    b_idx = np.repeat(np.arange(B), lens)
+    t_idx = np.concatenate([np.arange(L) for L in lens]) if B else np.zeros(0, np.int64)
+    if w.page_size:
+        P0 = w.page_size
+        src = (w.block_table[b_idx, t_idx // P0].astype(np.int64), t_idx % P0)
+    else:
+        src = (b_idx, t_idx)
+    used = int(sum((int(L) + page - 1) // page for L in lens))
+    n_pages = used + extra_pages
+    perm = permutation(perm_seed, n_pages)
+    max_blocks = max(1, (int(lens.max()) + page - 1) // page)
+    table = build_block_table(lens.astype(np.int32), page, max_blocks, perm)
+    dst = (table[b_idx, t_idx // page].astype(np.int64), t_idx % page)
+    hkv, d = w.k.shape[-2], w.k.shape[-1]
+    kp = np.zeros((n_pages, page, hkv, d), w.k.dtype)
+    vp = np.zeros((n_pages, page, hkv, d), w.v.dtype)
+    kp[dst] = w.k[src]
+    vp[dst] = w.v[src]
+    return dc_replace(w, name=w.name + f"_p{page}", k=kp, v=vp, seq_lens=w.seq_lens.copy(),
+                               page_size=page, block_table=table)

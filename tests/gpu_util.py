@@ -111,3 +111,6 @@ def small_page_twin_flags(w):
     cols = (w.num_q_heads // w.num_kv_heads) * w.q_len
     row_bytes = w.head_dim * w.kv_elem_bytes
     return 0x8 if cols >= 2 and row_bytes >= 128 else 0x2   # FD_FLAG_NO_HEAD_FUSION / FD_FLAG_CUDA_CORES
+
+
+repage = syn.repage   # the same logical K/V in shuffled pages of another size

@@ -6,7 +6,7 @@ import pytest
 
 import fd_synth as syn
 import oracle
-from gpu_util import check, run, sample_items
+from gpu_util import check, repage, run, sample_items
 
 pytestmark = pytest.mark.gpu
 
@@ -44,4 +44,22 @@ def test_full_size_config_sampled(config_id, flags, kv):
         b, h = items[:, 0], items[:, 1]
         stats = check(o[b, h], l[b, h], ro, rl, f"config {config_id} kv={kv}")
     print(f"config {config_id} flags={flags} kv={kv}: max|dO|={stats[0]:.3g} max rel(|r|>=1e-2)={stats[1]:.3g} "
+          f"max|dLSE|={stats[2]:.3g}")
+
+
+# Small pages at full size: workload 4 on one-token pages (tensor cores with
+# cp.async rows; CUDA cores with gathered rows), workload 5 on four-token pages,
+# workload 2 (MHA) on two-token pages (gathered rows).
+@pytest.mark.parametrize("config_id,page,flags", [(4, 1, 0), (4, 1, 2), (5, 4, 0), (2, 2, 0)])
+def test_full_size_config_small_pages_sampled(config_id, page, flags):
+    from decode_attention_decoding_gb300 import build
+    build.build()
+    w = repage(workload(config_id), page, perm_seed=100 + page)
+    o, l = run(w, flags=flags)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+    items = sample_items(w, 24, seed=config_id + page)
+    ro, rl = oracle.attend(w, items=items, threads=16)
+    b, h = items[:, 0], items[:, 1]
+    stats = check(o[b, h], l[b, h], ro, rl, f"config {config_id} P={page} flags={flags}")
+    print(f"config {config_id} P={page} flags={flags}: max|dO|={stats[0]:.3g} max rel={stats[1]:.3g} "
           f"max|dLSE|={stats[2]:.3g}")

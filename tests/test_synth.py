@@ -172,3 +172,18 @@ def test_fp8_workload_is_seeded_and_scaled():
     assert w.k_scale == float(np.float32(0.05)) and w.kv_bytes() == 19 * 2 * 64 * 2
     # codes are x / scale: with k_scale 0.05, |code value| ~ 20 |x|
     assert 5 < np.median(np.abs(w.k.view(np.int8).astype(np.int64) & 0x7F)) < 127
+
+
+@pytest.mark.parametrize("page", [1, 2, 8, 64])
+def test_repage_keeps_every_logical_row(page):
+    """repage moves K/V rows between layouts without changing any (request,
+    position) row; page entries are distinct and the rest of the table is -1."""
+    w = syn.make_contiguous(41, 3, 4, 2, 64, 200, [200, 5, 0])
+    p = syn.repage(syn.repage(w, 4, perm_seed=1), page, perm_seed=2)
+    for b, L in enumerate(w.seq_lens):
+        for t in range(int(L)):
+            e = p.block_table[b, t // page]
+            assert np.array_equal(p.k[e, t % page], w.k[b, t]) and np.array_equal(p.v[e, t % page], w.v[b, t])
+        assert np.all(p.block_table[b, (int(L) + page - 1) // page:] == -1)
+    used = p.block_table[p.block_table >= 0]
+    assert len(set(used.tolist())) == len(used)
