@@ -96,7 +96,7 @@ static fd_status encode_kv_map_4d(CUtensorMap *map, const void *base, int hkv, l
 
 // A rank-2 view {d, rows} of a paged K or V pool whose rows are (page, token,
 // kv head) triples of d elements, with one-row boxes and no swizzle: the
-// CUDA-core consumers gather pages under 8 tokens four rows per load.
+// CUDA-core consumers gather pages of 1 or 2 tokens four rows per load.
 static fd_status encode_kv_rows_2d(CUtensorMap *map, const void *base, long long rows, int kv, int d)
 {
     EncodeTiledFn fn = encode_fn();

@@ -128,10 +128,11 @@ typedef struct fd_options {
 #define FD_FLAG_TEST_STARVE_FIRST_TILE 0x1u
 
 /* Use the CUDA-core consumers for every group size.  By default GQA groups
- * (Hq/Hkv >= 2, and paged pools with pages of at least 8 tokens) run q.K^T
- * and P.V on the tensor cores (bf16 MMA, fp32 accumulation, softmax weights
- * rounded to bf16 for P.V); this flag selects the all-fp32 CUDA-core
- * arithmetic instead. */
+ * (Hq/Hkv x q_len >= 2 query columns per kv head, rows of at least 128 bytes
+ * or kv heads paired to reach them) run q.K^T and P.V on the tensor cores
+ * (bf16 or fp16 MMA, fp32 accumulation, softmax weights rounded to the MMA
+ * type for P.V), with any page size; this flag selects the all-fp32 CUDA-core
+ * arithmetic instead (up to 8 query columns per kv head). */
 #define FD_FLAG_CUDA_CORES 0x2u
 
 /* Tensor-core consumers: load each 64-dim part of a K/V tile as its own TMA
