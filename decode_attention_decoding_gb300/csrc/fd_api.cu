@@ -253,6 +253,7 @@ struct CallPlan {
     int merge_group;  // merge kernel's columns per launch head
     int merge_dim;    // merge kernel's dims per column
     int kv;           // K/V element type (kKv*): bf16, fp16 (q of the same type) or FP8
+    bool cp_async;    // paged, pages under 8 tokens, tensor cores: rows copied with cp.async
 };
 
 // Tensor-core consumers serve GQA groups; a row must fill at least one
@@ -463,6 +464,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     cp->group = group;
     cp->head_dim = d;
     cp->kv = kv;
+    cp->cp_async = false;   // the paged entry point sets it for pages under 8 tokens
     cp->merge_group = slots;
     cp->merge_dim = merge_dim;
     cp->mma = paired || use_mma(group, eb * d, opts);
@@ -508,7 +510,8 @@ fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUte
     cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_end_event) : nullptr;
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    cudaError_t e = launch_split(paged, cp.kv, cp.head_dim, cp.cons, cp.group, cp.sp, tmk, tmv, cp.launch);
+    cudaError_t e = launch_split(paged, cp.kv, cp.head_dim, cp.cons, cp.group, cp.cp_async, cp.sp, tmk, tmv,
+                                 cp.launch);
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess)
@@ -648,13 +651,13 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     const long long rows = (long long)num_pages * page_size;
     // Pages under 8 tokens on the tensor-core consumers: the producer copies
     // rows with cp.async into the swizzled layout; no tensor maps.
-    cp.sp.cp_async = 0;
+    cp.cp_async = false;
     if (cp.mma && page_size < 8) {
         if (rows * cp.sp.hkv >= (1ll << 32))   // pool rows must fit the producer's 32-bit row index
             return FD_ERR_UNSUPPORTED;
         std::memset(&tmk, 0, sizeof tmk);
         std::memset(&tmv, 0, sizeof tmv);
-        cp.sp.cp_async = 1;
+        cp.cp_async = true;
         cp.sp.k_pool = static_cast<const uint8_t *>(k_pages);
         cp.sp.v_pool = static_cast<const uint8_t *>(v_pages);
         cp.sp.box4d = 0;

@@ -135,12 +135,9 @@ struct SplitParams {
     // a tile's rows are gathered four per load (row of token o of page e for
     // kv head h: (e * P + o) * Hkv + h); 0 for one box per page.
     int gather4;
-    // Paged with pages under 8 tokens on the tensor-core consumers: 1 when the
-    // producers copy each valid row of a tile with per-thread 16-byte cp.async
-    // straight into the swizzled layout (no tensor maps), from the pools
-    // below.  The full barriers then expect kCpAsyncArrivals arrivals.
-    int cp_async;
-    const uint8_t *k_pool, *v_pool;   // [num_pages, P, Hkv, D] (cp_async only)
+    // Paged with pages under 8 tokens on the tensor-core consumers (the CPA
+    // instances): the pools [num_pages, P, Hkv, D] the producers copy rows from.
+    const uint8_t *k_pool, *v_pool;
     // Query columns of a launch head (see col_info): the caller's q is
     // [B, q_len, Hq, dh], and a launch head is fuse_f adjacent kv heads of
     // the caller read as one row of D elements (fused heads, tensor-core path
@@ -521,7 +518,7 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
 // chunks and lanes 16-31 its V chunks.  The full barrier of a stage expects
 // kCpAsyncArrivals arrivals: one per producer lane once its copies have
 // landed, and warp 0's lane 0 after it writes the tile's metadata.
-template <bool SW128, int D, int KV>
+template <int D, int KV>
 __device__ __forceinline__ void split_producer_cpa(const SplitParams &p, uint32_t stage0, const int *prefix,
                                                    int *meta, uint32_t full0, uint32_t empty0,
                                                    volatile int *abort_flag, int t_begin, int t_end, int lane,
@@ -629,14 +626,8 @@ __device__ __forceinline__ void split_producer_cpa(const SplitParams &p, uint32_
             const uint32_t row = __shfl_sync(0xffffffffu, prow, r - r_begin);
             const uint8_t *src = pool + (size_t)row * HD::kRowBytes;
 #pragma unroll
-            for (int c = lane & 15; c < kChunks; c += 16) {
-                uint32_t dst;
-                if constexpr (SW128)
-                    dst = sw128_addr<HD::kParts>(dst0, r, c, 6);
-                else
-                    dst = dst0 + r * HD::kRowBytes + c * 16;
-                cp_async_16(dst, src + c * 16, policy);
-            }
+            for (int c = lane & 15; c < kChunks; c += 16)
+                cp_async_16(sw128_addr<HD::kParts>(dst0, r, c, 6), src + c * 16, policy);
         }
         cp_async_mbar_arrive_noinc(full);
 
@@ -1445,8 +1436,8 @@ __global__ void __launch_bounds__(CPA ? kSplitThreadsCpAsync : kSplitThreads, 1)
     volatile int *abort_flag = misc;
     if (warp >= kConsumerWarps) {
         if constexpr (CPA)
-            split_producer_cpa<true, D, KV>(p, stage0, prefix, meta, full0, empty0, abort_flag, t_begin, t_end,
-                                            lane, warp - kConsumerWarps);
+            split_producer_cpa<D, KV>(p, stage0, prefix, meta, full0, empty0, abort_flag, t_begin, t_end, lane,
+                                      warp - kConsumerWarps);
         else
             split_producer<PAGED, CONS != kConsCudaCores, D, KV>(p, &tmk, &tmv, stage0, prefix, meta, full0,
                                                                  empty0, abort_flag, t_begin, t_end, lane);

@@ -71,12 +71,16 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
 // consumers on CUDA cores (group 1 to 8), on tensor cores (group 2 to 16,
 // swizzled K/V maps, rows of at least 128 bytes), or on tensor cores with two
 // fused kv heads per row (group = columns per head, 1 to 16; D = 2 x head_dim).
+// cp_async: paged with pages under 8 tokens on the tensor cores (the CPA
+// instances, 384 threads; tensor-core groups only).
 // Returns cudaErrorInvalidValue for an unsupported combination.
 template <bool PAGED, int KV, int D>
-cudaError_t launch_split_variant(int cons, int group, const SplitParams &p, const CUtensorMap &tmk,
-                                 const CUtensorMap &tmv, const SplitLaunch &c)
+cudaError_t launch_split_variant(int cons, int group, bool cp_async, const SplitParams &p,
+                                 const CUtensorMap &tmk, const CUtensorMap &tmv, const SplitLaunch &c)
 {
-    if (cons == kConsMma && p.cp_async) {   // pages under 8 tokens: rows copied with cp.async
+    if (cp_async) {   // pages under 8 tokens on the tensor cores: rows copied with cp.async
+        if (cons != kConsMma)
+            return cudaErrorInvalidValue;
         if constexpr (PAGED && Shape<D, KV>::kParts >= 1) {
             switch (group) {
             case 2: return launch_split_t<2, PAGED, kConsMma, KV, D, true>(p, tmk, tmv, c);
@@ -130,7 +134,7 @@ cudaError_t launch_split_variant(int cons, int group, const SplitParams &p, cons
     FD_SPLIT_VARIANTS_KV(X, P, kKvE4m3) FD_SPLIT_VARIANTS_KV(X, P, kKvE5m2)
 #define FD_SPLIT_VARIANTS(X) FD_SPLIT_VARIANTS_P(X, false) FD_SPLIT_VARIANTS_P(X, true)
 #define FD_EXTERN_SPLIT(P, KV, D)                                                                \
-    extern template cudaError_t launch_split_variant<P, KV, D>(int, int, const SplitParams &, \
+    extern template cudaError_t launch_split_variant<P, KV, D>(int, int, bool, const SplitParams &, \
                                                               const CUtensorMap &,             \
                                                               const CUtensorMap &, const SplitLaunch &);
 FD_SPLIT_VARIANTS(FD_EXTERN_SPLIT)
@@ -138,13 +142,13 @@ FD_SPLIT_VARIANTS(FD_EXTERN_SPLIT)
 
 // Split launch for a call: layout, K/V element type (kKv*) and head_dim pick
 // the variant.  Returns cudaErrorInvalidValue for an unsupported head_dim.
-inline cudaError_t launch_split(bool paged, int kv, int head_dim, int cons, int group,
+inline cudaError_t launch_split(bool paged, int kv, int head_dim, int cons, int group, bool cp_async,
                                 const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 const SplitLaunch &c)
 {
 #define FD_PICK_SPLIT(P, KV, D)                                                 \
     if (paged == P && kv == KV && head_dim == D)                              \
-        return launch_split_variant<P, KV, D>(cons, group, p, tmk, tmv, c);
+        return launch_split_variant<P, KV, D>(cons, group, cp_async, p, tmk, tmv, c);
     FD_SPLIT_VARIANTS(FD_PICK_SPLIT)
 #undef FD_PICK_SPLIT
     return cudaErrorInvalidValue;

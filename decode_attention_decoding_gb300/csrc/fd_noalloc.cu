@@ -206,7 +206,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     // The status word is the only part of the scratch that must start at zero.
     if (cudaMemsetAsync(sp.ws_err, 0, sizeof(unsigned int), launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;
-    if (launch_split_variant<false, kKvBf16, kD>(cons, group, sp, tmk, tmv, launch) != cudaSuccess)
+    if (launch_split_variant<false, kKvBf16, kD>(cons, group, false, sp, tmk, tmv, launch) != cudaSuccess)
         return FD_ERR_CUDA;
     if (launch_merge(group, kD, mp, batch * num_kv_heads, launch.stream) != cudaSuccess)
         return FD_ERR_CUDA;

@@ -10,6 +10,6 @@
 namespace fd {
 
 template cudaError_t launch_split_variant<FD_INST_PAGED, FD_INST_KV, FD_INST_D>(
-    int, int, const SplitParams &, const CUtensorMap &, const CUtensorMap &, const SplitLaunch &);
+    int, int, bool, const SplitParams &, const CUtensorMap &, const CUtensorMap &, const SplitLaunch &);
 
 }  // namespace fd
