@@ -56,7 +56,8 @@ def test_sixteen_columns(d, group, q_len):
         check(o, l, ro, rl, f"d={d} G={group} q_len={q_len} flags={flags} ctas={ctas}")
 
 
-@pytest.mark.parametrize("page", [8, 16, 128])
+# pages of 1 and 4 tokens: rows copied with cp.async into the tensor-core tiles
+@pytest.mark.parametrize("page", [1, 4, 8, 16, 128])
 def test_sixteen_columns_paged(page):
     w = syn.make_contiguous(2170 + page, len(LENS), 16, 2, 128, 1024, LENS, q_len=2)
     wp = contig_to_paged(w, page, perm_seed=page, poison=True)
