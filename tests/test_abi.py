@@ -255,3 +255,24 @@ def test_partial_slots_are_unique_and_bounded(sched):
                 assert slot not in seen
                 seen.add(slot)
                 assert slot < sched.shim_slots(B, hkv)
+
+
+def test_c_caller_compiles_links_and_sees_the_documented_checks(lib, tmp_path):
+    """A C11 program (tests/c_abi_check.c) includes the header, links libfd.so
+    and calls the host-side entry points: the boundary is usable from C."""
+    import shutil
+    import subprocess
+    from decode_attention_decoding_gb300 import build
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(build.LIB)
+    exe = str(tmp_path / "c_abi_check")
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(root, "include"), os.path.join(root, "tests", "c_abi_check.c"),
+                        "-L", libdir, "-lfd", "-Wl,-rpath," + libdir, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "C ABI checks passed" in r.stdout
