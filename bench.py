@@ -45,8 +45,8 @@ MAX_CTAS = 1024
 
 
 # ---------------------------------------------------------------------------
-# Algorithmic byte counts (K+V of valid tokens once, q, O, LSE,
-# the workspace partials written once and read once)
+# Algorithmic byte counts: K+V of the valid tokens once, q, O, LSE, and the
+# workspace partials written once and read once
 # ---------------------------------------------------------------------------
 
 def partial_count(lens, hkv, P):
