@@ -18,7 +18,8 @@ def rows_visible(L, q_len, i):
     return max(0, L - q_len + i + 1)
 
 
-@pytest.mark.parametrize("q_len", [2, 3, 8])
+# up to 16 new tokens: the most query columns per kv head the library takes
+@pytest.mark.parametrize("q_len", [2, 3, 8, 16])
 def test_each_row_is_brute_force_over_its_visible_prefix(q_len):
     hq, hkv, d = 4, 2, 64
     w = syn.make_contiguous(400 + q_len, len(LENS), hq, hkv, d, 130, LENS, q_len=q_len)
