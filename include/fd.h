@@ -238,7 +238,11 @@ fd_status fd_decode(const void *q, const void *k, const void *v,
  *   page_size    a divisor of 64 (1, 2, 4, ..., 32) or a multiple of 64; a
  *                page under 64 tokens must hold at least 128 bytes per kv head
  *                (an FP8 cache with head_dim 64 needs pages of 2 or more).
- *                Other sizes return FD_ERR_UNSUPPORTED.
+ *                Other sizes return FD_ERR_UNSUPPORTED.  Pages under 8 tokens
+ *                on the tensor-core consumers (GQA groups) are copied row by
+ *                row and need num_pages * page_size * num_kv_heads < 2^32
+ *                (FD_ERR_UNSUPPORTED otherwise; any pool that fits a GB300
+ *                does).
  *   seq_lens_dev [batch] int32, device, L_b in [0, max_blocks_per_seq * page_size];
  *                must not be NULL.
  *   Other arguments as for fd_decode.
