@@ -5,8 +5,12 @@ Default workload: MHA long-KV decode -- batch 1, 32 query heads = 32 kv heads,
 head_dim 128, kv_len 65536, contiguous [S, H, D] bf16 K/V, scale 1/sqrt(128)
 (1 GiB of K+V, larger than the 129 MB L2, so no flush is needed between
 steps).  A step is one fd_decode call: the split kernel plus the LSE merge.
+On one GPU the line also carries `workloads`: all five benchmark workloads
+timed under the same protocol (CUDA-graph replay of back-to-back calls, the
+split kernel timed by events the graph records).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+                  [--workloads 1,2,3,4,5|none]
 
 Under torchrun each rank runs its own replica of the workload (the path
 shards by request/head with no exchange), the timed region is bracketed by a
@@ -87,13 +91,13 @@ def byte_counts(w, P):
                 split=kv + q + ws + out)   # split reads K,V,q; writes partials or final O/LSE
 
 
-def consumers_label(args, w) -> str:
+def consumers_label(flags, w) -> str:
     """Which consumers the library's default choice runs for this workload."""
     G = w.num_q_heads // w.num_kv_heads
     fp8 = w.kv_dtype is not None
     row = w.head_dim * (1 if fp8 else 2)
-    mma = "mma.sync fp16 on FP8 codes" if fp8 else "mma.sync bf16"
-    if args.cuda_cores:
+    mma = "mma.sync fp16 on FP8 codes" if fp8 else "mma.sync bf16, P as two bf16 parts"
+    if flags & 0x2:   # FD_FLAG_CUDA_CORES
         return "cuda cores"
     if w.paged and w.page_size < 8:   # no fusion; rows copied or gathered
         if G >= 2 and row >= 128:
@@ -175,7 +179,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc:
@@ -187,11 +191,14 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t_start, t_end):
+        """Median SM clock and the throttle reasons seen over the samples taken
+        between t_start and t_end (wall clock; every sample if none fell there)."""
         if not self.lines:
             return None
+        inside = [ln for ts, ln in self.lines if t_start <= ts <= t_end + 0.1]
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in (inside or [ln for _, ln in self.lines]):
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -206,12 +213,175 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_in_timed_region": len(inside)}
 
 
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
+
+class Resident:
+    """One workload resident in HBM, called through the binding.  Workloads
+    whose K/V fit twice in L2 rotate through copies whose total exceeds 2x L2,
+    so every call streams its K/V from HBM."""
+
+    def __init__(self, fd, w, dev, l2, flags):
+        import torch
+        self.fd, self.w, self.flags = fd, w, flags
+        fp8 = w.kv_dtype is not None
+        self.kv_opts = dict(kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale) if fp8 else {}
+
+        def todev(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        def todev_kv(codes):
+            return torch.from_numpy(np.ascontiguousarray(codes)).to(dev) if fp8 else todev(codes)
+
+        B, hq, d = w.q.shape
+        self.q, k, v = todev(w.q), todev_kv(w.k), todev_kv(w.v)
+        self.lens = torch.from_numpy(w.seq_lens.astype(np.int32)).to(dev)
+        self.lens_h = torch.from_numpy(w.seq_lens.astype(np.int32))
+        self.table = torch.from_numpy(w.block_table.astype(np.int32)).to(dev) if w.paged else None
+        cap = w.max_blocks * w.page_size if w.paged else w.s_max
+        self.ws = fd.make_workspace(B, hq, w.num_kv_heads, d, cap, w.page_size, dev)
+        self.out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
+        self.kv_alloc = w.k.nbytes + w.v.nbytes
+        self.copies = 1
+        if l2 and self.kv_alloc < 2 * l2:
+            self.copies = int(np.ceil(2 * l2 / self.kv_alloc)) + 1
+        self.kvs = [(k, v)] + [(k.clone(), v.clone()) for _ in range(self.copies - 1)]
+        self.l2_note = (f"rotating {self.copies} K/V copies (> 2x L2)" if self.copies > 1
+                        else f"inputs {self.kv_alloc / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB, no flush")
+
+    def step(self, i, events=None):
+        w, fd = self.w, self.fd
+        kk, vv = self.kvs[i % self.copies]
+        if w.paged:
+            fd.fd_decode_paged(self.q, kk, vv, self.table, self.lens, self.lens_h, scale=w.scale, out=self.out,
+                               lse=self.lse, workspace=self.ws, split_events=events, flags=self.flags,
+                               **self.kv_opts)
+        else:
+            fd.fd_decode(self.q, kk, vv, self.lens, self.lens_h, scale=w.scale, out=self.out, lse=self.lse,
+                         workspace=self.ws, split_events=events, flags=self.flags, **self.kv_opts)
+
+    def chunk(self, steps):
+        """Calls per captured graph: 50, a whole number of K/V rotations."""
+        c = self.copies
+        return min(steps, 50 if c == 1 else c * max(1, 50 // c))
+
+
+def capture_graph(dev, stream, fn, n):
+    """A CUDA graph of fn(0) .. fn(n - 1), captured on a side stream."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(stream)
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            for i in range(n):
+                fn(i)
+    stream.wait_stream(cs)
+    return g
+
+
+def time_split_in_graph(res, dev, stream, chunk, calls):
+    """The split and merge kernels' times (µs) from CUDA events that the graph
+    itself records (the binding's split events become event nodes during
+    capture) around every split launch of a graph of `chunk` back-to-back
+    calls, replayed until `calls` calls were timed: split = its start to end
+    event, merge = the split's end event to the next call's start event.
+    An event node between two kernels stops the second from starting early
+    (programmatic dependent launch), so each figure carries its kernel's
+    launch latency; the caller scales them to the step time.
+    Returns (split µs, merge µs, how)."""
+    import torch
+    chunk = max(2, chunk)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(chunk)]
+    for a_, b_ in ev:          # torch creates the CUDA event on its first record
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+
+    def read(split, merge):
+        split += [a_.elapsed_time(b_) * 1e3 for a_, b_ in ev]
+        merge += [ev[i][1].elapsed_time(ev[i + 1][0]) * 1e3 for i in range(chunk - 1)]
+
+    split, merge = [], []
+    try:
+        g = capture_graph(dev, stream, lambda i: res.step(i, ev[i]), chunk)
+        g.replay()
+        torch.cuda.synchronize()
+        for _ in range(max(1, calls // chunk)):
+            g.replay()
+            torch.cuda.synchronize()
+            read(split, merge)
+        how = f"events in a CUDA graph of {chunk} calls, {len(split)} launches"
+    except Exception as exc:   # report it and time eager launches instead
+        torch.cuda.synchronize()
+        split, merge = [], []
+        for _ in range(max(1, min(calls, 1000) // chunk)):
+            for i in range(chunk):
+                res.step(i, ev[i])
+            torch.cuda.synchronize()
+            read(split, merge)
+        how = f"eager launches ({type(exc).__name__}: {str(exc)[:120]})"
+    return float(np.mean(split)), float(np.mean(merge)), how
+
+
+def split_share_of_step(us_per_call, split_ev, merge_ev):
+    """The split kernel's time within a step of the headline graph: the step
+    divided between the two kernels in proportion to their event times (so it
+    never exceeds the step)."""
+    return us_per_call * split_ev / (split_ev + merge_ev)
+
+
+def measure_workload(fd, w, dev, stream, l2, flags, P, peak_gbs, min_calls=1000, min_seconds=0.3, warmup=5):
+    """µs per call (a CUDA graph of back-to-back calls, replayed) and the split
+    kernel's time, for one workload; a `workloads` entry of the JSON line."""
+    import torch
+    res = Resident(fd, w, dev, l2, flags)
+    for i in range(warmup):
+        res.step(i)
+    torch.cuda.synchronize()
+    assert fd.fd_get_device_error(res.ws) == fd.FD_OK
+    chunk = res.chunk(min_calls)
+    g = capture_graph(dev, stream, res.step, chunk)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(2):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    # at least min_calls calls and min_seconds of timed work (so the clock
+    # sampler sees the timed region)
+    est = e0.elapsed_time(e1) * 1e-3 / chunk
+    reps = max(2, -(-min_calls // chunk), int(np.ceil(min_seconds / max(est * chunk, 1e-6))))
+    with ClockSampler(dev.index or 0) as clk:
+        t_wall0 = time.time()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+    us = e0.elapsed_time(e1) / (reps * chunk) * 1e3
+    split_ev, merge_ev, how = time_split_in_graph(res, dev, stream, chunk, min(min_calls, 500))
+    split_us = split_share_of_step(us, split_ev, merge_ev)
+    err = fd.fd_get_device_error(res.ws)
+    bc = byte_counts(w, P)
+    tbs = bc["call"] / (us * 1e-6) / 1e12
+    split_gbs = bc["split"] / (split_us * 1e-6) / 1e9
+    entry = {"us_per_call": us, "TB/s": tbs, "frac": tbs * 1e3 / peak_gbs,
+             "split_us": split_us, "split_frac": split_gbs / peak_gbs, "split_event_us": split_ev,
+             "merge_event_us": merge_ev, "split_timing": how,
+             "consumers": consumers_label(flags, w), "bytes_per_call": bc["call"], "calls_timed": reps * chunk,
+             "launch": f"cuda graph of {chunk} calls", "l2": res.l2_note, "clocks": clk.summary(t_wall0, t_wall1),
+             "device_error": fd.fd_status_string(err)}
+    del g, res
+    torch.cuda.empty_cache()
+    return entry
+
 
 def run_ours(args, rank, world):
     import torch
@@ -230,68 +400,27 @@ def run_ours(args, rank, world):
     B, hq, d = w.q.shape
     hkv = w.num_kv_heads
     fp8 = w.kv_dtype is not None
-    kv_opts = dict(kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale) if fp8 else {}
-
-    def todev(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    def todev_kv(codes):
-        if fp8:
-            return torch.from_numpy(np.ascontiguousarray(codes)).to(dev)
-        return todev(codes)
-
-    q, k, v = todev(w.q), todev_kv(w.k), todev_kv(w.v)
-    lens = torch.from_numpy(w.seq_lens.astype(np.int32)).to(dev)
-    lens_h = torch.from_numpy(w.seq_lens.astype(np.int32))
-    table = torch.from_numpy(w.block_table.astype(np.int32)).to(dev) if w.paged else None
-    cap = w.max_blocks * w.page_size if w.paged else w.s_max
-    ws = fd.make_workspace(B, hq, hkv, d, cap, w.page_size, dev)
-    out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
-    lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
     props = torch.cuda.get_device_properties(dev)
     P = props.multi_processor_count
     l2 = getattr(props, "L2_cache_size", 0) or 0
-
-    # L2 control: rotate through copies of K/V whose total exceeds 2x L2 when
-    # one copy would fit in L2 (config 1); otherwise the inputs alone exceed L2.
-    copies = 1
-    kv_alloc = (w.k.nbytes + w.v.nbytes)
-    if l2 and kv_alloc < 2 * l2:
-        copies = int(np.ceil(2 * l2 / kv_alloc)) + 1
-    kvs = [(k, v)] + [(k.clone(), v.clone()) for _ in range(copies - 1)]
     stream = torch.cuda.current_stream(dev)
-
     flags = fd.FD_FLAG_CUDA_CORES if args.cuda_cores else 0
-
-    def step(i, events=None):
-        kk, vv = kvs[i % copies]
-        if w.paged:
-            fd.fd_decode_paged(q, kk, vv, table, lens, lens_h, scale=w.scale, out=out, lse=lse, workspace=ws,
-                               split_events=events, flags=flags, **kv_opts)
-        else:
-            fd.fd_decode(q, kk, vv, lens, lens_h, scale=w.scale, out=out, lse=lse, workspace=ws,
-                         split_events=events, flags=flags, **kv_opts)
+    res = Resident(fd, w, dev, l2, flags)
+    peaks, peak_src = measured_peaks()
 
     for i in range(args.warmup):
-        step(i)
+        res.step(i)
     torch.cuda.synchronize()
-    assert fd.fd_get_device_error(ws) == fd.FD_OK
+    assert fd.fd_get_device_error(res.ws) == fd.FD_OK
 
     K = args.steps
     # Headline: replay a CUDA graph of `chunk` back-to-back calls (the way a
     # serving loop issues decode steps); eager per-call time is reported too.
-    chunk = min(K, 50 if copies == 1 else copies * max(1, 50 // copies))
+    chunk = res.chunk(K)
     graph, graph_error = None, None
     if not args.eager:
         try:
-            graph = torch.cuda.CUDAGraph()
-            cap_stream = torch.cuda.Stream(dev)
-            cap_stream.wait_stream(stream)
-            with torch.cuda.stream(cap_stream):
-                with torch.cuda.graph(graph, stream=cap_stream):
-                    for i in range(chunk):
-                        step(i)
-            stream.wait_stream(cap_stream)
+            graph = capture_graph(dev, stream, res.step, chunk)
             for _ in range(2):
                 graph.replay()
             torch.cuda.synchronize()
@@ -302,7 +431,7 @@ def run_ours(args, rank, world):
     K = reps * chunk if graph else K
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        # Timed region 1 (the headline): K back-to-back calls, nothing between them.
+        # The timed region: K back-to-back calls, nothing between them.
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
@@ -313,43 +442,33 @@ def run_ours(args, rank, world):
                 graph.replay()
         else:
             for i in range(K):
-                step(i)
+                res.step(i)
         e1.record(stream)
         torch.cuda.synchronize()
         t_wall1 = time.time()
         if dist:
             dist.barrier()
-        # Timed region 2 (the roofline): eager calls with CUDA events recorded
-        # on the stream around every split-kernel launch.
-        K2 = min(K, 2000)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K2)]
-        for a_, b_ in ev:          # torch creates the CUDA event on first record
-            a_.record(stream)
-            b_.record(stream)
-        torch.cuda.synchronize()
-        for i in range(K2):
-            step(i, ev[i])
-        torch.cuda.synchronize()
     ms_total = e0.elapsed_time(e1)
-    split_ms = [a_.elapsed_time(b_) for a_, b_ in ev]
-    # eager calls without events (host marshalling + two launches per call)
+    # The roofline's kernel time: events recorded by the graph around every
+    # split launch (a separate timed pass, same calls, same stream), scaled
+    # into the headline step.
+    split_ev, merge_ev, split_how = time_split_in_graph(res, dev, stream, res.chunk(K), min(K, 2000))
+    # eager calls (host marshalling + two launches per call)
     a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_eager = min(K, 500)
     torch.cuda.synchronize()
     a_.record(stream)
     for i in range(n_eager):
-        step(i)
+        res.step(i)
     b_.record(stream)
     torch.cuda.synchronize()
     eager_us = a_.elapsed_time(b_) / n_eager * 1e3
     ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / K
+    split_us = split_share_of_step(ms_step * 1e3, split_ev, merge_ev)
     bc = byte_counts(w, P)
     value_tbs = whole_job_tbs(bc["call"], world, ms_step)
-    split_avg_ms = float(np.mean(split_ms))
-    peaks, peak_src = measured_peaks()
-    achieved_gbs = bc["split"] / (split_avg_ms * 1e-3) / 1e9
+    achieved_gbs = bc["split"] / (split_us * 1e-6) / 1e9
     traffic = None
     try:
         tj = json.load(open(TRAFFIC_FILE))
@@ -363,55 +482,34 @@ def run_ours(args, rank, world):
     # result -> host, every step.
     e2e = None
     if not args.no_e2e:
-        hq_ = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory()
-        hk_, hv_ = (torch.from_numpy(np.ascontiguousarray(x).view(np.uint8 if fp8 else np.int16)).pin_memory()
-                    for x in (w.k, w.v))
-        hl_ = lens_h.pin_memory()
-        ho = torch.empty((B, hq, d), dtype=torch.float32).pin_memory()
-        hlse = torch.empty((B, hq), dtype=torch.float32).pin_memory()
-        dq, dk, dv = (torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (hq_, hk_, hv_))
-        dl = torch.empty_like(lens)
-        K2 = max(3, min(K, args.e2e_steps))
+        e2e = run_e2e(fd, res, dev, stream, bc, world, dist, max(3, min(K, args.e2e_steps)))
 
-        # Host->device copies of the step's inputs on the call's stream, whole
-        # tensors: on GB300 one pinned copy already runs at the link's rate
-        # (~211 GB/s), and splitting it over streams and chunks only added
-        # synchronisation (6.5 ms per step instead of 5.3 for workload 2).
-        def e2e_step():
-            dk.copy_(hk_, non_blocking=True)
-            dv.copy_(hv_, non_blocking=True)
-            dq.copy_(hq_, non_blocking=True)
-            dl.copy_(hl_, non_blocking=True)
-            qb = dq.view(torch.bfloat16)
-            kb, vb = (dk, dv) if fp8 else (dk.view(torch.bfloat16), dv.view(torch.bfloat16))
-            if w.paged:
-                fd.fd_decode_paged(qb, kb, vb, table, dl, lens_h, scale=w.scale, out=out, lse=lse, workspace=ws,
-                                   **kv_opts)
-            else:
-                fd.fd_decode(qb, kb, vb, dl, lens_h, scale=w.scale, out=out, lse=lse, workspace=ws, **kv_opts)
-            ho.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
+    err = fd.fd_get_device_error(res.ws)
+    headline_entry = {"us_per_call": ms_step * 1e3, "TB/s": value_tbs / world,
+                      "frac": value_tbs * 1e3 / world / peaks["hbm_gbs"], "split_us": split_us,
+                      "split_frac": achieved_gbs / peaks["hbm_gbs"], "split_event_us": split_ev,
+                      "merge_event_us": merge_ev, "split_timing": split_how,
+                      "consumers": consumers_label(flags, w), "bytes_per_call": bc["call"], "calls_timed": K,
+                      "launch": f"cuda graph of {chunk} calls" if graph else "eager", "l2": res.l2_note,
+                      "clocks": clk.summary(t_wall0, t_wall1), "device_error": fd.fd_status_string(err)}
+    l2_note, copies = res.l2_note, res.copies
+    del res, graph
+    torch.cuda.empty_cache()
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(K2):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(a.elapsed_time(b) / K2, dist, dev)
-        h2d = hq_.nbytes + hk_.nbytes + hv_.nbytes + hl_.nbytes
-        d2h = ho.numel() * 4 + hlse.numel() * 4
-        e2e = {"value": whole_job_tbs(bc["call"], world, e2e_ms), "unit": "TB/s",
-               "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": int(h2d),
-               "copies": "whole tensors, pinned host memory, on the call's stream",
-               "d2h_bytes_per_step": int(d2h), "steps": K2}
+    # Every benchmark workload under the same protocol (one GPU only: under
+    # torchrun the ranks run the headline replicas alone).
+    workloads = None
+    if world == 1 and args.workloads != "none" and not args.page:
+        workloads = {}
+        for c in [int(x) for x in args.workloads.split(",")]:
+            name = syn.CONFIG_NAMES[c]
+            if c == args.config:
+                workloads[name] = headline_entry
+                continue
+            wc = syn.make_config(c, kv_dtype=args.kv if args.kv != "bf16" else None)
+            workloads[name] = measure_workload(fd, wc, dev, stream, l2, flags, P, peaks["hbm_gbs"])
+            del wc
 
-    err = fd.fd_get_device_error(ws)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
@@ -432,20 +530,23 @@ def run_ours(args, rank, world):
                        else f"ragged sum={int(w.seq_lens.sum())}",
                        "layout": f"paged P={w.page_size}" if w.paged else "contiguous",
                        "split_ctas": P, "parallelism": f"replicas x{world}",
-                       "launch": f"cuda graph of {chunk} calls" if graph else "eager",
-                       "graph_error": graph_error, "eager_us_per_call": eager_us,
-                       "l2": (f"rotating {copies} K/V copies (> 2x L2)" if copies > 1
-                              else f"inputs {kv_alloc / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB, no flush")},
+                       "launch": headline_entry["launch"],
+                       "graph_error": graph_error, "eager_us_per_call": eager_us, "l2": l2_note,
+                       "kv_copies": copies},
             "bytes_per_call": bc["call"], "bytes_detail": bc,
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                         "kernel": "fd::split_kernel", "split_us": split_avg_ms * 1e3,
-                         "consumers": consumers_label(args, w),
+                         "kernel": "fd::split_kernel", "split_us": split_us,
+                         "split_us_how": "the headline step divided between the split and merge kernels in "
+                                         "proportion to their times from events recorded inside a CUDA graph",
+                         "split_event_us": split_ev, "merge_event_us": merge_ev, "split_timing": split_how,
+                         "consumers": consumers_label(flags, w),
                          "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"},
             "gpu_launches": 2 * K,        # split kernel + merge kernel per call
-            "clocks": clk.summary(t_wall0, t_wall1),
+            "clocks": headline_entry["clocks"],
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "workloads": workloads,
             "device_error": fd.fd_status_string(err),
         }
         print(json.dumps(line), flush=True)
@@ -453,18 +554,79 @@ def run_ours(args, rank, world):
         dist.destroy_process_group()
 
 
+def run_e2e(fd, res, dev, stream, bc, world, dist, steps):
+    """The same metric through the public API with host buffers: every step
+    copies q, K, V and the lengths from pinned host memory, decodes, and
+    copies O and LSE back (whole tensors on the call's stream: on GB300 one
+    pinned copy already runs at the host link's rate, and splitting it over
+    streams and chunks only added synchronisation)."""
+    import torch
+    w = res.w
+    fp8 = w.kv_dtype is not None
+    B, hq, d = w.q.shape
+    hq_ = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory()
+    hk_, hv_ = (torch.from_numpy(np.ascontiguousarray(x).view(np.uint8 if fp8 else np.int16)).pin_memory()
+                for x in (w.k, w.v))
+    hl_ = res.lens_h.pin_memory()
+    ho = torch.empty((B, hq, d), dtype=torch.float32).pin_memory()
+    hlse = torch.empty((B, hq), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (hq_, hk_, hv_))
+    dl = torch.empty_like(res.lens)
+
+    def e2e_step():
+        dk.copy_(hk_, non_blocking=True)
+        dv.copy_(hv_, non_blocking=True)
+        dq.copy_(hq_, non_blocking=True)
+        dl.copy_(hl_, non_blocking=True)
+        qb = dq.view(torch.bfloat16)
+        kb, vb = (dk, dv) if fp8 else (dk.view(torch.bfloat16), dv.view(torch.bfloat16))
+        if w.paged:
+            fd.fd_decode_paged(qb, kb, vb, res.table, dl, res.lens_h, scale=w.scale, out=res.out, lse=res.lse,
+                               workspace=res.ws, **res.kv_opts)
+        else:
+            fd.fd_decode(qb, kb, vb, dl, res.lens_h, scale=w.scale, out=res.out, lse=res.lse, workspace=res.ws,
+                         **res.kv_opts)
+        ho.copy_(res.out, non_blocking=True)
+        hlse.copy_(res.lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / steps, dist, dev)
+    h2d = hq_.nbytes + hk_.nbytes + hv_.nbytes + hl_.nbytes
+    d2h = ho.numel() * 4 + hlse.numel() * 4
+    out = {"value": whole_job_tbs(bc["call"], world, e2e_ms), "unit": "TB/s",
+           "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": int(h2d),
+           "copies": "whole tensors, pinned host memory, on the call's stream",
+           "d2h_bytes_per_step": int(d2h), "steps": steps}
+    del dq, dk, dv, hk_, hv_
+    return out
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w, n_rows):
-    """The first n_rows (b, h) query rows over their whole length."""
-    B, hq = w.batch, w.num_q_heads
-    rows = [(b, h) for b in range(B) for h in range(hq)][:max(1, n_rows)]
-    items = np.array([[b, h, 0, -1] for b, h in rows], dtype=np.int32)
-    toks = sum(int(w.seq_lens[b]) for b, _ in rows)
-    # bytes the oracle streams for these rows: K+V row per token (per query head)
-    return items, toks * w.head_dim * 2 * w.kv_elem_bytes
+def oracle_units(w, n_units):
+    """The first n_units (request, kv head) units, each with every query row
+    of its group over the whole kv length, and their algorithmic bytes: the
+    unit's K+V rows once (as the GPU's count, not once per query row), plus
+    its q rows, O rows and LSEs."""
+    B, hq, hkv, d = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    G = hq // hkv
+    units = [(b, g) for b in range(B) for g in range(hkv)][:max(1, n_units)]
+    items = np.array([[b, g * G + i, 0, -1] for b, g in units for i in range(G)], dtype=np.int32)
+    toks = sum(int(w.seq_lens[b]) for b, _ in units)
+    by = toks * d * 2 * w.kv_elem_bytes + len(units) * G * (d * 2 + d * 4 + 4)
+    return items, by, len(units)
 
 
 def time_oracle(w, items, threads):
@@ -474,26 +636,57 @@ def time_oracle(w, items, threads):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, seconds):
-    import oracle
-    oracle.build()
-    threads = os.cpu_count() or 1
-    total_rows = w.batch * w.num_q_heads
-    # calibrate on a few rows, then size the sample to about `seconds`
-    n = min(total_rows, threads)
-    items, by = oracle_sample(w, n)
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
+def oracle_rate(w, threads, seconds):
+    """TB/s of the oracle on `threads` threads over a sample of units sized to
+    take about `seconds`; returns (TB/s, seconds, units, repetitions)."""
+    total_units = w.batch * w.num_kv_heads
+    n = min(total_units, threads)
+    items, by, n = oracle_units(w, n)
     dt = time_oracle(w, items, threads)
-    n = int(min(total_rows, max(n, n * seconds / max(dt, 1e-3))))
-    items, by = oracle_sample(w, n)
+    n = int(min(total_units, max(n, n * seconds / max(dt, 1e-3))))
+    items, by, n = oracle_units(w, n)
     reps, total, t = 0, 0, 0.0
     while t < seconds and reps < 1000:
         t += time_oracle(w, items, threads)
         total += by
         reps += 1
-    return {"value": total / t / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
-            "seconds": t,
-            "sample": f"{n} of {total_rows} query rows (whole kv length each) x {reps} repetitions, "
-                      f"fp64 C oracle, {threads} threads; bytes = K+V rows streamed per query row"}
+    return total / t / 1e12, t, n, reps
+
+
+def cpu_baseline(w, seconds):
+    """The fp64 oracle as it stands on the host cores: on every core, and on one."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    total_units = w.batch * w.num_kv_heads
+    v_all, t_all, n_all, r_all = oracle_rate(w, threads, seconds * 0.6)
+    v_one, t_one, n_one, r_one = oracle_rate(w, 1, seconds * 0.4)
+    return {"value": v_all, "unit": "TB/s", "cores": threads, "kind": "oracle", "seconds": t_all,
+            "cpu_model": cpu_model(),
+            "sample": f"{n_all} of {total_units} (request, kv head) units, every query row of each over the "
+                      f"whole kv length, x {r_all} repetitions, fp64 C oracle, {threads} threads; bytes = "
+                      f"each unit's K+V once plus its q, O and LSE (the GPU's count)",
+            "single_thread": {"value": v_one, "unit": "TB/s", "cores": 1, "seconds": t_one,
+                              "sample": f"{n_one} units x {r_one} repetitions"}}
 
 
 def run_reference(args, rank, world):
@@ -503,20 +696,20 @@ def run_reference(args, rank, world):
     oracle.build()
     w = bench_workload(args)
     threads = os.cpu_count() or 1
-    total_rows = w.batch * w.num_q_heads
+    total_units = w.batch * w.num_kv_heads
     budget = max(1.0, args.reference_budget_s / max(1, args.steps + args.warmup))
-    n = min(total_rows, threads)
-    items, by = oracle_sample(w, n)
+    n = min(total_units, threads)
+    items, by, n = oracle_units(w, n)
     dt = time_oracle(w, items, threads)
-    n = int(min(total_rows, max(1, n * budget / max(dt, 1e-3))))
-    items, by = oracle_sample(w, n)
+    n = int(min(total_units, max(1, n * budget / max(dt, 1e-3))))
+    items, by, n = oracle_units(w, n)
     for _ in range(args.warmup):
         time_oracle(w, items, threads)
     ts = [time_oracle(w, items, threads) for _ in range(args.steps)]
     t = float(np.sum(ts))
     value = args.steps * by / t / 1e12
-    sample = (f"{n} of {total_rows} query rows per step (whole kv length each), fp64 C oracle, "
-              f"{threads} threads")
+    sample = (f"{n} of {total_units} (request, kv head) units per step, every query row of each over the whole "
+              f"kv length, fp64 C oracle, {threads} threads; bytes = each unit's K+V once plus q, O, LSE")
     line = {"metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -524,7 +717,7 @@ def run_reference(args, rank, world):
             "data": "synthetic (seeded N(0,1) bf16)", "impl": "reference",
             "config": {"workload": syn.CONFIG_NAMES[args.config], "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": "TB/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -546,6 +739,9 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of a CUDA graph")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="force the CUDA-core consumers for GQA groups (comparison runs)")
+    ap.add_argument("--workloads", default="1,2,3,4,5",
+                    help="benchmark workloads also timed on one GPU for the line's `workloads` object "
+                         "(comma-separated ids, or 'none')")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)

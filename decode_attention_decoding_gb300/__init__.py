@@ -26,7 +26,8 @@ __all__ = [
     "FD_ERR_CUDA", "FD_ERR_TIMEOUT", "FD_ERR_DEVICE_INPUT", "FD_FLAG_TEST_STARVE_FIRST_TILE",
     "FD_FLAG_CUDA_CORES", "FD_FLAG_NO_4D_BOXES", "FD_FLAG_NO_HEAD_FUSION", "FD_FLAG_NO_GATHER",
     "FD_FLAG_FUSE_HEADS", "FD_KV_AS_Q", "FD_KV_FP8_E4M3", "FD_KV_FP8_E5M2",
-    "fd_decode_noalloc",
+    "fd_decode_noalloc", "fd_decode_partial", "fd_decode_paged_partial", "fd_merge_partials",
+    "KV_END",
 ]
 
 FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
@@ -38,6 +39,7 @@ FD_FLAG_NO_HEAD_FUSION = 0x8
 FD_FLAG_NO_GATHER = 0x20
 FD_FLAG_FUSE_HEADS = 0x10
 FD_KV_AS_Q, FD_KV_FP8_E4M3, FD_KV_FP8_E5M2 = 0, 1, 2
+KV_END = 2 ** 31 - 1   # kv_end of a range that runs to the end of every request
 
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 
@@ -72,6 +74,14 @@ def _load():
     lib.fd_decode_paged.argtypes = [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                     _P, _SZ, ctypes.POINTER(FdOptions), _P]
     lib.fd_decode_paged.restype = _I
+    lib.fd_decode_partial.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _SZ,
+                                      ctypes.POINTER(FdOptions), _P]
+    lib.fd_decode_partial.restype = _I
+    lib.fd_decode_paged_partial.argtypes = [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                                            _P, _P, _P, _SZ, ctypes.POINTER(FdOptions), _P]
+    lib.fd_decode_paged_partial.restype = _I
+    lib.fd_merge_partials.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P]
+    lib.fd_merge_partials.restype = _I
     lib.fd_decode_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]
     lib.fd_decode_noalloc.restype = _I
     lib.fd_get_device_error.argtypes = [_P, _P]
@@ -297,6 +307,96 @@ def fd_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=No
                               workspace.numel(), ctypes.byref(opts), _stream_ptr(stream, q.device))
     if check and st != FD_OK:
         raise FdError(st, "fd_decode_paged")
+    return out, (None if lse is False else lse)
+
+
+def fd_decode_partial(q, k, v, seq_lens, kv_begin, kv_end=KV_END, seq_lens_host=None, scale=None,
+                      out=None, lse=None, workspace=None, num_ctas=0, flags=0, wait_timeout_ns=0,
+                      split_events=None, stream=None, check=True, dtype=None, kv_dtype=None, k_scale=1.0,
+                      v_scale=1.0):
+    """Attention over cache positions [kv_begin, min(L_b, kv_end)) of every
+    request (see fd_decode_partial in include/fd.h): k/v [B, S, Hkv, D] hold
+    the range (row t' = position kv_begin + t'); seq_lens are the whole
+    lengths.  Returns (out, lse): the output normalised over the range and its
+    natural-log LSE (-inf where the range holds no visible position)."""
+    _bits(q, "q")
+    kv_code = _kv_code(k, v, kv_dtype)
+    B, q_len, hq, d = _q_shape(q)
+    _, s_max, hkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out, lse = _outputs(q, out, lse)
+    if lse is False:
+        raise ValueError("a partial result needs its LSE")
+    if workspace is None:
+        workspace = make_workspace(B, hq, hkv, d, s_max, 0, q.device, q_len=q_len)
+    opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype), kv_code,
+                    k_scale, v_scale, q_len)
+    lh = None if seq_lens_host is None else seq_lens_host.to(torch.int32).contiguous().cpu()
+    st = _lib.fd_decode_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(_i32(seq_lens, "seq_lens")), _ptr(lh),
+                                B, hq, hkv, d, s_max, int(kv_begin), int(kv_end), float(scale), _ptr(out),
+                                _ptr(lse), _ptr(workspace), workspace.numel(), ctypes.byref(opts),
+                                _stream_ptr(stream, q.device))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_decode_partial")
+    return out, lse
+
+
+def fd_decode_paged_partial(q, k_pages, v_pages, block_table, seq_lens, kv_begin, kv_end=KV_END,
+                            seq_lens_host=None, scale=None, out=None, lse=None, workspace=None, num_ctas=0,
+                            flags=0, wait_timeout_ns=0, split_events=None, stream=None, check=True, dtype=None,
+                            kv_dtype=None, k_scale=1.0, v_scale=1.0):
+    """fd_decode_partial over a paged cache: block_table maps the range's own
+    tokens (token t' = position kv_begin + t'); see include/fd.h."""
+    _bits(q, "q")
+    kv_code = _kv_code(k_pages, v_pages, kv_dtype)
+    _i32(block_table, "block_table"); _i32(seq_lens, "seq_lens")
+    B, q_len, hq, d = _q_shape(q)
+    num_pages, page, hkv, _ = k_pages.shape
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out, lse = _outputs(q, out, lse)
+    if lse is False:
+        raise ValueError("a partial result needs its LSE")
+    if workspace is None:
+        workspace = make_workspace(B, hq, hkv, d, max_blocks * page, page, q.device, q_len=q_len)
+    opts = _options(num_ctas, flags, wait_timeout_ns, split_events, _dtype_code(q, dtype), kv_code,
+                    k_scale, v_scale, q_len)
+    lh = None if seq_lens_host is None else seq_lens_host.to(torch.int32).contiguous().cpu()
+    st = _lib.fd_decode_paged_partial(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), max_blocks,
+                                      _ptr(seq_lens), _ptr(lh), B, hq, hkv, d, page, num_pages, int(kv_begin),
+                                      int(kv_end), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                      workspace.numel(), ctypes.byref(opts), _stream_ptr(stream, q.device))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_decode_paged_partial")
+    return out, lse
+
+
+def fd_merge_partials(o_parts, lse_parts, out=None, lse=None, stream=None, check=True):
+    """Merge n partial sets (see fd_merge_partials in include/fd.h).
+
+    o_parts fp32 [n, *rows_shape, D] and lse_parts fp32 [n, *rows_shape] on
+    the device (e.g. every rank's fd_decode_partial result, stacked in rank
+    order); returns (out [*rows_shape, D], lse [*rows_shape])."""
+    for t, name in ((o_parts, "o_parts"), (lse_parts, "lse_parts")):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+    n, d = o_parts.shape[0], o_parts.shape[-1]
+    rows_shape = tuple(o_parts.shape[1:-1])
+    if tuple(lse_parts.shape) != (n,) + rows_shape:
+        raise ValueError(f"lse_parts must be {[n] + list(rows_shape)}")
+    rows = 1
+    for x in rows_shape:
+        rows *= x
+    if out is None:
+        out = torch.empty(rows_shape + (d,), dtype=torch.float32, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(rows_shape, dtype=torch.float32, device=o_parts.device)
+    st = _lib.fd_merge_partials(_ptr(o_parts), _ptr(lse_parts), n, rows, d, _ptr(out),
+                                None if lse is False else _ptr(lse), _stream_ptr(stream, o_parts.device))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_merge_partials")
     return out, (None if lse is False else lse)
 
 

@@ -138,21 +138,71 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
     return FD_OK;
 }
 
+constexpr size_t kMergeRoomBytes = 32u * 1024u;   // shared memory left beside a split CTA
+constexpr size_t kShortCallInFlightBytes = 96u * 1024u;   // K/V in flight per CTA on short calls
+
+// Shared-memory plan of the split kernel for the call's consumers, group,
+// head_dim, K/V element size and batch; fills the offsets and stage count in
+// sp and the byte size in launch.
+fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_bytes, int batch,
+                    double tiles_per_cta, SplitParams *sp, SplitLaunch *launch)
+{
+    const size_t stage_bytes = 2u * kTileTokens * (size_t)elem_bytes * (size_t)d;   // K and V tiles
+    const size_t red = align_up((size_t)reduction_floats(cons, group, d) * sizeof(float), 16);
+    const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
+    const size_t misc = 64;
+    const size_t per_stage_extra = 2 * 8 + kMetaInts * sizeof(int);   // 2 barriers + metadata
+    const size_t fixed = 1024 /* alignment slack */ + red + prefix + misc + 8 /* consumer barrier */;
+    const size_t avail = (size_t)dev.smem_optin;
+    if (avail <= fixed)
+        return FD_ERR_UNSUPPORTED;
+    int ns = (int)((avail - fixed) / (stage_bytes + per_stage_extra));
+    if (ns > kMaxStages)
+        ns = kMaxStages;
+    // Leave room beside the split CTA for merge CTAs, which are launched early
+    // (programmatic dependent launch) and then start the moment the split grid
+    // ends -- unless that costs the pipeline its fourth stage.  Measured on
+    // GB300: 32 KB free took the 1 GiB MHA call from 161.3 to 157.1 us and the
+    // small calls 1.5-1.7% faster; with 64 KB stages (3 -> 2) it cost 4%.
+    {
+        const size_t keep = kMergeRoomBytes;
+        int ns_keep = ns;
+        while (ns_keep > 2 && 1024 + fixed + ns_keep * (stage_bytes + per_stage_extra) + keep > avail)
+            --ns_keep;
+        if (ns_keep >= 4)
+            ns = ns_keep;
+    }
+    // A short call (few tiles per CTA) starts faster with less in flight: every
+    // CTA's first tiles arrive sooner when the launch burst is smaller.
+    // Measured on GB300 (MHA, 64 MiB, 13.5 tiles per CTA): 16.3 us with 5
+    // stages, 15.6 us with 3; long calls keep their stages (3 cost the 1 GiB
+    // call 3%).
+    if (tiles_per_cta < kFuseMinTilesPerCta) {
+        int ns_short = (int)(kShortCallInFlightBytes / stage_bytes);
+        ns_short = ns_short < 2 ? 2 : ns_short;
+        ns = ns < ns_short ? ns : ns_short;
+    }
+    if (ns < 2)
+        return FD_ERR_UNSUPPORTED;
+    sp->num_stages = ns;
+    sp->off_red = (uint32_t)(ns * stage_bytes);
+    sp->off_prefix = (uint32_t)(sp->off_red + red);
+    sp->off_bar = (uint32_t)(sp->off_prefix + prefix);
+    sp->off_meta = (uint32_t)(sp->off_bar + (2 * ns + 1) * 8);
+    sp->off_misc = (uint32_t)(sp->off_meta + ns * kMetaInts * sizeof(int));
+    launch->smem_bytes = 1024 + sp->off_misc + misc;
+    launch->smem_optin = (size_t)dev.smem_optin;
+    return launch->smem_bytes <= avail ? FD_OK : FD_ERR_UNSUPPORTED;
+}
+
 }  // namespace fd
 
 namespace {
 
 using namespace fd;
 
-constexpr int kVersion = 10300;   // 1.3.0
+constexpr int kVersion = 10400;   // 1.4.0
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
-constexpr size_t kMergeRoomBytes = 32u * 1024u;   // shared memory left beside a split CTA
-constexpr size_t kShortCallInFlightBytes = 96u * 1024u;   // K/V in flight per CTA on short calls
-
-struct DeviceInfo {
-    int sms = 0;
-    int smem_optin = 0;
-};
 
 // The one piece of state kept across calls: a cache of device properties.
 std::mutex g_dev_mu;
@@ -272,9 +322,9 @@ bool use_mma(int group, int row_bytes, const fd_options *opts)
 // tokens) and the call is long enough for the
 // wider tiles: measured on GB300, it lost up to a quarter of the time on
 // calls of under ~24 tiles per CTA (larger tiles, fewer of them per CTA,
-// twice the merge width) and gained 10-85% above that on such rows.
-constexpr double kFuseMinTilesPerCta = 24.0;
-
+// twice the merge width) and gained 10-85% above that on such rows: hence
+// the kFuseMinTilesPerCta threshold (fd_launch.h).
+//
 // Kv heads fused into one launch head, on the tensor-core path only, for
 // short rows and at least kFuseMinTilesPerCta (estimated) tiles per CTA
 // unless FD_FLAG_FUSE_HEADS forces it:
@@ -304,17 +354,44 @@ int fuse_factor(int cols, int hkv, int head_dim, int elem_bytes, int page_size, 
     return four ? 4 : 1;
 }
 
+// The cache positions a call covers: the whole cache (on = false), or the
+// range [begin, end) of the partial entry points, whose layout holds
+// position begin of each request at its row 0.
+struct KvRange {
+    bool on;
+    int begin, end;
+    // tokens of a request of length L that the call covers
+    long long tokens(long long L) const
+    {
+        if (!on)
+            return L;
+        const long long e = L < end ? L : end;
+        return e > begin ? e - begin : 0;
+    }
+};
+
 // KV tiles of a call (unfused): from the host copy of the lengths when the
 // caller passes one, else every request at the capacity `span`.
-long long estimate_tiles(const int32_t *seq_lens_host, int batch, int hkv, long long span)
+long long estimate_tiles(const int32_t *seq_lens_host, int batch, int hkv, long long span, const KvRange &r)
 {
     long long tiles = 0;
     if (seq_lens_host)
         for (int b = 0; b < batch; ++b)
-            tiles += ceil_div((long long)seq_lens_host[b], (long long)kTileTokens);
+            tiles += ceil_div(r.tokens(seq_lens_host[b]), (long long)kTileTokens);
     else
         tiles = (long long)batch * ceil_div(span, (long long)kTileTokens);
     return tiles * hkv;
+}
+
+// Host copy of the lengths against the layout's capacity: every L_b >= 0 and
+// the tokens the call covers at most cap.
+bool host_lens_valid(const int32_t *seq_lens_host, int batch, long long cap, const KvRange &r)
+{
+    if (seq_lens_host)
+        for (int b = 0; b < batch; ++b)
+            if (seq_lens_host[b] < 0 || r.tokens(seq_lens_host[b]) > cap)
+                return false;
+    return true;
 }
 
 // Workspace for every launch shape a call of this shape may take (fused or
@@ -331,65 +408,11 @@ size_t workspace_bytes_needed(int batch, int hq, int hkv, int head_dim, int q_le
     return need;
 }
 
-// Shared-memory plan of the split kernel for the call's consumers, group,
-// head_dim, K/V element size and batch; fills the offsets and stage count in
-// sp and the byte size in launch.
-fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_bytes, int batch,
-                    double tiles_per_cta, SplitParams *sp, SplitLaunch *launch)
-{
-    const size_t stage_bytes = 2u * kTileTokens * (size_t)elem_bytes * (size_t)d;   // K and V tiles
-    const size_t red = align_up((size_t)reduction_floats(cons, group, d) * sizeof(float), 16);
-    const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
-    const size_t misc = 64;
-    const size_t per_stage_extra = 2 * 8 + kMetaInts * sizeof(int);   // 2 barriers + metadata
-    const size_t fixed = 1024 /* alignment slack */ + red + prefix + misc + 8 /* consumer barrier */;
-    const size_t avail = (size_t)dev.smem_optin;
-    if (avail <= fixed)
-        return FD_ERR_UNSUPPORTED;
-    int ns = (int)((avail - fixed) / (stage_bytes + per_stage_extra));
-    if (ns > kMaxStages)
-        ns = kMaxStages;
-    // Leave room beside the split CTA for merge CTAs, which are launched early
-    // (programmatic dependent launch) and then start the moment the split grid
-    // ends -- unless that costs the pipeline its fourth stage.  Measured on
-    // GB300: 32 KB free took the 1 GiB MHA call from 161.3 to 157.1 us and the
-    // small calls 1.5-1.7% faster; with 64 KB stages (3 -> 2) it cost 4%.
-    {
-        const size_t keep = kMergeRoomBytes;
-        int ns_keep = ns;
-        while (ns_keep > 2 && 1024 + fixed + ns_keep * (stage_bytes + per_stage_extra) + keep > avail)
-            --ns_keep;
-        if (ns_keep >= 4)
-            ns = ns_keep;
-    }
-    // A short call (few tiles per CTA) starts faster with less in flight: every
-    // CTA's first tiles arrive sooner when the launch burst is smaller.
-    // Measured on GB300 (MHA, 64 MiB, 13.5 tiles per CTA): 16.3 us with 5
-    // stages, 15.6 us with 3; long calls keep their stages (3 cost the 1 GiB
-    // call 3%).
-    if (tiles_per_cta < kFuseMinTilesPerCta) {
-        int ns_short = (int)(kShortCallInFlightBytes / stage_bytes);
-        ns_short = ns_short < 2 ? 2 : ns_short;
-        ns = ns < ns_short ? ns : ns_short;
-    }
-    if (ns < 2)
-        return FD_ERR_UNSUPPORTED;
-    sp->num_stages = ns;
-    sp->off_red = (uint32_t)(ns * stage_bytes);
-    sp->off_prefix = (uint32_t)(sp->off_red + red);
-    sp->off_bar = (uint32_t)(sp->off_prefix + prefix);
-    sp->off_meta = (uint32_t)(sp->off_bar + (2 * ns + 1) * 8);
-    sp->off_misc = (uint32_t)(sp->off_meta + ns * kMetaInts * sizeof(int));
-    launch->smem_bytes = 1024 + sp->off_misc + misc;
-    launch->smem_optin = (size_t)dev.smem_optin;
-    return launch->smem_bytes <= avail ? FD_OK : FD_ERR_UNSUPPORTED;
-}
-
 fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const int32_t *seq_lens_dev,
                     const int32_t *block_table, int batch, int hq, int hkv, int cap, int s_max,
                     int head_dim, int page_size, int max_blocks, int num_pages, float scale, float *o,
-                    float *lse, void *workspace, long long est_tiles, const fd_options *opts,
-                    fd_stream_t stream)
+                    float *lse, void *workspace, long long est_tiles, const KvRange &range,
+                    const fd_options *opts, fd_stream_t stream)
 {
     int num_ctas = opts && opts->num_ctas > 0 ? opts->num_ctas : dev.sms;
     if (num_ctas > kMaxCtas)
@@ -450,6 +473,9 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     sp.fuse_dh = fuse == 4 ? head_dim : 0;   // only a shared 4-head row splits a column's dims
     sp.fuse_f = fuse;
     sp.q_len = q_len;
+    sp.range_on = range.on ? 1 : 0;
+    sp.kv_begin = range.on ? range.begin : 0;
+    sp.kv_end = range.on ? range.end : 0;
     sp.g_real = real_group;
     sp.n_cols = slots;
     // column slot n = (part, new token i, query head g), part-major; each part
@@ -499,7 +525,24 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     std::memcpy(mp.col_code, sp.col_code, sizeof mp.col_code);
     mp.seq_lens = seq_lens_dev;
     mp.cap = cap;
+    mp.range_on = sp.range_on;
+    mp.kv_begin = sp.kv_begin;
+    mp.kv_end = sp.kv_end;
     return FD_OK;
+}
+
+// Record a caller's timing event on `stream`.  Inside a stream capture the
+// record becomes an event node of the graph (cudaEventRecordExternal), so
+// every replay of the graph records it.
+bool record_event(cudaEvent_t ev, cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess)
+        return false;
+    const cudaError_t e = cs == cudaStreamCaptureStatusActive
+                              ? cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal)
+                              : cudaEventRecord(ev, stream);
+    return e == cudaSuccess;
 }
 
 fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUtensorMap &tmv,
@@ -508,13 +551,13 @@ fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUte
     cudaStream_t stream = cp.launch.stream;
     cudaEvent_t ev0 = opts ? static_cast<cudaEvent_t>(opts->split_start_event) : nullptr;
     cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_end_event) : nullptr;
-    if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess)
+    if (ev0 && !record_event(ev0, stream))
         return FD_ERR_CUDA;
     cudaError_t e = launch_split(paged, cp.kv, cp.head_dim, cp.cons, cp.group, cp.cp_async, cp.sp, tmk, tmv,
                                  cp.launch);
     if (e != cudaSuccess)
         return FD_ERR_CUDA;
-    if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess)
+    if (ev1 && !record_event(ev1, stream))
         return FD_ERR_CUDA;
     e = launch_merge(cp.merge_group, cp.merge_dim, cp.mp, cp.sp.batch * cp.sp.hkv, stream);
     if (e != cudaSuccess)
@@ -522,50 +565,25 @@ fd_status run(const CallPlan &cp, bool paged, const CUtensorMap &tmk, const CUte
     return FD_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_kv_len,
-                         int page_size)
+// A partial call's range: 0 <= begin <= end, and the position of the layout's
+// last row (begin + capacity) inside int32.
+bool range_valid(int begin, int end, long long cap)
 {
-    return fd_workspace_size_q(batch, num_q_heads, num_kv_heads, head_dim, max_kv_len, page_size, 1);
+    return begin >= 0 && end >= begin && (long long)begin + cap < (1ll << 31);
 }
 
-size_t fd_workspace_size_q(int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_kv_len,
-                           int page_size, int q_len)
-{
-    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kv_len < 0 ||
-        page_size < 0 || num_q_heads % num_kv_heads != 0 || q_len < 1 ||
-        (long long)(num_q_heads / num_kv_heads) * q_len > kMaxColumns)
-        return 0;
-    return workspace_bytes_needed(batch, num_q_heads, num_kv_heads, head_dim, q_len);
-}
-
-fd_status fd_workspace_init(void *workspace, size_t workspace_bytes, fd_stream_t stream)
-{
-    if (!workspace || workspace_bytes < 256 || !aligned(workspace, 256))
-        return FD_ERR_INVALID_ARG;
-    return cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? FD_OK
-               : FD_ERR_CUDA;
-}
-
-fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *seq_lens_dev,
-                    const int32_t *seq_lens_host, int batch, int num_q_heads, int num_kv_heads,
-                    int head_dim, int s_max, float scale, float *o, float *lse, void *workspace,
-                    size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
+fd_status decode_contiguous(const void *q, const void *k, const void *v, const int32_t *seq_lens_dev,
+                            const int32_t *seq_lens_host, int batch, int num_q_heads, int num_kv_heads,
+                            int head_dim, int s_max, const KvRange &range, float scale, float *o, float *lse,
+                            void *workspace, size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
 {
     fd_status st = check_common(q, o, workspace, batch, num_q_heads, num_kv_heads, head_dim, opts);
     if (st != FD_OK)
         return st;
     if (s_max < 0 || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (lse && !aligned(lse, 4)))
         return FD_ERR_INVALID_ARG;
-    if (seq_lens_host)
-        for (int b = 0; b < batch; ++b)
-            if (seq_lens_host[b] < 0 || seq_lens_host[b] > s_max)
-                return FD_ERR_INVALID_ARG;
+    if (!host_lens_valid(seq_lens_host, batch, s_max, range))
+        return FD_ERR_INVALID_ARG;
     if (!options_valid(opts))
         return FD_ERR_INVALID_ARG;
     if ((st = check_columns(num_q_heads, num_kv_heads, head_dim, 0, opts)) != FD_OK)
@@ -585,7 +603,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
     CallPlan cp;
     st = fill_plan(&cp, dev, q, seq_lens_dev, nullptr, batch, num_q_heads, num_kv_heads, s_max, s_max,
                    head_dim, 0, 0, 0, scale, o, lse, workspace,
-                   estimate_tiles(seq_lens_host, batch, num_kv_heads, s_max), opts, stream);
+                   estimate_tiles(seq_lens_host, batch, num_kv_heads, s_max, range), range, opts, stream);
     if (st != FD_OK)
         return st;
     alignas(64) CUtensorMap tmk, tmv;
@@ -596,12 +614,11 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
     return run(cp, false, tmk, tmv, opts);
 }
 
-fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_pages,
-                          const int32_t *block_table, int max_blocks_per_seq,
-                          const int32_t *seq_lens_dev, const int32_t *seq_lens_host, int batch,
-                          int num_q_heads, int num_kv_heads, int head_dim, int page_size,
-                          int num_pages, float scale, float *o, float *lse, void *workspace,
-                          size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
+fd_status decode_paged(const void *q, const void *k_pages, const void *v_pages, const int32_t *block_table,
+                       int max_blocks_per_seq, const int32_t *seq_lens_dev, const int32_t *seq_lens_host, int batch,
+                       int num_q_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
+                       const KvRange &range, float scale, float *o, float *lse, void *workspace,
+                       size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
 {
     fd_status st = check_common(q, o, workspace, batch, num_q_heads, num_kv_heads, head_dim, opts);
     if (st != FD_OK)
@@ -626,10 +643,8 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     if (cap >= (1ll << 31) || (long long)num_pages * page_size >= (1ll << 31) ||
         (long long)num_kv_heads * batch * ((cap + kTileTokens - 1) / kTileTokens) >= (1ll << 31))
         return FD_ERR_UNSUPPORTED;
-    if (seq_lens_host)
-        for (int b = 0; b < batch; ++b)
-            if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap)
-                return FD_ERR_INVALID_ARG;
+    if (!host_lens_valid(seq_lens_host, batch, cap, range))
+        return FD_ERR_INVALID_ARG;
     if (!options_valid(opts))
         return FD_ERR_INVALID_ARG;
     if (workspace_bytes < fd_workspace_size_q(batch, num_q_heads, num_kv_heads, head_dim, (int)cap,
@@ -644,7 +659,7 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     CallPlan cp;
     st = fill_plan(&cp, dev, q, seq_lens_dev, block_table, batch, num_q_heads, num_kv_heads, (int)cap, 0,
                    head_dim, page_size, max_blocks_per_seq, num_pages, scale, o, lse, workspace,
-                   estimate_tiles(seq_lens_host, batch, num_kv_heads, cap), opts, stream);
+                   estimate_tiles(seq_lens_host, batch, num_kv_heads, cap, range), range, opts, stream);
     if (st != FD_OK)
         return st;
     alignas(64) CUtensorMap tmk, tmv;
@@ -682,6 +697,105 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
                              cp.head_dim, &cp.sp)) != FD_OK)
         return st;
     return run(cp, true, tmk, tmv, opts);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fd_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_kv_len,
+                         int page_size)
+{
+    return fd_workspace_size_q(batch, num_q_heads, num_kv_heads, head_dim, max_kv_len, page_size, 1);
+}
+
+size_t fd_workspace_size_q(int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_kv_len,
+                           int page_size, int q_len)
+{
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kv_len < 0 ||
+        page_size < 0 || num_q_heads % num_kv_heads != 0 || q_len < 1 ||
+        (long long)(num_q_heads / num_kv_heads) * q_len > kMaxColumns)
+        return 0;
+    return workspace_bytes_needed(batch, num_q_heads, num_kv_heads, head_dim, q_len);
+}
+
+fd_status fd_workspace_init(void *workspace, size_t workspace_bytes, fd_stream_t stream)
+{
+    if (!workspace || workspace_bytes < 256 || !aligned(workspace, 256))
+        return FD_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? FD_OK
+               : FD_ERR_CUDA;
+}
+
+fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *seq_lens_dev,
+                    const int32_t *seq_lens_host, int batch, int num_q_heads, int num_kv_heads,
+                    int head_dim, int s_max, float scale, float *o, float *lse, void *workspace,
+                    size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
+{
+    return decode_contiguous(q, k, v, seq_lens_dev, seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim,
+                             s_max, KvRange{false, 0, 0}, scale, o, lse, workspace, workspace_bytes, opts, stream);
+}
+
+fd_status fd_decode_partial(const void *q, const void *k, const void *v, const int32_t *seq_lens_dev,
+                            const int32_t *seq_lens_host, int batch, int num_q_heads, int num_kv_heads,
+                            int head_dim, int s_max, int kv_begin, int kv_end, float scale, float *o_part,
+                            float *lse_part, void *workspace, size_t workspace_bytes, const fd_options *opts,
+                            fd_stream_t stream)
+{
+    if (!range_valid(kv_begin, kv_end, s_max) || !lse_part)
+        return FD_ERR_INVALID_ARG;
+    return decode_contiguous(q, k, v, seq_lens_dev, seq_lens_host, batch, num_q_heads, num_kv_heads, head_dim,
+                             s_max, KvRange{true, kv_begin, kv_end}, scale, o_part, lse_part, workspace,
+                             workspace_bytes, opts, stream);
+}
+
+fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                          const int32_t *block_table, int max_blocks_per_seq,
+                          const int32_t *seq_lens_dev, const int32_t *seq_lens_host, int batch,
+                          int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                          int num_pages, float scale, float *o, float *lse, void *workspace,
+                          size_t workspace_bytes, const fd_options *opts, fd_stream_t stream)
+{
+    return decode_paged(q, k_pages, v_pages, block_table, max_blocks_per_seq, seq_lens_dev, seq_lens_host, batch,
+                        num_q_heads, num_kv_heads, head_dim, page_size, num_pages, KvRange{false, 0, 0}, scale, o,
+                        lse, workspace, workspace_bytes, opts, stream);
+}
+
+fd_status fd_decode_paged_partial(const void *q, const void *k_pages, const void *v_pages,
+                                  const int32_t *block_table, int max_blocks_per_seq,
+                                  const int32_t *seq_lens_dev, const int32_t *seq_lens_host, int batch,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
+                                  int kv_begin, int kv_end, float scale, float *o_part, float *lse_part,
+                                  void *workspace, size_t workspace_bytes, const fd_options *opts,
+                                  fd_stream_t stream)
+{
+    if (max_blocks_per_seq <= 0 || page_size <= 0 ||
+        !range_valid(kv_begin, kv_end, (long long)max_blocks_per_seq * page_size) || !lse_part)
+        return FD_ERR_INVALID_ARG;
+    return decode_paged(q, k_pages, v_pages, block_table, max_blocks_per_seq, seq_lens_dev, seq_lens_host, batch,
+                        num_q_heads, num_kv_heads, head_dim, page_size, num_pages, KvRange{true, kv_begin, kv_end},
+                        scale, o_part, lse_part, workspace, workspace_bytes, opts, stream);
+}
+
+fd_status fd_merge_partials(const float *o_parts, const float *lse_parts, int num_parts, int rows, int head_dim,
+                            float *o, float *lse, fd_stream_t stream)
+{
+    if (num_parts < 1 || rows < 0 || !o_parts || !lse_parts || !o || !aligned(o_parts, 16) ||
+        !aligned(lse_parts, 4) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim))
+        return FD_ERR_UNSUPPORTED;
+    MergePartsParams mp;
+    mp.o_parts = o_parts;
+    mp.lse_parts = lse_parts;
+    mp.o = o;
+    mp.lse = lse;
+    mp.n = num_parts;
+    mp.rows = rows;
+    return launch_merge_parts(head_dim, mp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FD_OK
+                                                                                                   : FD_ERR_CUDA;
 }
 
 fd_status fd_get_device_error(void *workspace, fd_stream_t stream)

@@ -149,6 +149,11 @@ struct SplitParams {
     int col_code[kMaxColumnSlots];   // new token i | part << 4 | head g << 8, or -1 (host-computed)
     int q_f16;        // FP8 caches: 1 when q is fp16, 0 when bf16
     float v_scale;    // multiplies O (an FP8 cache's V dequantisation scale; 1 otherwise)
+    // A token range (the partial entry points): the layout holds cache
+    // positions kv_begin, kv_begin + 1, .. of each request at its rows 0, 1,
+    // .., and the call covers positions [kv_begin, min(L_b, kv_end)).
+    // range_on = 0: the whole cache, from position 0.
+    int range_on, kv_begin, kv_end;
 };
 
 struct MergeParams {
@@ -162,6 +167,7 @@ struct MergeParams {
     int col_code[kMaxColumnSlots];
     const int32_t *seq_lens;   // as in SplitParams (small batches: segment geometry)
     int cap;
+    int range_on, kv_begin, kv_end;   // as in SplitParams
 };
 
 constexpr int kMergeDirectBatch = 32;   // batches this small: segment geometry from the lengths
@@ -204,15 +210,34 @@ __device__ __forceinline__ void store_o(float *o, size_t row, int d, int fuse_dh
         o[row * fuse_dh + (d - part)] = v;
 }
 
-__device__ __forceinline__ int load_len(const SplitParams &p, int b, bool report)
+// Request b's lengths as the kernels use them.  L: its length L_b, from the
+// device array (every request at capacity when there is none).  n: the
+// tokens of the call's range that the layout holds, min(L_b, kv_end) -
+// kv_begin (L_b for a whole-cache call); they sit at layout rows 0 .. n - 1.
+// A negative L_b, or an n above the layout's capacity cap, is clamped (to 0,
+// to cap) and recorded in *report when it is given.
+struct ReqLen {
+    int L;   // L_b (whole cache: at most cap)
+    int n;   // tokens of the range, 0 .. cap
+};
+
+template <class P>
+__device__ __forceinline__ ReqLen req_len(const P &p, int b, unsigned int *report)
 {
-    int L = p.seq_lens ? p.seq_lens[b] : p.cap;
-    if (L < 0 || L > p.cap) {
-        if (report)
-            atomicOr(p.ws_err, kErrLength);
-        L = L < 0 ? 0 : p.cap;
+    const int off = p.range_on ? p.kv_begin : 0;
+    int L = p.seq_lens ? p.seq_lens[b] : off + p.cap;
+    bool bad = L < 0;
+    L = max(L, 0);
+    int n = p.range_on ? max(min(L, p.kv_end) - off, 0) : L;
+    if (n > p.cap) {
+        bad = true;
+        n = p.cap;
+        if (!p.range_on)
+            L = p.cap;
     }
-    return L;
+    if (bad && report)
+        atomicOr(report, kErrLength);
+    return ReqLen{L, n};
 }
 
 // Every lane waits (so each acquires the barrier's phase); the outcome is
@@ -249,10 +274,10 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
     const int B = p.batch;
     const int per = ceil_div(B, nthreads);
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
-    const bool report = blockIdx.x == 0;
+    unsigned int *report = blockIdx.x == 0 ? p.ws_err : nullptr;
     int local = 0;
     for (int b = b0; b < b1; ++b)
-        local += ceil_div(load_len(p, b, report), kTileTokens);
+        local += ceil_div(req_len(p, b, report).n, kTileTokens);
     int x = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -278,7 +303,7 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
     int run = x - local + (warp > 0 ? scan_tmp[warp - 1] : 0);
     for (int b = b0; b < b1; ++b) {
         prefix[b] = run * p.hkv;
-        run += ceil_div(load_len(p, b, false), kTileTokens);
+        run += ceil_div(req_len(p, b, nullptr).n, kTileTokens);
     }
     if (tid == nthreads - 1)
         prefix[B] = run * p.hkv;
@@ -330,7 +355,11 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     int nb = (prefix[b + 1] - prefix[b]) / p.hkv;
     int h = (t - prefix[b]) / nb;
     int j = (t - prefix[b]) - h * nb;
-    int L = load_len(p, b, false);
+    // L: the request's tokens in the layout; Lc: its length counted from the
+    // layout's row 0 (the causal limits of several new tokens)
+    const int off = p.range_on ? p.kv_begin : 0;
+    ReqLen rq = req_len(p, b, nullptr);
+    int L = rq.n, Lc = rq.L - off;
 
     // Paged: block-table entries in a ring of four 32-entry windows (one
     // entry per lane per window).  The current window is e0; e1..e3 are the
@@ -433,7 +462,7 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             int *m = meta + s * kMetaInts;
             m[0] = b;
             m[1] = h;
-            m[2] = L - token0;   // tokens of the request from this tile on (causal limits)
+            m[2] = Lc - token0;   // tokens of the request from this tile on (causal limits)
             m[3] = nvalid;
             m[4] = flags;
             m[5] = b * p.hkv + h;
@@ -497,7 +526,9 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
                     ++b;
                 } while (b < p.batch && prefix[b + 1] == prefix[b]);
                 nb = (prefix[b + 1] - prefix[b]) / p.hkv;
-                L = load_len(p, b, false);
+                rq = req_len(p, b, nullptr);
+                L = rq.n;
+                Lc = rq.L - off;
             }
         }
     }
@@ -539,7 +570,11 @@ __device__ __forceinline__ void split_producer_cpa(const SplitParams &p, uint32_
     int nb = (prefix[b + 1] - prefix[b]) / p.hkv;
     int h = (t - prefix[b]) / nb;
     int j = (t - prefix[b]) - h * nb;
-    int L = load_len(p, b, false);
+    // L: the request's tokens in the layout; Lc: its length counted from the
+    // layout's row 0 (the causal limits of several new tokens)
+    const int off = p.range_on ? p.kv_begin : 0;
+    ReqLen rq = req_len(p, b, nullptr);
+    int L = rq.n, Lc = rq.L - off;
 
     // Block-table entries of request b, pages win_base .. win_base + 127: lane
     // l holds entry win_base + l + 32 k in e[k].  The window advances 32
@@ -579,7 +614,7 @@ __device__ __forceinline__ void split_producer_cpa(const SplitParams &p, uint32_
             int *m = meta + s * kMetaInts;
             m[0] = b;
             m[1] = h;
-            m[2] = L - token0;
+            m[2] = Lc - token0;
             m[3] = nvalid;
             m[4] = flags;
             m[5] = b * p.hkv + h;
@@ -644,7 +679,9 @@ __device__ __forceinline__ void split_producer_cpa(const SplitParams &p, uint32_
                     ++b;
                 } while (b < p.batch && prefix[b + 1] == prefix[b]);
                 nb = (prefix[b + 1] - prefix[b]) / p.hkv;
-                L = load_len(p, b, false);
+                rq = req_len(p, b, nullptr);
+                L = rq.n;
+                Lc = rq.L - off;
             }
         }
     }
@@ -981,9 +1018,10 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
 // O^T[D x 8] += V^T[D x 16] . P^T[16 x 8].  Both are warp-level m16n8k16 MMAs
 // (bf16, or fp16 for fp16 and FP8 caches) with fp32 accumulation.  The tile
 // arrives with the 128-byte TMA swizzle, so the ldmatrix row reads are free
-// of bank conflicts.  P is rounded to the MMA type for the second product
-// and the running sum l adds up exactly those rounded weights (a second sum
-// of the exact weights gives the LSE).
+// of bank conflicts.  For the second product P is taken as a rounded part
+// plus its rounded remainder, both of the MMA type (two MMAs), and the
+// running sum l adds up exactly the weights that multiply V (a second sum of
+// the exact weights gives the LSE).
 //
 // Warps 2i and 2i+1 take tokens 16i..16i+15 of every tile.  Sharing the
 // columns, both form the scores (so each holds the softmax state), and for
@@ -1035,6 +1073,13 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
     constexpr int DR = PAIR ? D / 2 : D;         // dims kept per column in the reduction
     constexpr bool FP8 = kv_is_fp8(KV);
     constexpr bool MMA_F16 = KV != kKvBf16;   // fp16 MMAs for fp16 and FP8 caches
+    // P.V takes each weight as hi + lo, both of the MMA type, in two MMAs:
+    // hi is the weight rounded (8 significant bits in bf16, 11 in fp16), lo
+    // its rounded remainder, so the pair carries 16 or 22 bits.  fp16 weights
+    // are scaled by 2^15 first (a weight is at most 1), which keeps weights
+    // down to ~2^-39 clear of fp16's underflow; l and O share the scale,
+    // which cancels in O = acc / l.
+    constexpr float kPScale = MMA_F16 ? 32768.f : 1.f;
     static_assert(HD::kParts >= 1, "tensor-core rows span at least one 128-byte part");
     const int NS = p.num_stages;
     const int pair = cw >> 1, dhalf = cw & 1;
@@ -1219,6 +1264,7 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         // Per n8 tile: mask, online softmax over this warp's 16 tokens, P.
         float alpha[NT][2];
         uint32_t pb0[NT], pb1[NT];
+        uint32_t pe0[NT], pe1[NT];   // the remainders' B operands
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             // sc[0]: (token grp, column 2qd), sc[1]: (grp, 2qd+1), sc[2]: (grp+8, 2qd), sc[3]: (grp+8, 2qd+1);
@@ -1251,18 +1297,30 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                 pw[j + 2] = (x[j + 2] == kNegInf) ? 0.f : exp2_approx(x[j + 2] - m_new);
                 m[nt][j] = m_new;
             }
-            const uint32_t p_lo = pack_x2<MMA_F16>(pw[0], pw[1]);   // token grp, columns 2qd, 2qd+1
-            const uint32_t p_hi = pack_x2<MMA_F16>(pw[2], pw[3]);   // token grp + 8
+            float ps[4];   // the weights in the units of the P.V product
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                ps[i] = pw[i] * kPScale;
+            const uint32_t p_r0 = pack_x2<MMA_F16>(ps[0], ps[1]);   // token grp, columns 2qd, 2qd+1
+            const uint32_t p_r8 = pack_x2<MMA_F16>(ps[2], ps[3]);   // token grp + 8
             {
-                const float2 r_lo = x2_to_float2<MMA_F16>(p_lo), r_hi = x2_to_float2<MMA_F16>(p_hi);
-                l[nt][0] = l[nt][0] * alpha[nt][0] + (r_lo.x + r_hi.x);
-                l[nt][1] = l[nt][1] * alpha[nt][1] + (r_lo.y + r_hi.y);
+                float2 r0 = x2_to_float2<MMA_F16>(p_r0), r8 = x2_to_float2<MMA_F16>(p_r8);
+                // the remainder of each weight: ps - hi is exact in fp32
+                const uint32_t e_r0 = pack_x2<MMA_F16>(ps[0] - r0.x, ps[1] - r0.y);
+                const uint32_t e_r8 = pack_x2<MMA_F16>(ps[2] - r8.x, ps[3] - r8.y);
+                const float2 f0 = x2_to_float2<MMA_F16>(e_r0), f8 = x2_to_float2<MMA_F16>(e_r8);
+                r0 = make_float2(r0.x + f0.x, r0.y + f0.y);
+                r8 = make_float2(r8.x + f8.x, r8.y + f8.y);
+                pe0[nt] = movmatrix_trans(e_r0);
+                pe1[nt] = movmatrix_trans(e_r8);
+                l[nt][0] = l[nt][0] * alpha[nt][0] + (r0.x + r8.x);
+                l[nt][1] = l[nt][1] * alpha[nt][1] + (r0.y + r8.y);
                 lt[nt][0] = lt[nt][0] * alpha[nt][0] + (pw[0] + pw[2]);
                 lt[nt][1] = lt[nt][1] * alpha[nt][1] + (pw[1] + pw[3]);
             }
             // P^T as the B operand (k = token, n = column): transpose the 8x8 blocks.
-            pb0[nt] = movmatrix_trans(p_lo);
-            pb1[nt] = movmatrix_trans(p_hi);
+            pb0[nt] = movmatrix_trans(p_r0);
+            pb1[nt] = movmatrix_trans(p_r8);
         }
 
         // Rows past the request's end may hold anything (even NaN), and the
@@ -1303,6 +1361,9 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
                     mma_16816<MMA_F16>(acc[nt][i], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_16816<MMA_F16>(acc[nt][i], a0, a1, a2, a3, pe0[nt], pe1[nt]);
             }
         } else {
             // matrices (tokens 0-7 | 8-15) x (chunk c | c + 1): two 16-dim tiles per ldmatrix
@@ -1323,6 +1384,11 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
                 for (int nt = 0; nt < NT; ++nt) {
                     mma_16816<true>(acc[nt][2 * ii], a0, a1, a2, a3, pb0[nt], pb1[nt]);
                     mma_16816<true>(acc[nt][2 * ii + 1], b0, b1, b2, b3, pb0[nt], pb1[nt]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_16816<true>(acc[nt][2 * ii], a0, a1, a2, a3, pe0[nt], pe1[nt]);
+                    mma_16816<true>(acc[nt][2 * ii + 1], b0, b1, b2, b3, pe0[nt], pe1[nt]);
                 }
             }
         }
@@ -1469,10 +1535,8 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
     const bool small = p.batch <= kMergeDirectBatch;
     if (small && d < 32) {
         int L = 0;
-        if (d < p.batch) {
-            L = p.seq_lens ? p.seq_lens[d] : p.cap;
-            L = L < 0 ? 0 : (L > p.cap ? p.cap : L);   // clamped as the split kernel clamps
-        }
+        if (d < p.batch)
+            L = req_len(p, d, nullptr).n;   // clamped as the split kernel clamps
         const int t = ceil_div(L, kTileTokens);
         int x = t;
 #pragma unroll
@@ -1622,6 +1686,99 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
         acc += src[(size_t)i * stride] * s_w[i];
     store_o<D>(p.o, row, d, p.fuse_dh, part, acc);
     if (d == 0 && p.lse)
+        p.lse[row] = lse;
+}
+
+// ------------------------------------------------------------------ merge of caller partials
+//
+// Sequence sharding: each of n partial sets holds, for every query row, the
+// attention over one token range -- a normalised output O_s and its
+// natural-log LSE lse_s (the Flash-Decoding section of the FlashAttention
+// handbook page; the pass-2 merge of the sm120 article, section 2).  The
+// merge is the same as merge_kernel's: M = max_s lse_s, LSE = M + ln sum_s
+// exp(lse_s - M), O = sum_s O_s exp(lse_s - LSE); a set with lse_s = -inf saw
+// no token and contributes nothing (handbook exercise 2), and a row that no
+// set saw gets O = 0, LSE = -inf.
+
+struct MergePartsParams {
+    const float *o_parts;     // [n][rows][D]
+    const float *lse_parts;   // [n][rows]
+    float *o;                 // [rows][D]
+    float *lse;               // [rows] or null
+    int n, rows;
+};
+
+constexpr int kMergePartsWarps = 8;
+
+// One warp per query row: lane l takes sets l, l + 32, .. for the LSE, and
+// dims D/32 l .. D/32 (l + 1) - 1 of every set's output row (one coalesced
+// row read per set).
+template <int D>
+__global__ void __launch_bounds__(kMergePartsWarps * 32) merge_parts_kernel(const __grid_constant__ MergePartsParams p)
+{
+    constexpr int kVec = D / 32;   // 2, 4 or 8 dims per lane
+    static_assert(D % 64 == 0, "head_dim 64, 128 or 256");
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kMergePartsWarps + (threadIdx.x >> 5);
+    if (row >= p.rows)
+        return;   // warp-uniform
+    const size_t rows = (size_t)p.rows;
+    float M = kNegInf;
+    for (int s = lane; s < p.n; s += 32)
+        M = fmaxf(M, p.lse_parts[(size_t)s * rows + row]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float *dst = p.o + (size_t)row * D + lane * kVec;
+    if (M == kNegInf) {   // no set saw a token of this row
+#pragma unroll
+        for (int i = 0; i < kVec; ++i)
+            dst[i] = 0.f;
+        if (lane == 0 && p.lse)
+            p.lse[row] = kNegInf;
+        return;
+    }
+    float S = 0.f;
+    for (int s = lane; s < p.n; s += 32)
+        S += expf(p.lse_parts[(size_t)s * rows + row] - M);   // exp(-inf) = 0 for empty sets
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        S += __shfl_xor_sync(0xffffffffu, S, off);
+    const float lse = M + logf(S);
+    float acc[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i)
+        acc[i] = 0.f;
+    for (int s0 = 0; s0 < p.n; s0 += 32) {
+        const int s = s0 + lane;
+        const float w = s < p.n ? expf(p.lse_parts[(size_t)s * rows + row] - lse) : 0.f;
+        const int cnt = min(32, p.n - s0);
+        for (int i = 0; i < cnt; ++i) {
+            const float wi = __shfl_sync(0xffffffffu, w, i);
+            if (wi == 0.f)
+                continue;   // warp-uniform: an empty set (or a weight below fp32's range)
+            const float4 *src =
+                reinterpret_cast<const float4 *>(p.o_parts + ((size_t)(s0 + i) * rows + row) * D + lane * kVec);
+            if constexpr (kVec == 2) {
+                const float2 x = *reinterpret_cast<const float2 *>(src);
+                acc[0] += wi * x.x;
+                acc[1] += wi * x.y;
+            } else {
+#pragma unroll
+                for (int v = 0; v < kVec / 4; ++v) {
+                    const float4 x = src[v];
+                    acc[4 * v + 0] += wi * x.x;
+                    acc[4 * v + 1] += wi * x.y;
+                    acc[4 * v + 2] += wi * x.z;
+                    acc[4 * v + 3] += wi * x.w;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kVec; ++i)
+        dst[i] = acc[i];
+    if (lane == 0 && p.lse)
         p.lse[row] = lse;
 }
 

@@ -18,6 +18,24 @@ struct SplitLaunch {
     cudaStream_t stream;
 };
 
+// Device properties a launch plan needs.
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+// Calls with fewer (estimated) KV tiles per split CTA than this count as
+// short: they keep less K/V in flight per CTA, and kv heads are not fused
+// for them (fd_api.cu).
+constexpr double kFuseMinTilesPerCta = 24.0;
+
+// Shared-memory plan of the split kernel (fd_api.cu): pipeline stages, the
+// offsets of every region in sp, and the byte size in launch, for the call's
+// consumers (kCons*), column group, row dims d, K/V element size, batch and
+// estimated tiles per split CTA.  FD_ERR_UNSUPPORTED if two stages do not fit.
+fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_bytes, int batch,
+                    double tiles_per_cta, SplitParams *sp, SplitLaunch *launch);
+
 // K and V tensor maps of a call (fd_api.cu): rows are (token, kv head)
 // pairs of d elements of type kv (kKv*), loaded box_rows tokens at a time.
 // The tensor-core consumers (mma) take 128-byte swizzled boxes, as one 4-D
@@ -32,26 +50,33 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
 // Returns cudaErrorInvalidValue for an unsupported group size or head_dim.
 cudaError_t launch_merge(int group, int head_dim, const MergeParams &p, int grid, cudaStream_t stream);
 
+// Merge of n caller-supplied partial sets (fd_merge_partials); head_dim 64,
+// 128 or 256 (cudaErrorInvalidValue otherwise).
+cudaError_t launch_merge_parts(int head_dim, const MergePartsParams &p, cudaStream_t stream);
+
 // Shared by the split translation units.
 template <int G, bool PAGED, int CONS, int KV, int D, bool CPA = false>
 cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const SplitLaunch &c)
 {
     // Raise the kernel's dynamic shared-memory limit to the device's opt-in
-    // maximum, once per device (so later calls may be captured in a graph).
+    // maximum, once per device (so later calls may be captured in a graph);
+    // again if a launch is refused (the device's context was reset since).
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     const unsigned long long bit = 1ull << (dev & 63);
-    if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(split_kernel<G, PAGED, CONS, KV, D, CPA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)c.smem_optin);
-        if (e != cudaSuccess)
-            return e;
-        configured.fetch_or(bit, std::memory_order_release);
-    }
+    auto configure = [&]() -> cudaError_t {
+        const cudaError_t r = cudaFuncSetAttribute(split_kernel<G, PAGED, CONS, KV, D, CPA>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem_optin);
+        if (r == cudaSuccess)
+            configured.fetch_or(bit, std::memory_order_release);
+        return r;
+    };
+    if (!(configured.load(std::memory_order_acquire) & bit) && (e = configure()) != cudaSuccess)
+        return e;
     // Programmatic dependent launch: the kernel's prologue may overlap the
     // previous kernel in the stream; it waits for it before reading inputs.
     cudaLaunchAttribute attr[1];
@@ -64,7 +89,14 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
     cfg.stream = c.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, CONS, KV, D, CPA>, p, tmk, tmv);
+    e = cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, CONS, KV, D, CPA>, p, tmk, tmv);
+    if (e == cudaErrorInvalidValue) {   // a refused launch leaves no sticky error: clear it and retry once
+        (void)cudaGetLastError();
+        if ((e = configure()) != cudaSuccess)
+            return e;
+        e = cudaLaunchKernelEx(&cfg, split_kernel<G, PAGED, CONS, KV, D, CPA>, p, tmk, tmv);
+    }
+    return e;
 }
 
 // One split-kernel variant per (layout, K/V element type, row dims D):

@@ -45,4 +45,19 @@ cudaError_t launch_merge(int group, int head_dim, const MergeParams &p, int grid
     }
 }
 
+// Merge of caller-supplied partial sets: one warp per query row.
+cudaError_t launch_merge_parts(int head_dim, const MergePartsParams &p, cudaStream_t stream)
+{
+    if (p.rows == 0)
+        return cudaSuccess;
+    const dim3 grid((unsigned)((p.rows + kMergePartsWarps - 1) / kMergePartsWarps)), block(kMergePartsWarps * 32);
+    switch (head_dim) {
+    case 64: merge_parts_kernel<64><<<grid, block, 0, stream>>>(p); break;
+    case 128: merge_parts_kernel<128><<<grid, block, 0, stream>>>(p); break;
+    case 256: merge_parts_kernel<256><<<grid, block, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace fd

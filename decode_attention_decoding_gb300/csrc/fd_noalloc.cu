@@ -34,38 +34,72 @@ using namespace fd;
 
 constexpr size_t kNoallocScratchBytes = FD_NOALLOC_SCRATCH_BYTES;
 constexpr int kD = 128;   // the one head_dim this entry point serves
-using HD = Shape<kD, kKvBf16>;
 
 // The scratch: device-error word, tile prefix, partial LSEs and partial outputs.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 struct NoallocDevice {
     unsigned char *scratch = nullptr;   // device address of g_noalloc_scratch
-    int sms = 0;
-    int smem_optin = 0;
+    DeviceInfo info;
+    unsigned long long ctx_id = 0;      // the context the address belongs to (0: unknown)
 };
 
 std::mutex g_mu;
 NoallocDevice g_devs[64];
 bool g_ready[64] = {};
 
-// Once per device, with that device current: resolve the array's device
-// address (in host code its name is only a host-side stand-in) and the
-// properties the launch needs.
+// The current CUDA context's id, which the driver never reuses within a
+// process (a context created after cudaDeviceReset gets a new one); 0 when
+// there is no current context or the driver lacks the query.
+unsigned long long current_context_id()
+{
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static const GetCurrentFn get_current = []() -> GetCurrentFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                           cudaSuccess && q == cudaDriverEntryPointSuccess
+                   ? reinterpret_cast<GetCurrentFn>(p)
+                   : nullptr;
+    }();
+    static const GetIdFn get_id = []() -> GetIdFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                       q == cudaDriverEntryPointSuccess
+                   ? reinterpret_cast<GetIdFn>(p)
+                   : nullptr;
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Once per device and context, with that device current: resolve the
+// array's device address (in host code its name is only a host-side
+// stand-in) and the properties the launch needs.  The address belongs to
+// the context that was current when it was resolved, so it is resolved again
+// when the device's context has changed (after cudaDeviceReset), and on
+// every call if the driver cannot tell contexts apart.
 fd_status noalloc_setup(NoallocDevice *out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return FD_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_ready[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_ready[dev] || ctx == 0 || ctx != g_devs[dev].ctx_id) {
         NoallocDevice d;
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return FD_ERR_CUDA;
+            return FD_ERR_CUDA;   // (this call also makes the device's primary context current)
         d.scratch = static_cast<unsigned char *>(p);
-        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        d.ctx_id = current_context_id();
+        if (cudaDeviceGetAttribute(&d.info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.info.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
                 cudaSuccess)
             return FD_ERR_CUDA;
         g_devs[dev] = d;
@@ -117,7 +151,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     fd_status st = noalloc_setup(&dev);
     if (st != FD_OK)
         return st;
-    const int num_ctas = dev.sms;
+    const int num_ctas = dev.info.sms;
     const NoallocLayout wl = noalloc_layout(batch, batch * num_kv_heads + num_ctas, group);
     if (wl.total > kNoallocScratchBytes)
         return FD_ERR_WORKSPACE_TOO_SMALL;   // shape needs more scratch than the fixed array holds
@@ -152,30 +186,14 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     // one query head per kv head, tensor cores for GQA groups.
     const int cons = group >= 2 ? kConsMma : kConsCudaCores;
 
-    // Shared-memory plan (same rule as the workspace entry points).
-    const size_t red = align_up((size_t)reduction_floats(cons, group, kD) * sizeof(float), 16);
-    const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
-    const size_t misc = 64;
-    const size_t fixed = 1024 + red + prefix + misc + 8;
-    if ((size_t)dev.smem_optin <= fixed)
-        return FD_ERR_UNSUPPORTED;
-    int ns = (int)(((size_t)dev.smem_optin - fixed) / (HD::kStageBytes + 2 * 8 + kMetaInts * sizeof(int)));
-    if (ns > kMaxStages)
-        ns = kMaxStages;
-    if (ns < 2)
-        return FD_ERR_UNSUPPORTED;
-    sp.num_stages = ns;
-    sp.off_red = (uint32_t)(ns * HD::kStageBytes);
-    sp.off_prefix = (uint32_t)(sp.off_red + red);
-    sp.off_bar = (uint32_t)(sp.off_prefix + prefix);
-    sp.off_meta = (uint32_t)(sp.off_bar + (2 * ns + 1) * 8);
-    sp.off_misc = (uint32_t)(sp.off_meta + ns * kMetaInts * sizeof(int));
-
+    // Shared-memory plan: the workspace entry points' rule, with the tiles per
+    // CTA estimated from the capacity (as fd_decode does without host lengths).
     SplitLaunch launch;
     launch.grid = num_ctas;
-    launch.smem_bytes = 1024 + sp.off_misc + misc;
-    launch.smem_optin = (size_t)dev.smem_optin;
     launch.stream = reinterpret_cast<cudaStream_t>(stream);
+    const double est_tiles = (double)batch * num_kv_heads * ceil_div(s_max, kTileTokens);
+    if ((st = plan_smem(dev.info, cons, group, kD, 2, batch, est_tiles / num_ctas, &sp, &launch)) != FD_OK)
+        return st;
 
     MergeParams mp;
     std::memset(&mp, 0, sizeof mp);   // no fused heads; every field defined

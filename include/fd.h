@@ -106,7 +106,9 @@ typedef struct fd_options {
      * workspace header and returns instead of hanging. */
     unsigned long long wait_timeout_ns;
     /* Optional cudaEvent_t handles recorded on `stream` immediately before
-     * and after the split kernel (for timing the kernel alone); NULL = none. */
+     * and after the split kernel (for timing the kernel alone); NULL = none.
+     * During a stream capture they become event-record nodes of the graph
+     * (cudaEventRecordExternal), recorded by every replay. */
     void *split_start_event;
     void *split_end_event;
     /* Element type of q, K and V (fd_dtype); 0 = bf16. */
@@ -122,17 +124,15 @@ typedef struct fd_options {
     int q_len;
 } fd_options;
 
-/* Test hook: CTA 0 announces more bytes for its first tile than it loads, so
- * its consumers' wait can never complete and must run out.  Never set it in
- * production; the outputs of such a call are undefined. */
-#define FD_FLAG_TEST_STARVE_FIRST_TILE 0x1u
+/* ---- User flags (fd_options.flags) ---- */
 
 /* Use the CUDA-core consumers for every group size.  By default GQA groups
  * (Hq/Hkv x q_len >= 2 query columns per kv head, rows of at least 128 bytes
  * or kv heads paired to reach them) run q.K^T and P.V on the tensor cores
- * (bf16 or fp16 MMA, fp32 accumulation, softmax weights rounded to the MMA
- * type for P.V), with any page size; this flag selects the all-fp32 CUDA-core
- * arithmetic instead (up to 8 query columns per kv head). */
+ * (bf16 or fp16 MMA, fp32 accumulation; for P.V each softmax weight is
+ * taken as a rounded part plus its rounded remainder in two MMAs, 16 or 22
+ * significant bits), with any page size; this flag selects the all-fp32
+ * CUDA-core arithmetic instead (up to 8 query columns per kv head). */
 #define FD_FLAG_CUDA_CORES 0x2u
 
 /* Tensor-core consumers: load each 64-dim part of a K/V tile as its own TMA
@@ -168,8 +168,19 @@ typedef struct fd_options {
  * wins if both are set. */
 #define FD_FLAG_FUSE_HEADS 0x10u
 
+/* ---- Test hooks (fd_options.flags): for the library's own tests only ---- */
+
+/* CTA 0 announces more bytes for its first tile than it loads, so its
+ * consumers' wait can never complete and must run out (the bounded-wait
+ * test).  Never set it in production; the outputs of such a call are
+ * undefined. */
+#define FD_FLAG_TEST_STARVE_FIRST_TILE 0x1u
+
 /*
- * Bytes of workspace that fd_decode / fd_decode_paged need for this shape.
+ * Bytes of workspace that fd_decode / fd_decode_paged (and their partial
+ * forms) need for this shape.  The pages allocate their split partials per
+ * call; this sizing call has no counterpart there: it lets the caller own one
+ * workspace for every call of a shape.
  * Pure host function (no CUDA call).  The size does not depend on the
  * lengths: it holds a 256-byte header, the per-request tile prefix and one
  * fp32 partial (Hq/Hkv rows of head_dim outputs plus their log-sum-exp) per
@@ -192,12 +203,17 @@ size_t fd_workspace_size_q(int batch, int num_q_heads, int num_kv_heads, int hea
 /*
  * Zero-fill a workspace (its sticky device-error word must start at zero).
  * Call once after allocating a workspace, before its first use.
- * Stream-ordered, asynchronous.
+ * Stream-ordered, asynchronous.  No counterpart on the pages (workspace
+ * ownership is this library's).
  */
 fd_status fd_workspace_init(void *workspace, size_t workspace_bytes, fd_stream_t stream);
 
 /*
- * Decode attention over a contiguous KV cache.
+ * Decode attention over a contiguous KV cache.  Arithmetic: "纯手搓 flash
+ * decoding sm120", sections 1-2 (split the sequence, partial O and LSE per
+ * split, pass-2 merge by LSE) with the online softmax of the handbook's
+ * FlashAttention section; layout [seq, head, dim] per request as in that
+ * article's problem statement.
  *   q            [batch, num_q_heads, head_dim] bf16 or fp16, device.
  *   k, v         [batch, s_max, num_kv_heads, head_dim] device, row-major, of
  *                q's type or FP8 codes (fd_options.kv_dtype).
@@ -226,7 +242,10 @@ fd_status fd_decode(const void *q, const void *k, const void *v,
                     const fd_options *opts, fd_stream_t stream);
 
 /*
- * Decode attention over a paged KV cache.
+ * Decode attention over a paged KV cache.  Indirection: the PagedAttention
+ * section of "FlashAttention 与推理算子" (token t of a request in physical
+ * block block_table[t / page_size], slot t % page_size); arithmetic as for
+ * fd_decode.
  *   k_pages, v_pages [num_pages, page_size, num_kv_heads, head_dim] device, of
  *                q's type or FP8 codes (fd_options.kv_dtype).
  *   block_table  [batch, max_blocks_per_seq] int32, device, row-major: token t
@@ -255,6 +274,79 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
                           float *o, float *lse,
                           void *workspace, size_t workspace_bytes,
                           const fd_options *opts, fd_stream_t stream);
+
+/*
+ * Sequence sharding: attention over one range of cache positions, and the
+ * merge of such partial results.  Sources: the handbook's Flash-Decoding
+ * section (split-K decode: each split keeps its normalised output and
+ * softmax statistics, and the splits are combined by them; exercise 2: a
+ * split that saw no token is skipped) and the pass-2 merge by log-sum-exp of
+ * "纯手搓 flash decoding sm120", section 2 (written out at
+ * fd_merge_partials).  A rank that holds cache positions [kv_begin, kv_end) of
+ * every request computes its partial with fd_decode_partial (or the paged
+ * form); the ranks exchange the partials (n sets of [rows, head_dim] outputs
+ * and [rows] LSEs, e.g. one all-gather) and fd_merge_partials combines them
+ * into the result fd_decode would give on the whole cache.
+ */
+
+/*
+ * fd_decode over the cache positions [kv_begin, min(L_b, kv_end)) of every
+ * request.  k and v hold the range: row t' of request b
+ * ([batch, s_max, num_kv_heads, head_dim]) is cache position kv_begin + t'.
+ * seq_lens are the requests' whole lengths L_b (device; NULL = every request
+ * has kv_begin + s_max tokens), so several new tokens (fd_options.q_len) keep
+ * their causal limits at the whole sequence's positions.  The range of
+ * request b holds n_b = min(L_b, kv_end) - kv_begin tokens (0 if negative),
+ * and n_b <= s_max is required (seq_lens_host: FD_ERR_INVALID_ARG; a device
+ * value: clamped and reported as FD_ERR_DEVICE_INPUT).
+ *   kv_begin, kv_end  0 <= kv_begin <= kv_end (INT32_MAX: to the end), and
+ *                kv_begin + s_max < 2^31; else FD_ERR_INVALID_ARG.
+ *   o_part       [batch, (q_len,) num_q_heads, head_dim] fp32: the output
+ *                normalised over the range.
+ *   lse_part     [batch, (q_len,) num_q_heads] fp32, natural log, required
+ *                (NULL: FD_ERR_INVALID_ARG).  A row that sees no position of
+ *                the range gets O = 0 and LSE = -inf.
+ * Workspace and every other argument as for fd_decode (the workspace size
+ * of the shape with max_kv_len = s_max).
+ */
+fd_status fd_decode_partial(const void *q, const void *k, const void *v,
+                            const int32_t *seq_lens_dev, const int32_t *seq_lens_host,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim, int s_max,
+                            int kv_begin, int kv_end, float scale, float *o_part, float *lse_part,
+                            void *workspace, size_t workspace_bytes,
+                            const fd_options *opts, fd_stream_t stream);
+
+/*
+ * fd_decode_paged over the cache positions [kv_begin, min(L_b, kv_end)):
+ * block_table row b maps the range's own tokens, token t' = position
+ * kv_begin + t' in page block_table[b][t' / page_size], slot t' % page_size,
+ * and n_b <= max_blocks_per_seq * page_size is required.  seq_lens_dev is
+ * required; everything else as for fd_decode_partial and fd_decode_paged.
+ */
+fd_status fd_decode_paged_partial(const void *q, const void *k_pages, const void *v_pages,
+                                  const int32_t *block_table, int max_blocks_per_seq,
+                                  const int32_t *seq_lens_dev, const int32_t *seq_lens_host,
+                                  int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int page_size, int num_pages, int kv_begin, int kv_end, float scale,
+                                  float *o_part, float *lse_part, void *workspace, size_t workspace_bytes,
+                                  const fd_options *opts, fd_stream_t stream);
+
+/*
+ * Merge num_parts partial sets into one result, for every one of `rows`
+ * query rows (batch x q_len x num_q_heads):
+ *     M = max_s lse_s,  LSE = M + ln sum_s exp(lse_s - M),
+ *     O = sum_s O_s exp(lse_s - LSE);
+ * a set with lse_s = -inf is skipped, and a row that no set saw gets O = 0,
+ * LSE = -inf.
+ *   o_parts      [num_parts, rows, head_dim] fp32, device, 16-byte aligned.
+ *   lse_parts    [num_parts, rows] fp32, device (natural log).
+ *   o            [rows, head_dim] fp32, device, 16-byte aligned, written.
+ *   lse          [rows] fp32, device, written, or NULL.
+ * num_parts >= 1 and rows >= 0 (FD_ERR_INVALID_ARG otherwise); head_dim 64,
+ * 128 or 256 (FD_ERR_UNSUPPORTED otherwise).  No workspace; stream-ordered.
+ */
+fd_status fd_merge_partials(const float *o_parts, const float *lse_parts, int num_parts, int rows,
+                            int head_dim, float *o, float *lse, fd_stream_t stream);
 
 /* Bytes of the fixed device scratch array used by fd_decode_noalloc. */
 #define FD_NOALLOC_SCRATCH_BYTES (8u << 20)
@@ -309,11 +401,13 @@ fd_status fd_decode_noalloc(const void *q, const void *k, const void *v,
  * SYNCHRONISES `stream` (it copies one word to the host).
  */
 fd_status fd_get_device_error(void *workspace, fd_stream_t stream);
+/* (No counterpart on the pages: their kernels have no bounded waits and no
+ * device-side input checks to report.) */
 
-/* Human-readable name of a status; never NULL. */
+/* Human-readable name of a status; never NULL.  No counterpart on the pages. */
 const char *fd_status_string(fd_status status);
 
-/* Library version, major*10000 + minor*100 + patch. */
+/* Library version, major*10000 + minor*100 + patch.  No counterpart on the pages. */
 int fd_version(void);
 
 #ifdef __cplusplus

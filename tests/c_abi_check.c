@@ -64,6 +64,26 @@ int main(void)
                FD_ERR_UNSUPPORTED,
            "16 columns on CUDA cores");
 
+    /* sequence sharding: a partial needs its LSE; the range is checked */
+    expect(fd_decode_partial(q, q, q, NULL, NULL, 2, 8, 2, 128, 64, 0, 100, 0.1f, o, NULL, buf, 1u << 30, NULL,
+                             NULL) == FD_ERR_INVALID_ARG,
+           "partial without LSE");
+    expect(fd_decode_partial(q, q, q, NULL, NULL, 2, 8, 2, 128, 64, 50, 40, 0.1f, o, o, buf, 1u << 30, NULL,
+                             NULL) == FD_ERR_INVALID_ARG,
+           "range end before its begin");
+    expect(fd_decode_partial(q, q, q, NULL, NULL, 0, 8, 2, 128, 64, 0, 100, 0.1f, o, o, buf, 1u << 30, NULL,
+                             NULL) == FD_OK,
+           "empty batch partial");
+    expect(fd_decode_paged_partial(q, q, q, (const int32_t *)q, 4, NULL, NULL, 2, 8, 2, 128, 16, 8, 0, 64, 0.1f,
+                                   o, o, buf, 1u << 30, NULL, NULL) == FD_ERR_INVALID_ARG,
+           "paged partial without lengths");
+    expect(fd_merge_partials((const float *)q, (const float *)q, 0, 4, 128, o, NULL, NULL) == FD_ERR_INVALID_ARG,
+           "merge of no sets");
+    expect(fd_merge_partials((const float *)q, (const float *)q, 2, 4, 96, o, NULL, NULL) == FD_ERR_UNSUPPORTED,
+           "merge head_dim 96");
+    expect(fd_merge_partials((const float *)q, (const float *)q, 2, 0, 128, o, NULL, NULL) == FD_OK,
+           "merge of no rows");
+
     if (failures == 0)
         printf("C ABI checks passed\n");
     return failures == 0 ? 0 : 1;

@@ -7,8 +7,14 @@ import torch
 
 import fd_synth as syn
 
-# Tolerances: O elementwise |o - r| <= ATOL + RTOL |r|, LSE absolute.
+# Tolerances (the stated bounds: max-abs error <= 1e-2 and max-rel error
+# <= 1e-2 on O, 1e-3 absolute on LSE).  O passes elementwise when
+# |o - r| <= ATOL + RTOL |r|, and in addition the relative error over the
+# elements with |r| >= REL_FLOOR must stay within O_MAX_REL: a relative
+# error is meaningless next to zero, and O entries are weighted means of
+# N(0,1) values, so many sit near it.
 O_ATOL, O_RTOL, LSE_ATOL = 1e-2, 1e-2, 1e-3
+O_MAX_REL, REL_FLOOR = 1e-2, 1e-2
 
 
 def dev_bf16(bits, device="cuda", dtype="bf16"):
@@ -51,12 +57,13 @@ def run(w, dev=None, **kw):
 
 
 def check(o, lse, ro, rl, what=""):
-    """Assert the tolerance; return (max_abs_O, max_rel_O over |r|>=1e-2, max_abs_LSE)."""
+    """Assert the tolerances; return (max_abs_O, max_rel_O over |r|>=1e-2, max_abs_LSE)."""
     err = np.abs(o - ro)
     bad = err > O_ATOL + O_RTOL * np.abs(ro)
     assert not bad.any(), f"{what}: {int(bad.sum())} O elements out of tolerance, max err {err.max():.3g}"
-    big = np.abs(ro) >= 1e-2
+    big = np.abs(ro) >= REL_FLOOR
     max_rel = float((err[big] / np.abs(ro[big])).max()) if big.any() else 0.0
+    assert max_rel <= O_MAX_REL, f"{what}: max relative O error {max_rel:.3g} over |r| >= {REL_FLOOR}"
     lse_err = 0.0
     if lse is not None:
         fin = np.isfinite(rl)

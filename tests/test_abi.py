@@ -187,6 +187,87 @@ def test_paged_argument_checks(lib, fd):
         assert call_paged(lib, page=ok_page, B=0) == E.FD_OK
 
 
+def call_partial(lib, **over):
+    a = dict(q=ALIGNED, k=ALIGNED, v=ALIGNED, sl=None, slh=None, B=2, hq=8, hkv=2, d=128, smax=64, t0=0,
+             t1=2 ** 31 - 1, scale=0.1, o=ALIGNED, lse=ALIGNED, ws=ALIGNED, wsb=1 << 30, opts=None)
+    a.update(over)
+    f = lib.fd_decode_partial
+    f.restype = ctypes.c_int
+    return f(ctypes.c_void_p(a["q"]), ctypes.c_void_p(a["k"]), ctypes.c_void_p(a["v"]), a["sl"], a["slh"],
+             a["B"], a["hq"], a["hkv"], a["d"], a["smax"], a["t0"], a["t1"], ctypes.c_float(a["scale"]),
+             ctypes.c_void_p(a["o"]), ctypes.c_void_p(a["lse"]), ctypes.c_void_p(a["ws"]),
+             ctypes.c_size_t(a["wsb"]), a["opts"], None)
+
+
+def call_paged_partial(lib, **over):
+    a = dict(q=ALIGNED, k=ALIGNED, v=ALIGNED, table=ALIGNED, mb=4, sl=ALIGNED, slh=None, B=2, hq=8,
+             hkv=2, d=128, page=16, npages=8, t0=0, t1=2 ** 31 - 1, scale=0.1, o=ALIGNED, lse=ALIGNED,
+             ws=ALIGNED, wsb=1 << 30, opts=None)
+    a.update(over)
+    f = lib.fd_decode_paged_partial
+    f.restype = ctypes.c_int
+    return f(ctypes.c_void_p(a["q"]), ctypes.c_void_p(a["k"]), ctypes.c_void_p(a["v"]),
+             ctypes.c_void_p(a["table"]), a["mb"], ctypes.c_void_p(a["sl"]), a["slh"], a["B"], a["hq"],
+             a["hkv"], a["d"], a["page"], a["npages"], a["t0"], a["t1"], ctypes.c_float(a["scale"]),
+             ctypes.c_void_p(a["o"]), ctypes.c_void_p(a["lse"]), ctypes.c_void_p(a["ws"]),
+             ctypes.c_size_t(a["wsb"]), a["opts"], None)
+
+
+def test_partial_argument_checks(lib, fd):
+    """The range entry points check the range and the host lengths against the
+    range's own capacity (n_b = min(L_b, kv_end) - kv_begin <= s_max)."""
+    E = fd
+    assert call_partial(lib, lse=0) == E.FD_ERR_INVALID_ARG          # a partial needs its LSE
+    assert call_partial(lib, t0=-1) == E.FD_ERR_INVALID_ARG
+    assert call_partial(lib, t0=10, t1=9) == E.FD_ERR_INVALID_ARG
+    assert call_partial(lib, t0=2 ** 31 - 64) == E.FD_ERR_INVALID_ARG  # kv_begin + s_max past int32
+    assert call_partial(lib, t0=10, t1=10, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL   # empty range: valid
+    assert call_partial(lib, d=96) == E.FD_ERR_UNSUPPORTED
+    # capacity is the range's: s_max 64 holds positions kv_begin .. kv_begin + 63
+    lens = (ctypes.c_int32 * 2)(74, 5)
+    assert call_partial(lib, slh=lens, t0=10, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
+    lens = (ctypes.c_int32 * 2)(75, 5)
+    assert call_partial(lib, slh=lens, t0=10) == E.FD_ERR_INVALID_ARG
+    lens = (ctypes.c_int32 * 2)(1000, 5)                             # clipped by kv_end
+    assert call_partial(lib, slh=lens, t0=10, t1=70, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
+    lens = (ctypes.c_int32 * 2)(-1, 5)
+    assert call_partial(lib, slh=lens, t0=10) == E.FD_ERR_INVALID_ARG
+    assert call_partial(lib, B=0) == E.FD_OK
+    assert call_paged_partial(lib, lse=0) == E.FD_ERR_INVALID_ARG
+    assert call_paged_partial(lib, sl=0) == E.FD_ERR_INVALID_ARG
+    assert call_paged_partial(lib, t0=5, t1=4) == E.FD_ERR_INVALID_ARG
+    assert call_paged_partial(lib, page=24) == E.FD_ERR_UNSUPPORTED
+    lens = (ctypes.c_int32 * 2)(64 + 100, 0)                         # 4 pages of 16 from position 100
+    assert call_paged_partial(lib, slh=lens, t0=100, wsb=1024) == E.FD_ERR_WORKSPACE_TOO_SMALL
+    lens = (ctypes.c_int32 * 2)(65 + 100, 0)
+    assert call_paged_partial(lib, slh=lens, t0=100) == E.FD_ERR_INVALID_ARG
+    assert call_paged_partial(lib, B=0) == E.FD_OK
+
+
+def test_merge_partials_argument_checks(lib, fd):
+    E = fd
+    f = lib.fd_merge_partials
+    f.restype = ctypes.c_int
+
+    def call(op=ALIGNED, lp=ALIGNED, n=2, rows=4, d=128, o=ALIGNED, lse=ALIGNED):
+        return f(ctypes.c_void_p(op), ctypes.c_void_p(lp), n, rows, d, ctypes.c_void_p(o), ctypes.c_void_p(lse),
+                 None)
+
+    assert call(op=0) == E.FD_ERR_INVALID_ARG
+    assert call(lp=0) == E.FD_ERR_INVALID_ARG
+    assert call(o=0) == E.FD_ERR_INVALID_ARG
+    assert call(n=0) == E.FD_ERR_INVALID_ARG
+    assert call(rows=-1) == E.FD_ERR_INVALID_ARG
+    assert call(op=ALIGNED + 4) == E.FD_ERR_INVALID_ARG
+    assert call(o=ALIGNED + 8) == E.FD_ERR_INVALID_ARG
+    assert call(lp=ALIGNED + 2) == E.FD_ERR_INVALID_ARG
+    for d in (32, 96, 512):
+        assert call(d=d) == E.FD_ERR_UNSUPPORTED
+    for d in (64, 128, 256):
+        assert call(d=d, rows=0) == E.FD_OK       # nothing to merge: no launch
+    assert call(rows=0, lse=0) == E.FD_OK
+
+
 # ---------------------------------------------------------------------------
 # The split schedule (fd_sched.h), through a small g++-compiled shim
 # ---------------------------------------------------------------------------

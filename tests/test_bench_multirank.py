@@ -79,3 +79,20 @@ def test_reference_arm_rank1_prints_nothing():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_oracle_sample_bytes_count_each_kv_row_once():
+    """The CPU baseline's bytes follow the GPU's algorithmic count: every
+    (request, kv head) unit's K+V rows once, not once per query row of a GQA
+    group, plus its q rows, O rows and LSEs."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import fd_synth as syn
+    w = syn.make_contiguous(950, 3, 8, 2, 64, 100, [100, 7, 50])
+    items, by, n = bench.oracle_units(w, 10 ** 6)
+    assert n == 3 * 2 and items.shape == (3 * 8, 4)
+    bc = bench.byte_counts(w, 152)
+    assert by == bc["kv"] + bc["q"] + bc["out"]
+    items, by, n = bench.oracle_units(w, 1)   # request 0, kv head 0: its four query rows
+    assert n == 1 and sorted(items[:, 1].tolist()) == [0, 1, 2, 3]
+    assert by == 100 * 64 * 2 * 2 + 4 * (64 * 2 + 64 * 4 + 4)
