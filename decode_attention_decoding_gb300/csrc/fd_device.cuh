@@ -148,6 +148,25 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *desc, uint
         : "memory");
 }
 
+// Prefetch one box of a tiled tensor into L2 (3-D / 4-D coordinates).  A
+// hint: nothing lands in shared memory and nothing signals completion; the
+// unit skips elements outside the tensor.
+__device__ __forceinline__ void tma_prefetch_3d(const void *desc, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(desc)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const void *desc, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(desc)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 // L2 policy for data read exactly once (the KV cache stream).
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {

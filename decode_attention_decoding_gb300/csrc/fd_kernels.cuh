@@ -149,6 +149,7 @@ struct SplitParams {
     int col_code[kMaxColumnSlots];   // new token i | part << 4 | head g << 8, or -1 (host-computed)
     int q_f16;        // FP8 caches: 1 when q is fp16, 0 when bf16
     float v_scale;    // multiplies O (an FP8 cache's V dequantisation scale; 1 otherwise)
+    int prefetch_tiles;   // first tiles of a CTA prefetched into L2 before the dependency wait (0: none)
     // A token range (the partial entry points): the layout holds cache
     // positions kv_begin, kv_begin + 1, .. of each request at its rows 0, 1,
     // .., and the call covers positions [kv_begin, min(L_b, kv_end)).
@@ -222,10 +223,9 @@ struct ReqLen {
 };
 
 template <class P>
-__device__ __forceinline__ ReqLen req_len(const P &p, int b, unsigned int *report)
+__device__ __forceinline__ ReqLen req_len_of(const P &p, int L, unsigned int *report)
 {
     const int off = p.range_on ? p.kv_begin : 0;
-    int L = p.seq_lens ? p.seq_lens[b] : off + p.cap;
     bool bad = L < 0;
     L = max(L, 0);
     int n = p.range_on ? max(min(L, p.kv_end) - off, 0) : L;
@@ -238,6 +238,12 @@ __device__ __forceinline__ ReqLen req_len(const P &p, int b, unsigned int *repor
     if (bad && report)
         atomicOr(report, kErrLength);
     return ReqLen{L, n};
+}
+
+template <class P>
+__device__ __forceinline__ ReqLen req_len(const P &p, int b, unsigned int *report)
+{
+    return req_len_of(p, p.seq_lens ? p.seq_lens[b] : (p.range_on ? p.kv_begin : 0) + p.cap, report);
 }
 
 // Every lane waits (so each acquires the barrier's phase); the outcome is
@@ -266,7 +272,10 @@ __device__ __forceinline__ bool consumer_sync(uint32_t cbar, uint32_t &cph, uint
 
 // prefix[b] = Hkv * (tiles of requests < b), prefix[B] = total tiles.
 // All NTHREADS threads of the block take part.  scan_tmp: NTHREADS / 32 ints.
-template <int NTHREADS>
+// HINT: a plan for L2 prefetches only, made before the kernels ahead in the
+// stream have completed: the lengths are read around L1 (no stale line stays
+// there), nothing is reported and the workspace is not written.
+template <int NTHREADS, bool HINT = false>
 __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, int *scan_tmp)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -274,10 +283,18 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
     const int B = p.batch;
     const int per = ceil_div(B, nthreads);
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
-    unsigned int *report = blockIdx.x == 0 ? p.ws_err : nullptr;
+    unsigned int *report = blockIdx.x == 0 && !HINT ? p.ws_err : nullptr;
+    auto tiles_of = [&](int b, unsigned int *rep) -> int {
+        if constexpr (HINT) {
+            const int L = p.seq_lens ? __ldcg(p.seq_lens + b) : (p.range_on ? p.kv_begin : 0) + p.cap;
+            return ceil_div(req_len_of(p, L, nullptr).n, kTileTokens);
+        } else {
+            return ceil_div(req_len(p, b, rep).n, kTileTokens);
+        }
+    };
     int local = 0;
     for (int b = b0; b < b1; ++b)
-        local += ceil_div(req_len(p, b, report).n, kTileTokens);
+        local += tiles_of(b, report);
     int x = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -303,12 +320,12 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
     int run = x - local + (warp > 0 ? scan_tmp[warp - 1] : 0);
     for (int b = b0; b < b1; ++b) {
         prefix[b] = run * p.hkv;
-        run += ceil_div(req_len(p, b, nullptr).n, kTileTokens);
+        run += tiles_of(b, nullptr);
     }
     if (tid == nthreads - 1)
         prefix[B] = run * p.hkv;
     __syncthreads();
-    if (blockIdx.x == 0)
+    if (blockIdx.x == 0 && !HINT)
         for (int b = tid; b <= B; b += nthreads)
             p.ws_prefix[b] = prefix[b];
 }
@@ -537,6 +554,59 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
     if (lane == 0) {
         for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
             mbar_wait_bounded(full0 + 8 * (k % NS), (uint32_t)((k / NS) & 1), p.timeout_ns, nullptr);
+    }
+}
+
+// L2 prefetch of tiles [t_begin, t_end) of this CTA, issued by the producer
+// warp before the kernel waits for the kernels ahead of it in the stream:
+// the same boxes split_producer loads, one (tile, page, box) item per lane.
+// The plan (prefix) and the block-table entries are read before that wait
+// and may be stale; a prefetch only fills L2, which is where device memory
+// is kept coherent, so a stale plan wastes bandwidth and never changes a
+// result.  Table entries are read around L1 and entries outside the pool are
+// skipped.  Pages of 1 or 2 tokens gathered row by row are not prefetched.
+template <bool PAGED, bool SW128, int D, int KV>
+__device__ __forceinline__ void split_prefetch(const SplitParams &p, const CUtensorMap *tmk,
+                                               const CUtensorMap *tmv, const int *prefix, int t_begin,
+                                               int t_end, int lane)
+{
+    using HD = Shape<D, KV>;
+    if (PAGED && p.gather4)
+        return;
+    const int box_log2 = (SW128 && !p.box4d) ? 1 + (HD::kParts == 4 ? 2 : HD::kParts - 1) : 1;
+    const int P = p.page_size;
+    const bool small_pages = PAGED && P < kTileTokens;
+    const int pages_log2 = small_pages ? 6 - p.page_log2 : 0;   // pages per tile (log2)
+    const int per_tile_log2 = pages_log2 + box_log2;
+    const int items = (t_end - t_begin) << per_tile_log2;
+    for (int i = lane; i < items; i += 32) {
+        const int t = t_begin + (i >> per_tile_log2);
+        const int box = i & ((1 << box_log2) - 1), pg = (i >> box_log2) & ((1 << pages_log2) - 1);
+        const int b = request_of_tile(prefix, p.batch, t);
+        const int nb = (prefix[b + 1] - prefix[b]) / p.hkv;
+        const int h = (t - prefix[b]) / nb, j = (t - prefix[b]) - h * nb;
+        const int token0 = j * kTileTokens;
+        int row;
+        if constexpr (PAGED) {
+            const int tok = token0 + (pg << p.page_log2);
+            const int idx = small_pages ? tok >> p.page_log2 : tok / P;
+            if (idx >= p.max_blocks)
+                continue;
+            const int e = __ldcg(p.block_table + (size_t)b * p.max_blocks + idx);
+            if (e < 0 || e >= p.num_pages)
+                continue;
+            row = e * P + (small_pages ? 0 : token0 % P);
+        } else {
+            row = b * p.s_max + token0;
+        }
+        const bool is_v = SW128 && !p.box4d ? box >= HD::kParts : (box & 1) != 0;
+        const CUtensorMap *map = is_v ? tmv : tmk;
+        if (SW128 && p.box4d)
+            tma_prefetch_4d(map, 0, row, 0, h);
+        else if (SW128)
+            tma_prefetch_3d(map, (box & (HD::kParts - 1)) * HD::kPartElems, h, row);
+        else
+            tma_prefetch_3d(map, 0, h, row);
     }
 }
 
@@ -1485,8 +1555,21 @@ __global__ void __launch_bounds__(CPA ? kSplitThreadsCpAsync : kSplitThreads, 1)
         mbar_init_fence();
     }
     // Launched as a programmatic dependent of the previous kernel in the
-    // stream: everything above overlapped its tail; inputs and the workspace
-    // are touched only after it has completed.
+    // stream: everything up to the wait overlaps its tail, and inputs and the
+    // workspace are touched only after it has completed -- except for L2
+    // prefetches of this CTA's first tiles, planned from the lengths as they
+    // read now (split_prefetch), so that the first loads after the wait find
+    // their data in L2.
+    if constexpr (!CPA) {
+        if (p.prefetch_tiles > 0) {
+            build_prefix<kThreads, true>(p, prefix, misc + 1);   // ends with __syncthreads
+            int pb, pe;
+            cta_tile_range(prefix[p.batch], (int)gridDim.x, (int)blockIdx.x, &pb, &pe);
+            if (warp == kConsumerWarps && pb < pe)
+                split_prefetch<PAGED, CONS != kConsCudaCores, D, KV>(p, &tmk, &tmv, prefix, pb,
+                                                                     min(pe, pb + p.prefetch_tiles), lane);
+        }
+    }
     pdl_wait_prior_grid();
     // The merge kernel may launch now; it waits for this grid on its own.  Its
     // early part reads the lengths, which the kernels before this one (now

@@ -25,8 +25,9 @@ struct DeviceInfo {
 };
 
 // Calls with fewer (estimated) KV tiles per split CTA than this count as
-// short: they keep less K/V in flight per CTA, and kv heads are not fused
-// for them (fd_api.cu).
+// short: they keep less K/V in flight per CTA, kv heads are not fused for
+// them, and their CTAs prefetch nothing before the dependency wait
+// (fd_api.cu).
 constexpr double kFuseMinTilesPerCta = 24.0;
 
 // Shared-memory plan of the split kernel (fd_api.cu): pipeline stages, the

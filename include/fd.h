@@ -168,6 +168,13 @@ typedef struct fd_options {
  * wins if both are set. */
 #define FD_FLAG_FUSE_HEADS 0x10u
 
+/* Do not prefetch.  By default, in calls of at least 24 KV tiles per split
+ * CTA, each split CTA asks L2 for its first KV tiles while it waits for the
+ * kernels ahead of it in the stream to complete (a plan made from the
+ * lengths and block table as they read at that moment; a stale plan only
+ * costs bandwidth).  Results are identical; for comparisons only. */
+#define FD_FLAG_NO_PREFETCH 0x40u
+
 /* ---- Test hooks (fd_options.flags): for the library's own tests only ---- */
 
 /* CTA 0 announces more bytes for its first tile than it loads, so its
@@ -381,8 +388,11 @@ fd_status fd_merge_partials(const float *o_parts, const float *lse_parts, int nu
  * bytes, each region rounded up to 256 bytes; a larger shape returns
  * FD_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  * The first call on each device resolves the array's device address
- * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture.
+ * (cudaGetSymbolAddress) and caches it with the device's current context;
+ * make that first call before any stream capture.  A call that finds a
+ * different context (the device was reset with cudaDeviceReset) resolves the
+ * address again, so make the first call after a reset before any capture
+ * too.
  * Every call on a device shares the one array, which keeps the previous
  * call's contents; each call clears the part that must start at zero (the
  * status word) itself.  Calls whose kernels can overlap on the GPU (for

@@ -246,3 +246,53 @@ def test_one_workspace_across_many_calls_and_split_patterns():
         ro, rl = oracle.attend(w, threads=8)
         check(o, l, ro, rl, f"call {i}")
     assert fd.fd_get_device_error(ws) == fd.FD_OK
+
+
+NO_PREFETCH = 0x40   # FD_FLAG_NO_PREFETCH
+
+
+@pytest.mark.parametrize("flags", [0, CUDA_CORES])
+@pytest.mark.parametrize("page", [0, 16, 64, 128])
+def test_prefetch_before_the_wait_changes_no_result(page, flags):
+    """The L2 prefetch of each CTA's first tiles (issued before the
+    dependency wait, in calls of at least 24 tiles per CTA: 140 tiles on 3
+    CTAs here) is a hint: results are bitwise equal without it."""
+    w = syn.make_contiguous(480 + page, len(RAGGED), 16, 4, 128, 1024, RAGGED)
+    if page:
+        w = contig_to_paged(w, page, perm_seed=page, poison=True)
+    a = run(w, num_ctas=3, flags=flags)
+    b = run(w, num_ctas=3, flags=flags | NO_PREFETCH)
+    ro, rl = oracle.attend(w, threads=8)
+    check(a[0], a[1], ro, rl, f"prefetch P={page}")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_lengths_and_cache_rewritten_between_back_to_back_calls():
+    """Back-to-back calls on one stream whose lengths, block table and cache
+    are rewritten between them by device copies: every call sees its own
+    inputs (the prefetch plan made before a call's dependency wait may be
+    stale; the loads after it are not)."""
+    import decode_attention_decoding_gb300 as fd
+    # 124 and 130 pages in use: padded to one pool size
+    wa = contig_to_paged(syn.make_contiguous(490, 4, 8, 2, 128, 1024, [1024, 7, 300, 640]), 16, perm_seed=1,
+                         extra_pages=9)
+    wb = contig_to_paged(syn.make_contiguous(491, 4, 8, 2, 128, 1024, [64, 1000, 0, 999]), 16, perm_seed=2,
+                         extra_pages=3)
+    assert wa.k.shape == wb.k.shape and wa.block_table.shape == wb.block_table.shape
+    da, db = to_device(wa), to_device(wb)
+    cur = {k: v.clone() for k, v in da.items()}
+    ws = fd.make_workspace(4, 8, 2, 128, wa.block_table.shape[1] * 16, 16)
+    outs = []
+    for i in range(6):
+        src = da if i % 2 == 0 else db
+        for k in cur:                      # stream-ordered rewrite of every input
+            cur[k].copy_(src[k])
+        o, l = fd.fd_decode_paged(cur["q"], cur["k"], cur["v"], cur["block_table"], cur["seq_lens"],
+                                  scale=wa.scale, workspace=ws, num_ctas=2)   # 64 tiles per CTA: prefetching
+        outs.append((o.clone(), l.clone()))
+    torch.cuda.synchronize()
+    for i, (o, l) in enumerate(outs):
+        w = wa if i % 2 == 0 else wb
+        ro, rl = oracle.attend(w, threads=8)
+        check(o.cpu().numpy().astype(np.float64), l.cpu().numpy().astype(np.float64), ro, rl, f"call {i}")
+    assert fd.fd_get_device_error(ws) == fd.FD_OK
