@@ -138,7 +138,7 @@ def kernel_hash():
 def bench_workload(args):
     """The workload the arguments name: one of the five configurations, with
     an FP8 cache (--kv) and re-paged into pages of --page tokens when asked."""
-    w = syn.make_config(args.config, kv_dtype=args.kv if args.kv != "bf16" else None)
+    w = syn.make_config(args.config, kv_dtype=args.kv if args.kv != "bf16" else None, shrink=args.shrink)
     if args.page:
         w = syn.repage(w, args.page, perm_seed=syn.seed_for(args.config, syn.TENSOR_PERM) + args.page)
     return w
@@ -500,7 +500,7 @@ def run_ours(args, rank, world):
     # Every benchmark workload under the same protocol (one GPU only: under
     # torchrun the ranks run the headline replicas alone).
     workloads = None
-    if world == 1 and args.workloads != "none" and not args.page:
+    if world == 1 and args.workloads != "none" and not args.page and args.shrink == 1:
         workloads = {}
         for c in [int(x) for x in args.workloads.split(",")]:
             name = syn.CONFIG_NAMES[c]
@@ -525,7 +525,8 @@ def run_ours(args, rank, world):
                                             else "bf16"),
             "data": "synthetic (seeded N(0,1) bf16" + (", quantised once to FP8)" if fp8 else ")"),
             "impl": "ours",
-            "config": {"workload": syn.CONFIG_NAMES[args.config], "batch": B, "num_q_heads": hq,
+            "config": {"workload": syn.CONFIG_NAMES[args.config] + (f"_shrink{args.shrink}" if args.shrink > 1 else ""),
+                       "batch": B, "num_q_heads": hq,
                        "num_kv_heads": hkv, "head_dim": d,
                        "kv_lens": ("uniform " + str(int(w.seq_lens[0]))) if len(set(w.seq_lens.tolist())) == 1
                        else f"ragged sum={int(w.seq_lens.sum())}",
@@ -734,6 +735,9 @@ def main():
     ap.add_argument("--page", type=int, default=0,
                     help="re-page the workload's K/V into shuffled pages of this many tokens "
                          "(a divisor of 64 or a multiple of 64; 0 keeps its own layout)")
+    ap.add_argument("--shrink", type=int, default=1,
+                    help="divide the workload's lengths by this factor (a smaller case of the same launch "
+                         "shape, for profiler captures; never the benchmark's own numbers)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-e2e", action="store_true")

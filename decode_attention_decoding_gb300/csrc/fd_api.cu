@@ -140,14 +140,15 @@ fd_status encode_kv_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k, cons
 
 constexpr size_t kMergeRoomBytes = 32u * 1024u;   // shared memory left beside a split CTA
 constexpr size_t kShortCallInFlightBytes = 96u * 1024u;   // K/V in flight per CTA on short calls
-constexpr int kPrefetchStages = 4;   // tiles prefetched before the dependency wait, in pipeline stages
-constexpr size_t kPrefetchBytes = 768u * 1024u;   // at most this much K/V prefetched per CTA
+constexpr int kPrefetchStages = 4;   // long calls: tiles prefetched before the dependency wait, in stages
+constexpr int kPrefetchTiles = 24;    // at most this many tiles prefetched per CTA
+constexpr size_t kShortCallBytes = 1u << 20;   // calls with less K/V per split CTA are short
 
 // Shared-memory plan of the split kernel for the call's consumers, group,
 // head_dim, K/V element size and batch; fills the offsets and stage count in
 // sp and the byte size in launch.
 fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_bytes, int batch,
-                    double tiles_per_cta, SplitParams *sp, SplitLaunch *launch)
+                    double tiles_per_cta, double kv_bytes_per_cta, SplitParams *sp, SplitLaunch *launch)
 {
     const size_t stage_bytes = 2u * kTileTokens * (size_t)elem_bytes * (size_t)d;   // K and V tiles
     const size_t red = align_up((size_t)reduction_floats(cons, group, d) * sizeof(float), 16);
@@ -187,18 +188,27 @@ fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_
     if (ns < 2)
         return FD_ERR_UNSUPPORTED;
     sp->num_stages = ns;
-    // L2 prefetch before the dependency wait (long calls only): the tiles the
-    // first loads after the wait ask for, and three times as many again, at
-    // most kPrefetchBytes per CTA.  Measured on GB300 (same box, us per call,
-    // without -> with 1, 2, 4, 8 stages' worth): ragged GQA-4 (workload 3)
-    // 53.6 -> 50.2, 49.3, 48.2, 49.1; MHA 1 GiB 159.0 -> 156.0, 155.5, 155.0,
-    // 155.8; paged GQA-4 313.2 -> 310.7, 310.0, 309.3, 313.7; GQA-8 1 GiB
-    // 164.8 -> 164.2, 164.2, 164.9, 168.7.  A short call (MHA 64 MiB, 13.5
-    // tiles per CTA) lost 5-20%: its split CTAs launch beside the previous
-    // call's, a whole call early, and their prefetches only compete with it.
-    const bool prefetch = !(sp->flags & FD_FLAG_NO_PREFETCH) && tiles_per_cta >= kFuseMinTilesPerCta;
-    const int cap_tiles = (int)(kPrefetchBytes / stage_bytes);
-    sp->prefetch_tiles = prefetch ? (kPrefetchStages * ns < cap_tiles ? kPrefetchStages * ns : cap_tiles) : 0;
+    // L2 prefetch before the dependency wait, and when the merge lets the next
+    // call launch.  Measured on GB300 (same box, us per call):
+    //  * Long calls (over kShortCallBytes of K/V per CTA): the merge lets the
+    //    next call launch at once, so its split CTAs take each SM as this
+    //    call's CTA leaves it, and they prefetch kPrefetchStages stages' worth
+    //    of tiles (at most kPrefetchTiles).  Without -> with 1, 2, 4, 8
+    //    stages' worth: ragged GQA-4 (workload 3) 53.6 -> 50.2, 49.3, 48.2,
+    //    49.1; MHA 1 GiB 159.0 -> 156.0, 155.5, 155.0, 155.8; paged GQA-4 313.2
+    //    -> 310.7, 310.0, 309.3, 313.7; GQA-8 1 GiB 164.8 -> 164.2, 164.2,
+    //    164.9, 168.7.
+    //  * Short calls: their split CTAs fit two to an SM, so the next call's
+    //    CTAs launched beside this call's a whole call early and their
+    //    prefetches only competed with it (MHA 64 MiB: 16.7 -> 20.0 us).  The
+    //    merge therefore lets the next call launch only once this call's split
+    //    grid is complete, and one stage's worth is prefetched: 16.7 -> 15.7
+    //    us (two stages 16.1, four 17.1); FP8 ragged GQA-4 35.3 -> 34.7.
+    const bool short_call = kv_bytes_per_cta < (double)kShortCallBytes;
+    launch->late_trigger = short_call ? 1 : 0;
+    int pf = short_call ? ns : kPrefetchStages * ns;
+    pf = pf < kPrefetchTiles ? pf : kPrefetchTiles;
+    sp->prefetch_tiles = (sp->flags & FD_FLAG_NO_PREFETCH) ? 0 : pf;
     sp->off_red = (uint32_t)(ns * stage_bytes);
     sp->off_prefix = (uint32_t)(sp->off_red + red);
     sp->off_bar = (uint32_t)(sp->off_prefix + prefix);
@@ -515,8 +525,9 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
         return FD_ERR_UNSUPPORTED;   // over 8 columns need the tensor-core consumers
     cp->launch.grid = num_ctas;
     cp->launch.stream = reinterpret_cast<cudaStream_t>(stream);
-    fd_status st = plan_smem(dev, cp->cons, group, d, eb, batch, (double)est_tiles / num_ctas, &sp,
-                             &cp->launch);
+    const double kv_bytes = (double)est_tiles * 2.0 * kTileTokens * head_dim * eb;   // unfused tiles
+    fd_status st = plan_smem(dev, cp->cons, group, d, eb, batch, (double)est_tiles / num_ctas,
+                             kv_bytes / num_ctas, &sp, &cp->launch);
     if (st != FD_OK)
         return st;
 
@@ -539,6 +550,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     std::memcpy(mp.col_code, sp.col_code, sizeof mp.col_code);
     mp.seq_lens = seq_lens_dev;
     mp.cap = cap;
+    mp.late_trigger = cp->launch.late_trigger;
     mp.range_on = sp.range_on;
     mp.kv_begin = sp.kv_begin;
     mp.kv_end = sp.kv_end;

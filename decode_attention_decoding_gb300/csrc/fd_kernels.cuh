@@ -169,6 +169,9 @@ struct MergeParams {
     const int32_t *seq_lens;   // as in SplitParams (small batches: segment geometry)
     int cap;
     int range_on, kv_begin, kv_end;   // as in SplitParams
+    // 1: let the next kernel in the stream launch only once this grid's wait
+    // has returned (the split grid is complete) rather than at once.
+    int late_trigger;
 };
 
 constexpr int kMergeDirectBatch = 32;   // batches this small: segment geometry from the lengths
@@ -1636,8 +1639,13 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
             s_geo[2] = x * p.hkv;
     }
     __syncthreads();
-    pdl_launch_dependents();   // the next call's split kernel may start its prologue
+    // The next call's split kernel may start its prologue (and its L2
+    // prefetch) now, or, for short calls, once the split grid is complete.
+    if (!p.late_trigger)
+        pdl_launch_dependents();
     pdl_wait_prior_grid();
+    if (p.late_trigger)
+        pdl_launch_dependents();
     int pb, pe, T;
     if (small) {
         pb = s_geo[0];

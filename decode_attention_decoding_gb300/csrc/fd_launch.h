@@ -16,6 +16,7 @@ struct SplitLaunch {
     size_t smem_bytes;     // dynamic shared memory per CTA
     size_t smem_optin;     // the device's opt-in maximum (set once per kernel)
     cudaStream_t stream;
+    int late_trigger;      // the merge lets the next kernel launch only after its wait (MergeParams)
 };
 
 // Device properties a launch plan needs.
@@ -25,17 +26,18 @@ struct DeviceInfo {
 };
 
 // Calls with fewer (estimated) KV tiles per split CTA than this count as
-// short: they keep less K/V in flight per CTA, kv heads are not fused for
-// them, and their CTAs prefetch nothing before the dependency wait
-// (fd_api.cu).
+// short: they keep less K/V in flight per CTA and kv heads are not fused for
+// them (fd_api.cu).
 constexpr double kFuseMinTilesPerCta = 24.0;
 
 // Shared-memory plan of the split kernel (fd_api.cu): pipeline stages, the
-// offsets of every region in sp, and the byte size in launch, for the call's
-// consumers (kCons*), column group, row dims d, K/V element size, batch and
-// estimated tiles per split CTA.  FD_ERR_UNSUPPORTED if two stages do not fit.
+// offsets of every region in sp, the L2 prefetch before the dependency wait
+// (sp->prefetch_tiles), and the byte size and merge trigger in launch, for
+// the call's consumers (kCons*), column group, row dims d, K/V element size,
+// batch, and the estimated tiles and K/V bytes per split CTA.
+// FD_ERR_UNSUPPORTED if two stages do not fit.
 fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_bytes, int batch,
-                    double tiles_per_cta, SplitParams *sp, SplitLaunch *launch);
+                    double tiles_per_cta, double kv_bytes_per_cta, SplitParams *sp, SplitLaunch *launch);
 
 // K and V tensor maps of a call (fd_api.cu): rows are (token, kv head)
 // pairs of d elements of type kv (kKv*), loaded box_rows tokens at a time.

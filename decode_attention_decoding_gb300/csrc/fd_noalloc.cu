@@ -192,7 +192,8 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     launch.grid = num_ctas;
     launch.stream = reinterpret_cast<cudaStream_t>(stream);
     const double est_tiles = (double)batch * num_kv_heads * ceil_div(s_max, kTileTokens);
-    if ((st = plan_smem(dev.info, cons, group, kD, 2, batch, est_tiles / num_ctas, &sp, &launch)) != FD_OK)
+    if ((st = plan_smem(dev.info, cons, group, kD, 2, batch, est_tiles / num_ctas,
+                        est_tiles * 2.0 * kTileTokens * kD * 2 / num_ctas, &sp, &launch)) != FD_OK)
         return st;
 
     MergeParams mp;
@@ -212,6 +213,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     mp.g_real = group;
     mp.n_cols = group;
     mp.fuse_f = 1;
+    mp.late_trigger = launch.late_trigger;
     for (int n = 0; n < kMaxColumnSlots; ++n)
         mp.col_code[n] = n < group ? n << 8 : -1;
 

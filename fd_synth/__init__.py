@@ -451,23 +451,30 @@ def quantize_kv(w: Workload, fmt: str, scale: float, workers: int | None = None)
 FP8_CONFIG_SCALE = 0.125   # N(0,1) values (and workload 5's x8 keys) stay inside E4M3's range
 
 
-def make_config(config_id: int, kv_dtype: str | None = None) -> Workload:
+def make_config(config_id: int, kv_dtype: str | None = None, shrink: int = 1) -> Workload:
     """Build benchmark workload 1..5 at full size (optionally with an FP8 cache
-    quantised from the same values)."""
+    quantised from the same values).  shrink > 1 divides every length and
+    capacity by it (at least 64 tokens each where the workload has one long
+    request): the same shapes and structure, a smaller case for profiling."""
     if kv_dtype in ("e4m3", "e5m2"):
-        return quantize_kv(make_config(config_id), kv_dtype, FP8_CONFIG_SCALE)
+        return quantize_kv(make_config(config_id, shrink=shrink), kv_dtype, FP8_CONFIG_SCALE)
+    sh = max(1, int(shrink))
     lens = config_lens(config_id)
-    name = CONFIG_NAMES[config_id]
+    if sh > 1:
+        lens = np.maximum(lens // sh, 1 if config_id in (3, 4) else 64).astype(np.int32)
+    name = CONFIG_NAMES[config_id] + (f"_shrink{sh}" if sh > 1 else "")
     if config_id in (1, 2):
         return make_contiguous(config_id, 1, 32, 32, 128, int(lens[0]), lens, name)
     if config_id == 3:
-        return make_contiguous(3, 16, 32, 8, 128, 8192, lens, name)
+        return make_contiguous(3, 16, 32, 8, 128, max(8192 // sh, int(lens.max())), lens, name)
     if config_id == 4:
-        return make_paged(4, 64, 32, 8, 128, 16, lens, (16384 + 15) // 16, name)
+        cap = max(16384 // sh, int(lens.max()))
+        return make_paged(4, 64, 32, 8, 128, 16, lens, (cap + 15) // 16, name)
     if config_id == 5:
-        w = make_paged(5, 1, 64, 8, 128, 64, lens, 262144 // 64, name)
-        n_scaled = int(0.01 * 262144)
-        toks = np.sort(choose(seed_for(5, TENSOR_MASK), 262144, n_scaled))
+        L = int(lens[0])
+        w = make_paged(5, 1, 64, 8, 128, 64, lens, (L + 63) // 64, name)
+        n_scaled = int(0.01 * L)
+        toks = np.sort(choose(seed_for(5, TENSOR_MASK), L, n_scaled))
         _scale_keys_paged_fast(w, 0, toks, 8.0)
         w.meta["scaled_tokens"] = toks
         return w
