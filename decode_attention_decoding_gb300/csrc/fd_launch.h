@@ -17,6 +17,9 @@ struct SplitLaunch {
     size_t smem_optin;     // the device's opt-in maximum (set once per kernel)
     cudaStream_t stream;
     int late_trigger;      // the merge lets the next kernel launch only after its wait (MergeParams)
+    // Non-null: do not launch; store how many CTAs of the kernel fit on one
+    // SM with this shared memory (cudaOccupancyMaxActiveBlocksPerMultiprocessor).
+    int *blocks_per_sm = nullptr;
 };
 
 // Device properties a launch plan needs.
@@ -80,6 +83,10 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
     };
     if (!(configured.load(std::memory_order_acquire) & bit) && (e = configure()) != cudaSuccess)
         return e;
+    if (c.blocks_per_sm)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(c.blocks_per_sm, split_kernel<G, PAGED, CONS, KV, D, CPA>,
+                                                             CPA ? kSplitThreadsCpAsync : kSplitThreads,
+                                                             c.smem_bytes);
     // Programmatic dependent launch: the kernel's prologue may overlap the
     // previous kernel in the stream; it waits for it before reading inputs.
     cudaLaunchAttribute attr[1];
