@@ -53,24 +53,26 @@ MAX_CTAS = 1024
 # workspace partials written once and read once
 # ---------------------------------------------------------------------------
 
-def partial_count(lens, hkv, P):
-    """Number of (CTA, segment) partials the stream-K split writes (host mirror of fd_sched.h)."""
+SEG_COST = 2   # the split schedule's cost of a segment start, in tiles (the library's kSegCostTiles)
+
+
+def partial_count(lens, hkv, P, w=SEG_COST):
+    """Number of (CTA, segment) partials the split writes: a host mirror of the
+    library's schedule (contiguous runs of equal cost, a tile costing 1 and a
+    segment start w more)."""
     nt = [(int(L) + TILE - 1) // TILE for L in lens]
     T = hkv * sum(nt)
     if T == 0:
         return 0
-    base, rem = divmod(T, P)
-    cut = rem * (base + 1)
-
-    def cta(t):
-        return t // (base + 1) if t < cut else rem + (t - cut) // base
-
-    n = 0
-    first = 0
-    for b, k in enumerate(nt):
+    C = T + w * hkv * sum(1 for k in nt if k)
+    P = min(P, C)   # CTAs that take tiles
+    n, first, starts = 0, 0, 0
+    for k in nt:
         for _h in range(hkv):
             if k:
-                c0, c1 = cta(first), cta(first + k - 1)
+                starts += 1
+                pos0 = first + w * starts
+                c0, c1 = pos0 * P // C, (pos0 + k - 1) * P // C
                 if c1 > c0:
                     n += c1 - c0 + 1
                 first += k
@@ -78,13 +80,13 @@ def partial_count(lens, hkv, P):
 
 
 def byte_counts(w, P):
-    B, hq, d = w.q.shape
+    B, hq, d, ql = w.batch, w.num_q_heads, w.head_dim, w.q_len
     hkv, G = w.num_kv_heads, w.num_q_heads // w.num_kv_heads
     kv = w.kv_bytes()
-    q = B * hq * d * 2
-    out = B * hq * d * 4 + B * hq * 4
+    q = B * ql * hq * d * 2
+    out = B * ql * hq * d * 4 + B * ql * hq * 4
     parts = partial_count(w.seq_lens, hkv, P)
-    ws = parts * G * (d + 1) * 4
+    ws = parts * G * ql * (d + 1) * 4
     table = (sum((int(L) + w.page_size - 1) // w.page_size for L in w.seq_lens) * 4) if w.paged else 0
     return dict(kv=kv, q=q, out=out, ws_partials=parts, ws_once=ws, table=table, lens=B * 4,
                 call=kv + q + out + 2 * ws,
@@ -93,7 +95,7 @@ def byte_counts(w, P):
 
 def consumers_label(flags, w) -> str:
     """Which consumers the library's default choice runs for this workload."""
-    G = w.num_q_heads // w.num_kv_heads
+    G = w.num_q_heads // w.num_kv_heads * w.q_len   # query columns of a kv head
     fp8 = w.kv_dtype is not None
     row = w.head_dim * (1 if fp8 else 2)
     mma = "mma.sync fp16 on FP8 codes" if fp8 else "mma.sync bf16, P as two bf16 parts"
@@ -138,10 +140,18 @@ def kernel_hash():
 def bench_workload(args):
     """The workload the arguments name: one of the five configurations, with
     an FP8 cache (--kv) and re-paged into pages of --page tokens when asked."""
-    w = syn.make_config(args.config, kv_dtype=args.kv if args.kv != "bf16" else None, shrink=args.shrink)
+    w = syn.make_config(args.config, kv_dtype=args.kv if args.kv != "bf16" else None, shrink=args.shrink,
+                        head_dim=args.head_dim, q_len=args.q_len)
     if args.page:
         w = syn.repage(w, args.page, perm_seed=syn.seed_for(args.config, syn.TENSOR_PERM) + args.page)
     return w
+
+
+def workload_name(args, w):
+    """The workload's name: the configuration's, or the variant's (shrink,
+    head_dim, q_len)."""
+    variant = args.shrink > 1 or args.head_dim != 128 or args.q_len != 1
+    return w.name if variant else syn.CONFIG_NAMES[args.config]
 
 
 def measured_peaks():
@@ -237,15 +247,15 @@ class Resident:
         def todev_kv(codes):
             return torch.from_numpy(np.ascontiguousarray(codes)).to(dev) if fp8 else todev(codes)
 
-        B, hq, d = w.q.shape
+        B, hq, d = w.batch, w.num_q_heads, w.head_dim
         self.q, k, v = todev(w.q), todev_kv(w.k), todev_kv(w.v)
         self.lens = torch.from_numpy(w.seq_lens.astype(np.int32)).to(dev)
         self.lens_h = torch.from_numpy(w.seq_lens.astype(np.int32))
         self.table = torch.from_numpy(w.block_table.astype(np.int32)).to(dev) if w.paged else None
         cap = w.max_blocks * w.page_size if w.paged else w.s_max
-        self.ws = fd.make_workspace(B, hq, w.num_kv_heads, d, cap, w.page_size, dev)
-        self.out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
+        self.ws = fd.make_workspace(B, hq, w.num_kv_heads, d, cap, w.page_size, dev, q_len=w.q_len)
+        self.out = torch.empty(tuple(w.q.shape), dtype=torch.float32, device=dev)
+        self.lse = torch.empty(tuple(w.q.shape[:-1]), dtype=torch.float32, device=dev)
         self.kv_alloc = w.k.nbytes + w.v.nbytes
         self.copies = 1
         if l2 and self.kv_alloc < 2 * l2:
@@ -398,7 +408,7 @@ def run_ours(args, rank, world):
         dist.init_process_group("nccl", device_id=dev)
 
     w = bench_workload(args)
-    B, hq, d = w.q.shape
+    B, hq, d = w.batch, w.num_q_heads, w.head_dim
     hkv = w.num_kv_heads
     fp8 = w.kv_dtype is not None
     props = torch.cuda.get_device_properties(dev)
@@ -473,8 +483,8 @@ def run_ours(args, rank, world):
     traffic = None
     try:
         tj = json.load(open(TRAFFIC_FILE))
-        if (tj.get("kernel_hash") == kernel_hash() and tj.get("workload") == syn.CONFIG_NAMES[args.config]
-                and not args.page and args.kv == "bf16"):
+        if (tj.get("kernel_hash") == kernel_hash() and tj.get("workload") == workload_name(args, w)
+                and not args.page and args.kv == "bf16" and not args.cuda_cores):
             traffic = tj.get("traffic_bytes_per_launch")
     except Exception:
         pass
@@ -500,7 +510,8 @@ def run_ours(args, rank, world):
     # Every benchmark workload under the same protocol (one GPU only: under
     # torchrun the ranks run the headline replicas alone).
     workloads = None
-    if world == 1 and args.workloads != "none" and not args.page and args.shrink == 1:
+    if (world == 1 and args.workloads != "none" and not args.page and args.shrink == 1 and args.head_dim == 128
+            and args.q_len == 1):
         workloads = {}
         for c in [int(x) for x in args.workloads.split(",")]:
             name = syn.CONFIG_NAMES[c]
@@ -525,8 +536,7 @@ def run_ours(args, rank, world):
                                             else "bf16"),
             "data": "synthetic (seeded N(0,1) bf16" + (", quantised once to FP8)" if fp8 else ")"),
             "impl": "ours",
-            "config": {"workload": syn.CONFIG_NAMES[args.config] + (f"_shrink{args.shrink}" if args.shrink > 1 else ""),
-                       "batch": B, "num_q_heads": hq,
+            "config": {"workload": workload_name(args, w), "batch": B, "q_len": w.q_len, "num_q_heads": hq,
                        "num_kv_heads": hkv, "head_dim": d,
                        "kv_lens": ("uniform " + str(int(w.seq_lens[0]))) if len(set(w.seq_lens.tolist())) == 1
                        else f"ragged sum={int(w.seq_lens.sum())}",
@@ -565,13 +575,12 @@ def run_e2e(fd, res, dev, stream, bc, world, dist, steps):
     import torch
     w = res.w
     fp8 = w.kv_dtype is not None
-    B, hq, d = w.q.shape
     hq_ = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory()
     hk_, hv_ = (torch.from_numpy(np.ascontiguousarray(x).view(np.uint8 if fp8 else np.int16)).pin_memory()
                 for x in (w.k, w.v))
     hl_ = res.lens_h.pin_memory()
-    ho = torch.empty((B, hq, d), dtype=torch.float32).pin_memory()
-    hlse = torch.empty((B, hq), dtype=torch.float32).pin_memory()
+    ho = torch.empty(tuple(w.q.shape), dtype=torch.float32).pin_memory()
+    hlse = torch.empty(tuple(w.q.shape[:-1]), dtype=torch.float32).pin_memory()
     dq, dk, dv = (torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (hq_, hk_, hv_))
     dl = torch.empty_like(res.lens)
 
@@ -622,12 +631,13 @@ def oracle_units(w, n_units):
     of its group over the whole kv length, and their algorithmic bytes: the
     unit's K+V rows once (as the GPU's count, not once per query row), plus
     its q rows, O rows and LSEs."""
-    B, hq, hkv, d = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    B, hq, hkv, d, ql = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.q_len
     G = hq // hkv
     units = [(b, g) for b in range(B) for g in range(hkv)][:max(1, n_units)]
-    items = np.array([[b, g * G + i, 0, -1] for b, g in units for i in range(G)], dtype=np.int32)
+    items = np.array([[b, i * hq + g * G + j, 0, -1] for b, g in units for i in range(ql) for j in range(G)],
+                     dtype=np.int32)
     toks = sum(int(w.seq_lens[b]) for b, _ in units)
-    by = toks * d * 2 * w.kv_elem_bytes + len(units) * G * (d * 2 + d * 4 + 4)
+    by = toks * d * 2 * w.kv_elem_bytes + len(units) * ql * G * (d * 2 + d * 4 + 4)
     return items, by, len(units)
 
 
@@ -717,7 +727,7 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "input_dtype": f"bf16 q, FP8 {w.kv_dtype} K/V" if w.kv_dtype else "bf16",
             "data": "synthetic (seeded N(0,1) bf16)", "impl": "reference",
-            "config": {"workload": syn.CONFIG_NAMES[args.config], "parallelism": "host cores"},
+            "config": {"workload": workload_name(args, w), "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": "TB/s", "cores": threads, "kind": "oracle",
                              "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -738,6 +748,10 @@ def main():
     ap.add_argument("--shrink", type=int, default=1,
                     help="divide the workload's lengths by this factor (a smaller case of the same launch "
                          "shape, for profiler captures; never the benchmark's own numbers)")
+    ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256],
+                    help="the workload with this head_dim (its lengths, heads and layout)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="new query tokens per request (q [B, q_len, Hq, D], causal over the new tokens)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-e2e", action="store_true")

@@ -152,8 +152,8 @@ fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_
 {
     const size_t stage_bytes = 2u * kTileTokens * (size_t)elem_bytes * (size_t)d;   // K and V tiles
     const size_t red = align_up((size_t)reduction_floats(cons, group, d) * sizeof(float), 16);
-    const size_t prefix = align_up(sizeof(int) * (size_t)(batch + 1), 16);
-    const size_t misc = 64;
+    const size_t prefix = align_up(2 * sizeof(int) * (size_t)(batch + 1), 16);   // tile prefix, non-empty requests
+    const size_t misc = 128;   // abort flag, two scans' scratch
     const size_t per_stage_extra = 2 * 8 + kMetaInts * sizeof(int);   // 2 barriers + metadata
     const size_t fixed = 1024 /* alignment slack */ + red + prefix + misc + 8 /* consumer barrier */;
     const size_t avail = (size_t)dev.smem_optin;
@@ -498,6 +498,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     sp.fuse_dh = fuse == 4 ? head_dim : 0;   // only a shared 4-head row splits a column's dims
     sp.fuse_f = fuse;
     sp.q_len = q_len;
+    sp.seg_cost = kSegCostTiles;
     sp.range_on = range.on ? 1 : 0;
     sp.kv_begin = range.on ? range.begin : 0;
     sp.kv_end = range.on ? range.end : 0;
@@ -553,6 +554,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     mp.seq_lens = seq_lens_dev;
     mp.cap = cap;
     mp.late_trigger = cp->launch.late_trigger;
+    mp.seg_cost = sp.seg_cost;
     cp->two_per_sm = cp->launch.late_trigger && !(opts && opts->num_ctas > 0) && 2 * num_ctas <= kMaxCtas;
     mp.range_on = sp.range_on;
     mp.kv_begin = sp.kv_begin;

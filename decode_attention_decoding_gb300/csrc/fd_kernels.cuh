@@ -113,7 +113,7 @@ struct SplitParams {
     float *lse;                   // [B, Hq] or null
     float *ws_o;                  // [slots, G, D]
     float *ws_lse;                // [slots, G]
-    int32_t *ws_prefix;           // [B + 1]
+    int32_t *ws_prefix;           // [B + 1] tile prefix, then [B + 1] non-empty requests
     unsigned int *ws_err;
     int batch, hq, hkv;
     int cap;                      // largest valid length
@@ -150,6 +150,7 @@ struct SplitParams {
     int q_f16;        // FP8 caches: 1 when q is fp16, 0 when bf16
     float v_scale;    // multiplies O (an FP8 cache's V dequantisation scale; 1 otherwise)
     int prefetch_tiles;   // first tiles of a CTA prefetched into L2 before the dependency wait (0: none)
+    int seg_cost;         // the Schedule's cost of a segment start, in tiles
     // A token range (the partial entry points): the layout holds cache
     // positions kv_begin, kv_begin + 1, .. of each request at its rows 0, 1,
     // .., and the call covers positions [kv_begin, min(L_b, kv_end)).
@@ -172,6 +173,7 @@ struct MergeParams {
     // 1: let the next kernel in the stream launch only once this grid's wait
     // has returned (the split grid is complete) rather than at once.
     int late_trigger;
+    int seg_cost;      // as in SplitParams
 };
 
 constexpr int kMergeDirectBatch = 32;   // batches this small: segment geometry from the lengths
@@ -273,8 +275,10 @@ __device__ __forceinline__ bool consumer_sync(uint32_t cbar, uint32_t &cph, uint
     return ok;
 }
 
-// prefix[b] = Hkv * (tiles of requests < b), prefix[B] = total tiles.
-// All NTHREADS threads of the block take part.  scan_tmp: NTHREADS / 32 ints.
+// prefix[b] = Hkv * (tiles of requests < b), prefix[B] = total tiles, and
+// right after it nonempty[b] = prefix[B + 1 + b] = requests < b with at least
+// one tile (the Schedule's two arrays).  All NTHREADS threads of the block
+// take part.  scan_tmp: 2 * NTHREADS / 32 ints.
 // HINT: a plan for L2 prefetches only, made before the kernels ahead in the
 // stream have completed: the lengths are read around L1 (no stale line stays
 // there), nothing is reported and the workspace is not written.
@@ -284,6 +288,7 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int nthreads = NTHREADS, kWarps = nthreads / 32;
     const int B = p.batch;
+    int *nonempty = prefix + B + 1;
     const int per = ceil_div(B, nthreads);
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
     unsigned int *report = blockIdx.x == 0 && !HINT ? p.ws_err : nullptr;
@@ -295,41 +300,58 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
             return ceil_div(req_len(p, b, rep).n, kTileTokens);
         }
     };
-    int local = 0;
-    for (int b = b0; b < b1; ++b)
-        local += tiles_of(b, report);
-    int x = local;
+    int local = 0, local_ne = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int n = tiles_of(b, report);
+        local += n;
+        local_ne += n > 0;
+    }
+    int x = local, y = local_ne;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off)
-            x += y;
+        const int xo = __shfl_up_sync(0xffffffffu, x, off), yo = __shfl_up_sync(0xffffffffu, y, off);
+        if (lane >= off) {
+            x += xo;
+            y += yo;
+        }
     }
-    if (lane == 31)
+    if (lane == 31) {
         scan_tmp[warp] = x;
+        scan_tmp[kWarps + warp] = y;
+    }
     __syncthreads();
     if (warp == 0) {
-        int w = lane < kWarps ? scan_tmp[lane] : 0;
+        int wx = lane < kWarps ? scan_tmp[lane] : 0, wy = lane < kWarps ? scan_tmp[kWarps + lane] : 0;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, w, off);
-            if (lane >= off)
-                w += y;
+            const int xo = __shfl_up_sync(0xffffffffu, wx, off), yo = __shfl_up_sync(0xffffffffu, wy, off);
+            if (lane >= off) {
+                wx += xo;
+                wy += yo;
+            }
         }
-        if (lane < kWarps)
-            scan_tmp[lane] = w;
+        if (lane < kWarps) {
+            scan_tmp[lane] = wx;
+            scan_tmp[kWarps + lane] = wy;
+        }
     }
     __syncthreads();
     int run = x - local + (warp > 0 ? scan_tmp[warp - 1] : 0);
+    int run_ne = y - local_ne + (warp > 0 ? scan_tmp[kWarps + warp - 1] : 0);
     for (int b = b0; b < b1; ++b) {
         prefix[b] = run * p.hkv;
-        run += tiles_of(b, nullptr);
+        nonempty[b] = run_ne;
+        const int n = tiles_of(b, nullptr);
+        run += n;
+        run_ne += n > 0;
     }
-    if (tid == nthreads - 1)
+    if (tid == nthreads - 1) {
         prefix[B] = run * p.hkv;
+        nonempty[B] = run_ne;
+    }
     __syncthreads();
     if (blockIdx.x == 0 && !HINT)
-        for (int b = tid; b <= B; b += nthreads)
+        for (int b = tid; b <= 2 * B + 1; b += nthreads)
             p.ws_prefix[b] = prefix[b];
 }
 
@@ -1567,7 +1589,8 @@ __global__ void __launch_bounds__(CPA ? kSplitThreadsCpAsync : kSplitThreads, 1)
         if (p.prefetch_tiles > 0) {
             build_prefix<kThreads, true>(p, prefix, misc + 1);   // ends with __syncthreads
             int pb, pe;
-            cta_tile_range(prefix[p.batch], (int)gridDim.x, (int)blockIdx.x, &pb, &pe);
+            const Schedule hint{prefix, prefix + p.batch + 1, p.batch, p.hkv, p.seg_cost, (int)gridDim.x};
+            hint.range((int)blockIdx.x, &pb, &pe);
             if (warp == kConsumerWarps && pb < pe)
                 split_prefetch<PAGED, CONS != kConsCudaCores, D, KV>(p, &tmk, &tmv, prefix, pb,
                                                                      min(pe, pb + p.prefetch_tiles), lane);
@@ -1580,9 +1603,9 @@ __global__ void __launch_bounds__(CPA ? kSplitThreadsCpAsync : kSplitThreads, 1)
     pdl_launch_dependents();
     build_prefix<kThreads>(p, prefix, misc + 1);   // ends with __syncthreads
 
-    const int T = prefix[p.batch];
     int t_begin, t_end;
-    cta_tile_range(T, (int)gridDim.x, (int)blockIdx.x, &t_begin, &t_end);
+    const Schedule sched{prefix, prefix + p.batch + 1, p.batch, p.hkv, p.seg_cost, (int)gridDim.x};
+    sched.range((int)blockIdx.x, &t_begin, &t_end);
     if (t_begin >= t_end)
         return;
     volatile int *abort_flag = misc;
@@ -1614,7 +1637,9 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
 {
     __shared__ float s_w[kMaxCtas];
     __shared__ float s_lse;
-    __shared__ int s_geo[3];   // small batches: first tile of request b, its end, total tiles
+    // small batches: first tile of request b, its end, total tiles, non-empty
+    // requests before b, in all
+    __shared__ int s_geo[5];
     const int u = blockIdx.x, g = blockIdx.y;
     const int b = u / p.hkv, h = u - b * p.hkv;
     const int d = threadIdx.x;
@@ -1623,20 +1648,25 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
         int L = 0;
         if (d < p.batch)
             L = req_len(p, d, nullptr).n;   // clamped as the split kernel clamps
-        const int t = ceil_div(L, kTileTokens);
-        int x = t;
+        const int t = ceil_div(L, kTileTokens), e = t > 0;
+        int x = t, y = e;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, off);
-            if (d >= off)
-                x += y;
+            const int xo = __shfl_up_sync(0xffffffffu, x, off), yo = __shfl_up_sync(0xffffffffu, y, off);
+            if (d >= off) {
+                x += xo;
+                y += yo;
+            }
         }
         if (d == b) {
             s_geo[0] = (x - t) * p.hkv;
             s_geo[1] = x * p.hkv;
+            s_geo[3] = y - e;
         }
-        if (d == 31)
+        if (d == 31) {
             s_geo[2] = x * p.hkv;
+            s_geo[4] = y;
+        }
     }
     __syncthreads();
     // The next call's split kernel may start its prologue (and its L2
@@ -1646,15 +1676,19 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
     pdl_wait_prior_grid();
     if (p.late_trigger)
         pdl_launch_dependents();
-    int pb, pe, T;
+    int pb, pe, T, ne_b, ne;
     if (small) {
         pb = s_geo[0];
         pe = s_geo[1];
         T = s_geo[2];
+        ne_b = s_geo[3];
+        ne = s_geo[4];
     } else {
         pb = p.ws_prefix[b];
         pe = p.ws_prefix[b + 1];
         T = p.ws_prefix[p.batch];
+        ne_b = p.ws_prefix[p.batch + 1 + b];
+        ne = p.ws_prefix[2 * p.batch + 1];
     }
     const ColInfo col = col_info(p, b, h, g);   // g < n_cols (the grid's y extent)
     if (!col.valid)
@@ -1668,8 +1702,12 @@ __global__ void __launch_bounds__(D) merge_kernel(const __grid_constant__ MergeP
         return;
     }
     const int nb = (pe - pb) / p.hkv;
-    const int first = pb + h * nb, last = first + nb - 1;
-    const int c0 = cta_of_tile(T, p.num_ctas, first), c1 = cta_of_tile(T, p.num_ctas, last);
+    // the CTAs that own the segment's first and last tiles (the Schedule's
+    // cost positions, written out for one segment)
+    const long long cost = (long long)T + (long long)p.seg_cost * p.hkv * ne;
+    const long long ctas = cost < p.num_ctas ? cost : p.num_ctas;
+    const long long pos0 = (long long)pb + (long long)h * nb + (long long)p.seg_cost * ((long long)p.hkv * ne_b + h + 1);
+    const int c0 = (int)(pos0 * ctas / cost), c1 = (int)((pos0 + nb - 1) * ctas / cost);
     if (c0 == c1)
         return;   // one CTA saw the whole segment and wrote it
     const int n = c1 - c0 + 1;

@@ -33,6 +33,10 @@ struct DeviceInfo {
 // them (fd_api.cu).
 constexpr double kFuseMinTilesPerCta = 24.0;
 
+// The split Schedule's cost of a segment start, in tiles (fd_sched.h): a CTA
+// that touches one more segment takes this many fewer tiles.
+constexpr int kSegCostTiles = 2;
+
 // Shared-memory plan of the split kernel (fd_api.cu): pipeline stages, the
 // offsets of every region in sp, the L2 prefetch before the dependency wait
 // (sp->prefetch_tiles), and the byte size and merge trigger in launch, for

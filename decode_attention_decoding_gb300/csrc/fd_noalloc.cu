@@ -119,7 +119,7 @@ NoallocLayout noalloc_layout(int batch, int slots, int group)
 {
     NoallocLayout l;
     l.prefix_off = 256;
-    l.lse_off = align_up(l.prefix_off + sizeof(int) * (size_t)(batch + 1), 256);
+    l.lse_off = align_up(l.prefix_off + 2 * sizeof(int) * (size_t)(batch + 1), 256);   // prefix, non-empty counts
     l.o_off = align_up(l.lse_off + sizeof(float) * (size_t)slots * group, 256);
     l.total = align_up(l.o_off + sizeof(float) * (size_t)slots * group * kD, 256);
     return l;
@@ -181,6 +181,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     for (int n = 0; n < kMaxColumnSlots; ++n)
         sp.col_code[n] = n < group ? n << 8 : -1;   // token 0, part 0, query head n
     sp.timeout_ns = 2000000000ull;
+    sp.seg_cost = kSegCostTiles;
 
     // Consumers as fd_decode picks them for an unfused call: CUDA cores for
     // one query head per kv head, tensor cores for GQA groups.
@@ -214,6 +215,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     mp.n_cols = group;
     mp.fuse_f = 1;
     mp.late_trigger = launch.late_trigger;
+    mp.seg_cost = sp.seg_cost;
     for (int n = 0; n < kMaxColumnSlots; ++n)
         mp.col_code[n] = n < group ? n << 8 : -1;
 

@@ -362,14 +362,15 @@ def build_block_table(lens, page: int, max_blocks: int, perm: np.ndarray) -> np.
 def make_paged(config_id: int, batch: int, hq: int, hkv: int, d: int, page: int,
                lens, max_blocks: int, name: str = "", extra_pages: int = 0,
                dtype: str = "bf16", kv_dtype: str | None = None, k_scale: float = 1.0,
-               v_scale: float = 1.0) -> Workload:
+               v_scale: float = 1.0, q_len: int = 1) -> Workload:
     lens = np.asarray(lens, dtype=np.int32).reshape(batch)
     used = int(sum((int(L) + page - 1) // page for L in lens))
     num_pages = max(1, used + extra_pages)
     perm = permutation(seed_for(config_id, TENSOR_PERM), num_pages)
     table = build_block_table(lens, page, max_blocks, perm)
     k_scale, v_scale = fp32(k_scale), fp32(v_scale)
-    q = normal_bf16(seed_for(config_id, TENSOR_Q), (batch, hq, d), dtype=dtype)
+    qshape = (batch, hq, d) if q_len == 1 else (batch, q_len, hq, d)
+    q = normal_bf16(seed_for(config_id, TENSOR_Q), qshape, dtype=dtype)
     k, v = _kv(config_id, (num_pages, page, hkv, d), dtype, kv_dtype, k_scale, v_scale)
     return Workload(name or f"paged{config_id}", q, k, v, lens, hq, hkv, d, default_scale(d),
                     page_size=page, block_table=table, dtype=dtype, kv_dtype=kv_dtype,
@@ -451,28 +452,34 @@ def quantize_kv(w: Workload, fmt: str, scale: float, workers: int | None = None)
 FP8_CONFIG_SCALE = 0.125   # N(0,1) values (and workload 5's x8 keys) stay inside E4M3's range
 
 
-def make_config(config_id: int, kv_dtype: str | None = None, shrink: int = 1) -> Workload:
+def make_config(config_id: int, kv_dtype: str | None = None, shrink: int = 1, head_dim: int = 128,
+                q_len: int = 1) -> Workload:
     """Build benchmark workload 1..5 at full size (optionally with an FP8 cache
     quantised from the same values).  shrink > 1 divides every length and
     capacity by it (at least 64 tokens each where the workload has one long
-    request): the same shapes and structure, a smaller case for profiling."""
+    request): the same shapes and structure, a smaller case for profiling.
+    head_dim and q_len (new query tokens per request, q [B, q_len, Hq, D])
+    give variants of the workload with its lengths, heads and layout."""
     if kv_dtype in ("e4m3", "e5m2"):
-        return quantize_kv(make_config(config_id, shrink=shrink), kv_dtype, FP8_CONFIG_SCALE)
+        return quantize_kv(make_config(config_id, shrink=shrink, head_dim=head_dim, q_len=q_len), kv_dtype,
+                           FP8_CONFIG_SCALE)
     sh = max(1, int(shrink))
+    d = int(head_dim)
     lens = config_lens(config_id)
     if sh > 1:
         lens = np.maximum(lens // sh, 1 if config_id in (3, 4) else 64).astype(np.int32)
-    name = CONFIG_NAMES[config_id] + (f"_shrink{sh}" if sh > 1 else "")
+    name = CONFIG_NAMES[config_id] + (f"_shrink{sh}" if sh > 1 else "") + (f"_d{d}" if d != 128 else "") + \
+        (f"_qlen{q_len}" if q_len != 1 else "")
     if config_id in (1, 2):
-        return make_contiguous(config_id, 1, 32, 32, 128, int(lens[0]), lens, name)
+        return make_contiguous(config_id, 1, 32, 32, d, int(lens[0]), lens, name, q_len=q_len)
     if config_id == 3:
-        return make_contiguous(3, 16, 32, 8, 128, max(8192 // sh, int(lens.max())), lens, name)
+        return make_contiguous(3, 16, 32, 8, d, max(8192 // sh, int(lens.max())), lens, name, q_len=q_len)
     if config_id == 4:
         cap = max(16384 // sh, int(lens.max()))
-        return make_paged(4, 64, 32, 8, 128, 16, lens, (cap + 15) // 16, name)
+        return make_paged(4, 64, 32, 8, d, 16, lens, (cap + 15) // 16, name, q_len=q_len)
     if config_id == 5:
         L = int(lens[0])
-        w = make_paged(5, 1, 64, 8, 128, 64, lens, (L + 63) // 64, name)
+        w = make_paged(5, 1, 64, 8, d, 64, lens, (L + 63) // 64, name, q_len=q_len)
         n_scaled = int(0.01 * L)
         toks = np.sort(choose(seed_for(5, TENSOR_MASK), L, n_scaled))
         _scale_keys_paged_fast(w, 0, toks, 8.0)

@@ -280,33 +280,85 @@ def sched(tmp_path_factory):
                            "-I" + os.path.join(ROOT, "decode_attention_decoding_gb300", "csrc"),
                            os.path.join(ROOT, "tests", "sched_shim.cpp"), "-o", so])
     s = ctypes.CDLL(so)
-    s.shim_cta_of_tile.restype = ctypes.c_int
+    s.shim_schedule_cta_of_tile.restype = ctypes.c_int
     s.shim_request_of_tile.restype = ctypes.c_int
     s.shim_slots.restype = ctypes.c_int
     return s
 
 
-def ranges(sched, T, P):
+def make_plan(lens, hkv, tt=64):
+    """The Schedule's two arrays for these lengths: tile prefix and non-empty requests."""
+    ntiles = (np.asarray(lens, dtype=np.int64) + tt - 1) // tt
+    prefix = np.concatenate([[0], np.cumsum(ntiles * hkv)]).astype(np.int32)
+    nonempty = np.concatenate([[0], np.cumsum(ntiles > 0)]).astype(np.int32)
+    return ntiles, prefix, nonempty
+
+
+def ranges(sched, prefix, nonempty, hkv, w, P):
+    B = len(prefix) - 1
+    pre = (ctypes.c_int * len(prefix))(*prefix.tolist())
+    ne = (ctypes.c_int * len(nonempty))(*nonempty.tolist())
     out = []
     b, e = ctypes.c_int(), ctypes.c_int()
     for c in range(P):
-        sched.shim_cta_tile_range(T, P, c, ctypes.byref(b), ctypes.byref(e))
+        sched.shim_schedule_range(pre, ne, B, hkv, w, P, c, ctypes.byref(b), ctypes.byref(e))
         out.append((b.value, e.value))
-    return out
+    return out, pre, ne
 
 
-@pytest.mark.parametrize("T,P", [(0, 5), (3, 8), (8, 8), (100, 7), (2048, 152), (32768, 152), (65537, 1024)])
-def test_cta_ranges_partition_tiles_evenly(sched, T, P):
-    r = ranges(sched, T, P)
-    assert r[0][0] == 0 and r[-1][1] == T
-    for (b0, e0), (b1, _) in zip(r, r[1:]):
-        assert e0 == b1
-    sizes = [e - b for b, e in r]
-    assert max(sizes) - min(sizes) <= 1
-    for t in sorted(set([0, T - 1, T // 2, *range(0, T, max(1, T // 97))])):
-        if 0 <= t < T:
-            c = sched.shim_cta_of_tile(T, P, t)
-            assert r[c][0] <= t < r[c][1]
+def brute_positions(ntiles, hkv, w):
+    """Cost position of every tile, tile by tile: +1 per tile, +w at each segment start."""
+    pos, x = [], 0
+    for n in ntiles:
+        for _h in range(hkv):
+            for j in range(int(n)):
+                x += w if j == 0 else 0
+                pos.append(x)
+                x += 1
+    return pos, x
+
+
+@pytest.mark.parametrize("w", [0, 1, 2, 5])
+def test_schedule_partitions_tiles_by_cost(sched, w):
+    """Contiguous runs covering every tile once; the owner of a tile agrees
+    with the runs and with the tile's cost position (+1 per tile, +w at each
+    segment start); w = 0 gives runs of equal length."""
+    rng = np.random.default_rng(11 + w)
+    for trial in range(40):
+        B = int(rng.integers(1, 40))
+        hkv = int(rng.choice([1, 2, 8]))
+        lens = rng.integers(0, 3000, B)
+        lens[rng.random(B) < 0.2] = 0
+        ntiles, prefix, nonempty = make_plan(lens, hkv)
+        T = int(prefix[-1])
+        P = int(rng.integers(1, 300))
+        r, pre, ne = ranges(sched, prefix, nonempty, hkv, w, P)
+        assert r[0][0] == 0 and r[-1][1] == T
+        for (b0, e0), (b1, _) in zip(r, r[1:]):
+            assert e0 == b1 and b0 <= e0
+        pos, C = brute_positions(ntiles, hkv, w)
+        assert C == T + w * hkv * int((ntiles > 0).sum())
+        Pe = min(P, C)   # CTAs that take tiles
+        for c, (b0, e0) in enumerate(r):
+            if c >= Pe:
+                assert b0 == e0 == T
+            for t in range(b0, e0):
+                assert c * C <= pos[t] * Pe < (c + 1) * C
+        # the CTAs of a segment are consecutive and each owns some of its tiles
+        owners = {}
+        for c, (b0, e0) in enumerate(r):
+            for t in range(b0, e0):
+                b = int(np.searchsorted(prefix, t, side="right") - 1)
+                owners.setdefault((b, (t - prefix[b]) // ntiles[b]), set()).add(c)
+        for cs in owners.values():
+            assert cs == set(range(min(cs), max(cs) + 1))
+        for t in sorted(set([0, T - 1, T // 2, *range(0, T, max(1, T // 97))])):
+            if 0 <= t < T:
+                c = sched.shim_schedule_cta_of_tile(pre, ne, len(lens), hkv, w, P, t)
+                assert r[c][0] <= t < r[c][1]
+        if w == 0 and T:
+            sizes = [e - b for b, e in r]
+            assert max(sizes) - min(sizes) <= 1
 
 
 def test_partial_slots_are_unique_and_bounded(sched):
@@ -317,25 +369,23 @@ def test_partial_slots_are_unique_and_bounded(sched):
         hkv = int(rng.choice([1, 2, 8]))
         lens = rng.integers(0, 3000, B)
         lens[rng.random(B) < 0.2] = 0
-        ntiles = (lens + tt - 1) // tt
-        prefix = np.concatenate([[0], np.cumsum(ntiles * hkv)]).astype(np.int32)
-        T = int(prefix[-1])
+        ntiles, prefix, nonempty = make_plan(lens, hkv, tt)
         P = int(rng.integers(1, 300))
-        r = ranges(sched, T, P)
-        seen = set()
-        pre = (ctypes.c_int * len(prefix))(*prefix.tolist())
-        for c, (b0, e0) in enumerate(r):
-            segs = set()
-            for t in range(b0, e0):
-                b = sched.shim_request_of_tile(pre, B, t)
-                assert prefix[b] <= t < prefix[b + 1]
-                h = (t - prefix[b]) // ntiles[b]
-                segs.add(b * hkv + h)
-            for u in segs:
-                slot = u + c
-                assert slot not in seen
-                seen.add(slot)
-                assert slot < sched.shim_slots(B, hkv)
+        for w in (0, 2):
+            r, pre, ne = ranges(sched, prefix, nonempty, hkv, w, P)
+            seen = set()
+            for c, (b0, e0) in enumerate(r):
+                segs = set()
+                for t in range(b0, e0):
+                    b = sched.shim_request_of_tile(pre, B, t)
+                    assert prefix[b] <= t < prefix[b + 1]
+                    h = (t - prefix[b]) // ntiles[b]
+                    segs.add(b * hkv + h)
+                for u in segs:
+                    slot = u + c
+                    assert slot not in seen
+                    seen.add(slot)
+                    assert slot < sched.shim_slots(B, hkv)
 
 
 def test_c_caller_compiles_links_and_sees_the_documented_checks(lib, tmp_path):

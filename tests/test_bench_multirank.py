@@ -49,29 +49,35 @@ def test_max_over_ranks_and_weak_scaling_value():
 
 
 def test_partial_count_matches_schedule_brute_force():
+    """bench.partial_count mirrors the split schedule: tiles in contiguous runs
+    of equal cost (+1 per tile, +w at each segment start), one partial per
+    (CTA, segment) for segments split over several CTAs."""
     sys.path.insert(0, ROOT)
     import bench
     import numpy as np
     rng = np.random.default_rng(5)
     for _ in range(40):
         B = int(rng.integers(1, 20)); hkv = int(rng.choice([1, 2, 8])); P = int(rng.integers(1, 200))
+        w = int(rng.choice([0, 1, 2]))
         lens = rng.integers(0, 5000, B)
         nt = (lens + 63) // 64
-        owner = []
+        owner, pos, x = [], [], 0
         for b in range(B):
             for h in range(hkv):
-                owner += [(b, h)] * int(nt[b])
-        T = len(owner)
-        base, rem = divmod(T, P)
+                for j in range(int(nt[b])):
+                    x += w if j == 0 else 0
+                    owner.append((b, h))
+                    pos.append(x)
+                    x += 1
+        C = x
+        Pe = min(P, C)   # CTAs that take tiles
         counts = {}
-        t = 0
-        for c in range(P):
-            n = base + (1 if c < rem else 0)
-            for seg in set(owner[t:t + n]):
-                counts.setdefault(seg, set()).add(c)
-            t += n
+        for seg, p in zip(owner, pos):
+            counts.setdefault(seg, set()).add(p * Pe // C)
+        for cs in counts.values():   # a segment's CTAs are consecutive
+            assert cs == set(range(min(cs), max(cs) + 1))
         expect = sum(len(cs) for cs in counts.values() if len(cs) > 1)
-        assert bench.partial_count(lens, hkv, P) == expect
+        assert bench.partial_count(lens, hkv, P, w) == expect
 
 
 def test_reference_arm_rank1_prints_nothing():
