@@ -112,6 +112,11 @@ def consumers_label(flags, w) -> str:
                                         (G <= 16 if f == 2 else 4 * G <= 8) for f in (2, 4))
     if (G == 1 or row < 128) and not fused:
         return "cuda cores"
+    tc5_shape = (fused and w.kv_dtype == "e4m3" and w.head_dim == 128 and G <= 8 and w.num_kv_heads % 2 == 0
+                 and (not w.paged or w.page_size >= 64))
+    # FD_FLAG_TMEM_SCORES (0x80) forces the tcgen05 scores, FD_FLAG_NO_TMEM_SCORES (0x100) keeps the warp MMAs
+    if tc5_shape and not flags & 0x100 and (G <= 4 or flags & 0x80):
+        return "tensor cores (tcgen05 E4M3 scores into TMEM, mma.sync fp16 P.V), fused kv heads"
     return f"tensor cores ({mma})" + (", fused kv heads" if fused else "")
 
 
@@ -415,7 +420,8 @@ def run_ours(args, rank, world):
     P = props.multi_processor_count
     l2 = getattr(props, "L2_cache_size", 0) or 0
     stream = torch.cuda.current_stream(dev)
-    flags = fd.FD_FLAG_CUDA_CORES if args.cuda_cores else 0
+    flags = (fd.FD_FLAG_CUDA_CORES if args.cuda_cores else 0) | \
+        {"default": 0, "on": fd.FD_FLAG_TMEM_SCORES, "off": fd.FD_FLAG_NO_TMEM_SCORES}[args.tmem_scores]
     res = Resident(fd, w, dev, l2, flags)
     peaks, peak_src = measured_peaks()
 
@@ -758,6 +764,9 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of a CUDA graph")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="force the CUDA-core consumers for GQA groups (comparison runs)")
+    ap.add_argument("--tmem-scores", choices=("default", "on", "off"), default="default",
+                    help="E4M3 caches with paired kv heads: tcgen05 scores into TMEM for up to 4 columns per kv "
+                         "head (default), up to 8 (on), or never (off)")
     ap.add_argument("--workloads", default="1,2,3,4,5",
                     help="benchmark workloads also timed on one GPU for the line's `workloads` object "
                          "(comma-separated ids, or 'none')")

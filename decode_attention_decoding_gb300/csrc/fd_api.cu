@@ -155,7 +155,8 @@ fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_
     const size_t prefix = align_up(2 * sizeof(int) * (size_t)(batch + 1), 16);   // tile prefix, non-empty requests
     const size_t misc = 128;   // abort flag, two scans' scratch
     const size_t per_stage_extra = 2 * 8 + kMetaInts * sizeof(int);   // 2 barriers + metadata
-    const size_t fixed = 1024 /* alignment slack */ + red + prefix + misc + 8 /* consumer barrier */;
+    const size_t tc = cons == kConsTc5 ? align_up((size_t)kTc5Bytes, 16) : 0;   // TMEM-score region
+    const size_t fixed = 1024 /* alignment slack */ + tc + red + prefix + misc + 8 /* consumer barrier */;
     const size_t avail = (size_t)dev.smem_optin;
     if (avail <= fixed)
         return FD_ERR_UNSUPPORTED;
@@ -167,12 +168,15 @@ fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_
     // ends -- unless that costs the pipeline its fourth stage.  Measured on
     // GB300: 32 KB free took the 1 GiB MHA call from 161.3 to 157.1 us and the
     // small calls 1.5-1.7% faster; with 64 KB stages (3 -> 2) it cost 4%.
+    // The TMEM-score consumers hold each stage longer (the score MMAs, four
+    // warps per tile) and keep the stage instead: 5 rather than 4 stages took
+    // the FP8 calls 0.5-1% faster.
     {
         const size_t keep = kMergeRoomBytes;
         int ns_keep = ns;
         while (ns_keep > 2 && 1024 + fixed + ns_keep * (stage_bytes + per_stage_extra) + keep > avail)
             --ns_keep;
-        if (ns_keep >= 4)
+        if (ns_keep >= 4 && cons != kConsTc5)
             ns = ns_keep;
     }
     // A short call (few tiles per CTA) starts faster with less in flight: every
@@ -209,7 +213,8 @@ fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_
     int pf = short_call ? ns : kPrefetchStages * ns;
     pf = pf < kPrefetchTiles ? pf : kPrefetchTiles;
     sp->prefetch_tiles = (sp->flags & FD_FLAG_NO_PREFETCH) ? 0 : pf;
-    sp->off_red = (uint32_t)(ns * stage_bytes);
+    sp->off_tc = (uint32_t)(ns * stage_bytes);   // 1024-byte aligned: stages are multiples of 1 KB
+    sp->off_red = (uint32_t)(sp->off_tc + tc);
     sp->off_prefix = (uint32_t)(sp->off_red + red);
     sp->off_bar = (uint32_t)(sp->off_prefix + prefix);
     sp->off_meta = (uint32_t)(sp->off_bar + (2 * ns + 1) * 8);
@@ -521,6 +526,18 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     cp->merge_dim = merge_dim;
     cp->mma = paired || use_mma(group, eb * d, opts);
     cp->cons = paired ? kConsMmaPair : (cp->mma ? kConsMma : kConsCudaCores);
+    // Scores by tcgen05 MMAs into TMEM.  Their K operand is the tile's 128
+    // swizzled rows as 64-row boxes lay them out (head 0's 64 rows, then
+    // head 1's): contiguous caches and pages of 64 tokens or more.  Smaller
+    // pages interleave the heads page by page.  By default for up to
+    // kTc5DefaultColumns columns per kv head: their consumers' softmax work
+    // grows with the columns, the warp MMAs' does not (measured on GB300:
+    // 1 and 4 columns faster, 8 slower).
+    const bool tc5_shape = paired && kv == kKvE4m3 && d == 256 && group <= 8 &&
+                           (page_size == 0 || page_size >= kTileTokens);
+    if (tc5_shape && !(sp.flags & FD_FLAG_NO_TMEM_SCORES) &&
+        (group <= kTc5DefaultColumns || (sp.flags & FD_FLAG_TMEM_SCORES)))
+        cp->cons = kConsTc5;
     if (fuse > 1 && !use_mma(2, eb * d, opts))
         return FD_ERR_UNSUPPORTED;   // fusion is defined for the tensor-core consumers only
     if (!cp->mma && group > kMaxColumnsCudaCores)

@@ -413,3 +413,107 @@ __device__ __forceinline__ uint32_t pack_x2(float lo, float hi)
 }
 
 }  // namespace fd
+
+// ---------------------------------------------------------------- tcgen05 / TMEM
+
+namespace fd {
+
+// Tensor memory (TMEM): 512 columns x 128 lanes of 32-bit cells per SM.  An
+// address is lane << 16 | column.  Allocation is per CTA, by one whole warp,
+// in a power of two of at least 32 columns; the address lands in shared
+// memory at `slot`.  The same warp frees it before the CTA exits.
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Order tcgen05 operations around a thread synchronisation (a barrier or an
+// mbarrier wait): `before` ahead of the signalling side, `after` behind the
+// waiting side.
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout that TMA writes with 128-byte swizzling: rows of 128 bytes,
+// eight-row groups 1024 bytes apart, the 16-byte chunk c of row r stored at
+// chunk c ^ (r & 7).  The operand starts at `addr` (its group 1024-byte
+// aligned; a K step inside the 128-byte row adds its byte offset to addr).
+// Fields: start address >> 4 (bits 0-13), leading byte offset >> 4 (16-29;
+// unused here, set to 1), stride byte offset >> 4 (32-45: 1024 B between
+// row groups), the descriptor version 1 (46-47), base offset 0 (49-51), and
+// the swizzle mode 2 = 128-byte (61-63).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of a dense kind::f8f6f4 MMA with E4M3 A and B (both
+// K-major) and an fp32 accumulator: D format 1 = F32 (bits 4-5), A and B
+// formats 0 = E4M3 (7-9, 10-12), N >> 3 (17-22), M >> 4 (24-28).
+__host__ __device__ constexpr uint32_t umma_idesc_e4m3_f32(int m, int n)
+{
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// D[tmem] (+)= A . B^T for one K step of 32 FP8 elements, issued by one thread.
+__device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// One arrival on `bar` once every MMA this thread issued before has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Eight consecutive 32-bit columns of this thread's TMEM lane (warp w of a
+// warpgroup reaches lanes 32 (w % 4) .. 32 (w % 4) + 31; thread i its lane
+// base + i).  The registers are valid after tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Maximum of v over the 32 lanes of the warp, in every lane.
+__device__ __forceinline__ float warp_max_f32(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Two fp32 values rounded to E4M3 (nearest even, saturating at +-448), `lo`
+// in the low byte.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+}  // namespace fd

@@ -47,6 +47,28 @@ constexpr int kProducerWarps = 4;
 constexpr int kSplitThreads = kConsumerThreads + 32;                       // one producer warp
 constexpr int kSplitThreadsCpAsync = kConsumerThreads + 32 * kProducerWarps;
 constexpr int kPairs = kConsumerWarps / 2;
+// The TMEM-score instances (kConsTc5) add one warp that issues the
+// tensor-core score MMAs.
+constexpr int kSplitThreadsTc5 = kConsumerThreads + 64;
+// Their TMEM: kTc5Buffers score buffers of kTc5Cols fp32 columns each
+// (one per tile in flight; columns 16 k + 8 hh + c: E4M3 query part k of
+// column c of paired head hh; two parts for bf16 queries, three for fp16).
+constexpr int kTc5Buffers = 4;
+constexpr int kTc5MaxParts = 3;
+constexpr int kTc5Cols = 64;
+constexpr int kTc5TmemCols = kTc5Buffers * kTc5Cols;
+// Their shared region (SplitParams::off_tc, 1024-byte aligned): the query
+// operand (up to 48 rows of 128 E4M3 codes, swizzled), each consumer warp's weights
+// (32 tokens x 8 columns of fp16, high parts then low parts), the score
+// multipliers of each buffer (2 heads x 8 columns), the score-ready and
+// buffer-free barriers, and the TMEM address.
+constexpr int kTc5QBytes = 16 * kTc5MaxParts * 128;
+constexpr int kTc5PBytes = 2 * 32 * 8 * 2;   // per consumer warp
+constexpr int kTc5OffP = kTc5QBytes;
+constexpr int kTc5OffMul = kTc5OffP + kConsumerWarps * kTc5PBytes;
+constexpr int kTc5OffBar = kTc5OffMul + kTc5Buffers * 16 * 4;
+constexpr int kTc5OffSlot = kTc5OffBar + 2 * kTc5Buffers * 8;
+constexpr int kTc5Bytes = kTc5OffSlot + 16;
 constexpr int kPartBytes = kTileTokens * 128;           // 64 rows x 128 bytes: one swizzled part
 constexpr int kMaxStages = 16;
 constexpr int kMetaInts = 8;
@@ -76,16 +98,28 @@ struct Shape {
 enum : int {
     kConsCudaCores = 0,   // CUDA cores, any group
     kConsMma = 1,         // tensor cores: a warp pair shares the columns, splits the dims
-    kConsMmaPair = 2      // tensor cores on two fused kv heads: each warp of a pair takes one
+    kConsMmaPair = 2,     // tensor cores on two fused kv heads: each warp of a pair takes one
+    // two fused kv heads of an E4M3 cache: scores by tcgen05 MMAs into TMEM,
+    // P.V by warp MMAs; four warps per tile, two tiles in flight
+    kConsTc5 = 3
 };
+
+// Threads of a split CTA: the consumer warps and one producer warp; four
+// producer warps for the cp.async copies (CPA); one more warp issuing the
+// score MMAs for the TMEM-score consumers.
+__host__ __device__ constexpr int split_threads(int cons, bool cpa)
+{
+    return cpa ? kSplitThreadsCpAsync : (cons == kConsTc5 ? kSplitThreadsTc5 : kSplitThreads);
+}
 
 // Floats of the shared reduction region (partial O, m, and the weight sums)
 // for one segment: one state per warp on CUDA cores, one per warp pair (with
 // two weight sums) on tensor cores; with paired heads a pair holds both
-// heads' columns, d/2 dims each.
+// heads' columns, d/2 dims each (the TMEM-score consumers: four states of
+// both heads' columns, the same size).
 __host__ __device__ constexpr int reduction_floats(int cons, int group, int d)
 {
-    return cons == kConsMmaPair ? kPairs * 2 * group * (d / 2 + 3)
+    return (cons == kConsMmaPair || cons == kConsTc5) ? kPairs * 2 * group * (d / 2 + 3)
            : cons == kConsMma   ? kPairs * group * (d + 3)
                                 : kConsumerWarps * group * (d + 2);
 }
@@ -122,6 +156,7 @@ struct SplitParams {
     float scale_log2;             // scale * log2(e)
     int num_stages;
     uint32_t off_red, off_prefix, off_bar, off_meta, off_misc;
+    uint32_t off_tc;              // the TMEM-score instances' region (kTc5Bytes)
     unsigned long long timeout_ns;
     unsigned int flags;
     // Tensor-core path only: 1 when the K/V tensor maps are 4-D views
@@ -1547,17 +1582,452 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
     }
 }
 
+// ------------------------------------------------------------------ TMEM scores (E4M3, paired heads)
+
+// The score issuer of the TMEM-score instances: one warp.  For each tile of
+// the CTA it forms S = K . Q^T for both kv heads of the fused row with four
+// tcgen05 MMAs (M = 128 rows: the tile's 64 tokens of head 0, then those of
+// head 1, as the 128-byte parts of the swizzled K tile lie; N = 16 columns
+// per query part; K = 128 E4M3 dims in four steps of 32) into TMEM buffer
+// (tile index mod kTc5Buffers), and signals the buffer's ready barrier.
+//
+// The query operand holds each column's 16-bit query row as NP E4M3 parts of
+// x = q 2^-sh (sh per column, so that the column's largest |x| lies in
+// [128, 256)): part 0 = E4M3(x), and part k+1 = E4M3(16 r_k) of the
+// remainder r_k = (x scaled by 16^k) - (parts 0..k so scaled).  Each part
+// keeps 4 more significant bits, so NP = 2 parts carry a bf16 query's 8 and
+// NP = 3 an fp16 query's 11 exactly: x = sum_k part_k 16^-k for every element
+// within 2^13 of its column's largest; smaller ones are off by under 2^-21 of
+// the largest.  The consumers take S = (sum_k S_k 16^-k) 2^sh scale log2(e).
+template <int G>
+__device__ __forceinline__ void split_score_issuer(const SplitParams &p, uint8_t *tc, uint32_t stage0,
+                                                   const int *meta, uint32_t full0, uint32_t ready0,
+                                                   uint32_t free0, uint32_t tmem, volatile int *abort_flag,
+                                                   int t_begin, int t_end, int lane)
+{
+    static_assert(G >= 1 && G <= 8, "up to 8 query columns per kv head");
+    constexpr int kStage = Shape<256, kKvE4m3>::kStageBytes;
+    const bool qf16 = p.q_f16 != 0;
+    const int np = qf16 ? 3 : 2;                                    // query parts
+    const uint32_t idesc = umma_idesc_e4m3_f32(128, 16 * np);
+    const int NS = p.num_stages;
+    const uint32_t qop = smem_addr(tc);
+    float *mul_buf = reinterpret_cast<float *>(tc + kTc5OffMul);
+    // lane: query column (head hh, column c) = lane / 2, dims 64 (lane % 2) .. + 63
+    const int pc = lane >> 1, half = lane & 1;
+    const int hh = pc >> 3, c = pc & 7;
+    const int gcol = hh * G + c;
+    float my_mul = 0.f;   // this column's score multiplier (lanes with half == 0 publish it)
+
+    auto give_up = [&]() {
+        if (lane == 0) {
+            atomicOr(p.ws_err, kErrTimeout);
+            *abort_flag = 1;
+        }
+    };
+    // Query rows of segment (b, h) as the E4M3 operand (row 16 k + 8 hh + c
+    // holds part k of column c of head hh; padding columns zero) and this
+    // lane's column multiplier.
+    auto load_query = [&](int b, int h) {
+        const bool colv = c < G && p.col_code[gcol] >= 0;
+        float x[64];
+        float amax = 0.f;
+        if (colv) {
+            const ColInfo col = col_info(p, b, h, gcol);
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.q + col.row * 128 + half * 64);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint4 w = __ldg(src + k);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = qf16 ? f16x2_to_float2(ws[e]) : bf16x2_to_float2(ws[e]);
+                    x[8 * k + 2 * e] = f.x;
+                    x[8 * k + 2 * e + 1] = f.y;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+                amax = fmaxf(amax, fabsf(x[k]));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+                x[k] = 0.f;
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        int sh = 0;
+        if (amax > 0.f) {
+            const int e = ((__float_as_int(amax) >> 23) & 255) - 127;   // floor(log2 amax), normals
+            sh = min(max(e - 7, -120), 126);
+        }
+        const float down = __int_as_float((127 - sh) << 23);   // 2^-sh
+        my_mul = p.scale_log2 * __int_as_float((127 + sh) << 23);
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+            x[k] *= down;
+#pragma unroll
+        for (int part = 0; part < kTc5MaxParts; ++part) {
+            if (part >= np)
+                break;
+            const int row = 16 * part + 8 * hh + c;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {   // 16-dim chunk half * 4 + k of the row
+                uint32_t wd[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float *v = x + 16 * k + 4 * e;
+                    const uint16_t c01 = pack_e4m3x2(v[0], v[1]), c23 = pack_e4m3x2(v[2], v[3]);
+                    const float2 b01 = fp8x2_to_float2<kKvE4m3>(c01), b23 = fp8x2_to_float2<kKvE4m3>(c23);
+                    // the remainder, scaled for the next part (exact in fp32)
+                    v[0] = 16.f * (v[0] - b01.x);
+                    v[1] = 16.f * (v[1] - b01.y);
+                    v[2] = 16.f * (v[2] - b23.x);
+                    v[3] = 16.f * (v[3] - b23.y);
+                    wd[e] = (uint32_t)c01 | ((uint32_t)c23 << 16);
+                }
+                const int chunk = half * 4 + k;
+                const uint32_t a = qop + (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wd[0]), "r"(wd[1]),
+                             "r"(wd[2]), "r"(wd[3])
+                             : "memory");
+            }
+        }
+        // the MMAs (async proxy) read what these generic stores wrote
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+    };
+
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0;
+    for (int t = t_begin; t < t_end; ++t) {
+        const int i = t - t_begin;
+        if (!warp_wait(full0 + 8 * s, ph, p.timeout_ns, abort_flag)) {
+            give_up();
+            break;
+        }
+        const int *mt = meta + s * kMetaInts;
+        const int bi = i % kTc5Buffers;
+        if (mt[4] & kFirstInCta) {
+            // a new segment: the previous tile's MMAs (the last issued) must
+            // have read the query operand before it is rewritten
+            if (i > 0 && !warp_wait(ready0 + 8 * ((i - 1) % kTc5Buffers), (uint32_t)(((i - 1) / kTc5Buffers) & 1),
+                                    p.timeout_ns, abort_flag)) {
+                give_up();
+                break;
+            }
+            load_query(mt[0], mt[1]);
+        }
+        // the consumers of the tile kTc5Buffers back have read this buffer
+        if (!warp_wait(free0 + 8 * bi, (uint32_t)((i / kTc5Buffers) & 1) ^ 1u, p.timeout_ns, abort_flag)) {
+            give_up();
+            break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+            const uint32_t ktile = stage0 + s * kStage;
+            const uint32_t d = tmem + (uint32_t)(bi * kTc5Cols);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                umma_f8f6f4(d, umma_desc_sw128(ktile + 32 * k), umma_desc_sw128(qop + 32 * k), idesc, k > 0);
+            umma_commit(ready0 + 8 * bi);
+        }
+        if (half == 0)
+            mul_buf[bi * 16 + pc] = my_mul;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(ready0 + 8 * bi);   // the second arrival: the multipliers are written
+        ++issued;
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    // Before the TMEM is freed: wait (bounded) for the last MMAs issued.
+    if (issued > 0) {
+        const int k = issued - 1;
+        mbar_wait_bounded(ready0 + 8 * (k % kTc5Buffers), (uint32_t)((k / kTc5Buffers) & 1), p.timeout_ns, nullptr);
+    }
+    __syncwarp();
+}
+
+// The consumers of the TMEM-score instances (E4M3, two fused kv heads of 128
+// dims, up to 8 columns each).  The eight warps form two groups of four;
+// group g takes the CTA's tiles of index g (mod 2), so two tiles are in
+// flight.  In a group, warp w reads TMEM lanes 32 (w % 4) .. + 31: the
+// scores of 32 tokens of head (w % 4) / 2, one token per lane and its
+// head's columns in registers.  Each warp runs its own online softmax over
+// its tokens (column maxima by redux), stages its weights in shared memory
+// as two fp16 parts (as split_consumer_mma: hi, and the rounded remainder lo,
+// both of weights scaled by 2^15), reads them back as the B fragments of P.V,
+// and forms O^T += V^T . P^T over its head's 128 dims with warp MMAs on V
+// converted to fp16 in registers.  The four states of each head (2 groups x
+// 2 token halves) are combined at every segment's last tile in the CTA.
+template <int G>
+__device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t *smem, uint8_t *tc,
+                                                   uint32_t stage0, const int *meta, uint32_t full0,
+                                                   uint32_t empty0, uint32_t cbar, uint32_t ready0, uint32_t free0,
+                                                   uint32_t tmem, volatile int *abort_flag, int t_begin, int t_end,
+                                                   int cw, int lane)
+{
+    static_assert(G >= 1 && G <= 8, "up to 8 query columns per kv head");
+    using HD = Shape<256, kKvE4m3>;
+    constexpr int GT = 2 * G;    // columns of the launch head
+    constexpr int DR = 128;      // dims of one head
+    constexpr int DT = DR / 16;  // 16-dim tiles of P.V
+    constexpr float kPScale = 32768.f;
+    const int NS = p.num_stages;
+    const int gsel = cw >> 2, quad = cw & 3;
+    const int hh = quad >> 1, tokw = (quad & 1) * 32;
+    const int grp = lane >> 2, qd = lane & 3;
+    const int st = gsel * 2 + (quad & 1);   // this warp's state among the head's four
+    float *red_acc = reinterpret_cast<float *>(smem + p.off_red);   // [4 states][GT][DR]
+    float *red_m = red_acc + kPairs * GT * DR;                       // [4 states][GT]
+    float *red_l = red_m + kPairs * GT;                              // [2][4 states][GT]: l, then lt
+    const float *mul_buf = reinterpret_cast<const float *>(tc + kTc5OffMul);
+    const uint32_t pbuf = smem_addr(tc + kTc5OffP + cw * kTc5PBytes);
+    const uint32_t lane_row = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(hh * 8);
+    const int ctid = cw * 32 + lane;
+    const bool qf16 = p.q_f16 != 0;   // three query parts (fp16), else two (bf16)
+
+    float acc[DT][4];            // O^T fragments: dims 16 i + 2 grp (+1), columns 2 qd (+1)
+    float m[G], l[G], lt[G];     // m is the same in every lane; l, lt sum this lane's token
+    int lag[G];
+    auto reset = [&]() {
+#pragma unroll
+        for (int c = 0; c < G; ++c) {
+            m[c] = kNegInf;
+            l[c] = 0.f;
+            lt[c] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < DT; ++i)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                acc[i][k] = 0.f;
+    };
+    auto give_up = [&]() {
+        if (lane == 0) {
+            atomicOr(p.ws_err, kErrTimeout);
+            *abort_flag = 1;
+        }
+    };
+    reset();
+#pragma unroll
+    for (int c = 0; c < G; ++c)
+        lag[c] = p.q_len - 1 - col_info(p, 0, 0, hh * G + c).i;
+
+    int s = 0;
+    uint32_t ph = 0, cph = 0;
+    for (int t = t_begin; t < t_end; ++t) {
+        const int i = t - t_begin;
+        if (!warp_wait(full0 + 8 * s, ph, p.timeout_ns, abort_flag)) {
+            give_up();
+            return;
+        }
+        const int *mt = meta + s * kMetaInts;
+        const int b = mt[0], h = mt[1], rem = mt[2], nvalid = mt[3], flags = mt[4], u = mt[5];
+        bool ragged = false;
+        if ((i & 1) == gsel) {
+            const int bi = i % kTc5Buffers;
+            if (!warp_wait(ready0 + 8 * bi, (uint32_t)((i / kTc5Buffers) & 1), p.timeout_ns, abort_flag)) {
+                give_up();
+                return;
+            }
+            tc_fence_after();
+            // the query parts' scores of this lane's token (16 columns apart)
+            float s0[8], s1[8], s2[8];
+            const uint32_t tb = lane_row + (uint32_t)(bi * kTc5Cols);
+            tmem_ld_x8(tb, s0);
+            tmem_ld_x8(tb + 16, s1);
+            if (qf16)
+                tmem_ld_x8(tb + 32, s2);
+            // the buffer's multipliers, read before it is released: the issuer
+            // rewrites them with the buffer's next MMAs
+            float mul[G];
+#pragma unroll
+            for (int c = 0; c < G; ++c)
+                mul[c] = mul_buf[bi * 16 + hh * 8 + c];
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(free0 + 8 * bi);   // the buffer may take the next MMAs
+
+            // Mask, online softmax over this warp's 32 tokens, weights as hi + lo.
+            const int tok = tokw + lane;
+            float alpha[G];
+            uint32_t phi[4], plo[4];   // columns 2k, 2k + 1 of this lane's token (fp16 pairs)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                phi[k] = plo[k] = 0u;
+#pragma unroll
+            for (int c = 0; c < G; c += 2) {
+                float x[2], pw[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int cc = c + j < G ? c + j : c;
+                    const int lim = p.q_len == 1 ? nvalid : min(nvalid, rem - lag[cc]);
+                    const float sc = qf16 ? s0[cc] + (s1[cc] + s2[cc] * 0.0625f) * 0.0625f
+                                          : s0[cc] + s1[cc] * 0.0625f;
+                    x[j] = tok < lim ? sc * mul[cc] : kNegInf;
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (c + j >= G) {
+                        pw[j] = 0.f;
+                        continue;
+                    }
+                    const float m_new = fmaxf(m[c + j], warp_max_f32(x[j]));
+                    alpha[c + j] = (m[c + j] == kNegInf) ? 0.f : exp2_approx(m[c + j] - m_new);
+                    pw[j] = (x[j] == kNegInf) ? 0.f : exp2_approx(x[j] - m_new);
+                    m[c + j] = m_new;
+                }
+                const uint32_t hi = pack_f16x2(pw[0] * kPScale, pw[1] * kPScale);
+                const float2 hv = f16x2_to_float2(hi);
+                const uint32_t lo = pack_f16x2(pw[0] * kPScale - hv.x, pw[1] * kPScale - hv.y);
+                const float2 lv = f16x2_to_float2(lo);
+                phi[c >> 1] = hi;
+                plo[c >> 1] = lo;
+                l[c] = l[c] * alpha[c] + (hv.x + lv.x);
+                lt[c] = lt[c] * alpha[c] + pw[0];
+                if (c + 1 < G) {
+                    l[c + 1] = l[c + 1] * alpha[c + 1] + (hv.y + lv.y);
+                    lt[c + 1] = lt[c + 1] * alpha[c + 1] + pw[1];
+                }
+            }
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pbuf + lane * 16), "r"(phi[0]),
+                         "r"(phi[1]), "r"(phi[2]), "r"(phi[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pbuf + 512 + lane * 16), "r"(plo[0]),
+                         "r"(plo[1]), "r"(plo[2]), "r"(plo[3])
+                         : "memory");
+            __syncwarp();
+            // P^T B fragments: matrix k of each x4 is tokens 8k .. 8k + 7 of the warp's 32
+            uint32_t bh[4], bl[4];
+            ldmatrix_x4_trans(pbuf + lane * 16, bh[0], bh[1], bh[2], bh[3]);
+            ldmatrix_x4_trans(pbuf + 512 + lane * 16, bl[0], bl[1], bl[2], bl[3]);
+
+            const uint32_t vtile = stage0 + s * HD::kStageBytes + HD::kTileBytes;
+            // V rows past the request's end may hold anything (even NaN), and
+            // the tensor core would form 0 * NaN: zero this warp's rows of its head.
+            ragged = nvalid < tokw + 32;
+            if (ragged) {
+                const int first = nvalid > tokw ? nvalid : tokw;
+                for (int idx = lane; idx < (tokw + 32 - first) * 8; idx += 32) {
+                    const uint32_t a = sw128_addr<HD::kParts>(vtile, first + idx / 8, hh * 8 + idx % 8, 6);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                }
+                __syncwarp();
+            }
+
+            // O^T = alpha O^T + V^T . P^T over the head's 128 dims
+            // alpha of columns 2 qd and 2 qd + 1, by selects (an indexed read
+            // of alpha would put it in local memory)
+            float a0 = alpha[0], a1 = G > 1 ? alpha[G > 1 ? 1 : 0] : 1.f;
+#pragma unroll
+            for (int k = 1; 2 * k < G; ++k) {
+                const bool mine = qd == k;
+                a0 = mine ? alpha[2 * k] : a0;
+                a1 = mine ? alpha[2 * k + 1] : a1;
+            }
+#pragma unroll
+            for (int k = 0; k < DT; ++k) {
+                acc[k][0] *= a0;
+                acc[k][1] *= a1;
+                acc[k][2] *= a0;
+                acc[k][3] *= a1;
+            }
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                // matrices (tokens 0-7 | 8-15 of the k step) x (chunk c | c + 1)
+                const int vrow = tokw + 16 * ks + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+                for (int ii = 0; ii < DT / 2; ++ii) {
+                    const int c = 2 * ii;
+                    uint32_t r0, r1, r2, r3;
+                    ldmatrix_x4_trans(sw128_addr<HD::kParts>(vtile, vrow, hh * 8 + c + (lane >> 4), 6), r0, r1, r2,
+                                      r3);
+                    const uint32_t s0 = prmt(r0, 0u, 0x3120u), s1 = prmt(r1, 0u, 0x3120u);
+                    const uint32_t s2 = prmt(r2, 0u, 0x3120u), s3 = prmt(r3, 0u, 0x3120u);
+                    const uint32_t x0 = fp8x2_to_f16x2<kKvE4m3>(lo16(s0)), x1 = fp8x2_to_f16x2<kKvE4m3>(hi16(s0));
+                    const uint32_t x2 = fp8x2_to_f16x2<kKvE4m3>(lo16(s1)), x3 = fp8x2_to_f16x2<kKvE4m3>(hi16(s1));
+                    const uint32_t y0 = fp8x2_to_f16x2<kKvE4m3>(lo16(s2)), y1 = fp8x2_to_f16x2<kKvE4m3>(hi16(s2));
+                    const uint32_t y2 = fp8x2_to_f16x2<kKvE4m3>(lo16(s3)), y3 = fp8x2_to_f16x2<kKvE4m3>(hi16(s3));
+                    mma_16816<true>(acc[c], x0, x1, x2, x3, bh[2 * ks], bh[2 * ks + 1]);
+                    mma_16816<true>(acc[c + 1], y0, y1, y2, y3, bh[2 * ks], bh[2 * ks + 1]);
+                    mma_16816<true>(acc[c], x0, x1, x2, x3, bl[2 * ks], bl[2 * ks + 1]);
+                    mma_16816<true>(acc[c + 1], y0, y1, y2, y3, bl[2 * ks], bl[2 * ks + 1]);
+                }
+            }
+        }
+        if (ragged)   // order the zeroing stores before the next TMA write to this stage
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty0 + 8 * s);
+
+        if (flags & kLastInCta) {
+#pragma unroll
+            for (int c = 0; c < G; ++c)
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+                    l[c] += __shfl_xor_sync(0xffffffffu, l[c], o);
+                    lt[c] += __shfl_xor_sync(0xffffffffu, lt[c], o);
+                }
+            if (lane == 0) {
+#pragma unroll
+                for (int c = 0; c < G; ++c) {
+                    const int gcol = hh * G + c;
+                    red_m[st * GT + gcol] = m[c];
+                    red_l[st * GT + gcol] = l[c];
+                    red_l[(kPairs + st) * GT + gcol] = lt[c];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int c = 2 * qd + j;   // this lane's columns of the O^T fragments
+                if (c < G) {
+                    float *dst = red_acc + (st * GT + hh * G + c) * DR + 2 * grp;
+#pragma unroll
+                    for (int k = 0; k < DT; ++k) {
+                        dst[16 * k] = acc[k][j];
+                        dst[16 * k + 1] = acc[k][j + 2];
+                    }
+                }
+            }
+            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
+                give_up();
+                return;
+            }
+            combine_and_write<GT, kPairs, DR>(p, red_acc, red_m, red_l, red_l + kPairs * GT, ctid, b, h, u,
+                                              (flags & kOwnSegment) != 0);
+            if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
+                give_up();
+                return;
+            }
+            reset();
+        }
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ kernels
 
 // CPA: paged with pages under 8 tokens on the tensor-core consumers, rows
 // copied by kProducerWarps warps with cp.async (split_producer_cpa).
 template <int G, bool PAGED, int CONS, int KV, int D, bool CPA>
-__global__ void __launch_bounds__(CPA ? kSplitThreadsCpAsync : kSplitThreads, 1)
+__global__ void __launch_bounds__(split_threads(CONS, CPA), 1)
     split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv)
 {
     static_assert(!CPA || (PAGED && CONS != kConsCudaCores), "cp.async copies feed paged tensor-core launches");
-    constexpr int kThreads = CPA ? kSplitThreadsCpAsync : kSplitThreads;
+    static_assert(CONS != kConsTc5 || (KV == kKvE4m3 && D == 256 && !CPA),
+                  "TMEM scores: two fused E4M3 kv heads of 128 dims");
+    constexpr int kThreads = split_threads(CONS, CPA);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -1576,6 +2046,13 @@ __global__ void __launch_bounds__(CPA ? kSplitThreadsCpAsync : kSplitThreads, 1)
             mbar_init(empty0 + 8 * s, kConsumerWarps);
         }
         mbar_init(cbar, kConsumerWarps);
+        if constexpr (CONS == kConsTc5) {
+            const uint32_t ready0 = smem_addr(smem + p.off_tc + kTc5OffBar);
+            for (int k = 0; k < kTc5Buffers; ++k) {
+                mbar_init(ready0 + 8 * k, 2);                        // the MMAs' commit + the issuer
+                mbar_init(ready0 + 8 * (kTc5Buffers + k), 4);        // the four warps reading it
+            }
+        }
         misc[0] = 0;
         mbar_init_fence();
     }
@@ -1609,7 +2086,36 @@ __global__ void __launch_bounds__(CPA ? kSplitThreadsCpAsync : kSplitThreads, 1)
     if (t_begin >= t_end)
         return;
     volatile int *abort_flag = misc;
-    if (warp >= kConsumerWarps) {
+    if constexpr (CONS == kConsTc5) {
+        // The score issuer's warp holds the CTA's TMEM from here to the end;
+        // every warp reaches both barriers (the roles return, bounded, on
+        // their own), and the issuer has waited for its last MMAs.
+        uint8_t *tc = smem + p.off_tc;
+        const uint32_t ready0 = smem_addr(tc + kTc5OffBar), free0 = ready0 + 8 * kTc5Buffers;
+        const uint32_t slot = smem_addr(tc + kTc5OffSlot);
+        const int issuer = kConsumerWarps + 1;
+        if (warp == issuer)
+            tmem_alloc(slot, kTc5TmemCols);
+        tc_fence_before();
+        named_bar_sync(1, kThreads);
+        tc_fence_after();
+        const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tc + kTc5OffSlot);
+        if (warp == kConsumerWarps)
+            split_producer<PAGED, true, D, KV>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
+                                               t_begin, t_end, lane);
+        else if (warp == issuer)
+            split_score_issuer<G>(p, tc, stage0, meta, full0, ready0, free0, tmem, abort_flag, t_begin, t_end,
+                                  lane);
+        else
+            split_consumer_tc5<G>(p, smem, tc, stage0, meta, full0, empty0, cbar, ready0, free0, tmem,
+                                  abort_flag, t_begin, t_end, warp, lane);
+        tc_fence_before();
+        named_bar_sync(1, kThreads);
+        if (warp == issuer) {
+            tc_fence_after();
+            tmem_dealloc(tmem, kTc5TmemCols);
+        }
+    } else if (warp >= kConsumerWarps) {
         if constexpr (CPA)
             split_producer_cpa<D, KV>(p, stage0, prefix, meta, full0, empty0, abort_flag, t_begin, t_end, lane,
                                       warp - kConsumerWarps);

@@ -37,6 +37,10 @@ constexpr double kFuseMinTilesPerCta = 24.0;
 // that touches one more segment takes this many fewer tiles.
 constexpr int kSegCostTiles = 2;
 
+// The tcgen05 score consumers (kConsTc5) are the default for paired E4M3
+// heads of up to this many query columns per kv head (fd_api.cu).
+constexpr int kTc5DefaultColumns = 4;
+
 // Shared-memory plan of the split kernel (fd_api.cu): pipeline stages, the
 // offsets of every region in sp, the L2 prefetch before the dependency wait
 // (sp->prefetch_tiles), and the byte size and merge trigger in launch, for
@@ -89,8 +93,7 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
         return e;
     if (c.blocks_per_sm)
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(c.blocks_per_sm, split_kernel<G, PAGED, CONS, KV, D, CPA>,
-                                                             CPA ? kSplitThreadsCpAsync : kSplitThreads,
-                                                             c.smem_bytes);
+                                                             split_threads(CONS, CPA), c.smem_bytes);
     // Programmatic dependent launch: the kernel's prologue may overlap the
     // previous kernel in the stream; it waits for it before reading inputs.
     cudaLaunchAttribute attr[1];
@@ -98,7 +101,7 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)c.grid);
-    cfg.blockDim = dim3(CPA ? kSplitThreadsCpAsync : kSplitThreads);
+    cfg.blockDim = dim3(split_threads(CONS, CPA));
     cfg.dynamicSmemBytes = c.smem_bytes;
     cfg.stream = c.stream;
     cfg.attrs = attr;
@@ -116,7 +119,8 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
 // One split-kernel variant per (layout, K/V element type, row dims D):
 // consumers on CUDA cores (group 1 to 8), on tensor cores (group 2 to 16,
 // swizzled K/V maps, rows of at least 128 bytes), or on tensor cores with two
-// fused kv heads per row (group = columns per head, 1 to 16; D = 2 x head_dim).
+// fused kv heads per row (group = columns per head, 1 to 16; D = 2 x head_dim),
+// or with scores in TMEM (kConsTc5: E4M3, D = 256, group 1 to 8).
 // cp_async: paged with pages under 8 tokens on the tensor cores (the CPA
 // instances, 384 threads; tensor-core groups only).
 // Returns cudaErrorInvalidValue for an unsupported combination.
@@ -145,6 +149,18 @@ cudaError_t launch_split_variant(int cons, int group, bool cp_async, const Split
             case 4: return launch_split_t<4, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
             case 8: return launch_split_t<8, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
             case 16: return launch_split_t<16, PAGED, kConsMma, KV, D>(p, tmk, tmv, c);
+            default: return cudaErrorInvalidValue;
+            }
+        }
+        return cudaErrorInvalidValue;
+    }
+    if (cons == kConsTc5) {   // scores in TMEM: two fused E4M3 heads of 128 dims, up to 8 columns each
+        if constexpr (KV == kKvE4m3 && D == 256) {
+            switch (group) {
+            case 1: return launch_split_t<1, PAGED, kConsTc5, KV, D>(p, tmk, tmv, c);
+            case 2: return launch_split_t<2, PAGED, kConsTc5, KV, D>(p, tmk, tmv, c);
+            case 4: return launch_split_t<4, PAGED, kConsTc5, KV, D>(p, tmk, tmv, c);
+            case 8: return launch_split_t<8, PAGED, kConsTc5, KV, D>(p, tmk, tmv, c);
             default: return cudaErrorInvalidValue;
             }
         }
