@@ -1706,9 +1706,11 @@ __device__ __forceinline__ void split_score_issuer(const SplitParams &p, uint8_t
             give_up();
             break;
         }
-        const int *mt = meta + s * kMetaInts;
+        const uint32_t ma = smem_addr(meta + s * kMetaInts);   // 8-byte aligned
+        const uint2 m01 = lds64(ma), m45 = lds64(ma + 16);
+        const bool first = ((int)m45.x & kFirstInCta) != 0;
         const int bi = i % kTc5Buffers;
-        if (mt[4] & kFirstInCta) {
+        if (first) {
             // a new segment: the previous tile's MMAs (the last issued) must
             // have read the query operand before it is rewritten
             if (i > 0 && !warp_wait(ready0 + 8 * ((i - 1) % kTc5Buffers), (uint32_t)(((i - 1) / kTc5Buffers) & 1),
@@ -1716,7 +1718,7 @@ __device__ __forceinline__ void split_score_issuer(const SplitParams &p, uint8_t
                 give_up();
                 break;
             }
-            load_query(mt[0], mt[1]);
+            load_query((int)m01.x, (int)m01.y);
         }
         // the consumers of the tile kTc5Buffers back have read this buffer
         if (!warp_wait(free0 + 8 * bi, (uint32_t)((i / kTc5Buffers) & 1) ^ 1u, p.timeout_ns, abort_flag)) {
@@ -1825,8 +1827,10 @@ __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t
             give_up();
             return;
         }
-        const int *mt = meta + s * kMetaInts;
-        const int b = mt[0], h = mt[1], rem = mt[2], nvalid = mt[3], flags = mt[4], u = mt[5];
+        const uint32_t ma = smem_addr(meta + s * kMetaInts);   // 8-byte aligned
+        const uint2 mv0 = lds64(ma), mv1 = lds64(ma + 8), mv2 = lds64(ma + 16);
+        const int b = (int)mv0.x, h = (int)mv0.y, rem = (int)mv1.x, nvalid = (int)mv1.y, flags = (int)mv2.x,
+                  u = (int)mv2.y;
         bool ragged = false;
         if ((i & 1) == gsel) {
             const int bi = i % kTc5Buffers;
@@ -1845,9 +1849,16 @@ __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t
             // the buffer's multipliers, read before it is released: the issuer
             // rewrites them with the buffer's next MMAs
             float mul[G];
+            {
+                const uint32_t mb = smem_addr(mul_buf) + (uint32_t)(bi * 64 + hh * 32);
+                const uint4 m0 = lds128(mb), m1 = lds128(mb + 16);
+                const float mm[8] = {__uint_as_float(m0.x), __uint_as_float(m0.y), __uint_as_float(m0.z),
+                                     __uint_as_float(m0.w), __uint_as_float(m1.x), __uint_as_float(m1.y),
+                                     __uint_as_float(m1.z), __uint_as_float(m1.w)};
 #pragma unroll
-            for (int c = 0; c < G; ++c)
-                mul[c] = mul_buf[bi * 16 + hh * 8 + c];
+                for (int c = 0; c < G; ++c)
+                    mul[c] = mm[c];
+            }
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
