@@ -108,14 +108,15 @@ def consumers_label(flags, w) -> str:
     short = row < 256 or (w.paged and w.page_size < 64)
     tiles = sum((int(L) + 63) // 64 for L in w.seq_lens) * w.num_kv_heads
     long_call = tiles / 152 >= 24
-    fused = short and long_call and any(f * w.head_dim <= 256 and w.num_kv_heads % f == 0 and
-                                        (G <= 16 if f == 2 else 4 * G <= 8) for f in (2, 4))
+    fp8_single = fp8 and w.head_dim == 128 and G == 1   # paired at any length
+    fused = short and (long_call or fp8_single) and any(f * w.head_dim <= 256 and w.num_kv_heads % f == 0 and
+                                                        (G <= 16 if f == 2 else 4 * G <= 8) for f in (2, 4))
     if (G == 1 or row < 128) and not fused:
         return "cuda cores"
     tc5_shape = (fused and w.kv_dtype == "e4m3" and w.head_dim == 128 and G <= 8 and w.num_kv_heads % 2 == 0
                  and (not w.paged or w.page_size >= 64))
     # FD_FLAG_TMEM_SCORES (0x80) forces the tcgen05 scores, FD_FLAG_NO_TMEM_SCORES (0x100) keeps the warp MMAs
-    if tc5_shape and not flags & 0x100 and (G <= 4 or flags & 0x80):
+    if tc5_shape and not flags & 0x100 and ((G <= 4 and tiles / (2 * 152) >= 24) or flags & 0x80):
         return "tensor cores (tcgen05 E4M3 scores into TMEM, mma.sync fp16 P.V), fused kv heads"
     return f"tensor cores ({mma})" + (", fused kv heads" if fused else "")
 

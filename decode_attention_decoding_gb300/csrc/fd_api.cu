@@ -374,7 +374,12 @@ int fuse_factor(int cols, int hkv, int head_dim, int elem_bytes, int page_size, 
     // over 8 columns need the tensor-core consumers, whose rows span at least
     // 128 bytes: a shorter row (an FP8 head of 64 dims) is paired whenever it can be
     const bool needed = cols > kMaxColumnsCudaCores && head_dim * elem_bytes < 128;
-    const bool forced = (opts && (opts->flags & FD_FLAG_FUSE_HEADS)) || needed;
+    // One column per kv head of an FP8 cache with 128 dims would run on CUDA
+    // cores unfused; paired, it takes the tensor cores, which measured faster
+    // on GB300 at any length (MHA over a 32 MiB E4M3 cache: 16.3 -> 14.1 us,
+    // at half that length 12.9 -> 12.2 us).
+    const bool fp8_single = elem_bytes == 1 && head_dim == 128 && cols == 1;
+    const bool forced = (opts && (opts->flags & FD_FLAG_FUSE_HEADS)) || needed || fp8_single;
     if (!forced && (!short_rows || tiles_per_cta < kFuseMinTilesPerCta))
         return 1;
     const bool four = 4 * head_dim <= 256 && 4 * cols <= 8 && hkv % 4 == 0;
@@ -533,11 +538,14 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     // pages interleave the heads page by page.  By default for up to
     // kTc5DefaultColumns columns per kv head: their consumers' softmax work
     // grows with the columns, the warp MMAs' does not (measured on GB300:
-    // 1 and 4 columns faster, 8 slower).
+    // 1 and 4 columns faster, 8 slower); and for calls of at least
+    // kFuseMinTilesPerCta (paired) tiles per CTA, where their fixed costs
+    // (TMEM, the score round trip) amortise (MHA over a 32 MiB E4M3 cache,
+    // 6.7 tiles per CTA: 14.1 us with warp MMAs, 16.3 with them).
     const bool tc5_shape = paired && kv == kKvE4m3 && d == 256 && group <= 8 &&
                            (page_size == 0 || page_size >= kTileTokens);
-    if (tc5_shape && !(sp.flags & FD_FLAG_NO_TMEM_SCORES) &&
-        (group <= kTc5DefaultColumns || (sp.flags & FD_FLAG_TMEM_SCORES)))
+    const bool tc5_default = group <= kTc5DefaultColumns && est_tiles / (2.0 * num_ctas) >= kFuseMinTilesPerCta;
+    if (tc5_shape && !(sp.flags & FD_FLAG_NO_TMEM_SCORES) && (tc5_default || (sp.flags & FD_FLAG_TMEM_SCORES)))
         cp->cons = kConsTc5;
     if (fuse > 1 && !use_mma(2, eb * d, opts))
         return FD_ERR_UNSUPPORTED;   // fusion is defined for the tensor-core consumers only

@@ -145,8 +145,9 @@ typedef struct fd_options {
  * a kv head's rows are short (under 256 bytes: head_dim 64, or an FP8 cache
  * with head_dim up to 128, or pages under 64 tokens) and the call has at
  * least 24 KV tiles of 64 tokens per split CTA (counted from seq_lens_host
- * when given, else from the capacity), F adjacent kv heads are read as one
- * head of F * head_dim dims: [.., Hkv, D] and [.., Hkv/F, F*D] are the same
+ * when given, else from the capacity) -- or, whatever the call's length, the
+ * cache is FP8 with head_dim 128 and one query column per kv head -- F
+ * adjacent kv heads are read as one head of F * head_dim dims: [.., Hkv, D] and [.., Hkv/F, F*D] are the same
  * bytes, so each TMA row is F times longer.
  *   F = 4 when 4 * head_dim <= 256, 4 * G * q_len <= 8 and 4 divides Hkv: the
  *         four query groups share one tensor-core tile, with zeros for the
@@ -179,8 +180,9 @@ typedef struct fd_options {
  * are paired (head_dim 128; contiguous, or pages of at least 64 tokens) the
  * scores are by default formed with tcgen05 MMAs straight from the E4M3 K
  * tile into tensor memory, against the query split into E4M3 parts (two for
- * bf16, three for fp16: exact), when a kv head has at most 4 query columns;
- * warp MMAs on K converted to fp16 in registers otherwise.  Measured on
+ * bf16, three for fp16: exact), when a kv head has at most 4 query columns
+ * and the call has at least 24 paired KV tiles per split CTA; warp MMAs on
+ * K converted to fp16 in registers otherwise.  Measured on
  * GB300, the tcgen05 scores took the 1 GiB MHA call 6% and the ragged GQA-4
  * call 3% faster, and the GQA-8 call 2% slower.  This flag takes the
  * tcgen05 scores for up to 8 columns too; FD_FLAG_NO_TMEM_SCORES never

@@ -49,20 +49,24 @@ def test_contiguous_vs_oracle(group, hkv):
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
 def test_default_choice(group):
     """Paired E4M3 heads take the tcgen05 scores by default for up to 4
-    columns per kv head and the warp MMAs above: the default launch equals
-    the forced one bit for bit and differs from the other (the scores come
-    from another unit, summed in another order); all match the oracle."""
+    columns per kv head (on calls of at least 24 paired tiles per CTA: here
+    two CTAs) and the warp MMAs above: the default launch equals the forced
+    one bit for bit and differs from the other (the scores come from another
+    unit, summed in another order); all match the oracle."""
     w = workload(2150 + group, group)
     ro, rl = oracle.attend(w, threads=8)
-    runs = {name: run(w, num_ctas=7, flags=FUSE | f) for name, f in (("default", 0), ("tmem", TMEM),
+    runs = {name: run(w, num_ctas=2, flags=FUSE | f) for name, f in (("default", 0), ("tmem", TMEM),
                                                                       ("warp", NO_TMEM))}
     for name, (o, l) in runs.items():
         check(o, l, ro, rl, f"G={group} {name}")
     same, other = ("tmem", "warp") if group <= 4 else ("warp", "tmem")
     assert np.array_equal(runs["default"][0], runs[same][0]) and np.array_equal(runs["default"][1], runs[same][1])
     assert not np.array_equal(runs["default"][0], runs[other][0])
+    # a shorter call (7 CTAs, under 24 paired tiles each): the warp MMAs by default
+    o, l = run(w, num_ctas=7, flags=FUSE)
+    assert np.array_equal(o, run(w, num_ctas=7, flags=FUSE | NO_TMEM)[0])
     # both flags: the warp MMAs
-    o, l = run(w, num_ctas=7, flags=FUSE | TMEM | NO_TMEM)
+    o, l = run(w, num_ctas=2, flags=FUSE | TMEM | NO_TMEM)
     assert np.array_equal(o, runs["warp"][0]) and np.array_equal(l, runs["warp"][1])
 
 
