@@ -25,7 +25,7 @@ __all__ = [
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
     "FD_ERR_CUDA", "FD_ERR_TIMEOUT", "FD_ERR_DEVICE_INPUT", "FD_FLAG_TEST_STARVE_FIRST_TILE",
     "FD_FLAG_CUDA_CORES", "FD_FLAG_NO_4D_BOXES", "FD_FLAG_NO_HEAD_FUSION", "FD_FLAG_NO_GATHER",
-    "FD_FLAG_FUSE_HEADS", "FD_FLAG_NO_PREFETCH", "FD_FLAG_TMEM_SCORES", "FD_FLAG_NO_TMEM_SCORES", "FD_FLAG_FUSED_MERGE", "FD_KV_AS_Q", "FD_KV_FP8_E4M3", "FD_KV_FP8_E5M2",
+    "FD_FLAG_FUSE_HEADS", "FD_FLAG_NO_PREFETCH", "FD_FLAG_TMEM_SCORES", "FD_FLAG_NO_TMEM_SCORES", "FD_KV_AS_Q", "FD_KV_FP8_E4M3", "FD_KV_FP8_E5M2",
     "fd_decode_noalloc", "fd_decode_partial", "fd_decode_paged_partial", "fd_merge_partials",
     "KV_END",
 ]
@@ -41,7 +41,6 @@ FD_FLAG_FUSE_HEADS = 0x10
 FD_FLAG_NO_PREFETCH = 0x40
 FD_FLAG_TMEM_SCORES = 0x80
 FD_FLAG_NO_TMEM_SCORES = 0x100
-FD_FLAG_FUSED_MERGE = 0x200
 FD_KV_AS_Q, FD_KV_FP8_E4M3, FD_KV_FP8_E5M2 = 0, 1, 2
 KV_END = 2 ** 31 - 1   # kv_end of a range that runs to the end of every request
 

@@ -153,7 +153,7 @@ fd_status plan_smem(const DeviceInfo &dev, int cons, int group, int d, int elem_
     const size_t stage_bytes = 2u * kTileTokens * (size_t)elem_bytes * (size_t)d;   // K and V tiles
     const size_t red = align_up((size_t)reduction_floats(cons, group, d) * sizeof(float), 16);
     const size_t prefix = align_up(2 * sizeof(int) * (size_t)(batch + 1), 16);   // tile prefix, non-empty requests
-    const size_t misc = 128;   // abort flag, two scans' scratch, the merge flag (kMiscLastFlag)
+    const size_t misc = 128;   // abort flag, two scans' scratch
     const size_t per_stage_extra = 2 * 8 + kMetaInts * sizeof(int);   // 2 barriers + metadata
     const size_t tc = cons == kConsTc5 ? align_up((size_t)kTc5Bytes, 16) : 0;   // TMEM-score region
     const size_t fixed = 1024 /* alignment slack */ + tc + red + prefix + misc + 8 /* consumer barrier */;
@@ -434,12 +434,12 @@ bool host_lens_valid(const int32_t *seq_lens_host, int batch, long long cap, con
 size_t workspace_bytes_needed(int batch, int hq, int hkv, int head_dim, int q_len)
 {
     const int cols = (hq / hkv) * q_len;
-    size_t need = workspace_layout(batch, hkv, pow2_columns(cols), head_dim, hkv).total;
+    size_t need = workspace_layout(batch, hkv, pow2_columns(cols), head_dim).total;
     auto take = [&](size_t t) { need = t > need ? t : need; };
     if (2 * head_dim <= 256 && hkv % 2 == 0)   // paired heads: both heads' columns
-        take(workspace_layout(batch, hkv / 2, 2 * pow2_columns(cols), head_dim, hkv).total);
+        take(workspace_layout(batch, hkv / 2, 2 * pow2_columns(cols), head_dim).total);
     if (4 * head_dim <= 256 && 4 * cols <= 8 && hkv % 4 == 0)   // four heads in one row
-        take(workspace_layout(batch, hkv / 4, pow2_columns(4 * cols), 4 * head_dim, hkv).total);
+        take(workspace_layout(batch, hkv / 4, pow2_columns(4 * cols), 4 * head_dim).total);
     return need;
 }
 
@@ -471,9 +471,8 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     const int slots = paired ? 2 * group : group;        // column slots of a launch head
     const int d = fuse * head_dim;
     const int merge_dim = paired ? head_dim : d;
-    const int caller_hkv = hkv;
     hkv /= fuse;
-    const WorkspaceLayout wl = workspace_layout(batch, hkv, slots, merge_dim, caller_hkv);
+    const WorkspaceLayout wl = workspace_layout(batch, hkv, slots, merge_dim);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
 
     SplitParams &sp = cp->sp;
@@ -559,13 +558,6 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
                              kv_bytes / num_ctas, &sp, &cp->launch);
     if (st != FD_OK)
         return st;
-    // FD_FLAG_FUSED_MERGE: the split kernel merges its split segments itself
-    // (the last CTA of a segment to write its partial merges them) and no
-    // merge kernel runs.  Measured on GB300 (graph-replayed calls, µs): MHA
-    // 64 MiB 17.1 -> 17.1, ragged GQA-4 50.6 -> 51.1, its FP8 form 33.9 ->
-    // 36.4: the counting and the last CTA's merge sit on each CTA's tail,
-    // while the merge kernel's launch overlaps the split grid's.
-    sp.ws_cnt = (sp.flags & FD_FLAG_FUSED_MERGE) ? reinterpret_cast<int32_t *>(ws + wl.cnt_off) : nullptr;
 
     MergeParams &mp = cp->mp;
     std::memset(&mp, 0, sizeof mp);
@@ -638,11 +630,9 @@ fd_status run(CallPlan cp, bool paged, const CUtensorMap &tmk, const CUtensorMap
         return FD_ERR_CUDA;
     if (ev1 && !record_event(ev1, stream))
         return FD_ERR_CUDA;
-    if (!cp.sp.ws_cnt) {
-        e = launch_merge(cp.merge_group, cp.merge_dim, cp.mp, cp.sp.batch * cp.sp.hkv, stream);
-        if (e != cudaSuccess)
-            return FD_ERR_CUDA;
-    }
+    e = launch_merge(cp.merge_group, cp.merge_dim, cp.mp, cp.sp.batch * cp.sp.hkv, stream);
+    if (e != cudaSuccess)
+        return FD_ERR_CUDA;
     return FD_OK;
 }
 

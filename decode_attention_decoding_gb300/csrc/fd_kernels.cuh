@@ -72,7 +72,6 @@ constexpr int kTc5Bytes = kTc5OffSlot + 16;
 constexpr int kPartBytes = kTileTokens * 128;           // 64 rows x 128 bytes: one swizzled part
 constexpr int kMaxStages = 16;
 constexpr int kMetaInts = 8;
-constexpr int kMiscLastFlag = 31;   // int of the misc region: this CTA merges the segment (fixup_segment)
 constexpr int kRowsPerWarp = kTileTokens / kConsumerWarps;   // 8
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -130,11 +129,7 @@ __host__ __device__ constexpr int reduction_floats(int cons, int group, int d)
 // writes the tile's metadata.
 constexpr int kCpAsyncArrivals = 32 * kProducerWarps + 1;
 
-// Per-tile metadata, written by the producer into shared memory: request b,
-// launch head h, the request's tokens from the tile on (causal limits), valid
-// rows, flags, segment u, and the segment's first CTA and CTA count (the
-// merge inside the split kernel).
-// Its flags:
+// Per-tile metadata flags, written by the producer into shared memory.
 enum : int { kFirstInCta = 1, kLastInCta = 2, kOwnSegment = 4 };
 
 // Query columns of one kv head (group x new tokens): up to two n8 tiles on
@@ -154,11 +149,6 @@ struct SplitParams {
     float *ws_lse;                // [slots, G]
     int32_t *ws_prefix;           // [B + 1] tile prefix, then [B + 1] non-empty requests
     unsigned int *ws_err;
-    // Segment counters [B * Hkv], zero at rest: when set, the split kernel
-    // merges split segments itself (the last CTA to write a segment's partial
-    // merges them; fixup_segment) and no merge kernel runs.  Null: the merge
-    // kernel does it.
-    int32_t *ws_cnt;
     int batch, hq, hkv;
     int cap;                      // largest valid length
     int s_max;                    // contiguous: token rows per request
@@ -400,18 +390,6 @@ __device__ __forceinline__ void build_prefix(const SplitParams &p, int *prefix, 
             p.ws_prefix[b] = prefix[b];
 }
 
-// The CTAs of segment (b, h): the first, c0, and how many, from the cost
-// positions of its first and last tile (the Schedule of this grid).
-__device__ __forceinline__ void segment_ctas(const SplitParams &p, const int *prefix, int b, int h, int *c0,
-                                             int *n)
-{
-    const Schedule sc{prefix, prefix + p.batch + 1, p.batch, p.hkv, p.seg_cost, (int)gridDim.x};
-    const int nb = (prefix[b + 1] - prefix[b]) / p.hkv;
-    const long long pos0 = sc.seg_pos(b, h);
-    *c0 = sc.cta_at(pos0);
-    *n = sc.cta_at(pos0 + nb - 1) - *c0 + 1;
-}
-
 // ------------------------------------------------------------------ producer
 
 // Byte address of 16-byte chunk `chunk` (0 .. row bytes / 16 - 1) of `row`
@@ -526,7 +504,6 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
         }
     };
 
-    int seg_c0 = 0, seg_n = 1;   // the current segment's CTAs (tile metadata)
     int s = 0;
     uint32_t ph = 0;
     int issued = 0;
@@ -559,8 +536,6 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
         // pages of this tile that hold valid tokens (paged, P < 64)
         const int need = small_pages ? min(kTileTokens >> page_log2, (nvalid + P - 1) >> page_log2) : 1;
         if (lane == 0) {
-            if (flags & kFirstInCta)
-                segment_ctas(p, prefix, b, h, &seg_c0, &seg_n);
             int *m = meta + s * kMetaInts;
             m[0] = b;
             m[1] = h;
@@ -568,8 +543,6 @@ __device__ __forceinline__ void split_producer(const SplitParams &p, const CUten
             m[3] = nvalid;
             m[4] = flags;
             m[5] = b * p.hkv + h;
-            m[6] = seg_c0;
-            m[7] = seg_n;
             const uint32_t bytes = gather ? 2u * (uint32_t)(((nvalid + 3) >> 2) * 4 * HD::kRowBytes)
                                    : small_pages ? 2u * need * P * HD::kRowBytes
                                                  : (uint32_t)(2 * HD::kTileBytes);
@@ -743,7 +716,6 @@ __device__ __forceinline__ void split_producer_cpa(const SplitParams &p, uint32_
         return idx < p.max_blocks ? __ldg(p.block_table + (size_t)b * p.max_blocks + idx) : 0;
     };
 
-    int seg_c0 = 0, seg_n = 1;   // the current segment's CTAs (tile metadata)
     int s = 0;
     uint32_t ph = 0;
     int issued = 0;
@@ -769,8 +741,6 @@ __device__ __forceinline__ void split_producer_cpa(const SplitParams &p, uint32_
                 flags |= kLastInCta;
             if (seg_first >= t_begin && seg_first + nb <= t_end)
                 flags |= kOwnSegment;
-            if (flags & kFirstInCta)
-                segment_ctas(p, prefix, b, h, &seg_c0, &seg_n);
             int *m = meta + s * kMetaInts;
             m[0] = b;
             m[1] = h;
@@ -778,8 +748,6 @@ __device__ __forceinline__ void split_producer_cpa(const SplitParams &p, uint32_
             m[3] = nvalid;
             m[4] = flags;
             m[5] = b * p.hkv + h;
-            m[6] = seg_c0;
-            m[7] = seg_n;
             if (!(starve && issued == 0))
                 mbar_arrive(full);
         }
@@ -903,102 +871,6 @@ __device__ __forceinline__ void combine_and_write(const SplitParams &p, const fl
     }
 }
 
-// The merge inside the split kernel (ws_cnt set), run by every consumer
-// thread of a CTA that has just written its partial of split segment u
-// (normalised output and natural-log LSE, slot u + c, for CTAs c0 .. c0 +
-// n - 1).  After a barrier of the consumer threads, one thread fences (so
-// the CTA's partial writes, ordered before it by the barrier, precede the
-// count at device scope) and counts the partial in the segment's counter;
-// the CTA whose count is the n-th, the last to write, merges the segment's n
-// partials (read from L2) into its output and resets the counter.  No CTA waits for another, so any grid size
-// is safe.  The merge is the one of the Flash-Decoding section of the
-// FlashAttention handbook page: M = max_i lse_i, LSE = M + ln sum_i exp(lse_i
-// - M), O = sum_i O_i exp(lse_i - LSE), a partial with lse_i = -inf
-// contributing nothing; here in one pass over the partials, the running sums
-// rescaled when the maximum grows.  Returns false if a consumer barrier ran
-// out.
-template <int G, int D>
-__device__ __forceinline__ bool fixup_segment(const SplitParams &p, volatile int *last_flag, int c0, int n, int b,
-                                              int h, int u, int ctid, int lane, uint32_t cbar, uint32_t &cph,
-                                              const volatile int *abort_flag)
-{
-    if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane))
-        return false;
-    if (ctid == 0) {
-        __threadfence();   // the CTA's partial, before the count
-        const int before = atomicAdd(p.ws_cnt + u, 1);
-        const bool last = before == n - 1;
-        if (last) {
-            __threadfence();   // the other partials, before this CTA reads them
-            p.ws_cnt[u] = 0;
-        }
-        *last_flag = last ? 1 : 0;
-    }
-    if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane))
-        return false;
-    if (!*last_flag)
-        return true;
-    constexpr int kChunk = 8;
-    for (int idx = ctid; idx < G * D; idx += kConsumerThreads) {
-        const int g = idx / D, d = idx % D;
-        if (p.col_code[g] < 0)
-            continue;   // padding column
-        float M = kNegInf, S = 0.f, acc = 0.f;
-        for (int i0 = 0; i0 < n; i0 += kChunk) {
-            float lv[kChunk], ov[kChunk];
-#pragma unroll
-            for (int k = 0; k < kChunk; ++k) {
-                const size_t slot = (size_t)(u + c0 + i0 + k);
-                const bool in = i0 + k < n;
-                lv[k] = in ? __ldcg(p.ws_lse + slot * G + g) : kNegInf;
-                ov[k] = in ? __ldcg(p.ws_o + (slot * G + g) * D + d) : 0.f;
-            }
-#pragma unroll
-            for (int k = 0; k < kChunk; ++k) {
-                if (lv[k] == kNegInf)
-                    continue;
-                if (lv[k] > M) {
-                    const float r = expf(M - lv[k]);   // 0 while M = -inf
-                    S = S * r + 1.f;
-                    acc = acc * r + ov[k];
-                    M = lv[k];
-                } else {
-                    const float wgt = expf(lv[k] - M);
-                    S += wgt;
-                    acc += wgt * ov[k];
-                }
-            }
-        }
-        const ColInfo col = col_info(p, b, h, g);
-        const bool seen = M != kNegInf;   // some partial saw a visible token
-        store_o<D>(p.o, col.row, d, p.fuse_dh, col.dim0, seen ? acc / S : 0.f);
-        if (d == 0 && p.lse)
-            p.lse[col.row] = seen ? M + logf(S) : kNegInf;
-    }
-    return true;
-}
-
-// Requests with no tokens in the call get O = 0 and LSE = -inf in every
-// query row (no CTA has a tile of them); CTA c takes requests c, c + grid,
-// ...  Used when the split kernel merges its segments itself.  D: the
-// launch's row dims (fuse_f caller heads of D / fuse_f dims).
-template <int D>
-__device__ __forceinline__ void write_empty_requests(const SplitParams &p, const int *prefix, int tid, int nthreads)
-{
-    const int dh = D / p.fuse_f;
-    const int rows = p.q_len * p.hq;   // query rows of a request, [q_len, Hq]
-    for (int b = (int)blockIdx.x; b < p.batch; b += (int)gridDim.x) {
-        if (prefix[b + 1] != prefix[b])
-            continue;
-        float *o = p.o + (size_t)b * rows * dh;
-        for (int i = tid; i < rows * dh; i += nthreads)
-            o[i] = 0.f;
-        if (p.lse)
-            for (int i = tid; i < rows; i += nthreads)
-                p.lse[(size_t)b * rows + i] = kNegInf;
-    }
-}
-
 // Eight consecutive K or V elements of a shared-memory row, widened to fp32:
 // one 16-byte load of 16-bit values, or one 8-byte load of FP8 codes.
 template <int KV>
@@ -1099,7 +971,6 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
         }
         const int *mt = meta + s * kMetaInts;
         const int b = mt[0], h = mt[1], rem = mt[2], nvalid = mt[3], flags = mt[4], u = mt[5];
-        const int seg_c0 = mt[6], seg_n = mt[7];
 
         if (flags & kFirstInCta) {
             const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
@@ -1247,12 +1118,6 @@ __device__ __forceinline__ void split_consumer(const SplitParams &p, uint8_t *sm
             // 3. combine the warps and write the segment's result
             combine_and_write<G, WR, D>(p, red_acc, red_m, red_l, red_l, ctid, b, h, u,
                                         (flags & kOwnSegment) != 0);
-            if (p.ws_cnt && !(flags & kOwnSegment) &&
-                !fixup_segment<G, D>(p, abort_flag + kMiscLastFlag, seg_c0, seg_n, b, h, u, ctid, lane, cbar, cph,
-                                     abort_flag)) {
-                give_up();
-                return;
-            }
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
@@ -1409,7 +1274,6 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
         }
         const int *mt = meta + s * kMetaInts;
         const int b = mt[0], h = mt[1], rem = mt[2], nvalid = mt[3], flags = mt[4], u = mt[5];
-        const int seg_c0 = mt[6], seg_n = mt[7];
 
         if (flags & kFirstInCta) {
 #pragma unroll
@@ -1705,12 +1569,6 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
             }
             combine_and_write<GT, kPairs, DR>(p, red_acc, red_m, red_l, red_l + kPairs * GT, ctid, b, h, u,
                                               (flags & kOwnSegment) != 0);
-            if (p.ws_cnt && !(flags & kOwnSegment) &&
-                !fixup_segment<GT, DR>(p, abort_flag + kMiscLastFlag, seg_c0, seg_n, b, h, u, ctid, lane, cbar,
-                                       cph, abort_flag)) {
-                give_up();
-                return;
-            }
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
@@ -1970,9 +1828,9 @@ __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t
             return;
         }
         const uint32_t ma = smem_addr(meta + s * kMetaInts);   // 8-byte aligned
-        const uint2 mv0 = lds64(ma), mv1 = lds64(ma + 8), mv2 = lds64(ma + 16), mv3 = lds64(ma + 24);
+        const uint2 mv0 = lds64(ma), mv1 = lds64(ma + 8), mv2 = lds64(ma + 16);
         const int b = (int)mv0.x, h = (int)mv0.y, rem = (int)mv1.x, nvalid = (int)mv1.y, flags = (int)mv2.x,
-                  u = (int)mv2.y, seg_c0 = (int)mv3.x, seg_n = (int)mv3.y;
+                  u = (int)mv2.y;
         bool ragged = false;
         if ((i & 1) == gsel) {
             const int bi = i % kTc5Buffers;
@@ -2155,12 +2013,6 @@ __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t
             }
             combine_and_write<GT, kPairs, DR>(p, red_acc, red_m, red_l, red_l + kPairs * GT, ctid, b, h, u,
                                               (flags & kOwnSegment) != 0);
-            if (p.ws_cnt && !(flags & kOwnSegment) &&
-                !fixup_segment<GT, DR>(p, abort_flag + kMiscLastFlag, seg_c0, seg_n, b, h, u, ctid, lane, cbar,
-                                       cph, abort_flag)) {
-                give_up();
-                return;
-            }
             if (!consumer_sync(cbar, cph, p.timeout_ns, abort_flag, lane)) {
                 give_up();
                 return;
@@ -2233,14 +2085,11 @@ __global__ void __launch_bounds__(split_threads(CONS, CPA), 1)
         }
     }
     pdl_wait_prior_grid();
-    // The next kernel may launch now and waits for this grid on its own: the
-    // merge kernel (its early part reads the lengths, which the kernels
-    // before this one, now complete, may have written), or, when this grid
-    // merges its segments itself, the next call.
+    // The merge kernel may launch now; it waits for this grid on its own.  Its
+    // early part reads the lengths, which the kernels before this one (now
+    // complete) may have written.
     pdl_launch_dependents();
     build_prefix<kThreads>(p, prefix, misc + 1);   // ends with __syncthreads
-    if (p.ws_cnt)
-        write_empty_requests<D>(p, prefix, tid, kThreads);
 
     int t_begin, t_end;
     const Schedule sched{prefix, prefix + p.batch + 1, p.batch, p.hkv, p.seg_cost, (int)gridDim.x};

@@ -145,7 +145,6 @@ struct Schedule {
 // Workspace layout (byte offsets from the workspace base).
 struct WorkspaceLayout {
     size_t err_off;      // uint32 sticky error word
-    size_t cnt_off;      // int32 [batch * caller's kv heads] partials written per segment (zero at rest)
     size_t prefix_off;   // int32 [batch + 1] tile prefix, then int32 [batch + 1] non-empty requests
     size_t lse_off;      // fp32 [slots][group]
     size_t o_off;        // fp32 [slots][group][head_dim]
@@ -155,17 +154,12 @@ struct WorkspaceLayout {
 
 FD_HD size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// num_kv_heads: the launch's (fused) kv heads; caller_kv_heads: the caller's,
-// which size the segment counters.  Every launch shape of one call shape
-// (fused or not) finds the counters at the same place, so that a workspace
-// reused across them never takes a partial for a counter.
-FD_HD WorkspaceLayout workspace_layout(int batch, int num_kv_heads, int group, int head_dim, int caller_kv_heads)
+FD_HD WorkspaceLayout workspace_layout(int batch, int num_kv_heads, int group, int head_dim)
 {
     WorkspaceLayout w;
     w.slots = batch * num_kv_heads + kMaxCtas;
     w.err_off = 0;
-    w.cnt_off = 256;
-    w.prefix_off = align_up(w.cnt_off + sizeof(int) * (size_t)batch * caller_kv_heads, 256);
+    w.prefix_off = 256;
     w.lse_off = align_up(w.prefix_off + 2 * sizeof(int) * (size_t)(batch + 1), 256);
     w.o_off = align_up(w.lse_off + sizeof(float) * (size_t)w.slots * group, 256);
     w.total = align_up(w.o_off + sizeof(float) * (size_t)w.slots * group * head_dim, 256);

@@ -190,15 +190,6 @@ typedef struct fd_options {
 #define FD_FLAG_TMEM_SCORES 0x80u
 #define FD_FLAG_NO_TMEM_SCORES 0x100u
 
-/* One kernel per call: the split kernel merges the segments that several
- * CTAs share itself -- the last CTA to write a partial of a segment (counted
- * in the workspace, which must then come from fd_workspace_init and, after a
- * device error, be initialised again) merges the segment's partials -- and
- * no merge kernel runs.  By default a second kernel merges them: measured on
- * GB300 it was as fast or faster (up to 7% on short calls), its launch
- * overlapping the split kernel's tail.  Results agree to fp32 rounding. */
-#define FD_FLAG_FUSED_MERGE 0x200u
-
 /* ---- Test hooks (fd_options.flags): for the library's own tests only ---- */
 
 /* CTA 0 announces more bytes for its first tile than it loads, so its

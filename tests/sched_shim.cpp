@@ -14,8 +14,8 @@ int shim_schedule_cta_of_tile(const int *prefix, const int *nonempty, int batch,
     return s.cta_at(s.pos_of_tile(t));
 }
 int shim_request_of_tile(const int *prefix, int batch, int t) { return fd::request_of_tile(prefix, batch, t); }
-size_t shim_workspace_total(int batch, int hkv, int group, int d) { return fd::workspace_layout(batch, hkv, group, d, hkv).total; }
-int shim_slots(int batch, int hkv) { return fd::workspace_layout(batch, hkv, 1, 128, hkv).slots; }
+size_t shim_workspace_total(int batch, int hkv, int group, int d) { return fd::workspace_layout(batch, hkv, group, d).total; }
+int shim_slots(int batch, int hkv) { return fd::workspace_layout(batch, hkv, 1, 128).slots; }
 int shim_tile_tokens() { return fd::kTileTokens; }
 int shim_max_ctas() { return fd::kMaxCtas; }
 }
