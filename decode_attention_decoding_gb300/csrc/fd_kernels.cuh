@@ -8,7 +8,7 @@
 //     for a free shared-memory stage, writes the tile's metadata, and issues
 //     TMA loads of the K and V tiles (paged: one load per page, addressed
 //     through the block table) that complete on the stage's "full" mbarrier;
-//   * warps 0..7 are consumers, of one of three kinds (kCons*):
+//   * warps 0..7 are consumers, of one of four kinds (kCons*):
 //       - CUDA cores (shown here): warp w reads rows 8w..8w+7 of every tile,
 //         32/(D/8) rows at a time (a row spans D/8 lanes; each lane holds 8 of
 //         the D head dimensions, one 16-byte shared load, or 8 bytes of FP8
@@ -19,7 +19,10 @@
 //         fp32 accumulator rescaled by 2^(m_old - m_new) every tile, as in the
 //         handbook's FlashAttention section), and accumulates p * V;
 //       - tensor cores, a warp pair sharing the columns (split_consumer_mma);
-//       - tensor cores on two fused kv heads, one per warp of a pair.
+//       - tensor cores on two fused kv heads, one per warp of a pair;
+//       - for E4M3 caches on two fused kv heads: the scores from tcgen05 MMAs
+//         into tensor memory, issued by a tenth warp (split_score_issuer), and
+//         P.V on warp MMAs, four consumer warps per tile.
 //     Each consumer warp then releases the stage on its "empty" mbarrier --
 //     there is no CTA-wide barrier per tile.
 //   * At the last tile of a segment (request, kv head) within the CTA, the
