@@ -113,11 +113,11 @@ def consumers_label(flags, w) -> str:
                                                         (G <= 16 if f == 2 else 4 * G <= 8) for f in (2, 4))
     if (G == 1 or row < 128) and not fused:
         return "cuda cores"
-    tc5_shape = (fused and w.kv_dtype == "e4m3" and w.head_dim == 128 and G <= 8 and w.num_kv_heads % 2 == 0
+    tc5_shape = (fused and fp8 and w.head_dim == 128 and G <= 8 and w.num_kv_heads % 2 == 0
                  and (not w.paged or w.page_size >= 64))
     # FD_FLAG_TMEM_SCORES (0x80) forces the tcgen05 scores, FD_FLAG_NO_TMEM_SCORES (0x100) keeps the warp MMAs
     if tc5_shape and not flags & 0x100 and ((G <= 4 and tiles / (2 * 152) >= 24) or flags & 0x80):
-        return "tensor cores (tcgen05 E4M3 scores into TMEM, mma.sync fp16 P.V), fused kv heads"
+        return "tensor cores (tcgen05 FP8 scores into TMEM, mma.sync fp16 P.V), fused kv heads"
     return f"tensor cores ({mma})" + (", fused kv heads" if fused else "")
 
 

@@ -541,7 +541,7 @@ fd_status fill_plan(CallPlan *cp, const DeviceInfo &dev, const void *q, const in
     // kFuseMinTilesPerCta (paired) tiles per CTA, where their fixed costs
     // (TMEM, the score round trip) amortise (MHA over a 32 MiB E4M3 cache,
     // 6.7 tiles per CTA: 14.1 us with warp MMAs, 16.3 with them).
-    const bool tc5_shape = paired && kv == kKvE4m3 && d == 256 && group <= 8 &&
+    const bool tc5_shape = paired && kv_is_fp8(kv) && d == 256 && group <= 8 &&
                            (page_size == 0 || page_size >= kTileTokens);
     const bool tc5_default = group <= kTc5DefaultColumns && est_tiles / (2.0 * num_ctas) >= kFuseMinTilesPerCta;
     if (tc5_shape && !(sp.flags & FD_FLAG_NO_TMEM_SCORES) && (tc5_default || (sp.flags & FD_FLAG_TMEM_SCORES)))

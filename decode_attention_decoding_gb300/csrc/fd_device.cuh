@@ -455,12 +455,13 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t addr)
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor of a dense kind::f8f6f4 MMA with E4M3 A and B (both
-// K-major) and an fp32 accumulator: D format 1 = F32 (bits 4-5), A and B
-// formats 0 = E4M3 (7-9, 10-12), N >> 3 (17-22), M >> 4 (24-28).
-__host__ __device__ constexpr uint32_t umma_idesc_e4m3_f32(int m, int n)
+// Instruction descriptor of a dense kind::f8f6f4 MMA with A and B of one FP8
+// format (fmt 0 = E4M3, 1 = E5M2; both K-major) and an fp32 accumulator: D
+// format 1 = F32 (bits 4-5), A and B formats (7-9, 10-12), N >> 3 (17-22),
+// M >> 4 (24-28).
+__host__ __device__ constexpr uint32_t umma_idesc_fp8_f32(int m, int n, uint32_t fmt)
 {
-    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // D[tmem] (+)= A . B^T for one K step of 32 FP8 elements, issued by one thread.
@@ -513,6 +514,15 @@ __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi)
 {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two fp32 values rounded to E5M2 (nearest even, saturating at +-57344),
+// `lo` in the low byte.
+__device__ __forceinline__ uint16_t pack_e5m2x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
 }
 

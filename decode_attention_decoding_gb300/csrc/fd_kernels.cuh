@@ -20,7 +20,7 @@
 //         handbook's FlashAttention section), and accumulates p * V;
 //       - tensor cores, a warp pair sharing the columns (split_consumer_mma);
 //       - tensor cores on two fused kv heads, one per warp of a pair;
-//       - for E4M3 caches on two fused kv heads: the scores from tcgen05 MMAs
+//       - for FP8 caches on two fused kv heads: the scores from tcgen05 MMAs
 //         into tensor memory, issued by a tenth warp (split_score_issuer), and
 //         P.V on warp MMAs, four consumer warps per tile.
 //     Each consumer warp then releases the stage on its "empty" mbarrier --
@@ -54,10 +54,10 @@ constexpr int kPairs = kConsumerWarps / 2;
 // tensor-core score MMAs.
 constexpr int kSplitThreadsTc5 = kConsumerThreads + 64;
 // Their TMEM: kTc5Buffers score buffers of kTc5Cols fp32 columns each
-// (one per tile in flight; columns 16 k + 8 hh + c: E4M3 query part k of
-// column c of paired head hh; two parts for bf16 queries, three for fp16).
+// (one per tile in flight; columns 16 k + 8 hh + c: FP8 query part k of
+// column c of paired head hh; up to kTc5MaxParts parts).
 constexpr int kTc5Buffers = 4;
-constexpr int kTc5MaxParts = 3;
+constexpr int kTc5MaxParts = 4;
 constexpr int kTc5Cols = 64;
 constexpr int kTc5TmemCols = kTc5Buffers * kTc5Cols;
 // Their shared region (SplitParams::off_tc, 1024-byte aligned): the query
@@ -102,7 +102,7 @@ enum : int {
     kConsCudaCores = 0,   // CUDA cores, any group
     kConsMma = 1,         // tensor cores: a warp pair shares the columns, splits the dims
     kConsMmaPair = 2,     // tensor cores on two fused kv heads: each warp of a pair takes one
-    // two fused kv heads of an E4M3 cache: scores by tcgen05 MMAs into TMEM,
+    // two fused kv heads of an FP8 cache: scores by tcgen05 MMAs into TMEM,
     // P.V by warp MMAs; four warps per tile, two tiles in flight
     kConsTc5 = 3
 };
@@ -1591,28 +1591,39 @@ __device__ __forceinline__ void split_consumer_mma(const SplitParams &p, uint8_t
 // the CTA it forms S = K . Q^T for both kv heads of the fused row with four
 // tcgen05 MMAs (M = 128 rows: the tile's 64 tokens of head 0, then those of
 // head 1, as the 128-byte parts of the swizzled K tile lie; N = 16 columns
-// per query part; K = 128 E4M3 dims in four steps of 32) into TMEM buffer
+// per query part; K = 128 FP8 dims in four steps of 32) into TMEM buffer
 // (tile index mod kTc5Buffers), and signals the buffer's ready barrier.
 //
-// The query operand holds each column's 16-bit query row as NP E4M3 parts of
-// x = q 2^-sh (sh per column, so that the column's largest |x| lies in
-// [128, 256)): part 0 = E4M3(x), and part k+1 = E4M3(16 r_k) of the
-// remainder r_k = (x scaled by 16^k) - (parts 0..k so scaled).  Each part
-// keeps 4 more significant bits, so NP = 2 parts carry a bf16 query's 8 and
-// NP = 3 an fp16 query's 11 exactly: x = sum_k part_k 16^-k for every element
-// within 2^13 of its column's largest; smaller ones are off by under 2^-21 of
-// the largest.  The consumers take S = (sum_k S_k 16^-k) 2^sh scale log2(e).
-template <int G>
+// The query operand holds each column's 16-bit query row as NP parts in the
+// cache's FP8 format (A and B of one MMA share a format) of x = q 2^-sh (sh
+// per column, so that the column's largest |x| lies in [128, 256)): part 0 =
+// FP8(x), and part k+1 = FP8(R r_k) of the remainder r_k = (x scaled by R^k)
+// - (parts 0..k so scaled), R = 16 for E4M3 and 8 for E5M2.  Each part keeps
+// 4 (E4M3) or 3 (E5M2) more significant bits, so a bf16 query's 8 take 2 or
+// 3 parts and an fp16 query's 11 take 3 or 4: x = sum_k part_k R^-k exactly
+// for every element within 2^13 of its column's largest (E4M3; E5M2's range
+// covers every fp16 and bf16 ratio in use); smaller ones are off by under
+// 2^-21 of the largest.  The consumers take S = (sum_k S_k R^-k) 2^sh scale
+// log2(e).
+template <int KV>
+__host__ __device__ constexpr int tc5_query_parts(bool q_f16)
+{
+    return KV == kKvE4m3 ? (q_f16 ? 3 : 2) : (q_f16 ? 4 : 3);
+}
+
+template <int G, int KV>
 __device__ __forceinline__ void split_score_issuer(const SplitParams &p, uint8_t *tc, uint32_t stage0,
                                                    const int *meta, uint32_t full0, uint32_t ready0,
                                                    uint32_t free0, uint32_t tmem, volatile int *abort_flag,
                                                    int t_begin, int t_end, int lane)
 {
     static_assert(G >= 1 && G <= 8, "up to 8 query columns per kv head");
-    constexpr int kStage = Shape<256, kKvE4m3>::kStageBytes;
+    static_assert(KV == kKvE4m3 || KV == kKvE5m2, "FP8 caches");
+    constexpr int kStage = Shape<256, KV>::kStageBytes;
+    constexpr float kRadix = KV == kKvE4m3 ? 16.f : 8.f;   // R: one part's weight over the next
     const bool qf16 = p.q_f16 != 0;
-    const int np = qf16 ? 3 : 2;                                    // query parts
-    const uint32_t idesc = umma_idesc_e4m3_f32(128, 16 * np);
+    const int np = tc5_query_parts<KV>(qf16);               // query parts
+    const uint32_t idesc = umma_idesc_fp8_f32(128, 16 * np, KV == kKvE4m3 ? 0u : 1u);
     const int NS = p.num_stages;
     const uint32_t qop = smem_addr(tc);
     float *mul_buf = reinterpret_cast<float *>(tc + kTc5OffMul);
@@ -1679,13 +1690,14 @@ __device__ __forceinline__ void split_score_issuer(const SplitParams &p, uint8_t
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float *v = x + 16 * k + 4 * e;
-                    const uint16_t c01 = pack_e4m3x2(v[0], v[1]), c23 = pack_e4m3x2(v[2], v[3]);
-                    const float2 b01 = fp8x2_to_float2<kKvE4m3>(c01), b23 = fp8x2_to_float2<kKvE4m3>(c23);
+                    const uint16_t c01 = KV == kKvE4m3 ? pack_e4m3x2(v[0], v[1]) : pack_e5m2x2(v[0], v[1]);
+                    const uint16_t c23 = KV == kKvE4m3 ? pack_e4m3x2(v[2], v[3]) : pack_e5m2x2(v[2], v[3]);
+                    const float2 b01 = fp8x2_to_float2<KV>(c01), b23 = fp8x2_to_float2<KV>(c23);
                     // the remainder, scaled for the next part (exact in fp32)
-                    v[0] = 16.f * (v[0] - b01.x);
-                    v[1] = 16.f * (v[1] - b01.y);
-                    v[2] = 16.f * (v[2] - b23.x);
-                    v[3] = 16.f * (v[3] - b23.y);
+                    v[0] = kRadix * (v[0] - b01.x);
+                    v[1] = kRadix * (v[1] - b01.y);
+                    v[2] = kRadix * (v[2] - b23.x);
+                    v[3] = kRadix * (v[3] - b23.y);
                     wd[e] = (uint32_t)c01 | ((uint32_t)c23 << 16);
                 }
                 const int chunk = half * 4 + k;
@@ -1756,7 +1768,7 @@ __device__ __forceinline__ void split_score_issuer(const SplitParams &p, uint8_t
     __syncwarp();
 }
 
-// The consumers of the TMEM-score instances (E4M3, two fused kv heads of 128
+// The consumers of the TMEM-score instances (FP8, two fused kv heads of 128
 // dims, up to 8 columns each).  The eight warps form two groups of four;
 // group g takes the CTA's tiles of index g (mod 2), so two tiles are in
 // flight.  In a group, warp w reads TMEM lanes 32 (w % 4) .. + 31: the
@@ -1768,7 +1780,7 @@ __device__ __forceinline__ void split_score_issuer(const SplitParams &p, uint8_t
 // and forms O^T += V^T . P^T over its head's 128 dims with warp MMAs on V
 // converted to fp16 in registers.  The four states of each head (2 groups x
 // 2 token halves) are combined at every segment's last tile in the CTA.
-template <int G>
+template <int G, int KV>
 __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t *smem, uint8_t *tc,
                                                    uint32_t stage0, const int *meta, uint32_t full0,
                                                    uint32_t empty0, uint32_t cbar, uint32_t ready0, uint32_t free0,
@@ -1776,7 +1788,7 @@ __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t
                                                    int cw, int lane)
 {
     static_assert(G >= 1 && G <= 8, "up to 8 query columns per kv head");
-    using HD = Shape<256, kKvE4m3>;
+    using HD = Shape<256, KV>;
     constexpr int GT = 2 * G;    // columns of the launch head
     constexpr int DR = 128;      // dims of one head
     constexpr int DT = DR / 16;  // 16-dim tiles of P.V
@@ -1793,7 +1805,8 @@ __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t
     const uint32_t pbuf = smem_addr(tc + kTc5OffP + cw * kTc5PBytes);
     const uint32_t lane_row = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(hh * 8);
     const int ctid = cw * 32 + lane;
-    const bool qf16 = p.q_f16 != 0;   // three query parts (fp16), else two (bf16)
+    const int np = tc5_query_parts<KV>(p.q_f16 != 0);   // query parts
+    constexpr float kInvRadix = KV == kKvE4m3 ? 0.0625f : 0.125f;   // one part's weight over the previous
 
     float acc[DT][4];            // O^T fragments: dims 16 i + 2 grp (+1), columns 2 qd (+1)
     float m[G], l[G], lt[G];     // m is the same in every lane; l, lt sum this lane's token
@@ -1843,12 +1856,14 @@ __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t
             }
             tc_fence_after();
             // the query parts' scores of this lane's token (16 columns apart)
-            float s0[8], s1[8], s2[8];
+            float s0[8], s1[8], s2[8], s3[8];
             const uint32_t tb = lane_row + (uint32_t)(bi * kTc5Cols);
             tmem_ld_x8(tb, s0);
             tmem_ld_x8(tb + 16, s1);
-            if (qf16)
+            if (np > 2)
                 tmem_ld_x8(tb + 32, s2);
+            if (np > 3)
+                tmem_ld_x8(tb + 48, s3);
             // the buffer's multipliers, read before it is released: the issuer
             // rewrites them with the buffer's next MMAs
             float mul[G];
@@ -1882,8 +1897,9 @@ __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t
                 for (int j = 0; j < 2; ++j) {
                     const int cc = c + j < G ? c + j : c;
                     const int lim = p.q_len == 1 ? nvalid : min(nvalid, rem - lag[cc]);
-                    const float sc = qf16 ? s0[cc] + (s1[cc] + s2[cc] * 0.0625f) * 0.0625f
-                                          : s0[cc] + s1[cc] * 0.0625f;
+                    float sc = np > 3 ? s3[cc] : 0.f;
+                    sc = np > 2 ? s2[cc] + sc * kInvRadix : sc;
+                    sc = s0[cc] + (s1[cc] + sc * kInvRadix) * kInvRadix;
                     x[j] = tok < lim ? sc * mul[cc] : kNegInf;
                 }
 #pragma unroll
@@ -1964,10 +1980,10 @@ __device__ __forceinline__ void split_consumer_tc5(const SplitParams &p, uint8_t
                                       r3);
                     const uint32_t s0 = prmt(r0, 0u, 0x3120u), s1 = prmt(r1, 0u, 0x3120u);
                     const uint32_t s2 = prmt(r2, 0u, 0x3120u), s3 = prmt(r3, 0u, 0x3120u);
-                    const uint32_t x0 = fp8x2_to_f16x2<kKvE4m3>(lo16(s0)), x1 = fp8x2_to_f16x2<kKvE4m3>(hi16(s0));
-                    const uint32_t x2 = fp8x2_to_f16x2<kKvE4m3>(lo16(s1)), x3 = fp8x2_to_f16x2<kKvE4m3>(hi16(s1));
-                    const uint32_t y0 = fp8x2_to_f16x2<kKvE4m3>(lo16(s2)), y1 = fp8x2_to_f16x2<kKvE4m3>(hi16(s2));
-                    const uint32_t y2 = fp8x2_to_f16x2<kKvE4m3>(lo16(s3)), y3 = fp8x2_to_f16x2<kKvE4m3>(hi16(s3));
+                    const uint32_t x0 = fp8x2_to_f16x2<KV>(lo16(s0)), x1 = fp8x2_to_f16x2<KV>(hi16(s0));
+                    const uint32_t x2 = fp8x2_to_f16x2<KV>(lo16(s1)), x3 = fp8x2_to_f16x2<KV>(hi16(s1));
+                    const uint32_t y0 = fp8x2_to_f16x2<KV>(lo16(s2)), y1 = fp8x2_to_f16x2<KV>(hi16(s2));
+                    const uint32_t y2 = fp8x2_to_f16x2<KV>(lo16(s3)), y3 = fp8x2_to_f16x2<KV>(hi16(s3));
                     mma_16816<true>(acc[c], x0, x1, x2, x3, bh[2 * ks], bh[2 * ks + 1]);
                     mma_16816<true>(acc[c + 1], y0, y1, y2, y3, bh[2 * ks], bh[2 * ks + 1]);
                     mma_16816<true>(acc[c], x0, x1, x2, x3, bl[2 * ks], bl[2 * ks + 1]);
@@ -2039,8 +2055,8 @@ __global__ void __launch_bounds__(split_threads(CONS, CPA), 1)
                  const __grid_constant__ CUtensorMap tmv)
 {
     static_assert(!CPA || (PAGED && CONS != kConsCudaCores), "cp.async copies feed paged tensor-core launches");
-    static_assert(CONS != kConsTc5 || (KV == kKvE4m3 && D == 256 && !CPA),
-                  "TMEM scores: two fused E4M3 kv heads of 128 dims");
+    static_assert(CONS != kConsTc5 || (kv_is_fp8(KV) && D == 256 && !CPA),
+                  "TMEM scores: two fused FP8 kv heads of 128 dims");
     constexpr int kThreads = split_threads(CONS, CPA);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -2118,10 +2134,10 @@ __global__ void __launch_bounds__(split_threads(CONS, CPA), 1)
             split_producer<PAGED, true, D, KV>(p, &tmk, &tmv, stage0, prefix, meta, full0, empty0, abort_flag,
                                                t_begin, t_end, lane);
         else if (warp == issuer)
-            split_score_issuer<G>(p, tc, stage0, meta, full0, ready0, free0, tmem, abort_flag, t_begin, t_end,
+            split_score_issuer<G, KV>(p, tc, stage0, meta, full0, ready0, free0, tmem, abort_flag, t_begin, t_end,
                                   lane);
         else
-            split_consumer_tc5<G>(p, smem, tc, stage0, meta, full0, empty0, cbar, ready0, free0, tmem,
+            split_consumer_tc5<G, KV>(p, smem, tc, stage0, meta, full0, empty0, cbar, ready0, free0, tmem,
                                   abort_flag, t_begin, t_end, warp, lane);
         tc_fence_before();
         named_bar_sync(1, kThreads);

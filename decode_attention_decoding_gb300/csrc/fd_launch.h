@@ -120,7 +120,7 @@ cudaError_t launch_split_t(const SplitParams &p, const CUtensorMap &tmk, const C
 // consumers on CUDA cores (group 1 to 8), on tensor cores (group 2 to 16,
 // swizzled K/V maps, rows of at least 128 bytes), or on tensor cores with two
 // fused kv heads per row (group = columns per head, 1 to 16; D = 2 x head_dim),
-// or with scores in TMEM (kConsTc5: E4M3, D = 256, group 1 to 8).
+// or with scores in TMEM (kConsTc5: FP8, D = 256, group 1 to 8).
 // cp_async: paged with pages under 8 tokens on the tensor cores (the CPA
 // instances, 384 threads; tensor-core groups only).
 // Returns cudaErrorInvalidValue for an unsupported combination.
@@ -154,8 +154,8 @@ cudaError_t launch_split_variant(int cons, int group, bool cp_async, const Split
         }
         return cudaErrorInvalidValue;
     }
-    if (cons == kConsTc5) {   // scores in TMEM: two fused E4M3 heads of 128 dims, up to 8 columns each
-        if constexpr (KV == kKvE4m3 && D == 256) {
+    if (cons == kConsTc5) {   // scores in TMEM: two fused FP8 heads of 128 dims, up to 8 columns each
+        if constexpr (kv_is_fp8(KV) && D == 256) {
             switch (group) {
             case 1: return launch_split_t<1, PAGED, kConsTc5, KV, D>(p, tmk, tmv, c);
             case 2: return launch_split_t<2, PAGED, kConsTc5, KV, D>(p, tmk, tmv, c);

@@ -176,17 +176,18 @@ typedef struct fd_options {
  * costs bandwidth).  Results are identical; for comparisons only. */
 #define FD_FLAG_NO_PREFETCH 0x40u
 
-/* Scores on the tcgen05 tensor cores.  For an FP8 E4M3 cache whose kv heads
- * are paired (head_dim 128; contiguous, or pages of at least 64 tokens) the
- * scores are by default formed with tcgen05 MMAs straight from the E4M3 K
- * tile into tensor memory, against the query split into E4M3 parts (two for
- * bf16, three for fp16: exact), when a kv head has at most 4 query columns
- * and the call has at least 24 paired KV tiles per split CTA; warp MMAs on
- * K converted to fp16 in registers otherwise.  Measured on
- * GB300, the tcgen05 scores took the 1 GiB MHA call 6% and the ragged GQA-4
- * call 3% faster, and the GQA-8 call 2% slower.  This flag takes the
- * tcgen05 scores for up to 8 columns too; FD_FLAG_NO_TMEM_SCORES never
- * (it wins if both are set).  Results agree to fp32 rounding. */
+/* Scores on the tcgen05 tensor cores.  For an FP8 cache (E4M3 or E5M2) whose
+ * kv heads are paired (head_dim 128; contiguous, or pages of at least 64
+ * tokens) the scores are by default formed with tcgen05 MMAs straight from
+ * the FP8 K tile into tensor memory, against the query split into parts of
+ * the same FP8 format (exact: two to four parts for a bf16 or fp16 query),
+ * when a kv head has at most 4 query columns and the call has at least 24
+ * paired KV tiles per split CTA; warp MMAs on K converted to fp16 in
+ * registers otherwise.  Measured on GB300 (E4M3), the tcgen05 scores took
+ * the 1 GiB MHA call 6% and the ragged GQA-4 call 3% faster, and the GQA-8
+ * call 2% slower.  This flag takes the tcgen05 scores for up to 8 columns
+ * and any length too; FD_FLAG_NO_TMEM_SCORES never (it wins if both are
+ * set).  Results agree to fp32 rounding. */
 #define FD_FLAG_TMEM_SCORES 0x80u
 #define FD_FLAG_NO_TMEM_SCORES 0x100u
 
